@@ -1,0 +1,202 @@
+"""Oracle: the triggered plan's round and gate semantics, sequential definition.
+
+TEST INFRASTRUCTURE ONLY (see ``oracle/__init__``).
+
+Restated from the Iris "Triggered Plans" page (sections Model, The kernel author's contract,
+Memory ordering, Gates and rounds, Requirements and limits) and "Triggered SDMA Plans" (ROCm/iris
+pull 573, section Design notes):
+
+* Every chunk has a gate row; this model keeps, per virtual rank and per global chunk id, the
+  words ready, arrival, completion, error and the writer counter.  Rows of a rank's own chunks
+  use ready / completion / error / counter; rows of other ranks' chunks use arrival.
+* mark_ready: the writer counter goes up by one.  When it reaches round * writers the gate opens
+  (ready := round).  A count above round * writers records the round in ``error``.
+* The copy engine keeps one queue per (source, peer), holding the source's chunks in schedule
+  order.  A queue waits until the low 32 bits of ready are >= round, copies the chunk's regions
+  to the same offsets in the peer's buffer, then adds one to the peer's arrival word (and, in
+  this model, one to the source's completion word).  A queue never passes a closed gate:
+  later chunks wait behind it (head-of-line order).
+* wait(): this rank's chunks were marked exactly ``writers`` times this round (more is an
+  error, fewer a timeout naming the short chunks) and arrived at every peer; every other chunk
+  arrived here.
+* Rounds start at 1, go up by one per next_round and are never reset: at most 2**32 - 1.
+* close() in the middle of a round sends each chunk as it stands: gates not yet open are
+  opened and the queues drain.
+"""
+from __future__ import annotations
+
+from typing import Dict, List, Optional, Sequence, Tuple
+
+import numpy as np
+
+from . import schedule as S
+
+READY, ARRIVAL, COMPLETION, ERROR, COUNTER = range(5)
+NFIELDS = 5
+ROUND_LIMIT = (1 << 32) - 1
+
+OK, EXTRA, TIMEOUT = "OK", "EXTRA", "TIMEOUT"
+
+
+class StateError(RuntimeError):
+    pass
+
+
+class RoundLimitError(RuntimeError):
+    pass
+
+
+def copy_region(src: np.ndarray, dst: np.ndarray, reg: S.Region) -> None:
+    """Copy one region between two byte buffers, at the same offsets."""
+    off, rb, rows, pitch = reg
+    if rows == 0 or rb == 0:
+        return
+    if rows == 1:
+        dst[off:off + rb] = src[off:off + rb]
+        return
+    span = (rows - 1) * pitch + rb
+    sv = np.lib.stride_tricks.as_strided(src[off:off + span], shape=(rows, rb), strides=(pitch, 1))
+    dv = np.lib.stride_tricks.as_strided(dst[off:off + span], shape=(rows, rb), strides=(pitch, 1))
+    dv[...] = sv
+
+
+class Plan:
+    """P virtual ranks, each with a byte buffer, one schedule each, and a gate table each."""
+
+    def __init__(self, bufs: Sequence[np.ndarray], schedules: Sequence[S.Schedule],
+                 allgather: bool = True, initial_round: int = 1, validate: bool = True,
+                 copy_data: bool = True):
+        self.P = len(bufs)
+        if len(schedules) != self.P:
+            raise ValueError("one schedule per rank")
+        nbytes = len(bufs[0])
+        if any(len(b) != nbytes for b in bufs):
+            raise ValueError("symmetric buffers must have one size")
+        if not (1 <= initial_round <= ROUND_LIMIT):
+            raise ValueError("initial round out of range")
+        if validate:
+            S.validate(schedules, nbytes, allgather)
+        self.bufs = list(bufs)
+        self.copy_data = copy_data      # False: gate bookkeeping only (large workloads)
+        self.schedules = list(schedules)
+        self.first = S.first_chunks(schedules)
+        self.owner: List[int] = []
+        self.chunks: List[S.Chunk] = []
+        for r, sch in enumerate(schedules):
+            for ch in sch.chunks:
+                self.owner.append(r)
+                self.chunks.append(ch)
+        self.G = len(self.chunks)
+        self.round = initial_round
+        self.gates = np.zeros((self.P, self.G, NFIELDS), dtype=np.uint64)
+        prior = initial_round - 1      # gates as they stand after `prior` completed rounds
+        for c, ch in enumerate(self.chunks):
+            s = self.owner[c]
+            self.gates[s, c, READY] = prior
+            self.gates[s, c, COUNTER] = prior * ch.writers
+            self.gates[s, c, COMPLETION] = prior * (self.P - 1)
+            for p in range(self.P):
+                if p != s:
+                    self.gates[p, c, ARRIVAL] = prior
+        self.delivered = set()          # (chunk, peer) delivered in the current round
+        self.delivery_log: List[Tuple[int, int, int]] = []   # (source, peer, chunk) in order
+        self.state = "PREPARED"
+
+    # -- round ------------------------------------------------------------------
+    def start(self) -> int:
+        if self.state != "PREPARED":
+            raise StateError(f"start in state {self.state}")
+        self.state = "RUNNING"
+        return self.round
+
+    def chunks_of(self, r: int) -> range:
+        return range(self.first[r], self.first[r] + self.schedules[r].n_chunks)
+
+    def mark_ready(self, rank: int, c: int) -> None:
+        """One writer's mark on chunk c (global id) of its own rank."""
+        if self.owner[c] != rank:
+            raise ValueError("a rank marks only its own chunks")
+        row = self.gates[rank, c]
+        row[COUNTER] += 1
+        target = self.round * self.chunks[c].writers
+        if row[COUNTER] == target:
+            row[READY] = self.round
+        elif row[COUNTER] > target:
+            row[ERROR] = self.round
+
+    def gate_open(self, c: int) -> bool:
+        s = self.owner[c]
+        return (int(self.gates[s, c, READY]) & 0xFFFFFFFF) >= self.round
+
+    def copier_progress(self) -> int:
+        """Run every (source, peer) queue as far as its gates allow; returns deliveries made."""
+        n = 0
+        for s in range(self.P):
+            for p in range(self.P):
+                if p == s:
+                    continue
+                for c in self.chunks_of(s):
+                    if (c, p) in self.delivered:
+                        continue
+                    if not self.gate_open(c):
+                        break                       # head of line: later chunks wait
+                    if self.copy_data:
+                        for reg in self.chunks[c].regions:
+                            copy_region(self.bufs[s], self.bufs[p], reg)
+                    self.gates[p, c, ARRIVAL] += 1
+                    self.gates[s, c, COMPLETION] += 1
+                    self.delivered.add((c, p))
+                    self.delivery_log.append((s, p, c))
+                    n += 1
+        return n
+
+    def wait(self) -> Tuple[str, List[int], List[int]]:
+        """Completion check; returns (status, short chunk ids, extra chunk ids)."""
+        if self.state != "RUNNING":
+            raise StateError(f"wait in state {self.state}")
+        R = self.round
+        extra, short = [], []
+        for c, ch in enumerate(self.chunks):
+            s = self.owner[c]
+            cnt = int(self.gates[s, c, COUNTER])
+            if cnt > R * ch.writers or int(self.gates[s, c, ERROR]) != 0:
+                extra.append(c)
+            elif cnt < R * ch.writers:
+                short.append(c)
+            elif any(int(self.gates[p, c, ARRIVAL]) < R for p in range(self.P) if p != s):
+                short.append(c)
+        if extra:
+            self.state = "FAILED"
+            return EXTRA, short, extra
+        if short:
+            self.state = "FAILED"
+            return TIMEOUT, short, extra
+        self.state = "DONE"
+        return OK, short, extra
+
+    def next_round(self) -> int:
+        if self.state != "DONE":
+            raise StateError(f"next_round in state {self.state}")
+        if self.round >= ROUND_LIMIT:
+            raise RoundLimitError("a plan is limited to 2**32 - 1 rounds")
+        self.round += 1
+        self.delivered = set()
+        self.state = "PREPARED"
+        return self.round
+
+    def close(self) -> None:
+        """Close; mid-round, gates not yet open are opened and chunks sent as they stand."""
+        if self.state == "RUNNING":
+            for c in range(self.G):
+                if not self.gate_open(c):
+                    self.gates[self.owner[c], c, READY] = self.round
+            self.copier_progress()
+        self.state = "CLOSED"
+
+
+def expected_allgather(P: int, M: int, N: int, dtype: str, seed: int, rnd: int,
+                       elem_bytes: int) -> np.ndarray:
+    """Closed form: every virtual rank's buffer is the concatenation of all ranks' slices."""
+    from . import hashfill
+    return np.concatenate([hashfill.fill_slice_bytes(dtype, seed, r, rnd, M, N)
+                           for r in range(P)])

@@ -1,0 +1,219 @@
+"""Pins for the oracle's round and gate semantics (oracle/plan.py)."""
+import itertools
+
+import numpy as np
+import pytest
+
+from oracle import hashfill as H
+from oracle import plan as PL
+from oracle import schedule as S
+from oracle.plan import ARRIVAL, COMPLETION, COUNTER, ERROR, READY
+
+
+def make_plan(P, M, N, dtype, kind, initial_round=1, **kw):
+    e = {"bf16": 2, "f32": 4, "u8": 1}[dtype]
+    rb = N * e
+    slice_bytes = M * rb
+    bufs = [np.zeros(P * slice_bytes, dtype=np.uint8) for _ in range(P)]
+    scheds = []
+    for r in range(P):
+        off = r * slice_bytes
+        if kind == "whole":
+            scheds.append(S.whole(off, M, rb, rb, kw.get("np", 1)))
+        elif kind == "chunks":
+            scheds.append(S.chunks(off, M, rb, rb, kw["n"]))
+        else:
+            tm, tn = -(-M // kw["BM"]), -(-N // kw["BN"])
+            gm = kw.get("gm", 0)
+            order = (lambda s, tm=tm, tn=tn: S.order_grouped(s, tm, tn, gm)) if gm else None
+            scheds.append(S.tile_chunks(off, M, N, e, rb, kw["BM"], kw["BN"], kw["T"], order))
+    return PL.Plan(bufs, scheds, allgather=True, initial_round=initial_round), slice_bytes
+
+
+def produce_all(plan, P, M, N, dtype, seed, slice_bytes):
+    """Each rank writes its slice for this round, then marks every chunk writers times."""
+    for r in range(P):
+        plan.bufs[r][r * slice_bytes:(r + 1) * slice_bytes] = \
+            H.fill_slice_bytes(dtype, seed, r, plan.round, M, N)
+        for c in plan.chunks_of(r):
+            for _ in range(plan.chunks[c].writers):
+                plan.mark_ready(r, c)
+
+
+CASES = [
+    (2, 8, 16, "bf16", "whole", {"np": 1}),
+    (4, 12, 10, "f32", "chunks", {"n": 4}),
+    (3, 10, 9, "bf16", "tile_chunks", {"BM": 4, "BN": 4, "T": 2, "gm": 2}),
+    (2, 5, 7, "u8", "tile_chunks", {"BM": 2, "BN": 3, "T": 5}),
+    (8, 4, 8, "f32", "whole", {"np": 8}),
+]
+
+
+@pytest.mark.parametrize("P,M,N,dtype,kind,kw", CASES)
+def test_allgather_closed_form_and_gate_invariants(P, M, N, dtype, kind, kw):
+    seed = 99
+    plan, sb = make_plan(P, M, N, dtype, kind, **kw)
+    e = {"bf16": 2, "f32": 4, "u8": 1}[dtype]
+    for R in range(1, 4):
+        assert plan.start() == R
+        produce_all(plan, P, M, N, dtype, seed, sb)
+        plan.copier_progress()
+        assert plan.wait() == (PL.OK, [], [])
+        want = PL.expected_allgather(P, M, N, dtype, seed, R, e)
+        for q in range(P):
+            assert np.array_equal(plan.bufs[q], want), (R, q)
+        for c, ch in enumerate(plan.chunks):
+            s = plan.owner[c]
+            assert plan.gates[s, c, COUNTER] == R * ch.writers
+            assert plan.gates[s, c, READY] == R
+            assert plan.gates[s, c, COMPLETION] == R * (P - 1)
+            assert plan.gates[s, c, ERROR] == 0
+            for p in range(P):
+                assert plan.gates[p, c, ARRIVAL] == (R if p != s else 0)
+        # per source, arrivals summed over its chunks = round x chunks at every peer
+        for s in range(P):
+            for p in range(P):
+                if p != s:
+                    assert sum(int(plan.gates[p, c, ARRIVAL]) for c in plan.chunks_of(s)) == \
+                        R * plan.schedules[s].n_chunks
+        plan.next_round()
+
+
+def test_extra_mark_is_reported_and_missing_mark_times_out():
+    plan, sb = make_plan(2, 4, 4, "bf16", "chunks", n=2)
+    plan.start()
+    produce_all(plan, 2, 4, 4, "bf16", 1, sb)
+    plan.mark_ready(1, 3)                   # one mark too many on rank 1's second chunk
+    plan.copier_progress()
+    status, short, extra = plan.wait()
+    assert status == PL.EXTRA and extra == [3] and plan.gates[1, 3, ERROR] == 1
+    assert plan.state == "FAILED"
+
+    plan, sb = make_plan(2, 4, 4, "bf16", "chunks", n=2)
+    plan.start()
+    for r in range(2):
+        for c in plan.chunks_of(r):
+            if c != 1:
+                plan.mark_ready(r, c)
+    plan.copier_progress()
+    status, short, extra = plan.wait()
+    assert status == PL.TIMEOUT and short == [1] and extra == []
+    assert plan.gates[0, 1, READY] == 0 and plan.gates[1, 1, ARRIVAL] == 0
+
+
+def test_head_of_line_order():
+    plan, sb = make_plan(2, 6, 4, "bf16", "chunks", n=3)
+    plan.start()
+    plan.mark_ready(0, 2)                   # rank 0 completes its last chunk first
+    plan.mark_ready(0, 1)
+    plan.copier_progress()
+    assert plan.gates[1, 1, ARRIVAL] == 0 and plan.gates[1, 2, ARRIVAL] == 0
+    plan.mark_ready(0, 0)
+    plan.copier_progress()
+    assert [c for (s, p, c) in plan.delivery_log if s == 0] == [0, 1, 2]
+
+
+def test_round_limit():
+    top = (1 << 32) - 1
+    plan, sb = make_plan(2, 4, 4, "bf16", "whole", initial_round=top - 1)
+    for R in (top - 1, top):
+        assert plan.start() == R
+        produce_all(plan, 2, 4, 4, "bf16", 5, sb)
+        plan.copier_progress()
+        assert plan.wait()[0] == PL.OK
+        assert plan.gates[0, 0, READY] == R
+        if R < top:
+            plan.next_round()
+    with pytest.raises(PL.RoundLimitError):
+        plan.next_round()
+
+
+def test_state_machine():
+    plan, sb = make_plan(2, 4, 4, "bf16", "whole")
+    with pytest.raises(PL.StateError):
+        plan.wait()
+    with pytest.raises(PL.StateError):
+        plan.next_round()
+    plan.start()
+    with pytest.raises(PL.StateError):
+        plan.start()
+
+
+def test_close_mid_round_sends_chunks_as_they_stand():
+    P, M, N = 2, 4, 8
+    plan, sb = make_plan(P, M, N, "bf16", "chunks", n=2)
+    plan.start()
+    full = H.fill_slice_bytes("bf16", 4, 0, 1, M, N)
+    plan.bufs[0][:sb // 2] = full[:sb // 2]            # rank 0 wrote only its first block
+    plan.mark_ready(0, 0)
+    plan.close()
+    assert np.array_equal(plan.bufs[1][:sb], plan.bufs[0][:sb])
+    assert np.all(plan.bufs[1][sb // 2:sb] == 0)        # second block went as it stood
+    assert plan.state == "CLOSED"
+
+
+def test_bytes_outside_regions_untouched():
+    P, M, rb = 2, 4, 8
+    bufs = [np.full(P * M * rb, 0xEE, dtype=np.uint8) for _ in range(P)]
+    # each rank sends only the first 4 bytes of each of its rows (a 2D window)
+    scheds = [S.Schedule([S.Chunk([(r * M * rb, 4, M, rb)], 1)]) for r in range(P)]
+    plan = PL.Plan(bufs, scheds)
+    plan.start()
+    bufs[0][:M * rb] = 1
+    bufs[1][M * rb:] = 2
+    plan.mark_ready(0, 0)
+    plan.mark_ready(1, 1)
+    plan.copier_progress()
+    assert plan.wait()[0] == PL.OK
+    row = np.array([1] * 4 + [0xEE] * 4, dtype=np.uint8)
+    assert np.array_equal(bufs[1][:M * rb], np.tile(row, M))
+    row = np.array([2] * 4 + [0xEE] * 4, dtype=np.uint8)
+    assert np.array_equal(bufs[0][M * rb:], np.tile(row, M))
+
+
+def test_exhaustive_interleavings_tiny_plan():
+    """P=2, two chunks per rank, two writers per chunk: every interleaving of the eight marks
+    (each writer marks its two chunks in order, after writing its half of the chunk) with the
+    copier running after every event.  The gate never opens before both writers' marks of the
+    round, arrival never precedes ready, and every round ends with the closed-form buffers."""
+    P, rb = 2, 8
+    nrows = 4                                # per rank: 2 chunks x 2 rows
+    sb = nrows * rb
+    seqs = [(r, w) for r in range(P) for w in range(2)]     # four writers
+    events = [x for x in seqs for _ in range(2)]
+    orders = set(itertools.permutations(events))
+    assert len(orders) == 2520
+    for order in sorted(orders):
+        bufs = [np.zeros(P * sb, dtype=np.uint8) for _ in range(P)]
+        scheds = [S.Schedule([S.Chunk([(r * sb + k * 2 * rb, 2 * rb, 1, 2 * rb)], 2)
+                              for k in range(2)]) for r in range(P)]
+        plan = PL.Plan(bufs, scheds)
+        for R in (1, 2):
+            plan.start()
+            pos = {x: 0 for x in seqs}
+            for ev in order:
+                r, w = ev
+                k = pos[ev]
+                pos[ev] += 1
+                c = plan.first[r] + k
+                lo = r * sb + k * 2 * rb + w * rb          # writer w's row of chunk k
+                bufs[r][lo:lo + rb] = 16 * R + 4 * r + w
+                plan.mark_ready(r, c)
+                for cc in range(plan.G):
+                    s = plan.owner[cc]
+                    opened = int(plan.gates[s, cc, READY]) >= R
+                    assert opened == (int(plan.gates[s, cc, COUNTER]) >= R * 2)
+                plan.copier_progress()
+                for cc in range(plan.G):
+                    s = plan.owner[cc]
+                    for p in range(P):
+                        if p != s and int(plan.gates[p, cc, ARRIVAL]) >= R:
+                            assert int(plan.gates[s, cc, READY]) >= R
+            assert plan.wait()[0] == PL.OK
+            for q in range(P):
+                for r in range(P):
+                    for k in range(2):
+                        for w in range(2):
+                            lo = r * sb + k * 2 * rb + w * rb
+                            assert np.all(bufs[q][lo:lo + rb] == 16 * R + 4 * r + w)
+            plan.next_round()

@@ -1,0 +1,84 @@
+"""The triggered protocol with CPU threads as ranks (oracle/threaded.py)."""
+import numpy as np
+import pytest
+
+from oracle import hashfill as H
+from oracle import plan as PL
+from oracle import schedule as S
+from oracle.threaded import ThreadedRound, barrier_threads
+
+
+def _setup(P=3, M=8, N=8, n=4):
+    e = 2
+    rb = N * e
+    sb = M * rb
+    bufs = [np.zeros(P * sb, dtype=np.uint8) for _ in range(P)]
+    scheds = [S.chunks(r * sb, M, rb, rb, n) for r in range(P)]
+    plan = PL.Plan(bufs, scheds)
+    data = {r: H.fill_slice_bytes("bf16", 11, r, 1, M, N) for r in range(P)}
+
+    def write_unit(rank, c, u):
+        for (off, nb, rows, pitch) in plan.chunks[c].regions:
+            lo = off - rank * sb
+            plan.bufs[rank][off:off + nb] = data[rank][lo:lo + nb]
+
+    order = {r: [(c, 0) for c in plan.chunks_of(r)] for r in range(P)}
+    return plan, write_unit, order, data, sb
+
+
+def test_threaded_round_matches_closed_form():
+    plan, write_unit, order, data, sb = _setup()
+    status = ThreadedRound(plan, write_unit, order, programs=2).run()
+    assert status == (PL.OK, [], [])
+    want = np.concatenate([data[r] for r in range(plan.P)])
+    for q in range(plan.P):
+        assert np.array_equal(plan.bufs[q], want)
+
+
+def test_out_of_order_completion_is_correct_and_queues_keep_schedule_order():
+    plan, write_unit, order, data, sb = _setup(P=2, n=4)
+    for r in range(2):
+        order[r] = list(reversed(order[r]))          # the producer completes chunks backwards
+    delay = {(c, 0): 0.01 for c in range(plan.G)}
+    tr = ThreadedRound(plan, write_unit, order, delay=delay)
+    assert tr.run()[0] == PL.OK
+    for (s, p), log in tr.queue_log.items():
+        assert log == list(plan.chunks_of(s))        # head-of-line: schedule order per queue
+    want = np.concatenate([data[r] for r in range(2)])
+    assert all(np.array_equal(b, want) for b in plan.bufs)
+
+
+def test_missing_mark_times_out_naming_the_chunk():
+    plan, write_unit, order, data, sb = _setup(P=2, n=2)
+    tr = ThreadedRound(plan, write_unit, order, max_polls=200, skip={(2, 0)})
+    status, short, extra = tr.run()
+    # chunk 2 never opens; chunk 3 opened but waits behind it on the same queue
+    assert status == PL.TIMEOUT and short == [2, 3] and extra == []
+    assert int(plan.gates[1, 3, PL.READY]) == 1 and int(plan.gates[0, 3, PL.ARRIVAL]) == 0
+    assert (0, 1, 2) not in [(s, p, c) for (s, p, c) in tr.timeouts] and \
+        any(c == 2 for (s, p, c) in tr.timeouts)
+
+
+def test_extra_mark_reported():
+    plan, write_unit, order, data, sb = _setup(P=2, n=2)
+    status, short, extra = ThreadedRound(plan, write_unit, order, extra={(1, 0)}).run()
+    assert status == PL.EXTRA and extra == [1]
+
+
+def test_close_mid_round_drains():
+    plan, write_unit, order, data, sb = _setup(P=2, n=2)
+    tr = ThreadedRound(plan, write_unit, order, max_polls=100000, skip={(1, 0), (3, 0)})
+    assert tr.run(close_after=0.05) is None
+    assert plan.state == "CLOSED"
+    # every chunk was delivered once; the gates of the unmarked chunks were opened by close
+    assert all(int(plan.gates[p, c, PL.ARRIVAL]) == 1
+               for c in range(plan.G) for p in range(2) if p != plan.owner[c])
+
+
+@pytest.mark.parametrize("P", [2, 3, 8])
+def test_barrier_threads(P):
+    ys = barrier_threads(P, gen_calls=3)
+    for r in range(P):
+        want = np.full(P, 3)
+        want[r] = 0
+        assert np.array_equal(ys[r], want)
