@@ -1,0 +1,445 @@
+"""Python binding of the triggered-plan library (libdtt.so, C ABI in include/dtt.h).
+
+Argument marshalling only: every step of the path -- gate polls, copies, marks, checks,
+barriers -- runs in the library's CUDA kernels.  PyTorch supplies device memory and streams;
+buffers may be passed as torch tensors (their data pointer is used) or as integer device
+addresses.  The functions keep the C names (``dtt_plan_create`` ...); ``Plan`` and ``Schedule``
+are small owners around them.  Importing the package does not load the library; the first call
+does, and raises if libdtt.so has not been built (build with
+``python -m device_triggered_transfers_gb300.build``).
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+from typing import List, Optional, Sequence
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libdtt.so")
+
+MAX_RANKS = 16
+REPORT_MAX = 64
+GATE_WORDS = 8
+(GATE_READY, GATE_ARRIVAL, GATE_COMPLETION, GATE_ERROR, GATE_COUNTER, GATE_T_OPEN,
+ GATE_T_ARRIVE, GATE_COPIER) = range(8)
+
+OK, EINVAL, EOUTOFROWS, EOVERLAP, ECAPACITY, EROUNDLIMIT, ESTATE, EEXTRA, ETIMEDOUT, ECUDA, \
+    ENOMEM = 0, -1, -2, -3, -4, -5, -6, -7, -8, -9, -10
+ERROR_NAMES = {OK: "OK", EINVAL: "EINVAL", EOUTOFROWS: "EOUTOFROWS", EOVERLAP: "EOVERLAP",
+               ECAPACITY: "ECAPACITY", EROUNDLIMIT: "EROUNDLIMIT", ESTATE: "ESTATE",
+               EEXTRA: "EEXTRA", ETIMEDOUT: "ETIMEDOUT", ECUDA: "ECUDA", ENOMEM: "ENOMEM"}
+PREPARED, RUNNING, DONE, FAILED, CLOSING, CLOSED = range(6)
+BF16, F32, U8 = 0, 1, 2
+DTYPE_CODES = {"bf16": BF16, "f32": F32, "u8": U8}
+COPY_VEC16, COPY_TMA = 0, 1
+ORDER_ROW_MAJOR, ORDER_GROUPED = 0, 1
+MARK_PER_STEP, MARK_AT_END = 0, 1
+
+
+class dtt_region(C.Structure):
+    _fields_ = [("offset", C.c_uint64), ("row_bytes", C.c_uint64), ("rows", C.c_uint64),
+                ("pitch", C.c_uint64)]
+
+
+class dtt_order(C.Structure):
+    _fields_ = [("kind", C.c_uint32), ("group_m", C.c_uint32)]
+
+
+class dtt_plan_opts(C.Structure):
+    _fields_ = [("allgather", C.c_uint32), ("method", C.c_uint32), ("copier_ctas", C.c_uint32),
+                ("ctas_per_sm", C.c_uint32), ("copier_threads", C.c_uint32),
+                ("piece_bytes", C.c_uint32), ("timestamps", C.c_uint32),
+                ("initial_round", C.c_uint32), ("max_polls", C.c_uint64),
+                ("max_regions", C.c_uint64)]
+
+
+class dtt_handle(C.Structure):
+    _fields_ = [("gates", C.c_void_p), ("writers", C.c_void_p), ("status", C.c_void_p),
+                ("round", C.c_uint32), ("rank", C.c_uint32), ("P", C.c_uint32),
+                ("n_global", C.c_uint32), ("first_chunk", C.c_uint32), ("n_chunks", C.c_uint32),
+                ("flags", C.c_uint32), ("reserved", C.c_uint32)]
+
+
+class dtt_report(C.Structure):
+    _fields_ = [("status", C.c_int32), ("n_short", C.c_uint32), ("n_extra", C.c_uint32),
+                ("copier_timeouts", C.c_uint32), ("device_status", C.c_uint32),
+                ("round", C.c_uint32), ("short_chunks", C.c_uint32 * REPORT_MAX),
+                ("extra_chunks", C.c_uint32 * REPORT_MAX)]
+
+    @property
+    def shorts(self) -> List[int]:
+        return list(self.short_chunks[:min(self.n_short, REPORT_MAX)])
+
+    @property
+    def extras(self) -> List[int]:
+        return list(self.extra_chunks[:min(self.n_extra, REPORT_MAX)])
+
+
+class dtt_fill_desc(C.Structure):
+    _fields_ = [("dtype", C.c_uint32), ("seed", C.c_uint32), ("M", C.c_uint64),
+                ("N", C.c_uint64), ("pitch", C.c_uint64), ("buf_bytes", C.c_uint64),
+                ("slice_off", C.c_uint64 * MAX_RANKS),
+                ("BM", C.c_uint32), ("BN", C.c_uint32), ("num_programs", C.c_uint32),
+                ("tiles_per_chunk", C.c_uint32), ("order", dtt_order),
+                ("mark_mode", C.c_uint32), ("cluster", C.c_uint32), ("rank_mask", C.c_uint32),
+                ("threads", C.c_uint32)]
+
+
+ORDER_FN = C.CFUNCTYPE(C.c_int, C.c_uint64, C.c_void_p, C.POINTER(C.c_uint32),
+                       C.POINTER(C.c_uint32))
+
+_P = C.c_void_p
+_u32, _u64, _i32 = C.c_uint32, C.c_uint64, C.c_int32
+_SIGS = {
+    "dtt_last_error": (C.c_char_p, []),
+    "dtt_tile_of": (C.c_int, [C.POINTER(dtt_order), _u64, _u32, _u32, C.POINTER(_u32), C.POINTER(_u32)]),
+    "dtt_schedule_whole": (C.c_int, [_u64, _u64, _u64, _u64, _u32, C.POINTER(_P)]),
+    "dtt_schedule_chunks": (C.c_int, [_u64, _u64, _u64, _u64, _u32, C.POINTER(_P)]),
+    "dtt_schedule_tile_chunks": (C.c_int, [_u64, _u64, _u64, _u32, _u64, _u32, _u32, _u32,
+                                           C.POINTER(dtt_order), ORDER_FN, _P, C.POINTER(_P)]),
+    "dtt_schedule_empty": (C.c_int, [C.POINTER(_P)]),
+    "dtt_schedule_add_chunk": (C.c_int, [_P, C.POINTER(dtt_region), _u32, _u32]),
+    "dtt_schedule_info": (C.c_int, [_P, C.POINTER(_u32), C.POINTER(_u64)]),
+    "dtt_schedule_get": (C.c_int, [_P, _u32, C.POINTER(dtt_region), _u64, C.POINTER(_u64), C.POINTER(_u32)]),
+    "dtt_schedule_free": (None, [_P]),
+    "dtt_plan_opts_default": (None, [C.POINTER(dtt_plan_opts)]),
+    "dtt_plan_create": (C.c_int, [C.POINTER(_P), _u64, _u32, C.POINTER(_P), C.POINTER(dtt_plan_opts),
+                                  _P, C.POINTER(_P)]),
+    "dtt_plan_start": (C.c_int, [_P, _P, C.POINTER(dtt_handle)]),
+    "dtt_plan_handle": (C.c_int, [_P, _u32, C.POINTER(dtt_handle)]),
+    "dtt_plan_wait": (C.c_int, [_P, C.POINTER(dtt_report)]),
+    "dtt_plan_next_round": (C.c_int, [_P]),
+    "dtt_plan_close": (C.c_int, [_P]),
+    "dtt_plan_state": (C.c_int, [_P]),
+    "dtt_plan_round": (C.c_uint32, [_P]),
+    "dtt_plan_info": (C.c_int, [_P, C.POINTER(_u32), C.POINTER(_u32), C.POINTER(_u32), C.POINTER(_P)]),
+    "dtt_plan_read_gates": (C.c_int, [_P, C.POINTER(_u64), _u64]),
+    "dtt_allgather_host": (C.c_int, [_P, C.POINTER(_P), _P, _u32, _P, C.POINTER(dtt_report)]),
+    "dtt_fill_producer": (C.c_int, [C.POINTER(_P), _u32, C.POINTER(dtt_fill_desc),
+                                    C.POINTER(dtt_handle), _P]),
+    "dtt_publish": (C.c_int, [C.POINTER(dtt_handle), _u32, _u32, _u32, _u32, _P]),
+    "dtt_consumer_gather": (C.c_int, [_P, _u32, _P, _u64, _P, _u32, _P]),
+    "dtt_barrier_handrolled": (C.c_int, [C.POINTER(_P), C.POINTER(_P), _u32, _u32, _u64, _P, _P]),
+    "dtt_barrier_create": (C.c_int, [_u32, C.POINTER(_P)]),
+    "dtt_barrier_destroy": (None, [_P]),
+    "dtt_barrier_reveal": (C.c_int, [_P, C.POINTER(_P), C.POINTER(_P), C.POINTER(_P), _u32, _u64,
+                                     _P, _P]),
+}
+
+_lib = None
+
+
+def lib():
+    """The loaded libdtt.so (raises if it has not been built: there is no fallback)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"libdtt.so not built at {LIB_PATH}; run "
+                              "python -m device_triggered_transfers_gb300.build")
+        L = C.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGS.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = L
+    return _lib
+
+
+class DttError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"{ERROR_NAMES.get(code, code)}: {msg}")
+        self.code = code
+
+
+def _check(rc: int) -> int:
+    if rc != OK:
+        raise DttError(rc, lib().dtt_last_error().decode(errors="replace"))
+    return rc
+
+
+def _ptr(x) -> int:
+    """Device (or host) address of a torch tensor, or an integer address."""
+    if x is None:
+        return 0
+    if isinstance(x, int):
+        return x
+    return int(x.data_ptr())
+
+
+def _stream(s) -> int:
+    if s is None:
+        return 0
+    if isinstance(s, int):
+        return s
+    return int(s.cuda_stream)
+
+
+def _ptr_array(xs) -> C.Array:
+    arr = (C.c_void_p * max(1, len(xs)))()
+    for i, x in enumerate(xs):
+        arr[i] = _ptr(x) or None
+    return arr
+
+
+# ---- schedules --------------------------------------------------------------------------------
+class Schedule:
+    """Owner of a dtt_schedule*."""
+
+    def __init__(self, handle: int):
+        self._h = C.c_void_p(handle)
+
+    @property
+    def handle(self) -> C.c_void_p:
+        return self._h
+
+    def info(self):
+        n, r = _u32(), _u64()
+        _check(lib().dtt_schedule_info(self._h, C.byref(n), C.byref(r)))
+        return n.value, r.value
+
+    @property
+    def n_chunks(self) -> int:
+        return self.info()[0]
+
+    def chunk(self, i: int):
+        """(list of (offset, row_bytes, rows, pitch), writers) of chunk i."""
+        n, w = _u64(), _u32()
+        _check(lib().dtt_schedule_get(self._h, i, None, 0, C.byref(n), C.byref(w)))
+        regs = (dtt_region * max(1, n.value))()
+        _check(lib().dtt_schedule_get(self._h, i, regs, n.value, C.byref(n), C.byref(w)))
+        return [(r.offset, r.row_bytes, r.rows, r.pitch) for r in regs[:n.value]], w.value
+
+    def chunks(self):
+        return [self.chunk(i) for i in range(self.n_chunks)]
+
+    def add_chunk(self, regions, writers: int) -> None:
+        arr = (dtt_region * max(1, len(regions)))(*[dtt_region(*r) for r in regions])
+        _check(lib().dtt_schedule_add_chunk(self._h, arr, len(regions), writers))
+
+    def free(self) -> None:
+        if self._h and self._h.value:
+            lib().dtt_schedule_free(self._h)
+            self._h = C.c_void_p(0)
+
+    def __del__(self):
+        try:
+            self.free()
+        except Exception:
+            pass
+
+
+def dtt_schedule_whole(base_off, rows, row_bytes, pitch, num_programs) -> Schedule:
+    out = C.c_void_p()
+    _check(lib().dtt_schedule_whole(base_off, rows, row_bytes, pitch, num_programs, C.byref(out)))
+    return Schedule(out.value)
+
+
+def dtt_schedule_chunks(base_off, rows, row_bytes, pitch, num_chunks) -> Schedule:
+    out = C.c_void_p()
+    _check(lib().dtt_schedule_chunks(base_off, rows, row_bytes, pitch, num_chunks, C.byref(out)))
+    return Schedule(out.value)
+
+
+def dtt_schedule_tile_chunks(base_off, M, N, elem_bytes, pitch, BM, BN, tiles_per_chunk,
+                             order_kind=ORDER_ROW_MAJOR, group_m=0, order_fn=None) -> Schedule:
+    """order_fn: optional Python callable step -> (tm, tn) (host-side mapping)."""
+    out = C.c_void_p()
+    order = dtt_order(order_kind, group_m)
+    if order_fn is not None:
+        def cb(step, ctx, tm, tn):
+            try:
+                a, b = order_fn(step)
+                tm[0], tn[0] = a, b
+                return 0
+            except Exception:
+                return 1
+        fn = ORDER_FN(cb)
+    else:
+        fn = ORDER_FN()
+    _check(lib().dtt_schedule_tile_chunks(base_off, M, N, elem_bytes, pitch, BM, BN, tiles_per_chunk,
+                                          C.byref(order), fn, None, C.byref(out)))
+    return Schedule(out.value)
+
+
+def dtt_schedule_empty() -> Schedule:
+    out = C.c_void_p()
+    _check(lib().dtt_schedule_empty(C.byref(out)))
+    return Schedule(out.value)
+
+
+def dtt_tile_of(order_kind, group_m, step, tiles_m, tiles_n):
+    tm, tn = _u32(), _u32()
+    order = dtt_order(order_kind, group_m)
+    _check(lib().dtt_tile_of(C.byref(order), step, tiles_m, tiles_n, C.byref(tm), C.byref(tn)))
+    return tm.value, tn.value
+
+
+# ---- plans ------------------------------------------------------------------------------------
+def dtt_plan_opts_default(**over) -> dtt_plan_opts:
+    o = dtt_plan_opts()
+    lib().dtt_plan_opts_default(C.byref(o))
+    for k, v in over.items():
+        setattr(o, k, v)
+    return o
+
+
+class Plan:
+    """Owner of a dtt_plan* over P device buffers (kept alive here)."""
+
+    def __init__(self, bufs: Sequence, buf_bytes: int, schedules: Sequence[Optional[Schedule]],
+                 opts: Optional[dtt_plan_opts] = None, copy_stream=None):
+        self.bufs = list(bufs)
+        self.P = len(self.bufs)
+        self.buf_bytes = buf_bytes
+        self.copy_stream = copy_stream
+        scheds = (C.c_void_p * self.P)(*[(s.handle.value if s is not None else None)
+                                         for s in schedules])
+        out = C.c_void_p()
+        _check(lib().dtt_plan_create(_ptr_array(self.bufs), buf_bytes, self.P, scheds,
+                                     C.byref(opts) if opts is not None else None,
+                                     _stream(copy_stream), C.byref(out)))
+        self._h = out
+        self.handles = (dtt_handle * self.P)()
+
+    # the round
+    def start(self, producer_stream=None):
+        _check(lib().dtt_plan_start(self._h, _stream(producer_stream), self.handles))
+        return self.handles
+
+    def handle(self, rank: int) -> dtt_handle:
+        h = dtt_handle()
+        _check(lib().dtt_plan_handle(self._h, rank, C.byref(h)))
+        return h
+
+    def wait(self, raise_on_error: bool = True) -> dtt_report:
+        rep = dtt_report()
+        rc = lib().dtt_plan_wait(self._h, C.byref(rep))
+        if raise_on_error:
+            _check(rc)
+        return rep
+
+    def next_round(self) -> int:
+        _check(lib().dtt_plan_next_round(self._h))
+        return self.round
+
+    def close(self) -> None:
+        if self._h and self._h.value:
+            h, self._h = self._h, C.c_void_p(0)
+            _check(lib().dtt_plan_close(h))
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+        return False
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    @property
+    def state(self) -> int:
+        return lib().dtt_plan_state(self._h)
+
+    @property
+    def round(self) -> int:
+        return lib().dtt_plan_round(self._h)
+
+    def info(self):
+        n = _u32()
+        first = (C.c_uint32 * self.P)()
+        cnt = (C.c_uint32 * self.P)()
+        gates = C.c_void_p()
+        _check(lib().dtt_plan_info(self._h, C.byref(n), first, cnt, C.byref(gates)))
+        return n.value, list(first), list(cnt), gates.value
+
+    def read_gates(self) -> np.ndarray:
+        """The P gate tables as a uint64 array [P, n_global, 8]."""
+        n = self.info()[0]
+        out = np.zeros((self.P, n, GATE_WORDS), dtype=np.uint64)
+        _check(lib().dtt_plan_read_gates(self._h, out.ctypes.data_as(C.POINTER(_u64)), out.size))
+        return out
+
+    def allgather_host(self, host_slices: Sequence, host_out=None, out_rank: int = 0,
+                       stream=None, raise_on_error: bool = True) -> dtt_report:
+        rep = dtt_report()
+        rc = lib().dtt_allgather_host(self._h, _ptr_array(host_slices), _ptr(host_out) or None,
+                                      out_rank, _stream(stream), C.byref(rep))
+        if raise_on_error:
+            _check(rc)
+        return rep
+
+    def consumer_gather(self, rank: int, dst, max_polls: int, status, ctas: int, stream) -> None:
+        _check(lib().dtt_consumer_gather(self._h, rank, _ptr(dst), max_polls, _ptr(status), ctas,
+                                         _stream(stream)))
+
+
+def dtt_plan_create(bufs, buf_bytes, schedules, opts=None, copy_stream=None) -> Plan:
+    return Plan(bufs, buf_bytes, schedules, opts, copy_stream)
+
+
+# ---- producers and barriers -----------------------------------------------------------------
+def fill_desc(dtype: str, seed: int, M: int, N: int, pitch: int, buf_bytes: int,
+              slice_offs: Sequence[int], BM: int, BN: int, num_programs: int, tiles_per_chunk: int,
+              order_kind=ORDER_ROW_MAJOR, group_m=0, mark_mode=MARK_PER_STEP, cluster=1,
+              rank_mask=None, threads=0) -> dtt_fill_desc:
+    d = dtt_fill_desc()
+    d.dtype = DTYPE_CODES[dtype]
+    d.seed = seed & 0xFFFFFFFF
+    d.M, d.N, d.pitch, d.buf_bytes = M, N, pitch, buf_bytes
+    for i, o in enumerate(slice_offs):
+        d.slice_off[i] = o
+    d.BM, d.BN, d.num_programs, d.tiles_per_chunk = BM, BN, num_programs, tiles_per_chunk
+    d.order = dtt_order(order_kind, group_m)
+    d.mark_mode, d.cluster = mark_mode, cluster
+    d.rank_mask = ((1 << len(slice_offs)) - 1) if rank_mask is None else rank_mask
+    d.threads = threads
+    return d
+
+
+def dtt_fill_producer(bufs, desc: dtt_fill_desc, handles, stream=None) -> None:
+    _check(lib().dtt_fill_producer(_ptr_array(bufs), len(bufs), C.byref(desc), handles,
+                                   _stream(stream)))
+
+
+def dtt_publish(handles, first_chunk: int, n_chunks: int, marks: int = 0, stream=None) -> None:
+    _check(lib().dtt_publish(handles, len(handles), first_chunk, n_chunks, marks, _stream(stream)))
+
+
+def dtt_barrier_handrolled(signal, y, gen: int, max_polls: int, status, stream=None) -> None:
+    _check(lib().dtt_barrier_handrolled(_ptr_array(signal), _ptr_array(y), len(signal), gen,
+                                        max_polls, _ptr(status), _stream(stream)))
+
+
+class Barrier:
+    """Owner of the builtin barrier's state (dtt_barrier*)."""
+
+    def __init__(self, P: int):
+        out = C.c_void_p()
+        _check(lib().dtt_barrier_create(P, C.byref(out)))
+        self._h = out
+        self.P = P
+
+    def reveal(self, x, data, y, size: int, max_polls: int, status, stream=None) -> None:
+        _check(lib().dtt_barrier_reveal(self._h, _ptr_array(x), _ptr_array(data), _ptr_array(y),
+                                        size, max_polls, _ptr(status), _stream(stream)))
+
+    def destroy(self) -> None:
+        if self._h and self._h.value:
+            lib().dtt_barrier_destroy(self._h)
+            self._h = C.c_void_p(0)
+
+    def __del__(self):
+        try:
+            self.destroy()
+        except Exception:
+            pass
+
+
+def dtt_barrier_create(P: int) -> Barrier:
+    return Barrier(P)

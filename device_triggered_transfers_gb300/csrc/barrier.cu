@@ -1,0 +1,176 @@
+// The N-rank notify/wait barrier over virtual ranks (PyPTO, "Barrier: Signals Only").
+//
+// Every virtual rank is one CTA of one cooperative launch, so the ranks that wait on one
+// another are guaranteed to be resident together.  Thread 0 of each CTA does the rank's
+// notifies (atomic add, release, gpu scope) and waits (acquire loads, counted polls); a CTA
+// barrier then hands the result to the other threads.
+#include <cstdint>
+#include <new>
+
+#include "internal.h"
+
+namespace dtt {
+namespace {
+
+__device__ __forceinline__ void red_release_add_s32(int32_t* p, int32_t v) {
+    asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ int32_t ld_acquire_s32(const int32_t* p) {
+    int32_t v;
+    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ int32_t ld_relaxed_s32(const int32_t* p) {
+    int32_t v;
+    asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Notify row `me` of every peer's window, then wait for row src >= gen of my window for every
+// src != me.  window(q) returns rank q's window.  Thread 0 only.
+template <class Window>
+__device__ __forceinline__ int notify_wait(Window window, uint32_t me, uint32_t P, int32_t gen,
+                                           uint64_t max_polls) {
+    for (uint32_t peer = 0; peer < P; ++peer)
+        if (peer != me) red_release_add_s32(window(peer) + me, 1);
+    int rc = 0;
+    for (uint32_t src = 0; src < P && rc == 0; ++src) {
+        if (src == me) continue;
+        const int32_t* cell = window(me) + src;
+        uint64_t i = 0;
+        uint32_t ns = 0;
+        while (ld_acquire_s32(cell) < gen) {
+            if (++i >= max_polls) { rc = DTT_ETIMEDOUT; break; }
+            __nanosleep(ns);
+            ns = ns < 256 ? ns + 32 : 256;
+        }
+    }
+    return rc;
+}
+
+struct HandrolledParams {
+    int32_t* signal[DTT_MAX_RANKS];
+    int32_t* y[DTT_MAX_RANKS];
+    int32_t* status;
+    uint32_t P;
+    int32_t gen;
+    uint64_t max_polls;
+};
+
+__global__ void handrolled_kernel(const __grid_constant__ HandrolledParams p) {
+    const uint32_t me = blockIdx.x;
+    if (threadIdx.x == 0) {
+        auto window = [&](uint32_t q) { return p.signal[q]; };
+        p.status[me] = notify_wait(window, me, p.P, p.gen, p.max_polls);
+    }
+    __syncthreads();
+    // the observable: this rank's window, read cell by cell after the waits
+    for (uint32_t i = threadIdx.x; i < p.P; i += blockDim.x) p.y[me][i] = ld_relaxed_s32(p.signal[me] + i);
+}
+
+struct RevealParams {
+    const int32_t* x[DTT_MAX_RANKS];
+    int32_t* data[DTT_MAX_RANKS];
+    int32_t* y[DTT_MAX_RANKS];
+    int32_t* counters;     // P x P internal windows, row-major by rank
+    int32_t* status;
+    uint32_t P;
+    uint32_t size;
+    int32_t gen;
+    uint64_t max_polls;
+};
+
+__global__ void reveal_kernel(const __grid_constant__ RevealParams p) {
+    const uint32_t me = blockIdx.x;
+    for (uint32_t i = threadIdx.x; i < p.size; i += blockDim.x) p.data[me][i] = p.x[me][i];
+    __syncthreads();   // the staged slice precedes thread 0's release notifies
+    if (threadIdx.x == 0) {
+        auto window = [&](uint32_t q) { return p.counters + (uint64_t)q * p.P; };
+        p.status[me] = notify_wait(window, me, p.P, p.gen, p.max_polls);
+    }
+    __syncthreads();
+    const int32_t* peer = p.data[(me + 1) % p.P];
+    for (uint32_t i = threadIdx.x; i < p.size; i += blockDim.x) p.y[me][i] = ld_relaxed_s32(peer + i);
+}
+
+}  // namespace
+}  // namespace dtt
+
+struct dtt_barrier {
+    uint32_t P = 0;
+    int32_t* d_counters = nullptr;
+    int32_t gen = 0;
+};
+
+using namespace dtt;
+
+extern "C" {
+
+int dtt_barrier_handrolled(int32_t* const* signal, int32_t* const* y, uint32_t P, uint32_t gen,
+                           uint64_t max_polls, int32_t* status, cudaStream_t stream) {
+    if (!signal || !y || !status || P < 1 || P > DTT_MAX_RANKS || gen < 1 || gen > 0x7FFFFFFFu)
+        return fail(DTT_EINVAL, "dtt_barrier_handrolled: bad args");
+    HandrolledParams hp{};
+    for (uint32_t r = 0; r < P; ++r) {
+        if (!signal[r] || !y[r]) return fail(DTT_EINVAL, "dtt_barrier_handrolled: NULL window");
+        hp.signal[r] = signal[r];
+        hp.y[r] = y[r];
+    }
+    hp.status = status;
+    hp.P = P;
+    hp.gen = (int32_t)gen;
+    hp.max_polls = max_polls;
+    void* args[] = {&hp};
+    DTT_CUDA_TRY(cudaLaunchCooperativeKernel((const void*)handrolled_kernel, dim3(P), dim3(32), args, 0, stream));
+    return DTT_OK;
+}
+
+int dtt_barrier_create(uint32_t P, dtt_barrier** out) {
+    if (!out || P < 1 || P > DTT_MAX_RANKS) return fail(DTT_EINVAL, "dtt_barrier_create: bad args");
+    dtt_barrier* b = new (std::nothrow) dtt_barrier();
+    if (!b) return fail(DTT_ENOMEM, "dtt_barrier_create: out of memory");
+    b->P = P;
+    cudaError_t e = cudaMalloc(&b->d_counters, (size_t)P * P * sizeof(int32_t));
+    if (e == cudaSuccess) e = cudaMemset(b->d_counters, 0, (size_t)P * P * sizeof(int32_t));
+    if (e != cudaSuccess) {
+        cudaFree(b->d_counters);
+        delete b;
+        return fail(DTT_ECUDA, "dtt_barrier_create: %s", cudaGetErrorString(e));
+    }
+    *out = b;
+    return DTT_OK;
+}
+
+void dtt_barrier_destroy(dtt_barrier* b) {
+    if (!b) return;
+    cudaFree(b->d_counters);
+    delete b;
+}
+
+int dtt_barrier_reveal(dtt_barrier* b, const int32_t* const* x, int32_t* const* data,
+                       int32_t* const* y, uint32_t size, uint64_t max_polls, int32_t* status,
+                       cudaStream_t stream) {
+    if (!b || !x || !data || !y || !status) return fail(DTT_EINVAL, "dtt_barrier_reveal: bad args");
+    if (b->gen == 0x7FFFFFFF) return fail(DTT_EROUNDLIMIT, "dtt_barrier_reveal: generation limit reached");
+    RevealParams rp{};
+    for (uint32_t r = 0; r < b->P; ++r) {
+        if (!x[r] || !data[r] || !y[r]) return fail(DTT_EINVAL, "dtt_barrier_reveal: NULL slice");
+        rp.x[r] = x[r];
+        rp.data[r] = data[r];
+        rp.y[r] = y[r];
+    }
+    rp.counters = b->d_counters;
+    rp.status = status;
+    rp.P = b->P;
+    rp.size = size;
+    rp.gen = b->gen + 1;
+    rp.max_polls = max_polls;
+    void* args[] = {&rp};
+    DTT_CUDA_TRY(cudaLaunchCooperativeKernel((const void*)reveal_kernel, dim3(b->P), dim3(256), args, 0, stream));
+    b->gen += 1;
+    return DTT_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,219 @@
+// The hashed-fill producer: a persistent tiled producer that writes hash(seed, rank, round,
+// row, col) values into each rank's slice and marks chunks as it goes ("Triggered Plans",
+// section Model: program p takes steps p, p + num_programs, ..., stores the step's tile and
+// marks first_chunk + step / num_programs).  One launch covers every virtual rank
+// (blockIdx.y = rank).  A program is one CTA, or a thread-block cluster whose CTAs split each
+// tile by rows and mark once per step through dtt_mark_ready_cluster.
+#include <cstdint>
+
+#include <cuda_bf16.h>
+
+#include "dtt_device.cuh"
+#include "internal.h"
+#include "order.h"
+
+namespace dtt {
+namespace {
+
+struct FillParams {
+    char* bufs[DTT_MAX_RANKS];
+    dtt_handle h[DTT_MAX_RANKS];
+    uint64_t slice_off[DTT_MAX_RANKS];
+    uint64_t M, N, pitch;
+    uint32_t seed, BM, BN, NP, TPC;
+    uint32_t order_kind, group_m, mark_mode, cluster, rank_mask;
+    uint32_t vec;    // 16-byte stores allowed (bases, offsets, pitch and BN*elem aligned)
+};
+
+// MurmurHash3's 32-bit finaliser (public-domain hash by Austin Appleby).
+__device__ __forceinline__ uint32_t fmix32(uint32_t h) {
+    h ^= h >> 16;
+    h *= 0x85EBCA6Bu;
+    h ^= h >> 13;
+    h *= 0xC2B2AE35u;
+    h ^= h >> 16;
+    return h;
+}
+
+// ((h >> 8) - 2^23) * 2^-23: an exact float in [-1, 1).
+__device__ __forceinline__ float uniform(uint32_t h) {
+    return (float)((int32_t)(h >> 8) - (1 << 23)) * 0x1p-23f;
+}
+
+template <int DT> struct Elem;
+template <> struct Elem<DTT_BF16> {
+    static constexpr int bytes = 2;
+    static __device__ __forceinline__ uint4 pack(uint32_t salt, uint32_t idx) {
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const __nv_bfloat162 v = __floats2bfloat162_rn(uniform(fmix32((idx + 2 * i) ^ salt)),
+                                                           uniform(fmix32((idx + 2 * i + 1) ^ salt)));
+            w[i] = *reinterpret_cast<const uint32_t*>(&v);
+        }
+        return make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    static __device__ __forceinline__ void scalar(char* p, uint32_t salt, uint32_t idx) {
+        *reinterpret_cast<__nv_bfloat16*>(p) = __float2bfloat16_rn(uniform(fmix32(idx ^ salt)));
+    }
+};
+template <> struct Elem<DTT_F32> {
+    static constexpr int bytes = 4;
+    static __device__ __forceinline__ uint4 pack(uint32_t salt, uint32_t idx) {
+        return make_uint4(__float_as_uint(uniform(fmix32(idx ^ salt))),
+                          __float_as_uint(uniform(fmix32((idx + 1) ^ salt))),
+                          __float_as_uint(uniform(fmix32((idx + 2) ^ salt))),
+                          __float_as_uint(uniform(fmix32((idx + 3) ^ salt))));
+    }
+    static __device__ __forceinline__ void scalar(char* p, uint32_t salt, uint32_t idx) {
+        *reinterpret_cast<float*>(p) = uniform(fmix32(idx ^ salt));
+    }
+};
+template <> struct Elem<DTT_U8> {
+    static constexpr int bytes = 1;
+    static __device__ __forceinline__ uint4 pack(uint32_t salt, uint32_t idx) {
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            uint32_t x = 0;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) x |= (fmix32((idx + 4 * i + k) ^ salt) & 0xFFu) << (8 * k);
+            w[i] = x;
+        }
+        return make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    static __device__ __forceinline__ void scalar(char* p, uint32_t salt, uint32_t idx) {
+        *reinterpret_cast<uint8_t*>(p) = (uint8_t)(fmix32(idx ^ salt) & 0xFFu);
+    }
+};
+
+// Write rows [ra, rb) x cols [c0, c0 + cols) of rank r's slice.
+template <int DT>
+__device__ __forceinline__ void write_block(const FillParams& p, char* base, uint32_t salt,
+                                            uint64_t ra, uint64_t rb, uint64_t c0, uint64_t cols) {
+    using E = Elem<DT>;
+    constexpr uint32_t VPE = 16 / E::bytes;     // elements per 16-byte vector
+    if (ra >= rb || cols == 0) return;
+    const uint64_t nrows = rb - ra;
+    uint64_t nvec = 0;
+    if (p.vec) {
+        nvec = cols / VPE;
+        const uint64_t total = nrows * nvec;
+        for (uint64_t v = threadIdx.x; v < total; v += blockDim.x) {
+            const uint64_t i = v / nvec, k = v - i * nvec;
+            const uint64_t row = ra + i, col = c0 + k * VPE;
+            const uint32_t idx = (uint32_t)(row * p.N + col);
+            *reinterpret_cast<uint4*>(base + row * p.pitch + col * E::bytes) = E::pack(salt, idx);
+        }
+    }
+    const uint64_t done = nvec * VPE, tail = cols - done;
+    if (tail == 0) return;
+    const uint64_t total = nrows * tail;
+    for (uint64_t v = threadIdx.x; v < total; v += blockDim.x) {
+        const uint64_t i = v / tail, k = v - i * tail;
+        const uint64_t row = ra + i, col = c0 + done + k;
+        E::scalar(base + row * p.pitch + col * E::bytes, salt, (uint32_t)(row * p.N + col));
+    }
+}
+
+__device__ __forceinline__ void mark(const dtt_handle& h, uint32_t chunk, uint32_t cluster) {
+    if (cluster > 1)
+        dtt_mark_ready_cluster(h, chunk);
+    else
+        dtt_mark_ready(h, chunk);
+}
+
+template <int DT>
+__global__ void __launch_bounds__(1024) fill_kernel(const __grid_constant__ FillParams p) {
+    const uint32_t r = blockIdx.y;
+    if (!((p.rank_mask >> r) & 1u)) return;
+    const dtt_handle& h = p.h[r];
+    const uint32_t prog = blockIdx.x / p.cluster, crank = blockIdx.x % p.cluster;
+    const uint64_t tiles_m = (p.M + p.BM - 1) / p.BM, tiles_n = (p.N + p.BN - 1) / p.BN;
+    const uint64_t T = tiles_m * tiles_n;
+    const uint32_t salt = fmix32(p.seed ^ fmix32(r ^ fmix32(h.round)));
+    char* base = p.bufs[r] + p.slice_off[r];
+    for (uint64_t step = prog; step < T; step += p.NP) {
+        uint32_t tm, tn;
+        tile_of(p.order_kind, p.group_m, step, (uint32_t)tiles_m, (uint32_t)tiles_n, &tm, &tn);
+        const uint64_t r0 = (uint64_t)tm * p.BM, c0 = (uint64_t)tn * p.BN;
+        const uint64_t rows = min((uint64_t)p.BM, p.M - r0), cols = min((uint64_t)p.BN, p.N - c0);
+        const uint64_t per = (rows + p.cluster - 1) / p.cluster;
+        const uint64_t ra = r0 + min(rows, crank * per), rb = r0 + min(rows, (crank + 1) * per);
+        write_block<DT>(p, base, salt, ra, rb, c0, cols);
+        if (p.mark_mode == DTT_MARK_PER_STEP) mark(h, h.first_chunk + (uint32_t)(step / p.TPC), p.cluster);
+    }
+    if (p.mark_mode == DTT_MARK_AT_END) mark(h, h.first_chunk, p.cluster);
+}
+
+}  // namespace
+}  // namespace dtt
+
+using namespace dtt;
+
+extern "C" int dtt_fill_producer(void* const* bufs, uint32_t P, const dtt_fill_desc* d,
+                                 const dtt_handle* handles, cudaStream_t stream) {
+    if (!bufs || !d || !handles || P < 1 || P > DTT_MAX_RANKS)
+        return fail(DTT_EINVAL, "dtt_fill_producer: bad args");
+    if (d->M == 0 || d->N == 0 || d->BM == 0 || d->BN == 0 || d->num_programs == 0 ||
+        d->tiles_per_chunk == 0)
+        return fail(DTT_EINVAL, "dtt_fill_producer: sizes must be positive");
+    if (d->dtype > DTT_U8 || d->mark_mode > DTT_MARK_AT_END)
+        return fail(DTT_EINVAL, "dtt_fill_producer: bad dtype or mark mode");
+    const uint32_t cluster = d->cluster ? d->cluster : 1;
+    const uint32_t threads = d->threads ? d->threads : 256;
+    if (cluster > 8 || threads % 32 || threads > 1024)
+        return fail(DTT_EINVAL, "dtt_fill_producer: cluster <= 8, threads a multiple of 32 <= 1024");
+    if ((uint64_t)d->num_programs * cluster > 0x7FFFFFFFull)
+        return fail(DTT_EINVAL, "dtt_fill_producer: grid too large");
+    const uint32_t eb = d->dtype == DTT_BF16 ? 2 : d->dtype == DTT_F32 ? 4 : 1;
+    if (d->M > 1 && d->pitch < d->N * eb) return fail(DTT_EINVAL, "dtt_fill_producer: pitch < row bytes");
+    const uint64_t span = (d->M - 1) * d->pitch + d->N * eb;
+    for (uint32_t r = 0; r < P; ++r)
+        if (((d->rank_mask >> r) & 1u) && (d->slice_off[r] > d->buf_bytes || span > d->buf_bytes - d->slice_off[r]))
+            return fail(DTT_EINVAL, "dtt_fill_producer: rank %u's slice runs past its %llu-byte buffer", r,
+                        (unsigned long long)d->buf_bytes);
+    FillParams p{};
+    bool vec = (d->pitch % 16 == 0) && ((uint64_t)d->BN * eb % 16 == 0);
+    for (uint32_t r = 0; r < P; ++r) {
+        p.bufs[r] = static_cast<char*>(bufs[r]);
+        p.h[r] = handles[r];
+        p.slice_off[r] = d->slice_off[r];
+        vec = vec && (reinterpret_cast<uintptr_t>(bufs[r]) % 16 == 0) && (d->slice_off[r] % 16 == 0);
+    }
+    p.M = d->M;
+    p.N = d->N;
+    p.pitch = d->pitch;
+    p.seed = d->seed;
+    p.BM = d->BM;
+    p.BN = d->BN;
+    p.NP = d->num_programs;
+    p.TPC = d->tiles_per_chunk;
+    p.order_kind = d->order.kind;
+    p.group_m = d->order.group_m;
+    p.mark_mode = d->mark_mode;
+    p.cluster = cluster;
+    p.rank_mask = d->rank_mask;
+    p.vec = vec ? 1u : 0u;
+
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(d->num_programs * cluster, P, 1);
+    cfg.blockDim = dim3(threads, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = cluster > 1 ? 1 : 0;
+    cudaError_t e;
+    switch (d->dtype) {
+        case DTT_BF16: e = cudaLaunchKernelEx(&cfg, fill_kernel<DTT_BF16>, p); break;
+        case DTT_F32: e = cudaLaunchKernelEx(&cfg, fill_kernel<DTT_F32>, p); break;
+        default: e = cudaLaunchKernelEx(&cfg, fill_kernel<DTT_U8>, p); break;
+    }
+    if (e != cudaSuccess) return fail(DTT_ECUDA, "dtt_fill_producer: launch failed: %s", cudaGetErrorString(e));
+    return DTT_OK;
+}

@@ -1,0 +1,103 @@
+// Private declarations shared by the library's translation units: error reporting, the
+// copier's descriptor tables and the plan object.  Not part of the C ABI.
+#pragma once
+
+#include <cstdint>
+#include <cstdio>
+#include <string>
+#include <vector>
+
+#include <cuda_runtime.h>
+
+#include "dtt.h"
+
+namespace dtt {
+
+// Thread-local message behind dtt_last_error().
+void set_error(const char* fmt, ...);
+int fail(int code, const char* fmt, ...);
+
+#define DTT_CUDA_TRY(expr)                                                                   \
+    do {                                                                                     \
+        cudaError_t e_ = (expr);                                                             \
+        if (e_ != cudaSuccess)                                                               \
+            return ::dtt::fail(DTT_ECUDA, "%s: %s (%s:%d)", #expr, cudaGetErrorString(e_),   \
+                               __FILE__, __LINE__);                                          \
+    } while (0)
+
+// One unit of copier work: a sub-window of a region (rows x row_bytes, pitch apart) at byte
+// offset `off` of every buffer.  `vec` = 1 when off, row_bytes and pitch are multiples of 16.
+struct PieceDesc {
+    uint64_t off;
+    uint64_t pitch;
+    uint32_t row_bytes;
+    uint32_t rows;
+    uint32_t vec;
+    uint32_t pad;
+};
+
+// Per global chunk: its pieces [piece_begin, piece_begin + n_pieces), the copier CTA of its
+// source that takes piece 0 (`rot`), how many CTAs take part (n_part) and the source rank.
+struct ChunkDesc {
+    uint32_t piece_begin;
+    uint32_t n_pieces;
+    uint32_t rot;
+    uint32_t n_part;
+    uint32_t owner;
+    uint32_t writers;
+    uint64_t bytes;
+};
+
+// Plan-wide device status block.
+struct DevStatus {
+    uint32_t misuse;            // DTT_DEV_* bits from mark_ready
+    uint32_t copier_timeouts;   // copier CTAs that gave up on a gate
+    uint32_t timeout_chunk;     // smallest chunk id a copier CTA gave up on
+    uint32_t pad;
+};
+
+struct CopierParams {
+    char* bufs[DTT_MAX_RANKS];
+    uint64_t* gates;
+    const ChunkDesc* chunks;
+    const PieceDesc* pieces;
+    DevStatus* status;
+    uint32_t cta_base[DTT_MAX_RANKS + 1];
+    uint32_t first_chunk[DTT_MAX_RANKS];
+    uint32_t n_chunks[DTT_MAX_RANKS];
+    uint32_t P;
+    uint32_t n_global;
+    uint32_t round;
+    uint32_t flags;
+    uint64_t max_polls;
+};
+
+struct CheckParams {
+    const uint64_t* gates;
+    const ChunkDesc* chunks;
+    uint32_t P;
+    uint32_t n_global;
+    uint32_t round;
+};
+
+// Kernel launchers (copier.cu, check.cu).
+cudaError_t launch_copier(const CopierParams& p, uint32_t ctas, uint32_t threads, uint32_t method,
+                          cudaStream_t s);
+// Completion check: flags[c] = 0 delivered, 1 short, 2 extra marks.
+cudaError_t launch_check(const CheckParams& p, uint8_t* flags, cudaStream_t s);
+cudaError_t launch_force_open(uint64_t* gates, const ChunkDesc* chunks, uint32_t n_global,
+                              uint32_t round, cudaStream_t s);
+cudaError_t launch_consumer(const CopierParams& p, dtt_handle h, char* dst, uint64_t max_polls,
+                            int32_t* status, uint32_t ctas, cudaStream_t s);
+
+// Host schedule representation (schedule.cpp).
+struct HostChunk {
+    std::vector<dtt_region> regions;
+    uint32_t writers;
+};
+
+}  // namespace dtt
+
+struct dtt_schedule {
+    std::vector<dtt::HostChunk> chunks;
+};

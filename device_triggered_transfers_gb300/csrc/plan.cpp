@@ -1,0 +1,567 @@
+// The host side of a triggered plan: validation, gate tables, copier descriptor tables, and the
+// round state machine start -> wait -> next_round ("Triggered Plans", sections Model, The kernel
+// author's contract, Gates and rounds, Requirements and limits; "Triggered SDMA Plans", API and
+// Design notes).  One process drives all P virtual ranks, so the collective steps of the pages
+// (create, next_round, close) are single calls here.
+#include <algorithm>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "internal.h"
+
+using namespace dtt;
+
+struct dtt_plan {
+    uint32_t P = 0;
+    uint64_t buf_bytes = 0;
+    char* bufs[DTT_MAX_RANKS] = {};
+    dtt_plan_opts opts{};
+    int device = 0;
+
+    uint32_t n_global = 0;
+    uint32_t first_chunk[DTT_MAX_RANKS] = {};
+    uint32_t n_chunks[DTT_MAX_RANKS] = {};
+    std::vector<ChunkDesc> chunks;
+    std::vector<PieceDesc> pieces;
+    std::vector<uint32_t> writers;
+
+    uint32_t copier_ctas = 0;
+    uint32_t copier_threads = 0;
+    uint32_t cta_base[DTT_MAX_RANKS + 1] = {};
+
+    uint64_t* d_gates = nullptr;
+    uint32_t* d_writers = nullptr;
+    ChunkDesc* d_chunks = nullptr;
+    PieceDesc* d_pieces = nullptr;
+    DevStatus* d_status = nullptr;
+    uint8_t* d_flags = nullptr;
+    uint8_t* h_flags = nullptr;       // pinned
+    DevStatus* h_status = nullptr;    // pinned
+
+    cudaStream_t copy_stream = nullptr;
+    bool own_copy_stream = false;
+    cudaStream_t aux_stream = nullptr;
+    cudaEvent_t ev_producer = nullptr;
+    cudaStream_t producer_stream = nullptr;
+
+    int state = DTT_PLAN_PREPARED;
+    uint32_t round = 1;
+};
+
+namespace {
+
+struct RegionRef {
+    uint64_t lo, hi;     // byte extent [lo, hi)
+    uint32_t rank;
+    const dtt_region* reg;
+};
+
+// Do two regions share a byte?  Both are sorted row sets (pitch > 0 or a single row), so a
+// merge over their rows decides it exactly.
+bool regions_intersect(const dtt_region& a, const dtt_region& b) {
+    uint64_t i = 0, j = 0;
+    while (i < a.rows && j < b.rows) {
+        const uint64_t alo = a.offset + i * a.pitch, ahi = alo + a.row_bytes;
+        const uint64_t blo = b.offset + j * b.pitch, bhi = blo + b.row_bytes;
+        if (alo < bhi && blo < ahi) return true;
+        if (ahi <= bhi) ++i; else ++j;
+    }
+    return false;
+}
+
+void free_device(dtt_plan* p) {
+    cudaFree(p->d_gates);
+    cudaFree(p->d_writers);
+    cudaFree(p->d_chunks);
+    cudaFree(p->d_pieces);
+    cudaFree(p->d_status);
+    cudaFree(p->d_flags);
+    cudaFreeHost(p->h_flags);
+    cudaFreeHost(p->h_status);
+    if (p->ev_producer) cudaEventDestroy(p->ev_producer);
+    if (p->aux_stream) cudaStreamDestroy(p->aux_stream);
+    if (p->own_copy_stream && p->copy_stream) cudaStreamDestroy(p->copy_stream);
+    p->d_gates = nullptr;
+    p->d_writers = nullptr;
+    p->d_chunks = nullptr;
+    p->d_pieces = nullptr;
+    p->d_status = nullptr;
+    p->d_flags = nullptr;
+    p->h_flags = nullptr;
+    p->h_status = nullptr;
+    p->ev_producer = nullptr;
+    p->aux_stream = nullptr;
+    p->copy_stream = nullptr;
+}
+
+// Cut one region into copier pieces of at most piece_bytes: whole rows when a row fits,
+// otherwise column pieces of single rows.
+void cut_region(const dtt_region& r, uint64_t piece_bytes, bool bases_aligned,
+                std::vector<PieceDesc>* out) {
+    auto push = [&](uint64_t off, uint64_t rb, uint64_t rows, uint64_t pitch) {
+        PieceDesc pc{};
+        pc.off = off;
+        pc.pitch = rows > 1 ? pitch : rb;
+        pc.row_bytes = (uint32_t)rb;
+        pc.rows = (uint32_t)rows;
+        pc.vec = bases_aligned && (off % 16 == 0) && (rb % 16 == 0) && (rows <= 1 || pitch % 16 == 0);
+        out->push_back(pc);
+    };
+    if (r.rows == 0 || r.row_bytes == 0) return;
+    if (r.row_bytes >= piece_bytes) {
+        for (uint64_t i = 0; i < r.rows; ++i)
+            for (uint64_t c = 0; c < r.row_bytes; c += piece_bytes)
+                push(r.offset + i * r.pitch + c, std::min(piece_bytes, r.row_bytes - c), 1, 0);
+    } else {
+        const uint64_t per = std::max<uint64_t>(1, piece_bytes / r.row_bytes);
+        for (uint64_t i = 0; i < r.rows; i += per)
+            push(r.offset + i * r.pitch, r.row_bytes, std::min(per, r.rows - i), r.pitch);
+    }
+}
+
+dtt_handle make_handle(const dtt_plan* p, uint32_t r) {
+    dtt_handle h{};
+    h.gates = p->d_gates;
+    h.writers = p->d_writers;
+    h.status = &p->d_status->misuse;
+    h.round = p->round;
+    h.rank = r;
+    h.P = p->P;
+    h.n_global = p->n_global;
+    h.first_chunk = p->first_chunk[r];
+    h.n_chunks = p->n_chunks[r];
+    h.flags = p->opts.timestamps ? DTT_HANDLE_TIMESTAMPS : 0u;
+    return h;
+}
+
+CopierParams copier_params(const dtt_plan* p) {
+    CopierParams cp{};
+    for (uint32_t r = 0; r < p->P; ++r) {
+        cp.bufs[r] = p->bufs[r];
+        cp.first_chunk[r] = p->first_chunk[r];
+        cp.n_chunks[r] = p->n_chunks[r];
+    }
+    for (uint32_t r = 0; r <= p->P; ++r) cp.cta_base[r] = p->cta_base[r];
+    cp.gates = p->d_gates;
+    cp.chunks = p->d_chunks;
+    cp.pieces = p->d_pieces;
+    cp.status = p->d_status;
+    cp.P = p->P;
+    cp.n_global = p->n_global;
+    cp.round = p->round;
+    cp.flags = p->opts.timestamps ? DTT_HANDLE_TIMESTAMPS : 0u;
+    cp.max_polls = p->opts.max_polls;
+    return cp;
+}
+
+int validate_plan(dtt_plan* p, const dtt_schedule* const* scheds) {
+    const uint32_t P = p->P;
+    // ---- validation --------------------------------------------------------------------
+    uint64_t S = p->buf_bytes;
+    if (p->opts.allgather) {
+        if (p->buf_bytes % P) return fail(DTT_EINVAL, "plan: buffer does not split into P equal slices");
+        S = p->buf_bytes / P;
+    }
+    std::vector<RegionRef> refs;
+    uint64_t total_regions = 0;
+    for (uint32_t r = 0; r < P; ++r) {
+        const dtt_schedule* s = scheds ? scheds[r] : nullptr;
+        if (!s) continue;
+        for (const HostChunk& ch : s->chunks) {
+            if (ch.writers == 0) return fail(DTT_EINVAL, "plan: rank %u has a chunk with no writers", r);
+            for (const dtt_region& reg : ch.regions) {
+                ++total_regions;
+                if (reg.rows == 0 || reg.row_bytes == 0) continue;
+                if (reg.rows > 1 && reg.pitch < reg.row_bytes)
+                    return fail(DTT_EINVAL, "plan: rank %u region with pitch < row_bytes", r);
+                const uint64_t lo = reg.offset;
+                const uint64_t span = (reg.rows - 1) * reg.pitch + reg.row_bytes;
+                if (lo > p->buf_bytes || span > p->buf_bytes - lo)
+                    return fail(DTT_EINVAL, "plan: rank %u region [%llu, +%llu) outside the %llu-byte buffer",
+                                r, (unsigned long long)lo, (unsigned long long)span,
+                                (unsigned long long)p->buf_bytes);
+                const uint64_t hi = lo + span;
+                if (p->opts.allgather && (lo < r * S || hi > (uint64_t)(r + 1) * S))
+                    return fail(DTT_EOUTOFROWS, "plan: rank %u sends bytes outside its own rows", r);
+                refs.push_back(RegionRef{lo, hi, r, &reg});
+            }
+        }
+    }
+    if (p->opts.max_regions && total_regions > p->opts.max_regions)
+        return fail(DTT_ECAPACITY, "plan: %llu regions exceed the capacity of %llu",
+                    (unsigned long long)total_regions, (unsigned long long)p->opts.max_regions);
+    std::sort(refs.begin(), refs.end(), [](const RegionRef& a, const RegionRef& b) { return a.lo < b.lo; });
+    for (size_t i = 0; i < refs.size(); ++i)
+        for (size_t k = i + 1; k < refs.size() && refs[k].lo < refs[i].hi; ++k)
+            if (refs[k].rank != refs[i].rank && regions_intersect(*refs[i].reg, *refs[k].reg))
+                return fail(DTT_EOVERLAP, "plan: ranks %u and %u send the same bytes", refs[i].rank,
+                            refs[k].rank);
+
+    return DTT_OK;
+}
+
+int build_plan(dtt_plan* p, const dtt_schedule* const* scheds) {
+    const uint32_t P = p->P;
+    // ---- global chunk numbering and copier work ------------------------------------------
+    bool bases_aligned = true;
+    for (uint32_t r = 0; r < P; ++r) bases_aligned &= (reinterpret_cast<uintptr_t>(p->bufs[r]) % 16 == 0);
+    uint64_t src_bytes[DTT_MAX_RANKS] = {};
+    uint32_t n = 0;
+    for (uint32_t r = 0; r < P; ++r) {
+        const dtt_schedule* s = scheds ? scheds[r] : nullptr;
+        p->first_chunk[r] = n;
+        p->n_chunks[r] = s ? (uint32_t)s->chunks.size() : 0;
+        n += p->n_chunks[r];
+        if (s)
+            for (const HostChunk& ch : s->chunks)
+                for (const dtt_region& reg : ch.regions) src_bytes[r] += reg.rows * reg.row_bytes;
+    }
+    p->n_global = n;
+
+    // copier CTAs per sending rank, in proportion to its bytes (at least one each)
+    uint32_t senders = 0;
+    uint64_t all_bytes = 0;
+    for (uint32_t r = 0; r < P; ++r) {
+        if (p->n_chunks[r]) ++senders;
+        all_bytes += src_bytes[r];
+    }
+    uint32_t C = p->copier_ctas;
+    if (C < senders) C = senders;
+    uint32_t G[DTT_MAX_RANKS] = {};
+    uint32_t given = 0;
+    for (uint32_t r = 0; r < P; ++r) {
+        if (!p->n_chunks[r]) continue;
+        uint64_t g = all_bytes ? (uint64_t)C * src_bytes[r] / all_bytes : C / senders;
+        G[r] = (uint32_t)std::max<uint64_t>(1, g);
+        given += G[r];
+    }
+    while (given > C) {   // trim the largest shares
+        uint32_t big = 0;
+        for (uint32_t r = 1; r < P; ++r) if (G[r] > G[big]) big = r;
+        --G[big];
+        --given;
+    }
+    for (uint32_t r = 0; given < C && senders; r = (r + 1) % P)
+        if (p->n_chunks[r]) { ++G[r]; ++given; }
+    p->cta_base[0] = 0;
+    for (uint32_t r = 0; r < P; ++r) p->cta_base[r + 1] = p->cta_base[r] + G[r];
+    p->copier_ctas = std::max<uint32_t>(1, p->cta_base[P]);
+
+    const uint64_t piece_bytes = p->opts.piece_bytes;
+    for (uint32_t r = 0; r < P; ++r) {
+        const dtt_schedule* s = scheds ? scheds[r] : nullptr;
+        if (!s) continue;
+        uint64_t dealt = 0;
+        for (const HostChunk& ch : s->chunks) {
+            ChunkDesc cd{};
+            cd.piece_begin = (uint32_t)p->pieces.size();
+            for (const dtt_region& reg : ch.regions) {
+                cut_region(reg, piece_bytes, bases_aligned, &p->pieces);
+                cd.bytes += reg.rows * reg.row_bytes;
+            }
+            if (p->pieces.size() == cd.piece_begin) {   // an empty chunk still signals arrival
+                PieceDesc empty{};
+                p->pieces.push_back(empty);
+            }
+            cd.n_pieces = (uint32_t)p->pieces.size() - cd.piece_begin;
+            cd.rot = (uint32_t)(dealt % G[r]);
+            cd.n_part = std::min(cd.n_pieces, G[r]);
+            cd.owner = r;
+            cd.writers = ch.writers;
+            dealt += cd.n_pieces;
+            p->chunks.push_back(cd);
+            p->writers.push_back(ch.writers);
+        }
+    }
+    if (p->pieces.size() > 0xFFFFFFFFull) return fail(DTT_ECAPACITY, "plan: too many copier pieces");
+    return DTT_OK;
+}
+
+int upload(dtt_plan* p) {
+    const uint32_t P = p->P, n = p->n_global;
+    const uint64_t prior = p->round - 1;    // gates as they stand after `prior` rounds
+    std::vector<uint64_t> gates((uint64_t)P * n * DTT_GATE_WORDS, 0);
+    for (uint32_t c = 0; c < n; ++c) {
+        const ChunkDesc& cd = p->chunks[c];
+        uint64_t* own = &gates[((uint64_t)cd.owner * n + c) * DTT_GATE_WORDS];
+        own[DTT_GATE_READY] = prior;
+        own[DTT_GATE_COUNTER] = prior * cd.writers;
+        own[DTT_GATE_COMPLETION] = prior * (P - 1);
+        own[DTT_GATE_COPIER] = prior * cd.n_part;
+        for (uint32_t q = 0; q < P; ++q)
+            if (q != cd.owner) gates[((uint64_t)q * n + c) * DTT_GATE_WORDS + DTT_GATE_ARRIVAL] = prior;
+    }
+    const size_t n_gate_bytes = std::max<size_t>(1, gates.size() * sizeof(uint64_t));
+    DTT_CUDA_TRY(cudaMalloc(&p->d_gates, n_gate_bytes));
+    DTT_CUDA_TRY(cudaMalloc(&p->d_writers, std::max<size_t>(1, n * sizeof(uint32_t))));
+    DTT_CUDA_TRY(cudaMalloc(&p->d_chunks, std::max<size_t>(1, n * sizeof(ChunkDesc))));
+    DTT_CUDA_TRY(cudaMalloc(&p->d_pieces, std::max<size_t>(1, p->pieces.size() * sizeof(PieceDesc))));
+    DTT_CUDA_TRY(cudaMalloc(&p->d_status, sizeof(DevStatus)));
+    DTT_CUDA_TRY(cudaMalloc(&p->d_flags, std::max<size_t>(1, n)));
+    DTT_CUDA_TRY(cudaMallocHost(&p->h_flags, std::max<size_t>(1, n)));
+    DTT_CUDA_TRY(cudaMallocHost(&p->h_status, sizeof(DevStatus)));
+    if (!gates.empty())
+        DTT_CUDA_TRY(cudaMemcpy(p->d_gates, gates.data(), gates.size() * sizeof(uint64_t), cudaMemcpyHostToDevice));
+    if (n) {
+        DTT_CUDA_TRY(cudaMemcpy(p->d_writers, p->writers.data(), n * sizeof(uint32_t), cudaMemcpyHostToDevice));
+        DTT_CUDA_TRY(cudaMemcpy(p->d_chunks, p->chunks.data(), n * sizeof(ChunkDesc), cudaMemcpyHostToDevice));
+    }
+    if (!p->pieces.empty())
+        DTT_CUDA_TRY(cudaMemcpy(p->d_pieces, p->pieces.data(), p->pieces.size() * sizeof(PieceDesc),
+                                cudaMemcpyHostToDevice));
+    DevStatus st{};
+    st.timeout_chunk = 0xFFFFFFFFu;
+    DTT_CUDA_TRY(cudaMemcpy(p->d_status, &st, sizeof(st), cudaMemcpyHostToDevice));
+    return DTT_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+void dtt_plan_opts_default(dtt_plan_opts* o) {
+    if (!o) return;
+    std::memset(o, 0, sizeof(*o));
+    o->allgather = 1;
+    o->method = DTT_COPY_VEC16;
+    o->ctas_per_sm = 1;
+    o->copier_threads = 512;
+    o->piece_bytes = 65536;
+    o->timestamps = 1;
+    o->initial_round = 1;
+    o->max_polls = 1ull << 22;
+}
+
+int dtt_plan_create(void* const* bufs, uint64_t buf_bytes, uint32_t P,
+                    const dtt_schedule* const* scheds, const dtt_plan_opts* opts,
+                    cudaStream_t copy_stream, dtt_plan** out) {
+    if (!out) return fail(DTT_EINVAL, "dtt_plan_create: out is NULL");
+    *out = nullptr;
+    if (!bufs || P < 1 || P > DTT_MAX_RANKS || buf_bytes == 0)
+        return fail(DTT_EINVAL, "dtt_plan_create: need 1 <= P <= %d buffers of a positive size", DTT_MAX_RANKS);
+    dtt_plan* p = new (std::nothrow) dtt_plan();
+    if (!p) return fail(DTT_ENOMEM, "dtt_plan_create: out of memory");
+    if (opts) p->opts = *opts; else dtt_plan_opts_default(&p->opts);
+    dtt_plan_opts& o = p->opts;
+    if (o.initial_round == 0) o.initial_round = 1;
+    if (o.max_polls == 0) o.max_polls = 1ull << 22;
+    if (o.piece_bytes == 0) o.piece_bytes = 65536;
+    if (o.copier_threads == 0) o.copier_threads = 512;
+    if (o.ctas_per_sm == 0) o.ctas_per_sm = 1;
+    if (o.piece_bytes % 16 || o.copier_threads % 32 || o.copier_threads > 1024 ||
+        o.method != DTT_COPY_VEC16) {
+        delete p;
+        return fail(DTT_EINVAL, "dtt_plan_create: bad options (piece_bytes %% 16, threads %% 32 <= 1024, method)");
+    }
+    p->P = P;
+    p->buf_bytes = buf_bytes;
+    p->round = o.initial_round;
+    for (uint32_t r = 0; r < P; ++r) {
+        if (!bufs[r]) {
+            delete p;
+            return fail(DTT_EINVAL, "dtt_plan_create: buffer %u is NULL", r);
+        }
+        p->bufs[r] = static_cast<char*>(bufs[r]);
+    }
+    int rc = validate_plan(p, scheds);    // host-only checks come first
+    if (rc != DTT_OK) {
+        delete p;
+        return rc;
+    }
+    int sms = 0;
+    if (cudaGetDevice(&p->device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, p->device) != cudaSuccess) {
+        delete p;
+        return fail(DTT_ECUDA, "dtt_plan_create: no CUDA device");
+    }
+    p->copier_ctas = o.copier_ctas ? o.copier_ctas : (uint32_t)sms * o.ctas_per_sm;
+    p->copier_threads = o.copier_threads;
+    rc = build_plan(p, scheds);
+    if (rc == DTT_OK) rc = upload(p);
+    if (rc == DTT_OK) {
+        if (copy_stream) {
+            p->copy_stream = copy_stream;
+        } else {
+            int lo = 0, hi = 0;
+            cudaDeviceGetStreamPriorityRange(&lo, &hi);
+            if (cudaStreamCreateWithPriority(&p->copy_stream, cudaStreamNonBlocking, hi) != cudaSuccess)
+                rc = fail(DTT_ECUDA, "dtt_plan_create: cannot create the copy stream");
+            else
+                p->own_copy_stream = true;
+        }
+    }
+    if (rc == DTT_OK && cudaStreamCreateWithFlags(&p->aux_stream, cudaStreamNonBlocking) != cudaSuccess)
+        rc = fail(DTT_ECUDA, "dtt_plan_create: cannot create the aux stream");
+    if (rc == DTT_OK && cudaEventCreateWithFlags(&p->ev_producer, cudaEventDisableTiming) != cudaSuccess)
+        rc = fail(DTT_ECUDA, "dtt_plan_create: cannot create an event");
+    if (rc != DTT_OK) {           // all or nothing: free what was prepared
+        free_device(p);
+        delete p;
+        return rc;
+    }
+    p->state = DTT_PLAN_PREPARED;
+    *out = p;
+    return DTT_OK;
+}
+
+int dtt_plan_start(dtt_plan* p, cudaStream_t producer_stream, dtt_handle* handles) {
+    if (!p) return fail(DTT_EINVAL, "dtt_plan_start: NULL plan");
+    if (p->state != DTT_PLAN_PREPARED) return fail(DTT_ESTATE, "dtt_plan_start: plan is not PREPARED (state %d)", p->state);
+    if (producer_stream == p->copy_stream)
+        return fail(DTT_EINVAL, "dtt_plan_start: the producer stream must differ from the copy stream");
+    DevStatus st{};
+    st.timeout_chunk = 0xFFFFFFFFu;
+    DTT_CUDA_TRY(cudaMemcpyAsync(p->d_status, &st, sizeof(st), cudaMemcpyHostToDevice, p->copy_stream));
+    if (p->n_global) {
+        const CopierParams cp = copier_params(p);
+        DTT_CUDA_TRY(launch_copier(cp, p->copier_ctas, p->copier_threads, p->opts.method, p->copy_stream));
+    }
+    p->producer_stream = producer_stream;
+    if (handles)
+        for (uint32_t r = 0; r < p->P; ++r) handles[r] = make_handle(p, r);
+    p->state = DTT_PLAN_RUNNING;
+    return DTT_OK;
+}
+
+int dtt_plan_handle(const dtt_plan* p, uint32_t rank, dtt_handle* out) {
+    if (!p || !out || rank >= p->P) return fail(DTT_EINVAL, "dtt_plan_handle: bad args");
+    *out = make_handle(p, rank);
+    return DTT_OK;
+}
+
+int dtt_plan_wait(dtt_plan* p, dtt_report* report) {
+    if (!p) return fail(DTT_EINVAL, "dtt_plan_wait: NULL plan");
+    if (p->state != DTT_PLAN_RUNNING) return fail(DTT_ESTATE, "dtt_plan_wait: plan is not RUNNING (state %d)", p->state);
+    DTT_CUDA_TRY(cudaEventRecord(p->ev_producer, p->producer_stream));
+    DTT_CUDA_TRY(cudaStreamWaitEvent(p->copy_stream, p->ev_producer, 0));
+    CheckParams ck{};
+    ck.gates = p->d_gates;
+    ck.chunks = p->d_chunks;
+    ck.P = p->P;
+    ck.n_global = p->n_global;
+    ck.round = p->round;
+    if (p->n_global) {
+        DTT_CUDA_TRY(launch_check(ck, p->d_flags, p->copy_stream));
+        DTT_CUDA_TRY(cudaMemcpyAsync(p->h_flags, p->d_flags, p->n_global, cudaMemcpyDeviceToHost, p->copy_stream));
+    }
+    DTT_CUDA_TRY(cudaMemcpyAsync(p->h_status, p->d_status, sizeof(DevStatus), cudaMemcpyDeviceToHost, p->copy_stream));
+    DTT_CUDA_TRY(cudaStreamSynchronize(p->copy_stream));
+    dtt_report rep{};
+    rep.round = p->round;
+    rep.copier_timeouts = p->h_status->copier_timeouts;
+    rep.device_status = p->h_status->misuse;
+    for (uint32_t c = 0; c < p->n_global; ++c) {
+        if (p->h_flags[c] == 2) {
+            if (rep.n_extra < DTT_REPORT_MAX) rep.extra_chunks[rep.n_extra] = c;
+            ++rep.n_extra;
+        } else if (p->h_flags[c] == 1) {
+            if (rep.n_short < DTT_REPORT_MAX) rep.short_chunks[rep.n_short] = c;
+            ++rep.n_short;
+        }
+    }
+    int rc = DTT_OK;
+    if (rep.n_extra) {
+        rc = fail(DTT_EEXTRA, "dtt_plan_wait: %u chunk(s) got extra marks in round %u (first: %u)",
+                  rep.n_extra, p->round, rep.extra_chunks[0]);
+    } else if (rep.device_status) {
+        rc = fail(DTT_EINVAL, "dtt_plan_wait: a producer marked a chunk its rank does not own");
+    } else if (rep.n_short) {
+        rc = fail(DTT_ETIMEDOUT, "dtt_plan_wait: %u chunk(s) short in round %u (first: %u)",
+                  rep.n_short, p->round, rep.short_chunks[0]);
+    }
+    rep.status = rc;
+    if (report) *report = rep;
+    p->state = rc == DTT_OK ? DTT_PLAN_DONE : DTT_PLAN_FAILED;
+    return rc;
+}
+
+int dtt_plan_next_round(dtt_plan* p) {
+    if (!p) return fail(DTT_EINVAL, "dtt_plan_next_round: NULL plan");
+    if (p->state != DTT_PLAN_DONE) return fail(DTT_ESTATE, "dtt_plan_next_round: plan is not DONE (state %d)", p->state);
+    if (p->round == 0xFFFFFFFFu)
+        return fail(DTT_EROUNDLIMIT, "dtt_plan_next_round: a plan is limited to 2^32 - 1 rounds");
+    ++p->round;
+    p->state = DTT_PLAN_PREPARED;
+    return DTT_OK;
+}
+
+int dtt_plan_close(dtt_plan* p) {
+    if (!p) return DTT_OK;
+    int rc = DTT_OK;
+    if (p->state == DTT_PLAN_RUNNING) {
+        // what the producers queued so far is written first; then every gate still closed is
+        // opened, so the copier sends each chunk as it stands and exits
+        if (cudaStreamSynchronize(p->producer_stream) != cudaSuccess)
+            rc = fail(DTT_ECUDA, "dtt_plan_close: producer stream failed");
+        if (p->n_global && launch_force_open(p->d_gates, p->d_chunks, p->n_global, p->round, p->aux_stream) != cudaSuccess)
+            rc = fail(DTT_ECUDA, "dtt_plan_close: force-open launch failed");
+    }
+    if (p->aux_stream && cudaStreamSynchronize(p->aux_stream) != cudaSuccess) rc = fail(DTT_ECUDA, "dtt_plan_close: aux stream failed");
+    if (p->copy_stream && cudaStreamSynchronize(p->copy_stream) != cudaSuccess) rc = fail(DTT_ECUDA, "dtt_plan_close: copy stream failed");
+    p->state = DTT_PLAN_CLOSED;
+    free_device(p);
+    delete p;
+    return rc;
+}
+
+int dtt_plan_state(const dtt_plan* p) { return p ? p->state : DTT_EINVAL; }
+uint32_t dtt_plan_round(const dtt_plan* p) { return p ? p->round : 0; }
+
+int dtt_plan_info(const dtt_plan* p, uint32_t* n_global, uint32_t* first_chunk, uint32_t* n_chunks,
+                  uint64_t** gates_device) {
+    if (!p) return fail(DTT_EINVAL, "dtt_plan_info: NULL plan");
+    if (n_global) *n_global = p->n_global;
+    for (uint32_t r = 0; r < p->P; ++r) {
+        if (first_chunk) first_chunk[r] = p->first_chunk[r];
+        if (n_chunks) n_chunks[r] = p->n_chunks[r];
+    }
+    if (gates_device) *gates_device = p->d_gates;
+    return DTT_OK;
+}
+
+int dtt_plan_read_gates(dtt_plan* p, uint64_t* host, uint64_t n_words) {
+    if (!p || !host) return fail(DTT_EINVAL, "dtt_plan_read_gates: bad args");
+    const uint64_t need = (uint64_t)p->P * p->n_global * DTT_GATE_WORDS;
+    if (n_words < need) return fail(DTT_EINVAL, "dtt_plan_read_gates: need %llu words", (unsigned long long)need);
+    if (need == 0) return DTT_OK;
+    DTT_CUDA_TRY(cudaMemcpyAsync(host, p->d_gates, need * sizeof(uint64_t), cudaMemcpyDeviceToHost, p->copy_stream));
+    DTT_CUDA_TRY(cudaStreamSynchronize(p->copy_stream));
+    return DTT_OK;
+}
+
+int dtt_allgather_host(dtt_plan* p, const void* const* host_slices, void* host_out,
+                       uint32_t out_rank, cudaStream_t stream, dtt_report* report) {
+    if (!p || !host_slices) return fail(DTT_EINVAL, "dtt_allgather_host: bad args");
+    if (!p->opts.allgather) return fail(DTT_EINVAL, "dtt_allgather_host: needs an all-gather plan");
+    if (out_rank >= p->P) return fail(DTT_EINVAL, "dtt_allgather_host: out_rank out of range");
+    dtt_handle h[DTT_MAX_RANKS];
+    int rc = dtt_plan_start(p, stream, h);
+    if (rc != DTT_OK) return rc;
+    const uint64_t S = p->buf_bytes / p->P;
+    for (uint32_t r = 0; r < p->P; ++r)
+        if (host_slices[r])
+            DTT_CUDA_TRY(cudaMemcpyAsync(p->bufs[r] + r * S, host_slices[r], S, cudaMemcpyHostToDevice, stream));
+    rc = dtt_publish(h, p->P, 0, p->n_global, 0, stream);
+    if (rc != DTT_OK) return rc;
+    rc = dtt_plan_wait(p, report);
+    if (rc != DTT_OK) return rc;
+    if (host_out) {
+        DTT_CUDA_TRY(cudaMemcpyAsync(host_out, p->bufs[out_rank], p->buf_bytes, cudaMemcpyDeviceToHost, stream));
+        DTT_CUDA_TRY(cudaStreamSynchronize(stream));
+    }
+    return dtt_plan_next_round(p);
+}
+
+int dtt_consumer_gather(dtt_plan* p, uint32_t rank, void* dst, uint64_t max_polls, int32_t* status,
+                        uint32_t ctas, cudaStream_t stream) {
+    if (!p || !dst || !status || rank >= p->P) return fail(DTT_EINVAL, "dtt_consumer_gather: bad args");
+    if (p->state != DTT_PLAN_RUNNING) return fail(DTT_ESTATE, "dtt_consumer_gather: plan is not RUNNING");
+    if (stream == p->copy_stream) return fail(DTT_EINVAL, "dtt_consumer_gather: use a stream other than the copy stream");
+    if (!p->n_global) return DTT_OK;
+    const CopierParams cp = copier_params(p);
+    DTT_CUDA_TRY(launch_consumer(cp, make_handle(p, rank), static_cast<char*>(dst), max_polls, status, ctas, stream));
+    return DTT_OK;
+}
+
+}  // extern "C"

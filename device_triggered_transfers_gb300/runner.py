@@ -1,0 +1,101 @@
+"""Glue from a workload description (workloads.py) to library calls: the schedules from the
+library's builders, the plan, the fill producer's description, and one round of the path.
+
+Everything here is argument marshalling; the work runs in libdtt.so's kernels.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+from typing import List, Optional
+
+import torch
+
+from . import (MARK_AT_END, MARK_PER_STEP, ORDER_GROUPED, ORDER_ROW_MAJOR, Plan, Schedule,
+               dtt_fill_producer, dtt_plan_opts_default, dtt_schedule_chunks,
+               dtt_schedule_empty, dtt_schedule_tile_chunks, dtt_schedule_whole, fill_desc)
+
+
+def schedules_for(w) -> List[Schedule]:
+    """Each rank's schedule for workload ``w`` from the library's builders."""
+    out = []
+    rb = w.row_bytes
+    for r in range(w.P):
+        if r not in w.senders():
+            out.append(dtt_schedule_empty())
+            continue
+        off = w.slice_offset(r)
+        if w.kind == "whole":
+            out.append(dtt_schedule_whole(off, w.M, rb, rb, w.num_programs))
+        elif w.kind == "chunks":
+            out.append(dtt_schedule_chunks(off, w.M, rb, rb, w.num_chunks))
+        elif w.kind == "tile_chunks":
+            kind = ORDER_GROUPED if w.group_m else ORDER_ROW_MAJOR
+            out.append(dtt_schedule_tile_chunks(off, w.M, w.N, w.elem_bytes, rb, w.BM, w.BN,
+                                                w.tiles_per_chunk, kind, w.group_m))
+        else:
+            raise ValueError(f"unknown schedule kind {w.kind}")
+    return out
+
+
+def producer_desc(w, cluster: int = 1, programs: Optional[int] = None, threads: int = 0):
+    """The fill producer that matches ``w``'s schedule (same tiles, same order, same marks)."""
+    slice_offs = [w.slice_offset(r) for r in range(w.P)]
+    mask = 0
+    for r in w.senders():
+        mask |= 1 << r
+    if w.kind == "whole":
+        NP = w.num_programs
+        BM = -(-w.M // NP)
+        return fill_desc(w.dtype, w.seed, w.M, w.N, w.row_bytes, w.buf_bytes, slice_offs, BM, w.N, NP, 1,
+                         mark_mode=MARK_AT_END, cluster=1, rank_mask=mask, threads=threads)
+    if w.kind == "chunks":
+        BM = -(-w.M // w.num_chunks)
+        n = -(-w.M // BM)
+        NP = programs or n
+        return fill_desc(w.dtype, w.seed, w.M, w.N, w.row_bytes, w.buf_bytes, slice_offs, BM, w.N, NP, 1,
+                         mark_mode=MARK_PER_STEP, cluster=cluster, rank_mask=mask, threads=threads)
+    kind = ORDER_GROUPED if w.group_m else ORDER_ROW_MAJOR
+    return fill_desc(w.dtype, w.seed, w.M, w.N, w.row_bytes, w.buf_bytes, slice_offs, w.BM, w.BN,
+                     programs or w.num_programs, w.tiles_per_chunk, order_kind=kind,
+                     group_m=w.group_m, mark_mode=MARK_PER_STEP, cluster=cluster, rank_mask=mask,
+                     threads=threads)
+
+
+@dataclass
+class Setup:
+    w: object
+    bufs: List[torch.Tensor]
+    plan: Plan
+    desc: object
+    producer_stream: torch.cuda.Stream
+
+
+def make(w, opts=None, cluster: int = 1, programs: Optional[int] = None, threads: int = 0,
+         device: str = "cuda", fill_byte: int = 0) -> Setup:
+    """Allocate the P symmetric buffers (uint8, w.buf_bytes each), build the plan and producer."""
+    bufs = [torch.full((w.buf_bytes,), fill_byte, dtype=torch.uint8, device=device)
+            for _ in range(w.P)]
+    scheds = schedules_for(w)
+    if opts is None:
+        opts = dtt_plan_opts_default()
+    opts.allgather = 0 if w.broadcast else 1
+    plan = Plan(bufs, w.buf_bytes, scheds, opts)
+    for s in scheds:
+        s.free()
+    desc = producer_desc(w, cluster=cluster, programs=programs, threads=threads)
+    torch.cuda.synchronize()          # buffers initialised before any round starts
+    return Setup(w, bufs, plan, desc, torch.cuda.Stream())
+
+
+def run_round(st: Setup, raise_on_error: bool = True):
+    """One round: start (launches the copier), the fill producer, wait.  Returns the report."""
+    handles = st.plan.start(st.producer_stream)
+    dtt_fill_producer(st.bufs, st.desc, handles, st.producer_stream)
+    return st.plan.wait(raise_on_error=raise_on_error)
+
+
+def bench_launch(w) -> dict:
+    """The launch configuration the benchmark times for workload ``w`` (tests use it too)."""
+    if w.kind == "chunks":
+        return {"cluster": 8}
+    return {}

@@ -1,0 +1,400 @@
+/*
+ * dtt.h -- C ABI of the GB300-native triggered-plan library (device-triggered transfers).
+ *
+ * A triggered plan sends the output of a running producer kernel to every other rank without
+ * a host round trip per chunk: the producer marks each chunk of its output ready once it is
+ * written, and a copier moves the chunk to the same offsets in every peer's buffer and then
+ * signals its arrival there (Iris docs, "Triggered Plans", introduction and section Model;
+ * ROCm/iris pull 573, "Triggered SDMA Plans", introduction).  On one GB300 the P ranks are
+ * virtual ranks: P buffers of one size in the GPU's own HBM, driven by one process.  The
+ * copier is a persistent CUDA kernel that polls the gates (it stands where the pages use a
+ * copy engine's poll / copy / atomic packet chain).
+ *
+ * Conventions shared by every call:
+ *  - Return value: DTT_OK (0) or a negative DTT_E* code; dtt_last_error() then gives a message
+ *    (thread-local, valid until the next failing call on the same thread).
+ *  - Pointers named "device" are CUDA device addresses in the current device's context;
+ *    "host" pointers are ordinary (or pinned, where stated) host memory.  Streams are
+ *    cudaStream_t handles owned by the caller unless stated.
+ *  - Byte offsets inside a buffer are relative to the buffer's first byte.
+ *  - Nothing here takes a framework (torch) type.
+ */
+#ifndef DTT_H
+#define DTT_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---------------------------------------------------------------------------------------- */
+/* Limits and codes                                                                          */
+/* ---------------------------------------------------------------------------------------- */
+
+#define DTT_MAX_RANKS 16        /* virtual ranks per plan */
+#define DTT_REPORT_MAX 64       /* chunk ids listed in a dtt_report */
+#define DTT_LINEAR_MAX (1ull << 30)  /* linear regions are split at 1 GiB ("Triggered Plans",
+                                        section Model and section Requirements and limits) */
+
+enum {
+    DTT_OK = 0,
+    DTT_EINVAL = -1,       /* invalid argument */
+    DTT_EOUTOFROWS = -2,   /* all-gather: a schedule leaves its rank's own rows
+                              ("Triggered Plans", section Model, prepare_all_gather) */
+    DTT_EOVERLAP = -3,     /* two ranks send the same bytes
+                              ("Triggered Plans", section Requirements and limits) */
+    DTT_ECAPACITY = -4,    /* plan larger than its configured capacity */
+    DTT_EROUNDLIMIT = -5,  /* round would pass 2^32 - 1 ("Triggered Plans", Gates and rounds) */
+    DTT_ESTATE = -6,       /* call not valid in the plan's current state */
+    DTT_EEXTRA = -7,       /* a chunk got more marks than its writers
+                              ("Triggered Plans", The kernel author's contract, item 2) */
+    DTT_ETIMEDOUT = -8,    /* a wait gave up; the report names the short chunks (same item) */
+    DTT_ECUDA = -9,        /* a CUDA runtime call failed (message has the CUDA error) */
+    DTT_ENOMEM = -10       /* host or device allocation failed */
+};
+
+/* Plan states ("Triggered Plans", The kernel author's contract: done / FAILED / CLOSING). */
+enum {
+    DTT_PLAN_PREPARED = 0, /* created or advanced by next_round; start() is next */
+    DTT_PLAN_RUNNING = 1,  /* start() launched this round's copier */
+    DTT_PLAN_DONE = 2,     /* wait() found every chunk delivered */
+    DTT_PLAN_FAILED = 3,   /* wait() found extra marks or short chunks; only close() is valid */
+    DTT_PLAN_CLOSING = 4,  /* reserved (plans sharing queues) */
+    DTT_PLAN_CLOSED = 5
+};
+
+/* Element types of the library's producers. */
+enum { DTT_BF16 = 0, DTT_F32 = 1, DTT_U8 = 2 };
+
+/* Copier data paths. */
+enum {
+    DTT_COPY_VEC16 = 0,    /* 16-byte vector loads and stores, read once, fan out to peers */
+    DTT_COPY_TMA = 1       /* bulk async copies (cp.async.bulk) staged through shared memory */
+};
+
+/* ---------------------------------------------------------------------------------------- */
+/* Regions, chunks and schedules ("Triggered Plans", section Model)                          */
+/* ---------------------------------------------------------------------------------------- */
+
+/* One copy: `rows` rows of `row_bytes` bytes, `pitch` bytes apart, starting at byte
+ * `offset` of the buffer.  A byte range has rows == 1 and pitch == row_bytes.  The copy lands
+ * at the same offset in every peer's buffer. */
+typedef struct dtt_region {
+    uint64_t offset;
+    uint64_t row_bytes;
+    uint64_t rows;
+    uint64_t pitch;
+} dtt_region;
+
+/* A host-side list of chunks (ordered groups of regions, each with its writer count), in
+ * the order the producer completes them.  Opaque; owned by the caller, freed with
+ * dtt_schedule_free.  A plan copies what it needs at creation. */
+typedef struct dtt_schedule dtt_schedule;
+
+/* Producer step-to-tile order shared by the host builder and the library's producers, so
+ * the two cannot drift ("Triggered Plans", section Model: pass the kernel's own mapping).
+ * kind DTT_ORDER_ROW_MAJOR: step s -> (s / tiles_n, s % tiles_n).
+ * kind DTT_ORDER_GROUPED: groups of group_m tile rows swept column by column: with
+ *   g = s / (group_m * tiles_n), m0 = g * group_m, h = min(tiles_m - m0, group_m),
+ *   w = s % (group_m * tiles_n):  tm = m0 + w % h,  tn = w / h. */
+enum { DTT_ORDER_ROW_MAJOR = 0, DTT_ORDER_GROUPED = 1 };
+typedef struct dtt_order {
+    uint32_t kind;
+    uint32_t group_m;
+} dtt_order;
+
+/* A caller-supplied step-to-tile map for hand-written producers (host only).  Returns 0 and
+ * writes (tm, tn) for `step`. */
+typedef int (*dtt_order_fn)(uint64_t step, void* ctx, uint32_t* tm, uint32_t* tn);
+
+/* The builtin order on the host (the same function the library's producers run).
+ * Errors: DTT_EINVAL for an unknown kind, group_m == 0 with kind GROUPED, or step >= tiles. */
+int dtt_tile_of(const dtt_order* order, uint64_t step, uint32_t tiles_m, uint32_t tiles_n,
+                uint32_t* tm, uint32_t* tn);
+
+/* whole(): one chunk holding the block of `rows` rows (row_bytes each, pitch apart) at
+ * base_off, marked once by each of `num_programs` programs at their end: writers =
+ * num_programs ("Triggered Plans", section Model).  Contiguous rows form one byte range split
+ * into 1 GiB pieces, strided rows one 2D region.  Errors: DTT_EINVAL (num_programs == 0,
+ * pitch < row_bytes with rows > 1). */
+int dtt_schedule_whole(uint64_t base_off, uint64_t rows, uint64_t row_bytes, uint64_t pitch,
+                       uint32_t num_programs, dtt_schedule** out);
+
+/* chunks(): row blocks completed in order, one writer each ("Triggered Plans", section Model).
+ * Block size is ceil(rows / num_chunks) rows, the last block shorter (so fewer chunks than
+ * asked can result when the division is uneven; dtt_schedule_info reports the count).
+ * Errors: DTT_EINVAL (num_chunks == 0 or > rows, pitch < row_bytes). */
+int dtt_schedule_chunks(uint64_t base_off, uint64_t rows, uint64_t row_bytes, uint64_t pitch,
+                        uint32_t num_chunks, dtt_schedule** out);
+
+/* tile_chunks(): consecutive steps of a tiled producer over an M x N slice of elem_bytes
+ * elements whose rows are pitch bytes apart, starting at base_off.  Step s stores tile
+ * (tm, tn) given by `fn(s, ctx)` when fn is non-NULL, else by the builtin `order` (NULL means
+ * row-major).  Each tile is one 2D region clipped at the slice edges; chunk k holds steps
+ * [k*tiles_per_chunk, (k+1)*tiles_per_chunk) and has one writer per step ("Triggered Plans",
+ * section Model: the producer marks first_chunk + step / num_programs).  Errors: DTT_EINVAL
+ * (zero sizes, order not a bijection onto the tiles). */
+int dtt_schedule_tile_chunks(uint64_t base_off, uint64_t M, uint64_t N, uint32_t elem_bytes,
+                             uint64_t pitch, uint32_t BM, uint32_t BN, uint32_t tiles_per_chunk,
+                             const dtt_order* order, dtt_order_fn fn, void* ctx,
+                             dtt_schedule** out);
+
+/* An empty schedule: a rank that sends nothing (a broadcast's receivers, "Triggered Plans",
+ * section Requirements and limits), or the start of a hand-built schedule. */
+int dtt_schedule_empty(dtt_schedule** out);
+
+/* Append one chunk of n regions (copied) with `writers` marks per round.  Byte ranges longer
+ * than 1 GiB are split here.  Errors: DTT_EINVAL (writers == 0, n == 0, pitch < row_bytes). */
+int dtt_schedule_add_chunk(dtt_schedule* s, const dtt_region* regions, uint32_t n,
+                           uint32_t writers);
+
+/* Number of chunks and regions. */
+int dtt_schedule_info(const dtt_schedule* s, uint32_t* n_chunks, uint64_t* n_regions);
+
+/* Copy chunk `chunk`'s regions into regions_out (at most cap of them) and its writer count;
+ * *n_regions receives the chunk's region count. */
+int dtt_schedule_get(const dtt_schedule* s, uint32_t chunk, dtt_region* regions_out,
+                     uint64_t cap, uint64_t* n_regions, uint32_t* writers);
+
+void dtt_schedule_free(dtt_schedule* s);
+
+/* ---------------------------------------------------------------------------------------- */
+/* Plans ("Triggered Plans", sections Model, The kernel author's contract, Gates and rounds)  */
+/* ---------------------------------------------------------------------------------------- */
+
+typedef struct dtt_plan dtt_plan;
+
+typedef struct dtt_plan_opts {
+    uint32_t allgather;      /* 1: rank r's regions must lie in bytes [r*S, (r+1)*S), S =
+                                buf_bytes / P (prepare_all_gather's check); 0: only bounds */
+    uint32_t method;         /* DTT_COPY_VEC16 or DTT_COPY_TMA */
+    uint32_t copier_ctas;    /* copier CTAs; 0 = SM count x ctas_per_sm */
+    uint32_t ctas_per_sm;    /* used when copier_ctas == 0; 0 = 1 */
+    uint32_t copier_threads; /* threads per copier CTA (multiple of 32, <= 1024); 0 = 512 */
+    uint32_t piece_bytes;    /* largest unit of copier work (multiple of 16); 0 = 65536 */
+    uint32_t timestamps;     /* 1: stamp gate-open and arrival times (globaltimer, ns) */
+    uint32_t initial_round;  /* 0 or 1: rounds start at 1; larger: gates begin as if
+                                initial_round - 1 rounds had completed (round-limit tests) */
+    uint64_t max_polls;      /* copier polls of one gate before it gives up; 0 = 2^22 */
+    uint64_t max_regions;    /* capacity: regions in the plan; 0 = unlimited */
+} dtt_plan_opts;
+
+void dtt_plan_opts_default(dtt_plan_opts* opts);
+
+#define DTT_HANDLE_TIMESTAMPS 1u   /* dtt_handle.flags bit: stamp gate-open times */
+#define DTT_DEV_EBADCHUNK 1u       /* device status bit: a rank marked a chunk it does not own */
+
+/* Device-side view of a plan for one rank and one round, passed by value to producer and
+ * consumer kernels (the pages' TriggeredView handle).  Plain data; valid until the next
+ * dtt_plan_start of the same plan or its close. */
+typedef struct dtt_handle {
+    uint64_t* gates;          /* device: P gate tables, [P][n_global][8] uint64 */
+    const uint32_t* writers;  /* device: writers per global chunk */
+    uint32_t* status;         /* device: plan status word (device-side misuse bits) */
+    uint32_t round;
+    uint32_t rank;
+    uint32_t P;
+    uint32_t n_global;        /* chunks in the plan, all ranks */
+    uint32_t first_chunk;     /* global id of this rank's first chunk */
+    uint32_t n_chunks;        /* this rank's chunk count */
+    uint32_t flags;           /* bit 0: timestamps */
+    uint32_t reserved;
+} dtt_handle;
+
+/* Gate row: 64 bytes = 8 uint64 words per (rank, global chunk) ("Triggered Plans", Gates and
+ * rounds: ready, arrival and a writer counter; "Triggered SDMA Plans", Design notes: ready,
+ * arrival, completion, error, contributor counter).  Gates are never reset. */
+enum {
+    DTT_GATE_READY = 0,       /* owner's row: round of the last gate opening (low 32 bits
+                                 are compared with >= round) */
+    DTT_GATE_ARRIVAL = 1,     /* peer's row: one per round when the chunk has landed here */
+    DTT_GATE_COMPLETION = 2,  /* owner's row: deliveries made, (P-1) per round */
+    DTT_GATE_ERROR = 3,       /* owner's row: round of an extra mark, else 0 */
+    DTT_GATE_COUNTER = 4,     /* owner's row: writer marks, round*writers after a round */
+    DTT_GATE_T_OPEN = 5,      /* owner's row: globaltimer when the gate opened */
+    DTT_GATE_T_ARRIVE = 6,    /* peer's row: globaltimer when the arrival was signalled */
+    DTT_GATE_COPIER = 7,      /* owner's row: copier-internal progress counter */
+    DTT_GATE_WORDS = 8
+};
+
+/* Result of dtt_plan_wait. */
+typedef struct dtt_report {
+    int32_t status;           /* DTT_OK, DTT_EEXTRA or DTT_ETIMEDOUT */
+    uint32_t n_short;         /* chunks short of marks or of an arrival somewhere */
+    uint32_t n_extra;         /* chunks with more marks than writers this round */
+    uint32_t copier_timeouts; /* copier CTAs that gave up polling a gate */
+    uint32_t device_status;   /* device-side misuse bits (e.g. a mark on a foreign chunk) */
+    uint32_t round;
+    uint32_t short_chunks[DTT_REPORT_MAX];  /* the first n_short ids, ascending */
+    uint32_t extra_chunks[DTT_REPORT_MAX];  /* the first n_extra ids, ascending */
+} dtt_report;
+
+/* Create a plan over P symmetric buffers (bufs: host array of P device pointers, each
+ * buf_bytes long, 16-byte aligned for the vector path) with one schedule per rank (scheds:
+ * host array of P schedules; a NULL entry or empty schedule sends nothing).  Chunk ids are
+ * global: rank r's chunks follow those of ranks 0..r-1 ("Triggered Plans", section Model).
+ * Validates every region (inside the buffer; inside the rank's rows when opts->allgather;
+ * no byte sent by two ranks), allocates the gate tables and the copier's descriptor tables
+ * on the device, and leaves the plan PREPARED for round opts->initial_round (1 by default).
+ * copy_stream: a non-blocking stream for the copier, or NULL to let the plan create (and
+ * own) a high-priority one.  Creation succeeds for every rank or for none: on error nothing
+ * stays allocated ("Triggered Plans", The kernel author's contract).
+ * Errors: DTT_EINVAL, DTT_EOUTOFROWS, DTT_EOVERLAP, DTT_ECAPACITY, DTT_ENOMEM, DTT_ECUDA. */
+int dtt_plan_create(void* const* bufs, uint64_t buf_bytes, uint32_t P,
+                    const dtt_schedule* const* scheds, const dtt_plan_opts* opts,
+                    cudaStream_t copy_stream, dtt_plan** out);
+
+/* Start the current round: launch its copier on the plan's copy stream and fill handles[r]
+ * (host array of P) for every rank.  producer_stream is where the producers will run; wait()
+ * orders its check after the work queued there.  It must differ from the copy stream.
+ * The copier polls each source's gates in schedule order, so chunks completed out of order
+ * are correct but wait for earlier ones ("Triggered Plans", The kernel author's contract,
+ * item 1).  Errors: DTT_ESTATE (not PREPARED), DTT_EINVAL, DTT_ECUDA. */
+int dtt_plan_start(dtt_plan* plan, cudaStream_t producer_stream, dtt_handle* handles);
+
+/* The handle of one rank for the current round.  Errors: DTT_EINVAL. */
+int dtt_plan_handle(const dtt_plan* plan, uint32_t rank, dtt_handle* out);
+
+/* Block until the round is complete everywhere, then check it with a kernel: every chunk got
+ * exactly writers marks this round and arrived at every peer ("Triggered Plans", Gates and
+ * rounds; "Triggered SDMA Plans", Design notes, completion).  Fills *report when non-NULL.
+ * Returns DTT_OK (plan DONE), DTT_EEXTRA or DTT_ETIMEDOUT (plan FAILED; the report names the
+ * chunks), DTT_ESTATE (not RUNNING) or DTT_ECUDA. */
+int dtt_plan_wait(dtt_plan* plan, dtt_report* report);
+
+/* Advance to the next round: "done reading this round's data" ("Triggered Plans", The kernel
+ * author's contract, item 6).  Errors: DTT_ESTATE (not DONE), DTT_EROUNDLIMIT (the round is
+ * already 2^32 - 1; the plan stays DONE). */
+int dtt_plan_next_round(dtt_plan* plan);
+
+/* Close and free the plan.  In the middle of a round, gates not yet open are opened so the
+ * copier sends each chunk as it stands, and both streams are drained first ("Triggered
+ * Plans", The kernel author's contract, close()).  Always frees; returns DTT_ECUDA if a CUDA
+ * call failed on the way. */
+int dtt_plan_close(dtt_plan* plan);
+
+int dtt_plan_state(const dtt_plan* plan);
+uint32_t dtt_plan_round(const dtt_plan* plan);
+
+/* Plan layout: n_global chunks; first_chunk / n_chunks per rank (host arrays of P, may be
+ * NULL); *gates_device = the gate tables' device address. */
+int dtt_plan_info(const dtt_plan* plan, uint32_t* n_global, uint32_t* first_chunk,
+                  uint32_t* n_chunks, uint64_t** gates_device);
+
+/* Copy the P gate tables (P * n_global * 8 uint64, rank-major) to host memory `host`
+ * (n_words long).  Synchronises the copy stream.  Errors: DTT_EINVAL if n_words is short. */
+int dtt_plan_read_gates(dtt_plan* plan, uint64_t* host, uint64_t n_words);
+
+/* Host-buffer all-gather, one round end to end: copy each rank's slice (host_slices[r],
+ * pinned host memory, S = buf_bytes / P bytes) into its own rows, mark every chunk from a
+ * kernel queued after the copies on `stream`, let the copier fan the chunks out, wait, and
+ * copy rank out_rank's gathered buffer (buf_bytes) to host_out (pinned, may be NULL).  Then
+ * advances to the next round.  Needs an all-gather plan in state PREPARED.  The report is
+ * filled as by dtt_plan_wait.  Errors: as start / wait / next_round. */
+int dtt_allgather_host(dtt_plan* plan, const void* const* host_slices, void* host_out,
+                       uint32_t out_rank, cudaStream_t stream, dtt_report* report);
+
+/* ---------------------------------------------------------------------------------------- */
+/* Producers and consumers shipped with the library                                          */
+/* ---------------------------------------------------------------------------------------- */
+
+/* Marks of the fill producer. */
+enum {
+    DTT_MARK_PER_STEP = 0,   /* mark first_chunk + step / tiles_per_chunk after each step */
+    DTT_MARK_AT_END = 1      /* each program marks first_chunk once after its last step
+                                (whole(): "marked ready once per program at the end") */
+};
+
+/* Hashed-fill producer.  Rank r's slice is M x N elements of `dtype` with rows `pitch` bytes
+ * apart, starting at byte slice_off[r] of bufs[r].  It is produced as BM x BN tiles by
+ * num_programs programs per rank: program p takes steps p, p + num_programs, ... in `order`
+ * ("Triggered Plans", section Model, the persistent tiled producer), writes the tile and marks
+ * per mark_mode.  A program is one CTA, or a thread-block cluster of `cluster` CTAs that
+ * marks once per step after a cluster barrier (one writer).  Element (row, col) of rank r in
+ * round R holds hash(seed, r, R, row, col): with fmix32 the MurmurHash3 finaliser,
+ * salt = fmix32(seed ^ fmix32(r ^ fmix32(R))), h = fmix32((row*N + col) mod 2^32 ^ salt),
+ * u = ((h >> 8) - 2^23) * 2^-23 in [-1, 1); bf16 = u rounded to nearest even, f32 = u,
+ * u8 = h & 0xFF.  Only ranks whose bit is set in rank_mask produce. */
+typedef struct dtt_fill_desc {
+    uint32_t dtype;
+    uint32_t seed;
+    uint64_t M, N;
+    uint64_t pitch;
+    uint64_t buf_bytes;      /* size of every buffer: slices must lie inside it */
+    uint64_t slice_off[DTT_MAX_RANKS];
+    uint32_t BM, BN;
+    uint32_t num_programs;
+    uint32_t tiles_per_chunk;
+    dtt_order order;
+    uint32_t mark_mode;
+    uint32_t cluster;        /* 1..8 CTAs per program */
+    uint32_t rank_mask;
+    uint32_t threads;        /* threads per CTA; 0 = 256 */
+} dtt_fill_desc;
+
+/* Launch the fill producer for all P ranks on `stream` (handles: host array of P, from
+ * dtt_plan_start).  bufs: host array of P device pointers.  Errors: DTT_EINVAL, DTT_ECUDA. */
+int dtt_fill_producer(void* const* bufs, uint32_t P, const dtt_fill_desc* desc,
+                      const dtt_handle* handles, cudaStream_t stream);
+
+/* A producer that only marks: chunks [first_chunk, first_chunk + n_chunks) (global ids) each
+ * get `marks` marks, or their writer count when marks == 0, from one CTA per chunk launched on
+ * `stream`, on behalf of the rank that owns each chunk (handles: host array of P from
+ * dtt_plan_start).  Work queued earlier on `stream` -- host-to-device copies of the chunk's
+ * data, other kernels -- precedes the marks.  It serves host-fed rounds and lets a caller give
+ * a chunk an extra mark or leave one short ("Triggered Plans", The kernel author's contract,
+ * item 2, names both).  Errors: DTT_EINVAL, DTT_ECUDA. */
+int dtt_publish(const dtt_handle* handles, uint32_t P, uint32_t first_chunk, uint32_t n_chunks,
+                uint32_t marks, cudaStream_t stream);
+
+/* Consumer: rank `rank` waits for every chunk of the other ranks (in global id order, with
+ * the device-side wait, at most max_polls polls each) and copies its regions from the rank's
+ * own buffer bufs[rank] to the same offsets of `dst` (device, buf_bytes long) -- data read
+ * after the wait is this round's ("Triggered Plans", Memory ordering, Consumer).  Per-chunk
+ * results go to status (device int32 [n_global]: 0, or DTT_ETIMEDOUT).  Launch with at most
+ * `ctas` CTAs on `stream` (a third stream, concurrent with producer and copier).
+ * Errors: DTT_EINVAL, DTT_ESTATE (plan not RUNNING), DTT_ECUDA. */
+int dtt_consumer_gather(dtt_plan* plan, uint32_t rank, void* dst, uint64_t max_polls,
+                        int32_t* status, uint32_t ctas, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------------------- */
+/* N-rank notify/wait barrier (PyPTO, "Barrier: Signals Only")                               */
+/* ---------------------------------------------------------------------------------------- */
+
+/* Hand-rolled barrier over P virtual ranks, one CTA each in one cooperative launch.  Rank r
+ * adds 1 (atomic, release) to row r of every peer's window signal[peer] (device int32[P]),
+ * then waits until row src of its own window is >= gen for every src != r (acquire, at most
+ * max_polls polls each), then copies its window to y[r] (device int32[P]) (sections The idea
+ * and Walkthrough; counters are monotonic, so the gen-th use of one set of windows passes
+ * gen).  status (device int32[P]): 0, or DTT_ETIMEDOUT for a rank whose wait gave up.
+ * signal and y are host arrays of P device pointers.  Errors: DTT_EINVAL, DTT_ECUDA. */
+int dtt_barrier_handrolled(int32_t* const* signal, int32_t* const* y, uint32_t P, uint32_t gen,
+                           uint64_t max_polls, int32_t* status, cudaStream_t stream);
+
+/* The builtin barrier's state: P x P int32 internal counters on the device (zeroed at create)
+ * and the host's generation count.  Owned by the caller. */
+typedef struct dtt_barrier dtt_barrier;
+int dtt_barrier_create(uint32_t P, dtt_barrier** out);
+void dtt_barrier_destroy(dtt_barrier* b);
+
+/* The builtin reveal (section Walkthrough, the builtin reveal): every rank stages x[r] into
+ * data[r] (size int32 each), passes a barrier on the internal counters (no tally in any user
+ * window), then loads the next rank's staged slice: y[r] = data[(r + 1) % P].  x, data, y are
+ * host arrays of P device pointers; status as for dtt_barrier_handrolled. */
+int dtt_barrier_reveal(dtt_barrier* b, const int32_t* const* x, int32_t* const* data,
+                       int32_t* const* y, uint32_t size, uint64_t max_polls, int32_t* status,
+                       cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------------------- */
+/* Errors                                                                                    */
+/* ---------------------------------------------------------------------------------------- */
+
+const char* dtt_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DTT_H */

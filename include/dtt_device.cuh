@@ -1,0 +1,158 @@
+/*
+ * dtt_device.cuh -- device side of a triggered plan: mark_ready, arrived, wait.
+ *
+ * Include from producer and consumer kernels; the kernel receives a dtt_handle (include/dtt.h)
+ * by value.  Every function here is called by ALL threads of a CTA (dtt_mark_ready_cluster:
+ * of a cluster), outside divergent code, the same number of times in every thread ("Triggered
+ * Plans", The kernel author's contract, items 2 and 5).  They use __syncthreads internally.
+ *
+ * Memory ordering ("Triggered Plans", section Memory ordering), restated for one GPU:
+ *  - mark_ready: a CTA barrier orders every thread's earlier stores before thread 0, whose
+ *    acq_rel atomic add on the chunk's writer counter (gpu scope) is cumulative over them.
+ *    The writer whose add completes the round's count then stores ready = round with release
+ *    semantics: the copier acquires `ready`, not the counter, and the release keeps every
+ *    writer's stores (acquired through the counter's read-modify-write chain) ahead of it.
+ *    The pages' copy engine reads behind L2 and needs system scope; every reader here is an SM
+ *    of the same GPU, so gpu scope suffices.
+ *  - arrived / wait: thread 0 reads the gate with an acquire load (gpu scope); a CTA barrier
+ *    passes the result to the other threads, and data they load afterwards is this round's.
+ *    Polls are counted, never clock-bounded.
+ *  - A producer that writes through the async proxy (TMA stores) must complete those writes
+ *    (cp.async.bulk.wait_group 0) and issue fence.proxy.async before calling mark_ready.
+ */
+#ifndef DTT_DEVICE_CUH
+#define DTT_DEVICE_CUH
+
+#include <stdint.h>
+#include "dtt.h"
+
+namespace dtt_dev {
+
+__device__ __forceinline__ uint64_t ld_acquire(const uint64_t* p) {
+    uint64_t v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ uint64_t ld_relaxed(const uint64_t* p) {
+    uint64_t v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_release(uint64_t* p, uint64_t v) {
+    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ void st_relaxed(uint64_t* p, uint64_t v) {
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ uint64_t atom_add_acq_rel(uint64_t* p, uint64_t v) {
+    uint64_t old;
+    asm volatile("atom.acq_rel.gpu.global.add.u64 %0, [%1], %2;"
+                 : "=l"(old) : "l"(p), "l"(v) : "memory");
+    return old;
+}
+
+__device__ __forceinline__ void red_release_add(uint64_t* p, uint64_t v) {
+    asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ void red_relaxed_max(uint64_t* p, uint64_t v) {
+    asm volatile("red.relaxed.gpu.global.max.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ uint64_t globaltimer() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ bool first_thread() {
+    return threadIdx.x == 0 && threadIdx.y == 0 && threadIdx.z == 0;
+}
+
+__device__ __forceinline__ uint64_t* gate_row(const dtt_handle& h, uint32_t table, uint32_t chunk) {
+    return h.gates + ((uint64_t)table * h.n_global + chunk) * DTT_GATE_WORDS;
+}
+
+/* One writer's mark, issued by one thread after the caller's barrier. */
+__device__ __forceinline__ void mark_one(const dtt_handle& h, uint32_t chunk) {
+    if (chunk < h.first_chunk || chunk >= h.first_chunk + h.n_chunks) {
+        atomicOr(h.status, DTT_DEV_EBADCHUNK);
+        return;
+    }
+    uint64_t* row = gate_row(h, h.rank, chunk);
+    const uint64_t target = (uint64_t)h.round * h.writers[chunk];
+    const uint64_t now = atom_add_acq_rel(row + DTT_GATE_COUNTER, 1) + 1;
+    if (now == target) {
+        if (h.flags & DTT_HANDLE_TIMESTAMPS) st_relaxed(row + DTT_GATE_T_OPEN, globaltimer());
+        st_release(row + DTT_GATE_READY, h.round);
+    } else if (now > target) {
+        red_relaxed_max(row + DTT_GATE_ERROR, h.round);
+    }
+}
+
+/* The word a rank polls for `chunk`: its own chunks are local once ready; other ranks' chunks
+ * are here once they arrived. */
+__device__ __forceinline__ const uint64_t* wait_word(const dtt_handle& h, uint32_t chunk) {
+    const uint64_t* row = gate_row(h, h.rank, chunk);
+    const bool own = chunk >= h.first_chunk && chunk < h.first_chunk + h.n_chunks;
+    return row + (own ? DTT_GATE_READY : DTT_GATE_ARRIVAL);
+}
+
+}  // namespace dtt_dev
+
+/* Mark `chunk` (global id, one of this rank's) ready: one of its `writers` marks this round.
+ * Call after this CTA's writes to the chunk. */
+__device__ __forceinline__ void dtt_mark_ready(const dtt_handle& h, uint32_t chunk) {
+    __syncthreads();
+    if (dtt_dev::first_thread()) dtt_dev::mark_one(h, chunk);
+    __syncthreads();
+}
+
+/* Cluster form: every CTA of a thread-block cluster calls it after its writes; a cluster
+ * barrier (release / acquire, cluster scope) orders all of them before CTA 0's thread 0,
+ * which issues ONE mark.  The cluster counts as one writer. */
+__device__ __forceinline__ void dtt_mark_ready_cluster(const dtt_handle& h, uint32_t chunk) {
+    __syncthreads();
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+    uint32_t crank;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(crank));
+    if (crank == 0 && dtt_dev::first_thread()) dtt_dev::mark_one(h, chunk);
+    __syncthreads();
+}
+
+/* One poll: has `chunk` arrived here this round (own chunk: is it ready)? */
+__device__ __forceinline__ bool dtt_arrived(const dtt_handle& h, uint32_t chunk) {
+    __shared__ int dtt_arrived_flag;
+    __syncthreads();
+    if (dtt_dev::first_thread())
+        dtt_arrived_flag = (uint32_t)dtt_dev::ld_acquire(dtt_dev::wait_word(h, chunk)) >= h.round;
+    __syncthreads();
+    return dtt_arrived_flag != 0;
+}
+
+/* Wait until `chunk` has arrived here this round (own chunk: until it is ready), polling at
+ * most max_polls times.  Returns 0, or DTT_ETIMEDOUT if the polls ran out. */
+__device__ __forceinline__ int dtt_wait(const dtt_handle& h, uint32_t chunk, uint64_t max_polls) {
+    __shared__ int dtt_wait_result;
+    __syncthreads();
+    if (dtt_dev::first_thread()) {
+        const uint64_t* w = dtt_dev::wait_word(h, chunk);
+        int r = DTT_ETIMEDOUT;
+        uint32_t ns = 0;
+        for (uint64_t i = 0; i < max_polls; ++i) {
+            if ((uint32_t)dtt_dev::ld_acquire(w) >= h.round) { r = 0; break; }
+            __nanosleep(ns);
+            ns = ns < 256 ? ns + 32 : 256;
+        }
+        dtt_wait_result = r;
+    }
+    __syncthreads();
+    return dtt_wait_result;
+}
+
+#endif /* DTT_DEVICE_CUH */

@@ -1,0 +1,142 @@
+"""GPU parity: the CUDA triggered all-gather (copier, fill producer, gates, check) against the
+CPU oracle, bit for bit, through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from gpu_common import expected_bytes, oracle_plan, oracle_round, sample_offsets
+from oracle import plan as OP
+
+pytestmark = pytest.mark.gpu
+
+if torch.cuda.is_available():
+    from conftest import ensure_built
+    ensure_built()
+    import device_triggered_transfers_gb300 as D
+    from device_triggered_transfers_gb300 import runner
+
+
+def _gates_match(st, o):
+    g = st.plan.read_gates()
+    assert g.shape[:2] == o.gates.shape[:2]
+    np.testing.assert_array_equal(g[:, :, :5], o.gates)
+    return g
+
+
+def run_parity(w, rounds, opts=None, cluster=1, programs=None, threads=0):
+    st = runner.make(w, opts=opts, cluster=cluster, programs=programs, threads=threads)
+    o = oracle_plan(w)
+    try:
+        for R in range(1, rounds + 1):
+            rep = runner.run_round(st)
+            assert rep.status == D.OK and rep.copier_timeouts == 0
+            assert oracle_round(o, w) == (OP.OK, [], [])
+            for q in range(w.P):
+                np.testing.assert_array_equal(st.bufs[q].cpu().numpy(), o.bufs[q],
+                                              err_msg=f"round {R} buffer {q}")
+            g = _gates_match(st, o)
+            t_open, t_arr = g[:, :, D.GATE_T_OPEN], g[:, :, D.GATE_T_ARRIVE]
+            for c in range(o.G):
+                s = o.owner[c]
+                for p in range(w.P):
+                    if p != s:
+                        assert int(t_arr[p, c]) >= int(t_open[s, c]) > 0
+            st.plan.next_round()
+            o.next_round()
+    finally:
+        st.plan.close()
+
+
+SMALL = {
+    "c1": (W.C1, {}),
+    "chunks_ragged": (W.small(W.C2, M=70, N=256, num_chunks=8), {}),
+    "tiles_grouped_ragged": (W.Workload("t", P=3, M=300, N=200, dtype=W.BF16, kind="tile_chunks",
+                                        rounds=3, seed=7, BM=64, BN=48, num_programs=5,
+                                        tiles_per_chunk=5, group_m=2), {}),
+    "tiles_unaligned": (W.Workload("u", P=2, M=37, N=203, dtype=W.BF16, kind="tile_chunks",
+                                   rounds=2, seed=8, BM=16, BN=40, num_programs=3,
+                                   tiles_per_chunk=4), {}),
+    "whole_f32_8writers": (W.small(W.C4A, M=64, N=64, rounds=4), {}),
+    "bcast_u8": (W.Workload("b", P=4, M=64, N=4096, dtype=W.U8, kind="whole", rounds=2, seed=9,
+                            num_programs=8, broadcast=True), {}),
+    "chunks_cluster4": (W.small(W.C2, M=256, N=512, num_chunks=4), {"cluster": 4}),
+    "tiles_cluster2": (W.Workload("t2", P=3, M=300, N=200, dtype=W.BF16, kind="tile_chunks",
+                                  rounds=2, seed=10, BM=64, BN=48, num_programs=5,
+                                  tiles_per_chunk=5, group_m=2), {"cluster": 2}),
+    "small_pieces_few_ctas": (W.small(W.C2, M=64, N=1024, num_chunks=4),
+                              {"opts": dict(piece_bytes=4096, copier_ctas=7, copier_threads=128)}),
+    "many_ctas": (W.small(W.C2, M=32, N=256, num_chunks=2),
+                  {"opts": dict(copier_ctas=600, copier_threads=64)}),
+}
+
+
+@pytest.mark.parametrize("name", sorted(SMALL))
+def test_parity_small(name):
+    w, kw = SMALL[name]
+    kw = dict(kw)
+    opts = kw.pop("opts", None)
+    run_parity(w, min(w.rounds, 3), opts=D.dtt_plan_opts_default(**opts) if opts else None, **kw)
+
+
+def test_parity_c1_full():
+    run_parity(W.C1, W.C1.rounds)
+
+
+def test_parity_c4a_full_stale_data_check():
+    # 8 writers on one 4 MiB gate per rank, values change every round: a stale copy fails
+    run_parity(W.C4A, W.C4A.rounds)
+
+
+def _run_sampled(w, rounds, n_samples, launch):
+    st = runner.make(w, **launch)
+    o = oracle_plan(w, copy_data=False)
+    try:
+        for R in range(1, rounds + 1):
+            rep = runner.run_round(st)
+            assert rep.status == D.OK and rep.copier_timeouts == 0
+            assert oracle_round(o, w)[0] == OP.OK
+            offs = sample_offsets(w, n_samples, seed=R, o=o if R == 1 else None)
+            idx = torch.from_numpy(offs).cuda()
+            want = expected_bytes(w, R, offs)
+            for q in range(w.P):
+                got = st.bufs[q][idx].cpu().numpy()
+                np.testing.assert_array_equal(got, want, err_msg=f"round {R} buffer {q}")
+            _gates_match(st, o)
+            st.plan.next_round()
+            o.next_round()
+    finally:
+        st.plan.close()
+
+
+def test_parity_c2_full_bench_launch():
+    _run_sampled(W.C2, W.C2.rounds, 1 << 16, runner.bench_launch(W.C2))
+
+
+def test_parity_c3_full():
+    _run_sampled(W.C3, W.C3.rounds, 1 << 15, runner.bench_launch(W.C3))
+
+
+def test_parity_c4b_broadcast_full():
+    w = W.C4B
+    st = runner.make(w, **runner.bench_launch(w))
+    try:
+        regs = st.plan.info()
+        assert regs[0] == 1
+        _ = runner.run_round(st)
+        offs = sample_offsets(w, 1 << 16, seed=5)
+        offs = np.unique(np.concatenate([offs, [0, (1 << 30) - 1, 1 << 30, (2 << 30) - 1, 2 << 30,
+                                                w.buf_bytes - 1]]))
+        want = expected_bytes(w, 1, offs)
+        idx = torch.from_numpy(offs).cuda()
+        for q in range(w.P):
+            np.testing.assert_array_equal(st.bufs[q][idx].cpu().numpy(), want)
+    finally:
+        st.plan.close()
+
+
+def test_broadcast_split_into_1gib_copies():
+    s = runner.schedules_for(W.C4B)
+    regs, writers = s[0].chunk(0)
+    assert [r[1] for r in regs] == [1 << 30, 1 << 30, 1 << 29]
+    assert all(x.n_chunks == 0 for x in s[1:])

@@ -1,0 +1,209 @@
+"""GPU: the plan's protocol edges -- extra and missing marks, the round limit, close in
+mid-round, the consumer-side wait (and its timeout), state errors, the host-buffer round --
+each against what the oracle says for the same sequence of events."""
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from gpu_common import oracle_plan, oracle_round
+from oracle import hashfill as H
+from oracle import plan as OP
+
+pytestmark = pytest.mark.gpu
+
+if torch.cuda.is_available():
+    from conftest import ensure_built
+    ensure_built()
+    import device_triggered_transfers_gb300 as D
+    from device_triggered_transfers_gb300 import runner
+
+WS = W.Workload("p", P=2, M=64, N=128, dtype=W.BF16, kind="chunks", rounds=3, seed=21,
+                num_chunks=2)
+
+
+def _fast_timeout_opts():
+    return D.dtt_plan_opts_default(max_polls=20000)
+
+
+def test_extra_mark_is_reported():
+    st = runner.make(WS)
+    o = oracle_plan(WS)
+    try:
+        h = st.plan.start(st.producer_stream)
+        D.dtt_fill_producer(st.bufs, st.desc, h, st.producer_stream)
+        D.dtt_publish(h, 1, 1, 1, st.producer_stream)           # one mark too many on chunk 1
+        rep = st.plan.wait(raise_on_error=False)
+        assert rep.status == D.EEXTRA and rep.extras == [1]
+        assert st.plan.state == D.FAILED
+        o.start()
+        for r in range(2):
+            off = WS.slice_offset(r)
+            o.bufs[r][off:off + WS.slice_bytes] = H.fill_slice_bytes(WS.dtype, WS.seed, r, 1, WS.M, WS.N)
+            for c in o.chunks_of(r):
+                o.mark_ready(r, c)
+        o.mark_ready(0, 1)
+        o.copier_progress()
+        assert o.wait() == (OP.EXTRA, [], [1])
+        g = st.plan.read_gates()
+        np.testing.assert_array_equal(g[:, :, :5], o.gates)
+        with pytest.raises(D.DttError) as e:
+            st.plan.next_round()
+        assert e.value.code == D.ESTATE
+    finally:
+        st.plan.close()
+
+
+def test_missing_mark_times_out_and_names_short_chunks():
+    st = runner.make(WS, opts=_fast_timeout_opts())
+    o = oracle_plan(WS)
+    try:
+        h = st.plan.start(st.producer_stream)
+        D.dtt_publish(h, 0, 2, 0, st.producer_stream)   # rank 0: both chunks
+        D.dtt_publish(h, 3, 1, 0, st.producer_stream)   # rank 1: chunk 3 only; chunk 2 is short
+        rep = st.plan.wait(raise_on_error=False)
+        assert rep.status == D.ETIMEDOUT
+        o.start()
+        for c in (0, 1):
+            o.mark_ready(0, c)
+        o.mark_ready(1, 3)
+        o.copier_progress()
+        status, short, extra = o.wait()
+        assert status == OP.TIMEOUT and rep.shorts == short == [2, 3]
+        assert rep.copier_timeouts >= 1
+        g = st.plan.read_gates()
+        np.testing.assert_array_equal(g[:, :, :5], o.gates)
+    finally:
+        st.plan.close()
+
+
+def test_round_limit():
+    top = (1 << 32) - 1
+    st = runner.make(WS, opts=D.dtt_plan_opts_default(initial_round=top - 1))
+    o = oracle_plan(WS, initial_round=top - 1)
+    try:
+        for R in (top - 1, top):
+            assert st.plan.round == R
+            assert runner.run_round(st).status == D.OK
+            assert oracle_round(o, WS)[0] == OP.OK
+            np.testing.assert_array_equal(st.plan.read_gates()[:, :, :5], o.gates)
+            for q in range(2):
+                np.testing.assert_array_equal(st.bufs[q].cpu().numpy(), o.bufs[q])
+            if R < top:
+                st.plan.next_round()
+                o.next_round()
+        with pytest.raises(D.DttError) as e:
+            st.plan.next_round()
+        assert e.value.code == D.EROUNDLIMIT
+        assert st.plan.state == D.DONE
+    finally:
+        st.plan.close()
+
+
+def test_state_errors():
+    st = runner.make(WS)
+    try:
+        for f in (st.plan.wait, st.plan.next_round):
+            with pytest.raises(D.DttError) as e:
+                f()
+            assert e.value.code == D.ESTATE
+        st.plan.start(st.producer_stream)
+        with pytest.raises(D.DttError) as e:
+            st.plan.start(st.producer_stream)
+        assert e.value.code == D.ESTATE
+        D.dtt_fill_producer(st.bufs, st.desc, st.plan.handles, st.producer_stream)
+        assert st.plan.wait().status == D.OK
+    finally:
+        st.plan.close()
+
+
+def test_producer_stream_must_differ_from_copy_stream():
+    copy = torch.cuda.Stream()
+    bufs = [torch.zeros(WS.buf_bytes, dtype=torch.uint8, device="cuda") for _ in range(2)]
+    plan = D.Plan(bufs, WS.buf_bytes, runner.schedules_for(WS), copy_stream=copy)
+    with pytest.raises(D.DttError) as e:
+        plan.start(copy)
+    assert e.value.code == D.EINVAL
+    plan.close()
+
+
+def test_close_mid_round_sends_chunks_as_they_stand():
+    st = runner.make(WS)
+    o = oracle_plan(WS)
+    h = st.plan.start(st.producer_stream)
+    data = torch.arange(WS.slice_bytes, dtype=torch.int64).remainder(251).to(torch.uint8).cuda()
+    st.producer_stream.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(st.producer_stream):
+        st.bufs[0][:WS.slice_bytes // 2].copy_(data[:WS.slice_bytes // 2])
+    D.dtt_publish(h, 0, 1, 0, st.producer_stream)       # rank 0 marks its first chunk only
+    st.plan.close()                                      # opens every gate still closed
+    torch.cuda.synchronize()
+    o.start()
+    o.bufs[0][:WS.slice_bytes // 2] = data[:WS.slice_bytes // 2].cpu().numpy()
+    o.mark_ready(0, 0)
+    o.close()
+    for q in range(2):
+        np.testing.assert_array_equal(st.bufs[q].cpu().numpy(), o.bufs[q])
+
+
+def test_consumer_wait_reads_this_rounds_data():
+    w = W.small(W.C2, M=256, N=1024, num_chunks=4)
+    st = runner.make(w)
+    o = oracle_plan(w)
+    n_global = st.plan.info()[0]
+    dst = torch.zeros(w.buf_bytes, dtype=torch.uint8, device="cuda")
+    status = torch.full((n_global,), 99, dtype=torch.int32, device="cuda")
+    cons = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    try:
+        for R in (1, 2):
+            h = st.plan.start(st.producer_stream)
+            st.plan.consumer_gather(1, dst, 1 << 24, status, 4, cons)
+            D.dtt_fill_producer(st.bufs, st.desc, h, st.producer_stream)
+            st.plan.wait()
+            cons.synchronize()
+            assert oracle_round(o, w)[0] == OP.OK
+            assert status.cpu().tolist() == [0] * n_global
+            got = dst.cpu().numpy()
+            S = w.slice_bytes
+            for r in range(w.P):
+                if r != 1:   # every other rank's slice, as this round left it
+                    np.testing.assert_array_equal(got[r * S:(r + 1) * S], o.bufs[1][r * S:(r + 1) * S])
+            st.plan.next_round()
+            o.next_round()
+    finally:
+        st.plan.close()
+
+
+def test_consumer_wait_times_out_on_a_gate_nobody_opens():
+    st = runner.make(WS, opts=_fast_timeout_opts())
+    n_global = st.plan.info()[0]
+    dst = torch.zeros(WS.buf_bytes, dtype=torch.uint8, device="cuda")
+    status = torch.zeros((n_global,), dtype=torch.int32, device="cuda")
+    cons = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    st.plan.start(st.producer_stream)
+    st.plan.consumer_gather(0, dst, 2000, status, 2, cons)   # no producer runs this round
+    cons.synchronize()
+    assert status.cpu().tolist() == [0, 0, D.ETIMEDOUT, D.ETIMEDOUT]
+    st.plan.close()
+
+
+def test_allgather_from_host_buffers():
+    w = W.small(W.C2, M=128, N=512, num_chunks=4)
+    st = runner.make(w)
+    S = w.slice_bytes
+    try:
+        for R in (1, 2):
+            host = [torch.from_numpy(H.fill_slice_bytes(w.dtype, w.seed + R, r, R, w.M, w.N)).pin_memory()
+                    for r in range(w.P)]
+            out = torch.zeros(w.buf_bytes, dtype=torch.uint8).pin_memory()
+            rep = st.plan.allgather_host(host, out, out_rank=2, stream=st.producer_stream)
+            assert rep.status == D.OK
+            want = np.concatenate([h.numpy() for h in host])
+            np.testing.assert_array_equal(out.numpy(), want)
+            for q in range(w.P):
+                np.testing.assert_array_equal(st.bufs[q].cpu().numpy(), want)
+        assert st.plan.round == 3
+    finally:
+        st.plan.close()

@@ -1,0 +1,137 @@
+"""Host-side checks of libdtt.so that need no GPU: exports, schedule builders against the
+oracle's independent builders, the shared step-to-tile order, and plan validation."""
+import ctypes as C
+import itertools
+import os
+import re
+
+import numpy as np
+import pytest
+
+from conftest import ROOT, ensure_built
+
+ensure_built()
+
+import device_triggered_transfers_gb300 as D  # noqa: E402
+from oracle import schedule as OS  # noqa: E402
+
+
+def _declared_functions():
+    names = set()
+    for f in os.listdir(os.path.join(ROOT, "include")):
+        if not f.endswith(".h"):
+            continue
+        text = open(os.path.join(ROOT, "include", f)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^\s*(?:const\s+)?[\w\s\*]+?\b(dtt_\w+)\s*\(", text, flags=re.M):
+            names.add(m.group(1))
+    return names
+
+
+def test_library_exports_every_declared_function():
+    names = _declared_functions()
+    assert {"dtt_plan_create", "dtt_plan_start", "dtt_plan_wait", "dtt_plan_next_round",
+            "dtt_plan_close", "dtt_schedule_tile_chunks", "dtt_barrier_handrolled",
+            "dtt_fill_producer", "dtt_publish"} <= names
+    lib = C.CDLL(D.LIB_PATH)
+    missing = [n for n in sorted(names) if not hasattr(lib, n)]
+    assert not missing, missing
+    for n in names:          # the binding declares a signature for every one of them
+        assert n in D._SIGS, n
+
+
+def _regions(s):
+    return [(regs, w) for regs, w in s.chunks()]
+
+
+def _oracle(s):
+    return [([tuple(r) for r in c.regions], c.writers) for c in s.chunks]
+
+
+@pytest.mark.parametrize("rows,rb,pitch,np_", [(4, 64, 64, 1), (7, 12, 16, 3), (1, 5, 5, 2),
+                                               (3000, 1 << 20, 1 << 20, 8)])
+def test_whole_matches_oracle(rows, rb, pitch, np_):
+    a = D.dtt_schedule_whole(1024, rows, rb, pitch, np_)
+    assert _regions(a) == _oracle(OS.whole(1024, rows, rb, pitch, np_))
+
+
+@pytest.mark.parametrize("rows,rb,pitch,n", [(10, 4, 4, 4), (6, 4, 8, 3), (4096, 8192, 8192, 8),
+                                             (17, 6, 6, 5), (2560, 1 << 20, 1 << 20, 2)])
+def test_chunks_matches_oracle(rows, rb, pitch, n):
+    a = D.dtt_schedule_chunks(96, rows, rb, pitch, n)
+    assert _regions(a) == _oracle(OS.chunks(96, rows, rb, pitch, n))
+
+
+CASES = [(7, 5, 2, 2, 2, 1, 0), (9, 9, 1, 4, 3, 4, 3), (300, 200, 2, 64, 48, 5, 2),
+         (8000, 8064, 2, 128, 128, 148, 8), (2048, 4096, 2, 128, 128, 148, 0),
+         (13, 203, 2, 8, 16, 7, 1), (100, 100, 4, 100, 100, 1, 0)]
+
+
+@pytest.mark.parametrize("M,N,e,BM,BN,T,gm", CASES)
+def test_tile_chunks_matches_oracle(M, N, e, BM, BN, T, gm):
+    pitch = N * e + (16 if M < 50 else 0)
+    tm, tn = -(-M // BM), -(-N // BN)
+    a = D.dtt_schedule_tile_chunks(pitch * 2, M, N, e, pitch, BM, BN, T,
+                                   D.ORDER_GROUPED if gm else D.ORDER_ROW_MAJOR, gm)
+    order = (lambda s: OS.order_grouped(s, tm, tn, gm)) if gm else None
+    assert _regions(a) == _oracle(OS.tile_chunks(pitch * 2, M, N, e, pitch, BM, BN, T, order))
+
+
+def test_tile_chunks_with_python_order_and_bad_order():
+    fn = lambda s: (s % 3, s // 3)   # column-major over a 3 x 2 tile grid  # noqa: E731
+    a = D.dtt_schedule_tile_chunks(0, 6, 4, 1, 4, 2, 2, 2, order_fn=fn)
+    assert _regions(a) == _oracle(OS.tile_chunks(0, 6, 4, 1, 4, 2, 2, 2, fn))
+    with pytest.raises(D.DttError) as e:
+        D.dtt_schedule_tile_chunks(0, 6, 4, 1, 4, 2, 2, 2, order_fn=lambda s: (0, 0))
+    assert e.value.code == D.EINVAL
+
+
+@pytest.mark.parametrize("tm,tn,gm", [(63, 63, 8), (5, 7, 2), (16, 32, 1), (3, 3, 5)])
+def test_tile_of_matches_oracle(tm, tn, gm):
+    for s in range(tm * tn):
+        assert D.dtt_tile_of(D.ORDER_GROUPED, gm, s, tm, tn) == OS.order_grouped(s, tm, tn, gm)
+        assert D.dtt_tile_of(D.ORDER_ROW_MAJOR, 0, s, tm, tn) == OS.order_row_major(s, tm, tn)
+
+
+def test_hand_built_schedule_and_1gib_split():
+    s = D.dtt_schedule_empty()
+    s.add_chunk([(0, 5 * (1 << 29), 1, 5 * (1 << 29)), (100, 8, 3, 16)], 2)
+    regs, w = s.chunk(0)
+    assert w == 2
+    assert regs == [(0, 1 << 30, 1, 1 << 30), (1 << 30, 1 << 30, 1, 1 << 30),
+                    (2 << 30, 1 << 29, 1, 1 << 29), (100, 8, 3, 16)]
+    with pytest.raises(D.DttError):
+        s.add_chunk([(0, 8, 1, 8)], 0)
+
+
+def _create(bufs_n, buf_bytes, scheds, **opts):
+    o = D.dtt_plan_opts_default(**opts)
+    fake = [0x10000000 * (i + 1) for i in range(bufs_n)]   # never dereferenced by validation
+    try:
+        D.Plan(fake, buf_bytes, scheds, o).close()
+    except D.DttError as e:
+        return e.code
+    return D.OK
+
+
+def test_plan_validation_codes_without_a_gpu():
+    P, M, rb = 3, 8, 64
+    S = M * rb
+    good = [D.dtt_schedule_chunks(r * S, M, rb, rb, 2) for r in range(P)]
+    # a valid plan passes validation and only then needs the device
+    code = _create(P, P * S, good)
+    assert code in (D.ECUDA, D.OK)
+    bad = list(good)
+    bad[1] = D.dtt_schedule_whole(0, P * M, rb, rb, 1)    # the whole buffer, not its own rows
+    assert _create(P, P * S, bad) == D.EOUTOFROWS
+    assert _create(P, P * S, bad, allgather=0) == D.EOVERLAP
+    assert _create(P, P * S, good, max_regions=5) == D.ECAPACITY
+    outside = [D.dtt_schedule_whole(P * S - 8, 1, 16, 16, 1), None, None]
+    assert _create(P, P * S, outside, allgather=0) == D.EINVAL
+    # interleaved 2D windows that share no byte pass; shifted by one byte they overlap
+    a, b, c = D.dtt_schedule_empty(), D.dtt_schedule_empty(), D.dtt_schedule_empty()
+    a.add_chunk([(0, 4, 3, 8)], 1)
+    b.add_chunk([(4, 4, 3, 8)], 1)
+    c.add_chunk([(3, 4, 3, 8)], 1)
+    assert _create(2, 24, [a, b], allgather=0) in (D.ECUDA, D.OK)
+    assert _create(2, 24, [a, c], allgather=0) == D.EOVERLAP
