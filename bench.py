@@ -1,0 +1,364 @@
+"""Benchmark of the triggered all-gather on one GB300 (replicas on N GPUs under torchrun).
+
+A step is one round of the whole hot path on the 4-rank chunked workload: plan_start launches
+the round's copier, the hashed-fill producer writes every rank's 32 MiB slice in 512-row
+chunks and marks each one, the copier fans each ready chunk out to the three peers and signals
+arrival, and plan_wait runs the completion check and returns to the host; next_round ends the
+step.  Prints one JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--config NAME]
+
+--impl reference times the CPU oracle (the plain restatement of the method in oracle/) on the
+host cores, on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "delivered all-gather GB/s and % of HBM peak (1 GB300); gate-to-arrival latency"
+DEFAULT_CONFIG = W.C2.name
+
+# dram__bytes_read.sum + dram__bytes_write.sum per copier launch from one ncu capture of the
+# same workload and launch configuration (profiles/copier_c2_chunks_p4.md); None until taken or
+# once the kernel changes.
+NCU_TRAFFIC = {}
+
+
+def describe(w, launch) -> str:
+    if w.kind == "chunks":
+        sched = f"chunks() {w.num_chunks} x {w.M // w.num_chunks} rows, 1 writer each"
+    elif w.kind == "whole":
+        sched = f"whole() with {w.num_programs} writers"
+    else:
+        sched = (f"tile_chunks {w.BM}x{w.BN}, {w.num_programs} programs, "
+                 f"{w.tiles_per_chunk} tiles per chunk, GROUP_M={w.group_m}")
+    cl = launch.get("cluster", 1)
+    prod = f"; producer programs are {cl}-CTA clusters" if cl > 1 else ""
+    kind = "broadcast from rank 0" if w.broadcast else "in-place all-gather"
+    return (f"{w.name}: {kind}, P={w.P} virtual ranks, {w.dtype} [{w.buf_rows}, {w.N}] per "
+            f"buffer, {sched}{prod}")
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# ---- clocks ------------------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.dev), "-lms", "100"], stdout=self.out, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.out.close()
+        return False
+
+    def summary(self):
+        if self.proc is None:
+            return None
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                rows.append((float(parts[0]), float(parts[1]), parts[4:8]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, flags in rows for i, f in enumerate(flags)
+                          if f.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows),
+                "sm_max_mhz": max(r[1] for r in rows), "reasons": reasons, "samples": len(rows)}
+
+
+# ---- CPU oracle timing ---------------------------------------------------------------------------
+def oracle_sample_workload(w):
+    """A bounded sample of workload w for the CPU oracle: same P, row length, dtype and
+    schedule kind, fewer rows (one chunk's worth per rank for the chunked workload)."""
+    if w.kind == "chunks":
+        rows = max(1, min(128, w.M // w.num_chunks))
+        return W.small(w, M=rows, num_chunks=1), f"{rows} of {w.M} rows per rank, one chunk"
+    if w.kind == "tile_chunks":
+        rows = min(w.M, 2 * w.BM)
+        return W.small(w, M=rows), f"{rows} of {w.M} rows per rank"
+    rows = min(w.M, 256)
+    return W.small(w, M=rows, num_programs=min(w.num_programs, rows)), f"{rows} of {w.M} rows"
+
+
+def time_oracle(w, budget_s: float = 10.0, max_rounds: int = 1000):
+    """Run the oracle's sequential rounds on a sample of w until budget_s; GB/s delivered."""
+    from oracle.run import make_plan as oracle_plan, run_round as oracle_round
+    sw, what = oracle_sample_workload(w)
+    o = oracle_plan(sw)
+    n, t0 = 0, time.perf_counter()
+    while n < max_rounds:
+        status = oracle_round(o, sw)
+        assert status[0] == "OK"
+        o.next_round()
+        n += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return sw.delivered_bytes_per_round() * n / dt / 1e9, n, dt, what
+
+
+# ---- distributed helpers ---------------------------------------------------------------------------
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    return ws, int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def aggregate(elapsed_s: float, units: float, world: int):
+    """Whole-job figures: max elapsed over ranks, units summed over ranks."""
+    if world == 1:
+        return elapsed_s, units
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([elapsed_s], dtype=torch.float64, device=dev)
+    u = torch.tensor([units], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---- the two arms ------------------------------------------------------------------------------------
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if world > 1 and rank != 0:
+        return 0
+    w = W.CONFIGS[args.config]
+    sw, what = oracle_sample_workload(w)
+    from oracle.run import make_plan as oracle_plan, run_round as oracle_round
+    o = oracle_plan(sw)
+    for _ in range(args.warmup):
+        oracle_round(o, sw)
+        o.next_round()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        assert oracle_round(o, sw)[0] == "OK"
+        o.next_round()
+    dt = time.perf_counter() - t0
+    value = sw.delivered_bytes_per_round() * args.steps / dt / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+            "config": {"workload": describe(w, {}), "sample": what},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": what},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+def run_ours(args):
+    import torch
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.cuda.current_device()
+    import device_triggered_transfers_gb300 as D
+    from device_triggered_transfers_gb300 import runner
+
+    w = W.CONFIGS[args.config]
+    launch = runner.bench_launch(w)
+    # the copier runs on a stream the bench can put events on
+    copy_stream = torch.cuda.Stream(priority=-1)
+    st = runner.make(w, copy_stream=copy_stream, **launch)
+    prod = st.producer_stream
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(copy_stream)
+        h = st.plan.start(prod)
+        if ev is not None:
+            ev[1].record(copy_stream)
+            ev[2].record(prod)
+        D.dtt_fill_producer(st.bufs, st.desc, h, prod)
+        if ev is not None:
+            ev[3].record(prod)
+        st.plan.wait()
+        st.plan.next_round()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(dev) as clocks:
+        time.sleep(0.25)
+        e_start.record(prod)
+        for i in range(K):
+            step(evs[i])
+        e_end.record(prod)
+        torch.cuda.synchronize()
+        time.sleep(0.25)
+    barrier(world)
+    elapsed = e_start.elapsed_time(e_end) / 1e3
+    copier_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    fill_ms = [e[2].elapsed_time(e[3]) for e in evs]
+    D_round = w.delivered_bytes_per_round()
+    B_alg = w.algorithmic_bytes_per_round()
+    t_max, units = aggregate(elapsed, D_round * K, world)
+    value = units / t_max / 1e9
+
+    # gate-to-arrival latency and the copier window, from the gate timestamps of extra rounds
+    lat, windows = [], []
+    for _ in range(20):
+        step()
+        g = st.plan.read_gates()
+        n_global, first, n_chunks, _ = st.plan.info()
+        t_open_min, t_arr_max = None, 0
+        for r in range(w.P):
+            for c in range(first[r], first[r] + n_chunks[r]):
+                to = int(g[r, c, D.GATE_T_OPEN])
+                t_open_min = to if t_open_min is None else min(t_open_min, to)
+                for p in range(w.P):
+                    if p != r:
+                        ta = int(g[p, c, D.GATE_T_ARRIVE])
+                        lat.append(ta - to)
+                        t_arr_max = max(t_arr_max, ta)
+        windows.append((t_arr_max - t_open_min) / 1e9)
+    peak, peak_kind = load_peaks()
+    cop_s = statistics.mean(copier_ms) / 1e3
+    achieved = B_alg / cop_s / 1e9
+
+    # e2e: the host-buffer round through the public API: H2D of every rank's slice from pinned
+    # memory, the triggered fan-out, D2H of rank 0's gathered buffer
+    S = w.slice_bytes
+    host_in = [torch.empty(S, dtype=torch.uint8).pin_memory() for _ in range(w.P)]
+    for r in range(w.P):
+        host_in[r].copy_(st.bufs[r][w.slice_offset(r):w.slice_offset(r) + S].cpu())
+    host_out = torch.empty(w.buf_bytes, dtype=torch.uint8).pin_memory()
+    e2e_steps = max(1, min(K, 20))
+    for _ in range(2):
+        st.plan.allgather_host(host_in, host_out, 0, prod)
+    torch.cuda.synchronize()
+    x0, x1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    x0.record(prod)
+    for _ in range(e2e_steps):
+        st.plan.allgather_host(host_in, host_out, 0, prod)
+    x1.record(prod)
+    torch.cuda.synchronize()
+    e2e_t, e2e_units = aggregate(x0.elapsed_time(x1) / 1e3, D_round * e2e_steps, world)
+    e2e = {"value": e2e_units / e2e_t / 1e9, "unit": "GB/s", "h2d_bytes_per_step": S * w.P,
+           "d2h_bytes_per_step": w.buf_bytes}
+    st.plan.close()
+
+    if rank != 0:
+        return 0
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        v, n, dt, what = time_oracle(w, budget_s=args.cpu_seconds)
+        cpu = {"value": v, "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": f"{what}; {n} oracle round(s) in {dt:.1f} s"}
+    lat_sorted = sorted(lat)
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": t_max / K * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": {"workload": describe(w, launch), "parallelism": f"replicas{world}",
+                   "l2": "inputs larger than L2 (%d MiB of buffers)" % (w.P * w.buf_bytes >> 20),
+                   "step": "plan_start + fill producer + copier + plan_wait + next_round"},
+        "hbm_frac_end_to_end": {"of_measured": B_alg * units / D_round / t_max / 1e9 / peak,
+                                "of_spec_8000": B_alg * units / D_round / t_max / 1e9 / 8000.0},
+        "roofline": {"kernel": "copier_kernel", "bound": "hbm", "achieved": achieved,
+                     "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": NCU_TRAFFIC.get(w.name),
+                     "algorithmic_bytes_per_launch": B_alg},
+        "kernels_ms": {"copier_mean": statistics.mean(copier_ms),
+                       "fill_mean": statistics.mean(fill_ms)},
+        "copier_window": {"gbs_delivered": D_round / statistics.median(windows) / 1e9,
+                          "hbm_frac": B_alg / statistics.median(windows) / 1e9 / peak},
+        "gate_to_arrival_ns": {"median": lat_sorted[len(lat_sorted) // 2],
+                               "p99": lat_sorted[min(len(lat_sorted) - 1, int(len(lat_sorted) * 0.99))],
+                               "samples": len(lat_sorted)},
+        "e2e": e2e,
+        "gpu_launches": 3 * K,
+        "clocks": clocks.summary(),
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default=DEFAULT_CONFIG, choices=sorted(W.CONFIGS))
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -94,6 +94,7 @@ _P = C.c_void_p
 _u32, _u64, _i32 = C.c_uint32, C.c_uint64, C.c_int32
 _SIGS = {
     "dtt_last_error": (C.c_char_p, []),
+    "dtt_preload": (C.c_int, []),
     "dtt_tile_of": (C.c_int, [C.POINTER(dtt_order), _u64, _u32, _u32, C.POINTER(_u32), C.POINTER(_u32)]),
     "dtt_schedule_whole": (C.c_int, [_u64, _u64, _u64, _u64, _u32, C.POINTER(_P)]),
     "dtt_schedule_chunks": (C.c_int, [_u64, _u64, _u64, _u64, _u32, C.POINTER(_P)]),

@@ -96,6 +96,13 @@ __global__ void reveal_kernel(const __grid_constant__ RevealParams p) {
 }
 
 }  // namespace
+
+cudaError_t preload_barrier_kernels() {
+    cudaError_t e = prepare_kernel(handrolled_kernel);
+    if (e == cudaSuccess) e = prepare_kernel(reveal_kernel);
+    return e;
+}
+
 }  // namespace dtt
 
 struct dtt_barrier {
@@ -129,6 +136,8 @@ int dtt_barrier_handrolled(int32_t* const* signal, int32_t* const* y, uint32_t P
 
 int dtt_barrier_create(uint32_t P, dtt_barrier** out) {
     if (!out || P < 1 || P > DTT_MAX_RANKS) return fail(DTT_EINVAL, "dtt_barrier_create: bad args");
+    const int pre = preload_once();
+    if (pre != DTT_OK) return pre;
     dtt_barrier* b = new (std::nothrow) dtt_barrier();
     if (!b) return fail(DTT_ENOMEM, "dtt_barrier_create: out of memory");
     b->P = P;

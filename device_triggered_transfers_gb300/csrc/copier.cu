@@ -270,6 +270,15 @@ cudaError_t launch_consumer(const CopierParams& p, dtt_handle h, char* dst, uint
     return cudaGetLastError();
 }
 
+cudaError_t preload_copier_kernels() {
+    cudaError_t e = prepare_kernel(copier_kernel);
+    if (e == cudaSuccess) e = prepare_kernel(check_kernel);
+    if (e == cudaSuccess) e = prepare_kernel(force_open_kernel);
+    if (e == cudaSuccess) e = prepare_kernel(publish_kernel);
+    if (e == cudaSuccess) e = prepare_kernel(consumer_kernel);
+    return e;
+}
+
 }  // namespace dtt
 
 using namespace dtt;

@@ -147,6 +147,14 @@ __global__ void __launch_bounds__(1024) fill_kernel(const __grid_constant__ Fill
 }
 
 }  // namespace
+
+cudaError_t preload_fill_kernels() {
+    cudaError_t e = prepare_kernel(fill_kernel<DTT_BF16>);
+    if (e == cudaSuccess) e = prepare_kernel(fill_kernel<DTT_F32>);
+    if (e == cudaSuccess) e = prepare_kernel(fill_kernel<DTT_U8>);
+    return e;
+}
+
 }  // namespace dtt
 
 using namespace dtt;

@@ -90,6 +90,30 @@ cudaError_t launch_force_open(uint64_t* gates, const ChunkDesc* chunks, uint32_t
 cudaError_t launch_consumer(const CopierParams& p, dtt_handle h, char* dst, uint64_t max_polls,
                             int32_t* status, uint32_t ctas, cudaStream_t s);
 
+// An SM runs CTAs of one shared-memory carveout at a time: a kernel whose preferred L1/shared
+// split differs from that of the copier CTAs already resident cannot start on those SMs until
+// they drain, and with a copier CTA on every SM that is after the copier exits.  Every library
+// kernel therefore asks for the same split, the largest shared-memory share.
+constexpr int kCarveout = cudaSharedmemCarveoutMaxShared;
+
+// Load a kernel now (lazy module loading would otherwise load it at its first launch, which can
+// wait for the device to go idle) and give it the library's carveout.
+template <class K>
+cudaError_t prepare_kernel(K kernel) {
+    cudaFuncAttributes a;
+    cudaError_t e = cudaFuncGetAttributes(&a, kernel);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, kCarveout);
+    return e;
+}
+
+// Force-load each translation unit's kernels on the current device (see dtt_preload).
+cudaError_t preload_copier_kernels();
+cudaError_t preload_fill_kernels();
+cudaError_t preload_barrier_kernels();
+// dtt_preload() for library-internal callers: once per device, then a no-op.
+int preload_once();
+
 // Host schedule representation (schedule.cpp).
 struct HostChunk {
     std::vector<dtt_region> regions;

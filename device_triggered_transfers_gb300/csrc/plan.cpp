@@ -6,6 +6,7 @@
 #include <algorithm>
 #include <cstring>
 #include <new>
+#include <mutex>
 #include <vector>
 
 #include "internal.h"
@@ -318,7 +319,30 @@ int upload(dtt_plan* p) {
 
 }  // namespace
 
+namespace dtt {
+
+static std::mutex g_preload_mu;
+static uint64_t g_preloaded = 0;     // bit d: device d's kernels are loaded
+
+int preload_once() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return fail(DTT_ECUDA, "dtt_preload: no CUDA device");
+    std::lock_guard<std::mutex> lock(g_preload_mu);
+    const uint64_t bit = dev < 64 ? (1ull << dev) : 0;
+    if (bit && (g_preloaded & bit)) return DTT_OK;
+    cudaError_t e = preload_copier_kernels();
+    if (e == cudaSuccess) e = preload_fill_kernels();
+    if (e == cudaSuccess) e = preload_barrier_kernels();
+    if (e != cudaSuccess) return fail(DTT_ECUDA, "dtt_preload: %s", cudaGetErrorString(e));
+    g_preloaded |= bit;
+    return DTT_OK;
+}
+
+}  // namespace dtt
+
 extern "C" {
+
+int dtt_preload(void) { return preload_once(); }
 
 void dtt_plan_opts_default(dtt_plan_opts* o) {
     if (!o) return;
@@ -374,6 +398,11 @@ int dtt_plan_create(void* const* bufs, uint64_t buf_bytes, uint32_t P,
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, p->device) != cudaSuccess) {
         delete p;
         return fail(DTT_ECUDA, "dtt_plan_create: no CUDA device");
+    }
+    rc = preload_once();
+    if (rc != DTT_OK) {
+        delete p;
+        return rc;
     }
     p->copier_ctas = o.copier_ctas ? o.copier_ctas : (uint32_t)sms * o.ctas_per_sm;
     p->copier_threads = o.copier_threads;

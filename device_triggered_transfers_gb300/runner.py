@@ -71,15 +71,16 @@ class Setup:
 
 
 def make(w, opts=None, cluster: int = 1, programs: Optional[int] = None, threads: int = 0,
-         device: str = "cuda", fill_byte: int = 0) -> Setup:
-    """Allocate the P symmetric buffers (uint8, w.buf_bytes each), build the plan and producer."""
+         device: str = "cuda", fill_byte: int = 0, copy_stream=None) -> Setup:
+    """Allocate the P symmetric buffers (uint8, w.buf_bytes each), build the plan and producer.
+    copy_stream: a non-blocking stream for the copier (None: the plan makes its own)."""
     bufs = [torch.full((w.buf_bytes,), fill_byte, dtype=torch.uint8, device=device)
             for _ in range(w.P)]
     scheds = schedules_for(w)
     if opts is None:
         opts = dtt_plan_opts_default()
     opts.allgather = 0 if w.broadcast else 1
-    plan = Plan(bufs, w.buf_bytes, scheds, opts)
+    plan = Plan(bufs, w.buf_bytes, scheds, opts, copy_stream=copy_stream)
     for s in scheds:
         s.free()
     desc = producer_desc(w, cluster=cluster, programs=programs, threads=threads)

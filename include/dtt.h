@@ -393,6 +393,20 @@ int dtt_barrier_reveal(dtt_barrier* b, const int32_t* const* x, int32_t* const* 
 
 const char* dtt_last_error(void);
 
+/* Prepare every kernel of the library on the current device: load it now, and give it the
+ * library's shared-memory carveout (cudaSharedmemCarveoutMaxShared).
+ *  - With lazy module loading (the CUDA default) the first launch of a kernel may wait until
+ *    the device is idle, and a copier spinning on a gate keeps it busy until its polls run out.
+ *  - An SM runs CTAs of one L1/shared-memory split at a time.  The copier puts a CTA on every
+ *    SM, so a kernel whose preferred split differs (the driver derives one from occupancy when
+ *    none is set) cannot start until the copier exits.
+ * dtt_plan_create and dtt_barrier_create call it (once per device).  A caller's own producer
+ * and consumer kernels that run during a round need the same two steps: load them before the
+ * first round (cudaFuncGetAttributes) and set cudaFuncAttributePreferredSharedMemoryCarveout
+ * to cudaSharedmemCarveoutMaxShared.  Otherwise they start only after the copier gives up.
+ * Errors: DTT_ECUDA. */
+int dtt_preload(void);
+
 #ifdef __cplusplus
 }
 #endif

@@ -130,9 +130,11 @@ def test_producer_stream_must_differ_from_copy_stream():
 def test_close_mid_round_sends_chunks_as_they_stand():
     st = runner.make(WS)
     o = oracle_plan(WS)
-    h = st.plan.start(st.producer_stream)
+    # made before the round starts: a first-use kernel launched while the copier spins could
+    # wait on it (lazy module loading)
     data = torch.arange(WS.slice_bytes, dtype=torch.int64).remainder(251).to(torch.uint8).cuda()
     st.producer_stream.wait_stream(torch.cuda.current_stream())
+    h = st.plan.start(st.producer_stream)
     with torch.cuda.stream(st.producer_stream):
         st.bufs[0][:WS.slice_bytes // 2].copy_(data[:WS.slice_bytes // 2])
     D.dtt_publish(h, 0, 1, 0, st.producer_stream)       # rank 0 marks its first chunk only
