@@ -127,6 +127,8 @@ _SIGS = {
     "dtt_barrier_destroy": (None, [_P]),
     "dtt_barrier_reveal": (C.c_int, [_P, C.POINTER(_P), C.POINTER(_P), C.POINTER(_P), _u32, _u64,
                                      _P, _P]),
+    "dtt_barrier_reveal_noalloc": (C.c_int, [C.POINTER(_P), C.POINTER(_P), C.POINTER(_P), _u32,
+                                             _u32, _u64, _P, _P]),
 }
 
 _lib = None
@@ -444,3 +446,11 @@ class Barrier:
 
 def dtt_barrier_create(P: int) -> Barrier:
     return Barrier(P)
+
+
+def dtt_barrier_reveal_noalloc(x, data, y, size: int, max_polls: int, status, stream=None) -> None:
+    """The builtin reveal with its counters in the library's fixed device array: allocates
+    nothing (for callers that cannot allocate device memory at call time).  Calls that overlap
+    on the GPU share that array and race; run them on one stream."""
+    _check(lib().dtt_barrier_reveal_noalloc(_ptr_array(x), _ptr_array(data), _ptr_array(y),
+                                            len(x), size, max_polls, _ptr(status), _stream(stream)))

@@ -5,6 +5,7 @@
 // notifies (atomic add, release, gpu scope) and waits (acquire loads, counted polls); a CTA
 // barrier then hands the result to the other threads.
 #include <cstdint>
+#include <mutex>
 #include <new>
 
 #include "internal.h"
@@ -183,3 +184,68 @@ int dtt_barrier_reveal(dtt_barrier* b, const int32_t* const* x, int32_t* const* 
 }
 
 }  // extern "C"
+
+// ---- the reveal without any allocation ------------------------------------------------------
+// The builtin barrier's internal counters for dtt_barrier_reveal_noalloc live in this fixed
+// array (DTT_NOALLOC_MAX_RANKS^2 int32 = 1 KiB), part of the library's device image: every GPU
+// that loads the library holds it until the process exits.  Every call uses the same array.
+static __device__ __align__(256) int32_t g_reveal_counters[DTT_NOALLOC_MAX_RANKS * DTT_NOALLOC_MAX_RANKS];
+
+namespace {
+
+std::mutex g_noalloc_mu;
+int32_t* g_noalloc_counters[64] = {};   // device address of the array, per device id
+
+// Set-up, once per device with that device current.  In host code the array's name is only a
+// host-side stand-in, so its device address must come from cudaGetSymbolAddress.
+int noalloc_counters(int32_t** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return fail(DTT_ECUDA, "dtt_barrier_reveal_noalloc: no CUDA device");
+    if (dev < 0 || dev >= 64) return fail(DTT_EINVAL, "dtt_barrier_reveal_noalloc: device id %d not supported", dev);
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_counters[dev]) {
+        const int pre = preload_once();
+        if (pre != DTT_OK) return pre;
+        void* p = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&p, g_reveal_counters);
+        if (e != cudaSuccess || !p)
+            return fail(DTT_ECUDA, "dtt_barrier_reveal_noalloc: cudaGetSymbolAddress failed: %s",
+                        cudaGetErrorString(e));
+        g_noalloc_counters[dev] = static_cast<int32_t*>(p);
+    }
+    *out = g_noalloc_counters[dev];
+    return DTT_OK;
+}
+
+}  // namespace
+
+extern "C" int dtt_barrier_reveal_noalloc(const int32_t* const* x, int32_t* const* data,
+                                          int32_t* const* y, uint32_t P, uint32_t size,
+                                          uint64_t max_polls, int32_t* status, cudaStream_t stream) {
+    if (!x || !data || !y || !status) return fail(DTT_EINVAL, "dtt_barrier_reveal_noalloc: bad args");
+    if (P < 1 || P > DTT_NOALLOC_MAX_RANKS)
+        return fail(DTT_EINVAL, "dtt_barrier_reveal_noalloc: P = %u is outside 1..%d, the ranks its static counter array holds",
+                    P, DTT_NOALLOC_MAX_RANKS);
+    RevealParams rp{};
+    for (uint32_t r = 0; r < P; ++r) {
+        if (!x[r] || !data[r] || !y[r]) return fail(DTT_EINVAL, "dtt_barrier_reveal_noalloc: NULL slice");
+        rp.x[r] = x[r];
+        rp.data[r] = data[r];
+        rp.y[r] = y[r];
+    }
+    int32_t* counters = nullptr;
+    const int rc = noalloc_counters(&counters);
+    if (rc != DTT_OK) return rc;
+    // the array keeps the previous call's counts: clear the P x P cells this call uses, in
+    // stream order, so that this call's barrier is generation 1
+    DTT_CUDA_TRY(cudaMemsetAsync(counters, 0, (size_t)P * P * sizeof(int32_t), stream));
+    rp.counters = counters;
+    rp.status = status;
+    rp.P = P;
+    rp.size = size;
+    rp.gen = 1;
+    rp.max_polls = max_polls;
+    void* args[] = {&rp};
+    DTT_CUDA_TRY(cudaLaunchCooperativeKernel((const void*)reveal_kernel, dim3(P), dim3(256), args, 0, stream));
+    return DTT_OK;
+}

@@ -387,6 +387,30 @@ int dtt_barrier_reveal(dtt_barrier* b, const int32_t* const* x, int32_t* const* 
                        int32_t* const* y, uint32_t size, uint64_t max_polls, int32_t* status,
                        cudaStream_t stream);
 
+/* The same reveal for callers that cannot allocate device memory when they call it.  The
+ * pages have no counterpart: this entry point is this library's own addition.
+ * Who needs it: code whose device memory is owned entirely by another allocator (a caching
+ * allocator or a fixed arena that a stray cudaMalloc would fail against or fragment), and code
+ * that must not pay for an allocation while other work is in flight (cudaFree synchronises the
+ * whole device).  dtt_barrier_create allocates the counters with cudaMalloc; this call does
+ * not: the internal counters live in a fixed device array inside the library, sized for
+ * DTT_NOALLOC_MAX_RANKS ranks (DTT_NOALLOC_MAX_RANKS^2 int32 = 1 KiB), which every GPU that
+ * loads the library holds until the process exits.  The call itself calls no cudaMalloc,
+ * cudaFree or other allocating routine.
+ * Arguments, results and status are those of dtt_barrier_reveal, with P given directly.
+ *  - The first call on a device (that device current) looks up the array's device address
+ *    and prepares the library's kernels; make that first call before any stream capture.
+ *  - Every call clears the P x P counters it uses (stream-ordered, on `stream`) and then runs
+ *    one barrier generation on them.
+ *  - All calls share the one array: calls that overlap on the GPU (on different streams, or
+ *    from several threads) race on it and may pass their barrier early or time out.
+ *    Serialise them, for example on one stream.
+ * Errors: DTT_EINVAL (P outside 1..DTT_NOALLOC_MAX_RANKS, NULL pointers), DTT_ECUDA. */
+#define DTT_NOALLOC_MAX_RANKS 16
+int dtt_barrier_reveal_noalloc(const int32_t* const* x, int32_t* const* data, int32_t* const* y,
+                               uint32_t P, uint32_t size, uint64_t max_polls, int32_t* status,
+                               cudaStream_t stream);
+
 /* ---------------------------------------------------------------------------------------- */
 /* Errors                                                                                    */
 /* ---------------------------------------------------------------------------------------- */
