@@ -35,7 +35,7 @@ DEFAULT_CONFIG = W.C2.name
 # dram__bytes_read.sum + dram__bytes_write.sum per copier launch from one ncu capture of the
 # same workload and launch configuration (profiles/copier_c2_chunks_p4.md); None until taken or
 # once the kernel changes.
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {"c2_chunks_p4": 477961728}
 
 
 def describe(w, launch) -> str:
@@ -221,51 +221,68 @@ def run_ours(args):
     launch = runner.bench_launch(w)
     # the copier runs on a stream the bench can put events on
     copy_stream = torch.cuda.Stream(priority=-1)
-    st = runner.make(w, copy_stream=copy_stream, **launch)
+    opts = D.dtt_plan_opts_default(deferred_copier=1 if args.deferred else 0)
+    st = runner.make(w, opts=opts, copy_stream=copy_stream, **launch)
     prod = st.producer_stream
 
-    def step(ev=None):
-        if ev is not None:
-            ev[0].record(copy_stream)
-        h = st.plan.start(prod)
-        if ev is not None:
-            ev[1].record(copy_stream)
-            ev[2].record(prod)
-        D.dtt_fill_producer(st.bufs, st.desc, h, prod)
-        if ev is not None:
-            ev[3].record(prod)
-        st.plan.wait()
-        st.plan.next_round()
+    def make_step(plan, deferred):
+        """One round; ev = 4 events: copier launch bracket (copy stream), fill bracket."""
+        def step(ev=None):
+            if ev is not None and not deferred:
+                ev[0].record(copy_stream)
+            h = plan.start(prod)
+            if ev is not None and not deferred:
+                ev[1].record(copy_stream)
+            if ev is not None:
+                ev[2].record(prod)
+            D.dtt_fill_producer(st.bufs, st.desc, h, prod)
+            if ev is not None:
+                ev[3].record(prod)
+            if deferred:      # the copier starts once the producer has finished
+                copy_stream.wait_stream(prod)
+                if ev is not None:
+                    ev[0].record(copy_stream)
+                plan.launch_copier()
+                if ev is not None:
+                    ev[1].record(copy_stream)
+            plan.wait()
+            plan.next_round()
+        return step
 
+    def timed(step, K):
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(prod)
+        for i in range(K):
+            step(evs[i])
+        e1.record(prod)
+        torch.cuda.synchronize()
+        return (e0.elapsed_time(e1) / 1e3, [e[0].elapsed_time(e[1]) for e in evs],
+                [e[2].elapsed_time(e[3]) for e in evs])
+
+    step = make_step(st.plan, args.deferred)
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
-
     K = args.steps
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
-    e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize()
     with ClockSampler(dev) as clocks:
         time.sleep(0.25)
-        e_start.record(prod)
-        for i in range(K):
-            step(evs[i])
-        e_end.record(prod)
-        torch.cuda.synchronize()
+        elapsed, copier_ms, fill_ms = timed(step, K)
         time.sleep(0.25)
     barrier(world)
-    elapsed = e_start.elapsed_time(e_end) / 1e3
-    copier_ms = [e[0].elapsed_time(e[1]) for e in evs]
-    fill_ms = [e[2].elapsed_time(e[3]) for e in evs]
     D_round = w.delivered_bytes_per_round()
     B_alg = w.algorithmic_bytes_per_round()
     t_max, units = aggregate(elapsed, D_round * K, world)
     value = units / t_max / 1e9
+    peak, peak_kind = load_peaks()
+    cop_s = statistics.mean(copier_ms) / 1e3
+    achieved = B_alg / cop_s / 1e9
 
     # gate-to-arrival latency and the copier window, from the gate timestamps of extra rounds
     lat, windows = [], []
-    for _ in range(20):
+    for _ in range(args.latency_rounds):
         step()
         g = st.plan.read_gates()
         n_global, first, n_chunks, _ = st.plan.info()
@@ -280,31 +297,44 @@ def run_ours(args):
                         lat.append(ta - to)
                         t_arr_max = max(t_arr_max, ta)
         windows.append((t_arr_max - t_open_min) / 1e9)
-    peak, peak_kind = load_peaks()
-    cop_s = statistics.mean(copier_ms) / 1e3
-    achieved = B_alg / cop_s / 1e9
 
     # e2e: the host-buffer round through the public API: H2D of every rank's slice from pinned
     # memory, the triggered fan-out, D2H of rank 0's gathered buffer
-    S = w.slice_bytes
-    host_in = [torch.empty(S, dtype=torch.uint8).pin_memory() for _ in range(w.P)]
-    for r in range(w.P):
-        host_in[r].copy_(st.bufs[r][w.slice_offset(r):w.slice_offset(r) + S].cpu())
-    host_out = torch.empty(w.buf_bytes, dtype=torch.uint8).pin_memory()
-    e2e_steps = max(1, min(K, 20))
-    for _ in range(2):
-        st.plan.allgather_host(host_in, host_out, 0, prod)
-    torch.cuda.synchronize()
-    x0, x1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    x0.record(prod)
-    for _ in range(e2e_steps):
-        st.plan.allgather_host(host_in, host_out, 0, prod)
-    x1.record(prod)
-    torch.cuda.synchronize()
-    e2e_t, e2e_units = aggregate(x0.elapsed_time(x1) / 1e3, D_round * e2e_steps, world)
-    e2e = {"value": e2e_units / e2e_t / 1e9, "unit": "GB/s", "h2d_bytes_per_step": S * w.P,
-           "d2h_bytes_per_step": w.buf_bytes}
+    e2e = None
+    if not args.no_e2e and not w.broadcast:
+        S = w.slice_bytes
+        host_in = [torch.empty(S, dtype=torch.uint8).pin_memory() for _ in range(w.P)]
+        for r in range(w.P):
+            host_in[r].copy_(st.bufs[r][w.slice_offset(r):w.slice_offset(r) + S].cpu())
+        host_out = torch.empty(w.buf_bytes, dtype=torch.uint8).pin_memory()
+        e2e_steps = max(1, min(K, 20))
+        for _ in range(2):
+            st.plan.allgather_host(host_in, host_out, 0, prod)
+        torch.cuda.synchronize()
+        x0, x1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        x0.record(prod)
+        for _ in range(e2e_steps):
+            st.plan.allgather_host(host_in, host_out, 0, prod)
+        x1.record(prod)
+        torch.cuda.synchronize()
+        e2e_t, e2e_units = aggregate(x0.elapsed_time(x1) / 1e3, D_round * e2e_steps, world)
+        e2e = {"value": e2e_units / e2e_t / 1e9, "unit": "GB/s", "h2d_bytes_per_step": S * w.P,
+               "d2h_bytes_per_step": w.buf_bytes}
     st.plan.close()
+
+    # the same copier and producer one after the other (deferred plan): each kernel alone
+    iso = None
+    if not args.deferred and args.isolated_rounds:
+        o2 = D.dtt_plan_opts_default(deferred_copier=1, allgather=0 if w.broadcast else 1)
+        plan2 = D.Plan(st.bufs, w.buf_bytes, runner.schedules_for(w), o2, copy_stream=copy_stream)
+        step2 = make_step(plan2, True)
+        for _ in range(3):
+            step2()
+        _, c2, f2 = timed(step2, args.isolated_rounds)
+        plan2.close()
+        iso = {"copier_ms": statistics.mean(c2), "fill_ms": statistics.mean(f2),
+               "copier_gbs_algorithmic": B_alg / (statistics.mean(c2) / 1e3) / 1e9,
+               "copier_frac_of_measured": B_alg / (statistics.mean(c2) / 1e3) / 1e9 / peak}
 
     if rank != 0:
         return 0
@@ -313,14 +343,17 @@ def run_ours(args):
         v, n, dt, what = time_oracle(w, budget_s=args.cpu_seconds)
         cpu = {"value": v, "unit": "GB/s", "cores": 1, "kind": "oracle",
                "sample": f"{what}; {n} oracle round(s) in {dt:.1f} s"}
-    lat_sorted = sorted(lat)
+    lat_sorted = sorted(lat) or [0]
+    mode = "copier launched after the producer (no overlap)" if args.deferred else \
+        "copier launched at plan_start, overlapping the producer"
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": t_max / K * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
         "config": {"workload": describe(w, launch), "parallelism": f"replicas{world}",
                    "l2": "inputs larger than L2 (%d MiB of buffers)" % (w.P * w.buf_bytes >> 20),
-                   "step": "plan_start + fill producer + copier + plan_wait + next_round"},
+                   "step": "plan_start + fill producer + copier + plan_wait + next_round",
+                   "mode": mode},
         "hbm_frac_end_to_end": {"of_measured": B_alg * units / D_round / t_max / 1e9 / peak,
                                 "of_spec_8000": B_alg * units / D_round / t_max / 1e9 / 8000.0},
         "roofline": {"kernel": "copier_kernel", "bound": "hbm", "achieved": achieved,
@@ -329,11 +362,13 @@ def run_ours(args):
                      "algorithmic_bytes_per_launch": B_alg},
         "kernels_ms": {"copier_mean": statistics.mean(copier_ms),
                        "fill_mean": statistics.mean(fill_ms)},
-        "copier_window": {"gbs_delivered": D_round / statistics.median(windows) / 1e9,
-                          "hbm_frac": B_alg / statistics.median(windows) / 1e9 / peak},
+        "isolated": iso,
+        "copier_window": ({"gbs_delivered": D_round / statistics.median(windows) / 1e9,
+                           "hbm_frac": B_alg / statistics.median(windows) / 1e9 / peak}
+                          if windows else None),
         "gate_to_arrival_ns": {"median": lat_sorted[len(lat_sorted) // 2],
                                "p99": lat_sorted[min(len(lat_sorted) - 1, int(len(lat_sorted) * 0.99))],
-                               "samples": len(lat_sorted)},
+                               "samples": len(lat)},
         "e2e": e2e,
         "gpu_launches": 3 * K,
         "clocks": clocks.summary(),
@@ -352,6 +387,12 @@ def main(argv=None):
     ap.add_argument("--config", default=DEFAULT_CONFIG, choices=sorted(W.CONFIGS))
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--deferred", action="store_true",
+                    help="launch each round's copier after its producer (for profilers that "
+                         "serialise kernels)")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--latency-rounds", type=int, default=20)
+    ap.add_argument("--isolated-rounds", type=int, default=20)
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3

@@ -52,7 +52,8 @@ class dtt_plan_opts(C.Structure):
                 ("ctas_per_sm", C.c_uint32), ("copier_threads", C.c_uint32),
                 ("piece_bytes", C.c_uint32), ("timestamps", C.c_uint32),
                 ("initial_round", C.c_uint32), ("max_polls", C.c_uint64),
-                ("max_regions", C.c_uint64)]
+                ("max_regions", C.c_uint64), ("deferred_copier", C.c_uint32),
+                ("stages", C.c_uint32)]
 
 
 class dtt_handle(C.Structure):
@@ -110,6 +111,7 @@ _SIGS = {
                                   _P, C.POINTER(_P)]),
     "dtt_plan_start": (C.c_int, [_P, _P, C.POINTER(dtt_handle)]),
     "dtt_plan_handle": (C.c_int, [_P, _u32, C.POINTER(dtt_handle)]),
+    "dtt_plan_launch_copier": (C.c_int, [_P]),
     "dtt_plan_wait": (C.c_int, [_P, C.POINTER(dtt_report)]),
     "dtt_plan_next_round": (C.c_int, [_P]),
     "dtt_plan_close": (C.c_int, [_P]),
@@ -310,6 +312,9 @@ class Plan:
     def start(self, producer_stream=None):
         _check(lib().dtt_plan_start(self._h, _stream(producer_stream), self.handles))
         return self.handles
+
+    def launch_copier(self) -> None:
+        _check(lib().dtt_plan_launch_copier(self._h))
 
     def handle(self, rank: int) -> dtt_handle:
         h = dtt_handle()

@@ -156,6 +156,156 @@ __global__ void __launch_bounds__(1024) copier_kernel(const __grid_constant__ Co
     }
 }
 
+// ---- bulk-copy (TMA) path ----------------------------------------------------------------------
+// One thread per CTA drives the copy engine of its SM: bulk loads (cp.async.bulk, completing on
+// an mbarrier) fill a ring of shared-memory stages, and each stage is written back to every peer
+// with bulk stores.  Loads of later pieces overlap the stores of earlier ones.  The SM's other
+// resources stay free for the producer.  Every piece fits one stage (the plan cuts them so) and
+// is 16-byte aligned.
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+// Bounded wait for the phase with the given parity.  Returns false when the polls run out.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+    for (uint32_t i = 0; i < (1u << 26); ++i) {
+        uint32_t done;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(done) : "r"(bar), "r"(parity) : "memory");
+        if (done) return true;
+    }
+    return false;
+}
+
+__device__ __forceinline__ void bulk_load(uint32_t dst_smem, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(dst_smem), "l"(src), "r"(bytes), "r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void bulk_store(void* dst, uint32_t src_smem, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
+                 ::"l"(dst), "r"(src_smem), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+__global__ void __launch_bounds__(32) copier_bulk_kernel(const __grid_constant__ CopierParams p) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    if (threadIdx.x != 0) return;
+    const uint32_t b = blockIdx.x;
+    uint32_t s = 0;
+    while (s + 1 < p.P && b >= p.cta_base[s + 1]) ++s;
+    if (b < p.cta_base[s] || b >= p.cta_base[s + 1]) return;
+    const uint32_t G = p.cta_base[s + 1] - p.cta_base[s];
+    const uint32_t j = b - p.cta_base[s];
+    const uint32_t S = p.stages;
+    uint8_t* stage0 = smem;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)S * p.stage_bytes);
+    for (uint32_t i = 0; i < S; ++i) mbar_init(smem_addr(bars + i), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+
+    const char* src_base = p.bufs[s];
+    const uint64_t* table_s = p.gates + (uint64_t)s * p.n_global * DTT_GATE_WORDS;
+    uint64_t it0 = 0;          // items issued so far by this CTA (stage and phase bookkeeping)
+    uint64_t loads_hi = 0;     // loads issued: indices [0, loads_hi)
+    uint64_t waited_hi = 0;    // loads whose stage has been seen full: indices [0, waited_hi)
+    bool failed = false;
+
+    auto load = [&](const PieceDesc& pc, uint64_t idx) {
+        const uint32_t st = (uint32_t)(idx % S);
+        const uint32_t bar = smem_addr(bars + st);
+        const uint32_t dst = smem_addr(stage0 + (size_t)st * p.stage_bytes);
+        mbar_expect_tx(bar, pc.row_bytes * pc.rows);
+        for (uint32_t r = 0; r < pc.rows; ++r)
+            bulk_load(dst + r * pc.row_bytes, src_base + pc.off + (uint64_t)r * pc.pitch, pc.row_bytes, bar);
+        loads_hi = idx + 1;
+    };
+    auto store = [&](const PieceDesc& pc, uint64_t idx) {
+        const uint32_t st = (uint32_t)(idx % S);
+        const uint32_t src = smem_addr(stage0 + (size_t)st * p.stage_bytes);
+        for (uint32_t q = 0; q < p.P; ++q) {
+            if (q == s) continue;
+            char* dst = p.bufs[q] + pc.off;
+            for (uint32_t r = 0; r < pc.rows; ++r)
+                bulk_store(dst + (uint64_t)r * pc.pitch, src + r * pc.row_bytes, pc.row_bytes);
+        }
+        bulk_commit();
+    };
+
+    for (uint32_t k = 0; k < p.n_chunks[s] && !failed; ++k) {
+        const uint32_t c = p.first_chunk[s] + k;
+        const ChunkDesc cd = p.chunks[c];
+        if (!poll_gate(table_s + (uint64_t)c * DTT_GATE_WORDS + DTT_GATE_READY, p.round, p.max_polls)) {
+            atomicAdd(&p.status->copier_timeouts, 1u);
+            atomicMin(&p.status->timeout_chunk, c);
+            break;
+        }
+        fence_proxy_async_global();   // the producer's writes, acquired above, precede the bulk loads
+        const uint32_t i0 = (j + G - cd.rot) % G;
+        if (i0 >= cd.n_pieces) continue;
+        const uint32_t n = (cd.n_pieces - i0 + G - 1) / G;       // my pieces of this chunk
+        const PieceDesc* mine = p.pieces + cd.piece_begin + i0;  // stride G
+        const uint32_t pre = n < S - 1 ? n : S - 1;
+        for (uint32_t t = 0; t < pre; ++t) load(mine[(uint64_t)t * G], it0 + t);
+        for (uint32_t t = 0; t < n; ++t) {
+            const uint64_t idx = it0 + t;
+            if (!mbar_wait(smem_addr(bars + idx % S), (uint32_t)((idx / S) & 1))) {
+                atomicAdd(&p.status->bulk_timeouts, 1u);
+                failed = true;
+                break;
+            }
+            waited_hi = idx + 1;
+            store(mine[(uint64_t)t * G], idx);
+            const uint32_t u = t + S - 1;
+            if (u < n) {
+                if (t >= 1) bulk_wait_read1();    // piece t-1 has left the stage piece u reuses
+                load(mine[(uint64_t)u * G], it0 + u);
+            }
+        }
+        bulk_wait_all();              // every store of this chunk has been written
+        fence_proxy_async_global();   // ... and is ordered before the generic-proxy release below
+        it0 += n;
+        if (failed) break;
+        uint64_t* row = p.gates + ((uint64_t)s * p.n_global + c) * DTT_GATE_WORDS;
+        const uint64_t done = dtt_dev::atom_add_acq_rel(row + DTT_GATE_COPIER, 1) + 1;
+        if (done == (uint64_t)p.round * cd.n_part) {
+            for (uint32_t q = 0; q < p.P; ++q) {
+                if (q == s) continue;
+                uint64_t* prow = p.gates + ((uint64_t)q * p.n_global + c) * DTT_GATE_WORDS;
+                if (p.flags & DTT_HANDLE_TIMESTAMPS)
+                    dtt_dev::st_relaxed(prow + DTT_GATE_T_ARRIVE, dtt_dev::globaltimer());
+                dtt_dev::red_release_add(prow + DTT_GATE_ARRIVAL, 1);
+            }
+            dtt_dev::red_release_add(row + DTT_GATE_COMPLETION, p.P - 1);
+        }
+    }
+    // leave nothing in flight: stores, and (after a failed wait) loads still landing in the ring
+    bulk_wait_all();
+    for (uint64_t idx = waited_hi + (failed ? 1 : 0); idx < loads_hi; ++idx)
+        if (!mbar_wait(smem_addr(bars + idx % S), (uint32_t)((idx / S) & 1))) break;
+}
+
 // Completion check: flags[c] = 0 delivered, 1 short (marks or an arrival missing), 2 extra.
 __global__ void check_kernel(const __grid_constant__ CheckParams p, uint8_t* flags) {
     for (uint32_t c = blockIdx.x * blockDim.x + threadIdx.x; c < p.n_global;
@@ -240,8 +390,12 @@ __global__ void consumer_kernel(const __grid_constant__ CopierParams p, dtt_hand
 
 cudaError_t launch_copier(const CopierParams& p, uint32_t ctas, uint32_t threads, uint32_t method,
                           cudaStream_t s) {
-    (void)method;
-    copier_kernel<<<ctas, threads, 0, s>>>(p);
+    if (method == DTT_COPY_TMA) {
+        const size_t smem = bulk_smem_bytes(p.stage_bytes, p.stages);
+        copier_bulk_kernel<<<ctas, 32, smem, s>>>(p);
+    } else {
+        copier_kernel<<<ctas, threads, 0, s>>>(p);
+    }
     return cudaGetLastError();
 }
 
@@ -272,6 +426,10 @@ cudaError_t launch_consumer(const CopierParams& p, dtt_handle h, char* dst, uint
 
 cudaError_t preload_copier_kernels() {
     cudaError_t e = prepare_kernel(copier_kernel);
+    if (e == cudaSuccess) e = prepare_kernel(copier_bulk_kernel);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(copier_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kBulkSmemMax);
     if (e == cudaSuccess) e = prepare_kernel(check_kernel);
     if (e == cudaSuccess) e = prepare_kernel(force_open_kernel);
     if (e == cudaSuccess) e = prepare_kernel(publish_kernel);

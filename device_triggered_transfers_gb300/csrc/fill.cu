@@ -35,9 +35,14 @@ __device__ __forceinline__ uint32_t fmix32(uint32_t h) {
     return h;
 }
 
-// ((h >> 8) - 2^23) * 2^-23: an exact float in [-1, 1).
+// ((h >> 8) - 2^23) * 2^-23, an exact float in [-1, 1), built from bits: with k = h >> 8 and
+// m its low 23 bits, f = 1 + m 2^-23 and the result is f - 2 when k < 2^23, else f - 1.  Both
+// subtractions are exact, so this equals the integer form without an int-to-float conversion.
 __device__ __forceinline__ float uniform(uint32_t h) {
-    return (float)((int32_t)(h >> 8) - (1 << 23)) * 0x1p-23f;
+    const uint32_t k = h >> 8;
+    const float f = __uint_as_float((k & 0x7FFFFFu) | 0x3F800000u);
+    const float c = __uint_as_float(0x40000000u - (k & 0x800000u));
+    return f - c;
 }
 
 template <int DT> struct Elem;
@@ -94,23 +99,31 @@ __device__ __forceinline__ void write_block(const FillParams& p, char* base, uin
     using E = Elem<DT>;
     constexpr uint32_t VPE = 16 / E::bytes;     // elements per 16-byte vector
     if (ra >= rb || cols == 0) return;
-    const uint64_t nrows = rb - ra;
-    uint64_t nvec = 0;
+    const uint32_t nrows = (uint32_t)(rb - ra);
+    uint32_t nvec = 0;
     if (p.vec) {
-        nvec = cols / VPE;
-        const uint64_t total = nrows * nvec;
-        for (uint64_t v = threadIdx.x; v < total; v += blockDim.x) {
-            const uint64_t i = v / nvec, k = v - i * nvec;
-            const uint64_t row = ra + i, col = c0 + k * VPE;
-            const uint32_t idx = (uint32_t)(row * p.N + col);
-            *reinterpret_cast<uint4*>(base + row * p.pitch + col * E::bytes) = E::pack(salt, idx);
+        // thread t takes vectors t, t + blockDim, ... of the block; (row i, vector k) advances
+        // by a fixed quotient and remainder instead of a division per vector
+        nvec = (uint32_t)(cols / VPE);
+        if (nvec) {
+            const uint32_t total = nrows * nvec;
+            const uint32_t dq = blockDim.x / nvec, dr = blockDim.x % nvec;
+            uint32_t i = threadIdx.x / nvec, k = threadIdx.x % nvec;
+            for (uint32_t v = threadIdx.x; v < total; v += blockDim.x) {
+                const uint64_t row = ra + i, col = c0 + (uint64_t)k * VPE;
+                const uint32_t idx = (uint32_t)(row * p.N + col);
+                *reinterpret_cast<uint4*>(base + row * p.pitch + col * E::bytes) = E::pack(salt, idx);
+                i += dq;
+                k += dr;
+                if (k >= nvec) { k -= nvec; ++i; }
+            }
         }
     }
-    const uint64_t done = nvec * VPE, tail = cols - done;
+    const uint32_t done = nvec * VPE, tail = (uint32_t)cols - done;
     if (tail == 0) return;
-    const uint64_t total = nrows * tail;
-    for (uint64_t v = threadIdx.x; v < total; v += blockDim.x) {
-        const uint64_t i = v / tail, k = v - i * tail;
+    const uint32_t total = nrows * tail;
+    for (uint32_t v = threadIdx.x; v < total; v += blockDim.x) {
+        const uint32_t i = v / tail, k = v - i * tail;
         const uint64_t row = ra + i, col = c0 + done + k;
         E::scalar(base + row * p.pitch + col * E::bytes, salt, (uint32_t)(row * p.N + col));
     }
@@ -148,10 +161,18 @@ __global__ void __launch_bounds__(1024) fill_kernel(const __grid_constant__ Fill
 
 }  // namespace
 
+template <class K>
+static cudaError_t prepare_fill(K kernel) {
+    cudaError_t e = prepare_kernel(kernel);
+    // clusters of up to 16 CTAs (beyond the portable 8) for one-writer chunks
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    return e;
+}
+
 cudaError_t preload_fill_kernels() {
-    cudaError_t e = prepare_kernel(fill_kernel<DTT_BF16>);
-    if (e == cudaSuccess) e = prepare_kernel(fill_kernel<DTT_F32>);
-    if (e == cudaSuccess) e = prepare_kernel(fill_kernel<DTT_U8>);
+    cudaError_t e = prepare_fill(fill_kernel<DTT_BF16>);
+    if (e == cudaSuccess) e = prepare_fill(fill_kernel<DTT_F32>);
+    if (e == cudaSuccess) e = prepare_fill(fill_kernel<DTT_U8>);
     return e;
 }
 
@@ -170,11 +191,13 @@ extern "C" int dtt_fill_producer(void* const* bufs, uint32_t P, const dtt_fill_d
         return fail(DTT_EINVAL, "dtt_fill_producer: bad dtype or mark mode");
     const uint32_t cluster = d->cluster ? d->cluster : 1;
     const uint32_t threads = d->threads ? d->threads : 256;
-    if (cluster > 8 || threads % 32 || threads > 1024)
-        return fail(DTT_EINVAL, "dtt_fill_producer: cluster <= 8, threads a multiple of 32 <= 1024");
+    if (cluster > 16 || threads % 32 || threads > 1024)
+        return fail(DTT_EINVAL, "dtt_fill_producer: cluster <= 16, threads a multiple of 32 <= 1024");
     if ((uint64_t)d->num_programs * cluster > 0x7FFFFFFFull)
         return fail(DTT_EINVAL, "dtt_fill_producer: grid too large");
     const uint32_t eb = d->dtype == DTT_BF16 ? 2 : d->dtype == DTT_F32 ? 4 : 1;
+    if ((uint64_t)d->BM * d->BN >= (1ull << 31))
+        return fail(DTT_EINVAL, "dtt_fill_producer: a BM x BN tile must hold fewer than 2^31 elements");
     if (d->M > 1 && d->pitch < d->N * eb) return fail(DTT_EINVAL, "dtt_fill_producer: pitch < row bytes");
     const uint64_t span = (d->M - 1) * d->pitch + d->N * eb;
     for (uint32_t r = 0; r < P; ++r)

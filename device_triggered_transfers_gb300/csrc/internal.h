@@ -53,7 +53,7 @@ struct DevStatus {
     uint32_t misuse;            // DTT_DEV_* bits from mark_ready
     uint32_t copier_timeouts;   // copier CTAs that gave up on a gate
     uint32_t timeout_chunk;     // smallest chunk id a copier CTA gave up on
-    uint32_t pad;
+    uint32_t bulk_timeouts;     // bulk-copy waits (mbarrier, bulk groups) that gave up
 };
 
 struct CopierParams {
@@ -70,6 +70,8 @@ struct CopierParams {
     uint32_t round;
     uint32_t flags;
     uint64_t max_polls;
+    uint32_t stage_bytes;       // bulk-copy path: bytes per shared-memory stage (>= a piece)
+    uint32_t stages;            // bulk-copy path: stages in the ring
 };
 
 struct CheckParams {
@@ -80,7 +82,14 @@ struct CheckParams {
     uint32_t round;
 };
 
-// Kernel launchers (copier.cu, check.cu).
+// Bulk-copy copier: a ring of `stages` shared-memory stages of stage_bytes, then one mbarrier
+// per stage; at most kBulkSmemMax bytes of dynamic shared memory per CTA.
+constexpr size_t kBulkSmemMax = 200 * 1024;
+inline size_t bulk_smem_bytes(uint32_t stage_bytes, uint32_t stages) {
+    return (size_t)stage_bytes * stages + 8 * (size_t)stages;
+}
+
+// Kernel launchers (copier.cu).
 cudaError_t launch_copier(const CopierParams& p, uint32_t ctas, uint32_t threads, uint32_t method,
                           cudaStream_t s);
 // Completion check: flags[c] = 0 delivered, 1 short, 2 extra marks.

@@ -48,6 +48,7 @@ struct dtt_plan {
 
     int state = DTT_PLAN_PREPARED;
     uint32_t round = 1;
+    bool copier_launched = false;   // this round's copier is on the copy stream
 };
 
 namespace {
@@ -153,6 +154,8 @@ CopierParams copier_params(const dtt_plan* p) {
     cp.round = p->round;
     cp.flags = p->opts.timestamps ? DTT_HANDLE_TIMESTAMPS : 0u;
     cp.max_polls = p->opts.max_polls;
+    cp.stage_bytes = p->opts.piece_bytes;
+    cp.stages = p->opts.stages;
     return cp;
 }
 
@@ -276,6 +279,11 @@ int build_plan(dtt_plan* p, const dtt_schedule* const* scheds) {
         }
     }
     if (p->pieces.size() > 0xFFFFFFFFull) return fail(DTT_ECAPACITY, "plan: too many copier pieces");
+    if (p->opts.method == DTT_COPY_TMA)
+        for (const PieceDesc& pc : p->pieces)
+            if (pc.rows && !pc.vec)
+                return fail(DTT_EINVAL, "plan: the bulk-copy path needs 16-byte aligned regions "
+                                        "(offset, row bytes and pitch); use DTT_COPY_VEC16");
     return DTT_OK;
 }
 
@@ -373,10 +381,16 @@ int dtt_plan_create(void* const* bufs, uint64_t buf_bytes, uint32_t P,
     if (o.piece_bytes == 0) o.piece_bytes = 65536;
     if (o.copier_threads == 0) o.copier_threads = 512;
     if (o.ctas_per_sm == 0) o.ctas_per_sm = 1;
+    if (o.stages == 0) o.stages = 8;
     if (o.piece_bytes % 16 || o.copier_threads % 32 || o.copier_threads > 1024 ||
-        o.method != DTT_COPY_VEC16) {
+        (o.method != DTT_COPY_VEC16 && o.method != DTT_COPY_TMA)) {
         delete p;
         return fail(DTT_EINVAL, "dtt_plan_create: bad options (piece_bytes %% 16, threads %% 32 <= 1024, method)");
+    }
+    if (o.method == DTT_COPY_TMA && bulk_smem_bytes(o.piece_bytes, o.stages) > kBulkSmemMax) {
+        delete p;
+        return fail(DTT_EINVAL, "dtt_plan_create: stages x piece_bytes exceeds %zu bytes of shared memory",
+                    kBulkSmemMax);
     }
     p->P = P;
     p->buf_bytes = buf_bytes;
@@ -442,9 +456,11 @@ int dtt_plan_start(dtt_plan* p, cudaStream_t producer_stream, dtt_handle* handle
     DevStatus st{};
     st.timeout_chunk = 0xFFFFFFFFu;
     DTT_CUDA_TRY(cudaMemcpyAsync(p->d_status, &st, sizeof(st), cudaMemcpyHostToDevice, p->copy_stream));
-    if (p->n_global) {
+    p->copier_launched = false;
+    if (p->n_global && !p->opts.deferred_copier) {
         const CopierParams cp = copier_params(p);
         DTT_CUDA_TRY(launch_copier(cp, p->copier_ctas, p->copier_threads, p->opts.method, p->copy_stream));
+        p->copier_launched = true;
     }
     p->producer_stream = producer_stream;
     if (handles)
@@ -459,9 +475,23 @@ int dtt_plan_handle(const dtt_plan* p, uint32_t rank, dtt_handle* out) {
     return DTT_OK;
 }
 
+int dtt_plan_launch_copier(dtt_plan* p) {
+    if (!p) return fail(DTT_EINVAL, "dtt_plan_launch_copier: NULL plan");
+    if (p->state != DTT_PLAN_RUNNING) return fail(DTT_ESTATE, "dtt_plan_launch_copier: plan is not RUNNING");
+    if (p->copier_launched || !p->n_global) return DTT_OK;
+    DTT_CUDA_TRY(cudaEventRecord(p->ev_producer, p->producer_stream));
+    DTT_CUDA_TRY(cudaStreamWaitEvent(p->copy_stream, p->ev_producer, 0));
+    const CopierParams cp = copier_params(p);
+    DTT_CUDA_TRY(launch_copier(cp, p->copier_ctas, p->copier_threads, p->opts.method, p->copy_stream));
+    p->copier_launched = true;
+    return DTT_OK;
+}
+
 int dtt_plan_wait(dtt_plan* p, dtt_report* report) {
     if (!p) return fail(DTT_EINVAL, "dtt_plan_wait: NULL plan");
     if (p->state != DTT_PLAN_RUNNING) return fail(DTT_ESTATE, "dtt_plan_wait: plan is not RUNNING (state %d)", p->state);
+    const int lc = dtt_plan_launch_copier(p);    // deferred plans: the copier runs now
+    if (lc != DTT_OK) return lc;
     DTT_CUDA_TRY(cudaEventRecord(p->ev_producer, p->producer_stream));
     DTT_CUDA_TRY(cudaStreamWaitEvent(p->copy_stream, p->ev_producer, 0));
     CheckParams ck{};
@@ -525,6 +555,11 @@ int dtt_plan_close(dtt_plan* p) {
             rc = fail(DTT_ECUDA, "dtt_plan_close: producer stream failed");
         if (p->n_global && launch_force_open(p->d_gates, p->d_chunks, p->n_global, p->round, p->aux_stream) != cudaSuccess)
             rc = fail(DTT_ECUDA, "dtt_plan_close: force-open launch failed");
+        if (!p->copier_launched && p->n_global) {     // deferred: send the chunks now
+            if (cudaStreamSynchronize(p->aux_stream) != cudaSuccess ||
+                launch_copier(copier_params(p), p->copier_ctas, p->copier_threads, p->opts.method, p->copy_stream) != cudaSuccess)
+                rc = fail(DTT_ECUDA, "dtt_plan_close: copier launch failed");
+        }
     }
     if (p->aux_stream && cudaStreamSynchronize(p->aux_stream) != cudaSuccess) rc = fail(DTT_ECUDA, "dtt_plan_close: aux stream failed");
     if (p->copy_stream && cudaStreamSynchronize(p->copy_stream) != cudaSuccess) rc = fail(DTT_ECUDA, "dtt_plan_close: copy stream failed");

@@ -179,6 +179,11 @@ typedef struct dtt_plan_opts {
                                 initial_round - 1 rounds had completed (round-limit tests) */
     uint64_t max_polls;      /* copier polls of one gate before it gives up; 0 = 2^22 */
     uint64_t max_regions;    /* capacity: regions in the plan; 0 = unlimited */
+    uint32_t deferred_copier;/* 1: start() does not launch the copier; dtt_plan_launch_copier
+                                or wait() launches it after the work queued on the producer
+                                stream (no overlap; for profilers that serialise kernels) */
+    uint32_t stages;         /* DTT_COPY_TMA: shared-memory stages per copier CTA, each
+                                piece_bytes long (stages * piece_bytes <= 200 KiB); 0 = 8 */
 } dtt_plan_opts;
 
 void dtt_plan_opts_default(dtt_plan_opts* opts);
@@ -253,6 +258,11 @@ int dtt_plan_create(void* const* bufs, uint64_t buf_bytes, uint32_t P,
  * are correct but wait for earlier ones ("Triggered Plans", The kernel author's contract,
  * item 1).  Errors: DTT_ESTATE (not PREPARED), DTT_EINVAL, DTT_ECUDA. */
 int dtt_plan_start(dtt_plan* plan, cudaStream_t producer_stream, dtt_handle* handles);
+
+/* Deferred plans (opts.deferred_copier = 1): launch this round's copier now on the copy
+ * stream, ordered after the work queued so far on the producer stream.  A no-op when the copier
+ * is already running.  Errors: DTT_ESTATE (not RUNNING), DTT_ECUDA. */
+int dtt_plan_launch_copier(dtt_plan* plan);
 
 /* The handle of one rank for the current round.  Errors: DTT_EINVAL. */
 int dtt_plan_handle(const dtt_plan* plan, uint32_t rank, dtt_handle* out);
@@ -329,7 +339,7 @@ typedef struct dtt_fill_desc {
     uint32_t tiles_per_chunk;
     dtt_order order;
     uint32_t mark_mode;
-    uint32_t cluster;        /* 1..8 CTAs per program */
+    uint32_t cluster;        /* 1..16 CTAs per program (above 8 needs non-portable clusters) */
     uint32_t rank_mask;
     uint32_t threads;        /* threads per CTA; 0 = 256 */
 } dtt_fill_desc;

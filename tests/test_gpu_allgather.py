@@ -68,6 +68,18 @@ SMALL = {
                               {"opts": dict(piece_bytes=4096, copier_ctas=7, copier_threads=128)}),
     "many_ctas": (W.small(W.C2, M=32, N=256, num_chunks=2),
                   {"opts": dict(copier_ctas=600, copier_threads=64)}),
+    # the bulk-copy (TMA) copier: 1D pieces, per-row 2D pieces, a broadcast, few stages
+    "bulk_chunks_ragged": (W.small(W.C2, M=70, N=256, num_chunks=8),
+                           {"opts": dict(method=1, piece_bytes=16384)}),
+    "bulk_tiles_grouped": (W.Workload("tb", P=3, M=300, N=200, dtype=W.BF16, kind="tile_chunks",
+                                      rounds=3, seed=11, BM=64, BN=48, num_programs=5,
+                                      tiles_per_chunk=5, group_m=2),
+                           {"opts": dict(method=1, piece_bytes=8192, stages=4)}),
+    "bulk_whole_f32": (W.small(W.C4A, M=64, N=64, rounds=3),
+                       {"opts": dict(method=1, piece_bytes=4096, stages=2, copier_ctas=5)}),
+    "bulk_bcast_u8": (W.Workload("bb", P=4, M=64, N=4096, dtype=W.U8, kind="whole", rounds=2,
+                                 seed=12, num_programs=8, broadcast=True),
+                      {"opts": dict(method=1, piece_bytes=32768, stages=6)}),
 }
 
 
@@ -140,3 +152,16 @@ def test_broadcast_split_into_1gib_copies():
     regs, writers = s[0].chunk(0)
     assert [r[1] for r in regs] == [1 << 30, 1 << 30, 1 << 29]
     assert all(x.n_chunks == 0 for x in s[1:])
+
+
+def test_parity_c2_full_bulk_copier():
+    launch = dict(runner.bench_launch(W.C2))
+    launch["opts"] = D.dtt_plan_opts_default(method=D.COPY_TMA, piece_bytes=16384, stages=8)
+    _run_sampled(W.C2, 3, 1 << 15, launch)
+
+
+def test_bulk_copier_rejects_unaligned_regions():
+    w = SMALL["tiles_unaligned"][0]
+    with pytest.raises(D.DttError) as e:
+        runner.make(w, opts=D.dtt_plan_opts_default(method=D.COPY_TMA, piece_bytes=16384))
+    assert e.value.code == D.EINVAL
