@@ -123,6 +123,8 @@ _SIGS = {
     "dtt_fill_producer": (C.c_int, [C.POINTER(_P), _u32, C.POINTER(dtt_fill_desc),
                                     C.POINTER(dtt_handle), _P]),
     "dtt_publish": (C.c_int, [C.POINTER(dtt_handle), _u32, _u32, _u32, _u32, _P]),
+    "dtt_gemm_producer": (C.c_int, [_P, _P, C.POINTER(_P), _u32, _u32, _u32, _u32, _u64,
+                                    C.POINTER(_u64), _u32, C.POINTER(dtt_handle), _P, _P]),
     "dtt_consumer_gather": (C.c_int, [_P, _u32, _P, _u64, _P, _u32, _P]),
     "dtt_barrier_handrolled": (C.c_int, [C.POINTER(_P), C.POINTER(_P), _u32, _u32, _u64, _P, _P]),
     "dtt_barrier_create": (C.c_int, [_u32, C.POINTER(_P)]),
@@ -459,3 +461,11 @@ def dtt_barrier_reveal_noalloc(x, data, y, size: int, max_polls: int, status, st
     on the GPU share that array and race; run them on one stream."""
     _check(lib().dtt_barrier_reveal_noalloc(_ptr_array(x), _ptr_array(data), _ptr_array(y),
                                             len(x), size, max_polls, _ptr(status), _stream(stream)))
+
+
+def dtt_gemm_producer(A, Bt, bufs, M: int, N: int, K: int, ldc: int, slice_offs, num_programs: int,
+                      handles, err, stream=None) -> None:
+    """C_r = A_r . B for every rank (tcgen05 GEMM), marking each tile's chunk; see dtt.h."""
+    offs = (C.c_uint64 * len(bufs))(*slice_offs)
+    _check(lib().dtt_gemm_producer(_ptr(A), _ptr(Bt), _ptr_array(bufs), len(bufs), M, N, K, ldc, offs,
+                                   num_programs, handles, _ptr(err), _stream(stream)))

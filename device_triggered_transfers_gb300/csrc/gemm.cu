@@ -1,0 +1,364 @@
+// The GEMM producer: a persistent tcgen05 / TMEM bf16 GEMM that marks each 128 x 128 tile's
+// chunk as soon as the tile is stored ("Triggered Plans", section Model: a tiled producer "such
+// as a GEMM"; program p takes steps p, p + num_programs, ... and marks first_chunk + step /
+// num_programs).  One launch covers every virtual rank: C_r = A_r . B for r = 0..P-1.
+//
+// Per CTA (one per SM, 192 threads), warp-specialised:
+//   warp 4      TMA: loads 128 x 64 bf16 tiles of A_r and of B^T (K-major, 128-byte swizzle)
+//               into a ring of shared-memory stages, completing on mbarriers;
+//   warp 5      MMA: one thread issues tcgen05.mma (M = 128, N = 128, K = 16, fp32
+//               accumulate in TMEM) and commits each stage back to the TMA warp, and each
+//               finished tile to the epilogue;
+//   warps 0-3   epilogue: tcgen05.ld the accumulator (warp w owns TMEM lanes 32w..32w+31 =
+//               tile rows), round to bf16, store to the rank's buffer, then a named barrier
+//               over these 128 threads and one mark.
+// Two TMEM accumulators (2 x 128 columns) let the MMA warp start the next tile while the
+// epilogue drains the previous one.  Every wait is bounded; on a timeout the CTA records an
+// error, lets its copies and MMAs finish (bounded), frees its TMEM and returns.
+#include <cstdint>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "dtt_device.cuh"
+#include "internal.h"
+
+namespace dtt {
+namespace {
+
+constexpr uint32_t BM = 128, BN = 128, BK = 64, UMMA_K = 16;
+constexpr uint32_t STAGES = 6;
+constexpr uint32_t A_STAGE = BM * BK * 2;            // 16 KiB
+constexpr uint32_t B_STAGE = BN * BK * 2;            // 16 KiB
+constexpr uint32_t ACC_BUFS = 2;
+constexpr uint32_t TMEM_COLS = ACC_BUFS * BN;        // 256 fp32 columns
+constexpr uint32_t EPI_THREADS = 128;
+constexpr uint32_t THREADS = EPI_THREADS + 64;       // + TMA warp + MMA warp
+constexpr uint32_t TMA_WARP = 4, MMA_WARP = 5;
+constexpr uint32_t SMEM_BYTES = 1024 /* alignment slack */ + STAGES * (A_STAGE + B_STAGE) + 256;
+constexpr uint32_t WAIT_LIMIT = 1u << 26;
+
+// Instruction descriptor (kind::f16): D fp32, A and B bf16, both K-major, N = 128, M = 128.
+constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) | ((BN >> 3) << 17) | ((BM >> 4) << 24);
+
+struct GemmParams {
+    CUtensorMap tmA;     // A, all ranks stacked: [P*M rows, K] bf16, box 64 x 128
+    CUtensorMap tmB;     // B^T: [N rows, K] bf16, box 64 x 128
+    char* bufs[DTT_MAX_RANKS];
+    dtt_handle h[DTT_MAX_RANKS];
+    uint64_t slice_off[DTT_MAX_RANKS];
+    uint64_t ldc;
+    uint32_t P, M, N, K, NP;
+    uint32_t* err;
+};
+
+__device__ __forceinline__ uint32_t saddr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void bar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void bar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void bar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+// Bounded wait for the phase of the given parity; false when the limit ran out or another role
+// already reported an error.
+__device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t parity, volatile uint32_t* abort) {
+    for (uint32_t i = 0; i < WAIT_LIMIT; ++i) {
+        uint32_t done;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(done) : "r"(bar), "r"(parity) : "memory");
+        if (done) return true;
+        if ((i & 255) == 255 && *abort) return false;
+    }
+    return false;
+}
+
+// AND of v over the 128 epilogue threads (named barrier 1), the same result in every thread.
+__device__ __forceinline__ bool epi_all(bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, 1, %2, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r) : "r"((uint32_t)v), "n"(EPI_THREADS) : "memory");
+    return r != 0;
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int32_t x, int32_t y,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3}], [%4];"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar) : "memory");
+}
+
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((addr & 0x3FFFFu) >> 4);          // start address
+    d |= (uint64_t)1 << 16;                           // leading byte offset (unused here)
+    d |= (uint64_t)(1024u >> 4) << 32;                // stride byte offset
+    d |= (uint64_t)1 << 46;                           // descriptor version
+    d |= (uint64_t)2 << 61;                           // 128-byte swizzle
+    return d;
+}
+
+__device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "l"(a), "l"(b), "r"(IDESC), "r"(accumulate) : "memory");
+}
+
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                 ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// 32 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+          "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
+          "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]),
+          "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]),
+          "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(uint32_t lo, uint32_t hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(__uint_as_float(hi)), "f"(__uint_as_float(lo)));
+    return r;
+}
+
+__global__ void __launch_bounds__(THREADS, 1) gemm_producer_kernel(const __grid_constant__ GemmParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sA = smem;
+    uint8_t* sB = smem + STAGES * A_STAGE;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sB + STAGES * B_STAGE);
+    uint64_t* full = bars;                        // [STAGES]  TMA -> MMA
+    uint64_t* empty = bars + STAGES;              // [STAGES]  MMA -> TMA
+    uint64_t* acc_full = bars + 2 * STAGES;       // [2]       MMA -> epilogue
+    uint64_t* acc_empty = acc_full + ACC_BUFS;    // [2]       epilogue -> MMA
+    uint64_t* drain = acc_empty + ACC_BUFS;       // [1]       MMA teardown
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile uint32_t* abort_flag = tmem_slot + 1;
+
+    const uint32_t warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    if (threadIdx.x == 0) {
+        for (uint32_t i = 0; i < STAGES; ++i) {
+            bar_init(saddr(full + i), 1);
+            bar_init(saddr(empty + i), 1);
+        }
+        for (uint32_t i = 0; i < ACC_BUFS; ++i) {
+            bar_init(saddr(acc_full + i), 1);
+            bar_init(saddr(acc_empty + i), EPI_THREADS);
+        }
+        bar_init(saddr(drain), 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                     ::"r"(saddr(tmem_slot)), "r"(TMEM_COLS) : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    const uint32_t tiles_n = p.N / BN, tiles = (p.M / BM) * tiles_n, kblocks = p.K / BK;
+    auto fail = [&]() {
+        *abort_flag = 1;
+        atomicAdd(p.err, 1u);
+    };
+
+    if (warp == TMA_WARP) {
+        if (lane == 0) {
+            uint32_t stage = 0, phase = 0, issued = 0;
+            bool ok = true;
+            for (uint32_t r = 0; r < p.P && ok; ++r)
+                for (uint32_t s = blockIdx.x; s < tiles && ok; s += p.NP) {
+                    const int32_t row_a = (int32_t)(r * p.M + (s / tiles_n) * BM);
+                    const int32_t row_b = (int32_t)((s % tiles_n) * BN);
+                    for (uint32_t kb = 0; kb < kblocks; ++kb) {
+                        if (!bar_wait(saddr(empty + stage), phase ^ 1, abort_flag)) { fail(); ok = false; break; }
+                        bar_expect_tx(saddr(full + stage), A_STAGE + B_STAGE);
+                        tma_load_2d(saddr(sA + stage * A_STAGE), &p.tmA, (int32_t)(kb * BK), row_a, saddr(full + stage));
+                        tma_load_2d(saddr(sB + stage * B_STAGE), &p.tmB, (int32_t)(kb * BK), row_b, saddr(full + stage));
+                        ++issued;
+                        if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                    }
+                }
+            // the last loads of every stage have landed before the CTA can leave
+            volatile uint32_t never = 0;
+            for (uint32_t i = issued > STAGES ? issued - STAGES : 0; i < issued; ++i)
+                (void)bar_wait(saddr(full + i % STAGES), (i / STAGES) & 1, &never);
+        }
+    } else if (warp == MMA_WARP) {
+        if (lane == 0) {
+            uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+            bool ok = true;
+            for (uint32_t r = 0; r < p.P && ok; ++r)
+                for (uint32_t s = blockIdx.x; s < tiles && ok; s += p.NP) {
+                    if (!bar_wait(saddr(acc_empty + acc), acc_phase ^ 1, abort_flag)) { fail(); ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t d_tmem = tmem_base + acc * BN;
+                    for (uint32_t kb = 0; kb < kblocks; ++kb) {
+                        if (!bar_wait(saddr(full + stage), phase, abort_flag)) { fail(); ok = false; break; }
+                        tc_fence_after();
+                        const uint64_t da = smem_desc(saddr(sA + stage * A_STAGE));
+                        const uint64_t db = smem_desc(saddr(sB + stage * B_STAGE));
+#pragma unroll
+                        for (uint32_t k = 0; k < BK / UMMA_K; ++k)
+                            umma(d_tmem, da + 2 * k, db + 2 * k, (kb | k) != 0);
+                        umma_commit(saddr(empty + stage));     // the stage is free once these finish
+                        if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                    }
+                    if (!ok) break;
+                    umma_commit(saddr(acc_full + acc));        // the tile is complete in TMEM
+                    if (++acc == ACC_BUFS) { acc = 0; acc_phase ^= 1; }
+                }
+            // every MMA this thread issued has finished before TMEM is released
+            umma_commit(saddr(drain));
+            volatile uint32_t never = 0;
+            (void)bar_wait(saddr(drain), 0, &never);
+        }
+    } else {
+        // epilogue warps 0..3: thread t of warp w owns row 32w + t of every tile
+        uint32_t acc = 0, acc_phase = 0;
+        const uint32_t row_in_tile = warp * 32 + lane;
+        bool ok = true;
+        for (uint32_t r = 0; r < p.P && ok; ++r)
+            for (uint32_t s = blockIdx.x; s < tiles && ok; s += p.NP) {
+                bool mine = bar_wait(saddr(acc_full + acc), acc_phase, abort_flag);
+                if (!mine) fail();
+                // one decision for all 128 epilogue threads, so none is left at a barrier
+                if (!epi_all(mine && !*abort_flag)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t tm = s / tiles_n, tn = s % tiles_n;
+                char* crow = p.bufs[r] + p.slice_off[r] + (uint64_t)(tm * BM + row_in_tile) * p.ldc +
+                             (uint64_t)tn * BN * 2;
+                const uint32_t taddr = tmem_base + ((warp * 32u) << 16) + acc * BN;
+#pragma unroll 1
+                for (uint32_t g = 0; g < BN / 32; ++g) {
+                    uint32_t v[32];
+                    tmem_ld32(taddr + g * 32, v);
+                    uint4* dst = reinterpret_cast<uint4*>(crow + g * 64);
+#pragma unroll
+                    for (uint32_t q = 0; q < 4; ++q)
+                        dst[q] = make_uint4(pack_bf16x2(v[8 * q + 0], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
+                                            pack_bf16x2(v[8 * q + 4], v[8 * q + 5]), pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
+                }
+                tc_fence_before();
+                bar_arrive(saddr(acc_empty + acc));            // TMEM buffer may be overwritten
+                // the tile's stores by all 128 threads precede one mark
+                asm volatile("bar.sync 1, %0;" ::"n"(EPI_THREADS) : "memory");
+                if (threadIdx.x == 0) dtt_dev::mark_one(p.h[r], p.h[r].first_chunk + s / p.NP);
+                if (++acc == ACC_BUFS) { acc = 0; acc_phase ^= 1; }
+            }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS) : "memory");
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    }
+    return fn;
+}
+
+// A 2D bf16 K-major operand: rows x K elements, box 64 (K) x 128 (rows), 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t K) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {K, rows};
+    const cuuint64_t strides[1] = {K * 2};
+    const cuuint32_t box[2] = {BK, 128};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+cudaError_t preload_gemm_kernels() {
+    cudaError_t e = prepare_kernel(gemm_producer_kernel);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(gemm_producer_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+    return e;
+}
+
+}  // namespace dtt
+
+using namespace dtt;
+
+extern "C" int dtt_gemm_producer(const void* A, const void* Bt, void* const* bufs, uint32_t P, uint32_t M,
+                                 uint32_t N, uint32_t K, uint64_t ldc, const uint64_t* slice_off,
+                                 uint32_t num_programs, const dtt_handle* handles, uint32_t* err,
+                                 cudaStream_t stream) {
+    if (!A || !Bt || !bufs || !slice_off || !handles || !err || P < 1 || P > DTT_MAX_RANKS)
+        return fail(DTT_EINVAL, "dtt_gemm_producer: bad args");
+    if (M == 0 || N == 0 || K == 0 || M % BM || N % BN || K % BK)
+        return fail(DTT_EINVAL, "dtt_gemm_producer: M and N must be multiples of 128 and K of 64");
+    if (num_programs == 0 || ldc < (uint64_t)N * 2 || ldc % 16)
+        return fail(DTT_EINVAL, "dtt_gemm_producer: bad num_programs or ldc");
+    if (reinterpret_cast<uintptr_t>(A) % 16 || reinterpret_cast<uintptr_t>(Bt) % 16)
+        return fail(DTT_EINVAL, "dtt_gemm_producer: operands must be 16-byte aligned");
+    GemmParams gp{};
+    if (!make_map(&gp.tmA, A, (uint64_t)P * M, K) || !make_map(&gp.tmB, Bt, N, K))
+        return fail(DTT_ECUDA, "dtt_gemm_producer: cannot encode the tensor maps");
+    for (uint32_t r = 0; r < P; ++r) {
+        if (!bufs[r] || (reinterpret_cast<uintptr_t>(bufs[r]) + slice_off[r]) % 16)
+            return fail(DTT_EINVAL, "dtt_gemm_producer: rank %u's output is not 16-byte aligned", r);
+        gp.bufs[r] = static_cast<char*>(bufs[r]);
+        gp.h[r] = handles[r];
+        gp.slice_off[r] = slice_off[r];
+    }
+    gp.ldc = ldc;
+    gp.P = P;
+    gp.M = M;
+    gp.N = N;
+    gp.K = K;
+    gp.NP = num_programs;
+    gp.err = err;
+    gemm_producer_kernel<<<num_programs, THREADS, SMEM_BYTES, stream>>>(gp);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(DTT_ECUDA, "dtt_gemm_producer: launch failed: %s", cudaGetErrorString(e));
+    return DTT_OK;
+}

@@ -120,6 +120,7 @@ cudaError_t prepare_kernel(K kernel) {
 cudaError_t preload_copier_kernels();
 cudaError_t preload_fill_kernels();
 cudaError_t preload_barrier_kernels();
+cudaError_t preload_gemm_kernels();
 // dtt_preload() for library-internal callers: once per device, then a no-op.
 int preload_once();
 

@@ -341,6 +341,7 @@ int preload_once() {
     cudaError_t e = preload_copier_kernels();
     if (e == cudaSuccess) e = preload_fill_kernels();
     if (e == cudaSuccess) e = preload_barrier_kernels();
+    if (e == cudaSuccess) e = preload_gemm_kernels();
     if (e != cudaSuccess) return fail(DTT_ECUDA, "dtt_preload: %s", cudaGetErrorString(e));
     g_preloaded |= bit;
     return DTT_OK;

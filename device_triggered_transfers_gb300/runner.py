@@ -100,3 +100,47 @@ def bench_launch(w) -> dict:
     if w.kind == "chunks":
         return {"cluster": 8}
     return {}
+
+
+@dataclass
+class GemmSetup:
+    w: object
+    bufs: List[torch.Tensor]
+    plan: Plan
+    A: torch.Tensor
+    Bt: torch.Tensor
+    err: torch.Tensor
+    producer_stream: torch.cuda.Stream
+    num_programs: int
+
+
+def make_gemm(w, A, Bt, opts=None, num_programs: Optional[int] = None, copy_stream=None) -> GemmSetup:
+    """Plan + operands for the GEMM producer workload: each rank's slice is C_r, [M, N] bf16,
+    tiled 128 x 128 and chunked by the producer's program count.  A [P, M, K] and Bt [N, K] are
+    bf16 tensors (moved to the device here)."""
+    from . import COPY_VEC16
+    NP = num_programs or w.num_programs
+    w = type(w)(**{**w.__dict__, "tiles_per_chunk": NP, "num_programs": NP})
+    bufs = [torch.zeros(w.buf_bytes, dtype=torch.uint8, device="cuda") for _ in range(w.P)]
+    if opts is None:
+        opts = dtt_plan_opts_default()
+    opts.allgather = 1
+    opts.method = COPY_VEC16          # the GEMM's shared memory leaves no room for a bulk ring
+    scheds = schedules_for(w)
+    plan = Plan(bufs, w.buf_bytes, scheds, opts, copy_stream=copy_stream)
+    for s in scheds:
+        s.free()
+    st = GemmSetup(w, bufs, plan, A.to("cuda").contiguous(), Bt.to("cuda").contiguous(),
+                   torch.zeros(1, dtype=torch.int32, device="cuda"), torch.cuda.Stream(), NP)
+    torch.cuda.synchronize()
+    return st
+
+
+def run_gemm_round(st: GemmSetup, raise_on_error: bool = True):
+    from . import dtt_gemm_producer
+    w = st.w
+    handles = st.plan.start(st.producer_stream)
+    dtt_gemm_producer(st.A, st.Bt, st.bufs, w.M, w.N, w.K, w.row_bytes,
+                      [w.slice_offset(r) for r in range(w.P)], st.num_programs, handles, st.err,
+                      st.producer_stream)
+    return st.plan.wait(raise_on_error=raise_on_error)

@@ -349,6 +349,27 @@ typedef struct dtt_fill_desc {
 int dtt_fill_producer(void* const* bufs, uint32_t P, const dtt_fill_desc* desc,
                       const dtt_handle* handles, cudaStream_t stream);
 
+/* GEMM producer (tcgen05 tensor cores, TMEM accumulators, TMA loads): for every rank r,
+ * C_r = A_r . B with bf16 inputs, fp32 accumulation and round-to-nearest-even bf16 output,
+ * stored at bufs[r] + slice_off[r] as M rows of N elements, ldc bytes apart.  This is the
+ * tiled producer "such as a GEMM" of "Triggered Plans" (section Model).
+ *  - A: device bf16 [P][M][K], K contiguous.  Bt: device bf16 [N][K] = B transposed, K
+ *    contiguous.
+ *  - Persistent: num_programs CTAs, each taking 128 x 128 tiles p, p + num_programs, ... of
+ *    rank 0, then of rank 1, and so on, in row-major tile order.  After each tile's stores it
+ *    marks first_chunk + step / num_programs, so its schedule is
+ *    dtt_schedule_tile_chunks(slice_off[r], M, N, 2, ldc, 128, 128, num_programs, row-major).
+ *  - err: device uint32, incremented when a bounded internal wait gives up (0 after a clean
+ *    run).
+ *  - Needs M and N multiples of 128, K a multiple of 64, and 16-byte aligned operands and
+ *    outputs.  One CTA per SM uses ~194 KiB of shared memory, so it runs beside the vector
+ *    copier, not the bulk copier.
+ * Errors: DTT_EINVAL, DTT_ECUDA. */
+int dtt_gemm_producer(const void* A, const void* Bt, void* const* bufs, uint32_t P, uint32_t M,
+                      uint32_t N, uint32_t K, uint64_t ldc, const uint64_t* slice_off,
+                      uint32_t num_programs, const dtt_handle* handles, uint32_t* err,
+                      cudaStream_t stream);
+
 /* A producer that only marks: chunks [first_chunk, first_chunk + n_chunks) (global ids) each
  * get `marks` marks, or their writer count when marks == 0, from one CTA per chunk launched on
  * `stream`, on behalf of the rank that owns each chunk (handles: host array of P from
