@@ -63,6 +63,17 @@ def load_peaks():
         return 6800.0, "fallback"
 
 
+def load_tensor_peak():
+    """Dense bf16 tensor peak: the measured burst figure (a kernel timed on its own)."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), "measured burst"
+    except Exception:
+        return 1900.0, "fallback"
+
+
 # ---- clocks ------------------------------------------------------------------------------------
 class ClockSampler:
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -128,7 +139,7 @@ def oracle_sample_workload(w):
     if w.kind == "tile_chunks":
         rows = min(w.M, 2 * w.BM)
         return W.small(w, M=rows), f"{rows} of {w.M} rows per rank"
-    rows = min(w.M, 256)
+    rows = max(1, min(w.M, 256, (8 << 20) // w.row_bytes))      # at most 8 MiB per slice
     return W.small(w, M=rows, num_programs=min(w.num_programs, rows)), f"{rows} of {w.M} rows"
 
 
@@ -147,6 +158,30 @@ def time_oracle(w, budget_s: float = 10.0, max_rounds: int = 1000):
             break
     dt = time.perf_counter() - t0
     return sw.delivered_bytes_per_round() * n / dt / 1e9, n, dt, what
+
+
+def time_oracle_gemm(w, budget_s: float = 10.0, rows: int = 128):
+    """The oracle on a sample of the GEMM workload: C_r for `rows` rows of every rank (fp64
+    product of the bf16 operands, numpy's multithreaded BLAS), rounded to bf16 and copied to
+    the P-1 peers.  GB/s delivered."""
+    from oracle import gemm as OG
+    from oracle import hashfill as H
+    A, Bt = W.gemm_inputs(w.P, rows, w.N, w.K, w.seed)
+    Bt64 = Bt.double().numpy()
+    A64 = [A[r].double().numpy() for r in range(w.P)]
+    peers = [np.zeros((w.P, rows, w.N), dtype=np.uint16) for _ in range(w.P)]
+    n, t0 = 0, time.perf_counter()
+    while True:
+        for r in range(w.P):
+            c = H.f32_to_bf16_bits(OG.product(A64[r], Bt64).astype(np.float32))
+            for q in range(w.P):
+                peers[q][r] = c
+        n += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return (w.P * rows * w.N * 2 * (w.P - 1) * n / dt / 1e9, n, dt,
+            f"{rows} of {w.M} rows of C per rank")
 
 
 # ---- distributed helpers ---------------------------------------------------------------------------
@@ -222,7 +257,22 @@ def run_ours(args):
     # the copier runs on a stream the bench can put events on
     copy_stream = torch.cuda.Stream(priority=-1)
     opts = D.dtt_plan_opts_default(deferred_copier=1 if args.deferred else 0)
-    st = runner.make(w, opts=opts, copy_stream=copy_stream, **launch)
+    gemm = w.K > 0
+    if gemm:           # the GEMM producer: C_r = A_r . B, marking each tile's chunk
+        A, Bt = W.gemm_inputs(w.P, w.M, w.N, w.K, w.seed)
+        st = runner.make_gemm(w, A, Bt, opts=opts, copy_stream=copy_stream)
+        w_sched = st.w
+        offs = [w.slice_offset(r) for r in range(w.P)]
+
+        def produce(h):
+            D.dtt_gemm_producer(st.A, st.Bt, st.bufs, w.M, w.N, w.K, w.row_bytes, offs,
+                                st.num_programs, h, st.err, prod)
+    else:
+        st = runner.make(w, opts=opts, copy_stream=copy_stream, **launch)
+        w_sched = w
+
+        def produce(h):
+            D.dtt_fill_producer(st.bufs, st.desc, h, prod)
     prod = st.producer_stream
 
     def make_step(plan, deferred):
@@ -235,7 +285,7 @@ def run_ours(args):
                 ev[1].record(copy_stream)
             if ev is not None:
                 ev[2].record(prod)
-            D.dtt_fill_producer(st.bufs, st.desc, h, prod)
+            produce(h)
             if ev is not None:
                 ev[3].record(prod)
             if deferred:      # the copier starts once the producer has finished
@@ -301,7 +351,7 @@ def run_ours(args):
     # e2e: the host-buffer round through the public API: H2D of every rank's slice from pinned
     # memory, the triggered fan-out, D2H of rank 0's gathered buffer
     e2e = None
-    if not args.no_e2e and not w.broadcast:
+    if not args.no_e2e and not w.broadcast and not gemm:
         S = w.slice_bytes
         host_in = [torch.empty(S, dtype=torch.uint8).pin_memory() for _ in range(w.P)]
         for r in range(w.P):
@@ -326,42 +376,60 @@ def run_ours(args):
     iso = None
     if not args.deferred and args.isolated_rounds:
         o2 = D.dtt_plan_opts_default(deferred_copier=1, allgather=0 if w.broadcast else 1)
-        plan2 = D.Plan(st.bufs, w.buf_bytes, runner.schedules_for(w), o2, copy_stream=copy_stream)
+        plan2 = D.Plan(st.bufs, w.buf_bytes, runner.schedules_for(w_sched), o2, copy_stream=copy_stream)
         step2 = make_step(plan2, True)
         for _ in range(3):
             step2()
         _, c2, f2 = timed(step2, args.isolated_rounds)
         plan2.close()
-        iso = {"copier_ms": statistics.mean(c2), "fill_ms": statistics.mean(f2),
+        iso = {"copier_ms": statistics.mean(c2), "producer_ms": statistics.mean(f2),
                "copier_gbs_algorithmic": B_alg / (statistics.mean(c2) / 1e3) / 1e9,
-               "copier_frac_of_measured": B_alg / (statistics.mean(c2) / 1e3) / 1e9 / peak}
+               "copier_frac_of_measured": B_alg / (statistics.mean(c2) / 1e3) / 1e9 / peak,
+               "overlap_ratio": (t_max / K) / (max(statistics.mean(c2), statistics.mean(f2)) / 1e3)}
 
     if rank != 0:
         return 0
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
-        v, n, dt, what = time_oracle(w, budget_s=args.cpu_seconds)
-        cpu = {"value": v, "unit": "GB/s", "cores": 1, "kind": "oracle",
+        if gemm:
+            v, n, dt, what = time_oracle_gemm(w, budget_s=args.cpu_seconds)
+            cores = os.cpu_count()
+        else:
+            v, n, dt, what = time_oracle(w, budget_s=args.cpu_seconds)
+            cores = 1
+        cpu = {"value": v, "unit": "GB/s", "cores": cores, "kind": "oracle",
                "sample": f"{what}; {n} oracle round(s) in {dt:.1f} s"}
     lat_sorted = sorted(lat) or [0]
     mode = "copier launched after the producer (no overlap)" if args.deferred else \
         "copier launched at plan_start, overlapping the producer"
+    copier_roof = {"kernel": "copier_kernel", "bound": "hbm", "achieved": achieved,
+                   "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
+                   "traffic": NCU_TRAFFIC.get(w.name), "algorithmic_bytes_per_launch": B_alg}
+    if gemm:       # the dominant kernel is the tensor-core producer
+        flops = 2.0 * w.P * w.M * w.N * w.K
+        tf_peak, tf_kind = load_tensor_peak()
+        prod_s = statistics.mean(fill_ms) / 1e3
+        roofline = {"kernel": "gemm_producer_kernel", "bound": "tensor",
+                    "achieved": flops / prod_s / 1e12, "peak": tf_peak, "peak_kind": tf_kind,
+                    "unit": "TFLOP/s", "frac": flops / prod_s / 1e12 / tf_peak,
+                    "traffic": NCU_TRAFFIC.get(w.name + ":gemm"), "flops_per_launch": flops}
+    else:
+        roofline = copier_roof
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": t_max / K * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
         "config": {"workload": describe(w, launch), "parallelism": f"replicas{world}",
                    "l2": "inputs larger than L2 (%d MiB of buffers)" % (w.P * w.buf_bytes >> 20),
-                   "step": "plan_start + fill producer + copier + plan_wait + next_round",
+                   "step": "plan_start + %s producer + copier + plan_wait + next_round"
+                           % ("GEMM" if gemm else "fill"),
                    "mode": mode},
         "hbm_frac_end_to_end": {"of_measured": B_alg * units / D_round / t_max / 1e9 / peak,
                                 "of_spec_8000": B_alg * units / D_round / t_max / 1e9 / 8000.0},
-        "roofline": {"kernel": "copier_kernel", "bound": "hbm", "achieved": achieved,
-                     "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": NCU_TRAFFIC.get(w.name),
-                     "algorithmic_bytes_per_launch": B_alg},
+        "roofline": roofline,
+        "copier_roofline": copier_roof if gemm else None,
         "kernels_ms": {"copier_mean": statistics.mean(copier_ms),
-                       "fill_mean": statistics.mean(fill_ms)},
+                       "producer_mean": statistics.mean(fill_ms)},
         "isolated": iso,
         "copier_window": ({"gbs_delivered": D_round / statistics.median(windows) / 1e9,
                            "hbm_frac": B_alg / statistics.median(windows) / 1e9 / peak}
@@ -375,6 +443,51 @@ def run_ours(args):
         "cpu_baseline": cpu,
     }
     print(json.dumps(line))
+    return 0
+
+
+def run_barrier(args):
+    """Latency of the N-rank notify/wait barrier and the builtin reveal (P = 8 virtual ranks,
+    reveal SIZE = 256): one cooperative launch per barrier, CUDA events around K of them."""
+    import torch
+    import device_triggered_transfers_gb300 as D
+    P, size = W.BARRIER_P, W.BARRIER_SIZE
+    sig = [torch.zeros(P, dtype=torch.int32, device="cuda") for _ in range(P)]
+    y = [torch.zeros(P, dtype=torch.int32, device="cuda") for _ in range(P)]
+    status = torch.zeros(P, dtype=torch.int32, device="cuda")
+    x_np = W.barrier_payload(P, size)
+    x = [torch.from_numpy(x_np[r].copy()).cuda() for r in range(P)]
+    data = [torch.zeros(size, dtype=torch.int32, device="cuda") for _ in range(P)]
+    yr = [torch.zeros(size, dtype=torch.int32, device="cuda") for _ in range(P)]
+    b = D.Barrier(P)
+    s = torch.cuda.current_stream()
+    out = {}
+    gen = 0
+    for name in ("handrolled", "reveal"):
+        def one():
+            nonlocal gen
+            if name == "handrolled":
+                gen += 1
+                D.dtt_barrier_handrolled(sig, y, gen, 1 << 24, status, s)
+            else:
+                b.reveal(x, data, yr, size, 1 << 24, status, s)
+        for _ in range(args.warmup):
+            one()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        for _ in range(args.steps):
+            one()
+        e1.record(s)
+        torch.cuda.synchronize()
+        assert int(status.abs().sum()) == 0
+        out[name] = e0.elapsed_time(e1) / args.steps * 1e3
+    b.destroy()
+    print(json.dumps({"metric": "N-rank barrier latency (P=8 virtual ranks)", "unit": "us per barrier",
+                      "higher_is_better": False, "steps": args.steps, "warmup": args.warmup,
+                      "handrolled_us": out["handrolled"], "reveal_us": out["reveal"],
+                      "config": {"workload": "barrier: int32 [8,1] signal windows; reveal [1,256]",
+                                 "launch": "one cooperative launch per barrier, 8 CTAs"}}))
     return 0
 
 
@@ -393,9 +506,13 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--latency-rounds", type=int, default=20)
     ap.add_argument("--isolated-rounds", type=int, default=20)
+    ap.add_argument("--barrier", action="store_true",
+                    help="time the N-rank barrier and the builtin reveal instead")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
+    if args.barrier and args.impl == "ours":
+        return run_barrier(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

@@ -26,20 +26,27 @@
 namespace dtt {
 namespace {
 
-constexpr uint32_t BM = 128, BN = 128, BK = 64, UMMA_K = 16;
-constexpr uint32_t STAGES = 6;
+constexpr uint32_t BM = 128, BN = 128, BK = 64, UMMA_K = 16;   // BM x BN: the marked tile
 constexpr uint32_t A_STAGE = BM * BK * 2;            // 16 KiB
-constexpr uint32_t B_STAGE = BN * BK * 2;            // 16 KiB
 constexpr uint32_t ACC_BUFS = 2;
-constexpr uint32_t TMEM_COLS = ACC_BUFS * BN;        // 256 fp32 columns
 constexpr uint32_t EPI_THREADS = 128;
 constexpr uint32_t THREADS = EPI_THREADS + 64;       // + TMA warp + MMA warp
 constexpr uint32_t TMA_WARP = 4, MMA_WARP = 5;
-constexpr uint32_t SMEM_BYTES = 1024 /* alignment slack */ + STAGES * (A_STAGE + B_STAGE) + 256;
 constexpr uint32_t WAIT_LIMIT = 1u << 26;
 
-// Instruction descriptor (kind::f16): D fp32, A and B bf16, both K-major, N = 128, M = 128.
-constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) | ((BN >> 3) << 17) | ((BM >> 4) << 24);
+// One MMA covers TN columns: TN / 128 adjacent marked tiles of one tile row.  TN = 256 halves the
+// shared-memory traffic per FLOP for A (the 128 x 128 form needs ~112 B/clk of operand reads per
+// SM at full rate, close to what shared memory delivers).
+template <uint32_t TN>
+struct Cfg {
+    static constexpr uint32_t UNIT = TN / BN;                         // tiles per MMA block
+    static constexpr uint32_t STAGES = TN == 256 ? 4 : 6;
+    static constexpr uint32_t B_STAGE = TN * BK * 2;
+    static constexpr uint32_t TMEM_COLS = ACC_BUFS * TN;              // 256 or 512 fp32 columns
+    static constexpr uint32_t SMEM_BYTES = 1024 /* alignment slack */ + STAGES * (A_STAGE + B_STAGE) + 256;
+    // instruction descriptor (kind::f16): D fp32, A and B bf16, both K-major, N = TN, M = 128
+    static constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) | ((TN >> 3) << 17) | ((BM >> 4) << 24);
+};
 
 struct GemmParams {
     CUtensorMap tmA;     // A, all ranks stacked: [P*M rows, K] bf16, box 64 x 128
@@ -116,12 +123,13 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr) {
     return d;
 }
 
-__device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t accumulate) {
+__device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                     uint32_t accumulate) {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-        ::"r"(d_tmem), "l"(a), "l"(b), "r"(IDESC), "r"(accumulate) : "memory");
+        ::"r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(accumulate) : "memory");
 }
 
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
@@ -153,7 +161,13 @@ __device__ __forceinline__ uint32_t pack_bf16x2(uint32_t lo, uint32_t hi) {
     return r;
 }
 
+// Work is cut in units of TN / 128 adjacent tiles of one tile row; program p takes units p,
+// p + NP, ... of rank 0, then of rank 1, and so on.  Tile (tm, tn) is step tm * tiles_n + tn of
+// its rank and, once stored, gets one mark on chunk first_chunk + step / NP.
+template <uint32_t TN>
 __global__ void __launch_bounds__(THREADS, 1) gemm_producer_kernel(const __grid_constant__ GemmParams p) {
+    using G = Cfg<TN>;
+    constexpr uint32_t STAGES = G::STAGES, B_STAGE = G::B_STAGE, TMEM_COLS = G::TMEM_COLS;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sA = smem;
@@ -192,7 +206,8 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_producer_kernel(const __grid_
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
-    const uint32_t tiles_n = p.N / BN, tiles = (p.M / BM) * tiles_n, kblocks = p.K / BK;
+    const uint32_t tiles_n = p.N / BN, units_n = p.N / TN, units = (p.M / BM) * units_n;
+    const uint32_t kblocks = p.K / BK;
     auto fail = [&]() {
         *abort_flag = 1;
         atomicAdd(p.err, 1u);
@@ -203,9 +218,9 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_producer_kernel(const __grid_
             uint32_t stage = 0, phase = 0, issued = 0;
             bool ok = true;
             for (uint32_t r = 0; r < p.P && ok; ++r)
-                for (uint32_t s = blockIdx.x; s < tiles && ok; s += p.NP) {
-                    const int32_t row_a = (int32_t)(r * p.M + (s / tiles_n) * BM);
-                    const int32_t row_b = (int32_t)((s % tiles_n) * BN);
+                for (uint32_t u = blockIdx.x; u < units && ok; u += p.NP) {
+                    const int32_t row_a = (int32_t)(r * p.M + (u / units_n) * BM);
+                    const int32_t row_b = (int32_t)((u % units_n) * TN);
                     for (uint32_t kb = 0; kb < kblocks; ++kb) {
                         if (!bar_wait(saddr(empty + stage), phase ^ 1, abort_flag)) { fail(); ok = false; break; }
                         bar_expect_tx(saddr(full + stage), A_STAGE + B_STAGE);
@@ -225,10 +240,10 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_producer_kernel(const __grid_
             uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
             bool ok = true;
             for (uint32_t r = 0; r < p.P && ok; ++r)
-                for (uint32_t s = blockIdx.x; s < tiles && ok; s += p.NP) {
+                for (uint32_t u = blockIdx.x; u < units && ok; u += p.NP) {
                     if (!bar_wait(saddr(acc_empty + acc), acc_phase ^ 1, abort_flag)) { fail(); ok = false; break; }
                     tc_fence_after();
-                    const uint32_t d_tmem = tmem_base + acc * BN;
+                    const uint32_t d_tmem = tmem_base + acc * TN;
                     for (uint32_t kb = 0; kb < kblocks; ++kb) {
                         if (!bar_wait(saddr(full + stage), phase, abort_flag)) { fail(); ok = false; break; }
                         tc_fence_after();
@@ -236,7 +251,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_producer_kernel(const __grid_
                         const uint64_t db = smem_desc(saddr(sB + stage * B_STAGE));
 #pragma unroll
                         for (uint32_t k = 0; k < BK / UMMA_K; ++k)
-                            umma(d_tmem, da + 2 * k, db + 2 * k, (kb | k) != 0);
+                            umma(d_tmem, da + 2 * k, db + 2 * k, G::IDESC, (kb | k) != 0);
                         umma_commit(saddr(empty + stage));     // the stage is free once these finish
                         if (++stage == STAGES) { stage = 0; phase ^= 1; }
                     }
@@ -255,18 +270,18 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_producer_kernel(const __grid_
         const uint32_t row_in_tile = warp * 32 + lane;
         bool ok = true;
         for (uint32_t r = 0; r < p.P && ok; ++r)
-            for (uint32_t s = blockIdx.x; s < tiles && ok; s += p.NP) {
+            for (uint32_t u = blockIdx.x; u < units && ok; u += p.NP) {
                 bool mine = bar_wait(saddr(acc_full + acc), acc_phase, abort_flag);
                 if (!mine) fail();
                 // one decision for all 128 epilogue threads, so none is left at a barrier
                 if (!epi_all(mine && !*abort_flag)) { ok = false; break; }
                 tc_fence_after();
-                const uint32_t tm = s / tiles_n, tn = s % tiles_n;
+                const uint32_t tm = u / units_n, tn0 = (u % units_n) * G::UNIT;
                 char* crow = p.bufs[r] + p.slice_off[r] + (uint64_t)(tm * BM + row_in_tile) * p.ldc +
-                             (uint64_t)tn * BN * 2;
-                const uint32_t taddr = tmem_base + ((warp * 32u) << 16) + acc * BN;
+                             (uint64_t)tn0 * BN * 2;
+                const uint32_t taddr = tmem_base + ((warp * 32u) << 16) + acc * TN;
 #pragma unroll 1
-                for (uint32_t g = 0; g < BN / 32; ++g) {
+                for (uint32_t g = 0; g < TN / 32; ++g) {
                     uint32_t v[32];
                     tmem_ld32(taddr + g * 32, v);
                     uint4* dst = reinterpret_cast<uint4*>(crow + g * 64);
@@ -277,9 +292,11 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_producer_kernel(const __grid_
                 }
                 tc_fence_before();
                 bar_arrive(saddr(acc_empty + acc));            // TMEM buffer may be overwritten
-                // the tile's stores by all 128 threads precede one mark
+                // the unit's stores by all 128 threads precede one mark per tile
                 asm volatile("bar.sync 1, %0;" ::"n"(EPI_THREADS) : "memory");
-                if (threadIdx.x == 0) dtt_dev::mark_one(p.h[r], p.h[r].first_chunk + s / p.NP);
+                if (threadIdx.x == 0)
+                    for (uint32_t k = 0; k < G::UNIT; ++k)
+                        dtt_dev::mark_one(p.h[r], p.h[r].first_chunk + (tm * tiles_n + tn0 + k) / p.NP);
                 if (++acc == ACC_BUFS) { acc = 0; acc_phase ^= 1; }
             }
     }
@@ -302,13 +319,13 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// A 2D bf16 K-major operand: rows x K elements, box 64 (K) x 128 (rows), 128-byte swizzle.
-bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t K) {
+// A 2D bf16 K-major operand: rows x K elements, box 64 (K) x box_rows, 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t K, uint32_t box_rows) {
     auto fn = encode_fn();
     if (!fn) return false;
     const cuuint64_t dims[2] = {K, rows};
     const cuuint64_t strides[1] = {K * 2};
-    const cuuint32_t box[2] = {BK, 128};
+    const cuuint32_t box[2] = {BK, box_rows};
     const cuuint32_t estr[2] = {1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -317,10 +334,18 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t K) {
 
 }  // namespace
 
-cudaError_t preload_gemm_kernels() {
-    cudaError_t e = prepare_kernel(gemm_producer_kernel);
+template <uint32_t TN>
+static cudaError_t prepare_gemm() {
+    cudaError_t e = prepare_kernel(gemm_producer_kernel<TN>);
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(gemm_producer_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+        e = cudaFuncSetAttribute(gemm_producer_kernel<TN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)Cfg<TN>::SMEM_BYTES);
+    return e;
+}
+
+cudaError_t preload_gemm_kernels() {
+    cudaError_t e = prepare_gemm<128>();
+    if (e == cudaSuccess) e = prepare_gemm<256>();
     return e;
 }
 
@@ -340,8 +365,9 @@ extern "C" int dtt_gemm_producer(const void* A, const void* Bt, void* const* buf
         return fail(DTT_EINVAL, "dtt_gemm_producer: bad num_programs or ldc");
     if (reinterpret_cast<uintptr_t>(A) % 16 || reinterpret_cast<uintptr_t>(Bt) % 16)
         return fail(DTT_EINVAL, "dtt_gemm_producer: operands must be 16-byte aligned");
+    const uint32_t TN = (N % 256 == 0) ? 256 : 128;   // widest MMA block that tiles N
     GemmParams gp{};
-    if (!make_map(&gp.tmA, A, (uint64_t)P * M, K) || !make_map(&gp.tmB, Bt, N, K))
+    if (!make_map(&gp.tmA, A, (uint64_t)P * M, K, BM) || !make_map(&gp.tmB, Bt, N, K, TN))
         return fail(DTT_ECUDA, "dtt_gemm_producer: cannot encode the tensor maps");
     for (uint32_t r = 0; r < P; ++r) {
         if (!bufs[r] || (reinterpret_cast<uintptr_t>(bufs[r]) + slice_off[r]) % 16)
@@ -357,7 +383,10 @@ extern "C" int dtt_gemm_producer(const void* A, const void* Bt, void* const* buf
     gp.K = K;
     gp.NP = num_programs;
     gp.err = err;
-    gemm_producer_kernel<<<num_programs, THREADS, SMEM_BYTES, stream>>>(gp);
+    if (TN == 256)
+        gemm_producer_kernel<256><<<num_programs, THREADS, Cfg<256>::SMEM_BYTES, stream>>>(gp);
+    else
+        gemm_producer_kernel<128><<<num_programs, THREADS, Cfg<128>::SMEM_BYTES, stream>>>(gp);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return fail(DTT_ECUDA, "dtt_gemm_producer: launch failed: %s", cudaGetErrorString(e));
     return DTT_OK;
