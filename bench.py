@@ -32,13 +32,13 @@ import workloads as W  # noqa: E402
 METRIC = "delivered all-gather GB/s and % of HBM peak (1 GB300); gate-to-arrival latency"
 DEFAULT_CONFIG = W.C2.name
 
-# dram__bytes_read.sum + dram__bytes_write.sum per copier launch from one ncu capture of the
-# same workload and launch configuration (profiles/copier_c2_chunks_p4.md); None until taken or
-# once the kernel changes.
-NCU_TRAFFIC = {"c2_chunks_p4": 477961728}
+# dram__bytes_read.sum + dram__bytes_write.sum per launch of the named kernel from one ncu capture
+# of the same workload and launch configuration (the summaries under profiles/); absent until
+# taken, and dropped once the kernel changes.
+NCU_TRAFFIC = {}
 
 
-def describe(w, launch) -> str:
+def describe(w, launch, copier=None) -> str:
     if w.kind == "chunks":
         sched = f"chunks() {w.num_chunks} x {w.M // w.num_chunks} rows, 1 writer each"
     elif w.kind == "whole":
@@ -46,11 +46,22 @@ def describe(w, launch) -> str:
     else:
         sched = (f"tile_chunks {w.BM}x{w.BN}, {w.num_programs} programs, "
                  f"{w.tiles_per_chunk} tiles per chunk, GROUP_M={w.group_m}")
-    cl = launch.get("cluster", 1)
-    prod = f"; producer programs are {cl}-CTA clusters" if cl > 1 else ""
+    cl, grp = launch.get("cluster", 1), launch.get("group", 1)
+    prod = ""
+    if cl > 1:
+        prod = f"; producer: {launch.get('programs') or 'one per chunk'} program(s) per rank of {cl}-CTA clusters"
+    elif grp > 1:
+        prod = (f"; producer: {launch.get('programs') or 'one per chunk'} program(s) per rank, each a "
+                f"group of {grp} CTAs marking each chunk once")
+    cop = ""
+    if copier is not None:
+        cop = ("; copier: bulk copies, %d x %d KiB stages per SM" % (copier["stages"], copier["piece_bytes"] >> 10)
+               if copier["method"] == 1 else
+               "; copier: 16-byte vector copies, %d threads x %d CTA(s) per SM"
+               % (copier["copier_threads"], copier["ctas_per_sm"]))
     kind = "broadcast from rank 0" if w.broadcast else "in-place all-gather"
     return (f"{w.name}: {kind}, P={w.P} virtual ranks, {w.dtype} [{w.buf_rows}, {w.N}] per "
-            f"buffer, {sched}{prod}")
+            f"buffer, {sched}{prod}{cop}")
 
 
 def load_peaks():
@@ -253,10 +264,16 @@ def run_ours(args):
     from device_triggered_transfers_gb300 import runner
 
     w = W.CONFIGS[args.config]
-    launch = runner.bench_launch(w)
+    launch = dict(runner.bench_launch(w))
     # the copier runs on a stream the bench can put events on
     copy_stream = torch.cuda.Stream(priority=-1)
-    opts = D.dtt_plan_opts_default(deferred_copier=1 if args.deferred else 0)
+    # the plan times each copier launch itself (CUDA events recorded in the library), so the
+    # timed loop makes no per-step Python event calls for the copier
+    opts = launch.pop("opts", None) or D.dtt_plan_opts_default()
+    opts.deferred_copier = 1 if args.deferred else 0
+    opts.time_copier = 1
+    copier_method = {"method": opts.method, "piece_bytes": opts.piece_bytes, "stages": opts.stages,
+                     "copier_threads": opts.copier_threads, "ctas_per_sm": opts.ctas_per_sm}
     gemm = w.K > 0
     if gemm:           # the GEMM producer: C_r = A_r . B, marking each tile's chunk
         A, Bt = W.gemm_inputs(w.P, w.M, w.N, w.K, w.seed)
@@ -276,39 +293,36 @@ def run_ours(args):
     prod = st.producer_stream
 
     def make_step(plan, deferred):
-        """One round; ev = 4 events: copier launch bracket (copy stream), fill bracket."""
+        """One round.  ev: two events around the producer launch (producer stream), or None."""
         def step(ev=None):
-            if ev is not None and not deferred:
-                ev[0].record(copy_stream)
             h = plan.start(prod)
-            if ev is not None and not deferred:
-                ev[1].record(copy_stream)
             if ev is not None:
-                ev[2].record(prod)
+                ev[0].record(prod)
             produce(h)
             if ev is not None:
-                ev[3].record(prod)
+                ev[1].record(prod)
             if deferred:      # the copier starts once the producer has finished
-                copy_stream.wait_stream(prod)
-                if ev is not None:
-                    ev[0].record(copy_stream)
                 plan.launch_copier()
-                if ev is not None:
-                    ev[1].record(copy_stream)
             plan.wait()
             plan.next_round()
         return step
 
-    def timed(step, K):
-        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    def timed(plan, step, K, producer_events):
+        """K steps between two events on the producer stream; returns (seconds, copier ms per
+        launch from the plan's own events, producer ms per launch or None)."""
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)] \
+            if producer_events else [None] * K
+        c0 = plan.stats()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(prod)
         for i in range(K):
             step(evs[i])
         e1.record(prod)
         torch.cuda.synchronize()
-        return (e0.elapsed_time(e1) / 1e3, [e[0].elapsed_time(e[1]) for e in evs],
-                [e[2].elapsed_time(e[3]) for e in evs])
+        c1 = plan.stats()
+        cop = (c1[1] - c0[1]) / max(1, c1[2] - c0[2])
+        prod_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs) if producer_events else None
+        return e0.elapsed_time(e1) / 1e3, cop, prod_ms
 
     step = make_step(st.plan, args.deferred)
     for _ in range(args.warmup):
@@ -317,9 +331,10 @@ def run_ours(args):
     K = args.steps
     barrier(world)
     torch.cuda.synchronize()
+    # the GEMM is the dominant kernel of its workload: time its launches inside the timed region
     with ClockSampler(dev) as clocks:
         time.sleep(0.25)
-        elapsed, copier_ms, fill_ms = timed(step, K)
+        elapsed, copier_ms, producer_ms = timed(st.plan, step, K, producer_events=gemm)
         time.sleep(0.25)
     barrier(world)
     D_round = w.delivered_bytes_per_round()
@@ -327,7 +342,7 @@ def run_ours(args):
     t_max, units = aggregate(elapsed, D_round * K, world)
     value = units / t_max / 1e9
     peak, peak_kind = load_peaks()
-    cop_s = statistics.mean(copier_ms) / 1e3
+    cop_s = copier_ms / 1e3
     achieved = B_alg / cop_s / 1e9
 
     # gate-to-arrival latency and the copier window, from the gate timestamps of extra rounds
@@ -375,17 +390,18 @@ def run_ours(args):
     # the same copier and producer one after the other (deferred plan): each kernel alone
     iso = None
     if not args.deferred and args.isolated_rounds:
-        o2 = D.dtt_plan_opts_default(deferred_copier=1, allgather=0 if w.broadcast else 1)
+        o2 = D.dtt_plan_opts_default(deferred_copier=1, allgather=0 if w.broadcast else 1,
+                                     time_copier=1, **copier_method)
         plan2 = D.Plan(st.bufs, w.buf_bytes, runner.schedules_for(w_sched), o2, copy_stream=copy_stream)
         step2 = make_step(plan2, True)
         for _ in range(3):
             step2()
-        _, c2, f2 = timed(step2, args.isolated_rounds)
+        _, c2, f2 = timed(plan2, step2, args.isolated_rounds, producer_events=True)
         plan2.close()
-        iso = {"copier_ms": statistics.mean(c2), "producer_ms": statistics.mean(f2),
-               "copier_gbs_algorithmic": B_alg / (statistics.mean(c2) / 1e3) / 1e9,
-               "copier_frac_of_measured": B_alg / (statistics.mean(c2) / 1e3) / 1e9 / peak,
-               "overlap_ratio": (t_max / K) / (max(statistics.mean(c2), statistics.mean(f2)) / 1e3)}
+        iso = {"copier_ms": c2, "producer_ms": f2,
+               "copier_gbs_algorithmic": B_alg / (c2 / 1e3) / 1e9,
+               "copier_frac_of_measured": B_alg / (c2 / 1e3) / 1e9 / peak,
+               "overlap_ratio": (t_max / K) / (max(c2, f2) / 1e3)}
 
     if rank != 0:
         return 0
@@ -402,24 +418,26 @@ def run_ours(args):
     lat_sorted = sorted(lat) or [0]
     mode = "copier launched after the producer (no overlap)" if args.deferred else \
         "copier launched at plan_start, overlapping the producer"
-    copier_roof = {"kernel": "copier_kernel", "bound": "hbm", "achieved": achieved,
+    kname = "copier_bulk_kernel" if copier_method["method"] == D.COPY_TMA else "copier_kernel"
+    copier_roof = {"kernel": kname, "bound": "hbm", "achieved": achieved,
                    "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
-                   "traffic": NCU_TRAFFIC.get(w.name), "algorithmic_bytes_per_launch": B_alg}
+                   "traffic": NCU_TRAFFIC.get((w.name, kname)), "algorithmic_bytes_per_launch": B_alg}
     if gemm:       # the dominant kernel is the tensor-core producer
         flops = 2.0 * w.P * w.M * w.N * w.K
         tf_peak, tf_kind = load_tensor_peak()
-        prod_s = statistics.mean(fill_ms) / 1e3
+        prod_s = producer_ms / 1e3
         roofline = {"kernel": "gemm_producer_kernel", "bound": "tensor",
                     "achieved": flops / prod_s / 1e12, "peak": tf_peak, "peak_kind": tf_kind,
                     "unit": "TFLOP/s", "frac": flops / prod_s / 1e12 / tf_peak,
-                    "traffic": NCU_TRAFFIC.get(w.name + ":gemm"), "flops_per_launch": flops}
+                    "traffic": NCU_TRAFFIC.get((w.name, "gemm_producer_kernel")),
+                    "flops_per_launch": flops}
     else:
         roofline = copier_roof
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": t_max / K * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
-        "config": {"workload": describe(w, launch), "parallelism": f"replicas{world}",
+        "config": {"workload": describe(w, launch, copier_method), "parallelism": f"replicas{world}",
                    "l2": "inputs larger than L2 (%d MiB of buffers)" % (w.P * w.buf_bytes >> 20),
                    "step": "plan_start + %s producer + copier + plan_wait + next_round"
                            % ("GEMM" if gemm else "fill"),
@@ -428,8 +446,7 @@ def run_ours(args):
                                 "of_spec_8000": B_alg * units / D_round / t_max / 1e9 / 8000.0},
         "roofline": roofline,
         "copier_roofline": copier_roof if gemm else None,
-        "kernels_ms": {"copier_mean": statistics.mean(copier_ms),
-                       "producer_mean": statistics.mean(fill_ms)},
+        "kernels_ms": {"copier_mean": copier_ms, "producer_mean": producer_ms},
         "isolated": iso,
         "copier_window": ({"gbs_delivered": D_round / statistics.median(windows) / 1e9,
                            "hbm_frac": B_alg / statistics.median(windows) / 1e9 / peak}

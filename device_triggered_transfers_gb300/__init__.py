@@ -53,7 +53,7 @@ class dtt_plan_opts(C.Structure):
                 ("piece_bytes", C.c_uint32), ("timestamps", C.c_uint32),
                 ("initial_round", C.c_uint32), ("max_polls", C.c_uint64),
                 ("max_regions", C.c_uint64), ("deferred_copier", C.c_uint32),
-                ("stages", C.c_uint32)]
+                ("stages", C.c_uint32), ("time_copier", C.c_uint32), ("reserved", C.c_uint32)]
 
 
 class dtt_handle(C.Structure):
@@ -85,7 +85,8 @@ class dtt_fill_desc(C.Structure):
                 ("BM", C.c_uint32), ("BN", C.c_uint32), ("num_programs", C.c_uint32),
                 ("tiles_per_chunk", C.c_uint32), ("order", dtt_order),
                 ("mark_mode", C.c_uint32), ("cluster", C.c_uint32), ("rank_mask", C.c_uint32),
-                ("threads", C.c_uint32)]
+                ("threads", C.c_uint32), ("group", C.c_uint32), ("reserved", C.c_uint32),
+                ("group_counters", C.c_void_p)]
 
 
 ORDER_FN = C.CFUNCTYPE(C.c_int, C.c_uint64, C.c_void_p, C.POINTER(C.c_uint32),
@@ -119,6 +120,7 @@ _SIGS = {
     "dtt_plan_round": (C.c_uint32, [_P]),
     "dtt_plan_info": (C.c_int, [_P, C.POINTER(_u32), C.POINTER(_u32), C.POINTER(_u32), C.POINTER(_P)]),
     "dtt_plan_read_gates": (C.c_int, [_P, C.POINTER(_u64), _u64]),
+    "dtt_plan_stats": (C.c_int, [_P, C.POINTER(C.c_double), C.POINTER(C.c_double), C.POINTER(_u64)]),
     "dtt_allgather_host": (C.c_int, [_P, C.POINTER(_P), _P, _u32, _P, C.POINTER(dtt_report)]),
     "dtt_fill_producer": (C.c_int, [C.POINTER(_P), _u32, C.POINTER(dtt_fill_desc),
                                     C.POINTER(dtt_handle), _P]),
@@ -368,6 +370,12 @@ class Plan:
         _check(lib().dtt_plan_info(self._h, C.byref(n), first, cnt, C.byref(gates)))
         return n.value, list(first), list(cnt), gates.value
 
+    def stats(self):
+        """(copier_ms_last, copier_ms_total, rounds_timed) for plans with opts.time_copier."""
+        last, total, n = C.c_double(), C.c_double(), _u64()
+        _check(lib().dtt_plan_stats(self._h, C.byref(last), C.byref(total), C.byref(n)))
+        return last.value, total.value, n.value
+
     def read_gates(self) -> np.ndarray:
         """The P gate tables as a uint64 array [P, n_global, 8]."""
         n = self.info()[0]
@@ -397,8 +405,10 @@ def dtt_plan_create(bufs, buf_bytes, schedules, opts=None, copy_stream=None) -> 
 def fill_desc(dtype: str, seed: int, M: int, N: int, pitch: int, buf_bytes: int,
               slice_offs: Sequence[int], BM: int, BN: int, num_programs: int, tiles_per_chunk: int,
               order_kind=ORDER_ROW_MAJOR, group_m=0, mark_mode=MARK_PER_STEP, cluster=1,
-              rank_mask=None, threads=0) -> dtt_fill_desc:
+              rank_mask=None, threads=0, group=1, group_counters=None) -> dtt_fill_desc:
     d = dtt_fill_desc()
+    d.group = group
+    d.group_counters = _ptr(group_counters) or None
     d.dtype = DTYPE_CODES[dtype]
     d.seed = seed & 0xFFFFFFFF
     d.M, d.N, d.pitch, d.buf_bytes = M, N, pitch, buf_bytes

@@ -122,7 +122,7 @@ __global__ void __launch_bounds__(1024) copier_kernel(const __grid_constant__ Co
                                       p.round, p.max_polls);
             if (!ok) {
                 atomicAdd(&p.status->copier_timeouts, 1u);
-                atomicMin(&p.status->timeout_chunk, c);
+                atomicMax(&p.status->timeout_inv, 0xFFFFFFFFu - c);
             }
             s_go[k & 1] = ok;
         }
@@ -190,16 +190,26 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
     return false;
 }
 
-__device__ __forceinline__ void bulk_load(uint32_t dst_smem, const void* src, uint32_t bytes,
-                                          uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-        ::"r"(dst_smem), "l"(src), "r"(bytes), "r"(bar) : "memory");
+// L2 policy for the copier's own traffic: a source chunk is read once and a peer's copy is not
+// read again by the copier, so both are the first lines L2 gives up -- the chunks the producer
+// is writing right now stay cached until the copier reads them.
+__device__ __forceinline__ uint64_t evict_first_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
 }
 
-__device__ __forceinline__ void bulk_store(void* dst, uint32_t src_smem, uint32_t bytes) {
-    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
-                 ::"l"(dst), "r"(src_smem), "r"(bytes) : "memory");
+__device__ __forceinline__ void bulk_load(uint32_t dst_smem, const void* src, uint32_t bytes,
+                                          uint32_t bar, uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+        "[%0], [%1], %2, [%3], %4;"
+        ::"r"(dst_smem), "l"(src), "r"(bytes), "r"(bar), "l"(pol) : "memory");
+}
+
+__device__ __forceinline__ void bulk_store(void* dst, uint32_t src_smem, uint32_t bytes, uint64_t pol) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group.L2::cache_hint [%0], [%1], %2, %3;"
+                 ::"l"(dst), "r"(src_smem), "r"(bytes), "l"(pol) : "memory");
 }
 
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
@@ -219,6 +229,7 @@ __global__ void __launch_bounds__(32) copier_bulk_kernel(const __grid_constant__
     const uint32_t G = p.cta_base[s + 1] - p.cta_base[s];
     const uint32_t j = b - p.cta_base[s];
     const uint32_t S = p.stages;
+    const uint64_t pol = evict_first_policy();
     uint8_t* stage0 = smem;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)S * p.stage_bytes);
     for (uint32_t i = 0; i < S; ++i) mbar_init(smem_addr(bars + i), 1);
@@ -238,7 +249,7 @@ __global__ void __launch_bounds__(32) copier_bulk_kernel(const __grid_constant__
         const uint32_t dst = smem_addr(stage0 + (size_t)st * p.stage_bytes);
         mbar_expect_tx(bar, pc.row_bytes * pc.rows);
         for (uint32_t r = 0; r < pc.rows; ++r)
-            bulk_load(dst + r * pc.row_bytes, src_base + pc.off + (uint64_t)r * pc.pitch, pc.row_bytes, bar);
+            bulk_load(dst + r * pc.row_bytes, src_base + pc.off + (uint64_t)r * pc.pitch, pc.row_bytes, bar, pol);
         loads_hi = idx + 1;
     };
     auto store = [&](const PieceDesc& pc, uint64_t idx) {
@@ -248,7 +259,7 @@ __global__ void __launch_bounds__(32) copier_bulk_kernel(const __grid_constant__
             if (q == s) continue;
             char* dst = p.bufs[q] + pc.off;
             for (uint32_t r = 0; r < pc.rows; ++r)
-                bulk_store(dst + (uint64_t)r * pc.pitch, src + r * pc.row_bytes, pc.row_bytes);
+                bulk_store(dst + (uint64_t)r * pc.pitch, src + r * pc.row_bytes, pc.row_bytes, pol);
         }
         bulk_commit();
     };
@@ -258,7 +269,7 @@ __global__ void __launch_bounds__(32) copier_bulk_kernel(const __grid_constant__
         const ChunkDesc cd = p.chunks[c];
         if (!poll_gate(table_s + (uint64_t)c * DTT_GATE_WORDS + DTT_GATE_READY, p.round, p.max_polls)) {
             atomicAdd(&p.status->copier_timeouts, 1u);
-            atomicMin(&p.status->timeout_chunk, c);
+            atomicMax(&p.status->timeout_inv, 0xFFFFFFFFu - c);
             break;
         }
         fence_proxy_async_global();   // the producer's writes, acquired above, precede the bulk loads

@@ -23,6 +23,8 @@ struct FillParams {
     uint32_t seed, BM, BN, NP, TPC;
     uint32_t order_kind, group_m, mark_mode, cluster, rank_mask;
     uint32_t vec;    // 16-byte stores allowed (bases, offsets, pitch and BN*elem aligned)
+    uint32_t group;  // CTAs that write one step together and mark it once (counter-based)
+    uint32_t* counters;   // group > 1: one per (rank, step), zero between rounds
 };
 
 // MurmurHash3's 32-bit finaliser (public-domain hash by Austin Appleby).
@@ -35,25 +37,42 @@ __device__ __forceinline__ uint32_t fmix32(uint32_t h) {
     return h;
 }
 
-// ((h >> 8) - 2^23) * 2^-23, an exact float in [-1, 1), built from bits: with k = h >> 8 and
-// m its low 23 bits, f = 1 + m 2^-23 and the result is f - 2 when k < 2^23, else f - 1.  Both
-// subtractions are exact, so this equals the integer form without an int-to-float conversion.
+// fmix32 after its first xor-shift.
+__device__ __forceinline__ uint32_t fmix32_tail(uint32_t h) {
+    h *= 0x85EBCA6Bu;
+    h ^= h >> 13;
+    h *= 0xC2B2AE35u;
+    h ^= h >> 16;
+    return h;
+}
+
+// fmix32((idx + i) ^ salt) for the elements i < 16 of a vector whose first index idx is a
+// multiple of 16 / elem_bytes: idx + i = idx ^ i, and i leaves bits 16 and up alone, so the
+// salt, the index and the first xor-shift fold into one value per vector, B = X ^ (X >> 16)
+// with X = idx ^ salt, and element i hashes to fmix32_tail(B ^ i).
+__device__ __forceinline__ uint32_t vec_base(uint32_t idx, uint32_t salt) {
+    const uint32_t x = idx ^ salt;
+    return x ^ (x >> 16);
+}
+
+// ((h >> 8) - 2^23) * 2^-23, an exact float in [-1, 1), built from bits.  With m the mantissa
+// bits 8..30 of h, f = 1 + m 2^-23 lies in [1, 2); the result is (f - 1.5) + 0.5 when bit 31 of
+// h is set and (f - 1.5) - 0.5 otherwise.  Every step is exact, so this equals the integer form.
 __device__ __forceinline__ float uniform(uint32_t h) {
-    const uint32_t k = h >> 8;
-    const float f = __uint_as_float((k & 0x7FFFFFu) | 0x3F800000u);
-    const float c = __uint_as_float(0x40000000u - (k & 0x800000u));
-    return f - c;
+    const float f = __uint_as_float(((h >> 8) & 0x7FFFFFu) | 0x3F800000u);
+    const float half = __uint_as_float((~h & 0x80000000u) | 0x3F000000u);   // +-0.5
+    return (f - 1.5f) + half;
 }
 
 template <int DT> struct Elem;
 template <> struct Elem<DTT_BF16> {
     static constexpr int bytes = 2;
-    static __device__ __forceinline__ uint4 pack(uint32_t salt, uint32_t idx) {
+    static __device__ __forceinline__ uint4 pack(uint32_t b) {
         uint32_t w[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const __nv_bfloat162 v = __floats2bfloat162_rn(uniform(fmix32((idx + 2 * i) ^ salt)),
-                                                           uniform(fmix32((idx + 2 * i + 1) ^ salt)));
+        for (uint32_t i = 0; i < 4; ++i) {
+            const __nv_bfloat162 v = __floats2bfloat162_rn(uniform(fmix32_tail(b ^ (2 * i))),
+                                                           uniform(fmix32_tail(b ^ (2 * i + 1))));
             w[i] = *reinterpret_cast<const uint32_t*>(&v);
         }
         return make_uint4(w[0], w[1], w[2], w[3]);
@@ -64,11 +83,11 @@ template <> struct Elem<DTT_BF16> {
 };
 template <> struct Elem<DTT_F32> {
     static constexpr int bytes = 4;
-    static __device__ __forceinline__ uint4 pack(uint32_t salt, uint32_t idx) {
-        return make_uint4(__float_as_uint(uniform(fmix32(idx ^ salt))),
-                          __float_as_uint(uniform(fmix32((idx + 1) ^ salt))),
-                          __float_as_uint(uniform(fmix32((idx + 2) ^ salt))),
-                          __float_as_uint(uniform(fmix32((idx + 3) ^ salt))));
+    static __device__ __forceinline__ uint4 pack(uint32_t b) {
+        return make_uint4(__float_as_uint(uniform(fmix32_tail(b))),
+                          __float_as_uint(uniform(fmix32_tail(b ^ 1u))),
+                          __float_as_uint(uniform(fmix32_tail(b ^ 2u))),
+                          __float_as_uint(uniform(fmix32_tail(b ^ 3u))));
     }
     static __device__ __forceinline__ void scalar(char* p, uint32_t salt, uint32_t idx) {
         *reinterpret_cast<float*>(p) = uniform(fmix32(idx ^ salt));
@@ -76,14 +95,14 @@ template <> struct Elem<DTT_F32> {
 };
 template <> struct Elem<DTT_U8> {
     static constexpr int bytes = 1;
-    static __device__ __forceinline__ uint4 pack(uint32_t salt, uint32_t idx) {
+    static __device__ __forceinline__ uint4 pack(uint32_t b) {
         uint32_t w[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            uint32_t x = 0;
-#pragma unroll
-            for (int k = 0; k < 4; ++k) x |= (fmix32((idx + 4 * i + k) ^ salt) & 0xFFu) << (8 * k);
-            w[i] = x;
+        for (uint32_t i = 0; i < 4; ++i) {
+            // low bytes of four hashes into one word
+            const uint32_t lo = __byte_perm(fmix32_tail(b ^ (4 * i)), fmix32_tail(b ^ (4 * i + 1)), 0x0040);
+            const uint32_t hi = __byte_perm(fmix32_tail(b ^ (4 * i + 2)), fmix32_tail(b ^ (4 * i + 3)), 0x0040);
+            w[i] = __byte_perm(lo, hi, 0x5410);
         }
         return make_uint4(w[0], w[1], w[2], w[3]);
     }
@@ -112,7 +131,7 @@ __device__ __forceinline__ void write_block(const FillParams& p, char* base, uin
             for (uint32_t v = threadIdx.x; v < total; v += blockDim.x) {
                 const uint64_t row = ra + i, col = c0 + (uint64_t)k * VPE;
                 const uint32_t idx = (uint32_t)(row * p.N + col);
-                *reinterpret_cast<uint4*>(base + row * p.pitch + col * E::bytes) = E::pack(salt, idx);
+                *reinterpret_cast<uint4*>(base + row * p.pitch + col * E::bytes) = E::pack(vec_base(idx, salt));
                 i += dq;
                 k += dr;
                 if (k >= nvec) { k -= nvec; ++i; }
@@ -136,12 +155,31 @@ __device__ __forceinline__ void mark(const dtt_handle& h, uint32_t chunk, uint32
         dtt_mark_ready(h, chunk);
 }
 
+// A group of `group` CTAs acting as one writer: each CTA orders its stores before an acq_rel
+// add on the step's counter; the CTA whose add completes the group has acquired every other
+// CTA's stores, resets the counter for the next round (the next launch is stream-ordered after
+// this one) and issues the chunk's one mark.
+__device__ __forceinline__ void group_mark(const dtt_handle& h, uint32_t chunk, uint32_t* counter,
+                                           uint32_t group) {
+    __syncthreads();
+    if (dtt_dev::first_thread()) {
+        uint32_t old;
+        asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(counter) : "memory");
+        if (old + 1 == group) {
+            asm volatile("st.relaxed.gpu.global.u32 [%0], 0;" ::"l"(counter) : "memory");
+            dtt_dev::mark_one(h, chunk);
+        }
+    }
+    __syncthreads();
+}
+
 template <int DT>
 __global__ void __launch_bounds__(1024) fill_kernel(const __grid_constant__ FillParams p) {
     const uint32_t r = blockIdx.y;
     if (!((p.rank_mask >> r) & 1u)) return;
     const dtt_handle& h = p.h[r];
-    const uint32_t prog = blockIdx.x / p.cluster, crank = blockIdx.x % p.cluster;
+    const uint32_t team = p.cluster * p.group;          // CTAs of one program (one writer)
+    const uint32_t prog = blockIdx.x / team, member = blockIdx.x % team;
     const uint64_t tiles_m = (p.M + p.BM - 1) / p.BM, tiles_n = (p.N + p.BN - 1) / p.BN;
     const uint64_t T = tiles_m * tiles_n;
     const uint32_t salt = fmix32(p.seed ^ fmix32(r ^ fmix32(h.round)));
@@ -151,10 +189,16 @@ __global__ void __launch_bounds__(1024) fill_kernel(const __grid_constant__ Fill
         tile_of(p.order_kind, p.group_m, step, (uint32_t)tiles_m, (uint32_t)tiles_n, &tm, &tn);
         const uint64_t r0 = (uint64_t)tm * p.BM, c0 = (uint64_t)tn * p.BN;
         const uint64_t rows = min((uint64_t)p.BM, p.M - r0), cols = min((uint64_t)p.BN, p.N - c0);
-        const uint64_t per = (rows + p.cluster - 1) / p.cluster;
-        const uint64_t ra = r0 + min(rows, crank * per), rb = r0 + min(rows, (crank + 1) * per);
+        const uint64_t per = (rows + team - 1) / team;
+        const uint64_t ra = r0 + min(rows, member * per), rb = r0 + min(rows, (member + 1) * per);
         write_block<DT>(p, base, salt, ra, rb, c0, cols);
-        if (p.mark_mode == DTT_MARK_PER_STEP) mark(h, h.first_chunk + (uint32_t)(step / p.TPC), p.cluster);
+        if (p.mark_mode == DTT_MARK_PER_STEP) {
+            const uint32_t chunk = h.first_chunk + (uint32_t)(step / p.TPC);
+            if (p.group > 1)
+                group_mark(h, chunk, p.counters + (uint64_t)r * T + step, p.group);
+            else
+                mark(h, chunk, p.cluster);
+        }
     }
     if (p.mark_mode == DTT_MARK_AT_END) mark(h, h.first_chunk, p.cluster);
 }
@@ -190,10 +234,13 @@ extern "C" int dtt_fill_producer(void* const* bufs, uint32_t P, const dtt_fill_d
     if (d->dtype > DTT_U8 || d->mark_mode > DTT_MARK_AT_END)
         return fail(DTT_EINVAL, "dtt_fill_producer: bad dtype or mark mode");
     const uint32_t cluster = d->cluster ? d->cluster : 1;
+    const uint32_t group = d->group ? d->group : 1;
     const uint32_t threads = d->threads ? d->threads : 256;
     if (cluster > 16 || threads % 32 || threads > 1024)
         return fail(DTT_EINVAL, "dtt_fill_producer: cluster <= 16, threads a multiple of 32 <= 1024");
-    if ((uint64_t)d->num_programs * cluster > 0x7FFFFFFFull)
+    if (group > 1 && (cluster > 1 || d->mark_mode != DTT_MARK_PER_STEP || !d->group_counters))
+        return fail(DTT_EINVAL, "dtt_fill_producer: group writers need cluster 1, per-step marks and counters");
+    if ((uint64_t)d->num_programs * cluster * group > 0x7FFFFFFFull)
         return fail(DTT_EINVAL, "dtt_fill_producer: grid too large");
     const uint32_t eb = d->dtype == DTT_BF16 ? 2 : d->dtype == DTT_F32 ? 4 : 1;
     if ((uint64_t)d->BM * d->BN >= (1ull << 31))
@@ -205,7 +252,9 @@ extern "C" int dtt_fill_producer(void* const* bufs, uint32_t P, const dtt_fill_d
             return fail(DTT_EINVAL, "dtt_fill_producer: rank %u's slice runs past its %llu-byte buffer", r,
                         (unsigned long long)d->buf_bytes);
     FillParams p{};
-    bool vec = (d->pitch % 16 == 0) && ((uint64_t)d->BN * eb % 16 == 0);
+    // 16-byte stores need aligned rows and tile columns; the folded per-vector hash also needs
+    // every vector's first element index (row * N + col) to be a multiple of the vector width
+    bool vec = (d->pitch % 16 == 0) && ((uint64_t)d->BN * eb % 16 == 0) && (d->N % (16 / eb) == 0);
     for (uint32_t r = 0; r < P; ++r) {
         p.bufs[r] = static_cast<char*>(bufs[r]);
         p.h[r] = handles[r];
@@ -226,9 +275,11 @@ extern "C" int dtt_fill_producer(void* const* bufs, uint32_t P, const dtt_fill_d
     p.cluster = cluster;
     p.rank_mask = d->rank_mask;
     p.vec = vec ? 1u : 0u;
+    p.group = group;
+    p.counters = d->group_counters;
 
     cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3(d->num_programs * cluster, P, 1);
+    cfg.gridDim = dim3(d->num_programs * cluster * group, P, 1);
     cfg.blockDim = dim3(threads, 1, 1);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;

@@ -52,7 +52,7 @@ struct ChunkDesc {
 struct DevStatus {
     uint32_t misuse;            // DTT_DEV_* bits from mark_ready
     uint32_t copier_timeouts;   // copier CTAs that gave up on a gate
-    uint32_t timeout_chunk;     // smallest chunk id a copier CTA gave up on
+    uint32_t timeout_inv;       // 0xFFFFFFFF - (smallest chunk id a copier CTA gave up on); 0: none
     uint32_t bulk_timeouts;     // bulk-copy waits (mbarrier, bulk groups) that gave up
 };
 

@@ -49,6 +49,10 @@ struct dtt_plan {
     int state = DTT_PLAN_PREPARED;
     uint32_t round = 1;
     bool copier_launched = false;   // this round's copier is on the copy stream
+
+    cudaEvent_t ev_copier[2] = {};  // opts.time_copier: around each copier launch
+    double copier_ms_total = 0, copier_ms_last = 0;
+    uint64_t rounds_timed = 0;
 };
 
 namespace {
@@ -78,10 +82,12 @@ void free_device(dtt_plan* p) {
     cudaFree(p->d_chunks);
     cudaFree(p->d_pieces);
     cudaFree(p->d_status);
-    cudaFree(p->d_flags);
-    cudaFreeHost(p->h_flags);
     cudaFreeHost(p->h_status);
     if (p->ev_producer) cudaEventDestroy(p->ev_producer);
+    for (cudaEvent_t& e : p->ev_copier) {
+        if (e) cudaEventDestroy(e);
+        e = nullptr;
+    }
     if (p->aux_stream) cudaStreamDestroy(p->aux_stream);
     if (p->own_copy_stream && p->copy_stream) cudaStreamDestroy(p->copy_stream);
     p->d_gates = nullptr;
@@ -120,6 +126,18 @@ void cut_region(const dtt_region& r, uint64_t piece_bytes, bool bases_aligned,
         for (uint64_t i = 0; i < r.rows; i += per)
             push(r.offset + i * r.pitch, r.row_bytes, std::min(per, r.rows - i), r.pitch);
     }
+}
+
+CopierParams copier_params(const dtt_plan* p);
+
+// Launch this round's copier on the copy stream (bracketed by the timing events when asked).
+int launch_round_copier(dtt_plan* p) {
+    if (p->opts.time_copier) DTT_CUDA_TRY(cudaEventRecord(p->ev_copier[0], p->copy_stream));
+    DTT_CUDA_TRY(launch_copier(copier_params(p), p->copier_ctas, p->copier_threads, p->opts.method,
+                               p->copy_stream));
+    if (p->opts.time_copier) DTT_CUDA_TRY(cudaEventRecord(p->ev_copier[1], p->copy_stream));
+    p->copier_launched = true;
+    return DTT_OK;
 }
 
 dtt_handle make_handle(const dtt_plan* p, uint32_t r) {
@@ -306,10 +324,15 @@ int upload(dtt_plan* p) {
     DTT_CUDA_TRY(cudaMalloc(&p->d_writers, std::max<size_t>(1, n * sizeof(uint32_t))));
     DTT_CUDA_TRY(cudaMalloc(&p->d_chunks, std::max<size_t>(1, n * sizeof(ChunkDesc))));
     DTT_CUDA_TRY(cudaMalloc(&p->d_pieces, std::max<size_t>(1, p->pieces.size() * sizeof(PieceDesc))));
-    DTT_CUDA_TRY(cudaMalloc(&p->d_status, sizeof(DevStatus)));
-    DTT_CUDA_TRY(cudaMalloc(&p->d_flags, std::max<size_t>(1, n)));
-    DTT_CUDA_TRY(cudaMallocHost(&p->h_flags, std::max<size_t>(1, n)));
-    DTT_CUDA_TRY(cudaMallocHost(&p->h_status, sizeof(DevStatus)));
+    // status block and check flags side by side, so wait() reads both back with one copy
+    DTT_CUDA_TRY(cudaMalloc(&p->d_status, sizeof(DevStatus) + std::max<size_t>(1, n)));
+    DTT_CUDA_TRY(cudaMallocHost(&p->h_status, sizeof(DevStatus) + std::max<size_t>(1, n)));
+    p->d_flags = reinterpret_cast<uint8_t*>(p->d_status + 1);
+    p->h_flags = reinterpret_cast<uint8_t*>(p->h_status + 1);
+    if (p->opts.time_copier) {
+        DTT_CUDA_TRY(cudaEventCreate(&p->ev_copier[0]));
+        DTT_CUDA_TRY(cudaEventCreate(&p->ev_copier[1]));
+    }
     if (!gates.empty())
         DTT_CUDA_TRY(cudaMemcpy(p->d_gates, gates.data(), gates.size() * sizeof(uint64_t), cudaMemcpyHostToDevice));
     if (n) {
@@ -319,9 +342,7 @@ int upload(dtt_plan* p) {
     if (!p->pieces.empty())
         DTT_CUDA_TRY(cudaMemcpy(p->d_pieces, p->pieces.data(), p->pieces.size() * sizeof(PieceDesc),
                                 cudaMemcpyHostToDevice));
-    DevStatus st{};
-    st.timeout_chunk = 0xFFFFFFFFu;
-    DTT_CUDA_TRY(cudaMemcpy(p->d_status, &st, sizeof(st), cudaMemcpyHostToDevice));
+    DTT_CUDA_TRY(cudaMemset(p->d_status, 0, sizeof(DevStatus)));
     return DTT_OK;
 }
 
@@ -454,14 +475,11 @@ int dtt_plan_start(dtt_plan* p, cudaStream_t producer_stream, dtt_handle* handle
     if (p->state != DTT_PLAN_PREPARED) return fail(DTT_ESTATE, "dtt_plan_start: plan is not PREPARED (state %d)", p->state);
     if (producer_stream == p->copy_stream)
         return fail(DTT_EINVAL, "dtt_plan_start: the producer stream must differ from the copy stream");
-    DevStatus st{};
-    st.timeout_chunk = 0xFFFFFFFFu;
-    DTT_CUDA_TRY(cudaMemcpyAsync(p->d_status, &st, sizeof(st), cudaMemcpyHostToDevice, p->copy_stream));
+    DTT_CUDA_TRY(cudaMemsetAsync(p->d_status, 0, sizeof(DevStatus), p->copy_stream));
     p->copier_launched = false;
     if (p->n_global && !p->opts.deferred_copier) {
-        const CopierParams cp = copier_params(p);
-        DTT_CUDA_TRY(launch_copier(cp, p->copier_ctas, p->copier_threads, p->opts.method, p->copy_stream));
-        p->copier_launched = true;
+        const int rc = launch_round_copier(p);
+        if (rc != DTT_OK) return rc;
     }
     p->producer_stream = producer_stream;
     if (handles)
@@ -482,10 +500,7 @@ int dtt_plan_launch_copier(dtt_plan* p) {
     if (p->copier_launched || !p->n_global) return DTT_OK;
     DTT_CUDA_TRY(cudaEventRecord(p->ev_producer, p->producer_stream));
     DTT_CUDA_TRY(cudaStreamWaitEvent(p->copy_stream, p->ev_producer, 0));
-    const CopierParams cp = copier_params(p);
-    DTT_CUDA_TRY(launch_copier(cp, p->copier_ctas, p->copier_threads, p->opts.method, p->copy_stream));
-    p->copier_launched = true;
-    return DTT_OK;
+    return launch_round_copier(p);
 }
 
 int dtt_plan_wait(dtt_plan* p, dtt_report* report) {
@@ -501,12 +516,18 @@ int dtt_plan_wait(dtt_plan* p, dtt_report* report) {
     ck.P = p->P;
     ck.n_global = p->n_global;
     ck.round = p->round;
-    if (p->n_global) {
-        DTT_CUDA_TRY(launch_check(ck, p->d_flags, p->copy_stream));
-        DTT_CUDA_TRY(cudaMemcpyAsync(p->h_flags, p->d_flags, p->n_global, cudaMemcpyDeviceToHost, p->copy_stream));
-    }
-    DTT_CUDA_TRY(cudaMemcpyAsync(p->h_status, p->d_status, sizeof(DevStatus), cudaMemcpyDeviceToHost, p->copy_stream));
+    if (p->n_global) DTT_CUDA_TRY(launch_check(ck, p->d_flags, p->copy_stream));
+    DTT_CUDA_TRY(cudaMemcpyAsync(p->h_status, p->d_status, sizeof(DevStatus) + p->n_global,
+                                 cudaMemcpyDeviceToHost, p->copy_stream));   // status + flags
     DTT_CUDA_TRY(cudaStreamSynchronize(p->copy_stream));
+    if (p->opts.time_copier && p->copier_launched) {
+        float ms = 0;
+        if (cudaEventElapsedTime(&ms, p->ev_copier[0], p->ev_copier[1]) == cudaSuccess) {
+            p->copier_ms_last = ms;
+            p->copier_ms_total += ms;
+            ++p->rounds_timed;
+        }
+    }
     dtt_report rep{};
     rep.round = p->round;
     rep.copier_timeouts = p->h_status->copier_timeouts;
@@ -568,6 +589,15 @@ int dtt_plan_close(dtt_plan* p) {
     free_device(p);
     delete p;
     return rc;
+}
+
+int dtt_plan_stats(const dtt_plan* p, double* copier_ms_last, double* copier_ms_total,
+                   uint64_t* rounds_timed) {
+    if (!p) return fail(DTT_EINVAL, "dtt_plan_stats: NULL plan");
+    if (copier_ms_last) *copier_ms_last = p->copier_ms_last;
+    if (copier_ms_total) *copier_ms_total = p->copier_ms_total;
+    if (rounds_timed) *rounds_timed = p->rounds_timed;
+    return DTT_OK;
 }
 
 int dtt_plan_state(const dtt_plan* p) { return p ? p->state : DTT_EINVAL; }

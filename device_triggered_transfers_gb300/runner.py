@@ -37,8 +37,22 @@ def schedules_for(w) -> List[Schedule]:
     return out
 
 
-def producer_desc(w, cluster: int = 1, programs: Optional[int] = None, threads: int = 0):
-    """The fill producer that matches ``w``'s schedule (same tiles, same order, same marks)."""
+def producer_steps(w) -> int:
+    """Steps (tiles) of one rank's fill producer for workload ``w``."""
+    if w.kind == "whole":
+        BM = -(-w.M // w.num_programs)
+        return -(-w.M // BM)
+    if w.kind == "chunks":
+        BM = -(-w.M // w.num_chunks)
+        return -(-w.M // BM)
+    return (-(-w.M // w.BM)) * (-(-w.N // w.BN))
+
+
+def producer_desc(w, cluster: int = 1, programs: Optional[int] = None, threads: int = 0,
+                  group: int = 1, counters=None):
+    """The fill producer that matches ``w``'s schedule (same tiles, same order, same marks).
+    group > 1: each program is `group` CTAs that mark each step once (counters: device int32
+    [P * producer_steps(w)], zeroed)."""
     slice_offs = [w.slice_offset(r) for r in range(w.P)]
     mask = 0
     for r in w.senders():
@@ -53,12 +67,13 @@ def producer_desc(w, cluster: int = 1, programs: Optional[int] = None, threads: 
         n = -(-w.M // BM)
         NP = programs or n
         return fill_desc(w.dtype, w.seed, w.M, w.N, w.row_bytes, w.buf_bytes, slice_offs, BM, w.N, NP, 1,
-                         mark_mode=MARK_PER_STEP, cluster=cluster, rank_mask=mask, threads=threads)
+                         mark_mode=MARK_PER_STEP, cluster=cluster, rank_mask=mask, threads=threads,
+                         group=group, group_counters=counters)
     kind = ORDER_GROUPED if w.group_m else ORDER_ROW_MAJOR
     return fill_desc(w.dtype, w.seed, w.M, w.N, w.row_bytes, w.buf_bytes, slice_offs, w.BM, w.BN,
                      programs or w.num_programs, w.tiles_per_chunk, order_kind=kind,
                      group_m=w.group_m, mark_mode=MARK_PER_STEP, cluster=cluster, rank_mask=mask,
-                     threads=threads)
+                     threads=threads, group=group, group_counters=counters)
 
 
 @dataclass
@@ -68,10 +83,11 @@ class Setup:
     plan: Plan
     desc: object
     producer_stream: torch.cuda.Stream
+    counters: Optional[torch.Tensor] = None
 
 
 def make(w, opts=None, cluster: int = 1, programs: Optional[int] = None, threads: int = 0,
-         device: str = "cuda", fill_byte: int = 0, copy_stream=None) -> Setup:
+         device: str = "cuda", fill_byte: int = 0, copy_stream=None, group: int = 1) -> Setup:
     """Allocate the P symmetric buffers (uint8, w.buf_bytes each), build the plan and producer.
     copy_stream: a non-blocking stream for the copier (None: the plan makes its own)."""
     bufs = [torch.full((w.buf_bytes,), fill_byte, dtype=torch.uint8, device=device)
@@ -83,9 +99,13 @@ def make(w, opts=None, cluster: int = 1, programs: Optional[int] = None, threads
     plan = Plan(bufs, w.buf_bytes, scheds, opts, copy_stream=copy_stream)
     for s in scheds:
         s.free()
-    desc = producer_desc(w, cluster=cluster, programs=programs, threads=threads)
+    counters = None
+    if group > 1:
+        counters = torch.zeros(w.P * producer_steps(w), dtype=torch.int32, device=device)
+    desc = producer_desc(w, cluster=cluster, programs=programs, threads=threads, group=group,
+                         counters=counters)
     torch.cuda.synchronize()          # buffers initialised before any round starts
-    return Setup(w, bufs, plan, desc, torch.cuda.Stream())
+    return Setup(w, bufs, plan, desc, torch.cuda.Stream(), counters)
 
 
 def run_round(st: Setup, raise_on_error: bool = True):
@@ -96,9 +116,15 @@ def run_round(st: Setup, raise_on_error: bool = True):
 
 
 def bench_launch(w) -> dict:
-    """The launch configuration the benchmark times for workload ``w`` (tests use it too)."""
+    """The launch configuration the benchmark times for workload ``w`` (tests use it too).
+
+    Chunked workloads: the bulk-copy copier (one warp and a shared-memory ring per SM, so the
+    producer keeps the SM's threads and registers), and one program per rank made of a group of
+    38 CTAs (152 in all, one per SM) that writes the rank's chunks in order and marks each once,
+    so every rank's chunk k opens in wave k and the copier follows the waves."""
     if w.kind == "chunks":
-        return {"cluster": 8}
+        return {"group": 38, "programs": 1, "threads": 256,
+                "opts": dtt_plan_opts_default(method=1, piece_bytes=65536, stages=3)}
     return {}
 
 

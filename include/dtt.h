@@ -184,6 +184,9 @@ typedef struct dtt_plan_opts {
                                 stream (no overlap; for profilers that serialise kernels) */
     uint32_t stages;         /* DTT_COPY_TMA: shared-memory stages per copier CTA, each
                                 piece_bytes long (stages * piece_bytes <= 200 KiB); 0 = 8 */
+    uint32_t time_copier;    /* 1: time every copier launch with CUDA events on the copy
+                                stream (read with dtt_plan_stats) */
+    uint32_t reserved;
 } dtt_plan_opts;
 
 void dtt_plan_opts_default(dtt_plan_opts* opts);
@@ -293,6 +296,13 @@ uint32_t dtt_plan_round(const dtt_plan* plan);
 int dtt_plan_info(const dtt_plan* plan, uint32_t* n_global, uint32_t* first_chunk,
                   uint32_t* n_chunks, uint64_t** gates_device);
 
+/* Copier timing of a plan created with opts.time_copier = 1: the device time of the last
+ * round's copier launch and the sum over all timed rounds (milliseconds, from CUDA events
+ * recorded around each launch on the copy stream), and how many rounds were timed.  Values
+ * are updated by dtt_plan_wait.  Any pointer may be NULL.  Errors: DTT_EINVAL. */
+int dtt_plan_stats(const dtt_plan* plan, double* copier_ms_last, double* copier_ms_total,
+                   uint64_t* rounds_timed);
+
 /* Copy the P gate tables (P * n_global * 8 uint64, rank-major) to host memory `host`
  * (n_words long).  Synchronises the copy stream.  Errors: DTT_EINVAL if n_words is short. */
 int dtt_plan_read_gates(dtt_plan* plan, uint64_t* host, uint64_t n_words);
@@ -321,8 +331,10 @@ enum {
  * apart, starting at byte slice_off[r] of bufs[r].  It is produced as BM x BN tiles by
  * num_programs programs per rank: program p takes steps p, p + num_programs, ... in `order`
  * ("Triggered Plans", section Model, the persistent tiled producer), writes the tile and marks
- * per mark_mode.  A program is one CTA, or a thread-block cluster of `cluster` CTAs that
- * marks once per step after a cluster barrier (one writer).  Element (row, col) of rank r in
+ * per mark_mode.  A program is one CTA; or a thread-block cluster of `cluster` CTAs that
+ * marks once per step after a cluster barrier; or a group of `group` CTAs anywhere on the GPU
+ * whose last CTA to finish a step marks it once, after acquiring the others' stores through an
+ * acq_rel counter.  Either way the program is one writer.  Element (row, col) of rank r in
  * round R holds hash(seed, r, R, row, col): with fmix32 the MurmurHash3 finaliser,
  * salt = fmix32(seed ^ fmix32(r ^ fmix32(R))), h = fmix32((row*N + col) mod 2^32 ^ salt),
  * u = ((h >> 8) - 2^23) * 2^-23 in [-1, 1); bf16 = u rounded to nearest even, f32 = u,
@@ -342,6 +354,12 @@ typedef struct dtt_fill_desc {
     uint32_t cluster;        /* 1..16 CTAs per program (above 8 needs non-portable clusters) */
     uint32_t rank_mask;
     uint32_t threads;        /* threads per CTA; 0 = 256 */
+    uint32_t group;          /* > 1: a program is `group` CTAs that split each step's rows; the
+                                last of them to finish a step issues its one mark (per-step
+                                marks only, cluster must be 1) */
+    uint32_t reserved;
+    uint32_t* group_counters;/* group > 1: device uint32[P * steps per rank], zero before the
+                                first round (the producer leaves them zero after each round) */
 } dtt_fill_desc;
 
 /* Launch the fill producer for all P ranks on `stream` (handles: host array of P, from

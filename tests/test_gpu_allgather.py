@@ -24,8 +24,8 @@ def _gates_match(st, o):
     return g
 
 
-def run_parity(w, rounds, opts=None, cluster=1, programs=None, threads=0):
-    st = runner.make(w, opts=opts, cluster=cluster, programs=programs, threads=threads)
+def run_parity(w, rounds, opts=None, cluster=1, programs=None, threads=0, group=1):
+    st = runner.make(w, opts=opts, cluster=cluster, programs=programs, threads=threads, group=group)
     o = oracle_plan(w)
     try:
         for R in range(1, rounds + 1):
@@ -80,6 +80,14 @@ SMALL = {
     "bulk_bcast_u8": (W.Workload("bb", P=4, M=64, N=4096, dtype=W.U8, kind="whole", rounds=2,
                                  seed=12, num_programs=8, broadcast=True),
                       {"opts": dict(method=1, piece_bytes=32768, stages=6)}),
+    # group writers: several CTAs anywhere on the GPU write a step and mark it once
+    "chunks_group5": (W.small(W.C2, M=256, N=512, num_chunks=4), {"group": 5, "programs": 1}),
+    "chunks_group3_bulk": (W.small(W.C2, M=96, N=1024, num_chunks=6),
+                           {"group": 3, "programs": 2,
+                            "opts": dict(method=1, piece_bytes=16384, stages=4)}),
+    "tiles_group3": (W.Workload("tg", P=3, M=300, N=200, dtype=W.BF16, kind="tile_chunks",
+                                rounds=3, seed=13, BM=64, BN=48, num_programs=5,
+                                tiles_per_chunk=5, group_m=2), {"group": 3}),
 }
 
 
