@@ -186,10 +186,18 @@ def _stream(s) -> int:
 
 
 def _ptr_array(xs) -> C.Array:
+    if isinstance(xs, C.Array):       # already marshalled (see pointer_array)
+        return xs
     arr = (C.c_void_p * max(1, len(xs)))()
     for i, x in enumerate(xs):
         arr[i] = _ptr(x) or None
     return arr
+
+
+def pointer_array(xs) -> C.Array:
+    """The device addresses of ``xs`` (tensors or integers) as the C array the calls taking a
+    buffer list expect; build it once and pass it instead of the list on every round."""
+    return _ptr_array(list(xs))
 
 
 # ---- schedules --------------------------------------------------------------------------------

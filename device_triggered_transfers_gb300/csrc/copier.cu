@@ -318,7 +318,10 @@ __global__ void __launch_bounds__(32) copier_bulk_kernel(const __grid_constant__
 }
 
 // Completion check: flags[c] = 0 delivered, 1 short (marks or an arrival missing), 2 extra.
-__global__ void check_kernel(const __grid_constant__ CheckParams p, uint8_t* flags) {
+// wait()'s completion check, run after the copier and the producer: one flag per chunk, written
+// straight into the mapped host block.  The last CTA to finish copies the status words out,
+// zeroes them for the next round, and only then stores the sequence number the host polls for.
+__global__ void check_kernel(const __grid_constant__ CheckParams p) {
     for (uint32_t c = blockIdx.x * blockDim.x + threadIdx.x; c < p.n_global;
          c += gridDim.x * blockDim.x) {
         const ChunkDesc cd = p.chunks[c];
@@ -337,8 +340,32 @@ __global__ void check_kernel(const __grid_constant__ CheckParams p, uint8_t* fla
                 if (dtt_dev::ld_acquire(prow + DTT_GATE_ARRIVAL) < p.round) f = 1;
             }
         }
-        flags[c] = f;
+        p.host_flags[c] = f;
     }
+    __shared__ uint32_t s_last;
+    __syncthreads();                     // the CTA's flag stores, then one release for all of them
+    if (threadIdx.x == 0) {
+        uint32_t prev;
+        asm volatile("fence.acq_rel.sys;\n\t"
+                     "atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;"
+                     : "=r"(prev) : "l"(&p.status->check_arrive) : "memory");
+        s_last = prev == gridDim.x - 1;
+    }
+    __syncthreads();
+    if (!s_last || threadIdx.x != 0) return;
+    DevStatus* d = p.status;
+    volatile uint32_t* hs = &p.host->st.misuse;
+    hs[0] = d->misuse;
+    hs[1] = d->copier_timeouts;
+    hs[2] = d->timeout_inv;
+    hs[3] = d->bulk_timeouts;
+    d->misuse = 0;
+    d->copier_timeouts = 0;
+    d->timeout_inv = 0;
+    d->bulk_timeouts = 0;
+    d->check_arrive = 0;
+    asm volatile("fence.acq_rel.sys;\n\t"
+                 "st.release.sys.global.u32 [%0], %1;" ::"l"(&p.host->done), "r"(p.seq) : "memory");
 }
 
 // close() in mid-round: open every gate still closed so the copier sends chunks as they stand.
@@ -410,12 +437,12 @@ cudaError_t launch_copier(const CopierParams& p, uint32_t ctas, uint32_t threads
     return cudaGetLastError();
 }
 
-cudaError_t launch_check(const CheckParams& p, uint8_t* flags, cudaStream_t s) {
+cudaError_t launch_check(const CheckParams& p, cudaStream_t s) {
     const uint32_t threads = 256;
     uint32_t blocks = (p.n_global + threads - 1) / threads;
     if (blocks == 0) blocks = 1;
     if (blocks > 1024) blocks = 1024;
-    check_kernel<<<blocks, threads, 0, s>>>(p, flags);
+    check_kernel<<<blocks, threads, 0, s>>>(p);
     return cudaGetLastError();
 }
 

@@ -54,6 +54,18 @@ struct DevStatus {
     uint32_t copier_timeouts;   // copier CTAs that gave up on a gate
     uint32_t timeout_inv;       // 0xFFFFFFFF - (smallest chunk id a copier CTA gave up on); 0: none
     uint32_t bulk_timeouts;     // bulk-copy waits (mbarrier, bulk groups) that gave up
+    uint32_t check_arrive;      // check_kernel CTAs done with their chunks (the last one resets it)
+    uint32_t pad[3];
+};
+
+// A round's outcome in pinned, device-mapped host memory, written by check_kernel itself so that
+// wait() needs no device-to-host copy: the status words, then `done` (the sequence number of
+// the last check that finished, stored last with a system-scope release), then one flag byte per
+// chunk right after the struct (0 complete, 1 short, 2 extra marks).
+struct HostStatus {
+    DevStatus st;
+    uint32_t done;
+    uint32_t pad[7];
 };
 
 struct CopierParams {
@@ -80,6 +92,10 @@ struct CheckParams {
     uint32_t P;
     uint32_t n_global;
     uint32_t round;
+    uint32_t seq;               // stored in host->done once every flag and status word is there
+    DevStatus* status;          // the round's device status; the last CTA copies it out and zeroes it
+    HostStatus* host;           // device address of the mapped host block
+    uint8_t* host_flags;        // device address of its flag bytes
 };
 
 // Bulk-copy copier: a ring of `stages` shared-memory stages of stage_bytes, then one mbarrier
@@ -93,7 +109,7 @@ inline size_t bulk_smem_bytes(uint32_t stage_bytes, uint32_t stages) {
 cudaError_t launch_copier(const CopierParams& p, uint32_t ctas, uint32_t threads, uint32_t method,
                           cudaStream_t s);
 // Completion check: flags[c] = 0 delivered, 1 short, 2 extra marks.
-cudaError_t launch_check(const CheckParams& p, uint8_t* flags, cudaStream_t s);
+cudaError_t launch_check(const CheckParams& p, cudaStream_t s);
 cudaError_t launch_force_open(uint64_t* gates, const ChunkDesc* chunks, uint32_t n_global,
                               uint32_t round, cudaStream_t s);
 cudaError_t launch_consumer(const CopierParams& p, dtt_handle h, char* dst, uint64_t max_polls,

@@ -36,9 +36,10 @@ struct dtt_plan {
     ChunkDesc* d_chunks = nullptr;
     PieceDesc* d_pieces = nullptr;
     DevStatus* d_status = nullptr;
-    uint8_t* d_flags = nullptr;
-    uint8_t* h_flags = nullptr;       // pinned
-    DevStatus* h_status = nullptr;    // pinned
+    HostStatus* h_status = nullptr;   // pinned, mapped: check_kernel writes the round's outcome here
+    HostStatus* h_status_dev = nullptr;   // its device address
+    uint8_t* h_flags = nullptr;       // the flag bytes right after it
+    uint32_t wait_seq = 0;            // sequence number of the last check launched
 
     cudaStream_t copy_stream = nullptr;
     bool own_copy_stream = false;
@@ -50,9 +51,12 @@ struct dtt_plan {
     uint32_t round = 1;
     bool copier_launched = false;   // this round's copier is on the copy stream
 
-    cudaEvent_t ev_copier[2] = {};  // opts.time_copier: around each copier launch
+    // opts.time_copier: a ring of event pairs around the copier launches, read back lazily (when
+    // a pair comes round again, or in dtt_plan_stats) so that timing adds no wait to a round
+    static constexpr uint32_t kTimeRing = 64;
+    cudaEvent_t ev_copier[kTimeRing][2] = {};
+    uint64_t timed_launches = 0, timed_read = 0;
     double copier_ms_total = 0, copier_ms_last = 0;
-    uint64_t rounds_timed = 0;
 };
 
 namespace {
@@ -84,10 +88,11 @@ void free_device(dtt_plan* p) {
     cudaFree(p->d_status);
     cudaFreeHost(p->h_status);
     if (p->ev_producer) cudaEventDestroy(p->ev_producer);
-    for (cudaEvent_t& e : p->ev_copier) {
-        if (e) cudaEventDestroy(e);
-        e = nullptr;
-    }
+    for (auto& pair : p->ev_copier)
+        for (cudaEvent_t& e : pair) {
+            if (e) cudaEventDestroy(e);
+            e = nullptr;
+        }
     if (p->aux_stream) cudaStreamDestroy(p->aux_stream);
     if (p->own_copy_stream && p->copy_stream) cudaStreamDestroy(p->copy_stream);
     p->d_gates = nullptr;
@@ -95,9 +100,9 @@ void free_device(dtt_plan* p) {
     p->d_chunks = nullptr;
     p->d_pieces = nullptr;
     p->d_status = nullptr;
-    p->d_flags = nullptr;
     p->h_flags = nullptr;
     p->h_status = nullptr;
+    p->h_status_dev = nullptr;
     p->ev_producer = nullptr;
     p->aux_stream = nullptr;
     p->copy_stream = nullptr;
@@ -130,12 +135,40 @@ void cut_region(const dtt_region& r, uint64_t piece_bytes, bool bases_aligned,
 
 CopierParams copier_params(const dtt_plan* p);
 
-// Launch this round's copier on the copy stream (bracketed by the timing events when asked).
+// Add the timed copier launches up to `upto` (in launch order) to the copier statistics.
+int read_copier_times(dtt_plan* p, uint64_t upto) {
+    for (; p->timed_read < upto; ++p->timed_read) {
+        cudaEvent_t* pair = p->ev_copier[p->timed_read % dtt_plan::kTimeRing];
+        float ms = 0;
+        cudaError_t e = cudaEventElapsedTime(&ms, pair[0], pair[1]);
+        if (e == cudaErrorNotReady) {
+            DTT_CUDA_TRY(cudaEventSynchronize(pair[1]));
+            e = cudaEventElapsedTime(&ms, pair[0], pair[1]);
+        }
+        DTT_CUDA_TRY(e);
+        p->copier_ms_last = ms;
+        p->copier_ms_total += ms;
+    }
+    return DTT_OK;
+}
+
+// Launch this round's copier on the copy stream (bracketed by a pair of timing events when asked).
 int launch_round_copier(dtt_plan* p) {
-    if (p->opts.time_copier) DTT_CUDA_TRY(cudaEventRecord(p->ev_copier[0], p->copy_stream));
+    cudaEvent_t* pair = nullptr;
+    if (p->opts.time_copier) {
+        if (p->timed_launches - p->timed_read == dtt_plan::kTimeRing) {   // the oldest pair is reused
+            const int rc = read_copier_times(p, p->timed_read + 1);
+            if (rc != DTT_OK) return rc;
+        }
+        pair = p->ev_copier[p->timed_launches % dtt_plan::kTimeRing];
+        DTT_CUDA_TRY(cudaEventRecord(pair[0], p->copy_stream));
+    }
     DTT_CUDA_TRY(launch_copier(copier_params(p), p->copier_ctas, p->copier_threads, p->opts.method,
                                p->copy_stream));
-    if (p->opts.time_copier) DTT_CUDA_TRY(cudaEventRecord(p->ev_copier[1], p->copy_stream));
+    if (pair) {
+        DTT_CUDA_TRY(cudaEventRecord(pair[1], p->copy_stream));
+        ++p->timed_launches;
+    }
     p->copier_launched = true;
     return DTT_OK;
 }
@@ -324,14 +357,16 @@ int upload(dtt_plan* p) {
     DTT_CUDA_TRY(cudaMalloc(&p->d_writers, std::max<size_t>(1, n * sizeof(uint32_t))));
     DTT_CUDA_TRY(cudaMalloc(&p->d_chunks, std::max<size_t>(1, n * sizeof(ChunkDesc))));
     DTT_CUDA_TRY(cudaMalloc(&p->d_pieces, std::max<size_t>(1, p->pieces.size() * sizeof(PieceDesc))));
-    // status block and check flags side by side, so wait() reads both back with one copy
-    DTT_CUDA_TRY(cudaMalloc(&p->d_status, sizeof(DevStatus) + std::max<size_t>(1, n)));
-    DTT_CUDA_TRY(cudaMallocHost(&p->h_status, sizeof(DevStatus) + std::max<size_t>(1, n)));
-    p->d_flags = reinterpret_cast<uint8_t*>(p->d_status + 1);
+    // the round's status on the device; its outcome and the per-chunk flags in mapped host memory
+    DTT_CUDA_TRY(cudaMalloc(&p->d_status, sizeof(DevStatus)));
+    const size_t host_bytes = sizeof(HostStatus) + std::max<size_t>(1, n);
+    DTT_CUDA_TRY(cudaHostAlloc(&p->h_status, host_bytes, cudaHostAllocMapped | cudaHostAllocPortable));
+    std::memset(p->h_status, 0, host_bytes);
+    DTT_CUDA_TRY(cudaHostGetDevicePointer(reinterpret_cast<void**>(&p->h_status_dev), p->h_status, 0));
     p->h_flags = reinterpret_cast<uint8_t*>(p->h_status + 1);
     if (p->opts.time_copier) {
-        DTT_CUDA_TRY(cudaEventCreate(&p->ev_copier[0]));
-        DTT_CUDA_TRY(cudaEventCreate(&p->ev_copier[1]));
+        for (auto& pair : p->ev_copier)
+            for (cudaEvent_t& e : pair) DTT_CUDA_TRY(cudaEventCreate(&e));
     }
     if (!gates.empty())
         DTT_CUDA_TRY(cudaMemcpy(p->d_gates, gates.data(), gates.size() * sizeof(uint64_t), cudaMemcpyHostToDevice));
@@ -475,8 +510,7 @@ int dtt_plan_start(dtt_plan* p, cudaStream_t producer_stream, dtt_handle* handle
     if (p->state != DTT_PLAN_PREPARED) return fail(DTT_ESTATE, "dtt_plan_start: plan is not PREPARED (state %d)", p->state);
     if (producer_stream == p->copy_stream)
         return fail(DTT_EINVAL, "dtt_plan_start: the producer stream must differ from the copy stream");
-    DTT_CUDA_TRY(cudaMemsetAsync(p->d_status, 0, sizeof(DevStatus), p->copy_stream));
-    p->copier_launched = false;
+    p->copier_launched = false;      // the status words were zeroed by the last check (or upload)
     if (p->n_global && !p->opts.deferred_copier) {
         const int rc = launch_round_copier(p);
         if (rc != DTT_OK) return rc;
@@ -516,22 +550,29 @@ int dtt_plan_wait(dtt_plan* p, dtt_report* report) {
     ck.P = p->P;
     ck.n_global = p->n_global;
     ck.round = p->round;
-    if (p->n_global) DTT_CUDA_TRY(launch_check(ck, p->d_flags, p->copy_stream));
-    DTT_CUDA_TRY(cudaMemcpyAsync(p->h_status, p->d_status, sizeof(DevStatus) + p->n_global,
-                                 cudaMemcpyDeviceToHost, p->copy_stream));   // status + flags
-    DTT_CUDA_TRY(cudaStreamSynchronize(p->copy_stream));
-    if (p->opts.time_copier && p->copier_launched) {
-        float ms = 0;
-        if (cudaEventElapsedTime(&ms, p->ev_copier[0], p->ev_copier[1]) == cudaSuccess) {
-            p->copier_ms_last = ms;
-            p->copier_ms_total += ms;
-            ++p->rounds_timed;
+    ck.seq = ++p->wait_seq;
+    ck.status = p->d_status;
+    ck.host = p->h_status_dev;
+    ck.host_flags = p->h_status_dev ? reinterpret_cast<uint8_t*>(p->h_status_dev + 1) : nullptr;
+    DTT_CUDA_TRY(launch_check(ck, p->copy_stream));
+    // The check stores its sequence number last, after every flag and status word: poll that
+    // word, and ask the stream now and then so that a failed launch or a dead context ends the
+    // wait with the CUDA error instead of spinning.
+    const uint32_t* done = &p->h_status->done;
+    for (uint64_t spin = 1;; ++spin) {
+        if (__atomic_load_n(done, __ATOMIC_ACQUIRE) == ck.seq) break;
+        if ((spin & 4095) == 0) {
+            const cudaError_t e = cudaStreamQuery(p->copy_stream);
+            if (e == cudaErrorNotReady) continue;
+            if (e != cudaSuccess) return fail(DTT_ECUDA, "dtt_plan_wait: %s", cudaGetErrorString(e));
+            if (__atomic_load_n(done, __ATOMIC_ACQUIRE) == ck.seq) break;
+            return fail(DTT_ECUDA, "dtt_plan_wait: the check kernel finished without reporting");
         }
     }
     dtt_report rep{};
     rep.round = p->round;
-    rep.copier_timeouts = p->h_status->copier_timeouts;
-    rep.device_status = p->h_status->misuse;
+    rep.copier_timeouts = p->h_status->st.copier_timeouts;
+    rep.device_status = p->h_status->st.misuse;
     for (uint32_t c = 0; c < p->n_global; ++c) {
         if (p->h_flags[c] == 2) {
             if (rep.n_extra < DTT_REPORT_MAX) rep.extra_chunks[rep.n_extra] = c;
@@ -591,12 +632,14 @@ int dtt_plan_close(dtt_plan* p) {
     return rc;
 }
 
-int dtt_plan_stats(const dtt_plan* p, double* copier_ms_last, double* copier_ms_total,
+int dtt_plan_stats(dtt_plan* p, double* copier_ms_last, double* copier_ms_total,
                    uint64_t* rounds_timed) {
     if (!p) return fail(DTT_EINVAL, "dtt_plan_stats: NULL plan");
+    const int rc = read_copier_times(p, p->timed_launches);
+    if (rc != DTT_OK) return rc;
     if (copier_ms_last) *copier_ms_last = p->copier_ms_last;
     if (copier_ms_total) *copier_ms_total = p->copier_ms_total;
-    if (rounds_timed) *rounds_timed = p->rounds_timed;
+    if (rounds_timed) *rounds_timed = p->timed_read;
     return DTT_OK;
 }
 

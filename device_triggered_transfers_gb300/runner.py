@@ -12,7 +12,8 @@ import torch
 
 from . import (MARK_AT_END, MARK_PER_STEP, ORDER_GROUPED, ORDER_ROW_MAJOR, Plan, Schedule,
                dtt_fill_producer, dtt_plan_opts_default, dtt_schedule_chunks,
-               dtt_schedule_empty, dtt_schedule_tile_chunks, dtt_schedule_whole, fill_desc)
+               dtt_schedule_empty, dtt_schedule_tile_chunks, dtt_schedule_whole, fill_desc,
+               pointer_array)
 
 
 def schedules_for(w) -> List[Schedule]:
@@ -84,6 +85,7 @@ class Setup:
     desc: object
     producer_stream: torch.cuda.Stream
     counters: Optional[torch.Tensor] = None
+    buf_ptrs: object = None           # the buffers' addresses, marshalled once
 
 
 def make(w, opts=None, cluster: int = 1, programs: Optional[int] = None, threads: int = 0,
@@ -105,13 +107,13 @@ def make(w, opts=None, cluster: int = 1, programs: Optional[int] = None, threads
     desc = producer_desc(w, cluster=cluster, programs=programs, threads=threads, group=group,
                          counters=counters)
     torch.cuda.synchronize()          # buffers initialised before any round starts
-    return Setup(w, bufs, plan, desc, torch.cuda.Stream(), counters)
+    return Setup(w, bufs, plan, desc, torch.cuda.Stream(), counters, pointer_array(bufs))
 
 
 def run_round(st: Setup, raise_on_error: bool = True):
     """One round: start (launches the copier), the fill producer, wait.  Returns the report."""
     handles = st.plan.start(st.producer_stream)
-    dtt_fill_producer(st.bufs, st.desc, handles, st.producer_stream)
+    dtt_fill_producer(st.buf_ptrs, st.desc, handles, st.producer_stream)
     return st.plan.wait(raise_on_error=raise_on_error)
 
 

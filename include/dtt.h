@@ -297,10 +297,11 @@ int dtt_plan_info(const dtt_plan* plan, uint32_t* n_global, uint32_t* first_chun
                   uint32_t* n_chunks, uint64_t** gates_device);
 
 /* Copier timing of a plan created with opts.time_copier = 1: the device time of the last
- * round's copier launch and the sum over all timed rounds (milliseconds, from CUDA events
- * recorded around each launch on the copy stream), and how many rounds were timed.  Values
- * are updated by dtt_plan_wait.  Any pointer may be NULL.  Errors: DTT_EINVAL. */
-int dtt_plan_stats(const dtt_plan* plan, double* copier_ms_last, double* copier_ms_total,
+ * copier launch and the sum over all launches so far (milliseconds, from CUDA events recorded
+ * around each launch on the copy stream), and how many launches were timed.  The events are
+ * read here (waiting for the copy stream's launched copiers), not in dtt_plan_wait, so timing
+ * adds no synchronisation to a round.  Any pointer may be NULL.  Errors: DTT_EINVAL, DTT_ECUDA. */
+int dtt_plan_stats(dtt_plan* plan, double* copier_ms_last, double* copier_ms_total,
                    uint64_t* rounds_timed);
 
 /* Copy the P gate tables (P * n_global * 8 uint64, rank-major) to host memory `host`
