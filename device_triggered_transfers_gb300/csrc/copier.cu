@@ -462,6 +462,14 @@ cudaError_t launch_consumer(const CopierParams& p, dtt_handle h, char* dst, uint
     return cudaGetLastError();
 }
 
+cudaError_t copier_regs_per_thread(uint32_t method, int* regs) {
+    cudaFuncAttributes a{};
+    const cudaError_t e = method == DTT_COPY_TMA ? cudaFuncGetAttributes(&a, copier_bulk_kernel)
+                                                 : cudaFuncGetAttributes(&a, copier_kernel);
+    *regs = a.numRegs;
+    return e;
+}
+
 cudaError_t preload_copier_kernels() {
     cudaError_t e = prepare_kernel(copier_kernel);
     if (e == cudaSuccess) e = prepare_kernel(copier_bulk_kernel);

@@ -6,14 +6,14 @@
 // Per CTA (one per SM, 192 threads), warp-specialised:
 //   warp 4      TMA: loads 128 x 64 bf16 tiles of A_r and of B^T (K-major, 128-byte swizzle)
 //               into a ring of shared-memory stages, completing on mbarriers;
-//   warp 5      MMA: one thread issues tcgen05.mma (M = 128, N = 128, K = 16, fp32
-//               accumulate in TMEM) and commits each stage back to the TMA warp, and each
-//               finished tile to the epilogue;
+//   warp 5      MMA: one thread issues tcgen05.mma (M = 128, N = TN = 256 when N allows it,
+//               else 128, K = 16, fp32 accumulate in TMEM) and commits each stage back to the
+//               TMA warp, and each finished block of TN / 128 tiles to the epilogue;
 //   warps 0-3   epilogue: tcgen05.ld the accumulator (warp w owns TMEM lanes 32w..32w+31 =
 //               tile rows), round to bf16, store to the rank's buffer, then a named barrier
 //               over these 128 threads and one mark.
-// Two TMEM accumulators (2 x 128 columns) let the MMA warp start the next tile while the
-// epilogue drains the previous one.  Every wait is bounded; on a timeout the CTA records an
+// Two TMEM accumulators (2 x TN columns) let the MMA warp start the next block while the
+// epilogue drains the previous one; the epilogue marks each 128 x 128 tile of a block.  Every wait is bounded; on a timeout the CTA records an
 // error, lets its copies and MMAs finish (bounded), frees its TMEM and returns.
 #include <cstdint>
 

@@ -134,6 +134,7 @@ cudaError_t prepare_kernel(K kernel) {
 
 // Force-load each translation unit's kernels on the current device (see dtt_preload).
 cudaError_t preload_copier_kernels();
+cudaError_t copier_regs_per_thread(uint32_t method, int* regs);   // of the copier kernel for `method`
 cudaError_t preload_fill_kernels();
 cudaError_t preload_barrier_kernels();
 cudaError_t preload_gemm_kernels();

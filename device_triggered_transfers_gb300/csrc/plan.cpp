@@ -477,6 +477,25 @@ int dtt_plan_create(void* const* bufs, uint64_t buf_bytes, uint32_t P,
     }
     p->copier_ctas = o.copier_ctas ? o.copier_ctas : (uint32_t)sms * o.ctas_per_sm;
     p->copier_threads = o.copier_threads;
+    if (!o.deferred_copier) {
+        // The copier spins while the producer runs, so it must leave an SM room for producer
+        // CTAs: at most half of its threads (2048) and half of its registers (64 Ki) per SM.
+        int regs = 0;
+        if (copier_regs_per_thread(o.method, &regs) != cudaSuccess) {
+            delete p;
+            return fail(DTT_ECUDA, "dtt_plan_create: cannot query the copier kernel");
+        }
+        const uint64_t per_sm = (p->copier_ctas + (uint32_t)sms - 1) / (uint32_t)sms;
+        const uint64_t thr = o.method == DTT_COPY_TMA ? 32 : o.copier_threads;
+        if (per_sm * thr > 1024 || per_sm * thr * (uint64_t)regs > 32768) {
+            delete p;
+            return fail(DTT_EINVAL,
+                        "dtt_plan_create: %llu copier CTA(s) of %llu threads x %d registers per SM leave "
+                        "too little room for a producer beside the copier (at most 1024 threads and "
+                        "32768 registers per SM)",
+                        (unsigned long long)per_sm, (unsigned long long)thr, regs);
+        }
+    }
     rc = build_plan(p, scheds);
     if (rc == DTT_OK) rc = upload(p);
     if (rc == DTT_OK) {

@@ -249,6 +249,9 @@ typedef struct dtt_report {
  * copy_stream: a non-blocking stream for the copier, or NULL to let the plan create (and
  * own) a high-priority one.  Creation succeeds for every rank or for none: on error nothing
  * stays allocated ("Triggered Plans", The kernel author's contract).
+ * Unless opts->deferred_copier, the copier runs beside the producer, so its launch must leave
+ * every SM room for producer CTAs: creation fails with DTT_EINVAL when the copier CTAs of one
+ * SM would take more than 1024 threads or 32768 registers.
  * Errors: DTT_EINVAL, DTT_EOUTOFROWS, DTT_EOVERLAP, DTT_ECAPACITY, DTT_ENOMEM, DTT_ECUDA. */
 int dtt_plan_create(void* const* bufs, uint64_t buf_bytes, uint32_t P,
                     const dtt_schedule* const* scheds, const dtt_plan_opts* opts,

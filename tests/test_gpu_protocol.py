@@ -127,6 +127,22 @@ def test_producer_stream_must_differ_from_copy_stream():
     plan.close()
 
 
+def test_copier_must_leave_room_for_the_producer():
+    # a 1024-thread vector copier CTA on every SM would hold all of its registers while it spins,
+    # so no producer CTA could run beside it: refused unless the copier is deferred
+    bufs = [torch.zeros(WS.buf_bytes, dtype=torch.uint8, device="cuda") for _ in range(2)]
+    with pytest.raises(D.DttError) as e:
+        D.Plan(bufs, WS.buf_bytes, runner.schedules_for(WS),
+               D.dtt_plan_opts_default(copier_threads=1024))
+    assert e.value.code == D.EINVAL
+    st = runner.make(WS, opts=D.dtt_plan_opts_default(copier_threads=1024, deferred_copier=1))
+    try:
+        rep = runner.run_round(st)
+        assert rep.status == D.OK
+    finally:
+        st.plan.close()
+
+
 def test_close_mid_round_sends_chunks_as_they_stand():
     st = runner.make(WS)
     o = oracle_plan(WS)
