@@ -161,7 +161,8 @@ __global__ void __launch_bounds__(1024) copier_kernel(const __grid_constant__ Co
 // an mbarrier) fill a ring of shared-memory stages, and each stage is written back to every peer
 // with bulk stores.  Loads of later pieces overlap the stores of earlier ones.  The SM's other
 // resources stay free for the producer.  Every piece fits one stage (the plan cuts them so) and
-// is 16-byte aligned.
+// is 16-byte aligned.  A 2D window of short rows moves as one tensor-map box (one load, one
+// store per peer) instead of a bulk copy per row.
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -212,6 +213,23 @@ __device__ __forceinline__ void bulk_store(void* dst, uint32_t src_smem, uint32_
                  ::"l"(dst), "r"(src_smem), "r"(bytes), "l"(pol) : "memory");
 }
 
+// One box of a 2D window through its tensor map (8-byte elements, no swizzle): a load into a
+// shared-memory stage completing on an mbarrier, and a store from the stage.
+__device__ __forceinline__ void tensor_load(uint32_t dst_smem, const CUtensorMap* map, uint32_t x, uint32_t y,
+                                            uint32_t bar, uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+        "[%0], [%1, {%2, %3}], [%4], %5;"
+        ::"r"(dst_smem), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "l"(pol)
+        : "memory");
+}
+
+__device__ __forceinline__ void tensor_store(const CUtensorMap* map, uint32_t x, uint32_t y, uint32_t src_smem,
+                                             uint64_t pol) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group.L2::cache_hint [%0, {%1, %2}], [%3], %4;"
+                 ::"l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(src_smem), "l"(pol) : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
@@ -220,7 +238,7 @@ __device__ __forceinline__ void fence_proxy_async_global() {
 }
 
 __global__ void __launch_bounds__(32) copier_bulk_kernel(const __grid_constant__ CopierParams p) {
-    extern __shared__ __align__(128) uint8_t smem[];
+    extern __shared__ __align__(1024) uint8_t smem[];
     if (threadIdx.x != 0) return;
     const uint32_t b = blockIdx.x;
     uint32_t s = 0;
@@ -248,8 +266,12 @@ __global__ void __launch_bounds__(32) copier_bulk_kernel(const __grid_constant__
         const uint32_t bar = smem_addr(bars + st);
         const uint32_t dst = smem_addr(stage0 + (size_t)st * p.stage_bytes);
         mbar_expect_tx(bar, pc.row_bytes * pc.rows);
-        for (uint32_t r = 0; r < pc.rows; ++r)
-            bulk_load(dst + r * pc.row_bytes, src_base + pc.off + (uint64_t)r * pc.pitch, pc.row_bytes, bar, pol);
+        if (pc.tmap != kNoMap) {
+            tensor_load(dst, p.tmaps + (size_t)pc.tmap * p.P + s, pc.x, pc.y, bar, pol);
+        } else {
+            for (uint32_t r = 0; r < pc.rows; ++r)
+                bulk_load(dst + r * pc.row_bytes, src_base + pc.off + (uint64_t)r * pc.pitch, pc.row_bytes, bar, pol);
+        }
         loads_hi = idx + 1;
     };
     auto store = [&](const PieceDesc& pc, uint64_t idx) {
@@ -257,6 +279,10 @@ __global__ void __launch_bounds__(32) copier_bulk_kernel(const __grid_constant__
         const uint32_t src = smem_addr(stage0 + (size_t)st * p.stage_bytes);
         for (uint32_t q = 0; q < p.P; ++q) {
             if (q == s) continue;
+            if (pc.tmap != kNoMap) {
+                tensor_store(p.tmaps + (size_t)pc.tmap * p.P + q, pc.x, pc.y, src, pol);
+                continue;
+            }
             char* dst = p.bufs[q] + pc.off;
             for (uint32_t r = 0; r < pc.rows; ++r)
                 bulk_store(dst + (uint64_t)r * pc.pitch, src + r * pc.row_bytes, pc.row_bytes, pol);
@@ -317,7 +343,6 @@ __global__ void __launch_bounds__(32) copier_bulk_kernel(const __grid_constant__
         if (!mbar_wait(smem_addr(bars + idx % S), (uint32_t)((idx / S) & 1))) break;
 }
 
-// Completion check: flags[c] = 0 delivered, 1 short (marks or an arrival missing), 2 extra.
 // wait()'s completion check, run after the copier and the producer: one flag per chunk, written
 // straight into the mapped host block.  The last CTA to finish copies the status words out,
 // zeroes them for the next round, and only then stores the sequence number the host polls for.

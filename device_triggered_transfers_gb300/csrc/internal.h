@@ -7,11 +7,27 @@
 #include <string>
 #include <vector>
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include "dtt.h"
 
 namespace dtt {
+
+// The driver's tensor-map encoder (cuTensorMapEncodeTiled, through the runtime's entry-point
+// query so that the library needs no link against libcuda); nullptr if the driver lacks it.
+inline PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+        return static_cast<PFN_cuTensorMapEncodeTiled_v12000>(nullptr);
+    }();
+    return fn;
+}
 
 // Thread-local message behind dtt_last_error().
 void set_error(const char* fmt, ...);
@@ -25,15 +41,22 @@ int fail(int code, const char* fmt, ...);
                                __FILE__, __LINE__);                                          \
     } while (0)
 
+constexpr uint32_t kNoMap = 0xFFFFFFFFu;
+
 // One unit of copier work: a sub-window of a region (rows x row_bytes, pitch apart) at byte
 // offset `off` of every buffer.  `vec` = 1 when off, row_bytes and pitch are multiples of 16.
+// Bulk-copy path: `tmap` names the tensor-map shape that moves the whole window as one box
+// (maps [tmap * P + q] for buffer q), with the box origin at element column x (8-byte elements)
+// and row y; kNoMap: one bulk copy per row.
 struct PieceDesc {
     uint64_t off;
     uint64_t pitch;
     uint32_t row_bytes;
     uint32_t rows;
     uint32_t vec;
-    uint32_t pad;
+    uint32_t tmap;
+    uint32_t x;
+    uint32_t y;
 };
 
 // Per global chunk: its pieces [piece_begin, piece_begin + n_pieces), the copier CTA of its
@@ -70,6 +93,7 @@ struct HostStatus {
 
 struct CopierParams {
     char* bufs[DTT_MAX_RANKS];
+    const CUtensorMap* tmaps;   // bulk-copy path: [shape][rank] maps of the 2D windows (or null)
     uint64_t* gates;
     const ChunkDesc* chunks;
     const PieceDesc* pieces;
@@ -82,7 +106,7 @@ struct CopierParams {
     uint32_t round;
     uint32_t flags;
     uint64_t max_polls;
-    uint32_t stage_bytes;       // bulk-copy path: bytes per shared-memory stage (>= a piece)
+    uint32_t stage_bytes;       // bulk-copy path: bytes per shared-memory stage (>= a piece, 128-aligned)
     uint32_t stages;            // bulk-copy path: stages in the ring
 };
 
@@ -101,6 +125,10 @@ struct CheckParams {
 // Bulk-copy copier: a ring of `stages` shared-memory stages of stage_bytes, then one mbarrier
 // per stage; at most kBulkSmemMax bytes of dynamic shared memory per CTA.
 constexpr size_t kBulkSmemMax = 200 * 1024;
+// Shared-memory stage of the bulk-copy path: a piece, rounded up to the 128-byte alignment that
+// tensor copies need.
+inline uint32_t bulk_stage_bytes(uint32_t piece_bytes) { return (piece_bytes + 127u) & ~127u; }
+
 inline size_t bulk_smem_bytes(uint32_t stage_bytes, uint32_t stages) {
     return (size_t)stage_bytes * stages + 8 * (size_t)stages;
 }

@@ -13,6 +13,19 @@
 
 using namespace dtt;
 
+namespace {
+
+// A tensor-map shape of the bulk-copy path: boxes of `inner` 8-byte elements by `rows` rows, in
+// a buffer seen as rows of `pitch` bytes.  The plan encodes one map per (shape, buffer).
+struct MapShape {
+    uint32_t inner, rows;
+    uint64_t pitch;
+    bool operator==(const MapShape& o) const { return inner == o.inner && rows == o.rows && pitch == o.pitch; }
+};
+constexpr size_t kMaxMapShapes = 256;
+
+}  // namespace
+
 struct dtt_plan {
     uint32_t P = 0;
     uint64_t buf_bytes = 0;
@@ -26,6 +39,7 @@ struct dtt_plan {
     std::vector<ChunkDesc> chunks;
     std::vector<PieceDesc> pieces;
     std::vector<uint32_t> writers;
+    std::vector<MapShape> shapes;     // bulk-copy path: the tensor-map shapes of the 2D windows
 
     uint32_t copier_ctas = 0;
     uint32_t copier_threads = 0;
@@ -35,6 +49,7 @@ struct dtt_plan {
     uint32_t* d_writers = nullptr;
     ChunkDesc* d_chunks = nullptr;
     PieceDesc* d_pieces = nullptr;
+    CUtensorMap* d_tmaps = nullptr;   // [shape][rank]
     DevStatus* d_status = nullptr;
     HostStatus* h_status = nullptr;   // pinned, mapped: check_kernel writes the round's outcome here
     HostStatus* h_status_dev = nullptr;   // its device address
@@ -85,6 +100,7 @@ void free_device(dtt_plan* p) {
     cudaFree(p->d_writers);
     cudaFree(p->d_chunks);
     cudaFree(p->d_pieces);
+    cudaFree(p->d_tmaps);
     cudaFree(p->d_status);
     cudaFreeHost(p->h_status);
     if (p->ev_producer) cudaEventDestroy(p->ev_producer);
@@ -99,6 +115,7 @@ void free_device(dtt_plan* p) {
     p->d_writers = nullptr;
     p->d_chunks = nullptr;
     p->d_pieces = nullptr;
+    p->d_tmaps = nullptr;
     p->d_status = nullptr;
     p->h_flags = nullptr;
     p->h_status = nullptr;
@@ -108,28 +125,70 @@ void free_device(dtt_plan* p) {
     p->copy_stream = nullptr;
 }
 
+struct CutCtx {
+    uint64_t piece_bytes;
+    uint64_t buf_bytes;
+    bool bases_aligned;
+    bool tensor;                      // bulk-copy path: 2D windows as tensor-map boxes
+    std::vector<MapShape>* shapes;
+};
+
+// The shape index of a box, adding the shape if it is new; kNoMap when the table is full.
+uint32_t shape_of(const MapShape& m, std::vector<MapShape>* shapes) {
+    for (size_t i = 0; i < shapes->size(); ++i)
+        if ((*shapes)[i] == m) return (uint32_t)i;
+    if (shapes->size() >= kMaxMapShapes) return kNoMap;
+    shapes->push_back(m);
+    return (uint32_t)(shapes->size() - 1);
+}
+
+// Can this 2D window move as tensor-map boxes?  Rows of 16-byte multiples up to 2 KiB (256
+// elements of 8 bytes, the widest box), 16-byte aligned columns (a box's x coordinate must be),
+// and every row of the window inside the buffer's whole rows of `pitch` bytes.
+bool tensor_window(const dtt_region& r, const CutCtx& cx) {
+    if (!cx.tensor || !cx.bases_aligned || r.rows < 2 || r.pitch <= r.row_bytes) return false;
+    const uint64_t col = r.offset % r.pitch, row0 = r.offset / r.pitch;
+    return r.row_bytes % 16 == 0 && r.row_bytes <= 2048 && r.row_bytes < cx.piece_bytes &&
+           r.pitch % 16 == 0 && col % 16 == 0 && col + r.row_bytes <= r.pitch &&
+           (row0 + r.rows) * r.pitch <= cx.buf_bytes && r.pitch / 8 <= 0xFFFFFFFFull &&
+           cx.buf_bytes / r.pitch <= 0xFFFFFFFFull && (r.pitch >> 40) == 0;
+}
+
 // Cut one region into copier pieces of at most piece_bytes: whole rows when a row fits,
-// otherwise column pieces of single rows.
-void cut_region(const dtt_region& r, uint64_t piece_bytes, bool bases_aligned,
-                std::vector<PieceDesc>* out) {
-    auto push = [&](uint64_t off, uint64_t rb, uint64_t rows, uint64_t pitch) {
+// otherwise column pieces of single rows.  On the bulk-copy path a 2D window's pieces of whole
+// rows (at most 256 rows each, the tallest box) are tensor-map boxes when the window allows it.
+void cut_region(const dtt_region& r, const CutCtx& cx, std::vector<PieceDesc>* out) {
+    const uint64_t piece_bytes = cx.piece_bytes;
+    auto push = [&](uint64_t off, uint64_t rb, uint64_t rows, uint64_t pitch, uint32_t tmap) {
         PieceDesc pc{};
         pc.off = off;
         pc.pitch = rows > 1 ? pitch : rb;
         pc.row_bytes = (uint32_t)rb;
         pc.rows = (uint32_t)rows;
-        pc.vec = bases_aligned && (off % 16 == 0) && (rb % 16 == 0) && (rows <= 1 || pitch % 16 == 0);
+        pc.vec = cx.bases_aligned && (off % 16 == 0) && (rb % 16 == 0) && (rows <= 1 || pitch % 16 == 0);
+        pc.tmap = tmap;
+        if (tmap != kNoMap) {
+            pc.x = (uint32_t)((off % pitch) / 8);
+            pc.y = (uint32_t)(off / pitch);
+        }
         out->push_back(pc);
     };
     if (r.rows == 0 || r.row_bytes == 0) return;
     if (r.row_bytes >= piece_bytes) {
         for (uint64_t i = 0; i < r.rows; ++i)
             for (uint64_t c = 0; c < r.row_bytes; c += piece_bytes)
-                push(r.offset + i * r.pitch + c, std::min(piece_bytes, r.row_bytes - c), 1, 0);
+                push(r.offset + i * r.pitch + c, std::min(piece_bytes, r.row_bytes - c), 1, 0, kNoMap);
     } else {
-        const uint64_t per = std::max<uint64_t>(1, piece_bytes / r.row_bytes);
-        for (uint64_t i = 0; i < r.rows; i += per)
-            push(r.offset + i * r.pitch, r.row_bytes, std::min(per, r.rows - i), r.pitch);
+        const bool tensor = tensor_window(r, cx);
+        uint64_t per = std::max<uint64_t>(1, piece_bytes / r.row_bytes);
+        if (tensor) per = std::min<uint64_t>(per, 256);
+        for (uint64_t i = 0; i < r.rows; i += per) {
+            const uint64_t rows = std::min(per, r.rows - i);
+            const uint32_t tmap = tensor && rows > 1
+                ? shape_of(MapShape{(uint32_t)(r.row_bytes / 8), (uint32_t)rows, r.pitch}, cx.shapes)
+                : kNoMap;
+            push(r.offset + i * r.pitch, r.row_bytes, rows, r.pitch, tmap);
+        }
     }
 }
 
@@ -205,7 +264,8 @@ CopierParams copier_params(const dtt_plan* p) {
     cp.round = p->round;
     cp.flags = p->opts.timestamps ? DTT_HANDLE_TIMESTAMPS : 0u;
     cp.max_polls = p->opts.max_polls;
-    cp.stage_bytes = p->opts.piece_bytes;
+    cp.stage_bytes = bulk_stage_bytes(p->opts.piece_bytes);
+    cp.tmaps = p->d_tmaps;
     cp.stages = p->opts.stages;
     return cp;
 }
@@ -303,7 +363,8 @@ int build_plan(dtt_plan* p, const dtt_schedule* const* scheds) {
     for (uint32_t r = 0; r < P; ++r) p->cta_base[r + 1] = p->cta_base[r] + G[r];
     p->copier_ctas = std::max<uint32_t>(1, p->cta_base[P]);
 
-    const uint64_t piece_bytes = p->opts.piece_bytes;
+    const CutCtx cx{p->opts.piece_bytes, p->buf_bytes, bases_aligned, p->opts.method == DTT_COPY_TMA,
+                    &p->shapes};
     for (uint32_t r = 0; r < P; ++r) {
         const dtt_schedule* s = scheds ? scheds[r] : nullptr;
         if (!s) continue;
@@ -312,11 +373,12 @@ int build_plan(dtt_plan* p, const dtt_schedule* const* scheds) {
             ChunkDesc cd{};
             cd.piece_begin = (uint32_t)p->pieces.size();
             for (const dtt_region& reg : ch.regions) {
-                cut_region(reg, piece_bytes, bases_aligned, &p->pieces);
+                cut_region(reg, cx, &p->pieces);
                 cd.bytes += reg.rows * reg.row_bytes;
             }
             if (p->pieces.size() == cd.piece_begin) {   // an empty chunk still signals arrival
                 PieceDesc empty{};
+                empty.tmap = kNoMap;
                 p->pieces.push_back(empty);
             }
             cd.n_pieces = (uint32_t)p->pieces.size() - cd.piece_begin;
@@ -377,6 +439,26 @@ int upload(dtt_plan* p) {
     if (!p->pieces.empty())
         DTT_CUDA_TRY(cudaMemcpy(p->d_pieces, p->pieces.data(), p->pieces.size() * sizeof(PieceDesc),
                                 cudaMemcpyHostToDevice));
+    if (!p->shapes.empty()) {     // one map per (shape, buffer): 8-byte elements, no swizzle
+        auto encode = tensor_map_encoder();
+        if (!encode) return fail(DTT_ECUDA, "plan: the driver has no tensor-map encoder");
+        std::vector<CUtensorMap> maps(p->shapes.size() * P);
+        for (size_t i = 0; i < p->shapes.size(); ++i) {
+            const MapShape& m = p->shapes[i];
+            const cuuint64_t dims[2] = {m.pitch / 8, p->buf_bytes / m.pitch};
+            const cuuint64_t strides[1] = {m.pitch};
+            const cuuint32_t box[2] = {m.inner, m.rows};
+            const cuuint32_t estr[2] = {1, 1};
+            for (uint32_t q = 0; q < P; ++q)
+                if (encode(&maps[i * P + q], CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, p->bufs[q], dims, strides, box,
+                           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+                    return fail(DTT_ECUDA, "plan: cannot encode the tensor map of a %u x %u-byte window",
+                                m.rows, m.inner * 8);
+        }
+        DTT_CUDA_TRY(cudaMalloc(&p->d_tmaps, maps.size() * sizeof(CUtensorMap)));
+        DTT_CUDA_TRY(cudaMemcpy(p->d_tmaps, maps.data(), maps.size() * sizeof(CUtensorMap), cudaMemcpyHostToDevice));
+    }
     DTT_CUDA_TRY(cudaMemset(p->d_status, 0, sizeof(DevStatus)));
     return DTT_OK;
 }
@@ -438,13 +520,14 @@ int dtt_plan_create(void* const* bufs, uint64_t buf_bytes, uint32_t P,
     if (o.piece_bytes == 0) o.piece_bytes = 65536;
     if (o.copier_threads == 0) o.copier_threads = 512;
     if (o.ctas_per_sm == 0) o.ctas_per_sm = 1;
-    if (o.stages == 0) o.stages = 8;
+    if (o.stages == 0 && o.piece_bytes % 16 == 0)   // as many stages as fit, at most 8
+        o.stages = (uint32_t)std::max<size_t>(2, std::min<size_t>(8, kBulkSmemMax / (bulk_stage_bytes(o.piece_bytes) + 8)));
     if (o.piece_bytes % 16 || o.copier_threads % 32 || o.copier_threads > 1024 ||
         (o.method != DTT_COPY_VEC16 && o.method != DTT_COPY_TMA)) {
         delete p;
         return fail(DTT_EINVAL, "dtt_plan_create: bad options (piece_bytes %% 16, threads %% 32 <= 1024, method)");
     }
-    if (o.method == DTT_COPY_TMA && bulk_smem_bytes(o.piece_bytes, o.stages) > kBulkSmemMax) {
+    if (o.method == DTT_COPY_TMA && bulk_smem_bytes(bulk_stage_bytes(o.piece_bytes), o.stages) > kBulkSmemMax) {
         delete p;
         return fail(DTT_EINVAL, "dtt_plan_create: stages x piece_bytes exceeds %zu bytes of shared memory",
                     kBulkSmemMax);

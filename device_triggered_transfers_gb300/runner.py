@@ -125,15 +125,16 @@ def bench_launch(w) -> dict:
     38 CTAs (152 in all, one per SM) that writes the rank's chunks in order and marks each once,
     so every rank's chunk k opens in wave k and the copier follows the waves.
     whole(): the bulk-copy copier over the contiguous slices.
-    tile_chunks: 2D windows of short rows, which the 16-byte vector copier handles best; a
-    256-thread copier CTA per SM leaves the tiled producer more of each SM."""
+    tile_chunks (fill producer): the bulk-copy copier moving each tile as tensor-map boxes of
+    16 KiB, twelve in flight per SM.  The GEMM producer keeps the vector copier: its own
+    shared-memory ring leaves no room for a bulk-copy ring on the same SM."""
     if w.kind == "chunks":
         return {"group": 38, "programs": 1, "threads": 256,
                 "opts": dtt_plan_opts_default(method=1, piece_bytes=65536, stages=3)}
     if w.kind == "whole":
         return {"opts": dtt_plan_opts_default(method=1, piece_bytes=65536, stages=3)}
     if w.K == 0:
-        return {"opts": dtt_plan_opts_default(copier_threads=256)}
+        return {"opts": dtt_plan_opts_default(method=1, piece_bytes=16384, stages=12)}
     return {}
 
 

@@ -75,6 +75,14 @@ SMALL = {
                                       rounds=3, seed=11, BM=64, BN=48, num_programs=5,
                                       tiles_per_chunk=5, group_m=2),
                            {"opts": dict(method=1, piece_bytes=8192, stages=4)}),
+    # 2D windows as tensor-map boxes: boxes taller than 256 rows are split, rows over 2 KiB
+    # go row by row, clipped edge tiles get boxes of their own shape
+    "bulk_tall_tiles": (W.Workload("tt", P=2, M=700, N=64, dtype=W.BF16, kind="tile_chunks",
+                                   rounds=2, seed=14, BM=320, BN=16, num_programs=4,
+                                   tiles_per_chunk=4), {"opts": dict(method=1)}),
+    "bulk_wide_tiles": (W.Workload("tw", P=3, M=40, N=2400, dtype=W.BF16, kind="tile_chunks",
+                                   rounds=2, seed=15, BM=16, BN=1104, num_programs=3,
+                                   tiles_per_chunk=2), {"opts": dict(method=1, piece_bytes=65536)}),
     "bulk_whole_f32": (W.small(W.C4A, M=64, N=64, rounds=3),
                        {"opts": dict(method=1, piece_bytes=4096, stages=2, copier_ctas=5)}),
     "bulk_bcast_u8": (W.Workload("bb", P=4, M=64, N=4096, dtype=W.U8, kind="whole", rounds=2,
@@ -166,6 +174,12 @@ def test_parity_c2_full_bulk_copier():
     launch = dict(runner.bench_launch(W.C2))
     launch["opts"] = D.dtt_plan_opts_default(method=D.COPY_TMA, piece_bytes=16384, stages=8)
     _run_sampled(W.C2, 3, 1 << 15, launch)
+
+
+def test_parity_c3_full_tensor_copier():
+    launch = dict(runner.bench_launch(W.C3))
+    launch["opts"] = D.dtt_plan_opts_default(method=D.COPY_TMA, piece_bytes=65536, stages=3)
+    _run_sampled(W.C3, 3, 1 << 15, launch)
 
 
 def test_bulk_copier_rejects_unaligned_regions():
