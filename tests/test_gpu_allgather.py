@@ -176,9 +176,10 @@ def test_parity_c2_full_bulk_copier():
     _run_sampled(W.C2, 3, 1 << 15, launch)
 
 
-def test_parity_c3_full_tensor_copier():
+def test_parity_c3_full_vector_copier():
+    # the bench launch moves c3's tiles as tensor-map boxes; this is the 16-byte vector path
     launch = dict(runner.bench_launch(W.C3))
-    launch["opts"] = D.dtt_plan_opts_default(method=D.COPY_TMA, piece_bytes=65536, stages=3)
+    launch["opts"] = D.dtt_plan_opts_default(method=D.COPY_VEC16, copier_threads=256)
     _run_sampled(W.C3, 3, 1 << 15, launch)
 
 
