@@ -31,6 +31,7 @@ ERROR_NAMES = {OK: "OK", EINVAL: "EINVAL", EOUTOFROWS: "EOUTOFROWS", EOVERLAP: "
                ECAPACITY: "ECAPACITY", EROUNDLIMIT: "EROUNDLIMIT", ESTATE: "ESTATE",
                EEXTRA: "EEXTRA", ETIMEDOUT: "ETIMEDOUT", ECUDA: "ECUDA", ENOMEM: "ENOMEM"}
 PREPARED, RUNNING, DONE, FAILED, CLOSING, CLOSED = range(6)
+RC_CLOSING = 1      # dtt_plan_close left the plan CLOSING (not an error)
 BF16, F32, U8 = 0, 1, 2
 DTYPE_CODES = {"bf16": BF16, "f32": F32, "u8": U8}
 COPY_VEC16, COPY_TMA = 0, 1
@@ -344,10 +345,17 @@ class Plan:
         _check(lib().dtt_plan_next_round(self._h))
         return self.round
 
-    def close(self) -> None:
+    def close(self) -> int:
+        """Close the plan.  Returns OK, or RC_CLOSING when its copier waits behind an earlier
+        plan's copier on the same copy stream: the plan is then CLOSING, closing the earlier
+        plan finishes it, and a second close() releases it."""
         if self._h and self._h.value:
-            h, self._h = self._h, C.c_void_p(0)
-            _check(lib().dtt_plan_close(h))
+            rc = lib().dtt_plan_close(self._h)
+            if rc == RC_CLOSING:
+                return rc
+            self._h = C.c_void_p(0)
+            _check(rc)
+        return OK
 
     def __enter__(self):
         return self
@@ -364,6 +372,8 @@ class Plan:
 
     @property
     def state(self) -> int:
+        if not (self._h and self._h.value):
+            return CLOSED
         return lib().dtt_plan_state(self._h)
 
     @property

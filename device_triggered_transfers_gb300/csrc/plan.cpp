@@ -66,6 +66,13 @@ struct dtt_plan {
     uint32_t round = 1;
     bool copier_launched = false;   // this round's copier is on the copy stream
 
+    // Plans sharing a copy stream ("Triggered Plans", The kernel author's contract: CLOSING):
+    // the order of this plan's last copier launch among all plans, and an event after that
+    // copier, recorded when another plan uses the same stream.
+    uint64_t launch_seq = 0;
+    cudaEvent_t ev_done = nullptr;
+    bool done_valid = false;
+
     // opts.time_copier: a ring of event pairs around the copier launches, read back lazily (when
     // a pair comes round again, or in dtt_plan_stats) so that timing adds no wait to a round
     static constexpr uint32_t kTimeRing = 64;
@@ -104,6 +111,8 @@ void free_device(dtt_plan* p) {
     cudaFree(p->d_status);
     cudaFreeHost(p->h_status);
     if (p->ev_producer) cudaEventDestroy(p->ev_producer);
+    if (p->ev_done) cudaEventDestroy(p->ev_done);
+    p->ev_done = nullptr;
     for (auto& pair : p->ev_copier)
         for (cudaEvent_t& e : pair) {
             if (e) cudaEventDestroy(e);
@@ -211,8 +220,56 @@ int read_copier_times(dtt_plan* p, uint64_t upto) {
     return DTT_OK;
 }
 
+// ---- plans sharing the device -------------------------------------------------------------
+// Live plans (created and not yet released by dtt_plan_close) and closed plans whose device
+// memory is still held: cudaFree waits for the whole device, so memory is released only while
+// no plan's copier can be spinning on a gate (a spinning copier ends only when its producer
+// runs or its polls run out).
+std::mutex g_plans_mu;
+std::vector<dtt_plan*> g_live;
+std::vector<dtt_plan*> g_retired;
+uint64_t g_launch_seq = 0;
+
+bool may_spin(const dtt_plan* q) {
+    return (q->state == DTT_PLAN_RUNNING || q->state == DTT_PLAN_CLOSING) && q->copier_launched;
+}
+
+// Is p's copier queued behind an earlier plan's copier on the same stream that has not finished?
+bool blocked_behind(const dtt_plan* p) {
+    for (const dtt_plan* q : g_live)
+        if (q != p && q->copy_stream == p->copy_stream && q->launch_seq < p->launch_seq && may_spin(q) &&
+            !(q->done_valid && cudaEventQuery(q->ev_done) == cudaSuccess))
+            return true;
+    return false;
+}
+
+// Free the device memory of retired plans once no copier can be spinning.  Holds g_plans_mu.
+void reap_locked() {
+    for (const dtt_plan* q : g_live)
+        if (may_spin(q)) return;
+    for (dtt_plan* q : g_retired) {
+        free_device(q);
+        delete q;
+    }
+    g_retired.clear();
+}
+
 // Launch this round's copier on the copy stream (bracketed by a pair of timing events when asked).
 int launch_round_copier(dtt_plan* p) {
+    bool shared = false;
+    {
+        std::lock_guard<std::mutex> lock(g_plans_mu);
+        p->launch_seq = ++g_launch_seq;
+        for (dtt_plan* q : g_live) {
+            if (q == p || q->copy_stream != p->copy_stream) continue;
+            shared = true;
+            if (may_spin(q) && !q->done_valid) {     // mark where the earlier copier ends
+                DTT_CUDA_TRY(cudaEventRecord(q->ev_done, p->copy_stream));
+                q->done_valid = true;
+            }
+        }
+    }
+    p->done_valid = false;
     cudaEvent_t* pair = nullptr;
     if (p->opts.time_copier) {
         if (p->timed_launches - p->timed_read == dtt_plan::kTimeRing) {   // the oldest pair is reused
@@ -227,6 +284,10 @@ int launch_round_copier(dtt_plan* p) {
     if (pair) {
         DTT_CUDA_TRY(cudaEventRecord(pair[1], p->copy_stream));
         ++p->timed_launches;
+    }
+    if (shared) {
+        DTT_CUDA_TRY(cudaEventRecord(p->ev_done, p->copy_stream));
+        p->done_valid = true;
     }
     p->copier_launched = true;
     return DTT_OK;
@@ -509,6 +570,10 @@ int dtt_plan_create(void* const* bufs, uint64_t buf_bytes, uint32_t P,
                     cudaStream_t copy_stream, dtt_plan** out) {
     if (!out) return fail(DTT_EINVAL, "dtt_plan_create: out is NULL");
     *out = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_plans_mu);
+        reap_locked();
+    }
     if (!bufs || P < 1 || P > DTT_MAX_RANKS || buf_bytes == 0)
         return fail(DTT_EINVAL, "dtt_plan_create: need 1 <= P <= %d buffers of a positive size", DTT_MAX_RANKS);
     dtt_plan* p = new (std::nothrow) dtt_plan();
@@ -595,7 +660,8 @@ int dtt_plan_create(void* const* bufs, uint64_t buf_bytes, uint32_t P,
     }
     if (rc == DTT_OK && cudaStreamCreateWithFlags(&p->aux_stream, cudaStreamNonBlocking) != cudaSuccess)
         rc = fail(DTT_ECUDA, "dtt_plan_create: cannot create the aux stream");
-    if (rc == DTT_OK && cudaEventCreateWithFlags(&p->ev_producer, cudaEventDisableTiming) != cudaSuccess)
+    if (rc == DTT_OK && (cudaEventCreateWithFlags(&p->ev_producer, cudaEventDisableTiming) != cudaSuccess ||
+                         cudaEventCreateWithFlags(&p->ev_done, cudaEventDisableTiming) != cudaSuccess))
         rc = fail(DTT_ECUDA, "dtt_plan_create: cannot create an event");
     if (rc != DTT_OK) {           // all or nothing: free what was prepared
         free_device(p);
@@ -603,6 +669,10 @@ int dtt_plan_create(void* const* bufs, uint64_t buf_bytes, uint32_t P,
         return rc;
     }
     p->state = DTT_PLAN_PREPARED;
+    {
+        std::lock_guard<std::mutex> lock(g_plans_mu);
+        g_live.push_back(p);
+    }
     *out = p;
     return DTT_OK;
 }
@@ -710,8 +780,57 @@ int dtt_plan_next_round(dtt_plan* p) {
     return DTT_OK;
 }
 
+namespace {
+
+// Wait for p's last copier to finish (its gates are open by now).
+int drain_copier(dtt_plan* p) {
+    if (p->aux_stream && cudaStreamSynchronize(p->aux_stream) != cudaSuccess)
+        return fail(DTT_ECUDA, "dtt_plan_close: aux stream failed");
+    if (!p->copier_launched) return DTT_OK;
+    const cudaError_t e = p->done_valid ? cudaEventSynchronize(p->ev_done) : cudaStreamSynchronize(p->copy_stream);
+    return e == cudaSuccess ? DTT_OK : fail(DTT_ECUDA, "dtt_plan_close: copy stream failed: %s", cudaGetErrorString(e));
+}
+
+// The user is done with p: drop it from the live list, free it now or when nothing spins.
+void release(dtt_plan* p) {
+    std::lock_guard<std::mutex> lock(g_plans_mu);
+    g_live.erase(std::remove(g_live.begin(), g_live.end(), p), g_live.end());
+    g_retired.push_back(p);
+    reap_locked();
+}
+
+// Finish every CLOSING plan on `stream` that no longer waits behind an earlier copier.  Their
+// gates were opened by their own close, so each copier now runs to its end.
+int finish_closing(cudaStream_t stream) {
+    int rc = DTT_OK;
+    for (bool progress = true; progress;) {
+        progress = false;
+        dtt_plan* next = nullptr;
+        {
+            std::lock_guard<std::mutex> lock(g_plans_mu);
+            for (dtt_plan* q : g_live)
+                if (q->state == DTT_PLAN_CLOSING && q->copy_stream == stream && !blocked_behind(q) &&
+                    (!next || q->launch_seq < next->launch_seq))
+                    next = q;
+        }
+        if (next) {
+            const int r = drain_copier(next);
+            if (r != DTT_OK) rc = r;
+            next->state = DTT_PLAN_CLOSED;     // released by its owner's next dtt_plan_close
+            progress = true;
+        }
+    }
+    return rc;
+}
+
+}  // namespace
+
 int dtt_plan_close(dtt_plan* p) {
     if (!p) return DTT_OK;
+    if (p->state == DTT_PLAN_CLOSED) {      // finished by the close of the plan it waited behind
+        release(p);
+        return DTT_OK;
+    }
     int rc = DTT_OK;
     if (p->state == DTT_PLAN_RUNNING) {
         // what the producers queued so far is written first; then every gate still closed is
@@ -721,16 +840,29 @@ int dtt_plan_close(dtt_plan* p) {
         if (p->n_global && launch_force_open(p->d_gates, p->d_chunks, p->n_global, p->round, p->aux_stream) != cudaSuccess)
             rc = fail(DTT_ECUDA, "dtt_plan_close: force-open launch failed");
         if (!p->copier_launched && p->n_global) {     // deferred: send the chunks now
-            if (cudaStreamSynchronize(p->aux_stream) != cudaSuccess ||
-                launch_copier(copier_params(p), p->copier_ctas, p->copier_threads, p->opts.method, p->copy_stream) != cudaSuccess)
+            if (cudaStreamSynchronize(p->aux_stream) != cudaSuccess || launch_round_copier(p) != DTT_OK)
                 rc = fail(DTT_ECUDA, "dtt_plan_close: copier launch failed");
         }
     }
-    if (p->aux_stream && cudaStreamSynchronize(p->aux_stream) != cudaSuccess) rc = fail(DTT_ECUDA, "dtt_plan_close: aux stream failed");
-    if (p->copy_stream && cudaStreamSynchronize(p->copy_stream) != cudaSuccess) rc = fail(DTT_ECUDA, "dtt_plan_close: copy stream failed");
+    if (p->state == DTT_PLAN_RUNNING || p->state == DTT_PLAN_CLOSING) {
+        bool blocked;
+        {
+            std::lock_guard<std::mutex> lock(g_plans_mu);
+            blocked = blocked_behind(p);
+        }
+        if (blocked) {                      // queued behind an earlier plan's waiting copier
+            p->state = DTT_PLAN_CLOSING;
+            return rc == DTT_OK ? DTT_CLOSING : rc;
+        }
+        const int r = drain_copier(p);
+        if (r != DTT_OK) rc = r;
+    } else if (p->aux_stream && cudaStreamSynchronize(p->aux_stream) != cudaSuccess) {
+        rc = fail(DTT_ECUDA, "dtt_plan_close: aux stream failed");
+    }
     p->state = DTT_PLAN_CLOSED;
-    free_device(p);
-    delete p;
+    const int r = finish_closing(p->copy_stream);
+    if (r != DTT_OK) rc = r;
+    release(p);
     return rc;
 }
 

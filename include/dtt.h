@@ -39,6 +39,7 @@ extern "C" {
                                         section Model and section Requirements and limits) */
 
 enum {
+    DTT_CLOSING = 1,       /* not an error: dtt_plan_close left the plan CLOSING (see there) */
     DTT_OK = 0,
     DTT_EINVAL = -1,       /* invalid argument */
     DTT_EOUTOFROWS = -2,   /* all-gather: a schedule leaves its rank's own rows
@@ -61,7 +62,8 @@ enum {
     DTT_PLAN_RUNNING = 1,  /* start() launched this round's copier */
     DTT_PLAN_DONE = 2,     /* wait() found every chunk delivered */
     DTT_PLAN_FAILED = 3,   /* wait() found extra marks or short chunks; only close() is valid */
-    DTT_PLAN_CLOSING = 4,  /* reserved (plans sharing queues) */
+    DTT_PLAN_CLOSING = 4,  /* close() opened its gates, but its copier waits behind an earlier
+                              plan's copier on the same copy stream */
     DTT_PLAN_CLOSED = 5
 };
 
@@ -286,10 +288,23 @@ int dtt_plan_wait(dtt_plan* plan, dtt_report* report);
  * already 2^32 - 1; the plan stays DONE). */
 int dtt_plan_next_round(dtt_plan* plan);
 
-/* Close and free the plan.  In the middle of a round, gates not yet open are opened so the
- * copier sends each chunk as it stands, and both streams are drained first ("Triggered
- * Plans", The kernel author's contract, close()).  Always frees; returns DTT_ECUDA if a CUDA
- * call failed on the way. */
+/* Close the plan ("Triggered Plans", The kernel author's contract, close()).  In the middle of
+ * a round, the work already queued on the producer stream finishes first, then every gate
+ * still closed is opened, so the copier sends each chunk as it stands.
+ *
+ * Plans may share a copy stream (pass the same copy_stream to dtt_plan_create).  A copier
+ * then runs only after every copier launched before it on that stream.  If this plan's
+ * copier is queued behind an earlier plan's copier that is still waiting on that plan's gates,
+ * the plan cannot finish first: close returns DTT_CLOSING at once and leaves the plan CLOSING.
+ * Closing (or waiting on) the earlier plan lets it drain; closing the earlier plan also
+ * finishes every CLOSING plan behind it, which then reads CLOSED.  Call dtt_plan_close on a
+ * CLOSING or CLOSED plan again to release it.  Plans can be closed in any order.
+ *
+ * Otherwise the plan's copier is drained and the plan released; the pointer is invalid
+ * afterwards.  Device memory is freed at once, or, while another plan's copier may still be
+ * spinning on a gate, as soon as none is (cudaFree waits for the whole device).
+ * Returns DTT_OK, DTT_CLOSING, or DTT_ECUDA if a CUDA call failed on the way (the plan is
+ * released all the same). */
 int dtt_plan_close(dtt_plan* plan);
 
 int dtt_plan_state(const dtt_plan* plan);

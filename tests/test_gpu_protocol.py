@@ -225,3 +225,76 @@ def test_allgather_from_host_buffers():
         assert st.plan.round == 3
     finally:
         st.plan.close()
+
+
+# ---- plans sharing a copy stream ("Triggered Plans", The kernel author's contract: a plan
+# whose copies wait behind an earlier plan's waiting copies cannot finish first) -------------
+def _round1_everywhere(st, w):
+    o = oracle_plan(w)
+    assert oracle_round(o, w)[0] == OP.OK
+    for q in range(w.P):
+        np.testing.assert_array_equal(st.bufs[q].cpu().numpy(), o.bufs[q], err_msg=f"buffer {q}")
+
+
+def test_close_behind_an_earlier_waiting_plan_leaves_it_closing():
+    import time
+    copy = torch.cuda.Stream()
+    A = runner.make(WS, copy_stream=copy)
+    B = runner.make(WS, copy_stream=copy, fill_byte=7)
+    try:
+        hA = A.plan.start(A.producer_stream)       # A's copier waits for A's producer
+        hB = B.plan.start(B.producer_stream)       # B's copier is queued behind it
+        D.dtt_fill_producer(B.buf_ptrs, B.desc, hB, B.producer_stream)
+        t0 = time.perf_counter()
+        assert B.plan.close() == D.RC_CLOSING      # returns at once, B cannot finish first
+        assert time.perf_counter() - t0 < 1.0
+        assert B.plan.state == D.CLOSING
+        D.dtt_fill_producer(A.buf_ptrs, A.desc, hA, A.producer_stream)
+        assert A.plan.close() == D.OK              # closing A finishes both
+        assert B.plan.state == D.CLOSED
+        _round1_everywhere(A, WS)
+        _round1_everywhere(B, WS)
+        assert B.plan.close() == D.OK              # releases B
+        assert B.plan.state == D.CLOSED
+    finally:
+        A.plan.close()
+        B.plan.close()
+
+
+def test_closing_the_earlier_plan_does_not_wait_for_a_later_one():
+    import time
+    copy = torch.cuda.Stream()
+    A = runner.make(WS, copy_stream=copy)
+    B = runner.make(WS, copy_stream=copy)
+    try:
+        hA = A.plan.start(A.producer_stream)
+        hB = B.plan.start(B.producer_stream)       # B's producer has not run yet
+        D.dtt_fill_producer(A.buf_ptrs, A.desc, hA, A.producer_stream)
+        t0 = time.perf_counter()
+        assert A.plan.close() == D.OK              # drains A's copier only
+        assert time.perf_counter() - t0 < 1.0
+        D.dtt_fill_producer(B.buf_ptrs, B.desc, hB, B.producer_stream)
+        rep = B.plan.wait()
+        assert rep.status == D.OK and rep.copier_timeouts == 0
+        _round1_everywhere(B, WS)
+        B.plan.next_round()
+        assert runner.run_round(B).status == D.OK  # B goes on alone
+    finally:
+        A.plan.close()
+        B.plan.close()
+
+
+def test_nested_plans_close_in_with_blocks():
+    copy = torch.cuda.Stream()
+    A = runner.make(WS, copy_stream=copy)
+    B = runner.make(WS, copy_stream=copy)
+    with A.plan:
+        hA = A.plan.start(A.producer_stream)
+        with B.plan:
+            hB = B.plan.start(B.producer_stream)
+            D.dtt_fill_producer(B.buf_ptrs, B.desc, hB, B.producer_stream)
+        assert B.plan.state == D.CLOSING           # left the inner block behind A's copier
+        D.dtt_fill_producer(A.buf_ptrs, A.desc, hA, A.producer_stream)
+    assert B.plan.state == D.CLOSED                # the outer block's close finished it
+    _round1_everywhere(B, WS)
+    assert B.plan.close() == D.OK
