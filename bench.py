@@ -35,7 +35,9 @@ DEFAULT_CONFIG = W.C2.name
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of the named kernel from one ncu capture
 # of the same workload and launch configuration (the summaries under profiles/); absent until
 # taken, and dropped once the kernel changes.
-NCU_TRAFFIC = {("c2_chunks_p4", "copier_bulk_kernel"): 473749760}
+NCU_TRAFFIC = {("c2_chunks_p4", "copier_bulk_kernel"): 473749760,
+               # captured with 2000 rows per rank (--rows 2000) and scaled by the rows, 4x
+               ("c3_tiles_p8", "copier_bulk_kernel"): 8018596000}
 
 
 def describe(w, launch, copier=None) -> str:
@@ -222,11 +224,17 @@ def barrier(world: int):
 
 
 # ---- the two arms ------------------------------------------------------------------------------------
+def workload(args):
+    """The workload named by --config, with --rows rows per rank when given."""
+    w = W.CONFIGS[args.config]
+    return W.small(w, M=args.rows, name=f"{w.name}_rows{args.rows}") if args.rows else w
+
+
 def run_reference(args):
     world, rank, _ = dist_env()
     if world > 1 and rank != 0:
         return 0
-    w = W.CONFIGS[args.config]
+    w = workload(args)
     sw, what = oracle_sample_workload(w)
     from oracle.run import make_plan as oracle_plan, run_round as oracle_round
     o = oracle_plan(sw)
@@ -263,7 +271,7 @@ def run_ours(args):
     import device_triggered_transfers_gb300 as D
     from device_triggered_transfers_gb300 import runner
 
-    w = W.CONFIGS[args.config]
+    w = workload(args)
     launch = dict(runner.bench_launch(w))
     # the copier runs on a stream the bench can put events on
     copy_stream = torch.cuda.Stream(priority=-1)
@@ -280,10 +288,9 @@ def run_ours(args):
         A, Bt = W.gemm_inputs(w.P, w.M, w.N, w.K, w.seed)
         st = runner.make_gemm(w, A, Bt, opts=opts, copy_stream=copy_stream)
         w_sched = st.w
-        offs = [w.slice_offset(r) for r in range(w.P)]
 
         def produce(h):
-            D.dtt_gemm_producer(st.A, st.Bt, st.bufs, w.M, w.N, w.K, w.row_bytes, offs,
+            D.dtt_gemm_producer(st.A, st.Bt, st.buf_ptrs, w.M, w.N, w.K, w.row_bytes, st.slice_offs,
                                 st.num_programs, h, st.err, prod)
     else:
         st = runner.make(w, opts=opts, copy_stream=copy_stream, **launch)
@@ -446,10 +453,12 @@ def run_ours(args):
         flops = 2.0 * w.P * w.M * w.N * w.K
         tf_peak, tf_kind = load_tensor_peak()
         prod_s = producer_ms / 1e3
-        roofline = {"kernel": "gemm_producer_kernel", "bound": "tensor",
+        gname = "gemm2_producer_kernel" if (w.M % 256 == 0 and w.N % 256 == 0 and st.num_programs >= 2) \
+            else "gemm_producer_kernel"
+        roofline = {"kernel": gname, "bound": "tensor",
                     "achieved": flops / prod_s / 1e12, "peak": tf_peak, "peak_kind": tf_kind,
                     "unit": "TFLOP/s", "frac": flops / prod_s / 1e12 / tf_peak,
-                    "traffic": NCU_TRAFFIC.get((w.name, "gemm_producer_kernel")),
+                    "traffic": NCU_TRAFFIC.get((w.name, gname)),
                     "flops_per_launch": flops}
     else:
         roofline = copier_roof
@@ -546,6 +555,9 @@ def main(argv=None):
     ap.add_argument("--isolated-rounds", type=int, default=20)
     ap.add_argument("--barrier", action="store_true",
                     help="time the N-rank barrier and the builtin reveal instead")
+    ap.add_argument("--rows", type=int, default=0,
+                    help="rows per rank instead of the workload's (a smaller case of the same "
+                         "shape, for profiler captures; the default runs the workload as named)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3

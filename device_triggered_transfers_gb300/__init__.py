@@ -494,6 +494,6 @@ def dtt_barrier_reveal_noalloc(x, data, y, size: int, max_polls: int, status, st
 def dtt_gemm_producer(A, Bt, bufs, M: int, N: int, K: int, ldc: int, slice_offs, num_programs: int,
                       handles, err, stream=None) -> None:
     """C_r = A_r . B for every rank (tcgen05 GEMM), marking each tile's chunk; see dtt.h."""
-    offs = (C.c_uint64 * len(bufs))(*slice_offs)
+    offs = slice_offs if isinstance(slice_offs, C.Array) else (C.c_uint64 * len(bufs))(*slice_offs)
     _check(lib().dtt_gemm_producer(_ptr(A), _ptr(Bt), _ptr_array(bufs), len(bufs), M, N, K, ldc, offs,
                                    num_programs, handles, _ptr(err), _stream(stream)))

@@ -15,7 +15,9 @@
 // Two TMEM accumulators (2 x TN columns) let the MMA warp start the next block while the
 // epilogue drains the previous one; the epilogue marks each 128 x 128 tile of a block.  Every wait is bounded; on a timeout the CTA records an
 // error, lets its copies and MMAs finish (bounded), frees its TMEM and returns.
+#include <algorithm>
 #include <cstdint>
+#include <mutex>
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -32,7 +34,7 @@ constexpr uint32_t ACC_BUFS = 2;
 constexpr uint32_t EPI_THREADS = 128;
 constexpr uint32_t THREADS = EPI_THREADS + 64;       // + TMA warp + MMA warp
 constexpr uint32_t TMA_WARP = 4, MMA_WARP = 5;
-constexpr uint32_t WAIT_LIMIT = 1u << 26;
+constexpr uint32_t WAIT_LIMIT = 1u << 22;
 
 // One MMA covers TN columns: TN / 128 adjacent marked tiles of one tile row.  TN = 256 halves the
 // shared-memory traffic per FLOP for A (the 128 x 128 form needs ~112 B/clk of operand reads per
@@ -307,6 +309,229 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_producer_kernel(const __grid_
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS) : "memory");
 }
 
+// ---- the 2-CTA form -------------------------------------------------------------------------
+// A cluster of two CTAs on two SMs computes 256 x 256 blocks with tcgen05.mma.cta_group::2
+// (M = 256, N = 256): each CTA holds its 128 rows of A and its 128 columns of B^T per stage, so a
+// CTA moves 32 KiB per k-block instead of the 48 KiB the one-CTA 128 x 256 form needs, and each
+// CTA's TMEM receives its own 128 rows of the block.  One thread of the even CTA (the leader)
+// issues every MMA; the leader's mbarriers count both CTAs' loads (as bytes) and both
+// epilogues, and the MMA's completions are multicast to both CTAs.
+constexpr uint32_t G2_TN = 256;                       // block columns (B^T rows) per MMA
+constexpr uint32_t G2_BHALF = BN * BK * 2;            // 16 KiB: this CTA's 128 rows of B^T
+constexpr uint32_t G2_STAGES = 6;
+constexpr uint32_t G2_TMEM_COLS = ACC_BUFS * G2_TN;   // 512 fp32 columns
+constexpr uint32_t G2_SMEM = 1024 + G2_STAGES * (A_STAGE + G2_BHALF) + 256;
+constexpr uint32_t G2_IDESC = (1u << 4) | (1u << 7) | (1u << 10) | ((G2_TN >> 3) << 17) | ((256u >> 4) << 24);
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// The shared::cluster address of the same shared-memory offset in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t at_rank(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+
+__device__ __forceinline__ void bar_arrive_at(uint32_t cluster_bar) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
+}
+
+// A tile load into this CTA's shared memory that completes on the leader's mbarrier.
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, int32_t x, int32_t y,
+                                                 uint32_t cluster_bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.cta_group::2 "
+        "[%0], [%1, {%2, %3}], [%4];"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(cluster_bar) : "memory");
+}
+
+__device__ __forceinline__ void umma_pair(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                          uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(accumulate) : "memory");
+}
+
+// Arrive once on the mbarrier at this offset in both CTAs when the MMAs issued so far finish.
+__device__ __forceinline__ void umma_commit_both(uint32_t bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
+        ::"r"(bar), "h"((uint16_t)0x3) : "memory");
+}
+
+__device__ __forceinline__ void umma_commit_local2(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                 ::"r"(bar) : "memory");
+}
+
+// Cluster c of NC takes units c, c + NC, ... of rank 0, then of rank 1, and so on; a unit is a
+// 256 x 256 block, CTA q of the pair owns its rows 128 q .. 128 q + 127.  Tile (tm, tn) is step
+// tm * tiles_n + tn of its rank and, once stored, gets one mark on chunk first_chunk + step / NP.
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
+gemm2_producer_kernel(const __grid_constant__ GemmParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sA = smem;
+    uint8_t* sB = smem + G2_STAGES * A_STAGE;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sB + G2_STAGES * G2_BHALF);
+    uint64_t* full = bars;                        // [STAGES]  leader: both CTAs' loads -> MMA
+    uint64_t* empty = bars + G2_STAGES;           // [STAGES]  each CTA: MMA -> its TMA warp
+    uint64_t* acc_full = bars + 2 * G2_STAGES;    // [2]       each CTA: MMA -> its epilogue
+    uint64_t* acc_empty = acc_full + ACC_BUFS;    // [2]       leader: both epilogues -> MMA
+    uint64_t* drain = acc_empty + ACC_BUFS;       // [1]       leader: MMA teardown
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile uint32_t* abort_flag = tmem_slot + 1;
+
+    const uint32_t warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const uint32_t q = cluster_rank();
+    const bool leader = q == 0;
+    if (threadIdx.x == 0) {
+        for (uint32_t i = 0; i < G2_STAGES; ++i) {
+            bar_init(saddr(full + i), 1);            // the leader's expect_tx covers both CTAs' bytes
+            bar_init(saddr(empty + i), 1);
+        }
+        for (uint32_t i = 0; i < ACC_BUFS; ++i) {
+            bar_init(saddr(acc_full + i), 1);
+            bar_init(saddr(acc_empty + i), 2);       // one arrival per CTA's epilogue
+        }
+        bar_init(saddr(drain), 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;"
+                     ::"r"(saddr(tmem_slot)), "r"(G2_TMEM_COLS) : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    cluster_sync_all();          // both CTAs' barriers exist before either arrives remotely
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    const uint32_t tiles_n = p.N / BN, units_n = p.N / G2_TN, units = (p.M / 256) * units_n;
+    const uint32_t kblocks = p.K / BK;
+    const uint32_t c0 = blockIdx.x / 2, NC = gridDim.x / 2;
+    const uint32_t peer_abort = at_rank(saddr(tmem_slot + 1), q ^ 1);
+    auto fail = [&]() {
+        *abort_flag = 1;
+        asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(peer_abort), "r"(1u) : "memory");
+        atomicAdd(p.err, 1u);
+    };
+
+    if (warp == TMA_WARP) {
+        if (lane == 0) {
+            uint32_t stage = 0, phase = 0, issued = 0;
+            bool ok = true;
+            for (uint32_t r = 0; r < p.P && ok; ++r)
+                for (uint32_t u = c0; u < units && ok; u += NC) {
+                    const int32_t row_a = (int32_t)(r * p.M + (u / units_n) * 256 + q * BM);
+                    const int32_t row_b = (int32_t)((u % units_n) * G2_TN + q * BN);
+                    for (uint32_t kb = 0; kb < kblocks; ++kb) {
+                        if (!bar_wait(saddr(empty + stage), phase ^ 1, abort_flag)) { fail(); ok = false; break; }
+                        // The peer's loads may land before the leader's expect_tx (the barrier's
+                        // transaction count goes below zero for a while), but never a phase
+                        // early: its stage is free only once the MMA has consumed that stage.
+                        const uint32_t fb = at_rank(saddr(full + stage), 0);
+                        if (leader) bar_expect_tx(saddr(full + stage), 2 * (A_STAGE + G2_BHALF));
+                        tma_load_2d_pair(saddr(sA + stage * A_STAGE), &p.tmA, (int32_t)(kb * BK), row_a, fb);
+                        tma_load_2d_pair(saddr(sB + stage * G2_BHALF), &p.tmB, (int32_t)(kb * BK), row_b, fb);
+                        ++issued;
+                        if (++stage == G2_STAGES) { stage = 0; phase ^= 1; }
+                    }
+                }
+            // the leader's full barriers count both CTAs' loads: once its last phases complete,
+            // every load of the pair has landed
+            if (leader) {
+                volatile uint32_t never = 0;
+                for (uint32_t i = issued > G2_STAGES ? issued - G2_STAGES : 0; i < issued; ++i)
+                    (void)bar_wait(saddr(full + i % G2_STAGES), (i / G2_STAGES) & 1, &never);
+            }
+        }
+    } else if (warp == MMA_WARP) {
+        if (lane == 0 && leader) {
+            uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+            bool ok = true;
+            for (uint32_t r = 0; r < p.P && ok; ++r)
+                for (uint32_t u = c0; u < units && ok; u += NC) {
+                    if (!bar_wait(saddr(acc_empty + acc), acc_phase ^ 1, abort_flag)) { fail(); ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t d_tmem = tmem_base + acc * G2_TN;
+                    for (uint32_t kb = 0; kb < kblocks; ++kb) {
+                        if (!bar_wait(saddr(full + stage), phase, abort_flag)) { fail(); ok = false; break; }
+                        tc_fence_after();
+                        const uint64_t da = smem_desc(saddr(sA + stage * A_STAGE));
+                        const uint64_t db = smem_desc(saddr(sB + stage * G2_BHALF));
+#pragma unroll
+                        for (uint32_t k = 0; k < BK / UMMA_K; ++k)
+                            umma_pair(d_tmem, da + 2 * k, db + 2 * k, G2_IDESC, (kb | k) != 0);
+                        umma_commit_both(saddr(empty + stage));   // both CTAs' stages are free
+                        if (++stage == G2_STAGES) { stage = 0; phase ^= 1; }
+                    }
+                    if (!ok) break;
+                    umma_commit_both(saddr(acc_full + acc));      // the block is in both TMEMs
+                    if (++acc == ACC_BUFS) { acc = 0; acc_phase ^= 1; }
+                }
+            // every MMA has finished before either CTA releases TMEM or shared memory
+            umma_commit_local2(saddr(drain));
+            volatile uint32_t never = 0;
+            (void)bar_wait(saddr(drain), 0, &never);
+        }
+    } else {
+        // epilogue warps 0..3: thread t of warp w owns row 32w + t of this CTA's 128 rows
+        uint32_t acc = 0, acc_phase = 0;
+        const uint32_t row_in_tile = warp * 32 + lane;
+        bool ok = true;
+        for (uint32_t r = 0; r < p.P && ok; ++r)
+            for (uint32_t u = c0; u < units && ok; u += NC) {
+                bool mine = bar_wait(saddr(acc_full + acc), acc_phase, abort_flag);
+                if (!mine) fail();
+                if (!epi_all(mine && !*abort_flag)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t tm = (u / units_n) * 2 + q, tn0 = (u % units_n) * (G2_TN / BN);
+                char* crow = p.bufs[r] + p.slice_off[r] + (uint64_t)(tm * BM + row_in_tile) * p.ldc +
+                             (uint64_t)tn0 * BN * 2;
+                const uint32_t taddr = tmem_base + ((warp * 32u) << 16) + acc * G2_TN;
+#pragma unroll 1
+                for (uint32_t g = 0; g < G2_TN / 32; ++g) {
+                    uint32_t v[32];
+                    tmem_ld32(taddr + g * 32, v);
+                    uint4* dst = reinterpret_cast<uint4*>(crow + g * 64);
+#pragma unroll
+                    for (uint32_t j = 0; j < 4; ++j)
+                        dst[j] = make_uint4(pack_bf16x2(v[8 * j + 0], v[8 * j + 1]), pack_bf16x2(v[8 * j + 2], v[8 * j + 3]),
+                                            pack_bf16x2(v[8 * j + 4], v[8 * j + 5]), pack_bf16x2(v[8 * j + 6], v[8 * j + 7]));
+                }
+                tc_fence_before();
+                // every TMEM read and store of this CTA's rows precedes one arrival at the leader
+                // (the accumulator may be overwritten) and one mark per tile
+                asm volatile("bar.sync 1, %0;" ::"n"(EPI_THREADS) : "memory");
+                if (threadIdx.x == 0) {
+                    bar_arrive_at(at_rank(saddr(acc_empty + acc), 0));
+                    for (uint32_t k = 0; k < G2_TN / BN; ++k)
+                        dtt_dev::mark_one(p.h[r], p.h[r].first_chunk + (tm * tiles_n + tn0 + k) / p.NP);
+                }
+                if (++acc == ACC_BUFS) { acc = 0; acc_phase ^= 1; }
+            }
+    }
+    tc_fence_before();
+    cluster_sync_all();          // no CTA leaves while the pair's MMAs or loads may touch it
+    tc_fence_after();
+    if (warp == 0)
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(G2_TMEM_COLS)
+                     : "memory");
+}
+
 // A 2D bf16 K-major operand: rows x K elements, box 64 (K) x box_rows, 128-byte swizzle.
 bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t K, uint32_t box_rows) {
     auto fn = tensor_map_encoder();
@@ -318,6 +543,40 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t K, uint3
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The operands' tensor maps depend only on their addresses and shapes, so the last few are kept
+// and a repeated launch (every round of a plan) skips the encoding on the host.
+struct MapCacheEntry {
+    const void* A;
+    const void* Bt;
+    uint64_t rows_a, N, K;
+    uint32_t TN;
+    CUtensorMap tmA, tmB;
+};
+std::mutex g_map_mu;
+MapCacheEntry g_map_cache[8];
+uint32_t g_map_used = 0, g_map_next = 0;
+
+bool operand_maps(const void* A, const void* Bt, uint64_t rows_a, uint64_t N, uint64_t K, uint32_t TN,
+                  CUtensorMap* tmA, CUtensorMap* tmB) {
+    std::lock_guard<std::mutex> lock(g_map_mu);
+    for (uint32_t i = 0; i < g_map_used; ++i) {
+        const MapCacheEntry& e = g_map_cache[i];
+        if (e.A == A && e.Bt == Bt && e.rows_a == rows_a && e.N == N && e.K == K && e.TN == TN) {
+            *tmA = e.tmA;
+            *tmB = e.tmB;
+            return true;
+        }
+    }
+    MapCacheEntry e{A, Bt, rows_a, N, K, TN, {}, {}};
+    if (!make_map(&e.tmA, A, rows_a, K, BM) || !make_map(&e.tmB, Bt, N, K, TN)) return false;
+    g_map_cache[g_map_next] = e;
+    g_map_next = (g_map_next + 1) % 8;
+    if (g_map_used < 8) ++g_map_used;
+    *tmA = e.tmA;
+    *tmB = e.tmB;
+    return true;
 }
 
 }  // namespace
@@ -334,6 +593,9 @@ static cudaError_t prepare_gemm() {
 cudaError_t preload_gemm_kernels() {
     cudaError_t e = prepare_gemm<128>();
     if (e == cudaSuccess) e = prepare_gemm<256>();
+    if (e == cudaSuccess) e = prepare_kernel(gemm2_producer_kernel);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(gemm2_producer_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)G2_SMEM);
     return e;
 }
 
@@ -354,8 +616,10 @@ extern "C" int dtt_gemm_producer(const void* A, const void* Bt, void* const* buf
     if (reinterpret_cast<uintptr_t>(A) % 16 || reinterpret_cast<uintptr_t>(Bt) % 16)
         return fail(DTT_EINVAL, "dtt_gemm_producer: operands must be 16-byte aligned");
     const uint32_t TN = (N % 256 == 0) ? 256 : 128;   // widest MMA block that tiles N
+    // the 2-CTA form when the blocks tile both M and N and the launch can hold a CTA pair
+    const bool pair = M % 256 == 0 && N % 256 == 0 && num_programs >= 2;
     GemmParams gp{};
-    if (!make_map(&gp.tmA, A, (uint64_t)P * M, K, BM) || !make_map(&gp.tmB, Bt, N, K, TN))
+    if (!operand_maps(A, Bt, (uint64_t)P * M, N, K, pair ? BN : TN, &gp.tmA, &gp.tmB))
         return fail(DTT_ECUDA, "dtt_gemm_producer: cannot encode the tensor maps");
     for (uint32_t r = 0; r < P; ++r) {
         if (!bufs[r] || (reinterpret_cast<uintptr_t>(bufs[r]) + slice_off[r]) % 16)
@@ -371,7 +635,20 @@ extern "C" int dtt_gemm_producer(const void* A, const void* Bt, void* const* buf
     gp.K = K;
     gp.NP = num_programs;
     gp.err = err;
-    if (TN == 256)
+    if (pair) {
+        // a persistent grid: no more CTA pairs than can be resident at once
+        cudaLaunchConfig_t cfg{};
+        cfg.gridDim = dim3(2 * (num_programs / 2), 1, 1);
+        cfg.blockDim = dim3(THREADS, 1, 1);
+        cfg.dynamicSmemBytes = G2_SMEM;
+        cfg.stream = stream;
+        int fit = 0;
+        cudaError_t e = cudaOccupancyMaxActiveClusters(&fit, gemm2_producer_kernel, &cfg);
+        if (e != cudaSuccess || fit < 1)
+            return fail(DTT_ECUDA, "dtt_gemm_producer: no CTA pair fits (%s)", cudaGetErrorString(e));
+        const uint32_t pairs = std::min<uint32_t>(num_programs / 2, (uint32_t)fit);
+        gemm2_producer_kernel<<<2 * pairs, THREADS, G2_SMEM, stream>>>(gp);
+    } else if (TN == 256)
         gemm_producer_kernel<256><<<num_programs, THREADS, Cfg<256>::SMEM_BYTES, stream>>>(gp);
     else
         gemm_producer_kernel<128><<<num_programs, THREADS, Cfg<128>::SMEM_BYTES, stream>>>(gp);

@@ -148,6 +148,8 @@ class GemmSetup:
     err: torch.Tensor
     producer_stream: torch.cuda.Stream
     num_programs: int
+    buf_ptrs: object = None           # the buffers' addresses and slice offsets, marshalled once
+    slice_offs: object = None
 
 
 def make_gemm(w, A, Bt, opts=None, num_programs: Optional[int] = None, copy_stream=None) -> GemmSetup:
@@ -166,8 +168,11 @@ def make_gemm(w, A, Bt, opts=None, num_programs: Optional[int] = None, copy_stre
     plan = Plan(bufs, w.buf_bytes, scheds, opts, copy_stream=copy_stream)
     for s in scheds:
         s.free()
+    import ctypes
+    offs = (ctypes.c_uint64 * w.P)(*[w.slice_offset(r) for r in range(w.P)])
     st = GemmSetup(w, bufs, plan, A.to("cuda").contiguous(), Bt.to("cuda").contiguous(),
-                   torch.zeros(1, dtype=torch.int32, device="cuda"), torch.cuda.Stream(), NP)
+                   torch.zeros(1, dtype=torch.int32, device="cuda"), torch.cuda.Stream(), NP,
+                   pointer_array(bufs), offs)
     torch.cuda.synchronize()
     return st
 
@@ -176,7 +181,6 @@ def run_gemm_round(st: GemmSetup, raise_on_error: bool = True):
     from . import dtt_gemm_producer
     w = st.w
     handles = st.plan.start(st.producer_stream)
-    dtt_gemm_producer(st.A, st.Bt, st.bufs, w.M, w.N, w.K, w.row_bytes,
-                      [w.slice_offset(r) for r in range(w.P)], st.num_programs, handles, st.err,
-                      st.producer_stream)
+    dtt_gemm_producer(st.A, st.Bt, st.buf_ptrs, w.M, w.N, w.K, w.row_bytes, st.slice_offs,
+                      st.num_programs, handles, st.err, st.producer_stream)
     return st.plan.wait(raise_on_error=raise_on_error)

@@ -58,8 +58,11 @@ def _check(st, A, Bt, rows=None):
         assert err < 5e-3          # bf16 output rounding alone is about 2e-3
 
 
-@pytest.mark.parametrize("P,M,N,K,NP", [(2, 256, 384, 512, 5), (3, 128, 128, 64, 1),
-                                        (2, 384, 256, 1024, 4)])
+@pytest.mark.parametrize("P,M,N,K,NP", [
+    # one-CTA form (M or N not a multiple of 256, or a single program)
+    (2, 256, 384, 512, 5), (3, 128, 128, 64, 1), (2, 384, 256, 1024, 4),
+    # CTA-pair form: one k-block, an odd program count, an idle pair, a single pair
+    (1, 256, 256, 64, 2), (2, 768, 768, 192, 5), (3, 512, 256, 256, 8), (2, 256, 512, 512, 2)])
 def test_gemm_producer_small(P, M, N, K, NP):
     w = W.Workload("g", P=P, M=M, N=N, dtype=W.BF16, kind="tile_chunks", rounds=2, seed=31 + M,
                    BM=128, BN=128, num_programs=NP, tiles_per_chunk=NP, K=K)
