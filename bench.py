@@ -37,7 +37,8 @@ DEFAULT_CONFIG = W.C2.name
 # taken, and dropped once the kernel changes.
 NCU_TRAFFIC = {("c2_chunks_p4", "copier_bulk_kernel"): 473749760,
                # captured with 2000 rows per rank (--rows 2000) and scaled by the rows, 4x
-               ("c3_tiles_p8", "copier_bulk_kernel"): 8018596000}
+               ("c3_tiles_p8", "copier_bulk_kernel"): 8018596000,
+               ("c5_gemm_p4", "gemm2_producer_kernel"): 166012672}
 
 
 def describe(w, launch, copier=None) -> str:
