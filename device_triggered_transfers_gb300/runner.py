@@ -61,6 +61,14 @@ def producer_desc(w, cluster: int = 1, programs: Optional[int] = None, threads: 
     if w.kind == "whole":
         NP = w.num_programs
         BM = -(-w.M // NP)
+        if group > 1:
+            # each program is a group of CTAs that marks its one step once: the same NP marks as
+            # one mark per program at the end, when every program has exactly one step
+            if -(-w.M // BM) != NP:
+                raise ValueError("group writers on whole() need one step per program")
+            return fill_desc(w.dtype, w.seed, w.M, w.N, w.row_bytes, w.buf_bytes, slice_offs, BM, w.N, NP, NP,
+                             mark_mode=MARK_PER_STEP, cluster=1, rank_mask=mask, threads=threads,
+                             group=group, group_counters=counters)
         return fill_desc(w.dtype, w.seed, w.M, w.N, w.row_bytes, w.buf_bytes, slice_offs, BM, w.N, NP, 1,
                          mark_mode=MARK_AT_END, cluster=1, rank_mask=mask, threads=threads)
     if w.kind == "chunks":
@@ -124,7 +132,8 @@ def bench_launch(w) -> dict:
     producer keeps the SM's threads and registers), and one program per rank made of a group of
     38 CTAs (152 in all, one per SM) that writes the rank's chunks in order and marks each once,
     so every rank's chunk k opens in wave k and the copier follows the waves.
-    whole(): the bulk-copy copier over the contiguous slices.
+    whole(): the bulk-copy copier over the contiguous slices; the single chunk per rank opens only
+    when the whole slice is written, so the fill gets as many CTAs as the writers allow.
     tile_chunks (fill producer): the bulk-copy copier moving each tile as tensor-map boxes of
     16 KiB, twelve in flight per SM.  The GEMM producer keeps the vector copier: its own
     shared-memory ring leaves no room for a bulk-copy ring on the same SM."""
@@ -132,7 +141,14 @@ def bench_launch(w) -> dict:
         return {"group": 38, "programs": 1, "threads": 256,
                 "opts": dtt_plan_opts_default(method=1, piece_bytes=65536, stages=3)}
     if w.kind == "whole":
-        return {"opts": dtt_plan_opts_default(method=1, piece_bytes=65536, stages=3)}
+        opts = dtt_plan_opts_default(method=1, piece_bytes=65536, stages=3)
+        NP = w.num_programs
+        if -(-w.M // -(-w.M // NP)) == NP:
+            # one step per program: each writer becomes a group of CTAs (up to 8, enough to
+            # cover the SMs) that marks the chunk once
+            g = max(1, min(8, 152 // (len(w.senders()) * NP)))
+            return {"group": g, "threads": 512, "opts": opts}
+        return {"threads": 1024, "opts": opts}
     if w.K == 0:
         return {"opts": dtt_plan_opts_default(method=1, piece_bytes=16384, stages=12)}
     return {}

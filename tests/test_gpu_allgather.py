@@ -96,6 +96,9 @@ SMALL = {
     "tiles_group3": (W.Workload("tg", P=3, M=300, N=200, dtype=W.BF16, kind="tile_chunks",
                                 rounds=3, seed=13, BM=64, BN=48, num_programs=5,
                                 tiles_per_chunk=5, group_m=2), {"group": 3}),
+    "whole_f32_8writers_group4": (W.small(W.C4A, M=64, N=64, rounds=3),
+                                  {"group": 4, "opts": dict(method=1, piece_bytes=4096, stages=4)}),
+    "whole_1writer_group16": (W.small(W.C1, M=200), {"group": 16, "threads": 512}),
 }
 
 
@@ -114,6 +117,11 @@ def test_parity_c1_full():
 def test_parity_c4a_full_stale_data_check():
     # 8 writers on one 4 MiB gate per rank, values change every round: a stale copy fails
     run_parity(W.C4A, W.C4A.rounds)
+
+
+def test_parity_c4a_full_bench_launch():
+    # the benchmark's launch: each of the 8 writers is a group of CTAs marking once
+    run_parity(W.C4A, 4, **runner.bench_launch(W.C4A))
 
 
 def _run_sampled(w, rounds, n_samples, launch):
