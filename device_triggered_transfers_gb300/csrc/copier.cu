@@ -42,6 +42,13 @@ __device__ __forceinline__ uint8_t ld_cg8(const uint8_t* p) {
 
 // Copy one piece from buffer s to every other buffer: 16-byte vectors, kUnroll loads in
 // flight per thread, each value stored to all peers.
+// Tell the host through mapped memory that chunk c has reached every peer this round (the
+// gpu-scope arrival adds above it are ordered before this system-scope release).
+__device__ __forceinline__ void notify_host(const CopierParams& p, uint32_t c) {
+    if (p.host_arrived)
+        asm volatile("st.release.sys.global.u32 [%0], %1;" ::"l"(p.host_arrived + c), "r"(p.round) : "memory");
+}
+
 __device__ __forceinline__ void copy_piece_vec(const CopierParams& p, uint32_t s,
                                                const PieceDesc& pc) {
     const uint32_t rv = pc.row_bytes >> 4;
@@ -151,6 +158,7 @@ __global__ void __launch_bounds__(1024) copier_kernel(const __grid_constant__ Co
                     dtt_dev::red_release_add(prow + DTT_GATE_ARRIVAL, 1);
                 }
                 dtt_dev::red_release_add(row + DTT_GATE_COMPLETION, p.P - 1);
+                notify_host(p, c);
             }
         }
     }
@@ -335,6 +343,7 @@ __global__ void __launch_bounds__(32) copier_bulk_kernel(const __grid_constant__
                 dtt_dev::red_release_add(prow + DTT_GATE_ARRIVAL, 1);
             }
             dtt_dev::red_release_add(row + DTT_GATE_COMPLETION, p.P - 1);
+            notify_host(p, c);
         }
     }
     // leave nothing in flight: stores, and (after a failed wait) loads still landing in the ring

@@ -108,6 +108,7 @@ struct CopierParams {
     uint64_t max_polls;
     uint32_t stage_bytes;       // bulk-copy path: bytes per shared-memory stage (>= a piece, 128-aligned)
     uint32_t stages;            // bulk-copy path: stages in the ring
+    uint32_t* host_arrived;     // or null: mapped host words, word c = round once chunk c reached every peer
 };
 
 struct CheckParams {

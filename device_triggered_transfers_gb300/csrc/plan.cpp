@@ -56,6 +56,17 @@ struct dtt_plan {
     uint8_t* h_flags = nullptr;       // the flag bytes right after it
     uint32_t wait_seq = 0;            // sequence number of the last check launched
 
+    // host-buffer rounds (dtt_allgather_host): the copier stamps each chunk's arrival into
+    // mapped host words, the host copies the gathered bytes back as they arrive
+    uint32_t* h_arrived = nullptr;    // pinned, mapped: [n_global], word c = round of c's last arrival
+    uint32_t* h_arrived_dev = nullptr;
+    bool notify_host = false;         // the next copier launch stamps h_arrived
+    cudaEvent_t ev_copier_end = nullptr;   // after that launch: the copier has exited
+    cudaEvent_t ev_h2d = nullptr;
+    std::vector<cudaEvent_t> ev_pieces;   // one per host-to-device piece of the output rank's slice
+    cudaStream_t h2d_stream = nullptr;
+    cudaStream_t d2h_stream = nullptr;
+
     cudaStream_t copy_stream = nullptr;
     bool own_copy_stream = false;
     cudaStream_t aux_stream = nullptr;
@@ -113,6 +124,19 @@ void free_device(dtt_plan* p) {
     if (p->ev_producer) cudaEventDestroy(p->ev_producer);
     if (p->ev_done) cudaEventDestroy(p->ev_done);
     p->ev_done = nullptr;
+    if (p->ev_copier_end) cudaEventDestroy(p->ev_copier_end);
+    if (p->ev_h2d) cudaEventDestroy(p->ev_h2d);
+    for (cudaEvent_t e : p->ev_pieces) cudaEventDestroy(e);
+    p->ev_pieces.clear();
+    if (p->d2h_stream) cudaStreamDestroy(p->d2h_stream);
+    if (p->h2d_stream) cudaStreamDestroy(p->h2d_stream);
+    p->h2d_stream = nullptr;
+    if (p->h_arrived) cudaFreeHost(p->h_arrived);
+    p->ev_copier_end = nullptr;
+    p->ev_h2d = nullptr;
+    p->d2h_stream = nullptr;
+    p->h_arrived = nullptr;
+    p->h_arrived_dev = nullptr;
     for (auto& pair : p->ev_copier)
         for (cudaEvent_t& e : pair) {
             if (e) cudaEventDestroy(e);
@@ -289,6 +313,7 @@ int launch_round_copier(dtt_plan* p) {
         DTT_CUDA_TRY(cudaEventRecord(p->ev_done, p->copy_stream));
         p->done_valid = true;
     }
+    if (p->notify_host) DTT_CUDA_TRY(cudaEventRecord(p->ev_copier_end, p->copy_stream));
     p->copier_launched = true;
     return DTT_OK;
 }
@@ -327,6 +352,7 @@ CopierParams copier_params(const dtt_plan* p) {
     cp.max_polls = p->opts.max_polls;
     cp.stage_bytes = bulk_stage_bytes(p->opts.piece_bytes);
     cp.tmaps = p->d_tmaps;
+    cp.host_arrived = p->notify_host ? p->h_arrived_dev : nullptr;
     cp.stages = p->opts.stages;
     return cp;
 }
@@ -487,6 +513,10 @@ int upload(dtt_plan* p) {
     std::memset(p->h_status, 0, host_bytes);
     DTT_CUDA_TRY(cudaHostGetDevicePointer(reinterpret_cast<void**>(&p->h_status_dev), p->h_status, 0));
     p->h_flags = reinterpret_cast<uint8_t*>(p->h_status + 1);
+    const size_t arr_bytes = std::max<size_t>(1, n) * sizeof(uint32_t);
+    DTT_CUDA_TRY(cudaHostAlloc(&p->h_arrived, arr_bytes, cudaHostAllocMapped | cudaHostAllocPortable));
+    std::memset(p->h_arrived, 0, arr_bytes);
+    DTT_CUDA_TRY(cudaHostGetDevicePointer(reinterpret_cast<void**>(&p->h_arrived_dev), p->h_arrived, 0));
     if (p->opts.time_copier) {
         for (auto& pair : p->ev_copier)
             for (cudaEvent_t& e : pair) DTT_CUDA_TRY(cudaEventCreate(&e));
@@ -661,8 +691,13 @@ int dtt_plan_create(void* const* bufs, uint64_t buf_bytes, uint32_t P,
     if (rc == DTT_OK && cudaStreamCreateWithFlags(&p->aux_stream, cudaStreamNonBlocking) != cudaSuccess)
         rc = fail(DTT_ECUDA, "dtt_plan_create: cannot create the aux stream");
     if (rc == DTT_OK && (cudaEventCreateWithFlags(&p->ev_producer, cudaEventDisableTiming) != cudaSuccess ||
-                         cudaEventCreateWithFlags(&p->ev_done, cudaEventDisableTiming) != cudaSuccess))
+                         cudaEventCreateWithFlags(&p->ev_done, cudaEventDisableTiming) != cudaSuccess ||
+                         cudaEventCreateWithFlags(&p->ev_copier_end, cudaEventDisableTiming) != cudaSuccess ||
+                         cudaEventCreateWithFlags(&p->ev_h2d, cudaEventDisableTiming) != cudaSuccess))
         rc = fail(DTT_ECUDA, "dtt_plan_create: cannot create an event");
+    if (rc == DTT_OK && (cudaStreamCreateWithFlags(&p->d2h_stream, cudaStreamNonBlocking) != cudaSuccess ||
+                         cudaStreamCreateWithFlags(&p->h2d_stream, cudaStreamNonBlocking) != cudaSuccess))
+        rc = fail(DTT_ECUDA, "dtt_plan_create: cannot create the host-copy streams");
     if (rc != DTT_OK) {           // all or nothing: free what was prepared
         free_device(p);
         delete p;
@@ -907,20 +942,161 @@ int dtt_allgather_host(dtt_plan* p, const void* const* host_slices, void* host_o
     if (!p || !host_slices) return fail(DTT_EINVAL, "dtt_allgather_host: bad args");
     if (!p->opts.allgather) return fail(DTT_EINVAL, "dtt_allgather_host: needs an all-gather plan");
     if (out_rank >= p->P) return fail(DTT_EINVAL, "dtt_allgather_host: out_rank out of range");
+    const uint32_t P = p->P;
+    const uint64_t S = p->buf_bytes / P;
+    // the byte extent [lo, hi) of every chunk inside its rank's slice, from the copier's pieces
+    std::vector<uint64_t> lo(p->n_global, 0), hi(p->n_global, 0);
+    for (uint32_t c = 0; c < p->n_global; ++c) {
+        const ChunkDesc& cd = p->chunks[c];
+        const uint64_t base = (uint64_t)cd.owner * S;
+        uint64_t a = UINT64_MAX, b = 0;
+        for (uint32_t i = 0; i < cd.n_pieces; ++i) {
+            const PieceDesc& pc = p->pieces[cd.piece_begin + i];
+            if (!pc.rows) continue;
+            a = std::min(a, pc.off);
+            b = std::max(b, pc.off + (uint64_t)(pc.rows - 1) * pc.pitch + pc.row_bytes);
+        }
+        if (b) {
+            lo[c] = a - base;
+            hi[c] = b - base;
+        }
+    }
     dtt_handle h[DTT_MAX_RANKS];
+    p->notify_host = host_out != nullptr;        // the copier stamps each chunk's arrival
     int rc = dtt_plan_start(p, stream, h);
+    p->notify_host = false;
     if (rc != DTT_OK) return rc;
-    const uint64_t S = p->buf_bytes / p->P;
-    for (uint32_t r = 0; r < p->P; ++r)
-        if (host_slices[r])
-            DTT_CUDA_TRY(cudaMemcpyAsync(p->bufs[r] + r * S, host_slices[r], S, cudaMemcpyHostToDevice, stream));
-    rc = dtt_publish(h, p->P, 0, p->n_global, 0, stream);
-    if (rc != DTT_OK) return rc;
-    rc = dtt_plan_wait(p, report);
-    if (rc != DTT_OK) return rc;
+    const uint32_t round = p->round;
+
+    // Host to device in pieces; a chunk is marked as soon as the bytes it covers have landed, so
+    // the copier fans it out while later pieces are still in flight.
+    // pieces of a quarter of a slice, at least 4 MiB: the slices already pipeline one behind
+    // the other, and every piece boundary costs the copy engine a pause
+    const uint64_t kPiece = std::max<uint64_t>(4ull << 20, (S / 4 + 4095) & ~uint64_t(4095));
+    std::vector<uint64_t> copied(P, 0), back(P, 0);   // bytes copied in / copied back per slice
+    std::vector<uint32_t> marked(P);
+    for (uint32_t r = 0; r < P; ++r) {
+        marked[r] = p->first_chunk[r];
+        if (!host_slices[r]) copied[r] = S;
+    }
+    auto mark_ready_prefix = [&](uint32_t r) -> int {
+        const uint32_t end = p->first_chunk[r] + p->n_chunks[r];
+        uint32_t k = marked[r];
+        while (k < end && hi[k] <= copied[r]) ++k;
+        if (k == marked[r]) return DTT_OK;
+        const int prc = dtt_publish(h, P, marked[r], k - marked[r], 0, stream);
+        marked[r] = k;
+        return prc;
+    };
+    // Device to host: rank out_rank's gathered buffer, each slice as far as every chunk of it
+    // has arrived (out_rank's own slice as far as it was copied in).
+    auto copy_back = [&](uint32_t r, uint64_t upto) -> int {
+        if (upto <= back[r]) return DTT_OK;
+        DTT_CUDA_TRY(cudaMemcpyAsync(static_cast<char*>(host_out) + r * S + back[r],
+                                     p->bufs[out_rank] + r * S + back[r], upto - back[r],
+                                     cudaMemcpyDeviceToHost, p->d2h_stream));
+        back[r] = upto;
+        return DTT_OK;
+    };
+    auto arrived_prefix = [&](uint32_t r) -> uint64_t {
+        uint64_t x = S;
+        for (uint32_t c = p->first_chunk[r]; c < p->first_chunk[r] + p->n_chunks[r]; ++c)
+            if (__atomic_load_n(&p->h_arrived[c], __ATOMIC_ACQUIRE) != round) x = std::min(x, lo[c]);
+        return x;
+    };
+    // the output rank's own pieces, each copied back once its copy in has completed (asked of
+    // its event on the host, so no copy back queues behind a copy in on the device)
+    std::vector<std::pair<size_t, uint64_t>> own;   // (event index, copied prefix)
+    size_t own_next = 0;
+    auto poll = [&](bool final) -> int {
+        while (own_next < own.size()) {
+            const cudaError_t e = final ? cudaEventSynchronize(p->ev_pieces[own[own_next].first])
+                                        : cudaEventQuery(p->ev_pieces[own[own_next].first]);
+            if (e == cudaErrorNotReady) break;
+            if (e != cudaSuccess) return fail(DTT_ECUDA, "dtt_allgather_host: %s", cudaGetErrorString(e));
+            const int prc = copy_back(out_rank, own[own_next++].second);
+            if (prc != DTT_OK) return prc;
+        }
+        for (uint32_t r = 0; r < P; ++r) {
+            if (r == out_rank) continue;
+            const uint64_t x = arrived_prefix(r);
+            if (x == S || x >= back[r] + (1ull << 20) || (final && x > back[r])) {
+                const int prc = copy_back(r, x);
+                if (prc != DTT_OK) return prc;
+            }
+        }
+        return DTT_OK;
+    };
+    for (uint32_t r = 0; r < P; ++r) {             // ranks without host data: as they stand
+        if (host_slices[r]) continue;
+        rc = mark_ready_prefix(r);
+        if (rc != DTT_OK) return rc;
+    }
+    if (host_out && !host_slices[out_rank]) {
+        DTT_CUDA_TRY(cudaEventRecord(p->ev_h2d, stream));
+        DTT_CUDA_TRY(cudaStreamWaitEvent(p->d2h_stream, p->ev_h2d, 0));
+        rc = copy_back(out_rank, S);
+        if (rc != DTT_OK) return rc;
+    }
+    // the copies stream back to back on their own stream; the marks (kernels on `stream`) and
+    // the copies back each wait for the piece they depend on
+    DTT_CUDA_TRY(cudaEventRecord(p->ev_h2d, stream));       // after plan_start's work on `stream`
+    DTT_CUDA_TRY(cudaStreamWaitEvent(p->h2d_stream, p->ev_h2d, 0));
+    // slice by slice, so each slice (and the fan-out and copy back behind it) completes as early
+    // as it can; pieces within a slice let its chunks open before the whole slice is in
+    for (uint32_t r = 0; r < P; ++r) {
+        while (copied[r] < S) {
+            const uint64_t n = std::min(kPiece, S - copied[r]);
+            DTT_CUDA_TRY(cudaMemcpyAsync(p->bufs[r] + r * S + copied[r],
+                                         static_cast<const char*>(host_slices[r]) + copied[r], n,
+                                         cudaMemcpyHostToDevice, p->h2d_stream));
+            copied[r] += n;
+            DTT_CUDA_TRY(cudaEventRecord(p->ev_h2d, p->h2d_stream));
+            const uint32_t before = marked[r];
+            const uint32_t end = p->first_chunk[r] + p->n_chunks[r];
+            if (before < end && hi[before] <= copied[r]) {
+                DTT_CUDA_TRY(cudaStreamWaitEvent(stream, p->ev_h2d, 0));
+                rc = mark_ready_prefix(r);
+                if (rc != DTT_OK) return rc;
+            }
+            if (host_out && r == out_rank) {        // its own bytes go back once they are in
+                if (own.size() == p->ev_pieces.size()) {
+                    cudaEvent_t e = nullptr;
+                    DTT_CUDA_TRY(cudaEventCreateWithFlags(&e, cudaEventDisableTiming));
+                    p->ev_pieces.push_back(e);
+                }
+                DTT_CUDA_TRY(cudaEventRecord(p->ev_pieces[own.size()], p->h2d_stream));
+                own.emplace_back(own.size(), copied[r]);
+            }
+            if (host_out && (rc = poll(false)) != DTT_OK) return rc;
+        }
+    }
+    DTT_CUDA_TRY(cudaStreamWaitEvent(stream, p->ev_h2d, 0));   // every copy precedes the check
     if (host_out) {
-        DTT_CUDA_TRY(cudaMemcpyAsync(host_out, p->bufs[out_rank], p->buf_bytes, cudaMemcpyDeviceToHost, stream));
-        DTT_CUDA_TRY(cudaStreamSynchronize(stream));
+        // the rest as it arrives; once the copier has exited, whatever arrived is final
+        for (uint64_t spin = 1;; ++spin) {
+            if ((rc = poll(false)) != DTT_OK) return rc;
+            bool all = true;
+            for (uint32_t r = 0; r < P; ++r) all = all && back[r] == S;
+            if (all) break;
+            if ((spin & 1023) == 0) {
+                const cudaError_t e = cudaEventQuery(p->ev_copier_end);
+                if (e == cudaSuccess) break;
+                if (e != cudaErrorNotReady)
+                    return fail(DTT_ECUDA, "dtt_allgather_host: %s", cudaGetErrorString(e));
+            }
+        }
+        if ((rc = poll(true)) != DTT_OK) return rc;
+    }
+    rc = dtt_plan_wait(p, report);
+    if (rc != DTT_OK) {
+        cudaStreamSynchronize(p->d2h_stream);
+        return rc;
+    }
+    if (host_out) {
+        DTT_CUDA_TRY(cudaStreamSynchronize(p->d2h_stream));
+        for (uint32_t r = 0; r < P; ++r)
+            if (back[r] != S) return fail(DTT_ETIMEDOUT, "dtt_allgather_host: slice %u came back short", r);
     }
     return dtt_plan_next_round(p);
 }

@@ -328,11 +328,17 @@ int dtt_plan_stats(dtt_plan* plan, double* copier_ms_last, double* copier_ms_tot
 int dtt_plan_read_gates(dtt_plan* plan, uint64_t* host, uint64_t n_words);
 
 /* Host-buffer all-gather, one round end to end: copy each rank's slice (host_slices[r],
- * pinned host memory, S = buf_bytes / P bytes) into its own rows, mark every chunk from a
- * kernel queued after the copies on `stream`, let the copier fan the chunks out, wait, and
- * copy rank out_rank's gathered buffer (buf_bytes) to host_out (pinned, may be NULL).  Then
- * advances to the next round.  Needs an all-gather plan in state PREPARED.  The report is
- * filled as by dtt_plan_wait.  Errors: as start / wait / next_round. */
+ * pinned host memory, S = buf_bytes / P bytes; NULL: the rank's rows as they stand) into its
+ * own rows, let the copier fan the chunks out, wait, and copy rank out_rank's gathered buffer
+ * (buf_bytes) to host_out (pinned, may be NULL).  Then advances to the next round.
+ * The round is pipelined: slices go in rank by rank, in pieces, on a stream of the plan; each
+ * chunk is marked (a kernel on `stream`) as soon as the bytes it covers have landed, so the
+ * copier fans it out while later pieces are still in flight; the copier stamps each chunk's
+ * arrival into pinned, mapped host memory, and the host copies every slice of out_rank's
+ * buffer back, on another stream of the plan, as far as its chunks have arrived.  The call
+ * returns when everything has landed in host_out.  Needs an all-gather plan in state
+ * PREPARED.  The report is filled as by dtt_plan_wait.  Errors: as start / wait / next_round,
+ * DTT_ETIMEDOUT if a slice could not be copied back completely. */
 int dtt_allgather_host(dtt_plan* plan, const void* const* host_slices, void* host_out,
                        uint32_t out_rank, cudaStream_t stream, dtt_report* report);
 

@@ -207,22 +207,60 @@ def test_consumer_wait_times_out_on_a_gate_nobody_opens():
     st.plan.close()
 
 
-def test_allgather_from_host_buffers():
-    w = W.small(W.C2, M=128, N=512, num_chunks=4)
-    st = runner.make(w)
-    S = w.slice_bytes
+HOST_CASES = {
+    "chunks_one_piece": (W.small(W.C2, M=128, N=512, num_chunks=4), {}),
+    # 8 MiB slices go in as two 4 MiB pieces; 1 MiB chunks open as their bytes land
+    "chunks_two_pieces_bulk": (W.small(W.C2, M=2048, N=2048, num_chunks=8),
+                               {"opts": dict(method=1, piece_bytes=65536, stages=3)}),
+    # 2D tile windows (tensor-map boxes), grouped order, slices of two pieces
+    "tiles_two_pieces": (W.Workload("ht", P=3, M=3000, N=1024, dtype=W.BF16, kind="tile_chunks",
+                                    rounds=2, seed=41, BM=128, BN=128, num_programs=6,
+                                    tiles_per_chunk=6, group_m=4),
+                         {"opts": dict(method=1, piece_bytes=16384, stages=12)}),
+}
+
+
+@pytest.mark.parametrize("name", sorted(HOST_CASES))
+def test_allgather_from_host_buffers(name):
+    w, kw = HOST_CASES[name]
+    kw = dict(kw)
+    opts = kw.pop("opts", None)
+    st = runner.make(w, opts=D.dtt_plan_opts_default(**opts) if opts else None)
     try:
         for R in (1, 2):
             host = [torch.from_numpy(H.fill_slice_bytes(w.dtype, w.seed + R, r, R, w.M, w.N)).pin_memory()
                     for r in range(w.P)]
             out = torch.zeros(w.buf_bytes, dtype=torch.uint8).pin_memory()
-            rep = st.plan.allgather_host(host, out, out_rank=2, stream=st.producer_stream)
+            rep = st.plan.allgather_host(host, out, out_rank=w.P - 1, stream=st.producer_stream)
             assert rep.status == D.OK
             want = np.concatenate([h.numpy() for h in host])
             np.testing.assert_array_equal(out.numpy(), want)
             for q in range(w.P):
                 np.testing.assert_array_equal(st.bufs[q].cpu().numpy(), want)
         assert st.plan.round == 3
+    finally:
+        st.plan.close()
+
+
+def test_allgather_from_host_buffers_edges():
+    # a rank without host data sends its rows as they stand; a round without an output buffer
+    w = W.small(W.C2, M=1024, N=2048, num_chunks=4)
+    st = runner.make(w, fill_byte=5)
+    S = w.slice_bytes
+    try:
+        host = [torch.from_numpy(H.fill_slice_bytes(w.dtype, w.seed, r, 1, w.M, w.N)).pin_memory()
+                for r in range(w.P)]
+        host[1] = None
+        out = torch.zeros(w.buf_bytes, dtype=torch.uint8).pin_memory()
+        assert st.plan.allgather_host(host, out, out_rank=0, stream=st.producer_stream).status == D.OK
+        want = np.concatenate([h.numpy() if h is not None else np.full(S, 5, np.uint8) for h in host])
+        np.testing.assert_array_equal(out.numpy(), want)
+        host2 = [torch.from_numpy(H.fill_slice_bytes(w.dtype, w.seed, r, 2, w.M, w.N)).pin_memory()
+                 for r in range(w.P)]
+        assert st.plan.allgather_host(host2, None, stream=st.producer_stream).status == D.OK
+        want2 = np.concatenate([h.numpy() for h in host2])
+        for q in range(w.P):
+            np.testing.assert_array_equal(st.bufs[q].cpu().numpy(), want2)
     finally:
         st.plan.close()
 
