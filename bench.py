@@ -494,6 +494,90 @@ def run_ours(args):
     return 0
 
 
+def run_consumer(args):
+    """The consumer side of the plan: a GEMM over rank 0's gathered buffer, D = X . W^T with
+    X [P*M, N] (the all-gather's output) and W^T [consumer_n, N], each 128-row block loaded as
+    soon as its chunks have arrived.  Times, on the vector copier (the GEMM's shared-memory ring
+    leaves the bulk copier no room): the all-gather round alone, the GEMM alone (its chunks
+    already delivered), and the two overlapped in one round."""
+    import torch
+    import device_triggered_transfers_gb300 as D
+    from device_triggered_transfers_gb300 import runner
+    w = workload(args)
+    K, N2 = w.N, args.consumer_n
+    rows = w.buf_bytes // (2 * K)
+    g = torch.Generator().manual_seed(w.seed + 99)
+    Wt = (torch.randn(N2, K, generator=g) / K ** 0.5).to(torch.bfloat16).cuda()
+    out = torch.empty(rows, N2, dtype=torch.bfloat16, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    copy_stream, cons = torch.cuda.Stream(priority=-1), torch.cuda.Stream()
+    # the producer of the benchmark's launch (its chunks open one wave after another), with the
+    # vector copier
+    launch = {k: v for k, v in runner.bench_launch(w).items() if k != "opts"}
+    st = runner.make(w, opts=D.dtt_plan_opts_default(copier_threads=args.consumer_copier_threads),
+                     copy_stream=copy_stream, **launch)
+    prod = st.producer_stream
+
+    def ag():
+        h = st.plan.start(prod)
+        D.dtt_fill_producer(st.buf_ptrs, st.desc, h, prod)
+        st.plan.wait()
+        st.plan.next_round()
+
+    def overlapped():
+        h = st.plan.start(prod)
+        st.plan.gemm_consumer(0, Wt, out, N2, K, err, stream=cons)
+        D.dtt_fill_producer(st.buf_ptrs, st.desc, h, prod)
+        st.plan.wait()
+        prod.wait_stream(cons)
+        st.plan.next_round()
+
+    def timed(fn, K_):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(prod)
+        for _ in range(K_):
+            fn()
+        e1.record(prod)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / K_
+
+    K_ = max(3, min(args.steps, 50))
+    ag_ms = timed(ag, K_)
+    ov_ms = timed(overlapped, K_)
+    gemm = []
+    for _ in range(K_):                 # the GEMM alone: its chunks have all arrived
+        h = st.plan.start(prod)
+        D.dtt_fill_producer(st.buf_ptrs, st.desc, h, prod)
+        torch.cuda.synchronize()        # producer and copier done
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(cons)
+        st.plan.gemm_consumer(0, Wt, out, N2, K, err, stream=cons)
+        e1.record(cons)
+        st.plan.wait()
+        cons.synchronize()
+        st.plan.next_round()
+        gemm.append(e0.elapsed_time(e1))
+    gemm_ms = statistics.median(gemm)
+    st.plan.close()
+    assert int(err.item()) == 0
+    flops = 2.0 * rows * N2 * K
+    tf_peak, tf_kind = load_tensor_peak()
+    line = {"metric": "all-gather + consumer GEMM round, overlapped (1 GB300)", "unit": "ms per round",
+            "higher_is_better": False, "steps": K_, "value": ov_ms,
+            "config": {"workload": describe(w, launch) + f"; consumer GEMM: rank 0's [{rows}, {K}] bf16 "
+                                                           f"x W^T [{N2}, {K}], tcgen05, 148 CTAs",
+                       "copier": f"vector (16-byte) path, {args.consumer_copier_threads} threads per CTA"},
+            "all_gather_ms": ag_ms, "gemm_alone_ms": gemm_ms,
+            "sequential_ms": ag_ms + gemm_ms, "overlap_saving": 1.0 - ov_ms / (ag_ms + gemm_ms),
+            "gemm_alone_tflops": flops / (gemm_ms / 1e3) / 1e12,
+            "gemm_alone_frac": flops / (gemm_ms / 1e3) / 1e12 / tf_peak, "peak_kind": tf_kind}
+    print(json.dumps(line))
+    return 0
+
+
 def run_barrier(args):
     """Latency of the N-rank notify/wait barrier and the builtin reveal (P = 8 virtual ranks,
     reveal SIZE = 256): one cooperative launch per barrier, CUDA events around K of them."""
@@ -556,6 +640,10 @@ def main(argv=None):
     ap.add_argument("--isolated-rounds", type=int, default=20)
     ap.add_argument("--barrier", action="store_true",
                     help="time the N-rank barrier and the builtin reveal instead")
+    ap.add_argument("--consumer", action="store_true",
+                    help="time the all-gather with a consumer GEMM over its output, overlapped")
+    ap.add_argument("--consumer-n", type=int, default=4096)
+    ap.add_argument("--consumer-copier-threads", type=int, default=256)
     ap.add_argument("--rows", type=int, default=0,
                     help="rows per rank instead of the workload's (a smaller case of the same "
                          "shape, for profiler captures; the default runs the workload as named)")
@@ -564,6 +652,8 @@ def main(argv=None):
         args.warmup = 3
     if args.barrier and args.impl == "ours":
         return run_barrier(args)
+    if args.consumer and args.impl == "ours":
+        return run_consumer(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

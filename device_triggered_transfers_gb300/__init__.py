@@ -121,6 +121,8 @@ _SIGS = {
     "dtt_plan_round": (C.c_uint32, [_P]),
     "dtt_plan_info": (C.c_int, [_P, C.POINTER(_u32), C.POINTER(_u32), C.POINTER(_u32), C.POINTER(_P)]),
     "dtt_plan_read_gates": (C.c_int, [_P, C.POINTER(_u64), _u64]),
+    "dtt_gemm_consumer": (C.c_int, [_P, C.c_uint32, _P, C.c_uint32, C.c_uint32, _P, _u64, C.c_uint32,
+                                    _u64, _P, _P]),
     "dtt_plan_stats": (C.c_int, [_P, C.POINTER(C.c_double), C.POINTER(C.c_double), C.POINTER(_u64)]),
     "dtt_allgather_host": (C.c_int, [_P, C.POINTER(_P), _P, _u32, _P, C.POINTER(dtt_report)]),
     "dtt_fill_producer": (C.c_int, [C.POINTER(_P), _u32, C.POINTER(dtt_fill_desc),
@@ -409,6 +411,13 @@ class Plan:
         if raise_on_error:
             _check(rc)
         return rep
+
+    def gemm_consumer(self, rank: int, Wt, D, N: int, K: int, err, ldd: int = 0,
+                      num_programs: int = 0, max_polls: int = 0, stream=None) -> None:
+        """D = X . W^T over rank `rank`'s gathered buffer, each row block loaded once its chunks
+        have arrived (see dtt_gemm_consumer)."""
+        _check(lib().dtt_gemm_consumer(self._h, rank, _ptr(Wt), N, K, _ptr(D), ldd or 2 * N,
+                                       num_programs, max_polls, _ptr(err), _stream(stream)))
 
     def consumer_gather(self, rank: int, dst, max_polls: int, status, ctas: int, stream) -> None:
         _check(lib().dtt_consumer_gather(self._h, rank, _ptr(dst), max_polls, _ptr(status), ctas,

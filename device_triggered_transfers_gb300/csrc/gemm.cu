@@ -309,6 +309,174 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_producer_kernel(const __grid_
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS) : "memory");
 }
 
+// ---- the consumer form ----------------------------------------------------------------------
+// The peer kernel of a triggered plan ("Triggered Plans", Model: peer kernel wait(chunk); Memory
+// ordering, Consumer): D = X_q . W^T over rank q's gathered buffer X_q, loading each 128-row
+// block of X_q only once every chunk covering those rows has arrived at q this round (q's own
+// chunks: once they are ready), so the GEMM runs while the all-gather is still delivering.
+struct ConsumerParams {
+    CUtensorMap tmX;     // X_q: [rows, K] bf16, box 64 x 128
+    CUtensorMap tmW;     // W^T: [N, K] bf16, box 64 x TN
+    dtt_handle h;        // rank q's handle for this round
+    const uint32_t* order;   // row blocks in the order they are taken
+    const uint32_t* c0;      // per row block: the chunk ids [c0, c1] that cover it
+    const uint32_t* c1;
+    char* D;
+    uint64_t ldd;
+    uint64_t max_polls;
+    uint32_t blocks, N, K;
+    uint32_t* err;
+};
+
+// Bounded wait for every chunk in [c0, c1] at rank h.rank, then order the data read by the
+// bulk copies that follow after the acquire.
+__device__ __forceinline__ bool wait_chunks(const dtt_handle& h, uint32_t c0, uint32_t c1, uint64_t max_polls,
+                                            volatile uint32_t* abort) {
+    for (uint32_t c = c0; c <= c1; ++c) {
+        const uint64_t* w = dtt_dev::wait_word(h, c);
+        uint32_t ns = 0;
+        bool ok = false;
+        for (uint64_t i = 0; i < max_polls; ++i) {
+            if ((uint32_t)dtt_dev::ld_acquire(w) >= h.round) { ok = true; break; }
+            if ((i & 63) == 63 && *abort) return false;
+            __nanosleep(ns);
+            ns = ns < 256 ? ns + 32 : 256;
+        }
+        if (!ok) return false;
+    }
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    return true;
+}
+
+template <uint32_t TN>
+__global__ void __launch_bounds__(THREADS, 1) gemm_consumer_kernel(const __grid_constant__ ConsumerParams p) {
+    using G = Cfg<TN>;
+    constexpr uint32_t STAGES = G::STAGES, B_STAGE = G::B_STAGE, TMEM_COLS = G::TMEM_COLS;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sA = smem;
+    uint8_t* sB = smem + STAGES * A_STAGE;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sB + STAGES * B_STAGE);
+    uint64_t* full = bars;
+    uint64_t* empty = bars + STAGES;
+    uint64_t* acc_full = bars + 2 * STAGES;
+    uint64_t* acc_empty = acc_full + ACC_BUFS;
+    uint64_t* drain = acc_empty + ACC_BUFS;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile uint32_t* abort_flag = tmem_slot + 1;
+
+    const uint32_t warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    if (threadIdx.x == 0) {
+        for (uint32_t i = 0; i < STAGES; ++i) {
+            bar_init(saddr(full + i), 1);
+            bar_init(saddr(empty + i), 1);
+        }
+        for (uint32_t i = 0; i < ACC_BUFS; ++i) {
+            bar_init(saddr(acc_full + i), 1);
+            bar_init(saddr(acc_empty + i), EPI_THREADS);
+        }
+        bar_init(saddr(drain), 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                     ::"r"(saddr(tmem_slot)), "r"(TMEM_COLS) : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    const uint32_t units_n = p.N / TN, units = p.blocks * units_n, kblocks = p.K / BK;
+    auto fail = [&]() {
+        *abort_flag = 1;
+        atomicAdd(p.err, 1u);
+    };
+
+    if (warp == TMA_WARP) {
+        if (lane == 0) {
+            uint32_t stage = 0, phase = 0, issued = 0;
+            bool ok = true;
+            for (uint32_t u = blockIdx.x; u < units && ok; u += gridDim.x) {
+                const uint32_t b = p.order[u / units_n];
+                if (!wait_chunks(p.h, p.c0[b], p.c1[b], p.max_polls, abort_flag)) { fail(); break; }
+                const int32_t row_x = (int32_t)(b * BM), row_w = (int32_t)((u % units_n) * TN);
+                for (uint32_t kb = 0; kb < kblocks; ++kb) {
+                    if (!bar_wait(saddr(empty + stage), phase ^ 1, abort_flag)) { fail(); ok = false; break; }
+                    bar_expect_tx(saddr(full + stage), A_STAGE + B_STAGE);
+                    tma_load_2d(saddr(sA + stage * A_STAGE), &p.tmX, (int32_t)(kb * BK), row_x, saddr(full + stage));
+                    tma_load_2d(saddr(sB + stage * B_STAGE), &p.tmW, (int32_t)(kb * BK), row_w, saddr(full + stage));
+                    ++issued;
+                    if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                }
+            }
+            volatile uint32_t never = 0;
+            for (uint32_t i = issued > STAGES ? issued - STAGES : 0; i < issued; ++i)
+                (void)bar_wait(saddr(full + i % STAGES), (i / STAGES) & 1, &never);
+        }
+    } else if (warp == MMA_WARP) {
+        if (lane == 0) {
+            uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+            bool ok = true;
+            for (uint32_t u = blockIdx.x; u < units && ok; u += gridDim.x) {
+                if (!bar_wait(saddr(acc_empty + acc), acc_phase ^ 1, abort_flag)) { fail(); break; }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + acc * TN;
+                for (uint32_t kb = 0; kb < kblocks; ++kb) {
+                    if (!bar_wait(saddr(full + stage), phase, abort_flag)) { fail(); ok = false; break; }
+                    tc_fence_after();
+                    const uint64_t da = smem_desc(saddr(sA + stage * A_STAGE));
+                    const uint64_t db = smem_desc(saddr(sB + stage * B_STAGE));
+#pragma unroll
+                    for (uint32_t k = 0; k < BK / UMMA_K; ++k)
+                        umma(d_tmem, da + 2 * k, db + 2 * k, G::IDESC, (kb | k) != 0);
+                    umma_commit(saddr(empty + stage));
+                    if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                }
+                if (!ok) break;
+                umma_commit(saddr(acc_full + acc));
+                if (++acc == ACC_BUFS) { acc = 0; acc_phase ^= 1; }
+            }
+            umma_commit(saddr(drain));
+            volatile uint32_t never = 0;
+            (void)bar_wait(saddr(drain), 0, &never);
+        }
+    } else {
+        uint32_t acc = 0, acc_phase = 0;
+        const uint32_t row_in_tile = warp * 32 + lane;
+        for (uint32_t u = blockIdx.x; u < units; u += gridDim.x) {
+            bool mine = bar_wait(saddr(acc_full + acc), acc_phase, abort_flag);
+            if (!mine) fail();
+            if (!epi_all(mine && !*abort_flag)) break;
+            tc_fence_after();
+            const uint32_t b = p.order[u / units_n];
+            char* drow = p.D + (uint64_t)(b * BM + row_in_tile) * p.ldd + (uint64_t)(u % units_n) * TN * 2;
+            const uint32_t taddr = tmem_base + ((warp * 32u) << 16) + acc * TN;
+#pragma unroll 1
+            for (uint32_t g = 0; g < TN / 32; ++g) {
+                uint32_t v[32];
+                tmem_ld32(taddr + g * 32, v);
+                uint4* dst = reinterpret_cast<uint4*>(drow + g * 64);
+#pragma unroll
+                for (uint32_t j = 0; j < 4; ++j)
+                    dst[j] = make_uint4(pack_bf16x2(v[8 * j + 0], v[8 * j + 1]), pack_bf16x2(v[8 * j + 2], v[8 * j + 3]),
+                                        pack_bf16x2(v[8 * j + 4], v[8 * j + 5]), pack_bf16x2(v[8 * j + 6], v[8 * j + 7]));
+            }
+            tc_fence_before();
+            bar_arrive(saddr(acc_empty + acc));
+            if (++acc == ACC_BUFS) { acc = 0; acc_phase ^= 1; }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS) : "memory");
+}
+
 // ---- the 2-CTA form -------------------------------------------------------------------------
 // A cluster of two CTAs on two SMs computes 256 x 256 blocks with tcgen05.mma.cta_group::2
 // (M = 256, N = 256): each CTA holds its 128 rows of A and its 128 columns of B^T per stage, so a
@@ -590,9 +758,45 @@ static cudaError_t prepare_gemm() {
     return e;
 }
 
+template <uint32_t TN>
+static cudaError_t prepare_consumer() {
+    cudaError_t e = prepare_kernel(gemm_consumer_kernel<TN>);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(gemm_consumer_kernel<TN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)Cfg<TN>::SMEM_BYTES);
+    return e;
+}
+
+int launch_gemm_consumer(const ConsumerLaunch& cl, cudaStream_t stream) {
+    const uint32_t TN = (cl.N % 256 == 0) ? 256 : 128;
+    ConsumerParams cp{};
+    if (!operand_maps(cl.X, cl.Wt, cl.rows, cl.N, cl.K, TN, &cp.tmX, &cp.tmW))
+        return fail(DTT_ECUDA, "dtt_gemm_consumer: cannot encode the tensor maps");
+    cp.h = cl.h;
+    cp.order = cl.order;
+    cp.c0 = cl.c0;
+    cp.c1 = cl.c1;
+    cp.D = cl.D;
+    cp.ldd = cl.ldd;
+    cp.max_polls = cl.max_polls;
+    cp.blocks = cl.blocks;
+    cp.N = cl.N;
+    cp.K = cl.K;
+    cp.err = cl.err;
+    if (TN == 256)
+        gemm_consumer_kernel<256><<<cl.ctas, THREADS, Cfg<256>::SMEM_BYTES, stream>>>(cp);
+    else
+        gemm_consumer_kernel<128><<<cl.ctas, THREADS, Cfg<128>::SMEM_BYTES, stream>>>(cp);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(DTT_ECUDA, "dtt_gemm_consumer: launch failed: %s", cudaGetErrorString(e));
+    return DTT_OK;
+}
+
 cudaError_t preload_gemm_kernels() {
     cudaError_t e = prepare_gemm<128>();
     if (e == cudaSuccess) e = prepare_gemm<256>();
+    if (e == cudaSuccess) e = prepare_consumer<128>();
+    if (e == cudaSuccess) e = prepare_consumer<256>();
     if (e == cudaSuccess) e = prepare_kernel(gemm2_producer_kernel);
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(gemm2_producer_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)G2_SMEM);

@@ -164,6 +164,26 @@ cudaError_t prepare_kernel(K kernel) {
 // Force-load each translation unit's kernels on the current device (see dtt_preload).
 cudaError_t preload_copier_kernels();
 cudaError_t copier_regs_per_thread(uint32_t method, int* regs);   // of the copier kernel for `method`
+
+// The consumer GEMM (gemm.cu): D = X . W^T over one rank's gathered buffer X [rows, K] bf16,
+// each 128-row block loaded once the chunk ids [c0[b], c1[b]] have arrived at that rank.
+struct ConsumerLaunch {
+    const void* X;
+    uint64_t rows;
+    const void* Wt;
+    uint32_t N, K;
+    char* D;
+    uint64_t ldd;
+    dtt_handle h;
+    const uint32_t* order;
+    const uint32_t* c0;
+    const uint32_t* c1;
+    uint32_t blocks;
+    uint64_t max_polls;
+    uint32_t* err;
+    uint32_t ctas;
+};
+int launch_gemm_consumer(const ConsumerLaunch& cl, cudaStream_t stream);
 cudaError_t preload_fill_kernels();
 cudaError_t preload_barrier_kernels();
 cudaError_t preload_gemm_kernels();

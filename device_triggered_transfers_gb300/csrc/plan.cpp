@@ -67,6 +67,11 @@ struct dtt_plan {
     cudaStream_t h2d_stream = nullptr;
     cudaStream_t d2h_stream = nullptr;
 
+    // consumer GEMM: per 128-row block of one rank's buffer seen as [rows, K], the order the
+    // blocks are taken in and the chunk ids that cover each block (device, built on first use)
+    uint32_t cons_rank = UINT32_MAX, cons_K = 0, cons_blocks = 0, cons_cap = 0;
+    uint32_t* d_cons = nullptr;       // [3][blocks]: order, c0, c1
+
     cudaStream_t copy_stream = nullptr;
     bool own_copy_stream = false;
     cudaStream_t aux_stream = nullptr;
@@ -132,6 +137,8 @@ void free_device(dtt_plan* p) {
     if (p->h2d_stream) cudaStreamDestroy(p->h2d_stream);
     p->h2d_stream = nullptr;
     if (p->h_arrived) cudaFreeHost(p->h_arrived);
+    if (p->d_cons) cudaFree(p->d_cons);
+    p->d_cons = nullptr;
     p->ev_copier_end = nullptr;
     p->ev_h2d = nullptr;
     p->d2h_stream = nullptr;
@@ -937,18 +944,15 @@ int dtt_plan_read_gates(dtt_plan* p, uint64_t* host, uint64_t n_words) {
     return DTT_OK;
 }
 
-int dtt_allgather_host(dtt_plan* p, const void* const* host_slices, void* host_out,
-                       uint32_t out_rank, cudaStream_t stream, dtt_report* report) {
-    if (!p || !host_slices) return fail(DTT_EINVAL, "dtt_allgather_host: bad args");
-    if (!p->opts.allgather) return fail(DTT_EINVAL, "dtt_allgather_host: needs an all-gather plan");
-    if (out_rank >= p->P) return fail(DTT_EINVAL, "dtt_allgather_host: out_rank out of range");
-    const uint32_t P = p->P;
-    const uint64_t S = p->buf_bytes / P;
-    // the byte extent [lo, hi) of every chunk inside its rank's slice, from the copier's pieces
-    std::vector<uint64_t> lo(p->n_global, 0), hi(p->n_global, 0);
+namespace {
+
+// The byte extent [lo, hi) of every chunk in the buffers, from the copier's pieces (0, 0 for a
+// chunk without bytes).
+void chunk_extents(const dtt_plan* p, std::vector<uint64_t>* lo, std::vector<uint64_t>* hi) {
+    lo->assign(p->n_global, 0);
+    hi->assign(p->n_global, 0);
     for (uint32_t c = 0; c < p->n_global; ++c) {
         const ChunkDesc& cd = p->chunks[c];
-        const uint64_t base = (uint64_t)cd.owner * S;
         uint64_t a = UINT64_MAX, b = 0;
         for (uint32_t i = 0; i < cd.n_pieces; ++i) {
             const PieceDesc& pc = p->pieces[cd.piece_begin + i];
@@ -957,8 +961,29 @@ int dtt_allgather_host(dtt_plan* p, const void* const* host_slices, void* host_o
             b = std::max(b, pc.off + (uint64_t)(pc.rows - 1) * pc.pitch + pc.row_bytes);
         }
         if (b) {
-            lo[c] = a - base;
-            hi[c] = b - base;
+            (*lo)[c] = a;
+            (*hi)[c] = b;
+        }
+    }
+}
+
+}  // namespace
+
+int dtt_allgather_host(dtt_plan* p, const void* const* host_slices, void* host_out,
+                       uint32_t out_rank, cudaStream_t stream, dtt_report* report) {
+    if (!p || !host_slices) return fail(DTT_EINVAL, "dtt_allgather_host: bad args");
+    if (!p->opts.allgather) return fail(DTT_EINVAL, "dtt_allgather_host: needs an all-gather plan");
+    if (out_rank >= p->P) return fail(DTT_EINVAL, "dtt_allgather_host: out_rank out of range");
+    const uint32_t P = p->P;
+    const uint64_t S = p->buf_bytes / P;
+    // the byte extent [lo, hi) of every chunk inside its rank's slice
+    std::vector<uint64_t> lo, hi;
+    chunk_extents(p, &lo, &hi);
+    for (uint32_t c = 0; c < p->n_global; ++c) {
+        const uint64_t base = (uint64_t)p->chunks[c].owner * S;
+        if (hi[c]) {
+            lo[c] -= base;
+            hi[c] -= base;
         }
     }
     dtt_handle h[DTT_MAX_RANKS];
@@ -1099,6 +1124,78 @@ int dtt_allgather_host(dtt_plan* p, const void* const* host_slices, void* host_o
             if (back[r] != S) return fail(DTT_ETIMEDOUT, "dtt_allgather_host: slice %u came back short", r);
     }
     return dtt_plan_next_round(p);
+}
+
+int dtt_gemm_consumer(dtt_plan* p, uint32_t rank, const void* Wt, uint32_t N, uint32_t K, void* D,
+                      uint64_t ldd, uint32_t num_programs, uint64_t max_polls, uint32_t* err,
+                      cudaStream_t stream) {
+    if (!p || !Wt || !D || !err || rank >= p->P) return fail(DTT_EINVAL, "dtt_gemm_consumer: bad args");
+    if (p->state != DTT_PLAN_RUNNING) return fail(DTT_ESTATE, "dtt_gemm_consumer: plan is not RUNNING");
+    if (stream == p->copy_stream) return fail(DTT_EINVAL, "dtt_gemm_consumer: use a stream other than the copy stream");
+    const uint64_t row_bytes = 2ull * K;
+    if (N == 0 || K == 0 || N % 128 || K % 64 || p->buf_bytes % (row_bytes * 128))
+        return fail(DTT_EINVAL, "dtt_gemm_consumer: N must be a multiple of 128, K of 64, and the buffer "
+                                "a whole number of 128-row blocks of K bf16");
+    if (ldd < 2ull * N || ldd % 16 || reinterpret_cast<uintptr_t>(D) % 16 || reinterpret_cast<uintptr_t>(Wt) % 16)
+        return fail(DTT_EINVAL, "dtt_gemm_consumer: bad ldd or alignment");
+    const uint64_t rows = p->buf_bytes / row_bytes;
+    const uint32_t blocks = (uint32_t)(rows / 128);
+    if (!p->d_cons || p->cons_rank != rank || p->cons_K != K) {
+        // which chunks cover each block, and the blocks in the order their chunks open: by the
+        // chunk's place in its rank's schedule, then by rank
+        std::vector<uint64_t> lo, hi;
+        chunk_extents(p, &lo, &hi);
+        std::vector<uint32_t> c0(blocks, 1), c1(blocks, 0), key(blocks, UINT32_MAX), order(blocks);
+        const uint64_t bb = 128 * row_bytes;
+        for (uint32_t c = 0; c < p->n_global; ++c) {
+            if (!hi[c]) continue;
+            const uint32_t owner = p->chunks[c].owner, local = c - p->first_chunk[owner];
+            for (uint64_t b = lo[c] / bb; b < blocks && b * bb < hi[c]; ++b) {
+                if (c0[b] > c1[b]) c0[b] = c1[b] = c;
+                c0[b] = std::min(c0[b], c);
+                c1[b] = std::max(c1[b], c);
+                key[b] = std::min(key[b], local * DTT_MAX_RANKS + owner);
+            }
+        }
+        for (uint32_t b = 0; b < blocks; ++b) order[b] = b;
+        std::stable_sort(order.begin(), order.end(), [&](uint32_t x, uint32_t y) { return key[x] < key[y]; });
+        std::vector<uint32_t> table;
+        table.reserve(3 * (size_t)blocks);
+        table.insert(table.end(), order.begin(), order.end());
+        table.insert(table.end(), c0.begin(), c0.end());
+        table.insert(table.end(), c1.begin(), c1.end());
+        if (p->d_cons && p->cons_cap < blocks) {
+            DTT_CUDA_TRY(cudaFreeAsync(p->d_cons, stream));
+            p->d_cons = nullptr;
+        }
+        // stream-ordered: no wait for the rest of the device, where a copier may be spinning
+        if (!p->d_cons) {
+            DTT_CUDA_TRY(cudaMallocAsync(reinterpret_cast<void**>(&p->d_cons), table.size() * sizeof(uint32_t), stream));
+            p->cons_cap = blocks;
+        }
+        p->cons_blocks = blocks;
+        DTT_CUDA_TRY(cudaMemcpyAsync(p->d_cons, table.data(), table.size() * sizeof(uint32_t),
+                                     cudaMemcpyHostToDevice, stream));
+        p->cons_rank = rank;
+        p->cons_K = K;
+    }
+    ConsumerLaunch cl{};
+    cl.X = p->bufs[rank];
+    cl.rows = rows;
+    cl.Wt = Wt;
+    cl.N = N;
+    cl.K = K;
+    cl.D = static_cast<char*>(D);
+    cl.ldd = ldd;
+    cl.h = make_handle(p, rank);
+    cl.order = p->d_cons;
+    cl.c0 = p->d_cons + p->cons_blocks;
+    cl.c1 = p->d_cons + 2 * (size_t)p->cons_blocks;
+    cl.blocks = blocks;
+    cl.max_polls = max_polls ? max_polls : p->opts.max_polls;
+    cl.err = err;
+    cl.ctas = num_programs ? num_programs : 148;
+    return launch_gemm_consumer(cl, stream);
 }
 
 int dtt_consumer_gather(dtt_plan* p, uint32_t rank, void* dst, uint64_t max_polls, int32_t* status,

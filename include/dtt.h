@@ -424,6 +424,25 @@ int dtt_gemm_producer(const void* A, const void* Bt, void* const* bufs, uint32_t
 int dtt_publish(const dtt_handle* handles, uint32_t P, uint32_t first_chunk, uint32_t n_chunks,
                 uint32_t marks, cudaStream_t stream);
 
+/* Consumer GEMM, the peer-kernel side of a triggered plan ("Triggered Plans", Model: peer
+ * kernel wait(chunk); Memory ordering, Consumer): D = X . W^T, where X is rank `rank`'s buffer
+ * seen as [rows = buf_bytes / (2 K), K] bf16 (its gathered output), Wt = W^T [N, K] bf16
+ * (K-major, device) and D [rows, N] bf16 (device, rows ldd bytes apart).  Each 128-row block of
+ * X is loaded only after every chunk covering it has arrived at `rank` this round (its own
+ * chunks: once they are ready), polling at most max_polls times per chunk (0: the plan's), so
+ * the GEMM runs while the all-gather is still delivering.  tcgen05 / TMEM, fp32 accumulation,
+ * bf16 out, num_programs persistent CTAs (0: 148).  Call after dtt_plan_start, on a stream
+ * other than the copy stream.  A wait that runs out adds 1 to *err (device uint32) and the
+ * kernel stops.  Requirements: N % 128 == 0, K % 64 == 0, buf_bytes a multiple of 256 K,
+ * 16-byte aligned Wt, D and ldd.  The GEMM's shared-memory ring leaves no room for the
+ * bulk-copy copier's ring on the same SM, so the overlap needs the vector copier; beside the
+ * bulk copier the GEMM starts only as the copier's CTAs leave.  The first call for a (rank, K)
+ * builds a small table on the device (stream-ordered).
+ * Errors: DTT_EINVAL, DTT_ESTATE (plan not RUNNING), DTT_ECUDA. */
+int dtt_gemm_consumer(dtt_plan* plan, uint32_t rank, const void* Wt, uint32_t N, uint32_t K, void* D,
+                      uint64_t ldd, uint32_t num_programs, uint64_t max_polls, uint32_t* err,
+                      cudaStream_t stream);
+
 /* Consumer: rank `rank` waits for every chunk of the other ranks (in global id order, with
  * the device-side wait, at most max_polls polls each) and copies its regions from the rank's
  * own buffer bufs[rank] to the same offsets of `dst` (device, buf_bytes long) -- data read

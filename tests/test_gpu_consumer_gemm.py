@@ -1,0 +1,82 @@
+"""GPU: the consumer GEMM, the peer-kernel side of a triggered plan.  It is launched before the
+producer, so it can only be right if every row block waits for its chunks: the producer's
+values change every round, and a block read before its chunks arrived would hold the previous
+round's data.  The product is checked against the oracle's fp64 product of the gathered buffer
+the oracle computes for the same round (relative Frobenius error <= 1e-2)."""
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from gpu_common import oracle_plan, oracle_round
+from oracle import gemm as OG
+from oracle import plan as OP
+
+pytestmark = pytest.mark.gpu
+
+if torch.cuda.is_available():
+    from conftest import ensure_built
+    ensure_built()
+    import device_triggered_transfers_gb300 as D
+    from device_triggered_transfers_gb300 import runner
+
+TOL = 1e-2
+
+
+def _weights(N, K, seed):
+    g = torch.Generator().manual_seed(seed)
+    return (torch.randn(N, K, generator=g) / K ** 0.5).to(torch.bfloat16)
+
+
+@pytest.mark.parametrize("q,N2,programs", [(0, 256, 0), (3, 384, 7), (1, 128, 148)])
+def test_consumer_gemm_waits_for_its_rows(q, N2, programs):
+    w = W.small(W.C2, M=512, N=1024, num_chunks=4, rounds=3)      # 4 ranks x 4 chunks of 128 rows
+    K = w.N
+    rows = w.buf_bytes // (2 * K)
+    Wt = _weights(N2, K, 77 + q)
+    Wt_dev = Wt.cuda()
+    out = torch.zeros(rows, N2, dtype=torch.bfloat16, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    cons = torch.cuda.Stream()
+    st = runner.make(w)                                      # the vector copier: no shared memory
+    o = oracle_plan(w)
+    Wt64 = Wt.to(torch.float64).numpy()
+    torch.cuda.synchronize()
+    try:
+        for R in (1, 2, 3):
+            h = st.plan.start(st.producer_stream)
+            st.plan.gemm_consumer(q, Wt_dev, out, N2, K, err, num_programs=programs, stream=cons)
+            D.dtt_fill_producer(st.buf_ptrs, st.desc, h, st.producer_stream)
+            rep = st.plan.wait()
+            cons.synchronize()
+            assert rep.status == D.OK and int(err.item()) == 0
+            assert oracle_round(o, w)[0] == OP.OK
+            X = torch.from_numpy(o.bufs[q].copy()).view(torch.bfloat16).view(rows, K)
+            ref = OG.product(X.to(torch.float64).numpy(), Wt64)
+            got = out.cpu().to(torch.float64).numpy()
+            e = OG.rel_frobenius(got, ref)
+            assert e <= TOL and e < 5e-3, (R, e)
+            st.plan.next_round()
+            o.next_round()
+    finally:
+        st.plan.close()
+
+
+def test_consumer_gemm_rejects_bad_shapes():
+    w = W.small(W.C2, M=256, N=1024, num_chunks=2)
+    st = runner.make(w)
+    out = torch.zeros(8, dtype=torch.bfloat16, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    Wt = torch.zeros(128, 1024, dtype=torch.bfloat16, device="cuda")
+    try:
+        with pytest.raises(D.DttError) as e:            # not RUNNING
+            st.plan.gemm_consumer(0, Wt, out, 128, 1024, err)
+        assert e.value.code == D.ESTATE
+        h = st.plan.start(st.producer_stream)
+        with pytest.raises(D.DttError) as e:            # N not a multiple of 128
+            st.plan.gemm_consumer(0, Wt, out, 100, 1024, err)
+        assert e.value.code == D.EINVAL
+        D.dtt_fill_producer(st.buf_ptrs, st.desc, h, st.producer_stream)
+        assert st.plan.wait().status == D.OK
+    finally:
+        st.plan.close()
