@@ -174,6 +174,47 @@ def time_oracle(w, budget_s: float = 10.0, max_rounds: int = 1000):
     return sw.delivered_bytes_per_round() * n / dt / 1e9, n, dt, what
 
 
+def time_oracle_threaded(w, budget_s: float = 10.0, max_rounds: int = 1000):
+    """The threaded oracle (one producer thread per rank, one copier thread per (source, peer)
+    queue, gate words under a lock) on the same sample as time_oracle; GB/s delivered and the
+    thread count."""
+    from oracle import hashfill as H
+    from oracle.run import make_plan as oracle_plan
+    from oracle.threaded import ThreadedRound
+    sw, what = oracle_sample_workload(w)
+    if w.kind == "tile_chunks":     # one tile row per rank: a round of many small regions
+        sw, what = W.small(w, M=min(w.M, w.BM)), f"{min(w.M, w.BM)} of {w.M} rows per rank"
+    o = oracle_plan(sw)
+    n, t0 = 0, time.perf_counter()
+    while n < max_rounds:
+        data = {}
+
+        def write_unit(rank, c, u, o=o, data=data):
+            if rank not in data:        # the rank's slice for this round, computed by its thread
+                data[rank] = H.fill_slice_bytes(sw.dtype, sw.seed, rank, o.round, sw.M, sw.N)
+            base = sw.slice_offset(rank)
+            regs = o.chunks[c].regions
+            # one region per writer (tiles): writer u stores tile u; otherwise writer 0 stores
+            # the chunk and the others only mark
+            mine = [regs[u]] if len(regs) == o.chunks[c].writers else (regs if u == 0 else [])
+            for (off, nb, rows, pitch) in mine:
+                for i in range(rows):
+                    a = off + i * pitch
+                    o.bufs[rank][a:a + nb] = data[rank][a - base:a - base + nb]
+
+        order = {r: [(c, u) for c in o.chunks_of(r) for u in range(o.chunks[c].writers)]
+                 for r in sw.senders()}
+        status = ThreadedRound(o, write_unit, order, max_polls=10 ** 6, poll_sleep=1e-5).run()
+        assert status[0] == "OK", status
+        o.next_round()
+        n += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    threads = len(sw.senders()) * (sw.P - 1) + len(sw.senders())
+    return sw.delivered_bytes_per_round() * n / dt / 1e9, n, dt, what, threads
+
+
 def time_oracle_gemm(w, budget_s: float = 10.0, rows: int = 128):
     """The oracle on a sample of the GEMM workload: C_r for `rows` rows of every rank (fp64
     product of the bf16 operands, numpy's multithreaded BLAS), rounded to bf16 and copied to
@@ -443,6 +484,10 @@ def run_ours(args):
             cores = 1
         cpu = {"value": v, "unit": "GB/s", "cores": cores, "kind": "oracle",
                "sample": f"{what}; {n} oracle round(s) in {dt:.1f} s"}
+        if not gemm:    # the same sample with threads as ranks and copier queues
+            vt, nt, dtt, what_t, threads = time_oracle_threaded(w, budget_s=args.cpu_seconds / 2)
+            cpu["threaded"] = {"value": vt, "threads": threads, "host_cores": os.cpu_count(),
+                               "sample": f"{what_t}; {nt} threaded oracle round(s) in {dtt:.1f} s"}
     lat_sorted = sorted(lat) or [0]
     mode = "copier launched after the producer (no overlap)" if args.deferred else \
         "copier launched at plan_start, overlapping the producer"
