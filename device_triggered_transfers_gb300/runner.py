@@ -151,7 +151,8 @@ def bench_launch(w) -> dict:
         return {"threads": 1024, "opts": opts}
     if w.K == 0:
         return {"opts": dtt_plan_opts_default(method=1, piece_bytes=16384, stages=12)}
-    return {}
+    # the GEMM producer: two 256-thread vector copier CTAs per SM beside the GEMM's CTA
+    return {"opts": dtt_plan_opts_default(copier_threads=256, ctas_per_sm=2)}
 
 
 @dataclass

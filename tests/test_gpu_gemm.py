@@ -83,7 +83,7 @@ def test_gemm_producer_small(P, M, N, K, NP):
 def test_gemm_producer_full_size():
     w = W.C5
     A, Bt = W.gemm_inputs(w.P, w.M, w.N, w.K, w.seed)
-    st = runner.make_gemm(w, A, Bt)
+    st = runner.make_gemm(w, A, Bt, opts=runner.bench_launch(w)["opts"])    # the benchmark's launch
     rows = np.unique(np.concatenate([[0, 127, 128, w.M - 1],
                                      np.random.default_rng(7).integers(0, w.M, 60)]))
     try:
