@@ -623,6 +623,65 @@ def run_consumer(args):
     return 0
 
 
+def run_ce_fanout(args):
+    """Copy engines against the SM copier on the same fan-out: every rank's slice copied to the
+    P-1 peers with one device-to-device cudaMemcpyAsync per (source, peer), spread over a few
+    streams and not gated (the copy-engine transport the pages pre-arm), against this build's
+    copier moving the same bytes with its gates already open (a deferred plan)."""
+    import torch
+    import device_triggered_transfers_gb300 as D
+    from device_triggered_transfers_gb300 import runner
+    w = workload(args)
+    S = w.slice_bytes
+    launch = dict(runner.bench_launch(w))
+    opts = launch.pop("opts", None) or D.dtt_plan_opts_default()
+    opts.deferred_copier, opts.time_copier = 1, 1
+    st = runner.make(w, opts=opts, **launch)
+    prod = st.producer_stream
+    res = {}
+    for n_streams in (1, w.P - 1, w.P * (w.P - 1)):
+        streams = [torch.cuda.Stream() for _ in range(n_streams)]
+
+        def fan_out():
+            i = 0
+            for r in w.senders():
+                src = st.bufs[r][w.slice_offset(r):w.slice_offset(r) + S]
+                for q in range(w.P):
+                    if q == r:
+                        continue
+                    with torch.cuda.stream(streams[i % n_streams]):
+                        st.bufs[q][w.slice_offset(r):w.slice_offset(r) + S].copy_(src, non_blocking=True)
+                    i += 1
+        for _ in range(3):
+            fan_out()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        reps = 20
+        for _ in range(reps):
+            fan_out()
+        torch.cuda.synchronize()
+        dt = (time.perf_counter() - t0) / reps
+        res[f"ce_{n_streams}_streams_ms"] = dt * 1e3
+        res[f"ce_{n_streams}_streams_gbs_delivered"] = w.delivered_bytes_per_round() / dt / 1e9
+    for _ in range(3):                  # the SM copier alone: producer first, then the copier
+        runner.run_round(st)
+        st.plan.next_round()
+    c0 = st.plan.stats()
+    for _ in range(20):
+        runner.run_round(st)
+        st.plan.next_round()
+    c1 = st.plan.stats()
+    st.plan.close()
+    cop_ms = (c1[1] - c0[1]) / (c1[2] - c0[2])
+    res["sm_copier_ms"] = cop_ms
+    res["sm_copier_gbs_delivered"] = w.delivered_bytes_per_round() / (cop_ms / 1e3) / 1e9
+    line = {"metric": "fan-out of one all-gather round: copy engines vs the SM copier (1 GB300)",
+            "unit": "GB/s delivered", "higher_is_better": True,
+            "config": {"workload": describe(w, launch)}, **res}
+    print(json.dumps(line))
+    return 0
+
+
 def run_barrier(args):
     """Latency of the N-rank notify/wait barrier and the builtin reveal (P = 8 virtual ranks,
     reveal SIZE = 256): one cooperative launch per barrier, CUDA events around K of them."""
@@ -685,6 +744,8 @@ def main(argv=None):
     ap.add_argument("--isolated-rounds", type=int, default=20)
     ap.add_argument("--barrier", action="store_true",
                     help="time the N-rank barrier and the builtin reveal instead")
+    ap.add_argument("--ce-fanout", action="store_true",
+                    help="time the fan-out with copy engines (device-to-device memcpy) against the SM copier")
     ap.add_argument("--consumer", action="store_true",
                     help="time the all-gather with a consumer GEMM over its output, overlapped")
     ap.add_argument("--consumer-n", type=int, default=4096)
@@ -699,6 +760,8 @@ def main(argv=None):
         return run_barrier(args)
     if args.consumer and args.impl == "ours":
         return run_consumer(args)
+    if args.ce_fanout and args.impl == "ours":
+        return run_ce_fanout(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)
