@@ -149,8 +149,8 @@ def bench_launch(w) -> dict:
             g = max(1, min(8, 152 // (len(w.senders()) * NP)))
             return {"group": g, "threads": 512, "opts": opts}
         return {"threads": 1024, "opts": opts}
-    if w.K == 0:
-        return {"opts": dtt_plan_opts_default(method=1, piece_bytes=16384, stages=12)}
+    if w.K == 0:       # the tiled fill in 128-thread CTAs: more of them resident per SM
+        return {"threads": 128, "opts": dtt_plan_opts_default(method=1, piece_bytes=16384, stages=12)}
     # the GEMM producer: two 256-thread vector copier CTAs per SM beside the GEMM's CTA
     return {"opts": dtt_plan_opts_default(copier_threads=256, ctas_per_sm=2)}
 
