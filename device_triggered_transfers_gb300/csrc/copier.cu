@@ -111,7 +111,7 @@ __device__ __forceinline__ bool poll_gate(const uint64_t* ready, uint32_t round,
     }
 }
 
-__global__ void __launch_bounds__(1024) copier_kernel(const __grid_constant__ CopierParams p) {
+__device__ __forceinline__ void copier_body(const CopierParams& p) {
     __shared__ int s_go[2];
     const uint32_t b = blockIdx.x;
     uint32_t s = 0;
@@ -162,6 +162,18 @@ __global__ void __launch_bounds__(1024) copier_kernel(const __grid_constant__ Co
             }
         }
     }
+}
+
+// This round's copier CTAs count themselves out once their work (and every store and arrival
+// of it) is done; the check waits for the count instead of following the copier on its stream.
+__device__ __forceinline__ void count_out(const CopierParams& p) {
+    asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(&p.status->copier_exit) : "memory");
+}
+
+__global__ void __launch_bounds__(1024) copier_kernel(const __grid_constant__ CopierParams p) {
+    copier_body(p);
+    __syncthreads();
+    if (threadIdx.x == 0) count_out(p);
 }
 
 // ---- bulk-copy (TMA) path ----------------------------------------------------------------------
@@ -245,9 +257,8 @@ __device__ __forceinline__ void fence_proxy_async_global() {
     asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
-__global__ void __launch_bounds__(32) copier_bulk_kernel(const __grid_constant__ CopierParams p) {
+__device__ __forceinline__ void copier_bulk_body(const CopierParams& p) {
     extern __shared__ __align__(1024) uint8_t smem[];
-    if (threadIdx.x != 0) return;
     const uint32_t b = blockIdx.x;
     uint32_t s = 0;
     while (s + 1 < p.P && b >= p.cta_base[s + 1]) ++s;
@@ -352,10 +363,33 @@ __global__ void __launch_bounds__(32) copier_bulk_kernel(const __grid_constant__
         if (!mbar_wait(smem_addr(bars + idx % S), (uint32_t)((idx / S) & 1))) break;
 }
 
+__global__ void __launch_bounds__(32) copier_bulk_kernel(const __grid_constant__ CopierParams p) {
+    if (threadIdx.x != 0) return;       // one thread drives the CTA's bulk copies
+    copier_bulk_body(p);
+    count_out(p);
+}
+
 // wait()'s completion check, run after the copier and the producer: one flag per chunk, written
 // straight into the mapped host block.  The last CTA to finish copies the status words out,
 // zeroes them for the next round, and only then stores the sequence number the host polls for.
 __global__ void check_kernel(const __grid_constant__ CheckParams p) {
+    // launched after the producers on their stream; the copier counts its CTAs out
+    if (threadIdx.x == 0) {
+        uint32_t late = 0;
+        if (p.copier_ctas) {
+            late = 1;
+            uint32_t ns = 0;
+            for (uint64_t i = 0; i < p.max_polls; ++i) {
+                uint32_t n;
+                asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(n) : "l"(&p.status->copier_exit) : "memory");
+                if (n >= p.copier_ctas) { late = 0; break; }
+                __nanosleep(ns);
+                ns = ns < 1024 ? ns + 64 : 1024;
+            }
+        }
+        if (late) atomicExch(&p.status->check_late, 1u);
+    }
+    __syncthreads();
     for (uint32_t c = blockIdx.x * blockDim.x + threadIdx.x; c < p.n_global;
          c += gridDim.x * blockDim.x) {
         const ChunkDesc cd = p.chunks[c];
@@ -393,11 +427,15 @@ __global__ void check_kernel(const __grid_constant__ CheckParams p) {
     hs[1] = d->copier_timeouts;
     hs[2] = d->timeout_inv;
     hs[3] = d->bulk_timeouts;
+    hs[5] = d->copier_exit;
+    hs[6] = d->check_late;
     d->misuse = 0;
     d->copier_timeouts = 0;
     d->timeout_inv = 0;
     d->bulk_timeouts = 0;
     d->check_arrive = 0;
+    d->copier_exit = 0;
+    d->check_late = 0;
     asm volatile("fence.acq_rel.sys;\n\t"
                  "st.release.sys.global.u32 [%0], %1;" ::"l"(&p.host->done), "r"(p.seq) : "memory");
 }

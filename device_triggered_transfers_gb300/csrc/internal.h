@@ -78,7 +78,9 @@ struct DevStatus {
     uint32_t timeout_inv;       // 0xFFFFFFFF - (smallest chunk id a copier CTA gave up on); 0: none
     uint32_t bulk_timeouts;     // bulk-copy waits (mbarrier, bulk groups) that gave up
     uint32_t check_arrive;      // check_kernel CTAs done with their chunks (the last one resets it)
-    uint32_t pad[3];
+    uint32_t copier_exit;       // copier CTAs of this round that have finished
+    uint32_t check_late;        // 1: the check gave up waiting for the copier
+    uint32_t pad;
 };
 
 // A round's outcome in pinned, device-mapped host memory, written by check_kernel itself so that
@@ -118,6 +120,8 @@ struct CheckParams {
     uint32_t n_global;
     uint32_t round;
     uint32_t seq;               // stored in host->done once every flag and status word is there
+    uint32_t copier_ctas;       // wait until this many copier CTAs have finished (0: no copier)
+    uint64_t max_polls;         // bound of that wait
     DevStatus* status;          // the round's device status; the last CTA copies it out and zeroes it
     HostStatus* host;           // device address of the mapped host block
     uint8_t* host_flags;        // device address of its flag bytes

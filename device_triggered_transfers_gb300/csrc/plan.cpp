@@ -756,9 +756,11 @@ int dtt_plan_wait(dtt_plan* p, dtt_report* report) {
     if (p->state != DTT_PLAN_RUNNING) return fail(DTT_ESTATE, "dtt_plan_wait: plan is not RUNNING (state %d)", p->state);
     const int lc = dtt_plan_launch_copier(p);    // deferred plans: the copier runs now
     if (lc != DTT_OK) return lc;
-    DTT_CUDA_TRY(cudaEventRecord(p->ev_producer, p->producer_stream));
-    DTT_CUDA_TRY(cudaStreamWaitEvent(p->copy_stream, p->ev_producer, 0));
+    // The check follows the producers on their stream and waits on the device for the copier's
+    // CTAs to count themselves out (no event between the streams, no launch gap after the copier).
     CheckParams ck{};
+    ck.copier_ctas = p->copier_launched ? p->copier_ctas : 0;
+    ck.max_polls = 8 * p->opts.max_polls;
     ck.gates = p->d_gates;
     ck.chunks = p->d_chunks;
     ck.P = p->P;
@@ -768,7 +770,7 @@ int dtt_plan_wait(dtt_plan* p, dtt_report* report) {
     ck.status = p->d_status;
     ck.host = p->h_status_dev;
     ck.host_flags = p->h_status_dev ? reinterpret_cast<uint8_t*>(p->h_status_dev + 1) : nullptr;
-    DTT_CUDA_TRY(launch_check(ck, p->copy_stream));
+    DTT_CUDA_TRY(launch_check(ck, p->producer_stream));
     // The check stores its sequence number last, after every flag and status word: poll that
     // word, and ask the stream now and then so that a failed launch or a dead context ends the
     // wait with the CUDA error instead of spinning.
@@ -776,7 +778,7 @@ int dtt_plan_wait(dtt_plan* p, dtt_report* report) {
     for (uint64_t spin = 1;; ++spin) {
         if (__atomic_load_n(done, __ATOMIC_ACQUIRE) == ck.seq) break;
         if ((spin & 4095) == 0) {
-            const cudaError_t e = cudaStreamQuery(p->copy_stream);
+            const cudaError_t e = cudaStreamQuery(p->producer_stream);
             if (e == cudaErrorNotReady) continue;
             if (e != cudaSuccess) return fail(DTT_ECUDA, "dtt_plan_wait: %s", cudaGetErrorString(e));
             if (__atomic_load_n(done, __ATOMIC_ACQUIRE) == ck.seq) break;
@@ -787,6 +789,7 @@ int dtt_plan_wait(dtt_plan* p, dtt_report* report) {
     rep.round = p->round;
     rep.copier_timeouts = p->h_status->st.copier_timeouts;
     rep.device_status = p->h_status->st.misuse;
+    const bool late = p->h_status->st.check_late != 0;
     for (uint32_t c = 0; c < p->n_global; ++c) {
         if (p->h_flags[c] == 2) {
             if (rep.n_extra < DTT_REPORT_MAX) rep.extra_chunks[rep.n_extra] = c;
@@ -805,6 +808,8 @@ int dtt_plan_wait(dtt_plan* p, dtt_report* report) {
     } else if (rep.n_short) {
         rc = fail(DTT_ETIMEDOUT, "dtt_plan_wait: %u chunk(s) short in round %u (first: %u)",
                   rep.n_short, p->round, rep.short_chunks[0]);
+    } else if (late) {
+        rc = fail(DTT_ETIMEDOUT, "dtt_plan_wait: the copier had not finished when the check gave up");
     }
     rep.status = rc;
     if (report) *report = rep;

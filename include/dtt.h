@@ -278,9 +278,12 @@ int dtt_plan_handle(const dtt_plan* plan, uint32_t rank, dtt_handle* out);
 
 /* Block until the round is complete everywhere, then check it with a kernel: every chunk got
  * exactly writers marks this round and arrived at every peer ("Triggered Plans", Gates and
- * rounds; "Triggered SDMA Plans", Design notes, completion).  Fills *report when non-NULL.
+ * rounds; "Triggered SDMA Plans", Design notes, completion).  The check kernel is queued on
+ * the producer stream (after everything the producers queued) and waits on the device, at
+ * most 8 x max_polls polls, for the round's copier CTAs to finish; it writes its verdict into
+ * mapped host memory, which this call polls.  Fills *report when non-NULL.
  * Returns DTT_OK (plan DONE), DTT_EEXTRA or DTT_ETIMEDOUT (plan FAILED; the report names the
- * chunks), DTT_ESTATE (not RUNNING) or DTT_ECUDA. */
+ * chunks, or the copier had not finished), DTT_ESTATE (not RUNNING) or DTT_ECUDA. */
 int dtt_plan_wait(dtt_plan* plan, dtt_report* report);
 
 /* Advance to the next round: "done reading this round's data" ("Triggered Plans", The kernel
