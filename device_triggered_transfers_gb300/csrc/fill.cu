@@ -119,6 +119,16 @@ __device__ __forceinline__ void write_block(const FillParams& p, char* base, uin
     constexpr uint32_t VPE = 16 / E::bytes;     // elements per 16-byte vector
     if (ra >= rb || cols == 0) return;
     const uint32_t nrows = (uint32_t)(rb - ra);
+    if (p.vec && c0 == 0 && cols == p.N && p.pitch == p.N * E::bytes &&
+        (uint64_t)nrows * (p.N / VPE) < (1ull << 32)) {
+        // whole rows that follow each other: one contiguous range, vector v at byte 16 v of it
+        const uint32_t nv = nrows * (uint32_t)(p.N / VPE), step = blockDim.x * VPE;
+        uint4* d = reinterpret_cast<uint4*>(base + ra * p.pitch) + threadIdx.x;
+        uint32_t idx = (uint32_t)(ra * p.N) + threadIdx.x * VPE;
+        for (uint32_t v = threadIdx.x; v < nv; v += blockDim.x, d += blockDim.x, idx += step)
+            *d = E::pack(vec_base(idx, salt));
+        return;
+    }
     uint32_t nvec = 0;
     if (p.vec) {
         // thread t takes vectors t, t + blockDim, ... of the block; (row i, vector k) advances

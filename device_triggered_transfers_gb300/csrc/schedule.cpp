@@ -54,7 +54,7 @@ const char* dtt_last_error(void) { return g_err; }
 int dtt_tile_of(const dtt_order* order, uint64_t step, uint32_t tiles_m, uint32_t tiles_n,
                 uint32_t* tm, uint32_t* tn) {
     if (!tm || !tn || tiles_m == 0 || tiles_n == 0) return fail(DTT_EINVAL, "dtt_tile_of: bad args");
-    const uint32_t kind = order ? order->kind : DTT_ORDER_ROW_MAJOR;
+    const uint32_t kind = order ? order->kind : (uint32_t)DTT_ORDER_ROW_MAJOR;
     const uint32_t gm = order ? order->group_m : 0;
     if (kind != DTT_ORDER_ROW_MAJOR && kind != DTT_ORDER_GROUPED)
         return fail(DTT_EINVAL, "dtt_tile_of: unknown order kind %u", kind);
@@ -138,7 +138,7 @@ int dtt_schedule_tile_chunks(uint64_t base_off, uint64_t M, uint64_t N, uint32_t
         return fail(DTT_EINVAL, "dtt_schedule_tile_chunks: too many tiles");
     const uint32_t tiles_m = (uint32_t)tiles_m64, tiles_n = (uint32_t)tiles_n64;
     const uint64_t T = tiles_m64 * tiles_n64;
-    const uint32_t kind = order ? order->kind : DTT_ORDER_ROW_MAJOR;
+    const uint32_t kind = order ? order->kind : (uint32_t)DTT_ORDER_ROW_MAJOR;
     const uint32_t gm = order ? order->group_m : 0;
     if (!fn && kind != DTT_ORDER_ROW_MAJOR && !(kind == DTT_ORDER_GROUPED && gm > 0))
         return fail(DTT_EINVAL, "dtt_schedule_tile_chunks: bad builtin order");
