@@ -629,6 +629,10 @@ int dtt_plan_create(void* const* bufs, uint64_t buf_bytes, uint32_t P,
         delete p;
         return fail(DTT_EINVAL, "dtt_plan_create: bad options (piece_bytes %% 16, threads %% 32 <= 1024, method)");
     }
+    if (o.method == DTT_COPY_TMA && o.stages < 2) {      // the ring loads ahead by stages - 1
+        delete p;
+        return fail(DTT_EINVAL, "dtt_plan_create: the bulk-copy path needs at least 2 stages");
+    }
     if (o.method == DTT_COPY_TMA && bulk_smem_bytes(bulk_stage_bytes(o.piece_bytes), o.stages) > kBulkSmemMax) {
         delete p;
         return fail(DTT_EINVAL, "dtt_plan_create: stages x piece_bytes exceeds %zu bytes of shared memory",

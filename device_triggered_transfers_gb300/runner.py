@@ -128,8 +128,9 @@ def run_round(st: Setup, raise_on_error: bool = True):
 def bench_launch(w) -> dict:
     """The launch configuration the benchmark times for workload ``w`` (tests use it too).
 
-    Chunked workloads: the bulk-copy copier (one warp and a shared-memory ring per SM, so the
-    producer keeps the SM's threads and registers), and one program per rank made of a group of
+    Chunked workloads: the bulk-copy copier (three one-warp CTAs per SM, each with a ring of two
+    32 KiB stages, so the producer keeps the SM's threads and registers), and one program per
+    rank made of a group of
     38 CTAs (152 in all, one per SM) that writes the rank's chunks in order and marks each once,
     so every rank's chunk k opens in wave k and the copier follows the waves.
     whole(): the bulk-copy copier over the contiguous slices; the single chunk per rank opens only
@@ -137,9 +138,9 @@ def bench_launch(w) -> dict:
     tile_chunks (fill producer): the bulk-copy copier moving each tile as tensor-map boxes of
     16 KiB, twelve in flight per SM.  The GEMM producer keeps the vector copier: its own
     shared-memory ring leaves no room for a bulk-copy ring on the same SM."""
-    if w.kind == "chunks":
+    if w.kind == "chunks":     # three bulk-copy CTAs per SM: one thread alone cannot keep HBM busy
         return {"group": 38, "programs": 1, "threads": 256,
-                "opts": dtt_plan_opts_default(method=1, piece_bytes=65536, stages=3)}
+                "opts": dtt_plan_opts_default(method=1, piece_bytes=32768, stages=2, ctas_per_sm=3)}
     if w.kind == "whole":
         opts = dtt_plan_opts_default(method=1, piece_bytes=65536, stages=3)
         NP = w.num_programs

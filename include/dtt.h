@@ -185,8 +185,8 @@ typedef struct dtt_plan_opts {
                                 or wait() launches it after the work queued on the producer
                                 stream (no overlap; for profilers that serialise kernels) */
     uint32_t stages;         /* DTT_COPY_TMA: shared-memory stages per copier CTA, each
-                                piece_bytes long (stages * piece_bytes <= 200 KiB); 0 = as
-                                many as fit, at most 8 */
+                                piece_bytes long (2 <= stages, stages * piece_bytes <= 200 KiB);
+                                0 = as many as fit, at most 8 */
     uint32_t time_copier;    /* 1: time every copier launch with CUDA events on the copy
                                 stream (read with dtt_plan_stats) */
     uint32_t reserved;

@@ -143,6 +143,14 @@ def test_copier_must_leave_room_for_the_producer():
         st.plan.close()
 
 
+def test_bulk_copier_needs_two_stages():
+    bufs = [torch.zeros(WS.buf_bytes, dtype=torch.uint8, device="cuda") for _ in range(2)]
+    with pytest.raises(D.DttError) as e:
+        D.Plan(bufs, WS.buf_bytes, runner.schedules_for(WS),
+               D.dtt_plan_opts_default(method=D.COPY_TMA, piece_bytes=65536, stages=1))
+    assert e.value.code == D.EINVAL
+
+
 def test_close_mid_round_sends_chunks_as_they_stand():
     st = runner.make(WS)
     o = oracle_plan(WS)
