@@ -133,8 +133,9 @@ def bench_launch(w) -> dict:
     rank made of a group of
     38 CTAs (152 in all, one per SM) that writes the rank's chunks in order and marks each once,
     so every rank's chunk k opens in wave k and the copier follows the waves.
-    whole(): the bulk-copy copier over the contiguous slices; the single chunk per rank opens only
-    when the whole slice is written, so the fill gets as many CTAs as the writers allow.
+    whole(): the bulk-copy copier (two CTAs per SM, 2 x 56 KiB stages each) over the contiguous
+    slices; the single chunk per rank opens only when the whole slice is written, so the fill
+    gets as many CTAs as the writers allow.
     tile_chunks (fill producer): the bulk-copy copier moving each tile as tensor-map boxes of
     16 KiB, twelve in flight per SM.  The GEMM producer keeps the vector copier: its own
     shared-memory ring leaves no room for a bulk-copy ring on the same SM."""
@@ -142,7 +143,7 @@ def bench_launch(w) -> dict:
         return {"group": 38, "programs": 1, "threads": 256,
                 "opts": dtt_plan_opts_default(method=1, piece_bytes=32768, stages=2, ctas_per_sm=3)}
     if w.kind == "whole":
-        opts = dtt_plan_opts_default(method=1, piece_bytes=65536, stages=3)
+        opts = dtt_plan_opts_default(method=1, piece_bytes=57344, stages=2, ctas_per_sm=2)
         NP = w.num_programs
         if -(-w.M // -(-w.M // NP)) == NP:
             # one step per program: each writer becomes a group of CTAs (up to 8, enough to
