@@ -196,3 +196,34 @@ def test_bulk_copier_rejects_unaligned_regions():
     with pytest.raises(D.DttError) as e:
         runner.make(w, opts=D.dtt_plan_opts_default(method=D.COPY_TMA, piece_bytes=16384))
     assert e.value.code == D.EINVAL
+
+
+def test_many_rounds_keep_the_gates_and_data_right():
+    # 500 rounds of the benchmark's launch back to back: the gates follow the closed form of the
+    # round count, and the data is the last round's everywhere (sampled)
+    w = W.C2
+    R = 500
+    st = runner.make(w, **runner.bench_launch(w))
+    try:
+        for r in range(1, R + 1):
+            rep = runner.run_round(st)
+            assert rep.status == D.OK and rep.copier_timeouts == 0, r
+            if r < R:
+                st.plan.next_round()
+        g = st.plan.read_gates()
+        n_global, first, n_chunks, _ = st.plan.info()
+        for s in range(w.P):
+            for c in range(first[s], first[s] + n_chunks[s]):
+                assert int(g[s, c, D.GATE_READY]) == R and int(g[s, c, D.GATE_COUNTER]) == R
+                assert int(g[s, c, D.GATE_COMPLETION]) == R * (w.P - 1)
+                assert int(g[s, c, D.GATE_ERROR]) == 0
+                for q in range(w.P):
+                    if q != s:
+                        assert int(g[q, c, D.GATE_ARRIVAL]) == R
+        offs = sample_offsets(w, 1 << 15, seed=R)
+        want = expected_bytes(w, R, offs)
+        idx = torch.from_numpy(offs).cuda()
+        for q in range(w.P):
+            np.testing.assert_array_equal(st.bufs[q][idx].cpu().numpy(), want)
+    finally:
+        st.plan.close()

@@ -28,8 +28,11 @@ def _weights(N, K, seed):
     return (torch.randn(N, K, generator=g) / K ** 0.5).to(torch.bfloat16)
 
 
-@pytest.mark.parametrize("q,N2,programs", [(0, 256, 0), (3, 384, 7), (1, 128, 148)])
-def test_consumer_gemm_waits_for_its_rows(q, N2, programs):
+@pytest.mark.parametrize("q,N2,programs,bulk", [(0, 256, 0, False), (3, 384, 7, False),
+                                               (1, 128, 148, False), (2, 256, 0, True)])
+def test_consumer_gemm_waits_for_its_rows(q, N2, programs, bulk):
+    # bulk: beside the bulk-copy copier the GEMM's CTAs find no shared memory until the copier's
+    # CTAs leave, so there is no overlap, but the result must be the same
     w = W.small(W.C2, M=512, N=1024, num_chunks=4, rounds=3)      # 4 ranks x 4 chunks of 128 rows
     K = w.N
     rows = w.buf_bytes // (2 * K)
@@ -38,15 +41,19 @@ def test_consumer_gemm_waits_for_its_rows(q, N2, programs):
     out = torch.zeros(rows, N2, dtype=torch.bfloat16, device="cuda")
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     cons = torch.cuda.Stream()
-    st = runner.make(w)                                      # the vector copier: no shared memory
+    opts = D.dtt_plan_opts_default(method=D.COPY_TMA, piece_bytes=65536, stages=3) if bulk else None
+    st = runner.make(w, opts=opts)                           # default: the vector copier
     o = oracle_plan(w)
     Wt64 = Wt.to(torch.float64).numpy()
     torch.cuda.synchronize()
     try:
         for R in (1, 2, 3):
             h = st.plan.start(st.producer_stream)
-            st.plan.gemm_consumer(q, Wt_dev, out, N2, K, err, num_programs=programs, stream=cons)
+            if not bulk:
+                st.plan.gemm_consumer(q, Wt_dev, out, N2, K, err, num_programs=programs, stream=cons)
             D.dtt_fill_producer(st.buf_ptrs, st.desc, h, st.producer_stream)
+            if bulk:      # after the producer, so nothing it needs queues behind the GEMM's CTAs
+                st.plan.gemm_consumer(q, Wt_dev, out, N2, K, err, num_programs=programs, stream=cons)
             rep = st.plan.wait()
             cons.synchronize()
             assert rep.status == D.OK and int(err.item()) == 0
