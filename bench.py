@@ -542,9 +542,9 @@ def run_ours(args):
 def run_consumer(args):
     """The consumer side of the plan: a GEMM over rank 0's gathered buffer, D = X . W^T with
     X [P*M, N] (the all-gather's output) and W^T [consumer_n, N], each 128-row block loaded as
-    soon as its chunks have arrived.  Times, on the vector copier (the GEMM's shared-memory ring
-    leaves the bulk copier no room): the all-gather round alone, the GEMM alone (its chunks
-    already delivered), and the two overlapped in one round."""
+    soon as its chunks have arrived.  Times the all-gather round alone, the GEMM alone (its
+    chunks already delivered), and the two overlapped in one round; the copier is the bulk-copy
+    one with a ring small enough to leave the GEMM room, or the vector one."""
     import torch
     import device_triggered_transfers_gb300 as D
     from device_triggered_transfers_gb300 import runner
@@ -559,8 +559,13 @@ def run_consumer(args):
     # the producer of the benchmark's launch (its chunks open one wave after another), with the
     # vector copier
     launch = {k: v for k, v in runner.bench_launch(w).items() if k != "opts"}
-    st = runner.make(w, opts=D.dtt_plan_opts_default(copier_threads=args.consumer_copier_threads),
-                     copy_stream=copy_stream, **launch)
+    if args.consumer_copier == "bulk":    # one CTA per SM with a ring small enough for the GEMM's
+        copts = D.dtt_plan_opts_default(method=D.COPY_TMA, piece_bytes=32768, stages=2)
+        copier_desc = "bulk copies, one CTA per SM, 2 x 32 KiB stages"
+    else:
+        copts = D.dtt_plan_opts_default(copier_threads=args.consumer_copier_threads)
+        copier_desc = f"vector (16-byte) path, {args.consumer_copier_threads} threads per CTA"
+    st = runner.make(w, opts=copts, copy_stream=copy_stream, **launch)
     prod = st.producer_stream
 
     def ag():
@@ -614,7 +619,7 @@ def run_consumer(args):
             "higher_is_better": False, "steps": K_, "value": ov_ms,
             "config": {"workload": describe(w, launch) + f"; consumer GEMM: rank 0's [{rows}, {K}] bf16 "
                                                            f"x W^T [{N2}, {K}], tcgen05, 148 CTAs",
-                       "copier": f"vector (16-byte) path, {args.consumer_copier_threads} threads per CTA"},
+                       "copier": copier_desc},
             "all_gather_ms": ag_ms, "gemm_alone_ms": gemm_ms,
             "sequential_ms": ag_ms + gemm_ms, "overlap_saving": 1.0 - ov_ms / (ag_ms + gemm_ms),
             "gemm_alone_tflops": flops / (gemm_ms / 1e3) / 1e12,
@@ -750,6 +755,7 @@ def main(argv=None):
                     help="time the all-gather with a consumer GEMM over its output, overlapped")
     ap.add_argument("--consumer-n", type=int, default=4096)
     ap.add_argument("--consumer-copier-threads", type=int, default=256)
+    ap.add_argument("--consumer-copier", choices=["vector", "bulk"], default="vector")
     ap.add_argument("--rows", type=int, default=0,
                     help="rows per rank instead of the workload's (a smaller case of the same "
                          "shape, for profiler captures; the default runs the workload as named)")

@@ -348,10 +348,15 @@ __device__ __forceinline__ bool wait_chunks(const dtt_handle& h, uint32_t c0, ui
     return true;
 }
 
-template <uint32_t TN>
+// Shared memory of the consumer with ST stages: a smaller ring lets it sit beside a bulk-copy
+// copier's ring on the same SM.
+template <uint32_t TN, uint32_t ST>
+constexpr uint32_t consumer_smem() { return 1024 + ST * (A_STAGE + Cfg<TN>::B_STAGE) + 256; }
+
+template <uint32_t TN, uint32_t ST>
 __global__ void __launch_bounds__(THREADS, 1) gemm_consumer_kernel(const __grid_constant__ ConsumerParams p) {
     using G = Cfg<TN>;
-    constexpr uint32_t STAGES = G::STAGES, B_STAGE = G::B_STAGE, TMEM_COLS = G::TMEM_COLS;
+    constexpr uint32_t STAGES = ST, B_STAGE = G::B_STAGE, TMEM_COLS = G::TMEM_COLS;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sA = smem;
@@ -758,13 +763,30 @@ static cudaError_t prepare_gemm() {
     return e;
 }
 
-template <uint32_t TN>
+template <uint32_t TN, uint32_t ST>
 static cudaError_t prepare_consumer() {
-    cudaError_t e = prepare_kernel(gemm_consumer_kernel<TN>);
+    cudaError_t e = prepare_kernel(gemm_consumer_kernel<TN, ST>);
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(gemm_consumer_kernel<TN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)Cfg<TN>::SMEM_BYTES);
+        e = cudaFuncSetAttribute(gemm_consumer_kernel<TN, ST>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)consumer_smem<TN, ST>());
     return e;
+}
+
+// The deepest ring (at most the producer form's) whose shared memory fits in `budget` bytes;
+// the full ring when none of the smaller ones fits either (the GEMM then waits for room).
+template <uint32_t TN, uint32_t ST>
+static void launch_consumer_ring(const ConsumerParams& cp, uint32_t ctas, uint64_t budget, cudaStream_t s) {
+    if constexpr (ST > 2) {
+        if (consumer_smem<TN, ST>() > budget) {
+            launch_consumer_ring<TN, ST - 1>(cp, ctas, budget, s);
+            return;
+        }
+    }
+    if (consumer_smem<TN, ST>() > budget) {
+        gemm_consumer_kernel<TN, Cfg<TN>::STAGES><<<ctas, THREADS, consumer_smem<TN, Cfg<TN>::STAGES>(), s>>>(cp);
+        return;
+    }
+    gemm_consumer_kernel<TN, ST><<<ctas, THREADS, consumer_smem<TN, ST>(), s>>>(cp);
 }
 
 int launch_gemm_consumer(const ConsumerLaunch& cl, cudaStream_t stream) {
@@ -784,9 +806,9 @@ int launch_gemm_consumer(const ConsumerLaunch& cl, cudaStream_t stream) {
     cp.K = cl.K;
     cp.err = cl.err;
     if (TN == 256)
-        gemm_consumer_kernel<256><<<cl.ctas, THREADS, Cfg<256>::SMEM_BYTES, stream>>>(cp);
+        launch_consumer_ring<256, Cfg<256>::STAGES>(cp, cl.ctas, cl.smem_budget, stream);
     else
-        gemm_consumer_kernel<128><<<cl.ctas, THREADS, Cfg<128>::SMEM_BYTES, stream>>>(cp);
+        launch_consumer_ring<128, Cfg<128>::STAGES>(cp, cl.ctas, cl.smem_budget, stream);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return fail(DTT_ECUDA, "dtt_gemm_consumer: launch failed: %s", cudaGetErrorString(e));
     return DTT_OK;
@@ -795,8 +817,14 @@ int launch_gemm_consumer(const ConsumerLaunch& cl, cudaStream_t stream) {
 cudaError_t preload_gemm_kernels() {
     cudaError_t e = prepare_gemm<128>();
     if (e == cudaSuccess) e = prepare_gemm<256>();
-    if (e == cudaSuccess) e = prepare_consumer<128>();
-    if (e == cudaSuccess) e = prepare_consumer<256>();
+    if (e == cudaSuccess) e = prepare_consumer<128, 6>();
+    if (e == cudaSuccess) e = prepare_consumer<128, 5>();
+    if (e == cudaSuccess) e = prepare_consumer<128, 4>();
+    if (e == cudaSuccess) e = prepare_consumer<128, 3>();
+    if (e == cudaSuccess) e = prepare_consumer<128, 2>();
+    if (e == cudaSuccess) e = prepare_consumer<256, 4>();
+    if (e == cudaSuccess) e = prepare_consumer<256, 3>();
+    if (e == cudaSuccess) e = prepare_consumer<256, 2>();
     if (e == cudaSuccess) e = prepare_kernel(gemm2_producer_kernel);
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(gemm2_producer_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)G2_SMEM);

@@ -186,6 +186,7 @@ struct ConsumerLaunch {
     uint64_t max_polls;
     uint32_t* err;
     uint32_t ctas;
+    uint64_t smem_budget;       // shared memory a consumer CTA can have beside the copier's CTAs
 };
 int launch_gemm_consumer(const ConsumerLaunch& cl, cudaStream_t stream);
 cudaError_t preload_fill_kernels();

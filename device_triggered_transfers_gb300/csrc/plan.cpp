@@ -1204,6 +1204,15 @@ int dtt_gemm_consumer(dtt_plan* p, uint32_t rank, const void* Wt, uint32_t N, ui
     cl.max_polls = max_polls ? max_polls : p->opts.max_polls;
     cl.err = err;
     cl.ctas = num_programs ? num_programs : 148;
+    // room beside the copier: an SM has 228 KiB of shared memory, 1 KiB of it reserved per CTA
+    int sms = 0;
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, p->device);
+    uint64_t copier_smem = 0;
+    if (p->opts.method == DTT_COPY_TMA && sms > 0) {
+        const uint64_t per_sm = (p->copier_ctas + (uint32_t)sms - 1) / (uint32_t)sms;
+        copier_smem = per_sm * (bulk_smem_bytes(bulk_stage_bytes(p->opts.piece_bytes), p->opts.stages) + 1024);
+    }
+    cl.smem_budget = copier_smem + 2048 < 228 * 1024 ? 228 * 1024 - copier_smem - 1024 : 0;
     return launch_gemm_consumer(cl, stream);
 }
 

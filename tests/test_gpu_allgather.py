@@ -114,6 +114,10 @@ def test_parity_c1_full():
     run_parity(W.C1, W.C1.rounds)
 
 
+def test_parity_c1_full_bench_launch():
+    run_parity(W.C1, W.C1.rounds, **runner.bench_launch(W.C1))
+
+
 def test_parity_c4a_full_stale_data_check():
     # 8 writers on one 4 MiB gate per rank, values change every round: a stale copy fails
     run_parity(W.C4A, W.C4A.rounds)

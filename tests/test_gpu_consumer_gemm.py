@@ -28,11 +28,13 @@ def _weights(N, K, seed):
     return (torch.randn(N, K, generator=g) / K ** 0.5).to(torch.bfloat16)
 
 
-@pytest.mark.parametrize("q,N2,programs,bulk", [(0, 256, 0, False), (3, 384, 7, False),
-                                               (1, 128, 148, False), (2, 256, 0, True)])
+@pytest.mark.parametrize("q,N2,programs,bulk", [(0, 256, 0, None), (3, 384, 7, None),
+                                               (1, 128, 148, None), (2, 256, 0, "full"),
+                                               (0, 256, 0, "small"), (3, 128, 0, "small")])
 def test_consumer_gemm_waits_for_its_rows(q, N2, programs, bulk):
-    # bulk: beside the bulk-copy copier the GEMM's CTAs find no shared memory until the copier's
-    # CTAs leave, so there is no overlap, but the result must be the same
+    # bulk "full": the bulk-copy copier's 3 x 64 KiB ring leaves the GEMM no shared memory until
+    # the copier's CTAs leave, so there is no overlap, but the result must be the same; "small":
+    # a 2 x 32 KiB ring leaves room for the GEMM's shorter ring, and the two overlap
     w = W.small(W.C2, M=512, N=1024, num_chunks=4, rounds=3)      # 4 ranks x 4 chunks of 128 rows
     K = w.N
     rows = w.buf_bytes // (2 * K)
@@ -41,7 +43,9 @@ def test_consumer_gemm_waits_for_its_rows(q, N2, programs, bulk):
     out = torch.zeros(rows, N2, dtype=torch.bfloat16, device="cuda")
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     cons = torch.cuda.Stream()
-    opts = D.dtt_plan_opts_default(method=D.COPY_TMA, piece_bytes=65536, stages=3) if bulk else None
+    opts = {None: None,
+            "full": D.dtt_plan_opts_default(method=D.COPY_TMA, piece_bytes=65536, stages=3),
+            "small": D.dtt_plan_opts_default(method=D.COPY_TMA, piece_bytes=32768, stages=2)}[bulk]
     st = runner.make(w, opts=opts)                           # default: the vector copier
     o = oracle_plan(w)
     Wt64 = Wt.to(torch.float64).numpy()
@@ -49,10 +53,10 @@ def test_consumer_gemm_waits_for_its_rows(q, N2, programs, bulk):
     try:
         for R in (1, 2, 3):
             h = st.plan.start(st.producer_stream)
-            if not bulk:
+            if bulk != "full":
                 st.plan.gemm_consumer(q, Wt_dev, out, N2, K, err, num_programs=programs, stream=cons)
             D.dtt_fill_producer(st.buf_ptrs, st.desc, h, st.producer_stream)
-            if bulk:      # after the producer, so nothing it needs queues behind the GEMM's CTAs
+            if bulk == "full":      # after the producer: nothing it needs queues behind the GEMM
                 st.plan.gemm_consumer(q, Wt_dev, out, N2, K, err, num_programs=programs, stream=cons)
             rep = st.plan.wait()
             cons.synchronize()
