@@ -1,0 +1,83 @@
+"""GPU: a user's own kernels drive a plan through the public device header alone
+(`include/dtt_device.cuh`): a producer that writes its chunks and calls dtt_mark_ready, and a
+consumer on a third stream, launched before the producer, that calls dtt_wait per chunk and
+copies what arrived.  The kernels follow the header's contract for code that runs during a
+round (loaded and given the library's shared-memory carveout before the first round).  They
+are compiled here from tests/user_kernels.cu."""
+import ctypes as C
+import os
+import subprocess
+import tempfile
+
+import numpy as np
+import pytest
+import torch
+
+from conftest import ROOT
+
+pytestmark = pytest.mark.gpu
+
+if torch.cuda.is_available():
+    from conftest import ensure_built
+    ensure_built()
+    import device_triggered_transfers_gb300 as D
+
+
+def _build():
+    out = os.path.join(tempfile.mkdtemp(prefix="dtt_user_"), "libuser.so")
+    subprocess.run(["nvcc", "-gencode", "arch=compute_103a,code=sm_103a", "-O2", "-std=c++17",
+                    "-shared", "-Xcompiler", "-fPIC", "-I", os.path.join(ROOT, "include"),
+                    os.path.join(ROOT, "tests", "user_kernels.cu"), "-o", out], check=True)
+    lib = C.CDLL(out)
+    lib.user_kernels_prepare.restype = C.c_int
+    lib.user_produce.argtypes = [C.POINTER(D.dtt_handle), C.c_void_p, C.c_uint64, C.c_void_p]
+    lib.user_consume.argtypes = [C.POINTER(D.dtt_handle), C.c_void_p, C.c_void_p, C.c_uint64,
+                                 C.c_uint64, C.c_void_p, C.c_void_p]
+    return lib
+
+
+def _values(rank, rnd, n):
+    """The bytes the user producer stores (the formula in user_kernels.cu, restated)."""
+    i = np.arange(n, dtype=np.uint64)
+    x = ((i * np.uint64(2654435761)) & np.uint64(0xFFFFFFFF)).astype(np.uint32)
+    x ^= np.uint32((rank * 0x9E3779B9) & 0xFFFFFFFF) ^ np.uint32((rnd * 0x85EBCA6B) & 0xFFFFFFFF)
+    x ^= x >> np.uint32(15)
+    return (x & np.uint32(0xFF)).astype(np.uint8)
+
+
+def test_user_producer_and_consumer_kernels():
+    lib = _build()
+    assert lib.user_kernels_prepare() == 0
+    P, n, chunk = 3, 4, 1 << 20                  # 3 ranks x 4 chunks of 1 MiB
+    S = n * chunk
+    bufs = [torch.zeros(P * S, dtype=torch.uint8, device="cuda") for _ in range(P)]
+    scheds = [D.dtt_schedule_chunks(r * S, n, chunk, chunk, n) for r in range(P)]
+    plan = D.Plan(bufs, P * S, scheds, D.dtt_plan_opts_default(method=D.COPY_TMA, piece_bytes=65536,
+                                                               stages=3))
+    for s in scheds:
+        s.free()
+    q = 1                                        # the consuming rank
+    dst = torch.zeros(P * S, dtype=torch.uint8, device="cuda")
+    status = torch.full((P * n,), 99, dtype=torch.int32, device="cuda")
+    prod, cons = torch.cuda.Stream(), torch.cuda.Stream()
+    torch.cuda.synchronize()
+    try:
+        for rnd in (1, 2, 3):
+            h = plan.start(prod)
+            assert lib.user_consume(C.byref(h[q]), C.c_void_p(bufs[q].data_ptr()),
+                                    C.c_void_p(dst.data_ptr()), chunk, 1 << 24,
+                                    C.c_void_p(status.data_ptr()), C.c_void_p(cons.cuda_stream)) == 0
+            for r in range(P):
+                assert lib.user_produce(C.byref(h[r]), C.c_void_p(bufs[r].data_ptr() + r * S), chunk,
+                                        C.c_void_p(prod.cuda_stream)) == 0
+            rep = plan.wait()
+            cons.synchronize()
+            assert rep.status == D.OK and rep.copier_timeouts == 0
+            assert status.cpu().tolist() == [0] * (P * n)
+            want = np.concatenate([_values(r, rnd, S) for r in range(P)])
+            np.testing.assert_array_equal(dst.cpu().numpy(), want)      # this round's data, all of it
+            for b in bufs:
+                np.testing.assert_array_equal(b.cpu().numpy(), want)
+            plan.next_round()
+    finally:
+        plan.close()

@@ -1,0 +1,69 @@
+// A user's own producer and consumer kernels driving a triggered plan through the public
+// device header alone (the peer-kernel side of "Triggered Plans", Model; the kernel author's
+// contract).  Built by tests/test_gpu_user_kernels.py into a temporary shared object.
+//
+// producer: CTA c writes chunk c of the rank's slice (one writer per chunk), then marks it.
+// consumer: CTA c waits for chunk c at rank q, then copies it to dst; status[c] = 0 or timeout.
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "dtt_device.cuh"
+
+namespace {
+
+// The byte a producer stores at slice offset i of `rank` in `round`: any pattern that changes
+// with the round, so that a stale copy is caught.
+__device__ __forceinline__ uint8_t value_at(uint32_t rank, uint32_t round, uint64_t i) {
+    uint32_t x = (uint32_t)i * 2654435761u ^ (rank * 0x9E3779B9u) ^ (round * 0x85EBCA6Bu);
+    x ^= x >> 15;
+    return (uint8_t)x;
+}
+
+__global__ void user_producer(dtt_handle h, uint8_t* slice, uint64_t chunk_bytes) {
+    const uint32_t c = blockIdx.x;
+    const uint64_t base = (uint64_t)c * chunk_bytes;
+    for (uint64_t i = threadIdx.x; i < chunk_bytes; i += blockDim.x)
+        slice[base + i] = value_at(h.rank, h.round, base + i);
+    dtt_mark_ready(h, h.first_chunk + c);      // the whole CTA, after its stores
+}
+
+__global__ void user_consumer(dtt_handle h, const uint8_t* buf, uint8_t* dst, uint64_t chunk_bytes,
+                              uint64_t max_polls, int32_t* status) {
+    const uint32_t c = blockIdx.x;              // global chunk id; chunk c covers bytes c * chunk_bytes
+    const int r = dtt_wait(h, c, max_polls);
+    if (threadIdx.x == 0) status[c] = r;
+    if (r != 0) return;
+    const uint64_t base = (uint64_t)c * chunk_bytes;
+    for (uint64_t i = threadIdx.x; i < chunk_bytes; i += blockDim.x) dst[base + i] = buf[base + i];
+}
+
+}  // namespace
+
+// What the documented contract asks of a user's kernels before the first round: loaded now,
+// and the library's shared-memory carveout.
+extern "C" int user_kernels_prepare(void) {
+    cudaFuncAttributes a{};
+    if (cudaFuncGetAttributes(&a, user_producer) != cudaSuccess) return 1;
+    if (cudaFuncGetAttributes(&a, user_consumer) != cudaSuccess) return 1;
+    if (cudaFuncSetAttribute(user_producer, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared) != cudaSuccess)
+        return 1;
+    if (cudaFuncSetAttribute(user_consumer, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared) != cudaSuccess)
+        return 1;
+    return 0;
+}
+
+extern "C" int user_produce(const dtt_handle* h, void* slice, uint64_t chunk_bytes, cudaStream_t s) {
+    if (h->n_chunks == 0) return 0;
+    user_producer<<<h->n_chunks, 256, 0, s>>>(*h, static_cast<uint8_t*>(slice), chunk_bytes);
+    return cudaGetLastError() == cudaSuccess ? 0 : 1;
+}
+
+extern "C" int user_consume(const dtt_handle* h, const void* buf, void* dst, uint64_t chunk_bytes,
+                            uint64_t max_polls, int32_t* status, cudaStream_t s) {
+    user_consumer<<<h->n_global, 256, 0, s>>>(*h, static_cast<const uint8_t*>(buf), static_cast<uint8_t*>(dst),
+                                              chunk_bytes, max_polls, status);
+    return cudaGetLastError() == cudaSuccess ? 0 : 1;
+}
