@@ -321,7 +321,8 @@ def run_ours(args):
     # stream costs the round a few microseconds); the kernel-timing pass after it runs the same
     # launches on a plan that times each copier launch itself (CUDA events in the library)
     opts = launch.pop("opts", None) or D.dtt_plan_opts_default()
-    opts.deferred_copier = 1 if args.deferred else 0
+    if args.deferred:
+        opts.deferred_copier = 1
     opts.time_copier = 0
     copier_method = {"method": opts.method, "piece_bytes": opts.piece_bytes, "stages": opts.stages,
                      "copier_threads": opts.copier_threads, "ctas_per_sm": opts.ctas_per_sm}
@@ -489,8 +490,9 @@ def run_ours(args):
             cpu["threaded"] = {"value": vt, "threads": threads, "host_cores": os.cpu_count(),
                                "sample": f"{what_t}; {nt} threaded oracle round(s) in {dtt:.1f} s"}
     lat_sorted = sorted(lat) or [0]
-    mode = "copier launched after the producer (no overlap)" if args.deferred else \
-        "copier launched at plan_start, overlapping the producer"
+    mode = {0: "copier launched at plan_start, overlapping the producer",
+            1: "copier launched after the producer (no overlap)",
+            2: "copier launched right after the producer's launch, overlapping it"}[opts.deferred_copier]
     kname = "copier_bulk_kernel" if copier_method["method"] == D.COPY_TMA else "copier_kernel"
     copier_roof = {"kernel": kname, "bound": "hbm", "achieved": achieved,
                    "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,

@@ -666,7 +666,11 @@ int dtt_plan_create(void* const* bufs, uint64_t buf_bytes, uint32_t P,
     }
     p->copier_ctas = o.copier_ctas ? o.copier_ctas : (uint32_t)sms * o.ctas_per_sm;
     p->copier_threads = o.copier_threads;
-    if (!o.deferred_copier) {
+    if (o.deferred_copier > 2) {
+        delete p;
+        return fail(DTT_EINVAL, "dtt_plan_create: deferred_copier is 0, 1 or 2");
+    }
+    if (o.deferred_copier != 1) {
         // The copier spins while the producer runs, so it must leave an SM room for producer
         // CTAs: at most half of its threads (2048) and half of its registers (64 Ki) per SM.
         int regs = 0;
@@ -750,8 +754,10 @@ int dtt_plan_launch_copier(dtt_plan* p) {
     if (!p) return fail(DTT_EINVAL, "dtt_plan_launch_copier: NULL plan");
     if (p->state != DTT_PLAN_RUNNING) return fail(DTT_ESTATE, "dtt_plan_launch_copier: plan is not RUNNING");
     if (p->copier_launched || !p->n_global) return DTT_OK;
-    DTT_CUDA_TRY(cudaEventRecord(p->ev_producer, p->producer_stream));
-    DTT_CUDA_TRY(cudaStreamWaitEvent(p->copy_stream, p->ev_producer, 0));
+    if (p->opts.deferred_copier == 1) {   // after the producers: no overlap
+        DTT_CUDA_TRY(cudaEventRecord(p->ev_producer, p->producer_stream));
+        DTT_CUDA_TRY(cudaStreamWaitEvent(p->copy_stream, p->ev_producer, 0));
+    }
     return launch_round_copier(p);
 }
 
@@ -998,6 +1004,7 @@ int dtt_allgather_host(dtt_plan* p, const void* const* host_slices, void* host_o
     dtt_handle h[DTT_MAX_RANKS];
     p->notify_host = host_out != nullptr;        // the copier stamps each chunk's arrival
     int rc = dtt_plan_start(p, stream, h);
+    if (rc == DTT_OK && p->opts.deferred_copier == 2) rc = dtt_plan_launch_copier(p);   // needed early
     p->notify_host = false;
     if (rc != DTT_OK) return rc;
     const uint32_t round = p->round;

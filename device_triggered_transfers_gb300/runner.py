@@ -143,7 +143,10 @@ def bench_launch(w) -> dict:
         return {"group": 38, "programs": 1, "threads": 256,
                 "opts": dtt_plan_opts_default(method=1, piece_bytes=32768, stages=2, ctas_per_sm=3)}
     if w.kind == "whole":
-        opts = dtt_plan_opts_default(method=1, piece_bytes=57344, stages=2, ctas_per_sm=2)
+        # the copier is launched after the producer's launch (it has nothing to do before the
+        # whole slice is written)
+        opts = dtt_plan_opts_default(method=1, piece_bytes=57344, stages=2, ctas_per_sm=2,
+                                     deferred_copier=2)
         NP = w.num_programs
         if -(-w.M // -(-w.M // NP)) == NP:
             # one step per program: each writer becomes a group of CTAs (up to 8, enough to

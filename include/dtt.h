@@ -181,9 +181,12 @@ typedef struct dtt_plan_opts {
                                 initial_round - 1 rounds had completed (round-limit tests) */
     uint64_t max_polls;      /* copier polls of one gate before it gives up; 0 = 2^22 */
     uint64_t max_regions;    /* capacity: regions in the plan; 0 = unlimited */
-    uint32_t deferred_copier;/* 1: start() does not launch the copier; dtt_plan_launch_copier
-                                or wait() launches it after the work queued on the producer
-                                stream (no overlap; for profilers that serialise kernels) */
+    uint32_t deferred_copier;/* 0: start() launches the copier.  1: dtt_plan_launch_copier or
+                                wait() launches it after the work queued on the producer
+                                stream (no overlap; for profilers that serialise kernels).
+                                2: dtt_plan_launch_copier (or wait()) launches it with no
+                                dependency, so the caller can launch its producer first and
+                                the copier right after it, the two still overlapping */
     uint32_t stages;         /* DTT_COPY_TMA: shared-memory stages per copier CTA, each
                                 piece_bytes long (2 <= stages, stages * piece_bytes <= 200 KiB);
                                 0 = as many as fit, at most 8 */
@@ -252,7 +255,7 @@ typedef struct dtt_report {
  * copy_stream: a non-blocking stream for the copier, or NULL to let the plan create (and
  * own) a high-priority one.  Creation succeeds for every rank or for none: on error nothing
  * stays allocated ("Triggered Plans", The kernel author's contract).
- * Unless opts->deferred_copier, the copier runs beside the producer, so its launch must leave
+ * Unless opts->deferred_copier is 1, the copier runs beside the producer, so its launch must leave
  * every SM room for producer CTAs: creation fails with DTT_EINVAL when the copier CTAs of one
  * SM would take more than 1024 threads or 32768 registers.
  * Errors: DTT_EINVAL, DTT_EOUTOFROWS, DTT_EOVERLAP, DTT_ECAPACITY, DTT_ENOMEM, DTT_ECUDA. */
@@ -268,9 +271,10 @@ int dtt_plan_create(void* const* bufs, uint64_t buf_bytes, uint32_t P,
  * item 1).  Errors: DTT_ESTATE (not PREPARED), DTT_EINVAL, DTT_ECUDA. */
 int dtt_plan_start(dtt_plan* plan, cudaStream_t producer_stream, dtt_handle* handles);
 
-/* Deferred plans (opts.deferred_copier = 1): launch this round's copier now on the copy
- * stream, ordered after the work queued so far on the producer stream.  A no-op when the copier
- * is already running.  Errors: DTT_ESTATE (not RUNNING), DTT_ECUDA. */
+/* Plans with opts.deferred_copier set: launch this round's copier now on the copy stream --
+ * for deferred_copier = 1 ordered after the work queued so far on the producer stream, for
+ * deferred_copier = 2 with no such dependency (it runs beside the producer).  A no-op when the
+ * copier is already running.  Errors: DTT_ESTATE (not RUNNING), DTT_ECUDA. */
 int dtt_plan_launch_copier(dtt_plan* plan);
 
 /* The handle of one rank for the current round.  Errors: DTT_EINVAL. */
