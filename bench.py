@@ -419,6 +419,8 @@ def run_ours(args):
 
     # gate-to-arrival latency and the copier window, from the gate timestamps of extra rounds
     lat, windows = [], []
+    _, _, n_chunks_all, _ = st.plan.info()
+    n_chunks_total = sum(n_chunks_all[r] for r in w.senders())
     for _ in range(args.latency_rounds):
         step()
         g = st.plan.read_gates()
@@ -490,6 +492,12 @@ def run_ours(args):
             cpu["threaded"] = {"value": vt, "threads": threads, "host_cores": os.cpu_count(),
                                "sample": f"{what_t}; {nt} threaded oracle round(s) in {dtt:.1f} s"}
     lat_sorted = sorted(lat) or [0]
+    lat_med = lat_sorted[len(lat_sorted) // 2]
+    lat_p99 = lat_sorted[min(len(lat_sorted) - 1, int(len(lat_sorted) * 0.99))]
+    # the ideal time of one chunk's fan-out at the measured copy peak: one read of the chunk and
+    # P-1 writes of it, (S_c + (P-1) S_c) / peak
+    chunk_mean = len(w.senders()) * w.slice_bytes / max(1, n_chunks_total)
+    ideal_ns = w.P * chunk_mean / (peak * 1e9) * 1e9
     mode = {0: "copier launched at plan_start, overlapping the producer",
             1: "copier launched after the producer (no overlap)",
             2: "copier launched right after the producer's launch, overlapping it"}[opts.deferred_copier]
@@ -529,9 +537,11 @@ def run_ours(args):
         "copier_window": ({"gbs_delivered": D_round / statistics.median(windows) / 1e9,
                            "hbm_frac": B_alg / statistics.median(windows) / 1e9 / peak}
                           if windows else None),
-        "gate_to_arrival_ns": {"median": lat_sorted[len(lat_sorted) // 2],
-                               "p99": lat_sorted[min(len(lat_sorted) - 1, int(len(lat_sorted) * 0.99))],
-                               "samples": len(lat)},
+        "gate_to_arrival_ns": {"median": lat_med, "p99": lat_p99, "samples": len(lat),
+                               "chunk_bytes_mean": chunk_mean,
+                               "ideal_chunk_ns": ideal_ns,
+                               "median_over_ideal": lat_med / ideal_ns if ideal_ns else None,
+                               "p99_over_ideal": lat_p99 / ideal_ns if ideal_ns else None},
         "e2e": e2e,
         "gpu_launches": 3 * K,
         "clocks": clocks.summary(),

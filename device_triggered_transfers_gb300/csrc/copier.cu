@@ -384,7 +384,7 @@ __global__ void check_kernel(const __grid_constant__ CheckParams p) {
                 asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(n) : "l"(&p.status->copier_exit) : "memory");
                 if (n >= p.copier_ctas) { late = 0; break; }
                 __nanosleep(ns);
-                ns = ns < 1024 ? ns + 64 : 1024;
+                ns = ns < 128 ? ns + 32 : 128;   // a late wake-up delays the whole round
             }
         }
         if (late) atomicExch(&p.status->check_late, 1u);
