@@ -36,8 +36,6 @@ DEFAULT_CONFIG = W.C2.name
 # of the same workload and launch configuration (the summaries under profiles/); absent until
 # taken, and dropped once the kernel changes.
 NCU_TRAFFIC = {("c2_chunks_p4", "copier_bulk_kernel"): 474083584,
-               # captured with 2000 rows per rank (--rows 2000) and scaled by the rows, 4x
-               ("c3_tiles_p8", "copier_bulk_kernel"): 8009500160,
                ("c5_gemm_p4", "gemm2_producer_kernel"): 166012672}
 
 
@@ -56,9 +54,13 @@ def describe(w, launch, copier=None) -> str:
     elif grp > 1:
         prod = (f"; producer: {launch.get('programs') or 'one per chunk'} program(s) per rank, each a "
                 f"group of {grp} CTAs marking each chunk once")
+    if launch.get("pace"):
+        prod += (f"; producer paced: a program writes chunk k once chunk k-{launch['pace']} of its "
+                 f"rank is delivered")
     cop = ""
     if copier is not None:
-        cop = ("; copier: bulk copies, %d x %d KiB stages per SM" % (copier["stages"], copier["piece_bytes"] >> 10)
+        cop = ("; copier: bulk copies, %d CTA(s) per SM with %d x %d KiB stages each"
+               % (copier["ctas_per_sm"], copier["stages"], copier["piece_bytes"] >> 10)
                if copier["method"] == 1 else
                "; copier: 16-byte vector copies, %d threads x %d CTA(s) per SM"
                % (copier["copier_threads"], copier["ctas_per_sm"]))
@@ -332,24 +334,30 @@ def run_ours(args):
         st = runner.make_gemm(w, A, Bt, opts=opts, copy_stream=copy_stream)
         w_sched = st.w
 
-        def produce(h):
+        def produce(h, deferred=False):
             D.dtt_gemm_producer(st.A, st.Bt, st.buf_ptrs, w.M, w.N, w.K, w.row_bytes, st.slice_offs,
                                 st.num_programs, h, st.err, prod)
     else:
         st = runner.make(w, opts=opts, copy_stream=copy_stream, **launch)
         w_sched = w
 
-        def produce(h):
-            D.dtt_fill_producer(st.buf_ptrs, st.desc, h, prod)
+        # a paced producer waits for the copier, so a plan whose copier starts only after the
+        # producer gets the same producer without pacing
+        desc_unpaced = type(st.desc).from_buffer_copy(st.desc)
+        desc_unpaced.pace = 0
+
+        def produce(h, deferred=False):
+            D.dtt_fill_producer(st.buf_ptrs, desc_unpaced if deferred else st.desc, h, prod)
     prod = st.producer_stream
 
     def make_step(plan, deferred):
-        """One round.  ev: two events around the producer launch (producer stream), or None."""
+        """One round.  ev: two events around the producer launch (producer stream), or None.
+        deferred: the plan's copier starts only after the producer."""
         def step(ev=None):
             h = plan.start(prod)
             if ev is not None:
                 ev[0].record(prod)
-            produce(h)
+            produce(h, deferred)
             if ev is not None:
                 ev[1].record(prod)
             if deferred:      # the copier starts once the producer has finished
@@ -375,7 +383,7 @@ def run_ours(args):
         prod_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs) if producer_events else None
         return e0.elapsed_time(e1) / 1e3, cop, prod_ms
 
-    step = make_step(st.plan, args.deferred)
+    step = make_step(st.plan, opts.deferred_copier == 1)
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
@@ -408,7 +416,7 @@ def run_ours(args):
     # kernel-timing pass: K more rounds of the same step, CUDA events around every copier launch
     # (in the library, on the copy stream) and, for the GEMM, around every producer launch
     plan3 = side_plan(time_copier=1, deferred_copier=opts.deferred_copier)
-    step3 = make_step(plan3, args.deferred)
+    step3 = make_step(plan3, opts.deferred_copier == 1)
     for _ in range(3):
         step3()
     torch.cuda.synchronize()
@@ -651,6 +659,7 @@ def run_ce_fanout(args):
     w = workload(args)
     S = w.slice_bytes
     launch = dict(runner.bench_launch(w))
+    launch.pop("pace", None)          # the copier starts after the producer here
     opts = launch.pop("opts", None) or D.dtt_plan_opts_default()
     opts.deferred_copier, opts.time_copier = 1, 1
     st = runner.make(w, opts=opts, **launch)

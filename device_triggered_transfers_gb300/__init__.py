@@ -86,7 +86,7 @@ class dtt_fill_desc(C.Structure):
                 ("BM", C.c_uint32), ("BN", C.c_uint32), ("num_programs", C.c_uint32),
                 ("tiles_per_chunk", C.c_uint32), ("order", dtt_order),
                 ("mark_mode", C.c_uint32), ("cluster", C.c_uint32), ("rank_mask", C.c_uint32),
-                ("threads", C.c_uint32), ("group", C.c_uint32), ("reserved", C.c_uint32),
+                ("threads", C.c_uint32), ("group", C.c_uint32), ("pace", C.c_uint32),
                 ("group_counters", C.c_void_p)]
 
 
@@ -432,9 +432,10 @@ def dtt_plan_create(bufs, buf_bytes, schedules, opts=None, copy_stream=None) -> 
 def fill_desc(dtype: str, seed: int, M: int, N: int, pitch: int, buf_bytes: int,
               slice_offs: Sequence[int], BM: int, BN: int, num_programs: int, tiles_per_chunk: int,
               order_kind=ORDER_ROW_MAJOR, group_m=0, mark_mode=MARK_PER_STEP, cluster=1,
-              rank_mask=None, threads=0, group=1, group_counters=None) -> dtt_fill_desc:
+              rank_mask=None, threads=0, group=1, group_counters=None, pace=0) -> dtt_fill_desc:
     d = dtt_fill_desc()
     d.group = group
+    d.pace = pace
     d.group_counters = _ptr(group_counters) or None
     d.dtype = DTYPE_CODES[dtype]
     d.seed = seed & 0xFFFFFFFF

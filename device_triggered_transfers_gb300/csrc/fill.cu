@@ -25,7 +25,11 @@ struct FillParams {
     uint32_t vec;    // 16-byte stores allowed (bases, offsets, pitch and BN*elem aligned)
     uint32_t group;  // CTAs that write one step together and mark it once (counter-based)
     uint32_t* counters;   // group > 1: one per (rank, step), zero between rounds
+    uint32_t pace;        // > 0: wait for chunk k - pace to be reusable before chunk k
 };
+
+// Polls of the pacing wait: advisory, so it gives up after about a millisecond.
+constexpr uint64_t kPacePolls = 4096;
 
 // MurmurHash3's 32-bit finaliser (public-domain hash by Austin Appleby).
 __device__ __forceinline__ uint32_t fmix32(uint32_t h) {
@@ -194,7 +198,17 @@ __global__ void __launch_bounds__(1024) fill_kernel(const __grid_constant__ Fill
     const uint64_t T = tiles_m * tiles_n;
     const uint32_t salt = fmix32(p.seed ^ fmix32(r ^ fmix32(h.round)));
     char* base = p.bufs[r] + p.slice_off[r];
+    uint64_t paced = ~0ull;       // the last chunk this program waited for
     for (uint64_t step = prog; step < T; step += p.NP) {
+        if (p.pace) {
+            // keep the bytes written but not yet delivered within `pace` chunks of this rank:
+            // the copier then reads them from L2.  The result does not depend on the outcome.
+            const uint64_t k = step / p.TPC;
+            if (k >= p.pace && k != paced) {
+                (void)dtt_wait_reusable(h, h.first_chunk + (uint32_t)(k - p.pace), kPacePolls);
+                paced = k;
+            }
+        }
         uint32_t tm, tn;
         tile_of(p.order_kind, p.group_m, step, (uint32_t)tiles_m, (uint32_t)tiles_n, &tm, &tn);
         const uint64_t r0 = (uint64_t)tm * p.BM, c0 = (uint64_t)tn * p.BN;
@@ -287,6 +301,7 @@ extern "C" int dtt_fill_producer(void* const* bufs, uint32_t P, const dtt_fill_d
     p.vec = vec ? 1u : 0u;
     p.group = group;
     p.counters = d->group_counters;
+    p.pace = d->pace;
 
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(d->num_programs * cluster * group, P, 1);

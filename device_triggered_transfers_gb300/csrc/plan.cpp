@@ -814,7 +814,7 @@ int dtt_plan_wait(dtt_plan* p, dtt_report* report) {
         rc = fail(DTT_EEXTRA, "dtt_plan_wait: %u chunk(s) got extra marks in round %u (first: %u)",
                   rep.n_extra, p->round, rep.extra_chunks[0]);
     } else if (rep.device_status) {
-        rc = fail(DTT_EINVAL, "dtt_plan_wait: a producer marked a chunk its rank does not own");
+        rc = fail(DTT_EINVAL, "dtt_plan_wait: a kernel marked, or asked reusable of, a chunk its rank does not own");
     } else if (rep.n_short) {
         rc = fail(DTT_ETIMEDOUT, "dtt_plan_wait: %u chunk(s) short in round %u (first: %u)",
                   rep.n_short, p->round, rep.short_chunks[0]);

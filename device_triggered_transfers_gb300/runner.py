@@ -50,10 +50,11 @@ def producer_steps(w) -> int:
 
 
 def producer_desc(w, cluster: int = 1, programs: Optional[int] = None, threads: int = 0,
-                  group: int = 1, counters=None):
+                  group: int = 1, counters=None, pace: int = 0):
     """The fill producer that matches ``w``'s schedule (same tiles, same order, same marks).
     group > 1: each program is `group` CTAs that mark each step once (counters: device int32
-    [P * producer_steps(w)], zeroed)."""
+    [P * producer_steps(w)], zeroed).  pace > 0: a program waits for chunk k - pace of its rank
+    to be delivered before it writes chunk k (timing only)."""
     slice_offs = [w.slice_offset(r) for r in range(w.P)]
     mask = 0
     for r in w.senders():
@@ -68,21 +69,21 @@ def producer_desc(w, cluster: int = 1, programs: Optional[int] = None, threads: 
                 raise ValueError("group writers on whole() need one step per program")
             return fill_desc(w.dtype, w.seed, w.M, w.N, w.row_bytes, w.buf_bytes, slice_offs, BM, w.N, NP, NP,
                              mark_mode=MARK_PER_STEP, cluster=1, rank_mask=mask, threads=threads,
-                             group=group, group_counters=counters)
+                             group=group, group_counters=counters, pace=pace)
         return fill_desc(w.dtype, w.seed, w.M, w.N, w.row_bytes, w.buf_bytes, slice_offs, BM, w.N, NP, 1,
-                         mark_mode=MARK_AT_END, cluster=1, rank_mask=mask, threads=threads)
+                         mark_mode=MARK_AT_END, cluster=1, rank_mask=mask, threads=threads, pace=pace)
     if w.kind == "chunks":
         BM = -(-w.M // w.num_chunks)
         n = -(-w.M // BM)
         NP = programs or n
         return fill_desc(w.dtype, w.seed, w.M, w.N, w.row_bytes, w.buf_bytes, slice_offs, BM, w.N, NP, 1,
                          mark_mode=MARK_PER_STEP, cluster=cluster, rank_mask=mask, threads=threads,
-                         group=group, group_counters=counters)
+                         group=group, group_counters=counters, pace=pace)
     kind = ORDER_GROUPED if w.group_m else ORDER_ROW_MAJOR
     return fill_desc(w.dtype, w.seed, w.M, w.N, w.row_bytes, w.buf_bytes, slice_offs, w.BM, w.BN,
                      programs or w.num_programs, w.tiles_per_chunk, order_kind=kind,
                      group_m=w.group_m, mark_mode=MARK_PER_STEP, cluster=cluster, rank_mask=mask,
-                     threads=threads, group=group, group_counters=counters)
+                     threads=threads, group=group, group_counters=counters, pace=pace)
 
 
 @dataclass
@@ -97,7 +98,8 @@ class Setup:
 
 
 def make(w, opts=None, cluster: int = 1, programs: Optional[int] = None, threads: int = 0,
-         device: str = "cuda", fill_byte: int = 0, copy_stream=None, group: int = 1) -> Setup:
+         device: str = "cuda", fill_byte: int = 0, copy_stream=None, group: int = 1,
+         pace: int = 0) -> Setup:
     """Allocate the P symmetric buffers (uint8, w.buf_bytes each), build the plan and producer.
     copy_stream: a non-blocking stream for the copier (None: the plan makes its own)."""
     bufs = [torch.full((w.buf_bytes,), fill_byte, dtype=torch.uint8, device=device)
@@ -113,7 +115,7 @@ def make(w, opts=None, cluster: int = 1, programs: Optional[int] = None, threads
     if group > 1:
         counters = torch.zeros(w.P * producer_steps(w), dtype=torch.int32, device=device)
     desc = producer_desc(w, cluster=cluster, programs=programs, threads=threads, group=group,
-                         counters=counters)
+                         counters=counters, pace=pace)
     torch.cuda.synchronize()          # buffers initialised before any round starts
     return Setup(w, bufs, plan, desc, torch.cuda.Stream(), counters, pointer_array(bufs))
 
@@ -136,8 +138,11 @@ def bench_launch(w) -> dict:
     whole(): the bulk-copy copier (two CTAs per SM, 2 x 56 KiB stages each) over the contiguous
     slices; the single chunk per rank opens only when the whole slice is written, so the fill
     gets as many CTAs as the writers allow.
-    tile_chunks (fill producer): the bulk-copy copier moving each tile as tensor-map boxes of
-    16 KiB, twelve in flight per SM.  The GEMM producer keeps the vector copier: its own
+    tile_chunks (fill producer): the bulk-copy copier moving each 32 KiB tile as one tensor-map
+    box (three CTAs per SM, two stages each), and a producer paced two chunks ahead of the
+    copier (each program waits for chunk k - 2 of its rank to be delivered before it writes
+    chunk k), so the copier reads what the producer wrote from L2; that needs every producer
+    CTA resident at once (128-thread CTAs).  The GEMM producer keeps the vector copier: its own
     shared-memory ring leaves no room for a bulk-copy ring on the same SM."""
     if w.kind == "chunks":     # three bulk-copy CTAs per SM: one thread alone cannot keep HBM busy
         return {"group": 38, "programs": 1, "threads": 256,
@@ -154,8 +159,9 @@ def bench_launch(w) -> dict:
             g = max(1, min(8, 152 // (len(w.senders()) * NP)))
             return {"group": g, "threads": 512, "opts": opts}
         return {"threads": 1024, "opts": opts}
-    if w.K == 0:       # the tiled fill in 128-thread CTAs: more of them resident per SM
-        return {"threads": 128, "opts": dtt_plan_opts_default(method=1, piece_bytes=16384, stages=12)}
+    if w.K == 0:       # the tiled fill in 128-thread CTAs: all of them resident at once
+        return {"threads": 128, "pace": 2,
+                "opts": dtt_plan_opts_default(method=1, piece_bytes=32768, stages=2, ctas_per_sm=3)}
     # the GEMM producer: two 256-thread vector copier CTAs per SM beside the GEMM's CTA
     return {"opts": dtt_plan_opts_default(copier_threads=256, ctas_per_sm=2)}
 

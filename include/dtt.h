@@ -198,7 +198,8 @@ typedef struct dtt_plan_opts {
 void dtt_plan_opts_default(dtt_plan_opts* opts);
 
 #define DTT_HANDLE_TIMESTAMPS 1u   /* dtt_handle.flags bit: stamp gate-open times */
-#define DTT_DEV_EBADCHUNK 1u       /* device status bit: a rank marked a chunk it does not own */
+#define DTT_DEV_EBADCHUNK 1u       /* device status bit: a rank marked (or asked dtt_reusable of)
+                                      a chunk it does not own */
 
 /* Device-side view of a plan for one rank and one round, passed by value to producer and
  * consumer kernels (the pages' TriggeredView handle).  Plain data; valid until the next
@@ -390,7 +391,13 @@ typedef struct dtt_fill_desc {
     uint32_t group;          /* > 1: a program is `group` CTAs that split each step's rows; the
                                 last of them to finish a step issues its one mark (per-step
                                 marks only, cluster must be 1) */
-    uint32_t reserved;
+    uint32_t pace;           /* > 0: before its first step in chunk k >= pace, a program waits
+                                (advisory: at most ~1 ms, then it goes on) until chunk k - pace of
+                                its rank is reusable (dtt_reusable: delivered to every peer), so
+                                that the bytes written but not yet copied stay within `pace`
+                                chunks per rank and the copier reads them from L2.  Timing only:
+                                the data and marks are the same.  Needs the copier running beside
+                                the producer (deferred_copier 0 or 2). */
     uint32_t* group_counters;/* group > 1: device uint32[P * steps per rank], zero before the
                                 first round (the producer leaves them zero after each round) */
 } dtt_fill_desc;

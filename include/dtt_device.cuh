@@ -1,5 +1,5 @@
 /*
- * dtt_device.cuh -- device side of a triggered plan: mark_ready, arrived, wait.
+ * dtt_device.cuh -- device side of a triggered plan: mark_ready, arrived, wait, reusable.
  *
  * Include from producer and consumer kernels; the kernel receives a dtt_handle (include/dtt.h)
  * by value.  Every function here is called by ALL threads of a CTA (dtt_mark_ready_cluster:
@@ -17,6 +17,8 @@
  *  - arrived / wait: thread 0 reads the gate with an acquire load (gpu scope); a CTA barrier
  *    passes the result to the other threads, and data they load afterwards is this round's.
  *    Polls are counted, never clock-bounded.
+ *  - reusable: thread 0 acquires the chunk's completion word, which the copier bumps with a
+ *    release add after every copy of the chunk has landed (and so after its reads of it).
  *  - A producer that writes through the async proxy (TMA stores) must complete those writes
  *    (cp.async.bulk.wait_group 0) and issue fence.proxy.async before calling mark_ready.
  */
@@ -153,6 +155,54 @@ __device__ __forceinline__ int dtt_wait(const dtt_handle& h, uint32_t chunk, uin
     }
     __syncthreads();
     return dtt_wait_result;
+}
+
+/* Source side ("Triggered SDMA Plans", API: the device view's `reusable`; Design notes: the
+ * completion word of the gate row): has every copy of this rank's own `chunk` landed at every
+ * peer this round, so that the chunk's bytes may be written again?  True when the chunk's
+ * completion word has reached round * (P - 1), the copier's deliveries of it over all rounds.
+ * The acquire orders the copier's reads of the chunk before the caller's later writes.  A
+ * chunk of another rank sets DTT_DEV_EBADCHUNK in the plan's status word and returns false. */
+__device__ __forceinline__ bool dtt_reusable(const dtt_handle& h, uint32_t chunk) {
+    __shared__ int dtt_reusable_flag;
+    __syncthreads();
+    if (dtt_dev::first_thread()) {
+        int f = 0;
+        if (chunk < h.first_chunk || chunk >= h.first_chunk + h.n_chunks) {
+            atomicOr(h.status, DTT_DEV_EBADCHUNK);
+        } else {
+            const uint64_t* w = dtt_dev::gate_row(h, h.rank, chunk) + DTT_GATE_COMPLETION;
+            f = dtt_dev::ld_acquire(w) >= (uint64_t)h.round * (h.P - 1);
+        }
+        dtt_reusable_flag = f;
+    }
+    __syncthreads();
+    return dtt_reusable_flag != 0;
+}
+
+/* Wait until dtt_reusable(h, chunk), polling at most max_polls times.  Returns 0, or
+ * DTT_ETIMEDOUT if the polls ran out (or the chunk is not this rank's). */
+__device__ __forceinline__ int dtt_wait_reusable(const dtt_handle& h, uint32_t chunk, uint64_t max_polls) {
+    __shared__ int dtt_wait_reusable_result;
+    __syncthreads();
+    if (dtt_dev::first_thread()) {
+        int r = DTT_ETIMEDOUT;
+        if (chunk < h.first_chunk || chunk >= h.first_chunk + h.n_chunks) {
+            atomicOr(h.status, DTT_DEV_EBADCHUNK);
+        } else {
+            const uint64_t* w = dtt_dev::gate_row(h, h.rank, chunk) + DTT_GATE_COMPLETION;
+            const uint64_t target = (uint64_t)h.round * (h.P - 1);
+            uint32_t ns = 0;
+            for (uint64_t i = 0; i < max_polls; ++i) {
+                if (dtt_dev::ld_acquire(w) >= target) { r = 0; break; }
+                __nanosleep(ns);
+                ns = ns < 256 ? ns + 32 : 256;
+            }
+        }
+        dtt_wait_reusable_result = r;
+    }
+    __syncthreads();
+    return dtt_wait_reusable_result;
 }
 
 #endif /* DTT_DEVICE_CUH */

@@ -124,6 +124,16 @@ class Plan:
         elif row[COUNTER] > target:
             row[ERROR] = self.round
 
+    def reusable(self, rank: int, c: int) -> bool:
+        """Source side: has every copy of rank's own chunk c landed at every peer this round?
+        ("Triggered SDMA Plans", API: the device view's ``reusable``, which the page only names;
+        read here as the test on the gate row's completion word from its Design notes.)  Each
+        delivery adds one to the source's completion word, so the chunk is reusable once the
+        word holds round * (P - 1)."""
+        if self.owner[c] != rank:
+            raise ValueError("reusable is asked of a rank's own chunk")
+        return int(self.gates[rank, c, COMPLETION]) >= self.round * (self.P - 1)
+
     def gate_open(self, c: int) -> bool:
         s = self.owner[c]
         return (int(self.gates[s, c, READY]) & 0xFFFFFFFF) >= self.round

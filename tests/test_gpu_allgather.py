@@ -24,8 +24,9 @@ def _gates_match(st, o):
     return g
 
 
-def run_parity(w, rounds, opts=None, cluster=1, programs=None, threads=0, group=1):
-    st = runner.make(w, opts=opts, cluster=cluster, programs=programs, threads=threads, group=group)
+def run_parity(w, rounds, opts=None, cluster=1, programs=None, threads=0, group=1, pace=0):
+    st = runner.make(w, opts=opts, cluster=cluster, programs=programs, threads=threads, group=group,
+                     pace=pace)
     o = oracle_plan(w)
     try:
         for R in range(1, rounds + 1):
@@ -99,6 +100,21 @@ SMALL = {
     "whole_f32_8writers_group4": (W.small(W.C4A, M=64, N=64, rounds=3),
                                   {"group": 4, "opts": dict(method=1, piece_bytes=4096, stages=4)}),
     "whole_1writer_group16": (W.small(W.C1, M=200), {"group": 16, "threads": 512}),
+    # a paced producer: a program writes chunk k once chunk k - pace of its rank is delivered
+    "tiles_paced2_bulk": (W.Workload("tp", P=4, M=512, N=512, dtype=W.BF16, kind="tile_chunks",
+                                     rounds=3, seed=16, BM=64, BN=64, num_programs=6,
+                                     tiles_per_chunk=6, group_m=3),
+                          {"pace": 2, "threads": 128,
+                           "opts": dict(method=1, piece_bytes=8192, stages=2, ctas_per_sm=3)}),
+    "chunks_paced1": (W.small(W.C2, M=96, N=1024, num_chunks=6), {"pace": 1, "programs": 2}),
+    "tiles_paced1_group3": (W.Workload("tq", P=3, M=300, N=200, dtype=W.BF16, kind="tile_chunks",
+                                       rounds=3, seed=17, BM=64, BN=48, num_programs=5,
+                                       tiles_per_chunk=5, group_m=2), {"group": 3, "pace": 1}),
+    # pacing with the copier started after the producer: every pacing wait runs out (about a
+    # millisecond each) and the producer goes on; the data and gates are the same
+    "paced_copier_after_producer": (W.small(W.C2, M=64, N=512, num_chunks=4),
+                                    {"pace": 1, "programs": 1,
+                                     "opts": dict(deferred_copier=1)}),
 }
 
 

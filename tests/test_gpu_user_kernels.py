@@ -33,6 +33,10 @@ def _build():
     lib.user_produce.argtypes = [C.POINTER(D.dtt_handle), C.c_void_p, C.c_uint64, C.c_void_p]
     lib.user_consume.argtypes = [C.POINTER(D.dtt_handle), C.c_void_p, C.c_void_p, C.c_uint64,
                                  C.c_uint64, C.c_void_p, C.c_void_p]
+    lib.user_produce_paced.argtypes = [C.POINTER(D.dtt_handle), C.c_void_p, C.c_uint64, C.c_uint64,
+                                       C.c_void_p, C.c_void_p, C.c_void_p]
+    lib.user_probe.argtypes = [C.POINTER(D.dtt_handle), C.c_uint32, C.c_uint32, C.c_void_p,
+                               C.c_void_p]
     return lib
 
 
@@ -79,5 +83,71 @@ def test_user_producer_and_consumer_kernels():
             for b in bufs:
                 np.testing.assert_array_equal(b.cpu().numpy(), want)
             plan.next_round()
+    finally:
+        plan.close()
+
+
+def test_user_paced_producer_and_reusable():
+    # Source side: dtt_reusable is false for every chunk before this round's marks, true for all
+    # of them after wait(); a producer whose CTA c waits for chunk c - 1 to be reusable before it
+    # writes chunk c finishes the round with this round's data everywhere, and each wait ended
+    # only after chunk c - 1's arrival was signalled at every peer (gate timestamps).
+    lib = _build()
+    assert lib.user_kernels_prepare() == 0
+    P, n, chunk = 3, 5, 1 << 20
+    S = n * chunk
+    bufs = [torch.zeros(P * S, dtype=torch.uint8, device="cuda") for _ in range(P)]
+    scheds = [D.dtt_schedule_chunks(r * S, n, chunk, chunk, n) for r in range(P)]
+    plan = D.Plan(bufs, P * S, scheds, D.dtt_plan_opts_default(method=D.COPY_TMA, piece_bytes=65536,
+                                                               stages=3))
+    for s in scheds:
+        s.free()
+    prod = torch.cuda.Stream()
+    probe = torch.full((P, n), 7, dtype=torch.int32, device="cuda")
+    wst = torch.full((P, n), 99, dtype=torch.int32, device="cuda")
+    wend = torch.zeros((P, n), dtype=torch.int64, device="cuda")
+    torch.cuda.synchronize()
+    try:
+        for rnd in (1, 2, 3):
+            h = plan.start(prod)
+            for r in range(P):      # before any mark of this round
+                assert lib.user_probe(C.byref(h[r]), h[r].first_chunk, n,
+                                      C.c_void_p(probe[r].data_ptr()), C.c_void_p(prod.cuda_stream)) == 0
+            for r in range(P):
+                assert lib.user_produce_paced(C.byref(h[r]), C.c_void_p(bufs[r].data_ptr() + r * S),
+                                              chunk, 1 << 24, C.c_void_p(wst[r].data_ptr()),
+                                              C.c_void_p(wend[r].data_ptr()),
+                                              C.c_void_p(prod.cuda_stream)) == 0
+            rep = plan.wait()
+            assert rep.status == D.OK and rep.device_status == 0
+            prod.synchronize()
+            assert probe.cpu().tolist() == [[0] * n] * P
+            for r in range(P):
+                assert lib.user_probe(C.byref(h[r]), h[r].first_chunk, n,
+                                      C.c_void_p(probe[r].data_ptr()), C.c_void_p(prod.cuda_stream)) == 0
+            prod.synchronize()
+            assert probe.cpu().tolist() == [[1] * n] * P
+            assert wst[:, 1:].cpu().tolist() == [[0] * (n - 1)] * P
+            g = plan.read_gates()
+            for r in range(P):
+                for c in range(1, n):
+                    prev = h[r].first_chunk + c - 1
+                    arrivals = [int(g[q, prev, D.GATE_T_ARRIVE]) for q in range(P) if q != r]
+                    assert int(wend[r, c]) >= max(arrivals) > 0, (rnd, r, c)
+            want = np.concatenate([_values(r, rnd, S) for r in range(P)])
+            for b in bufs:
+                np.testing.assert_array_equal(b.cpu().numpy(), want)
+            plan.next_round()
+        # asking reusable of another rank's chunk is a misuse the round's wait reports
+        h = plan.start(prod)
+        assert lib.user_probe(C.byref(h[0]), h[1].first_chunk, 1, C.c_void_p(probe[0].data_ptr()),
+                              C.c_void_p(prod.cuda_stream)) == 0
+        for r in range(P):
+            assert lib.user_produce_paced(C.byref(h[r]), C.c_void_p(bufs[r].data_ptr() + r * S), chunk,
+                                          1 << 24, C.c_void_p(wst[r].data_ptr()),
+                                          C.c_void_p(wend[r].data_ptr()), C.c_void_p(prod.cuda_stream)) == 0
+        rep = plan.wait(raise_on_error=False)
+        assert rep.status == D.EINVAL and rep.device_status & 1
+        assert int(probe[0, 0].item()) == 0
     finally:
         plan.close()

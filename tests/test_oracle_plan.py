@@ -217,3 +217,43 @@ def test_exhaustive_interleavings_tiny_plan():
                             lo = r * sb + k * 2 * rb + w * rb
                             assert np.all(bufs[q][lo:lo + rb] == 16 * R + 4 * r + w)
             plan.next_round()
+
+
+def test_reusable_is_delivered_to_every_peer_this_round():
+    # reusable(c) holds exactly when chunk c has arrived at every other rank in this round: a
+    # test of completion against P - 1 without the round, or against one peer's arrival, fails
+    # in round 2 or before the last queue has delivered
+    rng = np.random.default_rng(3)
+    P = 3
+    plan, sb = make_plan(P, 6, 4, "bf16", "chunks", n=3)
+    for R in (1, 2, 3):
+        plan.start()
+        own = [(r, c) for r in range(P) for c in plan.chunks_of(r)]
+        for r, c in own:
+            assert not plan.reusable(r, c)          # nothing delivered yet this round
+        marks = [(r, c) for r, c in own for _ in range(plan.chunks[c].writers)]
+        for i in rng.permutation(len(marks)):
+            r, c = marks[i]
+            plan.mark_ready(r, c)
+            if rng.random() < 0.5:
+                plan.copier_progress()
+            for r2, c2 in own:
+                delivered = all(int(plan.gates[p, c2, ARRIVAL]) >= R for p in range(P) if p != r2)
+                assert plan.reusable(r2, c2) == delivered
+        plan.copier_progress()
+        assert all(plan.reusable(r, c) for r, c in own)
+        assert plan.wait()[0] == PL.OK
+        plan.next_round()
+    with pytest.raises(ValueError):
+        plan.reusable(0, plan.first[1])               # a chunk of another rank
+
+
+def test_reusable_follows_head_of_line_order():
+    plan, sb = make_plan(2, 6, 4, "bf16", "chunks", n=3)
+    plan.start()
+    plan.mark_ready(0, 1)                  # chunk 1 is ready but queued behind chunk 0
+    plan.copier_progress()
+    assert not plan.reusable(0, 1) and not plan.reusable(0, 0)
+    plan.mark_ready(0, 0)
+    plan.copier_progress()
+    assert plan.reusable(0, 0) and plan.reusable(0, 1) and not plan.reusable(0, 2)

@@ -4,6 +4,9 @@
 //
 // producer: CTA c writes chunk c of the rank's slice (one writer per chunk), then marks it.
 // consumer: CTA c waits for chunk c at rank q, then copies it to dst; status[c] = 0 or timeout.
+// paced producer: CTA c first waits until chunk c - 1 of its rank is reusable (delivered to
+// every peer), the source side of "Triggered SDMA Plans" (API: reusable).
+// probe: CTA i records dtt_reusable of chunk first + i.
 #include <cstdint>
 
 #include <cuda_runtime.h>
@@ -38,6 +41,32 @@ __global__ void user_consumer(dtt_handle h, const uint8_t* buf, uint8_t* dst, ui
     for (uint64_t i = threadIdx.x; i < chunk_bytes; i += blockDim.x) dst[base + i] = buf[base + i];
 }
 
+// A producer that waits, before CTA c writes chunk c, until chunk c - 1 of its rank has been
+// delivered everywhere (dtt_wait_reusable), and records the wait's result and when it ended.
+__global__ void user_producer_paced(dtt_handle h, uint8_t* slice, uint64_t chunk_bytes, uint64_t max_polls,
+                                    int32_t* wait_status, uint64_t* wait_end) {
+    const uint32_t c = blockIdx.x;
+    if (c > 0) {
+        const int r = dtt_wait_reusable(h, h.first_chunk + c - 1, max_polls);
+        if (threadIdx.x == 0) {
+            wait_status[c] = r;
+            uint64_t t;
+            asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+            wait_end[c] = t;
+        }
+    }
+    const uint64_t base = (uint64_t)c * chunk_bytes;
+    for (uint64_t i = threadIdx.x; i < chunk_bytes; i += blockDim.x)
+        slice[base + i] = value_at(h.rank, h.round, base + i);
+    dtt_mark_ready(h, h.first_chunk + c);
+}
+
+// CTA i asks dtt_reusable of global chunk first + i.
+__global__ void user_probe_reusable(dtt_handle h, uint32_t first, int32_t* out) {
+    const bool r = dtt_reusable(h, first + blockIdx.x);
+    if (threadIdx.x == 0) out[blockIdx.x] = r ? 1 : 0;
+}
+
 }  // namespace
 
 // What the documented contract asks of a user's kernels before the first round: loaded now,
@@ -50,6 +79,11 @@ extern "C" int user_kernels_prepare(void) {
                              cudaSharedmemCarveoutMaxShared) != cudaSuccess)
         return 1;
     if (cudaFuncSetAttribute(user_consumer, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared) != cudaSuccess)
+        return 1;
+    if (cudaFuncGetAttributes(&a, user_producer_paced) != cudaSuccess) return 1;
+    if (cudaFuncGetAttributes(&a, user_probe_reusable) != cudaSuccess) return 1;
+    if (cudaFuncSetAttribute(user_producer_paced, cudaFuncAttributePreferredSharedMemoryCarveout,
                              cudaSharedmemCarveoutMaxShared) != cudaSuccess)
         return 1;
     return 0;
@@ -65,5 +99,19 @@ extern "C" int user_consume(const dtt_handle* h, const void* buf, void* dst, uin
                             uint64_t max_polls, int32_t* status, cudaStream_t s) {
     user_consumer<<<h->n_global, 256, 0, s>>>(*h, static_cast<const uint8_t*>(buf), static_cast<uint8_t*>(dst),
                                               chunk_bytes, max_polls, status);
+    return cudaGetLastError() == cudaSuccess ? 0 : 1;
+}
+
+extern "C" int user_produce_paced(const dtt_handle* h, void* slice, uint64_t chunk_bytes, uint64_t max_polls,
+                                  int32_t* wait_status, uint64_t* wait_end, cudaStream_t s) {
+    if (h->n_chunks == 0) return 0;
+    user_producer_paced<<<h->n_chunks, 256, 0, s>>>(*h, static_cast<uint8_t*>(slice), chunk_bytes, max_polls,
+                                                    wait_status, wait_end);
+    return cudaGetLastError() == cudaSuccess ? 0 : 1;
+}
+
+extern "C" int user_probe(const dtt_handle* h, uint32_t first, uint32_t n, int32_t* out, cudaStream_t s) {
+    if (n == 0) return 0;
+    user_probe_reusable<<<n, 64, 0, s>>>(*h, first, out);
     return cudaGetLastError() == cudaSuccess ? 0 : 1;
 }
