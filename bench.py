@@ -35,8 +35,7 @@ DEFAULT_CONFIG = W.C2.name
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of the named kernel from one ncu capture
 # of the same workload and launch configuration (the summaries under profiles/); absent until
 # taken, and dropped once the kernel changes.
-NCU_TRAFFIC = {("c2_chunks_p4", "copier_bulk_kernel"): 474083584,
-               ("c5_gemm_p4", "gemm2_producer_kernel"): 166012672}
+NCU_TRAFFIC = {("c2_chunks_p4", "copier_bulk_kernel"): 474083584}
 
 
 def describe(w, launch, copier=None) -> str:

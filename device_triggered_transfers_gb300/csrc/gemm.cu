@@ -163,8 +163,9 @@ __device__ __forceinline__ uint32_t pack_bf16x2(uint32_t lo, uint32_t hi) {
     return r;
 }
 
-// Work is cut in units of TN / 128 adjacent tiles of one tile row; program p takes units p,
-// p + NP, ... of rank 0, then of rank 1, and so on.  Tile (tm, tn) is step tm * tiles_n + tn of
+// Work is cut in units of TN / 128 adjacent tiles of one tile row.  Every rank's units form one
+// sequence (rank 0's, then rank 1's, ...) and program p takes its units p, p + NP, ..., so no
+// program has more than one unit above the mean.  Tile (tm, tn) is step tm * tiles_n + tn of
 // its rank and, once stored, gets one mark on chunk first_chunk + step / NP.
 template <uint32_t TN>
 __global__ void __launch_bounds__(THREADS, 1) gemm_producer_kernel(const __grid_constant__ GemmParams p) {
@@ -219,8 +220,8 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_producer_kernel(const __grid_
         if (lane == 0) {
             uint32_t stage = 0, phase = 0, issued = 0;
             bool ok = true;
-            for (uint32_t r = 0; r < p.P && ok; ++r)
-                for (uint32_t u = blockIdx.x; u < units && ok; u += p.NP) {
+            for (uint32_t gu = blockIdx.x; gu < p.P * units && ok; gu += p.NP) {
+                    const uint32_t r = gu / units, u = gu % units;
                     const int32_t row_a = (int32_t)(r * p.M + (u / units_n) * BM);
                     const int32_t row_b = (int32_t)((u % units_n) * TN);
                     for (uint32_t kb = 0; kb < kblocks; ++kb) {
@@ -241,8 +242,8 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_producer_kernel(const __grid_
         if (lane == 0) {
             uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
             bool ok = true;
-            for (uint32_t r = 0; r < p.P && ok; ++r)
-                for (uint32_t u = blockIdx.x; u < units && ok; u += p.NP) {
+            for (uint32_t gu = blockIdx.x; gu < p.P * units && ok; gu += p.NP) {
+                    const uint32_t r = gu / units, u = gu % units;
                     if (!bar_wait(saddr(acc_empty + acc), acc_phase ^ 1, abort_flag)) { fail(); ok = false; break; }
                     tc_fence_after();
                     const uint32_t d_tmem = tmem_base + acc * TN;
@@ -271,8 +272,8 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_producer_kernel(const __grid_
         uint32_t acc = 0, acc_phase = 0;
         const uint32_t row_in_tile = warp * 32 + lane;
         bool ok = true;
-        for (uint32_t r = 0; r < p.P && ok; ++r)
-            for (uint32_t u = blockIdx.x; u < units && ok; u += p.NP) {
+        for (uint32_t gu = blockIdx.x; gu < p.P * units && ok; gu += p.NP) {
+                const uint32_t r = gu / units, u = gu % units;
                 bool mine = bar_wait(saddr(acc_full + acc), acc_phase, abort_flag);
                 if (!mine) fail();
                 // one decision for all 128 epilogue threads, so none is left at a barrier
@@ -547,8 +548,9 @@ __device__ __forceinline__ void umma_commit_local2(uint32_t bar) {
                  ::"r"(bar) : "memory");
 }
 
-// Cluster c of NC takes units c, c + NC, ... of rank 0, then of rank 1, and so on; a unit is a
-// 256 x 256 block, CTA q of the pair owns its rows 128 q .. 128 q + 127.  Tile (tm, tn) is step
+// A unit is a 256 x 256 block; every rank's units form one sequence (rank 0's, then rank 1's,
+// ...) and cluster c of NC takes its units c, c + NC, ...; CTA q of the pair owns the unit's
+// rows 128 q .. 128 q + 127.  Tile (tm, tn) is step
 // tm * tiles_n + tn of its rank and, once stored, gets one mark on chunk first_chunk + step / NP.
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 gemm2_producer_kernel(const __grid_constant__ GemmParams p) {
@@ -606,8 +608,8 @@ gemm2_producer_kernel(const __grid_constant__ GemmParams p) {
         if (lane == 0) {
             uint32_t stage = 0, phase = 0, issued = 0;
             bool ok = true;
-            for (uint32_t r = 0; r < p.P && ok; ++r)
-                for (uint32_t u = c0; u < units && ok; u += NC) {
+            for (uint32_t gu = c0; gu < p.P * units && ok; gu += NC) {
+                    const uint32_t r = gu / units, u = gu % units;
                     const int32_t row_a = (int32_t)(r * p.M + (u / units_n) * 256 + q * BM);
                     const int32_t row_b = (int32_t)((u % units_n) * G2_TN + q * BN);
                     for (uint32_t kb = 0; kb < kblocks; ++kb) {
@@ -635,8 +637,8 @@ gemm2_producer_kernel(const __grid_constant__ GemmParams p) {
         if (lane == 0 && leader) {
             uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
             bool ok = true;
-            for (uint32_t r = 0; r < p.P && ok; ++r)
-                for (uint32_t u = c0; u < units && ok; u += NC) {
+            for (uint32_t gu = c0; gu < p.P * units && ok; gu += NC) {
+                    const uint32_t r = gu / units, u = gu % units;
                     if (!bar_wait(saddr(acc_empty + acc), acc_phase ^ 1, abort_flag)) { fail(); ok = false; break; }
                     tc_fence_after();
                     const uint32_t d_tmem = tmem_base + acc * G2_TN;
@@ -665,8 +667,8 @@ gemm2_producer_kernel(const __grid_constant__ GemmParams p) {
         uint32_t acc = 0, acc_phase = 0;
         const uint32_t row_in_tile = warp * 32 + lane;
         bool ok = true;
-        for (uint32_t r = 0; r < p.P && ok; ++r)
-            for (uint32_t u = c0; u < units && ok; u += NC) {
+        for (uint32_t gu = c0; gu < p.P * units && ok; gu += NC) {
+                const uint32_t r = gu / units, u = gu % units;
                 bool mine = bar_wait(saddr(acc_full + acc), acc_phase, abort_flag);
                 if (!mine) fail();
                 if (!epi_all(mine && !*abort_flag)) { ok = false; break; }

@@ -188,10 +188,9 @@ def make_gemm(w, A, Bt, opts=None, num_programs: Optional[int] = None, copy_stre
     NP = num_programs or w.num_programs
     w = type(w)(**{**w.__dict__, "tiles_per_chunk": NP, "num_programs": NP})
     bufs = [torch.zeros(w.buf_bytes, dtype=torch.uint8, device="cuda") for _ in range(w.P)]
-    if opts is None:
-        opts = dtt_plan_opts_default()
+    if opts is None:                  # the vector copier: it needs no shared memory
+        opts = dtt_plan_opts_default(method=COPY_VEC16)
     opts.allgather = 1
-    opts.method = COPY_VEC16          # the GEMM's shared memory leaves no room for a bulk ring
     scheds = schedules_for(w)
     plan = Plan(bufs, w.buf_bytes, scheds, opts, copy_stream=copy_stream)
     for s in scheds:
