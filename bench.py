@@ -35,7 +35,14 @@ DEFAULT_CONFIG = W.C2.name
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of the named kernel from one ncu capture
 # of the same workload and launch configuration (the summaries under profiles/); absent until
 # taken, and dropped once the kernel changes.
-NCU_TRAFFIC = {("c2_chunks_p4", "copier_bulk_kernel"): 474083584}
+NCU_TRAFFIC = {("c2_chunks_p4", "copier_bulk_kernel"): 474083584,
+               # captured with 2000 rows per rank (--rows 2000) and scaled by the rows, 4x
+               ("c3_tiles_p8", "copier_bulk_kernel"): 8018295392,
+               ("c5_gemm_p4", "gemm2_producer_kernel"): 158154752}
+# DRAM bytes (read + write) of one whole round, producer, copier and check together, from an
+# ncu range-replay capture of three rounds of the benchmark's launch (--profile-rounds 3)
+ROUND_TRAFFIC = {"c2_chunks_p4": (2848171, 516156075), "c3_tiles_p8": (12696405, 8237207979),
+                 "c5_gemm_p4": (209710848, 248136875)}
 
 
 def describe(w, launch, copier=None) -> str:
@@ -386,6 +393,19 @@ def run_ours(args):
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
+    if args.profile_rounds:
+        # whole rounds (producer, copier and check together) inside one profiler range, for a
+        # range-replay capture of their DRAM traffic; no timing
+        torch.cuda.profiler.start()
+        for _ in range(args.profile_rounds):
+            step()
+        torch.cuda.synchronize()
+        torch.cuda.profiler.stop()
+        if rank == 0:
+            print(json.dumps({"profile_rounds": args.profile_rounds, "workload": w.name,
+                              "algorithmic_bytes_per_round": w.algorithmic_bytes_per_round(),
+                              "producer_bytes_per_round": len(w.senders()) * w.slice_bytes}))
+        return 0
     K = args.steps
     barrier(world)
     torch.cuda.synchronize()
@@ -511,7 +531,8 @@ def run_ours(args):
     kname = "copier_bulk_kernel" if copier_method["method"] == D.COPY_TMA else "copier_kernel"
     copier_roof = {"kernel": kname, "bound": "hbm", "achieved": achieved,
                    "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
-                   "traffic": NCU_TRAFFIC.get((w.name, kname)), "algorithmic_bytes_per_launch": B_alg}
+                   "traffic": NCU_TRAFFIC.get((w.name, kname)), "algorithmic_bytes_per_launch": B_alg,
+                   "round_dram_read_write": ROUND_TRAFFIC.get(w.name)}
     if gemm:       # the dominant kernel is the tensor-core producer
         flops = 2.0 * w.P * w.M * w.N * w.K
         tf_peak, tf_kind = load_tensor_peak()
@@ -776,6 +797,9 @@ def main(argv=None):
     ap.add_argument("--consumer-n", type=int, default=4096)
     ap.add_argument("--consumer-copier-threads", type=int, default=256)
     ap.add_argument("--consumer-copier", choices=["vector", "bulk"], default="vector")
+    ap.add_argument("--profile-rounds", type=int, default=0,
+                    help="run this many rounds after the warm-up inside a profiler range "
+                         "(cudaProfilerStart/Stop) and exit, for ncu --replay-mode app-range")
     ap.add_argument("--rows", type=int, default=0,
                     help="rows per rank instead of the workload's (a smaller case of the same "
                          "shape, for profiler captures; the default runs the workload as named)")
