@@ -243,7 +243,6 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_producer_kernel(const __grid_
             uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
             bool ok = true;
             for (uint32_t gu = blockIdx.x; gu < p.P * units && ok; gu += p.NP) {
-                    const uint32_t r = gu / units, u = gu % units;
                     if (!bar_wait(saddr(acc_empty + acc), acc_phase ^ 1, abort_flag)) { fail(); ok = false; break; }
                     tc_fence_after();
                     const uint32_t d_tmem = tmem_base + acc * TN;
@@ -322,6 +321,7 @@ struct ConsumerParams {
     const uint32_t* order;   // row blocks in the order they are taken
     const uint32_t* c0;      // per row block: the chunk ids [c0, c1] that cover it
     const uint32_t* c1;
+    const uint32_t* order2;  // pair form: pairs of row blocks (2 pb, 2 pb + 1) in the order taken
     char* D;
     uint64_t ldd;
     uint64_t max_polls;
@@ -638,7 +638,6 @@ gemm2_producer_kernel(const __grid_constant__ GemmParams p) {
             uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
             bool ok = true;
             for (uint32_t gu = c0; gu < p.P * units && ok; gu += NC) {
-                    const uint32_t r = gu / units, u = gu % units;
                     if (!bar_wait(saddr(acc_empty + acc), acc_phase ^ 1, abort_flag)) { fail(); ok = false; break; }
                     tc_fence_after();
                     const uint32_t d_tmem = tmem_base + acc * G2_TN;
@@ -701,6 +700,154 @@ gemm2_producer_kernel(const __grid_constant__ GemmParams p) {
     }
     tc_fence_before();
     cluster_sync_all();          // no CTA leaves while the pair's MMAs or loads may touch it
+    tc_fence_after();
+    if (warp == 0)
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(G2_TMEM_COLS)
+                     : "memory");
+}
+
+// ---- the consumer in the 2-CTA form ----------------------------------------------------------
+// D = X . W^T by CTA pairs.  A unit is a 256 x 256 block of D over the pair of 128-row blocks
+// (2 pb, 2 pb + 1) of X; CTA q of the pair waits for the chunks of its own row block 2 pb + q
+// before it loads it, so each half enters the MMA as soon as it has arrived.  Pair blocks are
+// taken in the order their later half opens (order2); cluster c of NC takes units c, c + NC, ...
+template <uint32_t ST>
+constexpr uint32_t g2c_smem() { return 1024 + ST * (A_STAGE + G2_BHALF) + 256; }
+
+template <uint32_t ST>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
+gemm2_consumer_kernel(const __grid_constant__ ConsumerParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sA = smem;
+    uint8_t* sB = smem + ST * A_STAGE;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sB + ST * G2_BHALF);
+    uint64_t* full = bars;                        // [ST]  leader: both CTAs' loads -> MMA
+    uint64_t* empty = bars + ST;                  // [ST]  each CTA: MMA -> its TMA warp
+    uint64_t* acc_full = bars + 2 * ST;           // [2]   each CTA: MMA -> its epilogue
+    uint64_t* acc_empty = acc_full + ACC_BUFS;    // [2]   leader: both epilogues -> MMA
+    uint64_t* drain = acc_empty + ACC_BUFS;       // [1]   leader: MMA teardown
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile uint32_t* abort_flag = tmem_slot + 1;
+
+    const uint32_t warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const uint32_t q = cluster_rank();
+    const bool leader = q == 0;
+    if (threadIdx.x == 0) {
+        for (uint32_t i = 0; i < ST; ++i) {
+            bar_init(saddr(full + i), 1);
+            bar_init(saddr(empty + i), 1);
+        }
+        for (uint32_t i = 0; i < ACC_BUFS; ++i) {
+            bar_init(saddr(acc_full + i), 1);
+            bar_init(saddr(acc_empty + i), 2);
+        }
+        bar_init(saddr(drain), 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;"
+                     ::"r"(saddr(tmem_slot)), "r"(G2_TMEM_COLS) : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    cluster_sync_all();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    const uint32_t units_n = p.N / G2_TN, units = (p.blocks / 2) * units_n, kblocks = p.K / BK;
+    const uint32_t c0 = blockIdx.x / 2, NC = gridDim.x / 2;
+    const uint32_t peer_abort = at_rank(saddr(tmem_slot + 1), q ^ 1);
+    auto fail = [&]() {
+        *abort_flag = 1;
+        asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(peer_abort), "r"(1u) : "memory");
+        atomicAdd(p.err, 1u);
+    };
+
+    if (warp == TMA_WARP) {
+        if (lane == 0) {
+            uint32_t stage = 0, phase = 0, issued = 0;
+            bool ok = true;
+            for (uint32_t u = c0; u < units && ok; u += NC) {
+                const uint32_t b = 2 * p.order2[u / units_n] + q;
+                if (!wait_chunks(p.h, p.c0[b], p.c1[b], p.max_polls, abort_flag)) { fail(); break; }
+                const int32_t row_a = (int32_t)(b * BM);
+                const int32_t row_b = (int32_t)((u % units_n) * G2_TN + q * BN);
+                for (uint32_t kb = 0; kb < kblocks; ++kb) {
+                    if (!bar_wait(saddr(empty + stage), phase ^ 1, abort_flag)) { fail(); ok = false; break; }
+                    const uint32_t fb = at_rank(saddr(full + stage), 0);
+                    if (leader) bar_expect_tx(saddr(full + stage), 2 * (A_STAGE + G2_BHALF));
+                    tma_load_2d_pair(saddr(sA + stage * A_STAGE), &p.tmX, (int32_t)(kb * BK), row_a, fb);
+                    tma_load_2d_pair(saddr(sB + stage * G2_BHALF), &p.tmW, (int32_t)(kb * BK), row_b, fb);
+                    ++issued;
+                    if (++stage == ST) { stage = 0; phase ^= 1; }
+                }
+            }
+            if (leader) {
+                volatile uint32_t never = 0;
+                for (uint32_t i = issued > ST ? issued - ST : 0; i < issued; ++i)
+                    (void)bar_wait(saddr(full + i % ST), (i / ST) & 1, &never);
+            }
+        }
+    } else if (warp == MMA_WARP) {
+        if (lane == 0 && leader) {
+            uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+            bool ok = true;
+            for (uint32_t u = c0; u < units && ok; u += NC) {
+                if (!bar_wait(saddr(acc_empty + acc), acc_phase ^ 1, abort_flag)) { fail(); break; }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + acc * G2_TN;
+                for (uint32_t kb = 0; kb < kblocks; ++kb) {
+                    if (!bar_wait(saddr(full + stage), phase, abort_flag)) { fail(); ok = false; break; }
+                    tc_fence_after();
+                    const uint64_t da = smem_desc(saddr(sA + stage * A_STAGE));
+                    const uint64_t db = smem_desc(saddr(sB + stage * G2_BHALF));
+#pragma unroll
+                    for (uint32_t k = 0; k < BK / UMMA_K; ++k)
+                        umma_pair(d_tmem, da + 2 * k, db + 2 * k, G2_IDESC, (kb | k) != 0);
+                    umma_commit_both(saddr(empty + stage));
+                    if (++stage == ST) { stage = 0; phase ^= 1; }
+                }
+                if (!ok) break;
+                umma_commit_both(saddr(acc_full + acc));
+                if (++acc == ACC_BUFS) { acc = 0; acc_phase ^= 1; }
+            }
+            umma_commit_local2(saddr(drain));
+            volatile uint32_t never = 0;
+            (void)bar_wait(saddr(drain), 0, &never);
+        }
+    } else {
+        uint32_t acc = 0, acc_phase = 0;
+        const uint32_t row_in_tile = warp * 32 + lane;
+        for (uint32_t u = c0; u < units; u += NC) {
+            bool mine = bar_wait(saddr(acc_full + acc), acc_phase, abort_flag);
+            if (!mine) fail();
+            if (!epi_all(mine && !*abort_flag)) break;
+            tc_fence_after();
+            const uint32_t b = 2 * p.order2[u / units_n] + q;
+            char* drow = p.D + (uint64_t)(b * BM + row_in_tile) * p.ldd + (uint64_t)(u % units_n) * G2_TN * 2;
+            const uint32_t taddr = tmem_base + ((warp * 32u) << 16) + acc * G2_TN;
+#pragma unroll 1
+            for (uint32_t g = 0; g < G2_TN / 32; ++g) {
+                uint32_t v[32];
+                tmem_ld32(taddr + g * 32, v);
+                uint4* dst = reinterpret_cast<uint4*>(drow + g * 64);
+#pragma unroll
+                for (uint32_t j = 0; j < 4; ++j)
+                    dst[j] = make_uint4(pack_bf16x2(v[8 * j + 0], v[8 * j + 1]), pack_bf16x2(v[8 * j + 2], v[8 * j + 3]),
+                                        pack_bf16x2(v[8 * j + 4], v[8 * j + 5]), pack_bf16x2(v[8 * j + 6], v[8 * j + 7]));
+            }
+            tc_fence_before();
+            // every TMEM read of this CTA's rows precedes one arrival at the leader
+            asm volatile("bar.sync 1, %0;" ::"n"(EPI_THREADS) : "memory");
+            if (threadIdx.x == 0) bar_arrive_at(at_rank(saddr(acc_empty + acc), 0));
+            if (++acc == ACC_BUFS) { acc = 0; acc_phase ^= 1; }
+        }
+    }
+    tc_fence_before();
+    cluster_sync_all();
     tc_fence_after();
     if (warp == 0)
         asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(G2_TMEM_COLS)
@@ -774,6 +921,15 @@ static cudaError_t prepare_consumer() {
     return e;
 }
 
+template <uint32_t ST>
+static cudaError_t prepare_consumer_pair() {
+    cudaError_t e = prepare_kernel(gemm2_consumer_kernel<ST>);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(gemm2_consumer_kernel<ST>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)g2c_smem<ST>());
+    return e;
+}
+
 // The deepest ring (at most the producer form's) whose shared memory fits in `budget` bytes;
 // the full ring when none of the smaller ones fits either (the GEMM then waits for room).
 template <uint32_t TN, uint32_t ST>
@@ -791,15 +947,36 @@ static void launch_consumer_ring(const ConsumerParams& cp, uint32_t ctas, uint64
     gemm_consumer_kernel<TN, ST><<<ctas, THREADS, consumer_smem<TN, ST>(), s>>>(cp);
 }
 
+// The pair form with the deepest ring (at most 6 stages, at least 3) that fits in `budget`, as
+// many clusters as can be resident at once; false when no such launch exists.
+template <uint32_t ST>
+static bool launch_consumer_pair(const ConsumerParams& cp, uint32_t ctas, uint64_t budget, cudaStream_t s) {
+    if constexpr (ST > 3) {
+        if (g2c_smem<ST>() > budget) return launch_consumer_pair<ST - 1>(cp, ctas, budget, s);
+    }
+    if (g2c_smem<ST>() > budget) return false;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(2 * (ctas / 2), 1, 1);
+    cfg.blockDim = dim3(THREADS, 1, 1);
+    cfg.dynamicSmemBytes = g2c_smem<ST>();
+    cfg.stream = s;
+    int fit = 0;
+    if (cudaOccupancyMaxActiveClusters(&fit, gemm2_consumer_kernel<ST>, &cfg) != cudaSuccess || fit < 1) {
+        (void)cudaGetLastError();
+        return false;
+    }
+    const uint32_t pairs = std::min<uint32_t>(ctas / 2, (uint32_t)fit);
+    gemm2_consumer_kernel<ST><<<2 * pairs, THREADS, g2c_smem<ST>(), s>>>(cp);
+    return true;
+}
+
 int launch_gemm_consumer(const ConsumerLaunch& cl, cudaStream_t stream) {
-    const uint32_t TN = (cl.N % 256 == 0) ? 256 : 128;
     ConsumerParams cp{};
-    if (!operand_maps(cl.X, cl.Wt, cl.rows, cl.N, cl.K, TN, &cp.tmX, &cp.tmW))
-        return fail(DTT_ECUDA, "dtt_gemm_consumer: cannot encode the tensor maps");
     cp.h = cl.h;
     cp.order = cl.order;
     cp.c0 = cl.c0;
     cp.c1 = cl.c1;
+    cp.order2 = cl.order2;
     cp.D = cl.D;
     cp.ldd = cl.ldd;
     cp.max_polls = cl.max_polls;
@@ -807,6 +984,19 @@ int launch_gemm_consumer(const ConsumerLaunch& cl, cudaStream_t stream) {
     cp.N = cl.N;
     cp.K = cl.K;
     cp.err = cl.err;
+    // CTA pairs (M = 256, N = 256 per MMA) when the blocks pair up and the columns tile by 256
+    if (cl.order2 && cl.N % 256 == 0 && cl.blocks % 2 == 0 && cl.ctas >= 2) {
+        if (!operand_maps(cl.X, cl.Wt, cl.rows, cl.N, cl.K, BN, &cp.tmX, &cp.tmW))
+            return fail(DTT_ECUDA, "dtt_gemm_consumer: cannot encode the tensor maps");
+        if (launch_consumer_pair<6>(cp, cl.ctas, cl.smem_budget, stream)) {
+            const cudaError_t e = cudaGetLastError();
+            if (e != cudaSuccess) return fail(DTT_ECUDA, "dtt_gemm_consumer: launch failed: %s", cudaGetErrorString(e));
+            return DTT_OK;
+        }
+    }
+    const uint32_t TN = (cl.N % 256 == 0) ? 256 : 128;
+    if (!operand_maps(cl.X, cl.Wt, cl.rows, cl.N, cl.K, TN, &cp.tmX, &cp.tmW))
+        return fail(DTT_ECUDA, "dtt_gemm_consumer: cannot encode the tensor maps");
     if (TN == 256)
         launch_consumer_ring<256, Cfg<256>::STAGES>(cp, cl.ctas, cl.smem_budget, stream);
     else
@@ -830,6 +1020,10 @@ cudaError_t preload_gemm_kernels() {
     if (e == cudaSuccess) e = prepare_kernel(gemm2_producer_kernel);
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(gemm2_producer_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)G2_SMEM);
+    if (e == cudaSuccess) e = prepare_consumer_pair<6>();
+    if (e == cudaSuccess) e = prepare_consumer_pair<5>();
+    if (e == cudaSuccess) e = prepare_consumer_pair<4>();
+    if (e == cudaSuccess) e = prepare_consumer_pair<3>();
     return e;
 }
 

@@ -182,6 +182,7 @@ struct ConsumerLaunch {
     const uint32_t* order;
     const uint32_t* c0;
     const uint32_t* c1;
+    const uint32_t* order2;     // pairs of row blocks in the order they are taken (pair form)
     uint32_t blocks;
     uint64_t max_polls;
     uint32_t* err;

@@ -70,7 +70,7 @@ struct dtt_plan {
     // consumer GEMM: per 128-row block of one rank's buffer seen as [rows, K], the order the
     // blocks are taken in and the chunk ids that cover each block (device, built on first use)
     uint32_t cons_rank = UINT32_MAX, cons_K = 0, cons_blocks = 0, cons_cap = 0;
-    uint32_t* d_cons = nullptr;       // [3][blocks]: order, c0, c1
+    uint32_t* d_cons = nullptr;       // [3][blocks] + [blocks / 2 + 1]: order, c0, c1, order2
 
     cudaStream_t copy_stream = nullptr;
     bool own_copy_stream = false;
@@ -1175,11 +1175,21 @@ int dtt_gemm_consumer(dtt_plan* p, uint32_t rank, const void* Wt, uint32_t N, ui
         }
         for (uint32_t b = 0; b < blocks; ++b) order[b] = b;
         std::stable_sort(order.begin(), order.end(), [&](uint32_t x, uint32_t y) { return key[x] < key[y]; });
+        // pairs of blocks (2 pb, 2 pb + 1) for the pair form, in the order their later half is taken
+        std::vector<uint32_t> pos(blocks), order2(blocks / 2), late(blocks / 2);
+        for (uint32_t i = 0; i < blocks; ++i) pos[order[i]] = i;
+        for (uint32_t pb = 0; pb < blocks / 2; ++pb) {
+            order2[pb] = pb;
+            late[pb] = std::max(pos[2 * pb], pos[2 * pb + 1]);
+        }
+        std::stable_sort(order2.begin(), order2.end(), [&](uint32_t x, uint32_t y) { return late[x] < late[y]; });
         std::vector<uint32_t> table;
-        table.reserve(3 * (size_t)blocks);
+        table.reserve(3 * (size_t)blocks + blocks / 2 + 1);
         table.insert(table.end(), order.begin(), order.end());
         table.insert(table.end(), c0.begin(), c0.end());
         table.insert(table.end(), c1.begin(), c1.end());
+        table.insert(table.end(), order2.begin(), order2.end());
+        table.push_back(0);
         if (p->d_cons && p->cons_cap < blocks) {
             DTT_CUDA_TRY(cudaFreeAsync(p->d_cons, stream));
             p->d_cons = nullptr;
@@ -1207,6 +1217,7 @@ int dtt_gemm_consumer(dtt_plan* p, uint32_t rank, const void* Wt, uint32_t N, ui
     cl.order = p->d_cons;
     cl.c0 = p->d_cons + p->cons_blocks;
     cl.c1 = p->d_cons + 2 * (size_t)p->cons_blocks;
+    cl.order2 = p->d_cons + 3 * (size_t)p->cons_blocks;
     cl.blocks = blocks;
     cl.max_polls = max_polls ? max_polls : p->opts.max_polls;
     cl.err = err;

@@ -28,14 +28,18 @@ def _weights(N, K, seed):
     return (torch.randn(N, K, generator=g) / K ** 0.5).to(torch.bfloat16)
 
 
-@pytest.mark.parametrize("q,N2,programs,bulk", [(0, 256, 0, None), (3, 384, 7, None),
-                                               (1, 128, 148, None), (2, 256, 0, "full"),
-                                               (0, 256, 0, "small"), (3, 128, 0, "small")])
-def test_consumer_gemm_waits_for_its_rows(q, N2, programs, bulk):
+@pytest.mark.parametrize("q,N2,programs,bulk,M", [(0, 256, 0, None, 512), (3, 384, 7, None, 512),
+                                                 (1, 128, 148, None, 512), (2, 256, 0, "full", 512),
+                                                 (0, 256, 0, "small", 512), (3, 128, 0, "small", 512),
+                                                 (1, 512, 2, None, 512), (2, 256, 7, None, 512),
+                                                 (1, 256, 0, None, 160)])
+def test_consumer_gemm_waits_for_its_rows(q, N2, programs, bulk, M):
     # bulk "full": the bulk-copy copier's 3 x 64 KiB ring leaves the GEMM no shared memory until
     # the copier's CTAs leave, so there is no overlap, but the result must be the same; "small":
-    # a 2 x 32 KiB ring leaves room for the GEMM's shorter ring, and the two overlap
-    w = W.small(W.C2, M=512, N=1024, num_chunks=4, rounds=3)      # 4 ranks x 4 chunks of 128 rows
+    # a 2 x 32 KiB ring leaves room for the GEMM's shorter ring, and the two overlap.  N2 a
+    # multiple of 256 over an even number of 128-row blocks runs the CTA-pair form (one pair with
+    # 2 programs, three with 7); M = 160 gives 5 blocks, so the one-CTA form
+    w = W.small(W.C2, M=M, N=1024, num_chunks=4 if M == 512 else 2, rounds=3)
     K = w.N
     rows = w.buf_bytes // (2 * K)
     Wt = _weights(N2, K, 77 + q)
