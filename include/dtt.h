@@ -448,10 +448,13 @@ int dtt_publish(const dtt_handle* handles, uint32_t P, uint32_t first_chunk, uin
  * bf16 out, num_programs persistent CTAs (0: 148).  Call after dtt_plan_start, on a stream
  * other than the copy stream.  A wait that runs out adds 1 to *err (device uint32) and the
  * kernel stops.  Requirements: N % 128 == 0, K % 64 == 0, buf_bytes a multiple of 256 K,
- * 16-byte aligned Wt, D and ldd.  The GEMM takes the deepest shared-memory ring (up to 4
- * stages of 48 KiB) that fits beside the plan's copier CTAs on an SM; where none fits (a
- * bulk-copy ring of ~200 KiB per SM) it starts only as the copier's CTAs leave.  The first
- * call for a (rank, K) builds a small table on the device (stream-ordered).
+ * 16-byte aligned Wt, D and ldd.  When N % 256 == 0, the rows form an even number of 128-row
+ * blocks and num_programs >= 2, CTA pairs (tcgen05 cta_group::2, 256 x 256 per MMA) compute it,
+ * each CTA waiting for its own row block, with the deepest ring of 6 to 3 stages of 32 KiB
+ * that fits beside the plan's copier CTAs on an SM; otherwise single CTAs (128 x 256 or
+ * 128 x 128) with up to 4 stages of 48 KiB.  Where no ring fits (a bulk-copy ring of ~200 KiB
+ * per SM) the GEMM starts only as the copier's CTAs leave.  The first call for a (rank, K)
+ * builds a small table on the device (stream-ordered).
  * Errors: DTT_EINVAL, DTT_ESTATE (plan not RUNNING), DTT_ECUDA. */
 int dtt_gemm_consumer(dtt_plan* plan, uint32_t rank, const void* Wt, uint32_t N, uint32_t K, void* D,
                       uint64_t ldd, uint32_t num_programs, uint64_t max_polls, uint32_t* err,
