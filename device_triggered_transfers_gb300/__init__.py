@@ -54,7 +54,7 @@ class dtt_plan_opts(C.Structure):
                 ("piece_bytes", C.c_uint32), ("timestamps", C.c_uint32),
                 ("initial_round", C.c_uint32), ("max_polls", C.c_uint64),
                 ("max_regions", C.c_uint64), ("deferred_copier", C.c_uint32),
-                ("stages", C.c_uint32), ("time_copier", C.c_uint32), ("reserved", C.c_uint32)]
+                ("stages", C.c_uint32), ("time_copier", C.c_uint32), ("host_piece_bytes", C.c_uint32)]
 
 
 class dtt_handle(C.Structure):

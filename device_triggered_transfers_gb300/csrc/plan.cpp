@@ -629,6 +629,10 @@ int dtt_plan_create(void* const* bufs, uint64_t buf_bytes, uint32_t P,
         delete p;
         return fail(DTT_EINVAL, "dtt_plan_create: bad options (piece_bytes %% 16, threads %% 32 <= 1024, method)");
     }
+    if (o.host_piece_bytes % 4096) {
+        delete p;
+        return fail(DTT_EINVAL, "dtt_plan_create: host_piece_bytes must be a multiple of 4096");
+    }
     if (o.method == DTT_COPY_TMA && o.stages < 2) {      // the ring loads ahead by stages - 1
         delete p;
         return fail(DTT_EINVAL, "dtt_plan_create: the bulk-copy path needs at least 2 stages");
@@ -1013,7 +1017,9 @@ int dtt_allgather_host(dtt_plan* p, const void* const* host_slices, void* host_o
     // the copier fans it out while later pieces are still in flight.
     // pieces of a quarter of a slice, at least 4 MiB: the slices already pipeline one behind
     // the other, and every piece boundary costs the copy engine a pause
-    const uint64_t kPiece = std::max<uint64_t>(4ull << 20, (S / 4 + 4095) & ~uint64_t(4095));
+    const uint64_t kPiece = p->opts.host_piece_bytes
+                                ? p->opts.host_piece_bytes
+                                : std::max<uint64_t>(4ull << 20, (S / 4 + 4095) & ~uint64_t(4095));
     std::vector<uint64_t> copied(P, 0), back(P, 0);   // bytes copied in / copied back per slice
     std::vector<uint32_t> marked(P);
     for (uint32_t r = 0; r < P; ++r) {

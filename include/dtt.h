@@ -192,7 +192,8 @@ typedef struct dtt_plan_opts {
                                 0 = as many as fit, at most 8 */
     uint32_t time_copier;    /* 1: time every copier launch with CUDA events on the copy
                                 stream (read with dtt_plan_stats) */
-    uint32_t reserved;
+    uint32_t host_piece_bytes;/* dtt_allgather_host: bytes per host-to-device copy (a multiple
+                                of 4096); 0 = a quarter of a slice, at least 4 MiB */
 } dtt_plan_opts;
 
 void dtt_plan_opts_default(dtt_plan_opts* opts);

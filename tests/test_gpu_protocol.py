@@ -225,6 +225,9 @@ HOST_CASES = {
                                     rounds=2, seed=41, BM=128, BN=128, num_programs=6,
                                     tiles_per_chunk=6, group_m=4),
                          {"opts": dict(method=1, piece_bytes=16384, stages=12)}),
+    # host copies of 12 KiB: many pieces per slice, chunk edges inside pieces
+    "chunks_small_host_pieces": (W.small(W.C2, M=96, N=1024, num_chunks=6),
+                                 {"opts": dict(host_piece_bytes=12288)}),
 }
 
 

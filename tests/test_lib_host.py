@@ -126,6 +126,7 @@ def test_plan_validation_codes_without_a_gpu():
     assert _create(P, P * S, bad) == D.EOUTOFROWS
     assert _create(P, P * S, bad, allgather=0) == D.EOVERLAP
     assert _create(P, P * S, good, max_regions=5) == D.ECAPACITY
+    assert _create(P, P * S, good, host_piece_bytes=1000) == D.EINVAL
     outside = [D.dtt_schedule_whole(P * S - 8, 1, 16, 16, 1), None, None]
     assert _create(P, P * S, outside, allgather=0) == D.EINVAL
     # interleaved 2D windows that share no byte pass; shifted by one byte they overlap
