@@ -97,16 +97,28 @@ template <> struct Elem<DTT_F32> {
         *reinterpret_cast<float*>(p) = uniform(fmix32(idx ^ salt));
     }
 };
+// fmix32_tail without its last xor-shift: the low byte of the full hash is the xor of bytes 0
+// and 2 of this value.
+__device__ __forceinline__ uint32_t fmix32_tail_open(uint32_t h) {
+    h *= 0x85EBCA6Bu;
+    h ^= h >> 13;
+    h *= 0xC2B2AE35u;
+    return h;
+}
+
 template <> struct Elem<DTT_U8> {
     static constexpr int bytes = 1;
     static __device__ __forceinline__ uint4 pack(uint32_t b) {
         uint32_t w[4];
 #pragma unroll
         for (uint32_t i = 0; i < 4; ++i) {
-            // low bytes of four hashes into one word
-            const uint32_t lo = __byte_perm(fmix32_tail(b ^ (4 * i)), fmix32_tail(b ^ (4 * i + 1)), 0x0040);
-            const uint32_t hi = __byte_perm(fmix32_tail(b ^ (4 * i + 2)), fmix32_tail(b ^ (4 * i + 3)), 0x0040);
-            w[i] = __byte_perm(lo, hi, 0x5410);
+            // the low bytes of four hashes g ^ (g >> 16) in one word: bytes 0 and 2 of each g
+            // gathered by two permutes per pair, then one xor for all four
+            const uint32_t g0 = fmix32_tail_open(b ^ (4 * i)), g1 = fmix32_tail_open(b ^ (4 * i + 1));
+            const uint32_t g2 = fmix32_tail_open(b ^ (4 * i + 2)), g3 = fmix32_tail_open(b ^ (4 * i + 3));
+            const uint32_t p = __byte_perm(g0, g1, 0x6240);   // g0.b0 g1.b0 g0.b2 g1.b2
+            const uint32_t q = __byte_perm(g2, g3, 0x6240);   // g2.b0 g3.b0 g2.b2 g3.b2
+            w[i] = __byte_perm(p, q, 0x5410) ^ __byte_perm(p, q, 0x7632);
         }
         return make_uint4(w[0], w[1], w[2], w[3]);
     }
