@@ -389,26 +389,25 @@ __global__ void check_kernel(const __grid_constant__ CheckParams p) {
         }
         if (late) atomicExch(&p.status->check_late, 1u);
     }
+    // Thread 0's acquire of the copier's count-out (every copier CTA adds to it with a release
+    // after its arrival signals) and the barrier order the gate words read below after all of
+    // the round's copier writes; the producers finished before this kernel started.  So the
+    // reads need no acquire of their own and go out together.
     __syncthreads();
     for (uint32_t c = blockIdx.x * blockDim.x + threadIdx.x; c < p.n_global;
          c += gridDim.x * blockDim.x) {
         const ChunkDesc cd = p.chunks[c];
         const uint64_t* row = p.gates + ((uint64_t)cd.owner * p.n_global + c) * DTT_GATE_WORDS;
-        const uint64_t cnt = dtt_dev::ld_acquire(row + DTT_GATE_COUNTER);
-        const uint64_t target = (uint64_t)p.round * cd.writers;
-        uint8_t f = 0;
-        if (cnt > target || dtt_dev::ld_relaxed(row + DTT_GATE_ERROR) != 0) {
-            f = 2;
-        } else if (cnt < target) {
-            f = 1;
-        } else {
-            for (uint32_t q = 0; q < p.P; ++q) {
-                if (q == cd.owner) continue;
-                const uint64_t* prow = p.gates + ((uint64_t)q * p.n_global + c) * DTT_GATE_WORDS;
-                if (dtt_dev::ld_acquire(prow + DTT_GATE_ARRIVAL) < p.round) f = 1;
-            }
+        const uint64_t cnt = dtt_dev::ld_relaxed(row + DTT_GATE_COUNTER);
+        const uint64_t err = dtt_dev::ld_relaxed(row + DTT_GATE_ERROR);
+        bool arrived = true;
+        for (uint32_t q = 0; q < p.P; ++q) {
+            if (q == cd.owner) continue;
+            const uint64_t* prow = p.gates + ((uint64_t)q * p.n_global + c) * DTT_GATE_WORDS;
+            arrived &= dtt_dev::ld_relaxed(prow + DTT_GATE_ARRIVAL) >= p.round;
         }
-        p.host_flags[c] = f;
+        const uint64_t target = (uint64_t)p.round * cd.writers;
+        p.host_flags[c] = (cnt > target || err != 0) ? 2 : (cnt < target || !arrived) ? 1 : 0;
     }
     __shared__ uint32_t s_last;
     __syncthreads();                     // the CTA's flag stores, then one release for all of them
