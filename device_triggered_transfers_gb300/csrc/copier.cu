@@ -40,8 +40,6 @@ __device__ __forceinline__ uint8_t ld_cg8(const uint8_t* p) {
     return (uint8_t)v;
 }
 
-// Copy one piece from buffer s to every other buffer: 16-byte vectors, kUnroll loads in
-// flight per thread, each value stored to all peers.
 // Tell the host through mapped memory that chunk c has reached every peer this round (the
 // gpu-scope arrival adds above it are ordered before this system-scope release).
 __device__ __forceinline__ void notify_host(const CopierParams& p, uint32_t c) {
@@ -49,6 +47,8 @@ __device__ __forceinline__ void notify_host(const CopierParams& p, uint32_t c) {
         asm volatile("st.release.sys.global.u32 [%0], %1;" ::"l"(p.host_arrived + c), "r"(p.round) : "memory");
 }
 
+// Copy one piece from buffer s to every other buffer: 16-byte vectors, kUnroll loads in
+// flight per thread, each value stored to all peers.
 __device__ __forceinline__ void copy_piece_vec(const CopierParams& p, uint32_t s,
                                                const PieceDesc& pc) {
     const uint32_t rv = pc.row_bytes >> 4;
@@ -412,11 +412,15 @@ __global__ void check_kernel(const __grid_constant__ CheckParams p) {
     __shared__ uint32_t s_last;
     __syncthreads();                     // the CTA's flag stores, then one release for all of them
     if (threadIdx.x == 0) {
-        uint32_t prev;
-        asm volatile("fence.acq_rel.sys;\n\t"
-                     "atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;"
-                     : "=r"(prev) : "l"(&p.status->check_arrive) : "memory");
-        s_last = prev == gridDim.x - 1;
+        if (gridDim.x == 1) {
+            s_last = 1;                  // the fence before the sequence number covers the flags
+        } else {
+            uint32_t prev;
+            asm volatile("fence.acq_rel.sys;\n\t"
+                         "atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;"
+                         : "=r"(prev) : "l"(&p.status->check_arrive) : "memory");
+            s_last = prev == gridDim.x - 1;
+        }
     }
     __syncthreads();
     if (!s_last || threadIdx.x != 0) return;
