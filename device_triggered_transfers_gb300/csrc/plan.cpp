@@ -1067,7 +1067,9 @@ int dtt_allgather_host(dtt_plan* p, const void* const* host_slices, void* host_o
         for (uint32_t r = 0; r < P; ++r) {
             if (r == out_rank) continue;
             const uint64_t x = arrived_prefix(r);
-            if (x == S || x >= back[r] + (1ull << 20) || (final && x > back[r])) {
+            // copies back of at least a host piece (or the slice's rest): on this GB300 a 4 MiB
+            // copy out, beside copies in, ran at ~110 GB/s against ~140 GB/s for 8 MiB
+            if (x == S || x >= back[r] + kPiece || (final && x > back[r])) {
                 const int prc = copy_back(r, x);
                 if (prc != DTT_OK) return prc;
             }
