@@ -2,8 +2,9 @@
 //
 // Every virtual rank is one CTA of one cooperative launch, so the ranks that wait on one
 // another are guaranteed to be resident together.  Thread 0 of each CTA does the rank's
-// notifies (atomic add, release, gpu scope) and waits (acquire loads, counted polls); a CTA
-// barrier then hands the result to the other threads.
+// notifies (one release fence, then relaxed atomic adds, gpu scope); thread src waits on the
+// cell of source src (relaxed loads, counted polls, then an acquire fence); a CTA barrier then
+// hands the result to the other threads.
 #include <cstdint>
 #include <mutex>
 #include <new>
@@ -13,42 +14,50 @@
 namespace dtt {
 namespace {
 
-__device__ __forceinline__ void red_release_add_s32(int32_t* p, int32_t v) {
-    asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
-__device__ __forceinline__ int32_t ld_acquire_s32(const int32_t* p) {
-    int32_t v;
-    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-
 __device__ __forceinline__ int32_t ld_relaxed_s32(const int32_t* p) {
     int32_t v;
     asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
 }
 
+__device__ __forceinline__ void red_relaxed_add_s32(int32_t* p, int32_t v) {
+    asm volatile("red.relaxed.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 // Notify row `me` of every peer's window, then wait for row src >= gen of my window for every
-// src != me.  window(q) returns rank q's window.  Thread 0 only.
+// src != me.  window(q) returns rank q's window.  Called by every thread of the CTA (needs
+// blockDim.x >= P); returns 0 or DTT_ETIMEDOUT in every thread.
+//  - notify: thread 0 makes one release fence, cumulative over the CTA's earlier stores (the
+//    barrier before the call), then relaxed adds that go out together;
+//  - wait: thread src polls cell src with relaxed loads (all sources at once, bounded), then an
+//    acquire fence; the closing CTA barrier passes the ordering to the other threads.
 template <class Window>
 __device__ __forceinline__ int notify_wait(Window window, uint32_t me, uint32_t P, int32_t gen,
                                            uint64_t max_polls) {
-    for (uint32_t peer = 0; peer < P; ++peer)
-        if (peer != me) red_release_add_s32(window(peer) + me, 1);
-    int rc = 0;
-    for (uint32_t src = 0; src < P && rc == 0; ++src) {
-        if (src == me) continue;
+    __shared__ int s_rc;
+    if (threadIdx.x == 0) {
+        s_rc = 0;
+        asm volatile("fence.acq_rel.gpu;" ::: "memory");
+        for (uint32_t peer = 0; peer < P; ++peer)
+            if (peer != me) red_relaxed_add_s32(window(peer) + me, 1);
+    }
+    __syncthreads();
+    const uint32_t src = threadIdx.x;
+    if (src < P && src != me) {
         const int32_t* cell = window(me) + src;
         uint64_t i = 0;
         uint32_t ns = 0;
-        while (ld_acquire_s32(cell) < gen) {
-            if (++i >= max_polls) { rc = DTT_ETIMEDOUT; break; }
+        bool ok = true;
+        while (ld_relaxed_s32(cell) < gen) {
+            if (++i >= max_polls) { ok = false; break; }
             __nanosleep(ns);
             ns = ns < 256 ? ns + 32 : 256;
         }
+        asm volatile("fence.acq_rel.gpu;" ::: "memory");
+        if (!ok) s_rc = DTT_ETIMEDOUT;
     }
-    return rc;
+    __syncthreads();
+    return s_rc;
 }
 
 struct HandrolledParams {
@@ -62,11 +71,9 @@ struct HandrolledParams {
 
 __global__ void handrolled_kernel(const __grid_constant__ HandrolledParams p) {
     const uint32_t me = blockIdx.x;
-    if (threadIdx.x == 0) {
-        auto window = [&](uint32_t q) { return p.signal[q]; };
-        p.status[me] = notify_wait(window, me, p.P, p.gen, p.max_polls);
-    }
-    __syncthreads();
+    auto window = [&](uint32_t q) { return p.signal[q]; };
+    const int rc = notify_wait(window, me, p.P, p.gen, p.max_polls);
+    if (threadIdx.x == 0) p.status[me] = rc;
     // the observable: this rank's window, read cell by cell after the waits
     for (uint32_t i = threadIdx.x; i < p.P; i += blockDim.x) p.y[me][i] = ld_relaxed_s32(p.signal[me] + i);
 }
@@ -87,11 +94,9 @@ __global__ void reveal_kernel(const __grid_constant__ RevealParams p) {
     const uint32_t me = blockIdx.x;
     for (uint32_t i = threadIdx.x; i < p.size; i += blockDim.x) p.data[me][i] = p.x[me][i];
     __syncthreads();   // the staged slice precedes thread 0's release notifies
-    if (threadIdx.x == 0) {
-        auto window = [&](uint32_t q) { return p.counters + (uint64_t)q * p.P; };
-        p.status[me] = notify_wait(window, me, p.P, p.gen, p.max_polls);
-    }
-    __syncthreads();
+    auto window = [&](uint32_t q) { return p.counters + (uint64_t)q * p.P; };
+    const int rc = notify_wait(window, me, p.P, p.gen, p.max_polls);
+    if (threadIdx.x == 0) p.status[me] = rc;
     const int32_t* peer = p.data[(me + 1) % p.P];
     for (uint32_t i = threadIdx.x; i < p.size; i += blockDim.x) p.y[me][i] = ld_relaxed_s32(peer + i);
 }
