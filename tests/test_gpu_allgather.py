@@ -100,6 +100,13 @@ SMALL = {
     "whole_f32_8writers_group4": (W.small(W.C4A, M=64, N=64, rounds=3),
                                   {"group": 4, "opts": dict(method=1, piece_bytes=4096, stages=4)}),
     "whole_1writer_group16": (W.small(W.C1, M=200), {"group": 16, "threads": 512}),
+    # one rank: no peers, so nothing is copied, but every chunk must still be marked, opened
+    # and counted complete (completion stays 0: P - 1 = 0 deliveries)
+    "single_rank_vec": (W.Workload("s1", P=1, M=64, N=256, dtype=W.BF16, kind="chunks", rounds=3,
+                                   seed=21, num_chunks=4), {}),
+    "single_rank_bulk": (W.Workload("s1b", P=1, M=64, N=256, dtype=W.BF16, kind="tile_chunks",
+                                    rounds=3, seed=22, BM=16, BN=64, num_programs=3,
+                                    tiles_per_chunk=3), {"opts": dict(method=1, piece_bytes=4096)}),
     # a paced producer: a program writes chunk k once chunk k - pace of its rank is delivered
     "tiles_paced2_bulk": (W.Workload("tp", P=4, M=512, N=512, dtype=W.BF16, kind="tile_chunks",
                                      rounds=3, seed=16, BM=64, BN=64, num_programs=6,

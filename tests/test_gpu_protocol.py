@@ -117,6 +117,27 @@ def test_state_errors():
         st.plan.close()
 
 
+def test_plan_without_chunks_runs_empty_rounds():
+    # every schedule empty: no copier is launched, the check has nothing to report, and rounds
+    # still advance one at a time
+    P, S = 3, 4096
+    bufs = [torch.zeros(P * S, dtype=torch.uint8, device="cuda") for _ in range(P)]
+    scheds = [D.dtt_schedule_empty() for _ in range(P)]
+    plan = D.Plan(bufs, P * S, scheds)
+    for s in scheds:
+        s.free()
+    prod = torch.cuda.Stream()
+    try:
+        for R in (1, 2, 3):
+            h = plan.start(prod)
+            assert [h[r].n_chunks for r in range(P)] == [0] * P and h[0].round == R
+            rep = plan.wait()
+            assert rep.status == D.OK and rep.n_short == 0 and rep.n_extra == 0
+            assert plan.next_round() == R + 1
+    finally:
+        plan.close()
+
+
 def test_producer_stream_must_differ_from_copy_stream():
     copy = torch.cuda.Stream()
     bufs = [torch.zeros(WS.buf_bytes, dtype=torch.uint8, device="cuda") for _ in range(2)]
