@@ -138,6 +138,49 @@ def test_plan_without_chunks_runs_empty_rounds():
         plan.close()
 
 
+@pytest.mark.parametrize("method", [0, 1])
+def test_zero_byte_chunk_opens_and_arrives(method):
+    # a chunk whose only region has no bytes still takes its writers' marks, opens, and arrives
+    # at every peer in schedule order between its neighbours ("Triggered Plans", Gates and rounds)
+    P, rows, rb = 3, 8, 256
+    S = rows * rb
+    bufs = [torch.zeros(P * S, dtype=torch.uint8, device="cuda") for _ in range(P)]
+    scheds = []
+    for r in range(P):
+        sc = D.dtt_schedule_empty()
+        sc.add_chunk([(r * S, 4 * rb, 1, 4 * rb)], 1)
+        sc.add_chunk([(r * S, 0, 1, 0)], 2)                    # zero bytes, two writers
+        sc.add_chunk([(r * S + 4 * rb, 4 * rb, 1, 4 * rb)], 1)
+        scheds.append(sc)
+    plan = D.Plan(bufs, P * S, scheds, D.dtt_plan_opts_default(method=method, piece_bytes=512))
+    for sc in scheds:
+        sc.free()
+    prod = torch.cuda.Stream()
+    try:
+        for R in (1, 2):
+            h = plan.start(prod)
+            want = torch.cat([torch.full((S,), 10 * R + r, dtype=torch.uint8) for r in range(P)])
+            with torch.cuda.stream(prod):
+                for r in range(P):
+                    bufs[r][r * S:(r + 1) * S].copy_(want[r * S:(r + 1) * S].cuda(), non_blocking=False)
+            D.dtt_publish(h, 0, 3 * P, 0, prod)        # every chunk: its writer count of marks
+            rep = plan.wait()
+            assert rep.status == D.OK
+            for q in range(P):
+                assert torch.equal(bufs[q].cpu(), want)
+            g = plan.read_gates()
+            for c in range(3 * P):
+                owner = c // 3
+                assert int(g[owner, c, D.GATE_READY]) == R
+                assert int(g[owner, c, D.GATE_COMPLETION]) == R * (P - 1)
+                for q in range(P):
+                    if q != owner:
+                        assert int(g[q, c, D.GATE_ARRIVAL]) == R
+            plan.next_round()
+    finally:
+        plan.close()
+
+
 def test_producer_stream_must_differ_from_copy_stream():
     copy = torch.cuda.Stream()
     bufs = [torch.zeros(WS.buf_bytes, dtype=torch.uint8, device="cuda") for _ in range(2)]
