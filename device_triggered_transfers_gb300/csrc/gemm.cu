@@ -164,9 +164,12 @@ __device__ __forceinline__ uint32_t pack_bf16x2(uint32_t lo, uint32_t hi) {
 }
 
 // Work is cut in units of TN / 128 adjacent tiles of one tile row.  Every rank's units form one
-// sequence (rank 0's, then rank 1's, ...) and program p takes its units p, p + NP, ..., so no
-// program has more than one unit above the mean.  Tile (tm, tn) is step tm * tiles_n + tn of
-// its rank and, once stored, gets one mark on chunk first_chunk + step / NP.
+// sequence, the ranks taking turns (unit 0 of rank 0, of rank 1, ..., then unit 1 of each), and
+// program p takes its places p, p + NP, ..., so no program has more than one unit above the
+// mean and every rank's chunks open at the same pace: the copier's CTAs of every source have
+// work all along, and the last chunks to open are small ones of every rank, not one rank's
+// whole tail.  Tile (tm, tn) is step tm * tiles_n + tn of its rank and, once stored, gets one
+// mark on chunk first_chunk + step / NP.
 template <uint32_t TN>
 __global__ void __launch_bounds__(THREADS, 1) gemm_producer_kernel(const __grid_constant__ GemmParams p) {
     using G = Cfg<TN>;
@@ -221,7 +224,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_producer_kernel(const __grid_
             uint32_t stage = 0, phase = 0, issued = 0;
             bool ok = true;
             for (uint32_t gu = blockIdx.x; gu < p.P * units && ok; gu += p.NP) {
-                    const uint32_t r = gu / units, u = gu % units;
+                    const uint32_t r = gu % p.P, u = gu / p.P;
                     const int32_t row_a = (int32_t)(r * p.M + (u / units_n) * BM);
                     const int32_t row_b = (int32_t)((u % units_n) * TN);
                     for (uint32_t kb = 0; kb < kblocks; ++kb) {
@@ -272,7 +275,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_producer_kernel(const __grid_
         const uint32_t row_in_tile = warp * 32 + lane;
         bool ok = true;
         for (uint32_t gu = blockIdx.x; gu < p.P * units && ok; gu += p.NP) {
-                const uint32_t r = gu / units, u = gu % units;
+                const uint32_t r = gu % p.P, u = gu / p.P;
                 bool mine = bar_wait(saddr(acc_full + acc), acc_phase, abort_flag);
                 if (!mine) fail();
                 // one decision for all 128 epilogue threads, so none is left at a barrier
@@ -548,9 +551,9 @@ __device__ __forceinline__ void umma_commit_local2(uint32_t bar) {
                  ::"r"(bar) : "memory");
 }
 
-// A unit is a 256 x 256 block; every rank's units form one sequence (rank 0's, then rank 1's,
-// ...) and cluster c of NC takes its units c, c + NC, ...; CTA q of the pair owns the unit's
-// rows 128 q .. 128 q + 127.  Tile (tm, tn) is step
+// A unit is a 256 x 256 block; every rank's units form one sequence, the ranks taking turns as
+// in the one-CTA form, and cluster c of NC takes its places c, c + NC, ...; CTA q of the pair
+// owns the unit's rows 128 q .. 128 q + 127.  Tile (tm, tn) is step
 // tm * tiles_n + tn of its rank and, once stored, gets one mark on chunk first_chunk + step / NP.
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 gemm2_producer_kernel(const __grid_constant__ GemmParams p) {
@@ -609,7 +612,7 @@ gemm2_producer_kernel(const __grid_constant__ GemmParams p) {
             uint32_t stage = 0, phase = 0, issued = 0;
             bool ok = true;
             for (uint32_t gu = c0; gu < p.P * units && ok; gu += NC) {
-                    const uint32_t r = gu / units, u = gu % units;
+                    const uint32_t r = gu % p.P, u = gu / p.P;
                     const int32_t row_a = (int32_t)(r * p.M + (u / units_n) * 256 + q * BM);
                     const int32_t row_b = (int32_t)((u % units_n) * G2_TN + q * BN);
                     for (uint32_t kb = 0; kb < kblocks; ++kb) {
@@ -667,7 +670,7 @@ gemm2_producer_kernel(const __grid_constant__ GemmParams p) {
         const uint32_t row_in_tile = warp * 32 + lane;
         bool ok = true;
         for (uint32_t gu = c0; gu < p.P * units && ok; gu += NC) {
-                const uint32_t r = gu / units, u = gu % units;
+                const uint32_t r = gu % p.P, u = gu / p.P;
                 bool mine = bar_wait(saddr(acc_full + acc), acc_phase, abort_flag);
                 if (!mine) fail();
                 if (!epi_all(mine && !*abort_flag)) { ok = false; break; }
