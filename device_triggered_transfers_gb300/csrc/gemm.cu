@@ -904,6 +904,42 @@ bool operand_maps(const void* A, const void* Bt, uint64_t rows_a, uint64_t N, ui
     return true;
 }
 
+// How many clusters of a CTA-pair kernel can be resident at once: a property of the kernel,
+// its shared memory and the device.  The query costs the host microseconds, so it is asked
+// once per (device, kernel) and reused by every later launch.
+struct FitEntry {
+    int dev;
+    const void* kernel;
+    int fit;
+};
+std::mutex g_fit_mu;
+FitEntry g_fit[16];
+uint32_t g_fit_used = 0;
+
+template <class Kern>
+int cluster_fit(Kern kernel, uint32_t smem) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    const void* key = reinterpret_cast<const void*>(kernel);
+    {
+        std::lock_guard<std::mutex> lock(g_fit_mu);
+        for (uint32_t i = 0; i < g_fit_used; ++i)
+            if (g_fit[i].dev == dev && g_fit[i].kernel == key) return g_fit[i].fit;
+    }
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(2, 1, 1);
+    cfg.blockDim = dim3(THREADS, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    int fit = 0;
+    if (cudaOccupancyMaxActiveClusters(&fit, kernel, &cfg) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    std::lock_guard<std::mutex> lock(g_fit_mu);
+    if (g_fit_used < 16) g_fit[g_fit_used++] = FitEntry{dev, key, fit};
+    return fit;
+}
+
 }  // namespace
 
 template <uint32_t TN>
@@ -958,16 +994,8 @@ static bool launch_consumer_pair(const ConsumerParams& cp, uint32_t ctas, uint64
         if (g2c_smem<ST>() > budget) return launch_consumer_pair<ST - 1>(cp, ctas, budget, s);
     }
     if (g2c_smem<ST>() > budget) return false;
-    cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3(2 * (ctas / 2), 1, 1);
-    cfg.blockDim = dim3(THREADS, 1, 1);
-    cfg.dynamicSmemBytes = g2c_smem<ST>();
-    cfg.stream = s;
-    int fit = 0;
-    if (cudaOccupancyMaxActiveClusters(&fit, gemm2_consumer_kernel<ST>, &cfg) != cudaSuccess || fit < 1) {
-        (void)cudaGetLastError();
-        return false;
-    }
+    const int fit = cluster_fit(gemm2_consumer_kernel<ST>, g2c_smem<ST>());
+    if (fit < 1) return false;
     const uint32_t pairs = std::min<uint32_t>(ctas / 2, (uint32_t)fit);
     gemm2_consumer_kernel<ST><<<2 * pairs, THREADS, g2c_smem<ST>(), s>>>(cp);
     return true;
@@ -1068,15 +1096,8 @@ extern "C" int dtt_gemm_producer(const void* A, const void* Bt, void* const* buf
     gp.err = err;
     if (pair) {
         // a persistent grid: no more CTA pairs than can be resident at once
-        cudaLaunchConfig_t cfg{};
-        cfg.gridDim = dim3(2 * (num_programs / 2), 1, 1);
-        cfg.blockDim = dim3(THREADS, 1, 1);
-        cfg.dynamicSmemBytes = G2_SMEM;
-        cfg.stream = stream;
-        int fit = 0;
-        cudaError_t e = cudaOccupancyMaxActiveClusters(&fit, gemm2_producer_kernel, &cfg);
-        if (e != cudaSuccess || fit < 1)
-            return fail(DTT_ECUDA, "dtt_gemm_producer: no CTA pair fits (%s)", cudaGetErrorString(e));
+        const int fit = cluster_fit(gemm2_producer_kernel, G2_SMEM);
+        if (fit < 1) return fail(DTT_ECUDA, "dtt_gemm_producer: no CTA pair fits on this device");
         const uint32_t pairs = std::min<uint32_t>(num_programs / 2, (uint32_t)fit);
         gemm2_producer_kernel<<<2 * pairs, THREADS, G2_SMEM, stream>>>(gp);
     } else if (TN == 256)
