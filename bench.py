@@ -38,7 +38,8 @@ DEFAULT_CONFIG = W.C2.name
 NCU_TRAFFIC = {("c2_chunks_p4", "copier_bulk_kernel"): 474083584,
                # captured with 2000 rows per rank (--rows 2000) and scaled by the rows, 4x
                ("c3_tiles_p8", "copier_bulk_kernel"): 8018295392,
-               ("c5_gemm_p4", "gemm2_producer_kernel"): 179372032}
+               ("c5_gemm_p4", "gemm2_producer_kernel"): 179372032,
+               ("c5_gemm_p4", "copier_kernel"): 206286848}
 # DRAM bytes (read + write) of one whole round, producer, copier and check together, from an
 # ncu range-replay capture of three rounds of the benchmark's launch (--profile-rounds 3)
 ROUND_TRAFFIC = {"c2_chunks_p4": (2848171, 516156075), "c3_tiles_p8": (12696405, 8237207979),
