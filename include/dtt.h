@@ -398,7 +398,9 @@ typedef struct dtt_fill_desc {
                                 that the bytes written but not yet copied stay within `pace`
                                 chunks per rank and the copier reads them from L2.  Timing only:
                                 the data and marks are the same.  Needs the copier running beside
-                                the producer (deferred_copier 0 or 2). */
+                                the producer (deferred_copier 0 or 2) and every producer CTA
+                                resident at once: a wait on a chunk whose writers are not yet
+                                running only runs out. */
     uint32_t* group_counters;/* group > 1: device uint32[P * steps per rank], zero before the
                                 first round (the producer leaves them zero after each round) */
 } dtt_fill_desc;
