@@ -314,6 +314,23 @@ extern "C" int dtt_fill_producer(void* const* bufs, uint32_t P, const dtt_fill_d
     p.group = group;
     p.counters = d->group_counters;
     p.pace = d->pace;
+    if (p.pace) {
+        // a paced program waits for chunks that other programs write: they must all be
+        // resident at once, or the waits only run out (the copier's CTAs take room too, so this
+        // is a necessary condition, not a sufficient one)
+        int per_sm = 0, sms = 0, dev = 0;
+        const void* k = d->dtype == DTT_BF16 ? (const void*)fill_kernel<DTT_BF16>
+                      : d->dtype == DTT_F32  ? (const void*)fill_kernel<DTT_F32>
+                                             : (const void*)fill_kernel<DTT_U8>;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, (int)threads, 0) != cudaSuccess)
+            return fail(DTT_ECUDA, "dtt_fill_producer: cannot query the producer's occupancy");
+        const uint64_t ctas = (uint64_t)d->num_programs * cluster * group * P;
+        if (ctas > (uint64_t)per_sm * (uint64_t)sms)
+            return fail(DTT_EINVAL, "dtt_fill_producer: a paced producer needs all its %llu CTAs resident "
+                                    "at once (at most %d per SM here)", (unsigned long long)ctas, per_sm);
+    }
 
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(d->num_programs * cluster * group, P, 1);

@@ -411,3 +411,18 @@ def test_nested_plans_close_in_with_blocks():
     assert B.plan.state == D.CLOSED                # the outer block's close finished it
     _round1_everywhere(B, WS)
     assert B.plan.close() == D.OK
+
+
+def test_paced_producer_that_cannot_be_resident_is_rejected():
+    # 8 ranks x 148 programs of 1024 threads cannot all be resident, so the pacing waits would
+    # only run out: the launch is refused, and closing the plan still drains its copier
+    w = W.Workload("pr", P=8, M=1024, N=1024, dtype=W.BF16, kind="tile_chunks", rounds=1, seed=31,
+                   BM=128, BN=128, num_programs=148, tiles_per_chunk=148)
+    st = runner.make(w, pace=2, threads=1024)
+    try:
+        h = st.plan.start(st.producer_stream)
+        with pytest.raises(D.DttError) as e:
+            D.dtt_fill_producer(st.buf_ptrs, st.desc, h, st.producer_stream)
+        assert e.value.code == D.EINVAL
+    finally:
+        st.plan.close()
