@@ -460,8 +460,45 @@ def dtt_publish(handles, first_chunk: int, n_chunks: int, marks: int = 0, stream
 
 
 def dtt_barrier_handrolled(signal, y, gen: int, max_polls: int, status, stream=None) -> None:
+    P = len(signal)
+    if len(y) != P:
+        raise DttError(EINVAL, f"dtt_barrier_handrolled: y has {len(y)} windows, need P = {P}")
+    for name, lst in (("signal", signal), ("y", y)):
+        for r, t in enumerate(lst):
+            n = _elements(t)
+            if t is None or (n is not None and n < P):
+                raise DttError(EINVAL, f"dtt_barrier_handrolled: {name}[{r}] holds {n} int32, need P = {P}")
+    n = _elements(status)
+    if status is None or (n is not None and n < P):
+        raise DttError(EINVAL, f"dtt_barrier_handrolled: status holds {n} int32, need P = {P}")
     _check(lib().dtt_barrier_handrolled(_ptr_array(signal), _ptr_array(y), len(signal), gen,
                                         max_polls, _ptr(status), _stream(stream)))
+
+
+def _elements(t) -> Optional[int]:
+    """Element count of a tensor argument; None for a raw address (its size is unknown here)."""
+    if t is None or isinstance(t, int):
+        return None
+    return int(t.numel())
+
+
+def _check_reveal_args(who: str, P: int, x, data, y, size: int, status) -> None:
+    """The reveal reads x[r] and writes data[r] and y[r] (size int32 each) for every rank r < P,
+    and status[r]: refuse short lists and short tensors before the kernel could run past them."""
+    if isinstance(x, C.Array) or isinstance(data, C.Array) or isinstance(y, C.Array):
+        raise DttError(EINVAL, f"{who}: pass lists of P slices, not marshalled arrays")
+    for name, lst in (("x", x), ("data", data), ("y", y)):
+        if len(lst) != P:
+            raise DttError(EINVAL, f"{who}: {name} has {len(lst)} slices, need P = {P}")
+        for r, t in enumerate(lst):
+            n = _elements(t)
+            if t is None or (n is not None and n < size):
+                raise DttError(EINVAL, f"{who}: {name}[{r}] holds {n} int32, need size = {size}")
+            if n is not None and getattr(t, "element_size", lambda: 4)() != 4:
+                raise DttError(EINVAL, f"{who}: {name}[{r}] is not a 4-byte (int32) tensor")
+    n = _elements(status)
+    if status is None or (n is not None and n < P):
+        raise DttError(EINVAL, f"{who}: status holds {n} int32, need P = {P}")
 
 
 class Barrier:
@@ -474,6 +511,7 @@ class Barrier:
         self.P = P
 
     def reveal(self, x, data, y, size: int, max_polls: int, status, stream=None) -> None:
+        _check_reveal_args("Barrier.reveal", self.P, x, data, y, size, status)
         _check(lib().dtt_barrier_reveal(self._h, _ptr_array(x), _ptr_array(data), _ptr_array(y),
                                         size, max_polls, _ptr(status), _stream(stream)))
 
@@ -497,6 +535,7 @@ def dtt_barrier_reveal_noalloc(x, data, y, size: int, max_polls: int, status, st
     """The builtin reveal with its counters in the library's fixed device array: allocates
     nothing (for callers that cannot allocate device memory at call time).  Calls that overlap
     on the GPU share that array and race; run them on one stream."""
+    _check_reveal_args("dtt_barrier_reveal_noalloc", len(x), x, data, y, size, status)
     _check(lib().dtt_barrier_reveal_noalloc(_ptr_array(x), _ptr_array(data), _ptr_array(y),
                                             len(x), size, max_polls, _ptr(status), _stream(stream)))
 

@@ -211,13 +211,17 @@ __global__ void __launch_bounds__(1024) fill_kernel(const __grid_constant__ Fill
     const uint32_t salt = fmix32(p.seed ^ fmix32(r ^ fmix32(h.round)));
     char* base = p.bufs[r] + p.slice_off[r];
     uint64_t paced = ~0ull;       // the last chunk this program waited for
+    bool pacing = p.pace != 0;    // off for the rest of the launch once a pacing wait runs out
     for (uint64_t step = prog; step < T; step += p.NP) {
-        if (p.pace) {
+        if (pacing) {
             // keep the bytes written but not yet delivered within `pace` chunks of this rank:
             // the copier then reads them from L2.  The result does not depend on the outcome.
+            // A wait that runs out means the copier is not keeping up (or not running): this
+            // CTA stops pacing, so it stalls at most once per launch.
             const uint64_t k = step / p.TPC;
             if (k >= p.pace && k != paced) {
-                (void)dtt_wait_reusable(h, h.first_chunk + (uint32_t)(k - p.pace), kPacePolls);
+                if (dtt_wait_reusable(h, h.first_chunk + (uint32_t)(k - p.pace), kPacePolls) != 0)
+                    pacing = false;
                 paced = k;
             }
         }
@@ -318,18 +322,42 @@ extern "C" int dtt_fill_producer(void* const* bufs, uint32_t P, const dtt_fill_d
         // a paced program waits for chunks that other programs write: they must all be
         // resident at once, or the waits only run out (the copier's CTAs take room too, so this
         // is a necessary condition, not a sufficient one)
-        int per_sm = 0, sms = 0, dev = 0;
+        // Ranks outside rank_mask exit at once and hold no room.  Clusters are placed whole, so
+        // for cluster > 1 the count that matters is of clusters the device can hold at once.
+        uint32_t producing = 0;
+        for (uint32_t r = 0; r < P; ++r) producing += (d->rank_mask >> r) & 1u;
         const void* k = d->dtype == DTT_BF16 ? (const void*)fill_kernel<DTT_BF16>
                       : d->dtype == DTT_F32  ? (const void*)fill_kernel<DTT_F32>
                                              : (const void*)fill_kernel<DTT_U8>;
-        if (cudaGetDevice(&dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, (int)threads, 0) != cudaSuccess)
-            return fail(DTT_ECUDA, "dtt_fill_producer: cannot query the producer's occupancy");
-        const uint64_t ctas = (uint64_t)d->num_programs * cluster * group * P;
-        if (ctas > (uint64_t)per_sm * (uint64_t)sms)
-            return fail(DTT_EINVAL, "dtt_fill_producer: a paced producer needs all its %llu CTAs resident "
-                                    "at once (at most %d per SM here)", (unsigned long long)ctas, per_sm);
+        if (cluster > 1) {
+            cudaLaunchConfig_t occ{};
+            occ.gridDim = dim3(d->num_programs * cluster * group, P, 1);
+            occ.blockDim = dim3(threads, 1, 1);
+            cudaLaunchAttribute ca[1];
+            ca[0].id = cudaLaunchAttributeClusterDimension;
+            ca[0].val.clusterDim.x = cluster;
+            ca[0].val.clusterDim.y = 1;
+            ca[0].val.clusterDim.z = 1;
+            occ.attrs = ca;
+            occ.numAttrs = 1;
+            int clusters = 0;
+            if (cudaOccupancyMaxActiveClusters(&clusters, k, &occ) != cudaSuccess)
+                return fail(DTT_ECUDA, "dtt_fill_producer: cannot query the producer's cluster occupancy");
+            const uint64_t need = (uint64_t)d->num_programs * group * producing;
+            if (need > (uint64_t)clusters)
+                return fail(DTT_EINVAL, "dtt_fill_producer: a paced producer needs all its %llu clusters "
+                                        "resident at once (at most %d here)", (unsigned long long)need, clusters);
+        } else {
+            int per_sm = 0, sms = 0, dev = 0;
+            if (cudaGetDevice(&dev) != cudaSuccess ||
+                cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+                cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, (int)threads, 0) != cudaSuccess)
+                return fail(DTT_ECUDA, "dtt_fill_producer: cannot query the producer's occupancy");
+            const uint64_t ctas = (uint64_t)d->num_programs * group * producing;
+            if (ctas > (uint64_t)per_sm * (uint64_t)sms)
+                return fail(DTT_EINVAL, "dtt_fill_producer: a paced producer needs all its %llu CTAs resident "
+                                        "at once (at most %d per SM here)", (unsigned long long)ctas, per_sm);
+        }
     }
 
     cudaLaunchConfig_t cfg{};

@@ -1080,6 +1080,16 @@ extern "C" int dtt_gemm_producer(const void* A, const void* Bt, void* const* buf
     GemmParams gp{};
     if (!operand_maps(A, Bt, (uint64_t)P * M, N, K, pair ? BN : TN, &gp.tmA, &gp.tmB))
         return fail(DTT_ECUDA, "dtt_gemm_producer: cannot encode the tensor maps");
+    // the producer marks first_chunk + (row-major tile index) / num_programs: every rank's part of
+    // the plan must have exactly that many chunks (tile_chunks with tiles_per_chunk = num_programs)
+    const uint64_t tiles = (uint64_t)(M / BM) * (N / BN);
+    const uint64_t want_chunks = (tiles + num_programs - 1) / num_programs;
+    for (uint32_t r = 0; r < P; ++r)
+        if (handles[r].n_chunks != want_chunks || handles[r].P != P || handles[r].rank != r)
+            return fail(DTT_EINVAL, "dtt_gemm_producer: rank %u's handle has %u chunks; a %u x %u output in "
+                                    "128 x 128 tiles over %u programs needs %llu (tile_chunks with "
+                                    "tiles_per_chunk = num_programs)", r, handles[r].n_chunks, M, N,
+                        num_programs, (unsigned long long)want_chunks);
     for (uint32_t r = 0; r < P; ++r) {
         if (!bufs[r] || (reinterpret_cast<uintptr_t>(bufs[r]) + slice_off[r]) % 16)
             return fail(DTT_EINVAL, "dtt_gemm_producer: rank %u's output is not 16-byte aligned", r);

@@ -127,13 +127,19 @@ def run_round(st: Setup, raise_on_error: bool = True):
     return st.plan.wait(raise_on_error=raise_on_error)
 
 
+def sm_count() -> int:
+    """Streaming multiprocessors of the current CUDA device (the launch shapes below scale with
+    it)."""
+    return int(torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count)
+
+
 def bench_launch(w) -> dict:
     """The launch configuration the benchmark times for workload ``w`` (tests use it too).
 
     Chunked workloads: the bulk-copy copier (three one-warp CTAs per SM, each with a ring of two
     32 KiB stages, so the producer keeps the SM's threads and registers), and one program per
     rank made of a group of
-    38 CTAs (152 in all, one per SM) that writes the rank's chunks in order and marks each once,
+    SMs / P CTAs (one per SM in all) that writes the rank's chunks in order and marks each once,
     so every rank's chunk k opens in wave k and the copier follows the waves.
     whole(): the bulk-copy copier (two CTAs per SM, 2 x 56 KiB stages each) over the contiguous
     slices; the single chunk per rank opens only when the whole slice is written, so the fill
@@ -144,8 +150,9 @@ def bench_launch(w) -> dict:
     chunk k), so the copier reads what the producer wrote from L2; that needs every producer
     CTA resident at once (128-thread CTAs).  The GEMM producer keeps the vector copier: its own
     shared-memory ring leaves no room for a bulk-copy ring on the same SM."""
+    sms = sm_count()
     if w.kind == "chunks":     # three bulk-copy CTAs per SM: one thread alone cannot keep HBM busy
-        return {"group": 38, "programs": 1, "threads": 256,
+        return {"group": max(1, sms // len(w.senders())), "programs": 1, "threads": 256,
                 "opts": dtt_plan_opts_default(method=1, piece_bytes=32768, stages=2, ctas_per_sm=3)}
     if w.kind == "whole":
         # the copier is launched after the producer's launch (it has nothing to do before the
@@ -156,7 +163,7 @@ def bench_launch(w) -> dict:
         if -(-w.M // -(-w.M // NP)) == NP:
             # one step per program: each writer becomes a group of CTAs (up to 8, enough to
             # cover the SMs) that marks the chunk once
-            g = max(1, min(8, 152 // (len(w.senders()) * NP)))
+            g = max(1, min(8, sms // (len(w.senders()) * NP)))
             return {"group": g, "threads": 512, "opts": opts}
         return {"threads": 1024, "opts": opts}
     if w.K == 0:       # the tiled fill in 128-thread CTAs: all of them resident at once

@@ -396,11 +396,14 @@ typedef struct dtt_fill_desc {
                                 (advisory: at most ~1 ms, then it goes on) until chunk k - pace of
                                 its rank is reusable (dtt_reusable: delivered to every peer), so
                                 that the bytes written but not yet copied stay within `pace`
-                                chunks per rank and the copier reads them from L2.  Timing only:
-                                the data and marks are the same.  Needs the copier running beside
-                                the producer (deferred_copier 0 or 2) and every producer CTA
-                                resident at once: a wait on a chunk whose writers are not yet
-                                running only runs out. */
+                                chunks per rank and the copier reads them from L2.  A CTA whose
+                                wait runs out stops pacing for the rest of the launch, so each
+                                CTA stalls at most once (~1 ms) per launch when the copier lags.
+                                Timing only: the data and marks are the same, and the wait is
+                                on a chunk earlier in schedule order whose writers have all
+                                marked it, so it cannot hold up any mark.  Needs the copier
+                                running beside the producer (deferred_copier 0 or 2) and every
+                                producer CTA resident at once (checked: DTT_EINVAL otherwise). */
     uint32_t* group_counters;/* group > 1: device uint32[P * steps per rank], zero before the
                                 first round (the producer leaves them zero after each round) */
 } dtt_fill_desc;
@@ -423,7 +426,8 @@ int dtt_fill_producer(void* const* bufs, uint32_t P, const dtt_fill_desc* desc,
  *  - err: device uint32, incremented when a bounded internal wait gives up (0 after a clean
  *    run).
  *  - Needs M and N multiples of 128, K a multiple of 64, and 16-byte aligned operands and
- *    outputs.  One CTA per SM uses ~194 KiB of shared memory, so it runs beside the vector
+ *    outputs.  Every handle must have ceil((M / 128) (N / 128) / num_programs) chunks (the
+ *    schedule above), else DTT_EINVAL before anything is launched.  One CTA per SM uses ~194 KiB of shared memory, so it runs beside the vector
  *    copier, not the bulk copier.
  * Errors: DTT_EINVAL, DTT_ECUDA. */
 int dtt_gemm_producer(const void* A, const void* Bt, void* const* bufs, uint32_t P, uint32_t M,

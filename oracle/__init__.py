@@ -15,6 +15,9 @@ Modules and what pins each (see the test files named):
   builder-defined.  fmix32 is pinned by published MurmurHash3 vectors, the bf16 rounding by
   torch's conversion, the uniform mapping by closed form (tests/test_oracle_hash.py).  The salt
   composition itself has no pin beyond its definition: "parity unpinned" for that part.
+* ``cfill``     the same values from a plain-C restatement (``fill.c``, compiled with gcc), so
+  full-size buffers can be compared byte for byte.  Pinned by the same vectors and closed forms
+  as ``hashfill`` and checked element by element against it (tests/test_oracle_hash.py).
 * ``schedule``  whole / chunks / tile_chunks builders, the step-to-tile orders, the global
   chunk numbering and plan validation.  Pinned by golden counts, the 1 GiB split, coverage by
   brute-force ownership maps and the order special cases (tests/test_oracle_schedule.py).

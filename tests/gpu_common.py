@@ -1,7 +1,8 @@
-"""Helpers shared by the GPU parity tests: the oracle side of a workload (oracle/run.py) and
-sampled byte offsets for full-size workloads."""
+"""Helpers shared by the GPU parity tests: the oracle side of a workload (oracle/run.py), the
+oracle's whole expected buffer (oracle/cfill.py), and sampled byte offsets."""
 import numpy as np
 
+from oracle import cfill
 from oracle.run import expected_bytes, make_plan as oracle_plan, run_round as oracle_round  # noqa: F401
 
 
@@ -17,3 +18,22 @@ def sample_offsets(w, n, seed, o=None):
                 ends += [off, off + rb - 1, last, last - rb + 1]
         offs.append(np.asarray(ends, dtype=np.int64))
     return np.unique(np.concatenate(offs))
+
+
+def expected_on_device(w, rnd):
+    """The oracle's closed form of every buffer after round rnd (computed on the host by the C
+    oracle), moved to the device so that whole buffers can be compared there."""
+    import torch
+    return torch.from_numpy(cfill.expected_buffer(w, rnd)).cuda()
+
+
+def assert_buffers_equal(bufs, want, what):
+    """Every byte of every buffer equals the oracle's; on a mismatch name the first bad byte."""
+    import torch
+    for q, b in enumerate(bufs):
+        if torch.equal(b, want):
+            continue
+        bad = (b != want).nonzero()
+        first = int(bad[0, 0])
+        raise AssertionError(f"{what}: buffer {q} differs from the oracle at {bad.shape[0]} byte(s), "
+                             f"first at offset {first} (got {int(b[first])}, want {int(want[first])})")

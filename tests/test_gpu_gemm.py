@@ -84,13 +84,11 @@ def test_gemm_producer_full_size():
     w = W.C5
     A, Bt = W.gemm_inputs(w.P, w.M, w.N, w.K, w.seed)
     st = runner.make_gemm(w, A, Bt, opts=runner.bench_launch(w)["opts"])    # the benchmark's launch
-    rows = np.unique(np.concatenate([[0, 127, 128, w.M - 1],
-                                     np.random.default_rng(7).integers(0, w.M, 60)]))
     try:
         for R in range(1, 3):
             rep = runner.run_gemm_round(st)
             assert rep.status == D.OK and int(st.err.item()) == 0
-            _check(st, A, Bt, rows=torch.from_numpy(rows))
+            _check(st, A, Bt)            # all 2048 rows of every rank, every copy bit for bit
             st.plan.next_round()
     finally:
         st.plan.close()

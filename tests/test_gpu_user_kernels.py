@@ -37,6 +37,8 @@ def _build():
                                        C.c_void_p, C.c_void_p, C.c_void_p]
     lib.user_probe.argtypes = [C.POINTER(D.dtt_handle), C.c_uint32, C.c_uint32, C.c_void_p,
                                C.c_void_p]
+    lib.user_produce_reverse.argtypes = [C.POINTER(D.dtt_handle), C.c_void_p, C.c_uint64, C.c_uint64,
+                                         C.c_void_p]
     return lib
 
 
@@ -149,5 +151,68 @@ def test_user_paced_producer_and_reusable():
         rep = plan.wait(raise_on_error=False)
         assert rep.status == D.EINVAL and rep.device_status & 1
         assert int(probe[0, 0].item()) == 0
+    finally:
+        plan.close()
+
+
+@pytest.mark.parametrize("method", [1, 0], ids=["bulk_copier", "vector_copier"])
+def test_out_of_order_producer_head_of_line(method):
+    # "Triggered Plans", The kernel author's contract, item 1, and "Triggered SDMA Plans",
+    # Testing (head-of-line ordering): a producer completes its chunks last to first.  The
+    # result is still correct -- buffers and gate words 0-4 equal the oracle's for the same
+    # order of marks -- only later: no chunk of a rank arrives anywhere before that rank's
+    # first chunk (the head of its queues) has opened, although the others opened earlier.
+    from oracle import plan as OP
+    from oracle import schedule as OS
+    lib = _build()
+    assert lib.user_kernels_prepare() == 0
+    P, n, chunk = 3, 4, 1 << 20
+    S = n * chunk
+    bufs = [torch.zeros(P * S, dtype=torch.uint8, device="cuda") for _ in range(P)]
+    scheds = [D.dtt_schedule_chunks(r * S, n, chunk, chunk, n) for r in range(P)]
+    opts = D.dtt_plan_opts_default(method=method, piece_bytes=65536, stages=3) if method == D.COPY_TMA \
+        else D.dtt_plan_opts_default(method=method, copier_threads=256)
+    plan = D.Plan(bufs, P * S, scheds, opts)
+    for s_ in scheds:
+        s_.free()
+    # the oracle: same schedules, marks in the same (reverse) order, queues run after each mark
+    o_bufs = [np.zeros(P * S, dtype=np.uint8) for _ in range(P)]
+    o = OP.Plan(o_bufs, [OS.chunks(r * S, n, chunk, chunk, n) for r in range(P)])
+    prod = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    try:
+        for rnd in (1, 2):
+            h = plan.start(prod)
+            for r in range(P):
+                assert lib.user_produce_reverse(C.byref(h[r]), C.c_void_p(bufs[r].data_ptr() + r * S),
+                                                chunk, 20000, C.c_void_p(prod.cuda_stream)) == 0
+            rep = plan.wait()
+            assert rep.status == D.OK and rep.copier_timeouts == 0
+            o.start()
+            log0 = len(o.delivery_log)
+            for r in range(P):
+                o.bufs[r][r * S:(r + 1) * S] = _values(r, rnd, S)
+                for k in reversed(range(n)):
+                    o.mark_ready(r, o.first[r] + k)
+                    o.copier_progress()
+                    if k > 0:           # head of line: nothing of rank r has moved yet
+                        assert all(s != r for (s, _, _) in o.delivery_log[log0:])
+            assert o.wait()[0] == OP.OK
+            g = plan.read_gates()
+            np.testing.assert_array_equal(g[:, :, :5], o.gates)
+            for q in range(P):
+                np.testing.assert_array_equal(bufs[q].cpu().numpy(), o.bufs[q])
+            for r in range(P):
+                head = h[r].first_chunk
+                t_head = int(g[r, head, D.GATE_T_OPEN])
+                opens = [int(g[r, head + k, D.GATE_T_OPEN]) for k in range(n)]
+                assert opens == sorted(opens, reverse=True)      # they opened last to first
+                assert opens[n - 1] + 3 * 20000 <= t_head         # ... with the spins between them
+                for k in range(n):
+                    for q in range(P):
+                        if q != r:
+                            assert int(g[q, head + k, D.GATE_T_ARRIVE]) >= t_head, (rnd, r, k, q)
+            plan.next_round()
+            o.next_round()
     finally:
         plan.close()

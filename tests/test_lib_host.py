@@ -136,3 +136,64 @@ def test_plan_validation_codes_without_a_gpu():
     c.add_chunk([(3, 4, 3, 8)], 1)
     assert _create(2, 24, [a, b], allgather=0) in (D.ECUDA, D.OK)
     assert _create(2, 24, [a, c], allgather=0) == D.EOVERLAP
+
+
+def _i32(n):
+    import torch
+    return torch.zeros(n, dtype=torch.int32)
+
+
+def test_reveal_wrappers_refuse_short_lists_and_tensors():
+    # the reveal reads and writes P slices of `size` int32 and P status words: a short list or
+    # tensor is refused on the host, before any kernel could run past it
+    P, size = 4, 16
+    ok = [_i32(size) for _ in range(P)]
+    cases = [
+        (ok, ok[:3], ok, _i32(P)),                         # data short of a slice
+        (ok, ok, ok[:2], _i32(P)),                         # y short of slices
+        (ok, ok, ok[:3] + [_i32(size - 1)], _i32(P)),      # one y slice too small
+        (ok[:3] + [_i32(1)], ok, ok, _i32(P)),             # one x slice too small
+        (ok, ok, ok, _i32(P - 1)),                         # status too small
+        (ok, ok, ok, None),
+    ]
+    for x, data, y, status in cases:
+        with pytest.raises(D.DttError) as e:
+            D.dtt_barrier_reveal_noalloc(x, data, y, size, 100, status)
+        assert e.value.code == D.EINVAL
+    import torch
+    with pytest.raises(D.DttError) as e:        # not int32
+        D.dtt_barrier_reveal_noalloc(ok, ok, [torch.zeros(size, dtype=torch.int16)] * P, size, 100, _i32(P))
+    assert e.value.code == D.EINVAL
+
+
+def test_barrier_reveal_method_refuses_short_lists():
+    b = D.Barrier.__new__(D.Barrier)      # the argument check runs before the library is called
+    b._h, b.P = C.c_void_p(0), 4
+    ok = [_i32(8) for _ in range(4)]
+    with pytest.raises(D.DttError) as e:
+        b.reveal(ok, ok[:3], ok, 8, 100, _i32(4))
+    assert e.value.code == D.EINVAL
+
+
+def test_handrolled_wrapper_refuses_short_windows():
+    P = 4
+    ok = [_i32(P) for _ in range(P)]
+    for signal, y, status in [(ok, ok[:3], _i32(P)), (ok[:3] + [_i32(P - 1)], ok, _i32(P)),
+                              (ok, ok, _i32(P - 1))]:
+        with pytest.raises(D.DttError) as e:
+            D.dtt_barrier_handrolled(signal, y, 1, 100, status)
+        assert e.value.code == D.EINVAL
+
+
+def test_library_grouped_order_short_last_group_golden():
+    # the order the library's producers run (dtt_tile_of) against the hand-worked tables
+    path = os.path.join(ROOT, "tests", "golden", "grouped_order.txt")
+    for line in open(path):
+        if not line.strip() or line.startswith("#"):
+            continue
+        row = line.split()
+        i = row.index(":")
+        tiles_m, tiles_n, gm = (int(x) for x in row[:i])
+        steps = [tuple(int(v) for v in t.split(",")) for t in row[i + 1:]]
+        got = [D.dtt_tile_of(D.ORDER_GROUPED, gm, s, tiles_m, tiles_n) for s in range(len(steps))]
+        assert got == steps

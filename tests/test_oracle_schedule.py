@@ -169,3 +169,22 @@ def test_validation_rejects_misuse():
     c = S.Schedule([S.Chunk([(3, 4, 3, 8)], 1)])
     with pytest.raises(S.PlanError):
         S.validate([a, c], 24, allgather=False)
+
+
+def _grouped_golden():
+    out = []
+    for row in _golden("grouped_order.txt"):
+        i = row.index(":")
+        tm_, tn_, gm = (int(x) for x in row[:i])
+        steps = [tuple(int(v) for v in t.split(",")) for t in row[i + 1:]]
+        out.append((tm_, tn_, gm, steps))
+    return out
+
+
+def test_grouped_order_short_last_group_golden():
+    # hand-worked tables (tests/golden/grouped_order.txt): the last group of tile rows is short
+    g = _grouped_golden()
+    assert len(g) >= 2
+    for tiles_m, tiles_n, gm, steps in g:
+        assert len(steps) == tiles_m * tiles_n
+        assert [S.order_grouped(s, tiles_m, tiles_n, gm) for s in range(len(steps))] == steps

@@ -61,6 +61,25 @@ __global__ void user_producer_paced(dtt_handle h, uint8_t* slice, uint64_t chunk
     dtt_mark_ready(h, h.first_chunk + c);
 }
 
+// Out-of-order completion ("Triggered Plans", The kernel author's contract, item 1): one CTA
+// writes the rank's chunks last to first, marking each after its stores, so chunk 0 -- the
+// head of every copier queue of this rank -- opens last.  `spin_ns` of busy time after each mark
+// leaves the later chunks open for a while before the head opens.
+__global__ void user_producer_reverse(dtt_handle h, uint8_t* slice, uint64_t chunk_bytes, uint64_t spin_ns) {
+    for (uint32_t k = h.n_chunks; k-- > 0;) {
+        const uint64_t base = (uint64_t)k * chunk_bytes;
+        for (uint64_t i = threadIdx.x; i < chunk_bytes; i += blockDim.x)
+            slice[base + i] = value_at(h.rank, h.round, base + i);
+        dtt_mark_ready(h, h.first_chunk + k);
+        if (threadIdx.x == 0 && spin_ns) {
+            uint64_t t0, t;
+            asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+            do { asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t)); } while (t - t0 < spin_ns);
+        }
+        __syncthreads();
+    }
+}
+
 // CTA i asks dtt_reusable of global chunk first + i.
 __global__ void user_probe_reusable(dtt_handle h, uint32_t first, int32_t* out) {
     const bool r = dtt_reusable(h, first + blockIdx.x);
@@ -79,6 +98,10 @@ extern "C" int user_kernels_prepare(void) {
                              cudaSharedmemCarveoutMaxShared) != cudaSuccess)
         return 1;
     if (cudaFuncSetAttribute(user_consumer, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared) != cudaSuccess)
+        return 1;
+    if (cudaFuncGetAttributes(&a, user_producer_reverse) != cudaSuccess) return 1;
+    if (cudaFuncSetAttribute(user_producer_reverse, cudaFuncAttributePreferredSharedMemoryCarveout,
                              cudaSharedmemCarveoutMaxShared) != cudaSuccess)
         return 1;
     if (cudaFuncGetAttributes(&a, user_producer_paced) != cudaSuccess) return 1;
@@ -113,5 +136,12 @@ extern "C" int user_produce_paced(const dtt_handle* h, void* slice, uint64_t chu
 extern "C" int user_probe(const dtt_handle* h, uint32_t first, uint32_t n, int32_t* out, cudaStream_t s) {
     if (n == 0) return 0;
     user_probe_reusable<<<n, 64, 0, s>>>(*h, first, out);
+    return cudaGetLastError() == cudaSuccess ? 0 : 1;
+}
+
+extern "C" int user_produce_reverse(const dtt_handle* h, void* slice, uint64_t chunk_bytes, uint64_t spin_ns,
+                                    cudaStream_t s) {
+    if (h->n_chunks == 0) return 0;
+    user_producer_reverse<<<1, 256, 0, s>>>(*h, static_cast<uint8_t*>(slice), chunk_bytes, spin_ns);
     return cudaGetLastError() == cudaSuccess ? 0 : 1;
 }
