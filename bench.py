@@ -322,18 +322,15 @@ def run_reference(args):
     return 0
 
 
-def run_ours(args):
+def measure_workload(w, args, K, warmup, latency_rounds, isolated_rounds, with_e2e, world=1,
+                     clocks_dev=None, early_us=None):
+    """Time K rounds of workload w in the launch the benchmark uses for it (runner.bench_launch),
+    then the kernel-timing pass, the gate timestamps, the isolated kernels and (optionally) the
+    host-buffer round.  Returns a dict of raw measurements (seconds, milliseconds, bytes)."""
     import torch
-    world, rank, local = dist_env()
-    if world > 1:
-        import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl")
-    dev = torch.cuda.current_device()
     import device_triggered_transfers_gb300 as D
     from device_triggered_transfers_gb300 import runner
 
-    w = workload(args)
     launch = dict(runner.bench_launch(w))
     # the copier runs on a stream the bench can put events on
     copy_stream = torch.cuda.Stream(priority=-1)
@@ -343,6 +340,8 @@ def run_ours(args):
     opts = launch.pop("opts", None) or D.dtt_plan_opts_default()
     if args.deferred:
         opts.deferred_copier = 1
+    if early_us is not None:
+        opts.early_copier_us = early_us
     opts.time_copier = 0
     copier_method = {"method": opts.method, "piece_bytes": opts.piece_bytes, "stages": opts.stages,
                      "copier_threads": opts.copier_threads, "ctas_per_sm": opts.ctas_per_sm}
@@ -395,6 +394,7 @@ def run_ours(args):
         for i in range(K):
             step(evs[i])
         e1.record(prod)
+        e1.synchronize()
         torch.cuda.synchronize()
         c1 = plan.stats()
         cop = (c1[1] - c0[1]) / max(1, c1[2] - c0[2])
@@ -402,9 +402,11 @@ def run_ours(args):
         return e0.elapsed_time(e1) / 1e3, cop, prod_ms
 
     step = make_step(st.plan, opts.deferred_copier == 1)
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         step()
     torch.cuda.synchronize()
+    out = {"w": w, "launch": launch, "copier_method": copier_method, "gemm": gemm,
+           "deferred_copier": opts.deferred_copier, "early_copier_us": opts.early_copier_us}
     if args.profile_rounds:
         # whole rounds (producer, copier and check together) inside one profiler range, for a
         # range-replay capture of their DRAM traffic; no timing
@@ -413,25 +415,24 @@ def run_ours(args):
             step()
         torch.cuda.synchronize()
         torch.cuda.profiler.stop()
-        if rank == 0:
-            print(json.dumps({"profile_rounds": args.profile_rounds, "workload": w.name,
-                              "algorithmic_bytes_per_round": w.algorithmic_bytes_per_round(),
-                              "producer_bytes_per_round": len(w.senders()) * w.slice_bytes}))
-        return 0
-    K = args.steps
+        st.plan.close()
+        out["profiled"] = True
+        return out
     barrier(world)
     torch.cuda.synchronize()
-    # the GEMM is the dominant kernel of its workload: time its launches inside the timed region
-    with ClockSampler(dev) as clocks:
-        time.sleep(0.25)
+    e_before = st.plan.early_stats()
+    if clocks_dev is not None:
+        with ClockSampler(clocks_dev) as clocks:
+            time.sleep(0.25)
+            elapsed, _, _ = timed(st.plan, step, K, producer_events=False)
+            time.sleep(0.25)
+        out["clocks"] = clocks.summary()
+    else:
         elapsed, _, _ = timed(st.plan, step, K, producer_events=False)
-        time.sleep(0.25)
+    e_after = st.plan.early_stats()
+    out["early"] = {k: e_after[k] - e_before[k] for k in e_after}
     barrier(world)
-    D_round = w.delivered_bytes_per_round()
-    B_alg = w.algorithmic_bytes_per_round()
-    t_max, units = aggregate(elapsed, D_round * K, world)
-    value = units / t_max / 1e9
-    peak, peak_kind = load_peaks()
+    out["elapsed_s"] = elapsed
 
     def side_plan(**over):
         """A second plan over the same buffers with the same copier launch."""
@@ -445,7 +446,8 @@ def run_ours(args):
         return plan
 
     # kernel-timing pass: K more rounds of the same step, CUDA events around every copier launch
-    # (in the library, on the copy stream) and, for the GEMM, around every producer launch
+    # (in the library, on the copy stream) and, for the GEMM, around every producer launch.  A
+    # timed plan launches its copier at plan_start, so each copier launch is one round's.
     plan3 = side_plan(time_copier=1, deferred_copier=opts.deferred_copier)
     step3 = make_step(plan3, opts.deferred_copier == 1)
     for _ in range(3):
@@ -453,14 +455,13 @@ def run_ours(args):
     torch.cuda.synchronize()
     t3, copier_ms, producer_ms = timed(plan3, step3, K, producer_events=gemm)
     plan3.close()
-    cop_s = copier_ms / 1e3
-    achieved = B_alg / cop_s / 1e9
+    out.update(timing_pass_s=t3, copier_ms=copier_ms, producer_ms=producer_ms)
 
     # gate-to-arrival latency and the copier window, from the gate timestamps of extra rounds
     lat, windows = [], []
     _, _, n_chunks_all, _ = st.plan.info()
-    n_chunks_total = sum(n_chunks_all[r] for r in w.senders())
-    for _ in range(args.latency_rounds):
+    out["n_chunks_total"] = sum(n_chunks_all[r] for r in w.senders())
+    for _ in range(latency_rounds):
         step()
         g = st.plan.read_gates()
         n_global, first, n_chunks, _ = st.plan.info()
@@ -475,11 +476,12 @@ def run_ours(args):
                         lat.append(ta - to)
                         t_arr_max = max(t_arr_max, ta)
         windows.append((t_arr_max - t_open_min) / 1e9)
+    out.update(lat=lat, windows=windows)
 
     # e2e: the host-buffer round through the public API: H2D of every rank's slice from pinned
     # memory, the triggered fan-out, D2H of rank 0's gathered buffer
-    e2e = None
-    if not args.no_e2e and not w.broadcast and not gemm:
+    out["e2e"] = None
+    if with_e2e and not w.broadcast and not gemm:
         S = w.slice_bytes
         host_in = [torch.empty(S, dtype=torch.uint8).pin_memory() for _ in range(w.P)]
         for r in range(w.P):
@@ -495,27 +497,159 @@ def run_ours(args):
             st.plan.allgather_host(host_in, host_out, 0, prod)
         x1.record(prod)
         torch.cuda.synchronize()
-        e2e_t, e2e_units = aggregate(x0.elapsed_time(x1) / 1e3, D_round * e2e_steps, world)
-        e2e = {"value": e2e_units / e2e_t / 1e9, "unit": "GB/s", "h2d_bytes_per_step": S * w.P,
-               "d2h_bytes_per_step": w.buf_bytes}
+        out["e2e"] = {"elapsed_s": x0.elapsed_time(x1) / 1e3, "steps": e2e_steps,
+                      "h2d_bytes_per_step": S * w.P, "d2h_bytes_per_step": w.buf_bytes}
     st.plan.close()
 
     # the same copier and producer one after the other (deferred plan): each kernel alone
-    iso = None
-    if not args.deferred and args.isolated_rounds:
+    out["isolated"] = None
+    if not args.deferred and isolated_rounds:
         plan2 = side_plan(time_copier=1, deferred_copier=1)
         step2 = make_step(plan2, True)
         for _ in range(3):
             step2()
-        _, c2, f2 = timed(plan2, step2, args.isolated_rounds, producer_events=True)
+        _, c2, f2 = timed(plan2, step2, isolated_rounds, producer_events=True)
         plan2.close()
+        out["isolated"] = {"copier_ms": c2, "producer_ms": f2}
+    out["num_programs"] = getattr(st, "num_programs", None)
+    del st
+    torch.cuda.empty_cache()
+    return out
+
+
+def summarize(m, K, t_max, units, peak, peak_kind):
+    """The JSON fields of one measured workload (see measure_workload)."""
+    import device_triggered_transfers_gb300 as D
+    w = m["w"]
+    D_round = w.delivered_bytes_per_round()
+    B_alg = w.algorithmic_bytes_per_round()
+    copier_method = m["copier_method"]
+    cop_s = m["copier_ms"] / 1e3
+    achieved = B_alg / cop_s / 1e9
+    kname = "copier_bulk_kernel" if copier_method["method"] == D.COPY_TMA else "copier_kernel"
+    copier_roof = {"kernel": kname, "bound": "hbm", "achieved": achieved,
+                   "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
+                   "traffic": NCU_TRAFFIC.get((w.name, kname)), "algorithmic_bytes_per_launch": B_alg,
+                   "round_dram_read_write": ROUND_TRAFFIC.get(w.name)}
+    if m["gemm"]:       # the dominant kernel is the tensor-core producer
+        flops = 2.0 * w.P * w.M * w.N * w.K
+        tf_peak, tf_kind = load_tensor_peak()
+        prod_s = m["producer_ms"] / 1e3
+        NP = m["num_programs"] or w.num_programs
+        gname = "gemm2_producer_kernel" if (w.M % 256 == 0 and w.N % 256 == 0 and NP >= 2) \
+            else "gemm_producer_kernel"
+        roofline = {"kernel": gname, "bound": "tensor",
+                    "achieved": flops / prod_s / 1e12, "peak": tf_peak, "peak_kind": tf_kind,
+                    "unit": "TFLOP/s", "frac": flops / prod_s / 1e12 / tf_peak,
+                    "traffic": NCU_TRAFFIC.get((w.name, gname)),
+                    "flops_per_launch": flops}
+    else:
+        roofline = copier_roof
+    lat_sorted = sorted(m["lat"]) or [0]
+    lat_med = lat_sorted[len(lat_sorted) // 2]
+    lat_p99 = lat_sorted[min(len(lat_sorted) - 1, int(len(lat_sorted) * 0.99))]
+    # the ideal time of one chunk's fan-out at the measured copy peak: one read of the chunk and
+    # P-1 writes of it, (S_c + (P-1) S_c) / peak
+    chunk_mean = len(w.senders()) * w.slice_bytes / max(1, m["n_chunks_total"])
+    ideal_ns = w.P * chunk_mean / (peak * 1e9) * 1e9
+    iso = None
+    if m["isolated"]:
+        c2, f2 = m["isolated"]["copier_ms"], m["isolated"]["producer_ms"]
         iso = {"copier_ms": c2, "producer_ms": f2,
                "copier_gbs_algorithmic": B_alg / (c2 / 1e3) / 1e9,
                "copier_frac_of_measured": B_alg / (c2 / 1e3) / 1e9 / peak,
                "overlap_ratio": (t_max / K) / (max(c2, f2) / 1e3)}
+    windows = m["windows"]
+    e2e = None
+    if m["e2e"]:
+        e2e = {"value": D_round * m["e2e"]["steps"] / m["e2e"]["elapsed_s"] / 1e9, "unit": "GB/s",
+               "h2d_bytes_per_step": m["e2e"]["h2d_bytes_per_step"],
+               "d2h_bytes_per_step": m["e2e"]["d2h_bytes_per_step"]}
+    return {
+        "ms_per_round": t_max / K * 1e3,
+        "gbs_delivered": units / t_max / 1e9,
+        "hbm_frac_end_to_end": {"of_measured": B_alg * units / D_round / t_max / 1e9 / peak,
+                                "of_spec_8000": B_alg * units / D_round / t_max / 1e9 / 8000.0},
+        "roofline": roofline,
+        "copier_roofline": copier_roof if m["gemm"] else None,
+        "kernels_ms": {"copier_mean": m["copier_ms"], "producer_mean": m["producer_ms"],
+                       "timing_pass_ms_per_step": m["timing_pass_s"] / K * 1e3},
+        "isolated": iso,
+        "copier_window": ({"gbs_delivered": D_round / statistics.median(windows) / 1e9,
+                           "hbm_frac": B_alg / statistics.median(windows) / 1e9 / peak}
+                          if windows else None),
+        "gate_to_arrival_ns": {"median": lat_med, "p99": lat_p99, "samples": len(m["lat"]),
+                               "chunk_bytes_mean": chunk_mean,
+                               "ideal_chunk_ns": ideal_ns,
+                               "median_over_ideal": lat_med / ideal_ns if ideal_ns else None,
+                               "p99_over_ideal": lat_p99 / ideal_ns if ideal_ns else None},
+        "early_copier": {"wait_us": m["early_copier_us"], **(m.get("early") or {})},
+        "e2e": e2e,
+    }
+
+
+# workloads measured beside the headline in the default run, with the steps each is timed over
+PER_CONFIG_STEPS = {"c1_whole_p2": 200, "c3_tiles_p8": 30, "c4a_writers8_p8": 100,
+                    "c4b_bcast_p8": 5, "c5_gemm_p4": 50}
+
+
+def run_ours(args):
+    import torch
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.cuda.current_device()
+    import device_triggered_transfers_gb300 as D  # noqa: F401
+
+    w = workload(args)
+    K = args.steps
+    early = None if args.early_us < 0 else args.early_us
+    m = measure_workload(w, args, K, args.warmup, args.latency_rounds, args.isolated_rounds,
+                         with_e2e=not args.no_e2e, world=world, clocks_dev=dev, early_us=early)
+    if m.get("profiled"):
+        if rank == 0:
+            print(json.dumps({"profile_rounds": args.profile_rounds, "workload": w.name,
+                              "algorithmic_bytes_per_round": w.algorithmic_bytes_per_round(),
+                              "producer_bytes_per_round": len(w.senders()) * w.slice_bytes}))
+        return 0
+    D_round = w.delivered_bytes_per_round()
+    t_max, units = aggregate(m["elapsed_s"], D_round * K, world)
+    if m["e2e"]:
+        e_t, e_units = aggregate(m["e2e"]["elapsed_s"], D_round * m["e2e"]["steps"], world)
+        m["e2e"]["elapsed_s"], m["e2e"]["steps"] = e_t, e_units / D_round
+    value = units / t_max / 1e9
+    peak, peak_kind = load_peaks()
+    s = summarize(m, K, t_max, units, peak, peak_kind)
+
+    # the other workloads, each timed the same way over fewer steps (single GPU only)
+    per_config = None
+    if world == 1 and args.per_config and not args.rows:
+        per_config = {}
+        for name, steps in PER_CONFIG_STEPS.items():
+            if name == w.name:
+                continue
+            wc = W.CONFIGS[name]
+            mc = measure_workload(wc, args, steps, 3, 5, 5, with_e2e=False, early_us=early)
+            Dc = wc.delivered_bytes_per_round()
+            sc = summarize(mc, steps, mc["elapsed_s"], Dc * steps, peak, peak_kind)
+            per_config[name] = {
+                "steps": steps, "ms_per_round": sc["ms_per_round"], "gbs_delivered": sc["gbs_delivered"],
+                "dominant_kernel": {k: sc["roofline"][k] for k in ("kernel", "bound", "achieved", "unit", "frac")},
+                "copier_frac_in_round": (sc["copier_roofline"] or sc["roofline"])["frac"],
+                "hbm_frac_end_to_end": sc["hbm_frac_end_to_end"]["of_measured"],
+                "copier_window_hbm_frac": (sc["copier_window"] or {}).get("hbm_frac"),
+                "isolated": sc["isolated"],
+                "gate_to_arrival_ns": {k: sc["gate_to_arrival_ns"][k] for k in
+                                       ("median", "p99", "median_over_ideal", "p99_over_ideal")},
+                "early_copier": sc["early_copier"],
+                "workload": describe(wc, mc["launch"], mc["copier_method"]),
+                "l2": l2_note(wc, dev)}
 
     if rank != 0:
         return 0
+    gemm = m["gemm"]
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
         if gemm:
@@ -530,62 +664,34 @@ def run_ours(args):
             vt, nt, dtt, what_t, threads = time_oracle_threaded(w, budget_s=args.cpu_seconds / 2)
             cpu["threaded"] = {"value": vt, "threads": threads, "host_cores": os.cpu_count(),
                                "sample": f"{what_t}; {nt} threaded oracle round(s) in {dtt:.1f} s"}
-    lat_sorted = sorted(lat) or [0]
-    lat_med = lat_sorted[len(lat_sorted) // 2]
-    lat_p99 = lat_sorted[min(len(lat_sorted) - 1, int(len(lat_sorted) * 0.99))]
-    # the ideal time of one chunk's fan-out at the measured copy peak: one read of the chunk and
-    # P-1 writes of it, (S_c + (P-1) S_c) / peak
-    chunk_mean = len(w.senders()) * w.slice_bytes / max(1, n_chunks_total)
-    ideal_ns = w.P * chunk_mean / (peak * 1e9) * 1e9
     mode = {0: "copier launched at plan_start, overlapping the producer",
             1: "copier launched after the producer (no overlap)",
-            2: "copier launched right after the producer's launch, overlapping it"}[opts.deferred_copier]
-    kname = "copier_bulk_kernel" if copier_method["method"] == D.COPY_TMA else "copier_kernel"
-    copier_roof = {"kernel": kname, "bound": "hbm", "achieved": achieved,
-                   "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
-                   "traffic": NCU_TRAFFIC.get((w.name, kname)), "algorithmic_bytes_per_launch": B_alg,
-                   "round_dram_read_write": ROUND_TRAFFIC.get(w.name)}
-    if gemm:       # the dominant kernel is the tensor-core producer
-        flops = 2.0 * w.P * w.M * w.N * w.K
-        tf_peak, tf_kind = load_tensor_peak()
-        prod_s = producer_ms / 1e3
-        gname = "gemm2_producer_kernel" if (w.M % 256 == 0 and w.N % 256 == 0 and st.num_programs >= 2) \
-            else "gemm_producer_kernel"
-        roofline = {"kernel": gname, "bound": "tensor",
-                    "achieved": flops / prod_s / 1e12, "peak": tf_peak, "peak_kind": tf_kind,
-                    "unit": "TFLOP/s", "frac": flops / prod_s / 1e12 / tf_peak,
-                    "traffic": NCU_TRAFFIC.get((w.name, gname)),
-                    "flops_per_launch": flops}
-    else:
-        roofline = copier_roof
+            2: "copier launched right after the producer's launch, overlapping it"}[m["deferred_copier"]]
+    if m["early_copier_us"] and m["deferred_copier"] != 1:
+        mode += ("; each round's copier launched early, by the previous round's plan_wait, and "
+                 "claimed by plan_start (waits up to %d us for it)" % m["early_copier_us"])
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": t_max / K * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
-        "config": {"workload": describe(w, launch, copier_method), "parallelism": f"replicas{world}",
+        "config": {"workload": describe(w, m["launch"], m["copier_method"]), "parallelism": f"replicas{world}",
                    "l2": l2_note(w, dev),
                    "step": "plan_start + %s producer + copier + plan_wait + next_round"
                            % ("GEMM" if gemm else "fill"),
                    "mode": mode},
-        "hbm_frac_end_to_end": {"of_measured": B_alg * units / D_round / t_max / 1e9 / peak,
-                                "of_spec_8000": B_alg * units / D_round / t_max / 1e9 / 8000.0},
-        "roofline": roofline,
-        "copier_roofline": copier_roof if gemm else None,
-        "kernels_ms": {"copier_mean": copier_ms, "producer_mean": producer_ms,
-                       "timing_pass_ms_per_step": t3 / K * 1e3},
-        "isolated": iso,
-        "copier_window": ({"gbs_delivered": D_round / statistics.median(windows) / 1e9,
-                           "hbm_frac": B_alg / statistics.median(windows) / 1e9 / peak}
-                          if windows else None),
-        "gate_to_arrival_ns": {"median": lat_med, "p99": lat_p99, "samples": len(lat),
-                               "chunk_bytes_mean": chunk_mean,
-                               "ideal_chunk_ns": ideal_ns,
-                               "median_over_ideal": lat_med / ideal_ns if ideal_ns else None,
-                               "p99_over_ideal": lat_p99 / ideal_ns if ideal_ns else None},
-        "e2e": e2e,
+        "hbm_frac_end_to_end": s["hbm_frac_end_to_end"],
+        "roofline": s["roofline"],
+        "copier_roofline": s["copier_roofline"],
+        "kernels_ms": s["kernels_ms"],
+        "isolated": s["isolated"],
+        "copier_window": s["copier_window"],
+        "gate_to_arrival_ns": s["gate_to_arrival_ns"],
+        "early_copier": s["early_copier"],
+        "e2e": s["e2e"],
         "gpu_launches": 3 * K,
-        "clocks": clocks.summary(),
+        "clocks": m.get("clocks"),
         "cpu_baseline": cpu,
+        "per_config": per_config,
     }
     print(json.dumps(line))
     return 0
@@ -812,6 +918,12 @@ def main(argv=None):
     ap.add_argument("--profile-rounds", type=int, default=0,
                     help="run this many rounds after the warm-up inside a profiler range "
                          "(cudaProfilerStart/Stop) and exit, for ncu --replay-mode app-range")
+    ap.add_argument("--early-us", type=int, default=-1,
+                    help="opts.early_copier_us for the timed plans (-1: the launch's own setting, "
+                         "0: off)")
+    ap.add_argument("--no-per-config", dest="per_config", action="store_false",
+                    help="time only the named workload (default: also the other workloads, "
+                         "reported under per_config)")
     ap.add_argument("--rows", type=int, default=0,
                     help="rows per rank instead of the workload's (a smaller case of the same "
                          "shape, for profiler captures; the default runs the workload as named)")

@@ -54,7 +54,8 @@ class dtt_plan_opts(C.Structure):
                 ("piece_bytes", C.c_uint32), ("timestamps", C.c_uint32),
                 ("initial_round", C.c_uint32), ("max_polls", C.c_uint64),
                 ("max_regions", C.c_uint64), ("deferred_copier", C.c_uint32),
-                ("stages", C.c_uint32), ("time_copier", C.c_uint32), ("host_piece_bytes", C.c_uint32)]
+                ("stages", C.c_uint32), ("time_copier", C.c_uint32), ("host_piece_bytes", C.c_uint32),
+                ("early_copier_us", C.c_uint32)]
 
 
 class dtt_handle(C.Structure):
@@ -118,6 +119,8 @@ _SIGS = {
     "dtt_plan_next_round": (C.c_int, [_P]),
     "dtt_plan_close": (C.c_int, [_P]),
     "dtt_plan_state": (C.c_int, [_P]),
+    "dtt_plan_early_stats": (C.c_int, [_P, C.POINTER(_u64), C.POINTER(_u64), C.POINTER(_u64),
+                                       C.POINTER(_u64)]),
     "dtt_plan_round": (C.c_uint32, [_P]),
     "dtt_plan_info": (C.c_int, [_P, C.POINTER(_u32), C.POINTER(_u32), C.POINTER(_u32), C.POINTER(_P)]),
     "dtt_plan_read_gates": (C.c_int, [_P, C.POINTER(_u64), _u64]),
@@ -395,6 +398,12 @@ class Plan:
         last, total, n = C.c_double(), C.c_double(), _u64()
         _check(lib().dtt_plan_stats(self._h, C.byref(last), C.byref(total), C.byref(n)))
         return last.value, total.value, n.value
+
+    def early_stats(self) -> dict:
+        """Early copiers so far (opts.early_copier_us): launched, claimed, expired, aborted."""
+        v = [_u64() for _ in range(4)]
+        _check(lib().dtt_plan_early_stats(self._h, *[C.byref(x) for x in v]))
+        return dict(zip(("launched", "claimed", "expired", "aborted"), (x.value for x in v)))
 
     def read_gates(self) -> np.ndarray:
         """The P gate tables as a uint64 array [P, n_global, 8]."""

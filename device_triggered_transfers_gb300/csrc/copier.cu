@@ -170,7 +170,82 @@ __device__ __forceinline__ void count_out(const CopierParams& p) {
     asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(&p.status->copier_exit) : "memory");
 }
 
+// ---- early launch --------------------------------------------------------------------------------
+// A copier that dtt_plan_wait launched for the next round before the host started that round
+// (opts.early_copier_us; it queues behind this round's copier on the copy stream, so its launch
+// costs the next round nothing -- the pages' "prepare" step arms the copy engine's queue ahead of
+// the round in the same way).  CTA 0's thread 0 waits until plan_start claims the round on the
+// mapped handshake word, or gives the round up after go_wait_ns with a compare-and-swap of its
+// own -- exactly one side wins -- and publishes the decision for the other CTAs.  A copier whose
+// round was given up (or aborted by the host) exits without touching a gate or a status word,
+// not even the count-out, and plan_start launches a fresh one.
+
+__device__ __forceinline__ uint64_t ld_acquire_sys(const uint64_t* p) {
+    uint64_t v;
+    asm volatile("ld.acquire.sys.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ uint64_t cas_sys(uint64_t* p, uint64_t cmp, uint64_t val) {
+    uint64_t old;
+    asm volatile("atom.acq_rel.sys.global.cas.b64 %0, [%1], %2, %3;"
+                 : "=l"(old) : "l"(p), "l"(cmp), "l"(val) : "memory");
+    return old;
+}
+
+// Thread 0 of CTA 0: has the host started this copier's round?  Bounded by go_wait_ns.
+__device__ __forceinline__ bool early_decide(const CopierParams& p) {
+    const uint64_t start = early_start_value(p.round), stop = early_stop_value(p.round);
+    const uint64_t t0 = dtt_dev::globaltimer();
+    bool go = false;
+    for (;;) {
+        const uint64_t v = ld_acquire_sys(p.go_host);
+        if (v == start) { go = true; break; }
+        if (v != p.go_prior) break;                          // the host aborted the round
+        if (dtt_dev::globaltimer() - t0 >= p.go_wait_ns) {
+            go = cas_sys(p.go_host, p.go_prior, stop) == start;   // the host may have just claimed it
+            break;
+        }
+        __nanosleep(256);
+    }
+    dtt_dev::st_release(&p.status->early_go, go ? start : stop);
+    return go;
+}
+
+// Thread 0 of every other CTA: CTA 0's decision, 1 go / 0 given up, or -1 when it did not come
+// within twice CTA 0's bound plus a millisecond (CTA 0's own wait is bounded, so this is a
+// safety net that ends the CTA as a copier timeout).
+__device__ __forceinline__ int early_follow(const CopierParams& p) {
+    const uint64_t start = early_start_value(p.round);
+    const uint64_t t0 = dtt_dev::globaltimer(), limit = 2 * p.go_wait_ns + 1000000;
+    uint32_t ns = 0;
+    for (;;) {
+        const uint64_t v = dtt_dev::ld_acquire(&p.status->early_go);
+        if (v >= start) return v == start ? 1 : 0;
+        if (dtt_dev::globaltimer() - t0 >= limit) return -1;
+        __nanosleep(ns);
+        ns = ns < 256 ? ns + 32 : 256;
+    }
+}
+
+// Thread 0: the early handshake of this CTA (1 go, 0 exit silently, -1 exit as a timeout).
+__device__ __forceinline__ int early_gate(const CopierParams& p) {
+    const int e = blockIdx.x == 0 ? (early_decide(p) ? 1 : 0) : early_follow(p);
+    if (e < 0) atomicAdd(&p.status->copier_timeouts, 1u);
+    return e;
+}
+
 __global__ void __launch_bounds__(1024) copier_kernel(const __grid_constant__ CopierParams p) {
+    if (p.go_host) {
+        __shared__ int s_early;
+        if (threadIdx.x == 0) s_early = early_gate(p);
+        __syncthreads();
+        const int e = s_early;
+        if (e <= 0) {
+            if (e < 0 && threadIdx.x == 0) count_out(p);
+            return;
+        }
+    }
     copier_body(p);
     __syncthreads();
     if (threadIdx.x == 0) count_out(p);
@@ -365,6 +440,13 @@ __device__ __forceinline__ void copier_bulk_body(const CopierParams& p) {
 
 __global__ void __launch_bounds__(32) copier_bulk_kernel(const __grid_constant__ CopierParams p) {
     if (threadIdx.x != 0) return;       // one thread drives the CTA's bulk copies
+    if (p.go_host) {
+        const int e = early_gate(p);
+        if (e <= 0) {
+            if (e < 0) count_out(p);
+            return;
+        }
+    }
     copier_bulk_body(p);
     count_out(p);
 }

@@ -81,7 +81,15 @@ struct DevStatus {
     uint32_t copier_exit;       // copier CTAs of this round that have finished
     uint32_t check_late;        // 1: the check gave up waiting for the copier
     uint32_t pad;
+    // An early copier's decision for its round R, published by its CTA 0 for the other CTAs:
+    // 2R (the host started round R: copy) or 2R + 1 (it expired or was aborted: exit).  Grows
+    // with the rounds and is never reset.
+    uint64_t early_go;
 };
+
+// Values of the early-copier handshake word for round R (HostStatus::go, DevStatus::early_go).
+inline __host__ __device__ uint64_t early_start_value(uint32_t round) { return 2ull * round; }
+inline __host__ __device__ uint64_t early_stop_value(uint32_t round) { return 2ull * round + 1; }
 
 // A round's outcome in pinned, device-mapped host memory, written by check_kernel itself so that
 // wait() needs no device-to-host copy: the status words, then `done` (the sequence number of
@@ -90,7 +98,14 @@ struct DevStatus {
 struct HostStatus {
     DevStatus st;
     uint32_t done;
-    uint32_t pad[7];
+    uint32_t pad;
+    // Early-copier handshake (opts.early_copier_us): a copier launched before its round waits
+    // until plan_start moves this word from the value it held at the launch (`go_prior`) to
+    // early_start_value(round); if that does not happen in time, the copier moves it to
+    // early_stop_value(round) itself and exits.  Both sides use a compare-and-swap at system
+    // scope, so exactly one of them decides.  The host also stores the stop value to abort.
+    uint64_t go;
+    uint64_t pad2[2];
 };
 
 struct CopierParams {
@@ -111,6 +126,12 @@ struct CopierParams {
     uint32_t stage_bytes;       // bulk-copy path: bytes per shared-memory stage (>= a piece, 128-aligned)
     uint32_t stages;            // bulk-copy path: stages in the ring
     uint32_t* host_arrived;     // or null: mapped host words, word c = round once chunk c reached every peer
+    // Early launch (null for a launch at plan_start): the device address of HostStatus::go, the
+    // value it held when this copier was launched, and how long CTA 0 waits for the host's
+    // start of the round (globaltimer ns) before it gives the round up.
+    uint64_t* go_host;
+    uint64_t go_prior;
+    uint64_t go_wait_ns;
 };
 
 struct CheckParams {

@@ -82,6 +82,16 @@ struct dtt_plan {
     uint32_t round = 1;
     bool copier_launched = false;   // this round's copier is on the copy stream
 
+    // opts.early_copier_us: wait() launches the next round's copier behind this round's, and
+    // start() claims it through HostStatus::go (see CopierParams::go_host).
+    bool host_atomics = false;      // the device and the host can share atomics on mapped memory
+    bool early_pending = false;     // an early copier for round early_round awaits its claim
+    bool early_launched = false;    // an early copier was ever launched (close drains the copy stream)
+    bool suppress_early = false;    // inside dtt_allgather_host: its rounds stamp arrivals for the host
+    uint32_t early_round = 0;
+    uint64_t go_shadow = 0;         // the value HostStatus::go holds (the host sees every change)
+    uint64_t early_launches = 0, early_claims = 0, early_expired = 0, early_aborts = 0;
+
     // Plans sharing a copy stream ("Triggered Plans", The kernel author's contract: CLOSING):
     // the order of this plan's last copier launch among all plans, and an event after that
     // copier, recorded when another plan uses the same stream.
@@ -262,7 +272,8 @@ std::vector<dtt_plan*> g_retired;
 uint64_t g_launch_seq = 0;
 
 bool may_spin(const dtt_plan* q) {
-    return (q->state == DTT_PLAN_RUNNING || q->state == DTT_PLAN_CLOSING) && q->copier_launched;
+    return ((q->state == DTT_PLAN_RUNNING || q->state == DTT_PLAN_CLOSING) && q->copier_launched) ||
+           q->early_pending;
 }
 
 // Is p's copier queued behind an earlier plan's copier on the same stream that has not finished?
@@ -362,6 +373,77 @@ CopierParams copier_params(const dtt_plan* p) {
     cp.host_arrived = p->notify_host ? p->h_arrived_dev : nullptr;
     cp.stages = p->opts.stages;
     return cp;
+}
+
+// ---- the early copier (opts.early_copier_us) ------------------------------------------------
+// Does another live plan use p's copy stream?  A copier launched early would hold that stream
+// until p's next start, so shared streams launch at start as before.
+bool stream_shared(const dtt_plan* p) {
+    std::lock_guard<std::mutex> lock(g_plans_mu);
+    for (const dtt_plan* q : g_live)
+        if (q != p && q->copy_stream == p->copy_stream) return true;
+    return false;
+}
+
+bool early_allowed(const dtt_plan* p) {
+    return p->opts.early_copier_us && p->host_atomics && p->n_global && !p->opts.time_copier &&
+           p->opts.deferred_copier != 1 && !p->suppress_early && p->round < 0xFFFFFFFFu &&
+           !stream_shared(p);
+}
+
+uint64_t* go_word(dtt_plan* p) { return &p->h_status->go; }
+
+bool cas_go(dtt_plan* p, uint64_t* expected, uint64_t desired) {
+    return __atomic_compare_exchange_n(go_word(p), expected, desired, false, __ATOMIC_ACQ_REL,
+                                       __ATOMIC_ACQUIRE);
+}
+
+// Launch round p->round + 1's copier now, on the copy stream behind this round's.
+int launch_early(dtt_plan* p) {
+    CopierParams cp = copier_params(p);
+    cp.round = p->round + 1;
+    cp.go_host = &p->h_status_dev->go;
+    cp.go_prior = p->go_shadow;
+    cp.go_wait_ns = (uint64_t)p->opts.early_copier_us * 1000;
+    DTT_CUDA_TRY(launch_copier(cp, p->copier_ctas, p->copier_threads, p->opts.method, p->copy_stream));
+    p->early_pending = true;
+    p->early_launched = true;
+    p->early_round = p->round + 1;
+    ++p->early_launches;
+    return DTT_OK;
+}
+
+// Take a pending early copier's round away from it: it exits without copying (if it has not
+// already given the round up itself).
+void abort_early(dtt_plan* p) {
+    if (!p->early_pending) return;
+    uint64_t expected = p->go_shadow;
+    const uint64_t stop = early_stop_value(p->early_round);
+    if (cas_go(p, &expected, stop)) {
+        p->go_shadow = stop;
+        ++p->early_aborts;
+    } else {
+        p->go_shadow = expected;      // it had given the round up already
+        ++p->early_expired;
+    }
+    p->early_pending = false;
+}
+
+// start(): claim the pending early copier for the current round.  True when it will copy this
+// round; false when it had already given the round up (then a fresh copier is needed).
+bool claim_early(dtt_plan* p) {
+    if (!p->early_pending) return false;
+    p->early_pending = false;
+    uint64_t expected = p->go_shadow;
+    const uint64_t start = early_start_value(p->round);
+    if (cas_go(p, &expected, start)) {
+        p->go_shadow = start;
+        ++p->early_claims;
+        return true;
+    }
+    p->go_shadow = expected;          // early_stop_value(round): it expired
+    ++p->early_expired;
+    return false;
 }
 
 int validate_plan(dtt_plan* p, const dtt_schedule* const* scheds) {
@@ -633,6 +715,10 @@ int dtt_plan_create(void* const* bufs, uint64_t buf_bytes, uint32_t P,
         delete p;
         return fail(DTT_EINVAL, "dtt_plan_create: host_piece_bytes must be a multiple of 4096");
     }
+    if (o.early_copier_us > 1000000) {
+        delete p;
+        return fail(DTT_EINVAL, "dtt_plan_create: early_copier_us is at most 1000000 (one second)");
+    }
     if (o.method == DTT_COPY_TMA && o.stages < 2) {      // the ring loads ahead by stages - 1
         delete p;
         return fail(DTT_EINVAL, "dtt_plan_create: the bulk-copy path needs at least 2 stages");
@@ -668,6 +754,10 @@ int dtt_plan_create(void* const* bufs, uint64_t buf_bytes, uint32_t P,
         delete p;
         return rc;
     }
+    int host_atomics = 0;
+    if (cudaDeviceGetAttribute(&host_atomics, cudaDevAttrHostNativeAtomicSupported, p->device) != cudaSuccess)
+        host_atomics = 0;
+    p->host_atomics = host_atomics != 0;
     p->copier_ctas = o.copier_ctas ? o.copier_ctas : (uint32_t)sms * o.ctas_per_sm;
     p->copier_threads = o.copier_threads;
     if (o.deferred_copier > 2) {
@@ -737,7 +827,11 @@ int dtt_plan_start(dtt_plan* p, cudaStream_t producer_stream, dtt_handle* handle
     if (producer_stream == p->copy_stream)
         return fail(DTT_EINVAL, "dtt_plan_start: the producer stream must differ from the copy stream");
     p->copier_launched = false;      // the status words were zeroed by the last check (or upload)
-    if (p->n_global && !p->opts.deferred_copier) {
+    if (p->early_pending && (p->early_round != p->round || p->notify_host))
+        abort_early(p);              // a host-buffer round needs a copier that stamps arrivals
+    if (claim_early(p)) {
+        p->copier_launched = true;   // launched by the last wait(), now claimed for this round
+    } else if (p->n_global && !p->opts.deferred_copier) {
         const int rc = launch_round_copier(p);
         if (rc != DTT_OK) return rc;
     }
@@ -785,6 +879,12 @@ int dtt_plan_wait(dtt_plan* p, dtt_report* report) {
     ck.host = p->h_status_dev;
     ck.host_flags = p->h_status_dev ? reinterpret_cast<uint8_t*>(p->h_status_dev + 1) : nullptr;
     DTT_CUDA_TRY(launch_check(ck, p->producer_stream));
+    // The next round's copier queues behind this one while the host waits: its launch leaves
+    // the next round's critical path.  It copies nothing until start() claims it.
+    if (early_allowed(p)) {
+        const int erc = launch_early(p);
+        if (erc != DTT_OK) return erc;
+    }
     // The check stores its sequence number last, after every flag and status word: poll that
     // word, and ask the stream now and then so that a failed launch or a dead context ends the
     // wait with the CUDA error instead of spinning.
@@ -794,8 +894,12 @@ int dtt_plan_wait(dtt_plan* p, dtt_report* report) {
         if ((spin & 4095) == 0) {
             const cudaError_t e = cudaStreamQuery(p->producer_stream);
             if (e == cudaErrorNotReady) continue;
-            if (e != cudaSuccess) return fail(DTT_ECUDA, "dtt_plan_wait: %s", cudaGetErrorString(e));
+            if (e != cudaSuccess) {
+                abort_early(p);
+                return fail(DTT_ECUDA, "dtt_plan_wait: %s", cudaGetErrorString(e));
+            }
             if (__atomic_load_n(done, __ATOMIC_ACQUIRE) == ck.seq) break;
+            abort_early(p);
             return fail(DTT_ECUDA, "dtt_plan_wait: the check kernel finished without reporting");
         }
     }
@@ -828,6 +932,7 @@ int dtt_plan_wait(dtt_plan* p, dtt_report* report) {
     rep.status = rc;
     if (report) *report = rep;
     p->state = rc == DTT_OK ? DTT_PLAN_DONE : DTT_PLAN_FAILED;
+    if (rc != DTT_OK) abort_early(p);    // a failed plan has no next round
     return rc;
 }
 
@@ -893,6 +998,10 @@ int dtt_plan_close(dtt_plan* p) {
         return DTT_OK;
     }
     int rc = DTT_OK;
+    abort_early(p);                          // a copier launched for a round that never starts
+    if (p->early_launched && p->state != DTT_PLAN_RUNNING && p->state != DTT_PLAN_CLOSING &&
+        cudaStreamSynchronize(p->copy_stream) != cudaSuccess)
+        rc = fail(DTT_ECUDA, "dtt_plan_close: copy stream failed");
     if (p->state == DTT_PLAN_RUNNING) {
         // what the producers queued so far is written first; then every gate still closed is
         // opened, so the copier sends each chunk as it stands and exits
@@ -938,6 +1047,16 @@ int dtt_plan_stats(dtt_plan* p, double* copier_ms_last, double* copier_ms_total,
     return DTT_OK;
 }
 
+int dtt_plan_early_stats(const dtt_plan* p, uint64_t* launched, uint64_t* claimed, uint64_t* expired,
+                         uint64_t* aborted) {
+    if (!p) return fail(DTT_EINVAL, "dtt_plan_early_stats: NULL plan");
+    if (launched) *launched = p->early_launches;
+    if (claimed) *claimed = p->early_claims;
+    if (expired) *expired = p->early_expired;
+    if (aborted) *aborted = p->early_aborts;
+    return DTT_OK;
+}
+
 int dtt_plan_state(const dtt_plan* p) { return p ? p->state : DTT_EINVAL; }
 uint32_t dtt_plan_round(const dtt_plan* p) { return p ? p->round : 0; }
 
@@ -958,8 +1077,10 @@ int dtt_plan_read_gates(dtt_plan* p, uint64_t* host, uint64_t n_words) {
     const uint64_t need = (uint64_t)p->P * p->n_global * DTT_GATE_WORDS;
     if (n_words < need) return fail(DTT_EINVAL, "dtt_plan_read_gates: need %llu words", (unsigned long long)need);
     if (need == 0) return DTT_OK;
-    DTT_CUDA_TRY(cudaMemcpyAsync(host, p->d_gates, need * sizeof(uint64_t), cudaMemcpyDeviceToHost, p->copy_stream));
-    DTT_CUDA_TRY(cudaStreamSynchronize(p->copy_stream));
+    // on the plan's own auxiliary stream: a copier launched early for the next round may hold
+    // the copy stream until that round starts
+    DTT_CUDA_TRY(cudaMemcpyAsync(host, p->d_gates, need * sizeof(uint64_t), cudaMemcpyDeviceToHost, p->aux_stream));
+    DTT_CUDA_TRY(cudaStreamSynchronize(p->aux_stream));
     return DTT_OK;
 }
 
@@ -1137,7 +1258,9 @@ int dtt_allgather_host(dtt_plan* p, const void* const* host_slices, void* host_o
         }
         if ((rc = poll(true)) != DTT_OK) return rc;
     }
+    p->suppress_early = true;
     rc = dtt_plan_wait(p, report);
+    p->suppress_early = false;
     if (rc != DTT_OK) {
         cudaStreamSynchronize(p->d2h_stream);
         return rc;

@@ -194,6 +194,22 @@ typedef struct dtt_plan_opts {
                                 stream (read with dtt_plan_stats) */
     uint32_t host_piece_bytes;/* dtt_allgather_host: bytes per host-to-device copy (a multiple
                                 of 4096); 0 = a quarter of a slice, at least 4 MiB */
+    uint32_t early_copier_us; /* > 0: dtt_plan_wait launches the NEXT round's copier right after
+                                this round's check, queued behind this round's copier, so that
+                                the next dtt_plan_start launches nothing (the pages' "prepare":
+                                the copy engine's queue is armed before the round).  That copier
+                                copies nothing until dtt_plan_start claims it; if no start comes
+                                within early_copier_us microseconds of it beginning to wait, it
+                                gives the round up and exits, and start launches a fresh copier.
+                                The claim and the give-up are one compare-and-swap each on a
+                                mapped host word, so exactly one side wins.  A failed wait,
+                                dtt_plan_close and dtt_allgather_host abort it.  While it waits it
+                                holds the copy stream and its SM resources: a device-wide
+                                synchronisation (cudaDeviceSynchronize, cudaFree) made between
+                                wait and the next start lasts until it gives up.  Ignored (the
+                                copier is launched at start) with time_copier, deferred_copier
+                                = 1, a copy stream another live plan uses, or a device without
+                                host-native atomics.  At most 1000000; 0 = off */
 } dtt_plan_opts;
 
 void dtt_plan_opts_default(dtt_plan_opts* opts);
@@ -332,8 +348,16 @@ int dtt_plan_info(const dtt_plan* plan, uint32_t* n_global, uint32_t* first_chun
 int dtt_plan_stats(dtt_plan* plan, double* copier_ms_last, double* copier_ms_total,
                    uint64_t* rounds_timed);
 
+/* Counts of a plan's early copiers (opts.early_copier_us) so far: launched by dtt_plan_wait,
+ * claimed by the next dtt_plan_start, found by the host to have given their round up (start then
+ * launched a fresh copier), and aborted by the host (failed wait, close, host-buffer round).  Any
+ * pointer may be NULL.  Errors: DTT_EINVAL. */
+int dtt_plan_early_stats(const dtt_plan* plan, uint64_t* launched, uint64_t* claimed,
+                         uint64_t* expired, uint64_t* aborted);
+
 /* Copy the P gate tables (P * n_global * 8 uint64, rank-major) to host memory `host`
- * (n_words long).  Synchronises the copy stream.  Errors: DTT_EINVAL if n_words is short. */
+ * (n_words long), on an internal stream of the plan, and wait for the copy.  Made mid-round it
+ * is a snapshot.  Errors: DTT_EINVAL if n_words is short. */
 int dtt_plan_read_gates(dtt_plan* plan, uint64_t* host, uint64_t n_words);
 
 /* Host-buffer all-gather, one round end to end: copy each rank's slice (host_slices[r],

@@ -197,3 +197,31 @@ def test_library_grouped_order_short_last_group_golden():
         steps = [tuple(int(v) for v in t.split(",")) for t in row[i + 1:]]
         got = [D.dtt_tile_of(D.ORDER_GROUPED, gm, s, tiles_m, tiles_n) for s in range(len(steps))]
         assert got == steps
+
+
+def test_binding_structs_match_the_c_header(tmp_path):
+    # every struct the binding passes by pointer has the header's size and field offsets
+    import shutil
+    import subprocess
+    if not shutil.which("gcc"):
+        pytest.skip("gcc not found")
+    structs = {"dtt_region": D.dtt_region, "dtt_order": D.dtt_order, "dtt_plan_opts": D.dtt_plan_opts,
+               "dtt_handle": D.dtt_handle, "dtt_report": D.dtt_report, "dtt_fill_desc": D.dtt_fill_desc}
+    lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "dtt.h"', 'int main(void) {']
+    for name, cls in structs.items():
+        lines.append(f'printf("{name} %zu\\n", sizeof({name}));')
+        for f in cls._fields_:
+            lines.append(f'printf("{name}.{f[0]} %zu\\n", offsetof({name}, {f[0]}));')
+    lines += ["return 0;", "}"]
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines))
+    exe = tmp_path / "layout"
+    cuda_inc = os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "include")
+    subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), "-I", cuda_inc, str(src), "-o", str(exe)],
+                   check=True)
+    got = dict(l.split() for l in subprocess.run([str(exe)], capture_output=True, text=True,
+                                                  check=True).stdout.splitlines())
+    for name, cls in structs.items():
+        assert int(got[name]) == C.sizeof(cls), name
+        for f in cls._fields_:
+            assert int(got[f"{name}.{f[0]}"]) == getattr(cls, f[0]).offset, (name, f[0])
