@@ -151,9 +151,15 @@ def bench_launch(w) -> dict:
     CTA resident at once (128-thread CTAs).  The GEMM producer keeps the vector copier: its own
     shared-memory ring leaves no room for a bulk-copy ring on the same SM."""
     sms = sm_count()
+    # Chunked and tiled workloads: each round's copier is launched early, by the previous
+    # round's wait, and claimed by start (it waits up to 2 ms for that), so the copier's launch
+    # leaves the round's critical path (c2: ~114 -> ~112 us per round).  whole() rounds are
+    # bound by the host's launches, where the early launch only moves one: they launch at start.
+    early = 2000
     if w.kind == "chunks":     # three bulk-copy CTAs per SM: one thread alone cannot keep HBM busy
         return {"group": max(1, sms // len(w.senders())), "programs": 1, "threads": 256,
-                "opts": dtt_plan_opts_default(method=1, piece_bytes=32768, stages=2, ctas_per_sm=3)}
+                "opts": dtt_plan_opts_default(method=1, piece_bytes=32768, stages=2, ctas_per_sm=3,
+                                              early_copier_us=early)}
     if w.kind == "whole":
         # the copier is launched after the producer's launch (it has nothing to do before the
         # whole slice is written)
@@ -168,9 +174,10 @@ def bench_launch(w) -> dict:
         return {"threads": 1024, "opts": opts}
     if w.K == 0:       # the tiled fill in 128-thread CTAs: all of them resident at once
         return {"threads": 128, "pace": 2,
-                "opts": dtt_plan_opts_default(method=1, piece_bytes=32768, stages=2, ctas_per_sm=3)}
+                "opts": dtt_plan_opts_default(method=1, piece_bytes=32768, stages=2, ctas_per_sm=3,
+                                              early_copier_us=early)}
     # the GEMM producer: two 256-thread vector copier CTAs per SM beside the GEMM's CTA
-    return {"opts": dtt_plan_opts_default(copier_threads=256, ctas_per_sm=2)}
+    return {"opts": dtt_plan_opts_default(copier_threads=256, ctas_per_sm=2, early_copier_us=early)}
 
 
 @dataclass

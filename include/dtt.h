@@ -206,7 +206,9 @@ typedef struct dtt_plan_opts {
                                 dtt_plan_close and dtt_allgather_host abort it.  While it waits it
                                 holds the copy stream and its SM resources: a device-wide
                                 synchronisation (cudaDeviceSynchronize, cudaFree) made between
-                                wait and the next start lasts until it gives up.  Ignored (the
+                                wait and the next start lasts until it gives up, and so does the
+                                first launch of a kernel not yet loaded (lazy module loading
+                                waits for the device to idle).  Ignored (the
                                 copier is launched at start) with time_copier, deferred_copier
                                 = 1, a copy stream another live plan uses, or a device without
                                 host-native atomics.  At most 1000000; 0 = off */
