@@ -22,6 +22,14 @@ pull 573, section Design notes):
 * Rounds start at 1, go up by one per next_round and are never reset: at most 2**32 - 1.
 * close() in the middle of a round sends each chunk as it stands: gates not yet open are
   opened and the queues drain.
+* Groups ("Triggered Plans", Not supported yet: "Waiting on a group" -- the page only names the
+  missing feature: no single counter covers several chunks or several source ranks).  Reading:
+  a group is a set of global chunk ids, possibly of several source ranks; each virtual rank keeps
+  one counter per group that goes up by one whenever one of the group's chunks becomes readable
+  at that rank -- another rank's chunk when its arrival is signalled there, the rank's own chunk
+  when its gate opens.  Every chunk becomes readable once per round at every rank, so after R
+  rounds the counter holds R * |group|, and a wait on the group passes when the counter reaches
+  round * |group|: exactly when every chunk of the group is readable there this round.
 """
 from __future__ import annotations
 
@@ -101,12 +109,59 @@ class Plan:
         self.delivered = set()          # (chunk, peer) delivered in the current round
         self.delivery_log: List[Tuple[int, int, int]] = []   # (source, peer, chunk) in order
         self.state = "PREPARED"
+        self.groups: List[List[int]] = []
+        self.groups_of: List[List[int]] = [[] for _ in range(self.G)]   # chunk -> its groups
+        self.group_counters = np.zeros((self.P, 0), dtype=np.uint64)
+        self.started = False
+
+    # -- groups -------------------------------------------------------------------
+    def define_groups(self, groups: Sequence[Sequence[int]]) -> None:
+        """Declare the groups (lists of global chunk ids; a chunk may be in several groups).
+        Allowed once, before the first round starts; counters begin as after the completed
+        rounds before the current one."""
+        if self.started or self.groups:
+            raise StateError("groups are defined once, before the first start")
+        for g in groups:
+            if not len(g) or len(set(g)) != len(g) or any(not (0 <= c < self.G) for c in g):
+                raise ValueError("a group is a non-empty set of chunk ids of the plan")
+        self.groups = [list(g) for g in groups]
+        self.groups_of = [[] for _ in range(self.G)]
+        for i, g in enumerate(self.groups):
+            for c in g:
+                self.groups_of[c].append(i)
+        prior = self.round - 1
+        self.group_counters = np.zeros((self.P, len(self.groups)), dtype=np.uint64)
+        for i, g in enumerate(self.groups):
+            self.group_counters[:, i] = prior * len(g)
+
+    def chunk_readable(self, rank: int, c: int) -> bool:
+        """Has chunk c become readable at rank this round (own chunk: gate open; another
+        rank's chunk: its arrival signalled here)?"""
+        if self.owner[c] == rank:
+            return self.gate_open(c)
+        return int(self.gates[rank, c, ARRIVAL]) >= self.round
+
+    def group_ready(self, rank: int, g: int) -> bool:
+        """The one test a group wait makes: the rank's counter of group g >= round * |g|."""
+        return int(self.group_counters[rank, g]) >= self.round * len(self.groups[g])
+
+    def _count_group(self, rank: int, c: int) -> None:
+        for g in self.groups_of[c]:
+            self.group_counters[rank, g] += 1
+
+    def signal_arrival(self, s: int, p: int, c: int) -> None:
+        """The end of one copy of chunk c from s to p: arrival at p, completion at s, and p's
+        counters of the chunk's groups."""
+        self.gates[p, c, ARRIVAL] += 1
+        self.gates[s, c, COMPLETION] += 1
+        self._count_group(p, c)
 
     # -- round ------------------------------------------------------------------
     def start(self) -> int:
         if self.state != "PREPARED":
             raise StateError(f"start in state {self.state}")
         self.state = "RUNNING"
+        self.started = True
         return self.round
 
     def chunks_of(self, r: int) -> range:
@@ -121,6 +176,7 @@ class Plan:
         target = self.round * self.chunks[c].writers
         if row[COUNTER] == target:
             row[READY] = self.round
+            self._count_group(rank, c)     # readable at its own rank from now on
         elif row[COUNTER] > target:
             row[ERROR] = self.round
 
@@ -153,8 +209,7 @@ class Plan:
                     if self.copy_data:
                         for reg in self.chunks[c].regions:
                             copy_region(self.bufs[s], self.bufs[p], reg)
-                    self.gates[p, c, ARRIVAL] += 1
-                    self.gates[s, c, COMPLETION] += 1
+                    self.signal_arrival(s, p, c)
                     self.delivered.add((c, p))
                     self.delivery_log.append((s, p, c))
                     n += 1

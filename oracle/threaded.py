@@ -18,7 +18,7 @@ from typing import Callable, Dict, List, Optional, Sequence
 import numpy as np
 
 from . import schedule as S
-from .plan import ARRIVAL, COMPLETION, COUNTER, ERROR, READY, Plan, copy_region
+from .plan import READY, Plan, copy_region
 
 
 class ThreadedRound:
@@ -32,7 +32,8 @@ class ThreadedRound:
 
     def __init__(self, plan: Plan, write_unit: Callable[[int, int, int], None],
                  order: Dict[int, List], programs: int = 1, max_polls: int = 20000,
-                 poll_sleep: float = 1e-5, skip=(), extra=(), delay: Optional[Dict] = None):
+                 poll_sleep: float = 1e-5, skip=(), extra=(), delay: Optional[Dict] = None,
+                 group_waits: Sequence = ()):
         self.plan = plan
         self.write_unit = write_unit
         self.order = order
@@ -46,6 +47,11 @@ class ThreadedRound:
         self.queue_log: Dict[tuple, List[int]] = {}
         self.timeouts: List[tuple] = []
         self.abort = threading.Event()
+        # consumers: (rank, group) pairs, each a thread that waits once on the group and then
+        # reads every chunk of it from the rank's own buffer; result per pair: "ok", "timeout"
+        # or "stale" (a chunk's bytes differ from its source's)
+        self.group_waits = list(group_waits)
+        self.consumer_results: Dict[tuple, str] = {}
 
     # atomics --------------------------------------------------------------------------------
     def _mark(self, rank: int, c: int) -> None:
@@ -86,10 +92,30 @@ class ThreadedRound:
             for reg in plan.chunks[c].regions:
                 copy_region(plan.bufs[s], plan.bufs[p], reg)
             with self.lock:
-                plan.gates[p, c, ARRIVAL] += 1
-                plan.gates[s, c, COMPLETION] += 1
+                plan.signal_arrival(s, p, c)
                 plan.delivered.add((c, p))
             log.append(c)
+
+    def _consumer(self, rank: int, g: int) -> None:
+        plan = self.plan
+        polls = 0
+        while True:
+            with self.lock:
+                if plan.group_ready(rank, g):
+                    break
+            polls += 1
+            if polls > self.max_polls or self.abort.is_set():
+                self.consumer_results[(rank, g)] = "timeout"
+                return
+            time.sleep(self.poll_sleep)
+        ok = True
+        for c in plan.groups[g]:
+            s = plan.owner[c]
+            for (off, nb, rows, pitch) in plan.chunks[c].regions:
+                for i in range(rows):
+                    a = off + i * pitch
+                    ok = ok and bool(np.array_equal(plan.bufs[rank][a:a + nb], plan.bufs[s][a:a + nb]))
+        self.consumer_results[(rank, g)] = "ok" if ok else "stale"
 
     def run(self, close_after: Optional[float] = None):
         """Start every thread, optionally close mid-round after ``close_after`` s, join, wait()."""
@@ -100,6 +126,8 @@ class ThreadedRound:
             for p in range(plan.P):
                 if p != s:
                     threads.append(threading.Thread(target=self._copier, args=(s, p)))
+        for (rank, g) in self.group_waits:
+            threads.append(threading.Thread(target=self._consumer, args=(rank, g)))
         for r in range(plan.P):
             for q in range(self.programs):
                 threads.append(threading.Thread(target=self._producer, args=(r, q)))

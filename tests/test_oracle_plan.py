@@ -257,3 +257,140 @@ def test_reusable_follows_head_of_line_order():
     plan.mark_ready(0, 0)
     plan.copier_progress()
     assert plan.reusable(0, 0) and plan.reusable(0, 1) and not plan.reusable(0, 2)
+
+
+# ---- groups ("Triggered Plans", Not supported yet: "Waiting on a group") ------------------------
+def _random_groups(plan, rng, n):
+    """n groups of random chunk sets, across source ranks; chunks may repeat across groups."""
+    out = []
+    for _ in range(n):
+        k = int(rng.integers(1, plan.G + 1))
+        out.append(sorted(int(c) for c in rng.choice(plan.G, size=k, replace=False)))
+    return out
+
+
+def test_group_counters_closed_form_after_each_round():
+    # each chunk becomes readable once per round at every rank (its own rank: when its gate
+    # opens), so after R rounds every rank's counter of group g holds R * |g|
+    rng = np.random.default_rng(5)
+    for P, kind, kw in [(3, "chunks", {"n": 3}), (4, "tile_chunks", {"BM": 2, "BN": 4, "T": 3}),
+                        (2, "whole", {"np": 2})]:
+        plan, sb = make_plan(P, 6, 8, "bf16", kind, **kw)
+        groups = _random_groups(plan, rng, 5) + [list(range(plan.G))]
+        plan.define_groups(groups)
+        for R in (1, 2, 3):
+            plan.start()
+            produce_all(plan, P, 6, 8, "bf16", 1, sb)
+            plan.copier_progress()
+            assert plan.wait()[0] == PL.OK
+            for q in range(P):
+                for g, members in enumerate(groups):
+                    assert int(plan.group_counters[q, g]) == R * len(members)
+            plan.next_round()
+
+
+def test_group_wait_passes_exactly_when_every_member_is_readable():
+    # the definition of waiting on a group: every chunk of it readable at the rank this round.
+    # Checked at every step of random mark orders with the copier run at random moments, in
+    # rounds 1-3 (a test against |g| without the round, or of arrival only, fails here)
+    rng = np.random.default_rng(9)
+    P = 3
+    plan, sb = make_plan(P, 6, 4, "bf16", "chunks", n=3)
+    groups = _random_groups(plan, rng, 8) + [[plan.first[1]], [plan.first[0], plan.first[2] + 1]]
+    plan.define_groups(groups)
+    for R in (1, 2, 3):
+        plan.start()
+        marks = [(r, c) for r in range(P) for c in plan.chunks_of(r) for _ in range(plan.chunks[c].writers)]
+
+        def check():
+            for q in range(P):
+                for g, members in enumerate(groups):
+                    assert plan.group_ready(q, g) == all(plan.chunk_readable(q, c) for c in members)
+        check()
+        for i in rng.permutation(len(marks)):
+            plan.mark_ready(*marks[i])
+            check()
+            if rng.random() < 0.4:
+                plan.copier_progress()
+                check()
+        plan.copier_progress()
+        check()
+        assert all(plan.group_ready(q, g) for q in range(P) for g in range(len(groups)))
+        assert plan.wait()[0] == PL.OK
+        plan.next_round()
+
+
+def test_group_of_own_chunks_opens_with_the_gates():
+    # a rank's own chunks count when their gates open, not when they reach peers
+    plan, sb = make_plan(2, 6, 4, "bf16", "chunks", n=3)
+    plan.define_groups([list(plan.chunks_of(0)), [plan.first[0], plan.first[1]]])
+    plan.start()
+    for c in plan.chunks_of(0):
+        plan.mark_ready(0, c)
+    assert plan.group_ready(0, 0)                   # no copy needed for rank 0's own chunks
+    assert not plan.group_ready(1, 0)               # nothing copied yet
+    plan.copier_progress()
+    assert plan.group_ready(1, 0)
+    assert not plan.group_ready(0, 1) and not plan.group_ready(1, 1)   # rank 1's chunk 0 not marked
+    plan.mark_ready(1, plan.first[1])
+    assert plan.group_ready(1, 1) and not plan.group_ready(0, 1)
+    plan.copier_progress()
+    assert plan.group_ready(0, 1)
+
+
+def test_group_head_of_line_and_initial_round():
+    # a group whose member waits behind a closed gate on its queue is not ready; counters of a
+    # plan that begins at round R0 start as after R0 - 1 rounds
+    plan, sb = make_plan(2, 6, 4, "bf16", "chunks", initial_round=7, n=3)
+    plan.define_groups([[plan.first[0] + 1], [plan.first[0], plan.first[0] + 2]])
+    assert list(plan.group_counters[:, 0]) == [6, 6] and list(plan.group_counters[:, 1]) == [12, 12]
+    plan.start()
+    plan.mark_ready(0, plan.first[0] + 1)           # queued behind chunk 0 on the way to rank 1
+    plan.copier_progress()
+    assert plan.group_ready(0, 0) and not plan.group_ready(1, 0)
+    plan.mark_ready(0, plan.first[0])
+    plan.copier_progress()
+    assert plan.group_ready(1, 0) and not plan.group_ready(1, 1)
+
+
+def test_group_definition_rules():
+    plan, sb = make_plan(2, 6, 4, "bf16", "chunks", n=3)
+    for bad in ([[]], [[0, 0]], [[plan.G]], [[-1]]):
+        with pytest.raises(ValueError):
+            plan.define_groups(bad)
+    plan.define_groups([[0, 1]])
+    with pytest.raises(PL.StateError):
+        plan.define_groups([[0]])                   # once per plan
+    plan2, _ = make_plan(2, 6, 4, "bf16", "chunks", n=3)
+    plan2.start()
+    with pytest.raises(PL.StateError):
+        plan2.define_groups([[0]])                  # before the first start
+
+
+def test_group_exhaustive_interleavings_tiny_plan():
+    # P = 2, two chunks per rank with two writers each, one group of all four chunks and one of
+    # the two ranks' first chunks: in every interleaving of the eight marks, with the copier run
+    # after each, a group is ready at a rank exactly when each of its chunks is readable there
+    P, rb = 2, 8
+    sb = 4 * rb
+    seqs = [(r, w) for r in range(P) for w in range(2)]
+    events = [x for x in seqs for _ in range(2)]
+    for order in sorted(set(itertools.permutations(events))):
+        bufs = [np.zeros(P * sb, dtype=np.uint8) for _ in range(P)]
+        scheds = [S.Schedule([S.Chunk([(r * sb + k * 2 * rb, 2 * rb, 1, 2 * rb)], 2)
+                              for k in range(2)]) for r in range(P)]
+        plan = PL.Plan(bufs, scheds)
+        groups = [[0, 1, 2, 3], [0, 2]]
+        plan.define_groups(groups)
+        plan.start()
+        pos = {x: 0 for x in seqs}
+        for ev in order:
+            r, w = ev
+            k = pos[ev]
+            pos[ev] += 1
+            plan.mark_ready(r, plan.first[r] + k)
+            plan.copier_progress()
+            for q in range(P):
+                for g, members in enumerate(groups):
+                    assert plan.group_ready(q, g) == all(plan.chunk_readable(q, c) for c in members)
+        assert all(plan.group_ready(q, g) for q in range(P) for g in range(2))

@@ -82,3 +82,33 @@ def test_barrier_threads(P):
         want = np.full(P, 3)
         want[r] = 0
         assert np.array_equal(ys[r], want)
+
+
+def test_group_waits_with_threads():
+    # consumer threads wait once on a group (chunks of several source ranks, one of them the
+    # consumer's own) and then read every chunk of it: the data is there; the producers complete
+    # chunks backwards, so the groups open only at the end of each queue
+    plan, write_unit, order, data, sb = _setup(P=3, n=4)
+    groups = [[0, 5, 10], [1, 2, 3], list(range(plan.G)), [7]]
+    plan.define_groups(groups)
+    for r in range(3):
+        order[r] = list(reversed(order[r]))
+    waits = [(q, g) for q in range(3) for g in range(len(groups))]
+    tr = ThreadedRound(plan, write_unit, order, delay={(c, 0): 0.003 for c in range(plan.G)},
+                       group_waits=waits)
+    assert tr.run()[0] == PL.OK
+    assert all(tr.consumer_results[k] == "ok" for k in waits), tr.consumer_results
+    for q in range(3):
+        for g, members in enumerate(groups):
+            assert int(plan.group_counters[q, g]) == len(members)
+
+
+def test_group_wait_times_out_on_a_missing_mark():
+    plan, write_unit, order, data, sb = _setup(P=2, n=2)
+    plan.define_groups([[0, 3], [0, 1]])
+    tr = ThreadedRound(plan, write_unit, order, max_polls=300, skip=[(3, 0)],
+                       group_waits=[(0, 0), (1, 0), (0, 1), (1, 1)])
+    status, short, extra = tr.run()
+    assert status == PL.TIMEOUT and short == [3]
+    assert tr.consumer_results[(0, 0)] == "timeout" and tr.consumer_results[(1, 0)] == "timeout"
+    assert tr.consumer_results[(0, 1)] == "ok" and tr.consumer_results[(1, 1)] == "ok"
