@@ -702,7 +702,8 @@ def run_consumer(args):
     X [P*M, N] (the all-gather's output) and W^T [consumer_n, N], each 128-row block loaded as
     soon as its chunks have arrived.  Times the all-gather round alone, the GEMM alone (its
     chunks already delivered), and the two overlapped in one round; the copier is the bulk-copy
-    one with a ring small enough to leave the GEMM room, or the vector one."""
+    one with a ring small enough to leave the GEMM room, or the vector one.  Both wait forms are
+    timed: one wait per chunk of a block, and one wait per block on a chunk group."""
     import torch
     import device_triggered_transfers_gb300 as D
     from device_triggered_transfers_gb300 import runner
@@ -718,59 +719,70 @@ def run_consumer(args):
     # vector copier
     launch = {k: v for k, v in runner.bench_launch(w).items() if k != "opts"}
     if args.consumer_copier == "bulk":    # one CTA per SM with a ring small enough for the GEMM's
-        copts = D.dtt_plan_opts_default(method=D.COPY_TMA, piece_bytes=32768, stages=2)
         copier_desc = "bulk copies, one CTA per SM, 2 x 32 KiB stages"
     else:
-        copts = D.dtt_plan_opts_default(copier_threads=args.consumer_copier_threads)
         copier_desc = f"vector (16-byte) path, {args.consumer_copier_threads} threads per CTA"
-    st = runner.make(w, opts=copts, copy_stream=copy_stream, **launch)
-    prod = st.producer_stream
 
-    def ag():
-        h = st.plan.start(prod)
-        D.dtt_fill_producer(st.buf_ptrs, st.desc, h, prod)
-        st.plan.wait()
-        st.plan.next_round()
+    def copts():
+        if args.consumer_copier == "bulk":
+            return D.dtt_plan_opts_default(method=D.COPY_TMA, piece_bytes=32768, stages=2)
+        return D.dtt_plan_opts_default(copier_threads=args.consumer_copier_threads)
 
-    def overlapped():
-        h = st.plan.start(prod)
-        st.plan.gemm_consumer(0, Wt, out, N2, K, err, stream=cons)
-        D.dtt_fill_producer(st.buf_ptrs, st.desc, h, prod)
-        st.plan.wait()
-        prod.wait_stream(cons)
-        st.plan.next_round()
+    def measure(grouped):
+        st = runner.make(w, opts=copts(), copy_stream=copy_stream, **launch)
+        n_groups = None
+        if grouped:     # one group per 128-row block of X, before the first round
+            n_groups, _ = st.plan.define_block_groups(128 * 2 * K)
+        prod = st.producer_stream
 
-    def timed(fn, K_):
-        for _ in range(3):
-            fn()
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(prod)
-        for _ in range(K_):
-            fn()
-        e1.record(prod)
-        torch.cuda.synchronize()
-        return e0.elapsed_time(e1) / K_
+        def ag():
+            h = st.plan.start(prod)
+            D.dtt_fill_producer(st.buf_ptrs, st.desc, h, prod)
+            st.plan.wait()
+            st.plan.next_round()
 
-    K_ = max(3, min(args.steps, 50))
-    ag_ms = timed(ag, K_)
-    ov_ms = timed(overlapped, K_)
-    gemm = []
-    for _ in range(K_):                 # the GEMM alone: its chunks have all arrived
-        h = st.plan.start(prod)
-        D.dtt_fill_producer(st.buf_ptrs, st.desc, h, prod)
-        torch.cuda.synchronize()        # producer and copier done
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(cons)
-        st.plan.gemm_consumer(0, Wt, out, N2, K, err, stream=cons)
-        e1.record(cons)
-        st.plan.wait()
-        cons.synchronize()
-        st.plan.next_round()
-        gemm.append(e0.elapsed_time(e1))
-    gemm_ms = statistics.median(gemm)
-    st.plan.close()
-    assert int(err.item()) == 0
+        def overlapped():
+            h = st.plan.start(prod)
+            st.plan.gemm_consumer(0, Wt, out, N2, K, err, stream=cons)
+            D.dtt_fill_producer(st.buf_ptrs, st.desc, h, prod)
+            st.plan.wait()
+            prod.wait_stream(cons)
+            st.plan.next_round()
+
+        def timed(fn, K_):
+            for _ in range(3):
+                fn()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(prod)
+            for _ in range(K_):
+                fn()
+            e1.record(prod)
+            torch.cuda.synchronize()
+            return e0.elapsed_time(e1) / K_
+
+        K_ = max(3, min(args.steps, 50))
+        ag_ms = timed(ag, K_)
+        ov_ms = timed(overlapped, K_)
+        gemm = []
+        for _ in range(K_):                 # the GEMM alone: its chunks have all arrived
+            h = st.plan.start(prod)
+            D.dtt_fill_producer(st.buf_ptrs, st.desc, h, prod)
+            torch.cuda.synchronize()        # producer and copier done
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(cons)
+            st.plan.gemm_consumer(0, Wt, out, N2, K, err, stream=cons)
+            e1.record(cons)
+            st.plan.wait()
+            cons.synchronize()
+            st.plan.next_round()
+            gemm.append(e0.elapsed_time(e1))
+        st.plan.close()
+        assert int(err.item()) == 0
+        return K_, ag_ms, ov_ms, statistics.median(gemm), n_groups
+
+    K_, ag_ms, ov_ms, gemm_ms, _ = measure(False)
+    _, ag_g, ov_g, gemm_g, n_groups = measure(True)
     flops = 2.0 * rows * N2 * K
     tf_peak, tf_kind = load_tensor_peak()
     line = {"metric": "all-gather + consumer GEMM round, overlapped (1 GB300)", "unit": "ms per round",
@@ -781,7 +793,10 @@ def run_consumer(args):
             "all_gather_ms": ag_ms, "gemm_alone_ms": gemm_ms,
             "sequential_ms": ag_ms + gemm_ms, "overlap_saving": 1.0 - ov_ms / (ag_ms + gemm_ms),
             "gemm_alone_tflops": flops / (gemm_ms / 1e3) / 1e12,
-            "gemm_alone_frac": flops / (gemm_ms / 1e3) / 1e12 / tf_peak, "peak_kind": tf_kind}
+            "gemm_alone_frac": flops / (gemm_ms / 1e3) / 1e12 / tf_peak, "peak_kind": tf_kind,
+            "group_waits": {"groups": n_groups, "overlapped_ms": ov_g, "all_gather_ms": ag_g,
+                            "gemm_alone_ms": gemm_g,
+                            "overlap_saving": 1.0 - ov_g / (ag_g + gemm_g)}}
     print(json.dumps(line))
     return 0
 

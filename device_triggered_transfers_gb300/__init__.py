@@ -62,7 +62,7 @@ class dtt_handle(C.Structure):
     _fields_ = [("gates", C.c_void_p), ("writers", C.c_void_p), ("status", C.c_void_p),
                 ("round", C.c_uint32), ("rank", C.c_uint32), ("P", C.c_uint32),
                 ("n_global", C.c_uint32), ("first_chunk", C.c_uint32), ("n_chunks", C.c_uint32),
-                ("flags", C.c_uint32), ("reserved", C.c_uint32)]
+                ("flags", C.c_uint32), ("reserved", C.c_uint32), ("groups", C.c_void_p)]
 
 
 class dtt_report(C.Structure):
@@ -121,6 +121,9 @@ _SIGS = {
     "dtt_plan_state": (C.c_int, [_P]),
     "dtt_plan_early_stats": (C.c_int, [_P, C.POINTER(_u64), C.POINTER(_u64), C.POINTER(_u64),
                                        C.POINTER(_u64)]),
+    "dtt_plan_define_groups": (C.c_int, [_P, _u32, C.POINTER(_u32), C.POINTER(_u32)]),
+    "dtt_plan_define_block_groups": (C.c_int, [_P, _u64, C.POINTER(_u32), C.POINTER(_u32)]),
+    "dtt_plan_read_group_counters": (C.c_int, [_P, C.POINTER(_u64), _u64]),
     "dtt_plan_round": (C.c_uint32, [_P]),
     "dtt_plan_info": (C.c_int, [_P, C.POINTER(_u32), C.POINTER(_u32), C.POINTER(_u32), C.POINTER(_P)]),
     "dtt_plan_read_gates": (C.c_int, [_P, C.POINTER(_u64), _u64]),
@@ -398,6 +401,35 @@ class Plan:
         last, total, n = C.c_double(), C.c_double(), _u64()
         _check(lib().dtt_plan_stats(self._h, C.byref(last), C.byref(total), C.byref(n)))
         return last.value, total.value, n.value
+
+    def define_groups(self, groups) -> int:
+        """Chunk groups (lists of global chunk ids), before the first start; see
+        dtt_plan_define_groups.  Returns the number of groups."""
+        groups = [list(g) for g in groups]
+        offs = [0]
+        for g in groups:
+            offs.append(offs[-1] + len(g))
+        o = (_u32 * len(offs))(*offs)
+        ids = (_u32 * max(1, offs[-1]))(*[c for g in groups for c in g])
+        _check(lib().dtt_plan_define_groups(self._h, len(groups), o, ids))
+        self.n_groups = len(groups)
+        return self.n_groups
+
+    def define_block_groups(self, block_bytes: int):
+        """One group per block of block_bytes bytes (the chunks touching it); returns
+        (n_groups, [group id of each block or None])."""
+        nb = -(-self.buf_bytes // block_bytes)
+        n = _u32()
+        bg = (_u32 * nb)()
+        _check(lib().dtt_plan_define_block_groups(self._h, block_bytes, C.byref(n), bg))
+        self.n_groups = n.value
+        return n.value, [None if x == 0xFFFFFFFF else x for x in bg]
+
+    def read_group_counters(self) -> np.ndarray:
+        """The group counters as a uint64 array [P, n_groups]."""
+        out = np.zeros((self.P, self.n_groups), dtype=np.uint64)
+        _check(lib().dtt_plan_read_group_counters(self._h, out.ctypes.data_as(C.POINTER(_u64)), out.size))
+        return out
 
     def early_stats(self) -> dict:
         """Early copiers so far (opts.early_copier_us): launched, claimed, expired, aborted."""

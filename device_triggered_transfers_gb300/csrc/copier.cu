@@ -156,6 +156,7 @@ __device__ __forceinline__ void copier_body(const CopierParams& p) {
                     if (p.flags & DTT_HANDLE_TIMESTAMPS)
                         dtt_dev::st_relaxed(prow + DTT_GATE_T_ARRIVE, dtt_dev::globaltimer());
                     dtt_dev::red_release_add(prow + DTT_GATE_ARRIVAL, 1);
+                    dtt_dev::count_groups(p.groups, q, c);
                 }
                 dtt_dev::red_release_add(row + DTT_GATE_COMPLETION, p.P - 1);
                 notify_host(p, c);
@@ -427,6 +428,7 @@ __device__ __forceinline__ void copier_bulk_body(const CopierParams& p) {
                 if (p.flags & DTT_HANDLE_TIMESTAMPS)
                     dtt_dev::st_relaxed(prow + DTT_GATE_T_ARRIVE, dtt_dev::globaltimer());
                 dtt_dev::red_release_add(prow + DTT_GATE_ARRIVAL, 1);
+                dtt_dev::count_groups(p.groups, q, c);
             }
             dtt_dev::red_release_add(row + DTT_GATE_COMPLETION, p.P - 1);
             notify_host(p, c);

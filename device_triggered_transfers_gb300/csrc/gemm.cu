@@ -325,6 +325,7 @@ struct ConsumerParams {
     const uint32_t* c0;      // per row block: the chunk ids [c0, c1] that cover it
     const uint32_t* c1;
     const uint32_t* order2;  // pair form: pairs of row blocks (2 pb, 2 pb + 1) in the order taken
+    const uint32_t* bgroup;  // per row block: its chunk group (one wait), or null: wait per chunk
     char* D;
     uint64_t ldd;
     uint64_t max_polls;
@@ -342,6 +343,29 @@ __device__ __forceinline__ bool wait_chunks(const dtt_handle& h, uint32_t c0, ui
         bool ok = false;
         for (uint64_t i = 0; i < max_polls; ++i) {
             if ((uint32_t)dtt_dev::ld_acquire(w) >= h.round) { ok = true; break; }
+            if ((i & 63) == 63 && *abort) return false;
+            __nanosleep(ns);
+            ns = ns < 256 ? ns + 32 : 256;
+        }
+        if (!ok) return false;
+    }
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    return true;
+}
+
+// Bounded wait for row block b's chunks: one poll of its group's counter when the plan has block
+// groups ("Triggered Plans", Not supported yet, "Waiting on a group"), else every chunk in turn.
+__device__ __forceinline__ bool wait_block(const ConsumerParams& p, uint32_t b, volatile uint32_t* abort) {
+    if (!p.bgroup) return wait_chunks(p.h, p.c0[b], p.c1[b], p.max_polls, abort);
+    const uint32_t g = p.bgroup[b];
+    if (g != 0xFFFFFFFFu) {                  // a block no chunk touches has nothing to wait for
+        const dtt_group_table* t = p.h.groups;
+        const uint64_t* w = t->counters + (uint64_t)p.h.rank * t->n_groups + g;
+        const uint64_t target = (uint64_t)p.h.round * t->size[g];
+        uint32_t ns = 0;
+        bool ok = false;
+        for (uint64_t i = 0; i < p.max_polls; ++i) {
+            if (dtt_dev::ld_acquire(w) >= target) { ok = true; break; }
             if ((i & 63) == 63 && *abort) return false;
             __nanosleep(ns);
             ns = ns < 256 ? ns + 32 : 256;
@@ -411,7 +435,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_consumer_kernel(const __grid_
             bool ok = true;
             for (uint32_t u = blockIdx.x; u < units && ok; u += gridDim.x) {
                 const uint32_t b = p.order[u / units_n];
-                if (!wait_chunks(p.h, p.c0[b], p.c1[b], p.max_polls, abort_flag)) { fail(); break; }
+                if (!wait_block(p, b, abort_flag)) { fail(); break; }
                 const int32_t row_x = (int32_t)(b * BM), row_w = (int32_t)((u % units_n) * TN);
                 for (uint32_t kb = 0; kb < kblocks; ++kb) {
                     if (!bar_wait(saddr(empty + stage), phase ^ 1, abort_flag)) { fail(); ok = false; break; }
@@ -775,7 +799,7 @@ gemm2_consumer_kernel(const __grid_constant__ ConsumerParams p) {
             bool ok = true;
             for (uint32_t u = c0; u < units && ok; u += NC) {
                 const uint32_t b = 2 * p.order2[u / units_n] + q;
-                if (!wait_chunks(p.h, p.c0[b], p.c1[b], p.max_polls, abort_flag)) { fail(); break; }
+                if (!wait_block(p, b, abort_flag)) { fail(); break; }
                 const int32_t row_a = (int32_t)(b * BM);
                 const int32_t row_b = (int32_t)((u % units_n) * G2_TN + q * BN);
                 for (uint32_t kb = 0; kb < kblocks; ++kb) {
@@ -1008,6 +1032,7 @@ int launch_gemm_consumer(const ConsumerLaunch& cl, cudaStream_t stream) {
     cp.c0 = cl.c0;
     cp.c1 = cl.c1;
     cp.order2 = cl.order2;
+    cp.bgroup = cl.bgroup;
     cp.D = cl.D;
     cp.ldd = cl.ldd;
     cp.max_polls = cl.max_polls;

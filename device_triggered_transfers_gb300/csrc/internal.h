@@ -132,6 +132,7 @@ struct CopierParams {
     uint64_t* go_host;
     uint64_t go_prior;
     uint64_t go_wait_ns;
+    const dtt_group_table* groups;   // device: the plan's chunk groups, or null
 };
 
 struct CheckParams {
@@ -204,6 +205,7 @@ struct ConsumerLaunch {
     const uint32_t* c0;
     const uint32_t* c1;
     const uint32_t* order2;     // pairs of row blocks in the order they are taken (pair form)
+    const uint32_t* bgroup;     // per block: its chunk group id (block groups), or null
     uint32_t blocks;
     uint64_t max_polls;
     uint32_t* err;

@@ -67,9 +67,20 @@ struct dtt_plan {
     cudaStream_t h2d_stream = nullptr;
     cudaStream_t d2h_stream = nullptr;
 
+    // chunk groups (dtt_plan_define_groups): the device table and its arrays, and the block size
+    // when they were defined by position (dtt_plan_define_block_groups; 0 otherwise)
+    uint32_t n_groups = 0;
+    std::vector<uint32_t> group_size;
+    std::vector<uint32_t> block_group;   // block -> group id (UINT32_MAX: no chunk touches it)
+    uint64_t group_block_bytes = 0;
+    dtt_group_table* d_group_table = nullptr;
+    uint64_t* d_group_counters = nullptr;
+    uint32_t* d_group_arrays = nullptr;   // size, chunk_off, chunk_ids back to back
+
     // consumer GEMM: per 128-row block of one rank's buffer seen as [rows, K], the order the
     // blocks are taken in and the chunk ids that cover each block (device, built on first use)
     uint32_t cons_rank = UINT32_MAX, cons_K = 0, cons_blocks = 0, cons_cap = 0;
+    bool cons_grouped = false;
     uint32_t* d_cons = nullptr;       // [3][blocks] + [blocks / 2 + 1]: order, c0, c1, order2
 
     cudaStream_t copy_stream = nullptr;
@@ -149,6 +160,12 @@ void free_device(dtt_plan* p) {
     if (p->h_arrived) cudaFreeHost(p->h_arrived);
     if (p->d_cons) cudaFree(p->d_cons);
     p->d_cons = nullptr;
+    cudaFree(p->d_group_table);
+    cudaFree(p->d_group_counters);
+    cudaFree(p->d_group_arrays);
+    p->d_group_table = nullptr;
+    p->d_group_counters = nullptr;
+    p->d_group_arrays = nullptr;
     p->ev_copier_end = nullptr;
     p->ev_h2d = nullptr;
     p->d2h_stream = nullptr;
@@ -348,6 +365,7 @@ dtt_handle make_handle(const dtt_plan* p, uint32_t r) {
     h.first_chunk = p->first_chunk[r];
     h.n_chunks = p->n_chunks[r];
     h.flags = p->opts.timestamps ? DTT_HANDLE_TIMESTAMPS : 0u;
+    h.groups = p->d_group_table;
     return h;
 }
 
@@ -372,6 +390,7 @@ CopierParams copier_params(const dtt_plan* p) {
     cp.tmaps = p->d_tmaps;
     cp.host_arrived = p->notify_host ? p->h_arrived_dev : nullptr;
     cp.stages = p->opts.stages;
+    cp.groups = p->d_group_table;
     return cp;
 }
 
@@ -922,7 +941,10 @@ int dtt_plan_wait(dtt_plan* p, dtt_report* report) {
         rc = fail(DTT_EEXTRA, "dtt_plan_wait: %u chunk(s) got extra marks in round %u (first: %u)",
                   rep.n_extra, p->round, rep.extra_chunks[0]);
     } else if (rep.device_status) {
-        rc = fail(DTT_EINVAL, "dtt_plan_wait: a kernel marked, or asked reusable of, a chunk its rank does not own");
+        rc = fail(DTT_EINVAL, "dtt_plan_wait: %s",
+                  (rep.device_status & DTT_DEV_EBADCHUNK)
+                      ? "a kernel marked, or asked reusable of, a chunk its rank does not own"
+                      : "a kernel waited on a group the plan does not have");
     } else if (rep.n_short) {
         rc = fail(DTT_ETIMEDOUT, "dtt_plan_wait: %u chunk(s) short in round %u (first: %u)",
                   rep.n_short, p->round, rep.short_chunks[0]);
@@ -1044,6 +1066,119 @@ int dtt_plan_stats(dtt_plan* p, double* copier_ms_last, double* copier_ms_total,
     if (copier_ms_last) *copier_ms_last = p->copier_ms_last;
     if (copier_ms_total) *copier_ms_total = p->copier_ms_total;
     if (rounds_timed) *rounds_timed = p->timed_read;
+    return DTT_OK;
+}
+
+int dtt_plan_define_groups(dtt_plan* p, uint32_t n_groups, const uint32_t* offsets, const uint32_t* chunk_ids) {
+    if (!p || !offsets || (!chunk_ids && offsets[n_groups]) || n_groups == 0)
+        return fail(DTT_EINVAL, "dtt_plan_define_groups: bad args");
+    if (p->n_groups) return fail(DTT_ESTATE, "dtt_plan_define_groups: the plan's groups are defined already");
+    if (p->state != DTT_PLAN_PREPARED || p->round != p->opts.initial_round || p->wait_seq || p->early_launched)
+        return fail(DTT_ESTATE, "dtt_plan_define_groups: groups are defined before the plan's first start");
+    if (offsets[0] != 0) return fail(DTT_EINVAL, "dtt_plan_define_groups: offsets[0] must be 0");
+    // per group: its members, distinct and in range; per chunk: the groups it belongs to (CSR)
+    std::vector<uint32_t> size(n_groups), chunk_off(p->n_global + 1, 0);
+    std::vector<uint32_t> seen(p->n_global, UINT32_MAX);
+    for (uint32_t g = 0; g < n_groups; ++g) {
+        if (offsets[g + 1] <= offsets[g])
+            return fail(DTT_EINVAL, "dtt_plan_define_groups: group %u is empty (or offsets decrease)", g);
+        for (uint32_t i = offsets[g]; i < offsets[g + 1]; ++i) {
+            const uint32_t c = chunk_ids[i];
+            if (c >= p->n_global) return fail(DTT_EINVAL, "dtt_plan_define_groups: chunk id %u out of range", c);
+            if (seen[c] == g) return fail(DTT_EINVAL, "dtt_plan_define_groups: chunk %u twice in group %u", c, g);
+            seen[c] = g;
+            ++chunk_off[c + 1];
+        }
+        size[g] = offsets[g + 1] - offsets[g];
+    }
+    for (uint32_t c = 0; c < p->n_global; ++c) chunk_off[c + 1] += chunk_off[c];
+    std::vector<uint32_t> ids(chunk_off[p->n_global]), fill(chunk_off.begin(), chunk_off.end() - 1);
+    for (uint32_t g = 0; g < n_groups; ++g)
+        for (uint32_t i = offsets[g]; i < offsets[g + 1]; ++i) ids[fill[chunk_ids[i]]++] = g;
+    // counters begin as after the rounds before this one
+    const uint64_t prior = p->round - 1;
+    std::vector<uint64_t> counters((uint64_t)p->P * n_groups);
+    for (uint32_t q = 0; q < p->P; ++q)
+        for (uint32_t g = 0; g < n_groups; ++g) counters[(uint64_t)q * n_groups + g] = prior * size[g];
+    std::vector<uint32_t> arrays;
+    arrays.reserve(size.size() + chunk_off.size() + ids.size() + 1);
+    arrays.insert(arrays.end(), size.begin(), size.end());
+    arrays.insert(arrays.end(), chunk_off.begin(), chunk_off.end());
+    arrays.insert(arrays.end(), ids.begin(), ids.end());
+    arrays.push_back(0);
+    // no copier of this plan runs yet; plain allocations and copies are ordered before its first
+    // start (on the legacy stream, which the plan's non-blocking streams do not wait for, so
+    // the copies are synchronous here)
+    DTT_CUDA_TRY(cudaMalloc(&p->d_group_counters, counters.size() * sizeof(uint64_t)));
+    DTT_CUDA_TRY(cudaMalloc(&p->d_group_arrays, arrays.size() * sizeof(uint32_t)));
+    DTT_CUDA_TRY(cudaMalloc(&p->d_group_table, sizeof(dtt_group_table)));
+    DTT_CUDA_TRY(cudaMemcpy(p->d_group_counters, counters.data(), counters.size() * sizeof(uint64_t),
+                            cudaMemcpyHostToDevice));
+    DTT_CUDA_TRY(cudaMemcpy(p->d_group_arrays, arrays.data(), arrays.size() * sizeof(uint32_t),
+                            cudaMemcpyHostToDevice));
+    dtt_group_table t{};
+    t.counters = p->d_group_counters;
+    t.size = p->d_group_arrays;
+    t.chunk_off = p->d_group_arrays + n_groups;
+    t.chunk_ids = p->d_group_arrays + n_groups + (p->n_global + 1);
+    t.n_groups = n_groups;
+    DTT_CUDA_TRY(cudaMemcpy(p->d_group_table, &t, sizeof(t), cudaMemcpyHostToDevice));
+    p->n_groups = n_groups;
+    p->group_size = size;
+    return DTT_OK;
+}
+
+int dtt_plan_define_block_groups(dtt_plan* p, uint64_t block_bytes, uint32_t* n_groups, uint32_t* block_group) {
+    if (!p || block_bytes == 0) return fail(DTT_EINVAL, "dtt_plan_define_block_groups: bad args");
+    const uint64_t nb = (p->buf_bytes + block_bytes - 1) / block_bytes;
+    if (nb > 0xFFFFFFF0ull) return fail(DTT_EINVAL, "dtt_plan_define_block_groups: too many blocks");
+    // the blocks each chunk touches, from the copier's pieces (every row of every piece)
+    std::vector<std::vector<uint32_t>> members(nb);
+    for (uint32_t c = 0; c < p->n_global; ++c) {
+        const ChunkDesc& cd = p->chunks[c];
+        uint64_t last = UINT64_MAX;
+        std::vector<uint64_t> touched;
+        for (uint32_t i = 0; i < cd.n_pieces; ++i) {
+            const PieceDesc& pc = p->pieces[cd.piece_begin + i];
+            for (uint32_t r = 0; r < pc.rows; ++r) {
+                const uint64_t lo = pc.off + (uint64_t)r * pc.pitch, hi = lo + pc.row_bytes;
+                for (uint64_t b = lo / block_bytes; b * block_bytes < hi; ++b)
+                    if (b != last) {
+                        touched.push_back(b);
+                        last = b;
+                    }
+            }
+        }
+        std::sort(touched.begin(), touched.end());
+        touched.erase(std::unique(touched.begin(), touched.end()), touched.end());
+        for (uint64_t b : touched) members[b].push_back(c);
+    }
+    std::vector<uint32_t> offsets(1, 0), ids, bg(nb, UINT32_MAX);
+    for (uint64_t b = 0; b < nb; ++b) {
+        if (members[b].empty()) continue;
+        bg[b] = (uint32_t)(offsets.size() - 1);
+        ids.insert(ids.end(), members[b].begin(), members[b].end());
+        offsets.push_back((uint32_t)ids.size());
+    }
+    if (offsets.size() < 2) return fail(DTT_EINVAL, "dtt_plan_define_block_groups: no chunk touches any block");
+    const int rc = dtt_plan_define_groups(p, (uint32_t)(offsets.size() - 1), offsets.data(), ids.data());
+    if (rc != DTT_OK) return rc;
+    p->group_block_bytes = block_bytes;
+    p->block_group = bg;
+    if (n_groups) *n_groups = p->n_groups;
+    if (block_group) std::copy(bg.begin(), bg.end(), block_group);
+    return DTT_OK;
+}
+
+int dtt_plan_read_group_counters(dtt_plan* p, uint64_t* host, uint64_t n_words) {
+    if (!p || !host) return fail(DTT_EINVAL, "dtt_plan_read_group_counters: bad args");
+    if (!p->n_groups) return fail(DTT_EINVAL, "dtt_plan_read_group_counters: the plan has no groups");
+    const uint64_t need = (uint64_t)p->P * p->n_groups;
+    if (n_words < need)
+        return fail(DTT_EINVAL, "dtt_plan_read_group_counters: need %llu words", (unsigned long long)need);
+    DTT_CUDA_TRY(cudaMemcpyAsync(host, p->d_group_counters, need * sizeof(uint64_t), cudaMemcpyDeviceToHost,
+                                 p->aux_stream));
+    DTT_CUDA_TRY(cudaStreamSynchronize(p->aux_stream));
     return DTT_OK;
 }
 
@@ -1287,7 +1422,10 @@ int dtt_gemm_consumer(dtt_plan* p, uint32_t rank, const void* Wt, uint32_t N, ui
         return fail(DTT_EINVAL, "dtt_gemm_consumer: bad ldd or alignment");
     const uint64_t rows = p->buf_bytes / row_bytes;
     const uint32_t blocks = (uint32_t)(rows / 128);
-    if (!p->d_cons || p->cons_rank != rank || p->cons_K != K) {
+    // with block groups of this block size, each block is one group wait
+    const bool grouped = p->n_groups && p->group_block_bytes == 128 * row_bytes &&
+                         p->block_group.size() >= blocks;
+    if (!p->d_cons || p->cons_rank != rank || p->cons_K != K || p->cons_grouped != grouped) {
         // which chunks cover each block, and the blocks in the order their chunks open: by the
         // chunk's place in its rank's schedule, then by rank
         std::vector<uint64_t> lo, hi;
@@ -1315,12 +1453,14 @@ int dtt_gemm_consumer(dtt_plan* p, uint32_t rank, const void* Wt, uint32_t N, ui
         }
         std::stable_sort(order2.begin(), order2.end(), [&](uint32_t x, uint32_t y) { return late[x] < late[y]; });
         std::vector<uint32_t> table;
-        table.reserve(3 * (size_t)blocks + blocks / 2 + 1);
+        table.reserve(4 * (size_t)blocks + blocks / 2 + 1);
         table.insert(table.end(), order.begin(), order.end());
         table.insert(table.end(), c0.begin(), c0.end());
         table.insert(table.end(), c1.begin(), c1.end());
         table.insert(table.end(), order2.begin(), order2.end());
         table.push_back(0);
+        if (grouped) table.insert(table.end(), p->block_group.begin(), p->block_group.begin() + blocks);
+        else table.insert(table.end(), blocks, 0u);
         if (p->d_cons && p->cons_cap < blocks) {
             DTT_CUDA_TRY(cudaFreeAsync(p->d_cons, stream));
             p->d_cons = nullptr;
@@ -1335,6 +1475,7 @@ int dtt_gemm_consumer(dtt_plan* p, uint32_t rank, const void* Wt, uint32_t N, ui
                                      cudaMemcpyHostToDevice, stream));
         p->cons_rank = rank;
         p->cons_K = K;
+        p->cons_grouped = grouped;
     }
     ConsumerLaunch cl{};
     cl.X = p->bufs[rank];
@@ -1349,6 +1490,7 @@ int dtt_gemm_consumer(dtt_plan* p, uint32_t rank, const void* Wt, uint32_t N, ui
     cl.c0 = p->d_cons + p->cons_blocks;
     cl.c1 = p->d_cons + 2 * (size_t)p->cons_blocks;
     cl.order2 = p->d_cons + 3 * (size_t)p->cons_blocks;
+    cl.bgroup = grouped ? p->d_cons + 3 * (size_t)p->cons_blocks + p->cons_blocks / 2 + 1 : nullptr;
     cl.blocks = blocks;
     cl.max_polls = max_polls ? max_polls : p->opts.max_polls;
     cl.err = err;

@@ -219,6 +219,23 @@ void dtt_plan_opts_default(dtt_plan_opts* opts);
 #define DTT_HANDLE_TIMESTAMPS 1u   /* dtt_handle.flags bit: stamp gate-open times */
 #define DTT_DEV_EBADCHUNK 1u       /* device status bit: a rank marked (or asked dtt_reusable of)
                                       a chunk it does not own */
+#define DTT_DEV_EBADGROUP 2u       /* device status bit: a wait named a group the plan lacks */
+
+/* A plan's chunk groups on the device (dtt_plan_define_groups), owned by the plan.  A group is a
+ * set of global chunk ids, of any source ranks.  Each virtual rank q has one counter per group,
+ * counters[q * n_groups + g], that goes up by one whenever a member becomes readable at q: the
+ * copier adds one when it signals a member's arrival at q, and the mark that opens a member's
+ * gate adds one at its own rank.  So after R rounds every counter holds R * size[g], and a wait
+ * on group g passes at round * size[g] ("Triggered Plans", Not supported yet: "Waiting on a
+ * group" -- no single counter covers several chunks or several source ranks). */
+typedef struct dtt_group_table {
+    uint64_t* counters;          /* [P][n_groups], monotonic, never reset */
+    const uint32_t* size;        /* [n_groups] members per group */
+    const uint32_t* chunk_off;   /* [n_global + 1]: chunk c's groups are */
+    const uint32_t* chunk_ids;   /*   chunk_ids[chunk_off[c] .. chunk_off[c + 1]) */
+    uint32_t n_groups;
+    uint32_t reserved;
+} dtt_group_table;
 
 /* Device-side view of a plan for one rank and one round, passed by value to producer and
  * consumer kernels (the pages' TriggeredView handle).  Plain data; valid until the next
@@ -235,6 +252,7 @@ typedef struct dtt_handle {
     uint32_t n_chunks;        /* this rank's chunk count */
     uint32_t flags;           /* bit 0: timestamps */
     uint32_t reserved;
+    const dtt_group_table* groups;   /* device: the plan's groups, or NULL (none defined) */
 } dtt_handle;
 
 /* Gate row: 64 bytes = 8 uint64 words per (rank, global chunk) ("Triggered Plans", Gates and
@@ -349,6 +367,30 @@ int dtt_plan_info(const dtt_plan* plan, uint32_t* n_global, uint32_t* first_chun
  * adds no synchronisation to a round.  Any pointer may be NULL.  Errors: DTT_EINVAL, DTT_ECUDA. */
 int dtt_plan_stats(dtt_plan* plan, double* copier_ms_last, double* copier_ms_total,
                    uint64_t* rounds_timed);
+
+/* Define the plan's chunk groups ("Triggered Plans", Not supported yet: "Waiting on a group";
+ * see dtt_group_table): group g holds the global chunk ids chunk_ids[offsets[g] ..
+ * offsets[g + 1]) (host arrays; offsets has n_groups + 1 entries, offsets[0] = 0).  A chunk may
+ * belong to several groups; within a group ids are distinct.  Kernels then wait once per group
+ * with dtt_wait_group.  Allowed once per plan, before its first dtt_plan_start; the counters
+ * begin as after the rounds before opts.initial_round.  The tables live on the device until the
+ * plan is closed.  Errors: DTT_EINVAL (empty group, id out of range or repeated in a group,
+ * n_groups == 0), DTT_ESTATE (started already, or groups defined already), DTT_ECUDA. */
+int dtt_plan_define_groups(dtt_plan* plan, uint32_t n_groups, const uint32_t* offsets,
+                           const uint32_t* chunk_ids);
+
+/* Groups by position: group b holds every chunk with a byte in [b * block_bytes, (b + 1) *
+ * block_bytes) of the buffers, b = 0 .. ceil(buf_bytes / block_bytes) - 1 (for example the
+ * 128-row blocks a consumer GEMM loads: block_bytes = 128 rows x row bytes).  A block no chunk
+ * touches gets no group of its own: *n_groups (may be NULL) receives the count and block_group
+ * (host, may be NULL, ceil(buf_bytes / block_bytes) entries) each block's group id, or
+ * UINT32_MAX.  Otherwise as dtt_plan_define_groups. */
+int dtt_plan_define_block_groups(dtt_plan* plan, uint64_t block_bytes, uint32_t* n_groups,
+                                 uint32_t* block_group);
+
+/* Copy the group counters (P * n_groups uint64, rank-major) to host memory and wait for the
+ * copy.  Errors: DTT_EINVAL (no groups, n_words short), DTT_ECUDA. */
+int dtt_plan_read_group_counters(dtt_plan* plan, uint64_t* host, uint64_t n_words);
 
 /* Counts of a plan's early copiers (opts.early_copier_us) so far: launched by dtt_plan_wait,
  * claimed by the next dtt_plan_start, found by the host to have given their round up (start then

@@ -1,5 +1,6 @@
 /*
- * dtt_device.cuh -- device side of a triggered plan: mark_ready, arrived, wait, reusable.
+ * dtt_device.cuh -- device side of a triggered plan: mark_ready, arrived, wait, reusable and
+ * the group waits.
  *
  * Include from producer and consumer kernels; the kernel receives a dtt_handle (include/dtt.h)
  * by value.  Every function here is called by ALL threads of a CTA (dtt_mark_ready_cluster:
@@ -19,6 +20,9 @@
  *    Polls are counted, never clock-bounded.
  *  - reusable: thread 0 acquires the chunk's completion word, which the copier bumps with a
  *    release add after every copy of the chunk has landed (and so after its reads of it).
+ *  - groups: the copier's arrival signal at a peer and the mark that opens a gate are followed
+ *    by a release add on that rank's counters of the chunk's groups; dtt_wait_group acquires the
+ *    counter, so data of every member read after it is this round's.
  *  - A producer that writes through the async proxy (TMA stores) must complete those writes
  *    (cp.async.bulk.wait_group 0) and issue fence.proxy.async before calling mark_ready.
  */
@@ -79,6 +83,15 @@ __device__ __forceinline__ uint64_t* gate_row(const dtt_handle& h, uint32_t tabl
     return h.gates + ((uint64_t)table * h.n_global + chunk) * DTT_GATE_WORDS;
 }
 
+/* Chunk `chunk` became readable at rank `rank`: one release add on each of that rank's counters
+ * of the chunk's groups (none when the plan has no groups). */
+__device__ __forceinline__ void count_groups(const dtt_group_table* g, uint32_t rank, uint32_t chunk) {
+    if (!g) return;
+    const uint32_t a = g->chunk_off[chunk], b = g->chunk_off[chunk + 1];
+    uint64_t* row = g->counters + (uint64_t)rank * g->n_groups;
+    for (uint32_t i = a; i < b; ++i) red_release_add(row + g->chunk_ids[i], 1);
+}
+
 /* One writer's mark, issued by one thread after the caller's barrier. */
 __device__ __forceinline__ void mark_one(const dtt_handle& h, uint32_t chunk) {
     if (chunk < h.first_chunk || chunk >= h.first_chunk + h.n_chunks) {
@@ -91,9 +104,21 @@ __device__ __forceinline__ void mark_one(const dtt_handle& h, uint32_t chunk) {
     if (now == target) {
         if (h.flags & DTT_HANDLE_TIMESTAMPS) st_relaxed(row + DTT_GATE_T_OPEN, globaltimer());
         st_release(row + DTT_GATE_READY, h.round);
+        count_groups(h.groups, h.rank, chunk);     // readable at its own rank from now on
     } else if (now > target) {
         red_relaxed_max(row + DTT_GATE_ERROR, h.round);
     }
+}
+
+/* The counter a rank polls for group g and the count that completes this round; null when the
+ * plan has no group g (a misuse bit is set). */
+__device__ __forceinline__ const uint64_t* group_word(const dtt_handle& h, uint32_t g, uint64_t* target) {
+    if (!h.groups || g >= h.groups->n_groups) {
+        atomicOr(h.status, DTT_DEV_EBADGROUP);
+        return nullptr;
+    }
+    *target = (uint64_t)h.round * h.groups->size[g];
+    return h.groups->counters + (uint64_t)h.rank * h.groups->n_groups + g;
 }
 
 /* The word a rank polls for `chunk`: its own chunks are local once ready; other ranks' chunks
@@ -155,6 +180,43 @@ __device__ __forceinline__ int dtt_wait(const dtt_handle& h, uint32_t chunk, uin
     }
     __syncthreads();
     return dtt_wait_result;
+}
+
+/* One poll of group g ("Triggered Plans", Not supported yet: "Waiting on a group"): has every
+ * chunk of the group become readable here this round (other ranks' chunks arrived, this rank's
+ * own chunks ready)?  A group the plan does not have sets DTT_DEV_EBADGROUP and reads false. */
+__device__ __forceinline__ bool dtt_group_arrived(const dtt_handle& h, uint32_t g) {
+    __shared__ int dtt_group_arrived_flag;
+    __syncthreads();
+    if (dtt_dev::first_thread()) {
+        uint64_t target = 0;
+        const uint64_t* w = dtt_dev::group_word(h, g, &target);
+        dtt_group_arrived_flag = w && dtt_dev::ld_acquire(w) >= target;
+    }
+    __syncthreads();
+    return dtt_group_arrived_flag != 0;
+}
+
+/* Wait until dtt_group_arrived(h, g), polling one counter at most max_polls times: one wait
+ * covers every chunk of the group, of any source rank.  Returns 0, or DTT_ETIMEDOUT if the polls
+ * ran out (or the plan has no group g).  Data read after it is this round's. */
+__device__ __forceinline__ int dtt_wait_group(const dtt_handle& h, uint32_t g, uint64_t max_polls) {
+    __shared__ int dtt_wait_group_result;
+    __syncthreads();
+    if (dtt_dev::first_thread()) {
+        uint64_t target = 0;
+        const uint64_t* w = dtt_dev::group_word(h, g, &target);
+        int r = DTT_ETIMEDOUT;
+        uint32_t ns = 0;
+        for (uint64_t i = 0; w && i < max_polls; ++i) {
+            if (dtt_dev::ld_acquire(w) >= target) { r = 0; break; }
+            __nanosleep(ns);
+            ns = ns < 256 ? ns + 32 : 256;
+        }
+        dtt_wait_group_result = r;
+    }
+    __syncthreads();
+    return dtt_wait_group_result;
 }
 
 /* Source side ("Triggered SDMA Plans", API: the device view's `reusable`; Design notes: the

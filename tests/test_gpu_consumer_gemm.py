@@ -131,3 +131,79 @@ def test_consumer_gemm_full_size_bench_launch():
             st.plan.next_round()
     finally:
         st.plan.close()
+
+
+def _oracle_block_groups(o, block_bytes, nbytes):
+    """The oracle's groups by position: block b holds every chunk with a byte in it (from the
+    oracle's own chunk regions, row by row)."""
+    nb = -(-nbytes // block_bytes)
+    members = [[] for _ in range(nb)]
+    for c, ch in enumerate(o.chunks):
+        touched = set()
+        for (off, rb, rows, pitch) in ch.regions:
+            for i in range(rows):
+                lo = off + i * pitch
+                touched.update(range(lo // block_bytes, (lo + rb - 1) // block_bytes + 1))
+        for b in touched:
+            members[b].append(c)
+    ids, groups = [], []
+    for b in range(nb):
+        if members[b]:
+            ids.append(len(groups))
+            groups.append(sorted(members[b]))
+        else:
+            ids.append(None)
+    return groups, ids
+
+
+GROUPED = {
+    # chunks of exactly one 128-row block each; the pair form
+    "chunks_pair": (W.small(W.C2, M=512, N=1024, num_chunks=4, rounds=3), 0, 256, 0),
+    # 80-row chunks: blocks straddle two chunks and chunks two blocks; the one-CTA form
+    "chunks_straddle": (W.small(W.C2, M=160, N=1024, num_chunks=2, rounds=3), 1, 256, 0),
+    # tiles in the grouped order: a chunk's tiles lie in several blocks, a block's in several chunks
+    "tiles_grouped": (W.Workload("tg", P=2, M=256, N=1024, dtype=W.BF16, kind="tile_chunks", rounds=3,
+                                 seed=41, BM=64, BN=256, num_programs=3, tiles_per_chunk=3, group_m=2),
+                      1, 384, 7),
+}
+
+
+@pytest.mark.parametrize("name", sorted(GROUPED))
+def test_consumer_gemm_with_block_groups(name):
+    # "Triggered Plans", Not supported yet, "Waiting on a group": one group per 128-row block of
+    # X, so the GEMM waits once per block.  The groups equal the oracle's blocks-by-position, the
+    # counters the oracle's after every round, and D the oracle's fp64 product
+    w, q, N2, programs = GROUPED[name]
+    K = w.N
+    rows = w.buf_bytes // (2 * K)
+    Wt = _weights(N2, K, 91)
+    Wt_dev = Wt.cuda()
+    out = torch.zeros(rows, N2, dtype=torch.bfloat16, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    cons = torch.cuda.Stream()
+    st = runner.make(w)
+    o = oracle_plan(w)
+    groups, ids = _oracle_block_groups(o, 128 * 2 * K, w.buf_bytes)
+    n, bg = st.plan.define_block_groups(128 * 2 * K)
+    assert n == len(groups) and bg == ids
+    o.define_groups(groups)
+    Wt64 = Wt.to(torch.float64).numpy()
+    torch.cuda.synchronize()
+    try:
+        for R in (1, 2, 3):
+            h = st.plan.start(st.producer_stream)
+            st.plan.gemm_consumer(q, Wt_dev, out, N2, K, err, num_programs=programs, stream=cons)
+            D.dtt_fill_producer(st.buf_ptrs, st.desc, h, st.producer_stream)
+            rep = st.plan.wait()
+            cons.synchronize()
+            assert rep.status == D.OK and int(err.item()) == 0 and rep.device_status == 0
+            assert oracle_round(o, w)[0] == OP.OK
+            np.testing.assert_array_equal(st.plan.read_group_counters(), o.group_counters)
+            X = torch.from_numpy(o.bufs[q].copy()).view(torch.bfloat16).view(rows, K)
+            ref = OG.product(X.to(torch.float64).numpy(), Wt64)
+            e = OG.rel_frobenius(out.cpu().to(torch.float64).numpy(), ref)
+            assert e <= TOL and e < 5e-3, (R, e)
+            st.plan.next_round()
+            o.next_round()
+    finally:
+        st.plan.close()

@@ -39,6 +39,11 @@ def _build():
                                C.c_void_p]
     lib.user_produce_reverse.argtypes = [C.POINTER(D.dtt_handle), C.c_void_p, C.c_uint64, C.c_uint64,
                                          C.c_void_p]
+    lib.user_group_consume.argtypes = [C.POINTER(D.dtt_handle), C.c_uint32, C.c_void_p, C.c_void_p,
+                                       C.c_uint64, C.c_void_p, C.c_void_p, C.c_uint64, C.c_void_p,
+                                       C.c_void_p]
+    lib.user_group_probe_launch.argtypes = [C.POINTER(D.dtt_handle), C.c_uint32, C.c_uint32, C.c_void_p,
+                                            C.c_void_p]
     return lib
 
 
@@ -214,5 +219,86 @@ def test_out_of_order_producer_head_of_line(method):
                             assert int(g[q, head + k, D.GATE_T_ARRIVE]) >= t_head, (rnd, r, k, q)
             plan.next_round()
             o.next_round()
+    finally:
+        plan.close()
+
+
+def test_group_waits_in_a_users_consumer_kernel():
+    # "Triggered Plans", Not supported yet, "Waiting on a group": groups of chunks from several
+    # source ranks (one of them the consumer's own), one wait each, in a consumer kernel launched
+    # before the producers on a third stream.  Every group's data is this round's; the group
+    # counters equal the oracle's (R * |g| at every rank); asking an undefined group is a misuse
+    # that wait reports.
+    from oracle import plan as OP
+    from oracle import schedule as OS
+    lib = _build()
+    assert lib.user_kernels_prepare() == 0
+    P, n, chunk = 3, 4, 1 << 18
+    S = n * chunk
+    bufs = [torch.zeros(P * S, dtype=torch.uint8, device="cuda") for _ in range(P)]
+    scheds = [D.dtt_schedule_chunks(r * S, n, chunk, chunk, n) for r in range(P)]
+    plan = D.Plan(bufs, P * S, scheds, D.dtt_plan_opts_default(method=D.COPY_TMA, piece_bytes=65536, stages=3))
+    for s_ in scheds:
+        s_.free()
+    groups = [[0, 4, 8], [1, 2, 3], list(range(P * n)), [7], [11, 5, 9, 1]]
+    assert plan.define_groups(groups) == len(groups)
+    with pytest.raises(D.DttError) as e:
+        plan.define_groups(groups)                       # once per plan
+    assert e.value.code == D.ESTATE
+    o = OP.Plan([np.zeros(P * S, dtype=np.uint8) for _ in range(P)],
+                [OS.chunks(r * S, n, chunk, chunk, n) for r in range(P)])
+    o.define_groups(groups)
+    goff = torch.tensor(np.cumsum([0] + [len(g) for g in groups]), dtype=torch.int32, device="cuda")
+    gids = torch.tensor([c for g in groups for c in g], dtype=torch.int32, device="cuda")
+    prod, cons = torch.cuda.Stream(), torch.cuda.Stream()
+    dst = [torch.zeros(P * S, dtype=torch.uint8, device="cuda") for _ in range(P)]
+    status = torch.full((P, len(groups)), 99, dtype=torch.int32, device="cuda")
+    probe = torch.full((len(groups),), 7, dtype=torch.int32, device="cuda")
+    torch.cuda.synchronize()
+    try:
+        for rnd in (1, 2, 3):
+            h = plan.start(prod)
+            assert lib.user_group_probe_launch(C.byref(h[0]), 0, len(groups), C.c_void_p(probe.data_ptr()),
+                                               C.c_void_p(prod.cuda_stream)) == 0
+            for q in range(P):
+                assert lib.user_group_consume(C.byref(h[q]), len(groups), C.c_void_p(bufs[q].data_ptr()),
+                                              C.c_void_p(dst[q].data_ptr()), chunk, C.c_void_p(goff.data_ptr()),
+                                              C.c_void_p(gids.data_ptr()), 1 << 24,
+                                              C.c_void_p(status[q].data_ptr()), C.c_void_p(cons.cuda_stream)) == 0
+            for r in range(P):
+                assert lib.user_produce(C.byref(h[r]), C.c_void_p(bufs[r].data_ptr() + r * S), chunk,
+                                        C.c_void_p(prod.cuda_stream)) == 0
+            rep = plan.wait()
+            cons.synchronize()
+            assert rep.status == D.OK and rep.device_status == 0
+            assert probe.cpu().tolist() == [0] * len(groups)      # before this round's marks
+            assert status.cpu().tolist() == [[0] * len(groups)] * P
+            want = np.concatenate([_values(r, rnd, S) for r in range(P)])
+            for q in range(P):
+                got = dst[q].cpu().numpy()
+                for g in groups:
+                    for c in g:
+                        np.testing.assert_array_equal(got[c * chunk:(c + 1) * chunk], want[c * chunk:(c + 1) * chunk])
+            o.start()
+            for r in range(P):
+                o.bufs[r][r * S:(r + 1) * S] = _values(r, rnd, S)
+                for c in o.chunks_of(r):
+                    o.mark_ready(r, c)
+            o.copier_progress()
+            assert o.wait()[0] == OP.OK
+            np.testing.assert_array_equal(plan.read_group_counters(), o.group_counters)
+            np.testing.assert_array_equal(plan.read_gates()[:, :, :5], o.gates)
+            plan.next_round()
+            o.next_round()
+        # a group the plan does not have: the wait gives up at once and wait() reports the misuse
+        h = plan.start(prod)
+        assert lib.user_group_probe_launch(C.byref(h[1]), len(groups), 1, C.c_void_p(probe.data_ptr()),
+                                           C.c_void_p(prod.cuda_stream)) == 0
+        for r in range(P):
+            assert lib.user_produce(C.byref(h[r]), C.c_void_p(bufs[r].data_ptr() + r * S), chunk,
+                                    C.c_void_p(prod.cuda_stream)) == 0
+        rep = plan.wait(raise_on_error=False)
+        assert rep.status == D.EINVAL and rep.device_status & 2
+        assert int(probe[0].item()) == 0
     finally:
         plan.close()

@@ -80,6 +80,28 @@ __global__ void user_producer_reverse(dtt_handle h, uint8_t* slice, uint64_t chu
     }
 }
 
+// Group consumer ("Triggered Plans", Not supported yet, "Waiting on a group"): CTA g waits ONCE
+// on group g (members gids[goff[g] .. goff[g + 1]), global chunk c covering bytes
+// [c * chunk_bytes, (c + 1) * chunk_bytes) of every buffer), then copies every member to dst.
+__global__ void user_group_consumer(dtt_handle h, const uint8_t* buf, uint8_t* dst, uint64_t chunk_bytes,
+                                    const uint32_t* goff, const uint32_t* gids, uint64_t max_polls,
+                                    int32_t* status) {
+    const uint32_t g = blockIdx.x;
+    const int r = dtt_wait_group(h, g, max_polls);
+    if (threadIdx.x == 0) status[g] = r;
+    if (r != 0) return;
+    for (uint32_t i = goff[g]; i < goff[g + 1]; ++i) {
+        const uint64_t base = (uint64_t)gids[i] * chunk_bytes;
+        for (uint64_t x = threadIdx.x; x < chunk_bytes; x += blockDim.x) dst[base + x] = buf[base + x];
+    }
+}
+
+// CTA i records dtt_group_arrived of group first + i.
+__global__ void user_group_probe(dtt_handle h, uint32_t first, int32_t* out) {
+    const bool a = dtt_group_arrived(h, first + blockIdx.x);
+    if (threadIdx.x == 0) out[blockIdx.x] = a ? 1 : 0;
+}
+
 // CTA i asks dtt_reusable of global chunk first + i.
 __global__ void user_probe_reusable(dtt_handle h, uint32_t first, int32_t* out) {
     const bool r = dtt_reusable(h, first + blockIdx.x);
@@ -104,6 +126,11 @@ extern "C" int user_kernels_prepare(void) {
     if (cudaFuncSetAttribute(user_producer_reverse, cudaFuncAttributePreferredSharedMemoryCarveout,
                              cudaSharedmemCarveoutMaxShared) != cudaSuccess)
         return 1;
+    if (cudaFuncGetAttributes(&a, user_group_consumer) != cudaSuccess) return 1;
+    if (cudaFuncSetAttribute(user_group_consumer, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared) != cudaSuccess)
+        return 1;
+    if (cudaFuncGetAttributes(&a, user_group_probe) != cudaSuccess) return 1;
     if (cudaFuncGetAttributes(&a, user_producer_paced) != cudaSuccess) return 1;
     if (cudaFuncGetAttributes(&a, user_probe_reusable) != cudaSuccess) return 1;
     if (cudaFuncSetAttribute(user_producer_paced, cudaFuncAttributePreferredSharedMemoryCarveout,
@@ -143,5 +170,20 @@ extern "C" int user_produce_reverse(const dtt_handle* h, void* slice, uint64_t c
                                     cudaStream_t s) {
     if (h->n_chunks == 0) return 0;
     user_producer_reverse<<<1, 256, 0, s>>>(*h, static_cast<uint8_t*>(slice), chunk_bytes, spin_ns);
+    return cudaGetLastError() == cudaSuccess ? 0 : 1;
+}
+
+extern "C" int user_group_consume(const dtt_handle* h, uint32_t n_groups, const void* buf, void* dst,
+                                  uint64_t chunk_bytes, const uint32_t* goff, const uint32_t* gids,
+                                  uint64_t max_polls, int32_t* status, cudaStream_t s) {
+    user_group_consumer<<<n_groups, 256, 0, s>>>(*h, static_cast<const uint8_t*>(buf), static_cast<uint8_t*>(dst),
+                                                 chunk_bytes, goff, gids, max_polls, status);
+    return cudaGetLastError() == cudaSuccess ? 0 : 1;
+}
+
+extern "C" int user_group_probe_launch(const dtt_handle* h, uint32_t first, uint32_t n, int32_t* out,
+                                       cudaStream_t s) {
+    if (n == 0) return 0;
+    user_group_probe<<<n, 64, 0, s>>>(*h, first, out);
     return cudaGetLastError() == cudaSuccess ? 0 : 1;
 }
