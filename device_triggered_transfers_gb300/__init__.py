@@ -58,11 +58,16 @@ class dtt_plan_opts(C.Structure):
                 ("early_copier_us", C.c_uint32)]
 
 
+class dtt_group_table(C.Structure):
+    _fields_ = [("counters", C.c_void_p), ("size", C.c_void_p), ("chunk_off", C.c_void_p),
+                ("chunk_ids", C.c_void_p), ("n_groups", C.c_uint32), ("reserved", C.c_uint32)]
+
+
 class dtt_handle(C.Structure):
     _fields_ = [("gates", C.c_void_p), ("writers", C.c_void_p), ("status", C.c_void_p),
                 ("round", C.c_uint32), ("rank", C.c_uint32), ("P", C.c_uint32),
                 ("n_global", C.c_uint32), ("first_chunk", C.c_uint32), ("n_chunks", C.c_uint32),
-                ("flags", C.c_uint32), ("reserved", C.c_uint32), ("groups", C.c_void_p)]
+                ("flags", C.c_uint32), ("reserved", C.c_uint32), ("groups", dtt_group_table)]
 
 
 class dtt_report(C.Structure):

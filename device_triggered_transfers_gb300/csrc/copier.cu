@@ -47,6 +47,40 @@ __device__ __forceinline__ void notify_host(const CopierParams& p, uint32_t c) {
         asm volatile("st.release.sys.global.u32 [%0], %1;" ::"l"(p.host_arrived + c), "r"(p.round) : "memory");
 }
 
+// Chunk c of source s has landed at every peer: per peer its arrival signal (and time stamp) and
+// the peer's counters of the chunk's groups, then the source's completion word and the host
+// stamp.  The chunk's group ids are read first; then ONE release fence covers every signal (a
+// fence followed by relaxed writes is a release pattern in the PTX memory model): it orders
+// every copy of the chunk -- this thread's, or those acquired from the CTAs that made them
+// through the piece counter -- before each of them.
+__device__ __forceinline__ void signal_arrivals(const CopierParams& p, uint32_t s, uint32_t c) {
+    constexpr uint32_t kIdsInRegs = 4;
+    uint32_t ga = 0, gb = 0, ids[kIdsInRegs];
+    if (p.groups.counters) {
+        ga = p.groups.chunk_off[c];
+        gb = p.groups.chunk_off[c + 1];
+#pragma unroll
+        for (uint32_t j = 0; j < kIdsInRegs; ++j) ids[j] = ga + j < gb ? p.groups.chunk_ids[ga + j] : 0;
+    }
+    dtt_dev::fence_acq_rel();
+    for (uint32_t q = 0; q < p.P; ++q) {
+        if (q == s) continue;
+        uint64_t* prow = p.gates + ((uint64_t)q * p.n_global + c) * DTT_GATE_WORDS;
+        if (p.flags & DTT_HANDLE_TIMESTAMPS) dtt_dev::st_relaxed(prow + DTT_GATE_T_ARRIVE, dtt_dev::globaltimer());
+        dtt_dev::red_relaxed_add(prow + DTT_GATE_ARRIVAL, 1);
+        if (gb > ga) {
+            uint64_t* grow = p.groups.counters + (uint64_t)q * p.groups.n_groups;
+#pragma unroll
+            for (uint32_t j = 0; j < kIdsInRegs; ++j)
+                if (ga + j < gb) dtt_dev::red_relaxed_add(grow + ids[j], 1);
+            for (uint32_t i = ga + kIdsInRegs; i < gb; ++i) dtt_dev::red_relaxed_add(grow + p.groups.chunk_ids[i], 1);
+        }
+    }
+    uint64_t* row = p.gates + ((uint64_t)s * p.n_global + c) * DTT_GATE_WORDS;
+    dtt_dev::red_relaxed_add(row + DTT_GATE_COMPLETION, p.P - 1);
+    notify_host(p, c);
+}
+
 // Copy one piece from buffer s to every other buffer: 16-byte vectors, kUnroll loads in
 // flight per thread, each value stored to all peers.
 __device__ __forceinline__ void copy_piece_vec(const CopierParams& p, uint32_t s,
@@ -148,19 +182,7 @@ __device__ __forceinline__ void copier_body(const CopierParams& p) {
         if (threadIdx.x == 0) {
             uint64_t* row = p.gates + ((uint64_t)s * p.n_global + c) * DTT_GATE_WORDS;
             const uint64_t done = dtt_dev::atom_add_acq_rel(row + DTT_GATE_COPIER, 1) + 1;
-            if (done == (uint64_t)p.round * cd.n_part) {
-                // last piece of the chunk: signal arrival at every peer
-                for (uint32_t q = 0; q < p.P; ++q) {
-                    if (q == s) continue;
-                    uint64_t* prow = p.gates + ((uint64_t)q * p.n_global + c) * DTT_GATE_WORDS;
-                    if (p.flags & DTT_HANDLE_TIMESTAMPS)
-                        dtt_dev::st_relaxed(prow + DTT_GATE_T_ARRIVE, dtt_dev::globaltimer());
-                    dtt_dev::red_release_add(prow + DTT_GATE_ARRIVAL, 1);
-                    dtt_dev::count_groups(p.groups, q, c);
-                }
-                dtt_dev::red_release_add(row + DTT_GATE_COMPLETION, p.P - 1);
-                notify_host(p, c);
-            }
+            if (done == (uint64_t)p.round * cd.n_part) signal_arrivals(p, s, c);   // the chunk's last piece
         }
     }
 }
@@ -421,18 +443,7 @@ __device__ __forceinline__ void copier_bulk_body(const CopierParams& p) {
         if (failed) break;
         uint64_t* row = p.gates + ((uint64_t)s * p.n_global + c) * DTT_GATE_WORDS;
         const uint64_t done = dtt_dev::atom_add_acq_rel(row + DTT_GATE_COPIER, 1) + 1;
-        if (done == (uint64_t)p.round * cd.n_part) {
-            for (uint32_t q = 0; q < p.P; ++q) {
-                if (q == s) continue;
-                uint64_t* prow = p.gates + ((uint64_t)q * p.n_global + c) * DTT_GATE_WORDS;
-                if (p.flags & DTT_HANDLE_TIMESTAMPS)
-                    dtt_dev::st_relaxed(prow + DTT_GATE_T_ARRIVE, dtt_dev::globaltimer());
-                dtt_dev::red_release_add(prow + DTT_GATE_ARRIVAL, 1);
-                dtt_dev::count_groups(p.groups, q, c);
-            }
-            dtt_dev::red_release_add(row + DTT_GATE_COMPLETION, p.P - 1);
-            notify_host(p, c);
-        }
+        if (done == (uint64_t)p.round * cd.n_part) signal_arrivals(p, s, c);
     }
     // leave nothing in flight: stores, and (after a failed wait) loads still landing in the ring
     bulk_wait_all();

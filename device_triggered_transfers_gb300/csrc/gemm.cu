@@ -359,9 +359,9 @@ __device__ __forceinline__ bool wait_block(const ConsumerParams& p, uint32_t b, 
     if (!p.bgroup) return wait_chunks(p.h, p.c0[b], p.c1[b], p.max_polls, abort);
     const uint32_t g = p.bgroup[b];
     if (g != 0xFFFFFFFFu) {                  // a block no chunk touches has nothing to wait for
-        const dtt_group_table* t = p.h.groups;
-        const uint64_t* w = t->counters + (uint64_t)p.h.rank * t->n_groups + g;
-        const uint64_t target = (uint64_t)p.h.round * t->size[g];
+        const dtt_group_table& t = p.h.groups;
+        const uint64_t* w = t.counters + (uint64_t)p.h.rank * t.n_groups + g;
+        const uint64_t target = (uint64_t)p.h.round * t.size[g];
         uint32_t ns = 0;
         bool ok = false;
         for (uint64_t i = 0; i < p.max_polls; ++i) {

@@ -132,7 +132,7 @@ struct CopierParams {
     uint64_t* go_host;
     uint64_t go_prior;
     uint64_t go_wait_ns;
-    const dtt_group_table* groups;   // device: the plan's chunk groups, or null
+    dtt_group_table groups;     // the plan's chunk groups (counters == null: none)
 };
 
 struct CheckParams {

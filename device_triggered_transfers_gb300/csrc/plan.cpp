@@ -73,7 +73,6 @@ struct dtt_plan {
     std::vector<uint32_t> group_size;
     std::vector<uint32_t> block_group;   // block -> group id (UINT32_MAX: no chunk touches it)
     uint64_t group_block_bytes = 0;
-    dtt_group_table* d_group_table = nullptr;
     uint64_t* d_group_counters = nullptr;
     uint32_t* d_group_arrays = nullptr;   // size, chunk_off, chunk_ids back to back
 
@@ -160,10 +159,8 @@ void free_device(dtt_plan* p) {
     if (p->h_arrived) cudaFreeHost(p->h_arrived);
     if (p->d_cons) cudaFree(p->d_cons);
     p->d_cons = nullptr;
-    cudaFree(p->d_group_table);
     cudaFree(p->d_group_counters);
     cudaFree(p->d_group_arrays);
-    p->d_group_table = nullptr;
     p->d_group_counters = nullptr;
     p->d_group_arrays = nullptr;
     p->ev_copier_end = nullptr;
@@ -353,6 +350,18 @@ int launch_round_copier(dtt_plan* p) {
     return DTT_OK;
 }
 
+// The plan's group table with device addresses (all null when it has no groups).
+dtt_group_table group_table(const dtt_plan* p) {
+    dtt_group_table t{};
+    if (!p->n_groups) return t;
+    t.counters = p->d_group_counters;
+    t.size = p->d_group_arrays;
+    t.chunk_off = p->d_group_arrays + p->n_groups;
+    t.chunk_ids = p->d_group_arrays + p->n_groups + (p->n_global + 1);
+    t.n_groups = p->n_groups;
+    return t;
+}
+
 dtt_handle make_handle(const dtt_plan* p, uint32_t r) {
     dtt_handle h{};
     h.gates = p->d_gates;
@@ -365,7 +374,7 @@ dtt_handle make_handle(const dtt_plan* p, uint32_t r) {
     h.first_chunk = p->first_chunk[r];
     h.n_chunks = p->n_chunks[r];
     h.flags = p->opts.timestamps ? DTT_HANDLE_TIMESTAMPS : 0u;
-    h.groups = p->d_group_table;
+    h.groups = group_table(p);
     return h;
 }
 
@@ -390,7 +399,7 @@ CopierParams copier_params(const dtt_plan* p) {
     cp.tmaps = p->d_tmaps;
     cp.host_arrived = p->notify_host ? p->h_arrived_dev : nullptr;
     cp.stages = p->opts.stages;
-    cp.groups = p->d_group_table;
+    cp.groups = group_table(p);
     return cp;
 }
 
@@ -1111,18 +1120,10 @@ int dtt_plan_define_groups(dtt_plan* p, uint32_t n_groups, const uint32_t* offse
     // the copies are synchronous here)
     DTT_CUDA_TRY(cudaMalloc(&p->d_group_counters, counters.size() * sizeof(uint64_t)));
     DTT_CUDA_TRY(cudaMalloc(&p->d_group_arrays, arrays.size() * sizeof(uint32_t)));
-    DTT_CUDA_TRY(cudaMalloc(&p->d_group_table, sizeof(dtt_group_table)));
     DTT_CUDA_TRY(cudaMemcpy(p->d_group_counters, counters.data(), counters.size() * sizeof(uint64_t),
                             cudaMemcpyHostToDevice));
     DTT_CUDA_TRY(cudaMemcpy(p->d_group_arrays, arrays.data(), arrays.size() * sizeof(uint32_t),
                             cudaMemcpyHostToDevice));
-    dtt_group_table t{};
-    t.counters = p->d_group_counters;
-    t.size = p->d_group_arrays;
-    t.chunk_off = p->d_group_arrays + n_groups;
-    t.chunk_ids = p->d_group_arrays + n_groups + (p->n_global + 1);
-    t.n_groups = n_groups;
-    DTT_CUDA_TRY(cudaMemcpy(p->d_group_table, &t, sizeof(t), cudaMemcpyHostToDevice));
     p->n_groups = n_groups;
     p->group_size = size;
     return DTT_OK;

@@ -221,7 +221,8 @@ void dtt_plan_opts_default(dtt_plan_opts* opts);
                                       a chunk it does not own */
 #define DTT_DEV_EBADGROUP 2u       /* device status bit: a wait named a group the plan lacks */
 
-/* A plan's chunk groups on the device (dtt_plan_define_groups), owned by the plan.  A group is a
+/* A plan's chunk groups (dtt_plan_define_groups): device arrays owned by the plan, their
+ * addresses carried by value in every handle.  A group is a
  * set of global chunk ids, of any source ranks.  Each virtual rank q has one counter per group,
  * counters[q * n_groups + g], that goes up by one whenever a member becomes readable at q: the
  * copier adds one when it signals a member's arrival at q, and the mark that opens a member's
@@ -252,7 +253,7 @@ typedef struct dtt_handle {
     uint32_t n_chunks;        /* this rank's chunk count */
     uint32_t flags;           /* bit 0: timestamps */
     uint32_t reserved;
-    const dtt_group_table* groups;   /* device: the plan's groups, or NULL (none defined) */
+    dtt_group_table groups;   /* the plan's groups (device arrays); counters == NULL: none */
 } dtt_handle;
 
 /* Gate row: 64 bytes = 8 uint64 words per (rank, global chunk) ("Triggered Plans", Gates and

@@ -20,9 +20,9 @@
  *    Polls are counted, never clock-bounded.
  *  - reusable: thread 0 acquires the chunk's completion word, which the copier bumps with a
  *    release add after every copy of the chunk has landed (and so after its reads of it).
- *  - groups: the copier's arrival signal at a peer and the mark that opens a gate are followed
- *    by a release add on that rank's counters of the chunk's groups; dtt_wait_group acquires the
- *    counter, so data of every member read after it is this round's.
+ *  - groups: the mark that opens a gate, and the copier's arrival signal at a peer, add one to
+ *    that rank's counters of the chunk's groups after a release fence; dtt_wait_group acquires
+ *    the counter, so data of every member read after it is this round's.
  *  - A producer that writes through the async proxy (TMA stores) must complete those writes
  *    (cp.async.bulk.wait_group 0) and issue fence.proxy.async before calling mark_ready.
  */
@@ -65,6 +65,12 @@ __device__ __forceinline__ void red_release_add(uint64_t* p, uint64_t v) {
     asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
+__device__ __forceinline__ void red_relaxed_add(uint64_t* p, uint64_t v) {
+    asm volatile("red.relaxed.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ void fence_acq_rel() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
 __device__ __forceinline__ void red_relaxed_max(uint64_t* p, uint64_t v) {
     asm volatile("red.relaxed.gpu.global.max.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
@@ -83,15 +89,6 @@ __device__ __forceinline__ uint64_t* gate_row(const dtt_handle& h, uint32_t tabl
     return h.gates + ((uint64_t)table * h.n_global + chunk) * DTT_GATE_WORDS;
 }
 
-/* Chunk `chunk` became readable at rank `rank`: one release add on each of that rank's counters
- * of the chunk's groups (none when the plan has no groups). */
-__device__ __forceinline__ void count_groups(const dtt_group_table* g, uint32_t rank, uint32_t chunk) {
-    if (!g) return;
-    const uint32_t a = g->chunk_off[chunk], b = g->chunk_off[chunk + 1];
-    uint64_t* row = g->counters + (uint64_t)rank * g->n_groups;
-    for (uint32_t i = a; i < b; ++i) red_release_add(row + g->chunk_ids[i], 1);
-}
-
 /* One writer's mark, issued by one thread after the caller's barrier. */
 __device__ __forceinline__ void mark_one(const dtt_handle& h, uint32_t chunk) {
     if (chunk < h.first_chunk || chunk >= h.first_chunk + h.n_chunks) {
@@ -103,8 +100,19 @@ __device__ __forceinline__ void mark_one(const dtt_handle& h, uint32_t chunk) {
     const uint64_t now = atom_add_acq_rel(row + DTT_GATE_COUNTER, 1) + 1;
     if (now == target) {
         if (h.flags & DTT_HANDLE_TIMESTAMPS) st_relaxed(row + DTT_GATE_T_OPEN, globaltimer());
-        st_release(row + DTT_GATE_READY, h.round);
-        count_groups(h.groups, h.rank, chunk);     // readable at its own rank from now on
+        if (h.groups.counters) {
+            // the chunk is readable at its own rank from now on: it counts in the rank's counter
+            // of each of its groups.  The chunk's group ids are read first, then one release
+            // fence covers the gate and every counter (each relaxed write after the fence is a
+            // release pattern)
+            const uint32_t a = h.groups.chunk_off[chunk], b = h.groups.chunk_off[chunk + 1];
+            uint64_t* grow = h.groups.counters + (uint64_t)h.rank * h.groups.n_groups;
+            fence_acq_rel();
+            st_relaxed(row + DTT_GATE_READY, h.round);
+            for (uint32_t i = a; i < b; ++i) red_relaxed_add(grow + h.groups.chunk_ids[i], 1);
+        } else {
+            st_release(row + DTT_GATE_READY, h.round);
+        }
     } else if (now > target) {
         red_relaxed_max(row + DTT_GATE_ERROR, h.round);
     }
@@ -113,12 +121,12 @@ __device__ __forceinline__ void mark_one(const dtt_handle& h, uint32_t chunk) {
 /* The counter a rank polls for group g and the count that completes this round; null when the
  * plan has no group g (a misuse bit is set). */
 __device__ __forceinline__ const uint64_t* group_word(const dtt_handle& h, uint32_t g, uint64_t* target) {
-    if (!h.groups || g >= h.groups->n_groups) {
+    if (!h.groups.counters || g >= h.groups.n_groups) {
         atomicOr(h.status, DTT_DEV_EBADGROUP);
         return nullptr;
     }
-    *target = (uint64_t)h.round * h.groups->size[g];
-    return h.groups->counters + (uint64_t)h.rank * h.groups->n_groups + g;
+    *target = (uint64_t)h.round * h.groups.size[g];
+    return h.groups.counters + (uint64_t)h.rank * h.groups.n_groups + g;
 }
 
 /* The word a rank polls for `chunk`: its own chunks are local once ready; other ranks' chunks

@@ -206,7 +206,7 @@ def test_binding_structs_match_the_c_header(tmp_path):
     if not shutil.which("gcc"):
         pytest.skip("gcc not found")
     structs = {"dtt_region": D.dtt_region, "dtt_order": D.dtt_order, "dtt_plan_opts": D.dtt_plan_opts,
-               "dtt_handle": D.dtt_handle, "dtt_report": D.dtt_report, "dtt_fill_desc": D.dtt_fill_desc}
+               "dtt_group_table": D.dtt_group_table, "dtt_handle": D.dtt_handle, "dtt_report": D.dtt_report, "dtt_fill_desc": D.dtt_fill_desc}
     lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "dtt.h"', 'int main(void) {']
     for name, cls in structs.items():
         lines.append(f'printf("{name} %zu\\n", sizeof({name}));')
