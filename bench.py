@@ -323,7 +323,7 @@ def run_reference(args):
 
 
 def measure_workload(w, args, K, warmup, latency_rounds, isolated_rounds, with_e2e, world=1,
-                     clocks_dev=None, early_us=None):
+                     clocks_dev=None, early_us=None, method=None):
     """Time K rounds of workload w in the launch the benchmark uses for it (runner.bench_launch),
     then the kernel-timing pass, the gate timestamps, the isolated kernels and (optionally) the
     host-buffer round.  Returns a dict of raw measurements (seconds, milliseconds, bytes)."""
@@ -338,6 +338,11 @@ def measure_workload(w, args, K, warmup, latency_rounds, isolated_rounds, with_e
     # stream costs the round a few microseconds); the kernel-timing pass after it runs the same
     # launches on a plan that times each copier launch itself (CUDA events in the library)
     opts = launch.pop("opts", None) or D.dtt_plan_opts_default()
+    if method is not None and method != opts.method:
+        # another transport under the same producer: the copy engines need no copier kernel
+        # (nothing to launch early, nothing to pace against)
+        opts = D.dtt_plan_opts_default(method=method)
+        launch.pop("pace", None)
     if args.deferred:
         opts.deferred_copier = 1
     if early_us is not None:
@@ -448,14 +453,17 @@ def measure_workload(w, args, K, warmup, latency_rounds, isolated_rounds, with_e
     # kernel-timing pass: K more rounds of the same step, CUDA events around every copier launch
     # (in the library, on the copy stream) and, for the GEMM, around every producer launch.  A
     # timed plan launches its copier at plan_start, so each copier launch is one round's.
-    plan3 = side_plan(time_copier=1, deferred_copier=opts.deferred_copier)
-    step3 = make_step(plan3, opts.deferred_copier == 1)
-    for _ in range(3):
-        step3()
-    torch.cuda.synchronize()
-    t3, copier_ms, producer_ms = timed(plan3, step3, K, producer_events=gemm)
-    plan3.close()
-    out.update(timing_pass_s=t3, copier_ms=copier_ms, producer_ms=producer_ms)
+    if opts.method == D.COPY_ENGINE:      # no copier kernel: the round is the transport's time
+        out.update(timing_pass_s=elapsed, copier_ms=elapsed / K * 1e3, producer_ms=None)
+    else:
+        plan3 = side_plan(time_copier=1, deferred_copier=opts.deferred_copier)
+        step3 = make_step(plan3, opts.deferred_copier == 1)
+        for _ in range(3):
+            step3()
+        torch.cuda.synchronize()
+        t3, copier_ms, producer_ms = timed(plan3, step3, K, producer_events=gemm)
+        plan3.close()
+        out.update(timing_pass_s=t3, copier_ms=copier_ms, producer_ms=producer_ms)
 
     # gate-to-arrival latency and the copier window, from the gate timestamps of extra rounds
     lat, windows = [], []
@@ -503,7 +511,7 @@ def measure_workload(w, args, K, warmup, latency_rounds, isolated_rounds, with_e
 
     # the same copier and producer one after the other (deferred plan): each kernel alone
     out["isolated"] = None
-    if not args.deferred and isolated_rounds:
+    if not args.deferred and isolated_rounds and opts.method != D.COPY_ENGINE:
         plan2 = side_plan(time_copier=1, deferred_copier=1)
         step2 = make_step(plan2, True)
         for _ in range(3):
@@ -854,6 +862,21 @@ def run_ce_fanout(args):
     cop_ms = (c1[1] - c0[1]) / (c1[2] - c0[2])
     res["sm_copier_ms"] = cop_ms
     res["sm_copier_gbs_delivered"] = w.delivered_bytes_per_round() / (cop_ms / 1e3) / 1e9
+    del st
+    torch.cuda.empty_cache()
+    # whole gated rounds, the benchmark's producer each time: the copy engines driven by the
+    # plan's host proxy (poll, copy, atomic per chunk) against the benchmark's SM copier launch
+    peak, peak_kind = load_peaks()
+    K = max(3, min(args.steps, 100))
+    gated = {}
+    for name, method in (("copy_engines", D.COPY_ENGINE), ("sm_copier", None)):
+        m = measure_workload(w, args, K, 3, 5, 0, with_e2e=False, method=method)
+        sm = summarize(m, K, m["elapsed_s"], w.delivered_bytes_per_round() * K, peak, peak_kind)
+        gated[name] = {"ms_per_round": sm["ms_per_round"], "gbs_delivered": sm["gbs_delivered"],
+                       "hbm_frac_end_to_end": sm["hbm_frac_end_to_end"]["of_measured"],
+                       "gate_to_arrival_ns": {k: sm["gate_to_arrival_ns"][k] for k in
+                                              ("median", "p99", "median_over_ideal", "p99_over_ideal")}}
+    res["gated_rounds"] = gated
     line = {"metric": "fan-out of one all-gather round: copy engines vs the SM copier (1 GB300)",
             "unit": "GB/s delivered", "higher_is_better": True,
             "config": {"workload": describe(w, launch)}, **res}

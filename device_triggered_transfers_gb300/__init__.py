@@ -34,7 +34,7 @@ PREPARED, RUNNING, DONE, FAILED, CLOSING, CLOSED = range(6)
 RC_CLOSING = 1      # dtt_plan_close left the plan CLOSING (not an error)
 BF16, F32, U8 = 0, 1, 2
 DTYPE_CODES = {"bf16": BF16, "f32": F32, "u8": U8}
-COPY_VEC16, COPY_TMA = 0, 1
+COPY_VEC16, COPY_TMA, COPY_ENGINE = 0, 1, 2
 ORDER_ROW_MAJOR, ORDER_GROUPED = 0, 1
 MARK_PER_STEP, MARK_AT_END = 0, 1
 
@@ -67,7 +67,8 @@ class dtt_handle(C.Structure):
     _fields_ = [("gates", C.c_void_p), ("writers", C.c_void_p), ("status", C.c_void_p),
                 ("round", C.c_uint32), ("rank", C.c_uint32), ("P", C.c_uint32),
                 ("n_global", C.c_uint32), ("first_chunk", C.c_uint32), ("n_chunks", C.c_uint32),
-                ("flags", C.c_uint32), ("reserved", C.c_uint32), ("groups", dtt_group_table)]
+                ("flags", C.c_uint32), ("reserved", C.c_uint32), ("groups", dtt_group_table),
+                ("host_ready", C.c_void_p)]
 
 
 class dtt_report(C.Structure):

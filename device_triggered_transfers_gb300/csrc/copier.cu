@@ -548,6 +548,28 @@ __global__ void force_open_kernel(uint64_t* gates, const ChunkDesc* chunks, uint
     }
 }
 
+// The copy-engine transport's ATOMIC step: stream-ordered after every copy of chunk c to every
+// peer (so those bytes are visible to this kernel), one thread signals as the SM copier does.
+__global__ void ce_signal_kernel(const __grid_constant__ CeSignalParams p) {
+    if (threadIdx.x != 0) return;
+    dtt_dev::fence_acq_rel();
+    for (uint32_t q = 0; q < p.P; ++q) {
+        if (q == p.s) continue;
+        uint64_t* prow = p.gates + ((uint64_t)q * p.n_global + p.c) * DTT_GATE_WORDS;
+        if (p.flags & DTT_HANDLE_TIMESTAMPS) dtt_dev::st_relaxed(prow + DTT_GATE_T_ARRIVE, dtt_dev::globaltimer());
+        dtt_dev::red_relaxed_add(prow + DTT_GATE_ARRIVAL, 1);
+        if (p.groups.counters) {
+            uint64_t* grow = p.groups.counters + (uint64_t)q * p.groups.n_groups;
+            for (uint32_t i = p.groups.chunk_off[p.c]; i < p.groups.chunk_off[p.c + 1]; ++i)
+                dtt_dev::red_relaxed_add(grow + p.groups.chunk_ids[i], 1);
+        }
+    }
+    uint64_t* row = p.gates + ((uint64_t)p.s * p.n_global + p.c) * DTT_GATE_WORDS;
+    dtt_dev::red_relaxed_add(row + DTT_GATE_COMPLETION, p.P - 1);
+    if (p.host_arrived)
+        asm volatile("st.release.sys.global.u32 [%0], %1;" ::"l"(p.host_arrived + p.c), "r"(p.round) : "memory");
+}
+
 struct PublishParams {
     dtt_handle h[DTT_MAX_RANKS];
     uint32_t P;
@@ -624,6 +646,11 @@ cudaError_t launch_force_open(uint64_t* gates, const ChunkDesc* chunks, uint32_t
     return cudaGetLastError();
 }
 
+cudaError_t launch_ce_signal(const CeSignalParams& p, cudaStream_t s) {
+    ce_signal_kernel<<<1, 32, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_consumer(const CopierParams& p, dtt_handle h, char* dst, uint64_t max_polls,
                             int32_t* status, uint32_t ctas, cudaStream_t s) {
     if (ctas == 0) ctas = 1;
@@ -650,6 +677,7 @@ cudaError_t preload_copier_kernels() {
     if (e == cudaSuccess) e = prepare_kernel(force_open_kernel);
     if (e == cudaSuccess) e = prepare_kernel(publish_kernel);
     if (e == cudaSuccess) e = prepare_kernel(consumer_kernel);
+    if (e == cudaSuccess) e = prepare_kernel(ce_signal_kernel);
     return e;
 }
 

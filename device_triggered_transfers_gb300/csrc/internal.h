@@ -167,6 +167,15 @@ cudaError_t launch_copier(const CopierParams& p, uint32_t ctas, uint32_t threads
 cudaError_t launch_check(const CheckParams& p, cudaStream_t s);
 cudaError_t launch_force_open(uint64_t* gates, const ChunkDesc* chunks, uint32_t n_global,
                               uint32_t round, cudaStream_t s);
+// Copy-engine transport: after every copy of chunk c (source s) has landed, one warp signals its
+// arrival at each peer, the peers' group counters and s's completion word (as the SM copier does).
+struct CeSignalParams {
+    uint64_t* gates;
+    dtt_group_table groups;
+    uint32_t* host_arrived;     // or null
+    uint32_t P, n_global, s, c, round, flags;
+};
+cudaError_t launch_ce_signal(const CeSignalParams& p, cudaStream_t s);
 cudaError_t launch_consumer(const CopierParams& p, dtt_handle h, char* dst, uint64_t max_polls,
                             int32_t* status, uint32_t ctas, cudaStream_t s);
 

@@ -4,9 +4,13 @@
 // Design notes).  One process drives all P virtual ranks, so the collective steps of the pages
 // (create, next_round, close) are single calls here.
 #include <algorithm>
+#include <atomic>
+#include <chrono>
+#include <condition_variable>
 #include <cstring>
 #include <new>
 #include <mutex>
+#include <thread>
 #include <vector>
 
 #include "internal.h"
@@ -23,6 +27,28 @@ struct MapShape {
     bool operator==(const MapShape& o) const { return inner == o.inner && rows == o.rows && pitch == o.pitch; }
 };
 constexpr size_t kMaxMapShapes = 256;
+
+// The copy-engine transport (opts.method = DTT_COPY_ENGINE): a proxy thread of the plan stands in
+// for the pages' pre-armed copy-engine queues.  start() hands it a round; it polls the mapped gate
+// words in each source's schedule order and issues each open chunk's copies on the (source, peer)
+// streams, then the chunk's signal kernel after joining them.
+struct CeProxy {
+    std::thread thread;
+    std::mutex mu;
+    std::condition_variable cv;
+    bool stop = false;
+    bool busy = false;                  // issuing `round`
+    uint32_t round = 0;
+    std::atomic<bool> open_all{false};  // close() in mid-round: every chunk goes as it stands
+    int rc = DTT_OK;                    // DTT_ETIMEDOUT: a gate stayed closed past the bound
+    uint32_t stuck_chunk = 0;
+    uint32_t* h_ready = nullptr;        // pinned, mapped: word c = round of chunk c's last opening
+    uint32_t* h_ready_dev = nullptr;
+    std::vector<cudaStream_t> streams;  // [s * P + q]
+    std::vector<cudaEvent_t> ev;        // [s * P + q]
+    std::vector<uint32_t> reg_begin;    // chunk c's regions: regs[reg_begin[c] .. reg_begin[c + 1])
+    std::vector<dtt_region> regs;
+};
 
 }  // namespace
 
@@ -91,6 +117,7 @@ struct dtt_plan {
     int state = DTT_PLAN_PREPARED;
     uint32_t round = 1;
     bool copier_launched = false;   // this round's copier is on the copy stream
+    CeProxy* ce = nullptr;          // opts.method == DTT_COPY_ENGINE
 
     // opts.early_copier_us: wait() launches the next round's copier behind this round's, and
     // start() claims it through HostStatus::go (see CopierParams::go_host).
@@ -138,7 +165,10 @@ bool regions_intersect(const dtt_region& a, const dtt_region& b) {
     return false;
 }
 
+void stop_ce(dtt_plan* p);
+
 void free_device(dtt_plan* p) {
+    stop_ce(p);
     cudaFree(p->d_gates);
     cudaFree(p->d_writers);
     cudaFree(p->d_chunks);
@@ -375,6 +405,7 @@ dtt_handle make_handle(const dtt_plan* p, uint32_t r) {
     h.n_chunks = p->n_chunks[r];
     h.flags = p->opts.timestamps ? DTT_HANDLE_TIMESTAMPS : 0u;
     h.groups = group_table(p);
+    h.host_ready = p->ce ? p->ce->h_ready_dev : nullptr;
     return h;
 }
 
@@ -415,6 +446,7 @@ bool stream_shared(const dtt_plan* p) {
 
 bool early_allowed(const dtt_plan* p) {
     return p->opts.early_copier_us && p->host_atomics && p->n_global && !p->opts.time_copier &&
+           p->opts.method != DTT_COPY_ENGINE &&
            p->opts.deferred_copier != 1 && !p->suppress_early && p->round < 0xFFFFFFFFu &&
            !stream_shared(p);
 }
@@ -472,6 +504,190 @@ bool claim_early(dtt_plan* p) {
     p->go_shadow = expected;          // early_stop_value(round): it expired
     ++p->early_expired;
     return false;
+}
+
+// ---- the copy-engine transport (opts.method = DTT_COPY_ENGINE) -----------------------------------
+// Issue chunk c of source s: every region to every peer on the (s, q) queue, then -- once all of
+// them have landed (the other queues' events joined onto the last one) -- the signal kernel.
+int ce_issue(dtt_plan* p, uint32_t s, uint32_t c, uint32_t round) {
+    CeProxy& ce = *p->ce;
+    const uint32_t P = p->P;
+    uint32_t last = UINT32_MAX;
+    for (uint32_t q = 0; q < P; ++q) {
+        if (q == s) continue;
+        cudaStream_t st = ce.streams[s * P + q];
+        for (uint32_t i = ce.reg_begin[c]; i < ce.reg_begin[c + 1]; ++i) {
+            const dtt_region& r = ce.regs[i];
+            if (r.rows == 0 || r.row_bytes == 0) continue;
+            if (r.rows == 1)
+                DTT_CUDA_TRY(cudaMemcpyAsync(p->bufs[q] + r.offset, p->bufs[s] + r.offset, r.row_bytes,
+                                             cudaMemcpyDeviceToDevice, st));
+            else
+                DTT_CUDA_TRY(cudaMemcpy2DAsync(p->bufs[q] + r.offset, r.pitch, p->bufs[s] + r.offset, r.pitch,
+                                               r.row_bytes, r.rows, cudaMemcpyDeviceToDevice, st));
+        }
+        last = q;
+    }
+    if (last == UINT32_MAX) return DTT_OK;        // one rank: nothing to copy or signal
+    cudaStream_t sl = ce.streams[s * P + last];
+    for (uint32_t q = 0; q < P; ++q) {
+        if (q == s || q == last) continue;
+        DTT_CUDA_TRY(cudaEventRecord(ce.ev[s * P + q], ce.streams[s * P + q]));
+        DTT_CUDA_TRY(cudaStreamWaitEvent(sl, ce.ev[s * P + q], 0));
+    }
+    CeSignalParams sp{};
+    sp.gates = p->d_gates;
+    sp.groups = group_table(p);
+    sp.host_arrived = nullptr;
+    sp.P = P;
+    sp.n_global = p->n_global;
+    sp.s = s;
+    sp.c = c;
+    sp.round = round;
+    sp.flags = p->opts.timestamps ? DTT_HANDLE_TIMESTAMPS : 0u;
+    DTT_CUDA_TRY(launch_ce_signal(sp, sl));
+    return DTT_OK;
+}
+
+// One round on the proxy thread: every source's chunks in schedule order, each as soon as its
+// gate's host word shows the round.  Gives up when no gate has opened for max_polls x 256 ns
+// (about a second at the default), leaving the rest unsent for wait() to report.
+int ce_run_round(dtt_plan* p, uint32_t round) {
+    CeProxy& ce = *p->ce;
+    const uint32_t P = p->P;
+    uint32_t next[DTT_MAX_RANKS], end[DTT_MAX_RANKS];
+    uint64_t remaining = 0;
+    for (uint32_t s = 0; s < P; ++s) {
+        next[s] = p->first_chunk[s];
+        end[s] = p->first_chunk[s] + p->n_chunks[s];
+        remaining += p->n_chunks[s];
+    }
+    const auto bound = std::chrono::nanoseconds(256 * std::max<uint64_t>(p->opts.max_polls, 1));
+    auto last_progress = std::chrono::steady_clock::now();
+    for (uint64_t spin = 0; remaining; ++spin) {
+        bool progress = false;
+        for (uint32_t s = 0; s < P; ++s) {
+            while (next[s] < end[s]) {
+                const uint32_t c = next[s];
+                const bool open = __atomic_load_n(&ce.h_ready[c], __ATOMIC_ACQUIRE) >= round ||
+                                  ce.open_all.load(std::memory_order_acquire);
+                if (!open) break;                 // head of line: this source's later chunks wait
+                const int rc = ce_issue(p, s, c, round);
+                if (rc != DTT_OK) return rc;
+                ++next[s];
+                --remaining;
+                progress = true;
+            }
+        }
+        if (progress) {
+            last_progress = std::chrono::steady_clock::now();
+        } else if ((spin & 63) == 63) {
+            if (std::chrono::steady_clock::now() - last_progress > bound) {
+                uint32_t stuck = UINT32_MAX;
+                for (uint32_t s = 0; s < P; ++s)
+                    if (next[s] < end[s]) stuck = std::min(stuck, next[s]);
+                ce.stuck_chunk = stuck;
+                return fail(DTT_ETIMEDOUT, "copy-engine proxy: chunk %u's gate stayed closed", stuck);
+            }
+            std::this_thread::yield();
+        }
+    }
+    return DTT_OK;
+}
+
+void ce_main(dtt_plan* p) {
+    CeProxy& ce = *p->ce;
+    int dev = p->device;
+    cudaSetDevice(dev);
+    for (;;) {
+        uint32_t round;
+        {
+            std::unique_lock<std::mutex> lock(ce.mu);
+            ce.cv.wait(lock, [&] { return ce.stop || ce.busy; });
+            if (ce.stop) return;
+            round = ce.round;
+        }
+        const int rc = ce_run_round(p, round);
+        {
+            std::lock_guard<std::mutex> lock(ce.mu);
+            ce.rc = rc;
+            ce.busy = false;
+        }
+        ce.cv.notify_all();
+    }
+}
+
+// Set up the proxy: the regions of every chunk, the queues, the mapped gate words and the thread.
+int start_ce(dtt_plan* p, const dtt_schedule* const* scheds) {
+    p->ce = new (std::nothrow) CeProxy();
+    if (!p->ce) return fail(DTT_ENOMEM, "dtt_plan_create: out of memory");
+    CeProxy& ce = *p->ce;
+    const uint32_t P = p->P;
+    ce.reg_begin.push_back(0);
+    for (uint32_t r = 0; r < P; ++r) {
+        const dtt_schedule* sc = scheds ? scheds[r] : nullptr;
+        if (!sc) continue;
+        for (const HostChunk& ch : sc->chunks) {
+            ce.regs.insert(ce.regs.end(), ch.regions.begin(), ch.regions.end());
+            ce.reg_begin.push_back((uint32_t)ce.regs.size());
+        }
+    }
+    const size_t words = std::max<size_t>(1, p->n_global);
+    DTT_CUDA_TRY(cudaHostAlloc(&ce.h_ready, words * sizeof(uint32_t), cudaHostAllocMapped | cudaHostAllocPortable));
+    for (size_t c = 0; c < words; ++c) ce.h_ready[c] = p->round - 1;   // as after the rounds before
+    DTT_CUDA_TRY(cudaHostGetDevicePointer(reinterpret_cast<void**>(&ce.h_ready_dev), ce.h_ready, 0));
+    ce.streams.assign((size_t)P * P, nullptr);
+    ce.ev.assign((size_t)P * P, nullptr);
+    for (uint32_t s = 0; s < P; ++s)
+        for (uint32_t q = 0; q < P; ++q) {
+            if (q == s) continue;
+            DTT_CUDA_TRY(cudaStreamCreateWithFlags(&ce.streams[s * P + q], cudaStreamNonBlocking));
+            DTT_CUDA_TRY(cudaEventCreateWithFlags(&ce.ev[s * P + q], cudaEventDisableTiming));
+        }
+    try {
+        ce.thread = std::thread(ce_main, p);
+    } catch (...) {
+        return fail(DTT_ENOMEM, "dtt_plan_create: cannot start the copy-engine proxy thread");
+    }
+    return DTT_OK;
+}
+
+void stop_ce(dtt_plan* p) {
+    if (!p->ce) return;
+    CeProxy& ce = *p->ce;
+    if (ce.thread.joinable()) {
+        {
+            std::lock_guard<std::mutex> lock(ce.mu);
+            ce.stop = true;
+        }
+        ce.cv.notify_all();
+        ce.thread.join();
+    }
+    for (cudaStream_t st : ce.streams)
+        if (st) cudaStreamDestroy(st);
+    for (cudaEvent_t e : ce.ev)
+        if (e) cudaEventDestroy(e);
+    if (ce.h_ready) cudaFreeHost(ce.h_ready);
+    delete p->ce;
+    p->ce = nullptr;
+}
+
+// Wait until the proxy has issued (or given up on) this round's chunks, then order the producer
+// stream after every queue.  Returns the proxy's status.
+int ce_join(dtt_plan* p, cudaStream_t after) {
+    CeProxy& ce = *p->ce;
+    {
+        std::unique_lock<std::mutex> lock(ce.mu);
+        ce.cv.wait(lock, [&] { return !ce.busy; });
+    }
+    for (uint32_t s = 0; s < p->P; ++s)
+        for (uint32_t q = 0; q < p->P; ++q) {
+            if (q == s) continue;
+            DTT_CUDA_TRY(cudaEventRecord(ce.ev[s * p->P + q], ce.streams[s * p->P + q]));
+            if (after) DTT_CUDA_TRY(cudaStreamWaitEvent(after, ce.ev[s * p->P + q], 0));
+            else DTT_CUDA_TRY(cudaEventSynchronize(ce.ev[s * p->P + q]));
+        }
+    return ce.rc;
 }
 
 int validate_plan(dtt_plan* p, const dtt_schedule* const* scheds) {
@@ -735,7 +951,7 @@ int dtt_plan_create(void* const* bufs, uint64_t buf_bytes, uint32_t P,
     if (o.stages == 0 && o.piece_bytes % 16 == 0)   // as many stages as fit, at most 8
         o.stages = (uint32_t)std::max<size_t>(2, std::min<size_t>(8, kBulkSmemMax / (bulk_stage_bytes(o.piece_bytes) + 8)));
     if (o.piece_bytes % 16 || o.copier_threads % 32 || o.copier_threads > 1024 ||
-        (o.method != DTT_COPY_VEC16 && o.method != DTT_COPY_TMA)) {
+        (o.method != DTT_COPY_VEC16 && o.method != DTT_COPY_TMA && o.method != DTT_COPY_ENGINE)) {
         delete p;
         return fail(DTT_EINVAL, "dtt_plan_create: bad options (piece_bytes %% 16, threads %% 32 <= 1024, method)");
     }
@@ -792,7 +1008,7 @@ int dtt_plan_create(void* const* bufs, uint64_t buf_bytes, uint32_t P,
         delete p;
         return fail(DTT_EINVAL, "dtt_plan_create: deferred_copier is 0, 1 or 2");
     }
-    if (o.deferred_copier != 1) {
+    if (o.deferred_copier != 1 && o.method != DTT_COPY_ENGINE) {
         // The copier spins while the producer runs, so it must leave an SM room for producer
         // CTAs: at most half of its threads (2048) and half of its registers (64 Ki) per SM.
         int regs = 0;
@@ -813,6 +1029,7 @@ int dtt_plan_create(void* const* bufs, uint64_t buf_bytes, uint32_t P,
     }
     rc = build_plan(p, scheds);
     if (rc == DTT_OK) rc = upload(p);
+    if (rc == DTT_OK && o.method == DTT_COPY_ENGINE) rc = start_ce(p, scheds);
     if (rc == DTT_OK) {
         if (copy_stream) {
             p->copy_stream = copy_stream;
@@ -857,7 +1074,16 @@ int dtt_plan_start(dtt_plan* p, cudaStream_t producer_stream, dtt_handle* handle
     p->copier_launched = false;      // the status words were zeroed by the last check (or upload)
     if (p->early_pending && (p->early_round != p->round || p->notify_host))
         abort_early(p);              // a host-buffer round needs a copier that stamps arrivals
-    if (claim_early(p)) {
+    if (p->ce) {                     // the proxy issues this round's copies as gates open
+        {
+            std::lock_guard<std::mutex> lock(p->ce->mu);
+            p->ce->round = p->round;
+            p->ce->rc = DTT_OK;
+            p->ce->open_all.store(false);
+            p->ce->busy = p->n_global != 0;
+        }
+        p->ce->cv.notify_all();
+    } else if (claim_early(p)) {
         p->copier_launched = true;   // launched by the last wait(), now claimed for this round
     } else if (p->n_global && !p->opts.deferred_copier) {
         const int rc = launch_round_copier(p);
@@ -879,7 +1105,7 @@ int dtt_plan_handle(const dtt_plan* p, uint32_t rank, dtt_handle* out) {
 int dtt_plan_launch_copier(dtt_plan* p) {
     if (!p) return fail(DTT_EINVAL, "dtt_plan_launch_copier: NULL plan");
     if (p->state != DTT_PLAN_RUNNING) return fail(DTT_ESTATE, "dtt_plan_launch_copier: plan is not RUNNING");
-    if (p->copier_launched || !p->n_global) return DTT_OK;
+    if (p->copier_launched || !p->n_global || p->ce) return DTT_OK;
     if (p->opts.deferred_copier == 1) {   // after the producers: no overlap
         DTT_CUDA_TRY(cudaEventRecord(p->ev_producer, p->producer_stream));
         DTT_CUDA_TRY(cudaStreamWaitEvent(p->copy_stream, p->ev_producer, 0));
@@ -894,6 +1120,8 @@ int dtt_plan_wait(dtt_plan* p, dtt_report* report) {
     if (lc != DTT_OK) return lc;
     // The check follows the producers on their stream and waits on the device for the copier's
     // CTAs to count themselves out (no event between the streams, no launch gap after the copier).
+    int ce_rc = DTT_OK;
+    if (p->ce) ce_rc = ce_join(p, p->producer_stream);   // the check follows every queue
     CheckParams ck{};
     ck.copier_ctas = p->copier_launched ? p->copier_ctas : 0;
     ck.max_polls = 8 * p->opts.max_polls;
@@ -933,7 +1161,7 @@ int dtt_plan_wait(dtt_plan* p, dtt_report* report) {
     }
     dtt_report rep{};
     rep.round = p->round;
-    rep.copier_timeouts = p->h_status->st.copier_timeouts;
+    rep.copier_timeouts = p->h_status->st.copier_timeouts + (ce_rc == DTT_ETIMEDOUT ? 1u : 0u);
     rep.device_status = p->h_status->st.misuse;
     const bool late = p->h_status->st.check_late != 0;
     for (uint32_t c = 0; c < p->n_global; ++c) {
@@ -1040,6 +1268,11 @@ int dtt_plan_close(dtt_plan* p) {
             rc = fail(DTT_ECUDA, "dtt_plan_close: producer stream failed");
         if (p->n_global && launch_force_open(p->d_gates, p->d_chunks, p->n_global, p->round, p->aux_stream) != cudaSuccess)
             rc = fail(DTT_ECUDA, "dtt_plan_close: force-open launch failed");
+        if (p->ce) {                 // the proxy sends every chunk as it stands, then drains
+            p->ce->open_all.store(true);
+            const int jr = ce_join(p, nullptr);
+            if (jr != DTT_OK && jr != DTT_ETIMEDOUT) rc = jr;
+        }
         if (!p->copier_launched && p->n_global) {     // deferred: send the chunks now
             if (cudaStreamSynchronize(p->aux_stream) != cudaSuccess || launch_round_copier(p) != DTT_OK)
                 rc = fail(DTT_ECUDA, "dtt_plan_close: copier launch failed");
@@ -1249,6 +1482,7 @@ int dtt_allgather_host(dtt_plan* p, const void* const* host_slices, void* host_o
                        uint32_t out_rank, cudaStream_t stream, dtt_report* report) {
     if (!p || !host_slices) return fail(DTT_EINVAL, "dtt_allgather_host: bad args");
     if (!p->opts.allgather) return fail(DTT_EINVAL, "dtt_allgather_host: needs an all-gather plan");
+    if (p->ce) return fail(DTT_EINVAL, "dtt_allgather_host: needs an SM copier (not DTT_COPY_ENGINE)");
     if (out_rank >= p->P) return fail(DTT_EINVAL, "dtt_allgather_host: out_rank out of range");
     const uint32_t P = p->P;
     const uint64_t S = p->buf_bytes / P;

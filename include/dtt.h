@@ -73,7 +73,16 @@ enum { DTT_BF16 = 0, DTT_F32 = 1, DTT_U8 = 2 };
 /* Copier data paths. */
 enum {
     DTT_COPY_VEC16 = 0,    /* 16-byte vector loads and stores, read once, fan out to peers */
-    DTT_COPY_TMA = 1       /* bulk async copies (cp.async.bulk) staged through shared memory */
+    DTT_COPY_TMA = 1,      /* bulk async copies (cp.async.bulk) staged through shared memory */
+    DTT_COPY_ENGINE = 2    /* the GPU's copy engines, driven by a host proxy thread of the plan
+                              (no copier kernel): the closest CUDA analogue of the pages' copy-engine
+                              queues.  The producer's gate-opening mark also stamps the round into
+                              a mapped host word; the proxy polls those words in schedule order
+                              (POLL_REGMEM), issues one cudaMemcpyAsync / cudaMemcpy2DAsync per
+                              region and peer on one stream per (source, peer) queue (COPY), and
+                              once the chunk's copies to every peer are done a one-warp kernel adds
+                              its arrivals, group counts and completion (ATOMIC).  Each source
+                              byte is read once per peer.  dtt_allgather_host needs an SM copier. */
 };
 
 /* ---------------------------------------------------------------------------------------- */
@@ -254,6 +263,9 @@ typedef struct dtt_handle {
     uint32_t flags;           /* bit 0: timestamps */
     uint32_t reserved;
     dtt_group_table groups;   /* the plan's groups (device arrays); counters == NULL: none */
+    uint32_t* host_ready;     /* DTT_COPY_ENGINE plans: device address of mapped host words, word c
+                                 = the round chunk c's gate last opened in (the mark that opens a
+                                 gate stores it after a system-scope fence); NULL otherwise */
 } dtt_handle;
 
 /* Gate row: 64 bytes = 8 uint64 words per (rank, global chunk) ("Triggered Plans", Gates and

@@ -113,6 +113,12 @@ __device__ __forceinline__ void mark_one(const dtt_handle& h, uint32_t chunk) {
         } else {
             st_release(row + DTT_GATE_READY, h.round);
         }
+        if (h.host_ready) {
+            // a copy-engine plan: the host proxy issues the copies once it reads this word, so
+            // the chunk's data is made visible at system scope first
+            asm volatile("fence.acq_rel.sys;\n\t"
+                         "st.relaxed.sys.global.u32 [%0], %1;" ::"l"(h.host_ready + chunk), "r"(h.round) : "memory");
+        }
     } else if (now > target) {
         red_relaxed_max(row + DTT_GATE_ERROR, h.round);
     }

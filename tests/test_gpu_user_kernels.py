@@ -160,7 +160,7 @@ def test_user_paced_producer_and_reusable():
         plan.close()
 
 
-@pytest.mark.parametrize("method", [1, 0], ids=["bulk_copier", "vector_copier"])
+@pytest.mark.parametrize("method", [1, 0, 2], ids=["bulk_copier", "vector_copier", "copy_engines"])
 def test_out_of_order_producer_head_of_line(method):
     # "Triggered Plans", The kernel author's contract, item 1, and "Triggered SDMA Plans",
     # Testing (head-of-line ordering): a producer completes its chunks last to first.  The
@@ -177,6 +177,7 @@ def test_out_of_order_producer_head_of_line(method):
     scheds = [D.dtt_schedule_chunks(r * S, n, chunk, chunk, n) for r in range(P)]
     opts = D.dtt_plan_opts_default(method=method, piece_bytes=65536, stages=3) if method == D.COPY_TMA \
         else D.dtt_plan_opts_default(method=method, copier_threads=256)
+    opts.max_polls = 1 << 24         # the copy-engine proxy's bound: ~4 s
     plan = D.Plan(bufs, P * S, scheds, opts)
     for s_ in scheds:
         s_.free()
