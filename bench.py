@@ -900,14 +900,17 @@ def run_barrier(args):
     s = torch.cuda.current_stream()
     out = {}
     gen = 0
+    # arguments checked and marshalled once, as a caller that reuses its windows would do
+    hargs = D.HandrolledArgs(sig, y, status)
+    rargs = D.RevealArgs(x, data, yr, size, status)
     for name in ("handrolled", "reveal"):
         def one():
             nonlocal gen
             if name == "handrolled":
                 gen += 1
-                D.dtt_barrier_handrolled(sig, y, gen, 1 << 24, status, s)
+                D.dtt_barrier_handrolled(hargs, gen=gen, max_polls=1 << 24, stream=s)
             else:
-                b.reveal(x, data, yr, size, 1 << 24, status, s)
+                b.reveal(rargs, max_polls=1 << 24, stream=s)
         for _ in range(args.warmup):
             one()
         torch.cuda.synchronize()

@@ -334,10 +334,18 @@ class Plan:
                                      _stream(copy_stream), C.byref(out)))
         self._h = out
         self.handles = (dtt_handle * self.P)()
+        # the round's calls, looked up once (a round is four calls; their lookups are not free)
+        L = lib()
+        self._start, self._wait, self._next = L.dtt_plan_start, L.dtt_plan_wait, L.dtt_plan_next_round
+        self._stream_obj, self._stream_int = None, 0
 
     # the round
     def start(self, producer_stream=None):
-        _check(lib().dtt_plan_start(self._h, _stream(producer_stream), self.handles))
+        if producer_stream is not self._stream_obj:
+            self._stream_obj, self._stream_int = producer_stream, _stream(producer_stream)
+        rc = self._start(self._h, self._stream_int, self.handles)
+        if rc:
+            _check(rc)
         return self.handles
 
     def launch_copier(self) -> None:
@@ -350,13 +358,15 @@ class Plan:
 
     def wait(self, raise_on_error: bool = True) -> dtt_report:
         rep = dtt_report()
-        rc = lib().dtt_plan_wait(self._h, C.byref(rep))
-        if raise_on_error:
+        rc = self._wait(self._h, C.byref(rep))
+        if rc and raise_on_error:
             _check(rc)
         return rep
 
     def next_round(self) -> int:
-        _check(lib().dtt_plan_next_round(self._h))
+        rc = self._next(self._h)
+        if rc:
+            _check(rc)
         return self.round
 
     def close(self) -> int:
@@ -498,16 +508,36 @@ def fill_desc(dtype: str, seed: int, M: int, N: int, pitch: int, buf_bytes: int,
 
 
 def dtt_fill_producer(bufs, desc: dtt_fill_desc, handles, stream=None) -> None:
-    _check(lib().dtt_fill_producer(_ptr_array(bufs), len(bufs), C.byref(desc), handles,
-                                   _stream(stream)))
+    rc = lib().dtt_fill_producer(_ptr_array(bufs), len(bufs), C.byref(desc), handles, _stream(stream))
+    if rc:
+        _check(rc)
 
 
 def dtt_publish(handles, first_chunk: int, n_chunks: int, marks: int = 0, stream=None) -> None:
     _check(lib().dtt_publish(handles, len(handles), first_chunk, n_chunks, marks, _stream(stream)))
 
 
-def dtt_barrier_handrolled(signal, y, gen: int, max_polls: int, status, stream=None) -> None:
-    P = len(signal)
+class HandrolledArgs:
+    """The hand-rolled barrier's windows checked once and marshalled (see RevealArgs)."""
+
+    def __init__(self, signal, y, status):
+        P = len(signal)
+        _check_handrolled_args(P, signal, y, status)
+        self.P = P
+        self.signal, self.y, self.status = _ptr_array(signal), _ptr_array(y), _ptr(status)
+        self._keep = (signal, y, status)
+
+
+def dtt_barrier_handrolled(signal, y=None, gen: int = 1, max_polls: int = 1 << 24, status=None,
+                           stream=None) -> None:
+    """signal may be a HandrolledArgs (then y and status come from it)."""
+    a = signal if isinstance(signal, HandrolledArgs) else HandrolledArgs(signal, y, status)
+    rc = lib().dtt_barrier_handrolled(a.signal, a.y, a.P, gen, max_polls, a.status, _stream(stream))
+    if rc:
+        _check(rc)
+
+
+def _check_handrolled_args(P, signal, y, status) -> None:
     if len(y) != P:
         raise DttError(EINVAL, f"dtt_barrier_handrolled: y has {len(y)} windows, need P = {P}")
     for name, lst in (("signal", signal), ("y", y)):
@@ -518,8 +548,6 @@ def dtt_barrier_handrolled(signal, y, gen: int, max_polls: int, status, stream=N
     n = _elements(status)
     if status is None or (n is not None and n < P):
         raise DttError(EINVAL, f"dtt_barrier_handrolled: status holds {n} int32, need P = {P}")
-    _check(lib().dtt_barrier_handrolled(_ptr_array(signal), _ptr_array(y), len(signal), gen,
-                                        max_polls, _ptr(status), _stream(stream)))
 
 
 def _elements(t) -> Optional[int]:
@@ -548,6 +576,20 @@ def _check_reveal_args(who: str, P: int, x, data, y, size: int, status) -> None:
         raise DttError(EINVAL, f"{who}: status holds {n} int32, need P = {P}")
 
 
+class RevealArgs:
+    """The reveal's slices checked once (lengths, sizes, element type) and marshalled: pass it to
+    Barrier.reveal / dtt_barrier_reveal_noalloc in place of the three lists and the status
+    tensor when the same buffers are used call after call."""
+
+    def __init__(self, x, data, y, size: int, status, P: Optional[int] = None, who="reveal"):
+        P = len(x) if P is None else P
+        _check_reveal_args(who, P, x, data, y, size, status)
+        self.P, self.size = P, size
+        self.x, self.data, self.y = _ptr_array(x), _ptr_array(data), _ptr_array(y)
+        self.status = _ptr(status)
+        self._keep = (x, data, y, status)      # the tensors stay alive with the arrays
+
+
 class Barrier:
     """Owner of the builtin barrier's state (dtt_barrier*)."""
 
@@ -557,10 +599,16 @@ class Barrier:
         self._h = out
         self.P = P
 
-    def reveal(self, x, data, y, size: int, max_polls: int, status, stream=None) -> None:
-        _check_reveal_args("Barrier.reveal", self.P, x, data, y, size, status)
-        _check(lib().dtt_barrier_reveal(self._h, _ptr_array(x), _ptr_array(data), _ptr_array(y),
-                                        size, max_polls, _ptr(status), _stream(stream)))
+    def reveal(self, x, data=None, y=None, size: int = 0, max_polls: int = 1 << 24, status=None,
+               stream=None) -> None:
+        """y[r] = data[(r + 1) % P] after each rank staged x[r] into data[r] (see
+        dtt_barrier_reveal).  x may be a RevealArgs (then data, y, size and status come from it)."""
+        a = x if isinstance(x, RevealArgs) else RevealArgs(x, data, y, size, status, self.P, "Barrier.reveal")
+        if a.P != self.P:
+            raise DttError(EINVAL, f"Barrier.reveal: arguments for {a.P} ranks, barrier of {self.P}")
+        rc = lib().dtt_barrier_reveal(self._h, a.x, a.data, a.y, a.size, max_polls, a.status, _stream(stream))
+        if rc:
+            _check(rc)
 
     def destroy(self) -> None:
         if self._h and self._h.value:
@@ -578,13 +626,15 @@ def dtt_barrier_create(P: int) -> Barrier:
     return Barrier(P)
 
 
-def dtt_barrier_reveal_noalloc(x, data, y, size: int, max_polls: int, status, stream=None) -> None:
+def dtt_barrier_reveal_noalloc(x, data=None, y=None, size: int = 0, max_polls: int = 1 << 24,
+                               status=None, stream=None) -> None:
     """The builtin reveal with its counters in the library's fixed device array: allocates
     nothing (for callers that cannot allocate device memory at call time).  Calls that overlap
-    on the GPU share that array and race; run them on one stream."""
-    _check_reveal_args("dtt_barrier_reveal_noalloc", len(x), x, data, y, size, status)
-    _check(lib().dtt_barrier_reveal_noalloc(_ptr_array(x), _ptr_array(data), _ptr_array(y),
-                                            len(x), size, max_polls, _ptr(status), _stream(stream)))
+    on the GPU share that array and race; run them on one stream.  x may be a RevealArgs."""
+    a = x if isinstance(x, RevealArgs) else RevealArgs(x, data, y, size, status, None,
+                                                       "dtt_barrier_reveal_noalloc")
+    _check(lib().dtt_barrier_reveal_noalloc(a.x, a.data, a.y, a.P, a.size, max_polls, a.status,
+                                            _stream(stream)))
 
 
 def dtt_gemm_producer(A, Bt, bufs, M: int, N: int, K: int, ldc: int, slice_offs, num_programs: int,

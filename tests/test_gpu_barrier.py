@@ -78,3 +78,36 @@ def test_reveal(P, size):
         assert all(int(s.abs().sum()) == 0 for s in sig)   # no tally in any user window
     finally:
         b.destroy()
+
+
+def test_prepared_arguments_give_the_same_barriers():
+    # arguments checked and marshalled once (HandrolledArgs / RevealArgs), reused call after
+    # call: the same results as the list form, the page's columns and reveal
+    P, size = 8, 64
+    sig = [torch.zeros(P, dtype=torch.int32, device="cuda") for _ in range(P)]
+    y = [torch.zeros(P, dtype=torch.int32, device="cuda") for _ in range(P)]
+    status = torch.full((P,), 99, dtype=torch.int32, device="cuda")
+    ha = D.HandrolledArgs(sig, y, status)
+    for gen in (1, 2, 3):
+        D.dtt_barrier_handrolled(ha, gen=gen, max_polls=1 << 24)
+        torch.cuda.synchronize()
+        assert status.cpu().tolist() == [0] * P
+        want = OB.handrolled(np.zeros((P, P), dtype=np.int64), gen)
+        for r in range(P):
+            assert y[r].cpu().tolist() == want[r].tolist()
+    x_np = W.barrier_payload(P, size, seed=3)
+    x = [torch.from_numpy(x_np[r].copy()).cuda() for r in range(P)]
+    data = [torch.zeros(size, dtype=torch.int32, device="cuda") for _ in range(P)]
+    yr = [torch.zeros(size, dtype=torch.int32, device="cuda") for _ in range(P)]
+    ra = D.RevealArgs(x, data, yr, size, status)
+    b = D.Barrier(P)
+    try:
+        for _ in range(3):
+            b.reveal(ra, max_polls=1 << 24)
+            torch.cuda.synchronize()
+            assert status.cpu().tolist() == [0] * P
+            want = OB.reveal(x_np)
+            for r in range(P):
+                np.testing.assert_array_equal(yr[r].cpu().numpy(), want[r])
+    finally:
+        b.destroy()

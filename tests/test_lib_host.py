@@ -225,3 +225,17 @@ def test_binding_structs_match_the_c_header(tmp_path):
         assert int(got[name]) == C.sizeof(cls), name
         for f in cls._fields_:
             assert int(got[f"{name}.{f[0]}"]) == getattr(cls, f[0]).offset, (name, f[0])
+
+
+def test_prepared_barrier_arguments_are_checked_once_at_construction():
+    ok = [_i32(8) for _ in range(4)]
+    with pytest.raises(D.DttError):
+        D.RevealArgs(ok, ok[:3], ok, 8, _i32(4))
+    with pytest.raises(D.DttError):
+        D.HandrolledArgs(ok, ok, _i32(3))
+    a = D.RevealArgs(ok, ok, ok, 8, _i32(4))
+    assert a.P == 4 and a.size == 8
+    b = D.Barrier.__new__(D.Barrier)
+    b._h, b.P = C.c_void_p(0), 5
+    with pytest.raises(D.DttError):            # prepared for 4 ranks, barrier of 5
+        b.reveal(a)
