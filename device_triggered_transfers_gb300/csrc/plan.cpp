@@ -1026,6 +1026,25 @@ int dtt_plan_create(void* const* bufs, uint64_t buf_bytes, uint32_t P,
                         "32768 registers per SM)",
                         (unsigned long long)per_sm, (unsigned long long)thr, regs);
         }
+        if (o.method == DTT_COPY_TMA) {
+            // Every copier CTA must be resident at once: a copier CTA still waiting for shared
+            // memory keeps the (lower-priority) producer's CTAs from being scheduled, and the
+            // resident copier CTAs then wait for gates that nothing opens until their polls run out.
+            int sm_smem = 0, reserved = 0;
+            if (cudaDeviceGetAttribute(&sm_smem, cudaDevAttrMaxSharedMemoryPerMultiprocessor, p->device) != cudaSuccess ||
+                cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, p->device) != cudaSuccess) {
+                delete p;
+                return fail(DTT_ECUDA, "dtt_plan_create: cannot query the shared memory per SM");
+            }
+            const uint64_t need = per_sm * (bulk_smem_bytes(bulk_stage_bytes(o.piece_bytes), o.stages) + (uint64_t)reserved);
+            if (need > (uint64_t)sm_smem) {
+                delete p;
+                return fail(DTT_EINVAL,
+                            "dtt_plan_create: %llu copier CTA(s) per SM need %llu bytes of shared memory, the SM "
+                            "has %d: lower ctas_per_sm, stages or piece_bytes",
+                            (unsigned long long)per_sm, (unsigned long long)need, sm_smem);
+            }
+        }
     }
     rc = build_plan(p, scheds);
     if (rc == DTT_OK) rc = upload(p);

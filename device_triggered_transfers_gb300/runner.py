@@ -136,9 +136,9 @@ def sm_count() -> int:
 def bench_launch(w) -> dict:
     """The launch configuration the benchmark times for workload ``w`` (tests use it too).
 
-    Chunked workloads: the bulk-copy copier (three one-warp CTAs per SM, each with a ring of two
-    32 KiB stages, so the producer keeps the SM's threads and registers), and one program per
-    rank made of a group of
+    Chunked workloads: the bulk-copy copier (six one-warp CTAs per SM, each with a ring of two
+    16 KiB stages, so the producer keeps the SM's threads and registers; c2 rounds ~0.5-1 us
+    shorter than three CTAs with 32 KiB stages), and one program per rank made of a group of
     SMs / P CTAs (one per SM in all) that writes the rank's chunks in order and marks each once,
     so every rank's chunk k opens in wave k and the copier follows the waves.
     whole(): the bulk-copy copier (two CTAs per SM, 2 x 56 KiB stages each) over the contiguous
@@ -156,9 +156,9 @@ def bench_launch(w) -> dict:
     # leaves the round's critical path (c2: ~114 -> ~112 us per round).  whole() rounds are
     # bound by the host's launches, where the early launch only moves one: they launch at start.
     early = 2000
-    if w.kind == "chunks":     # three bulk-copy CTAs per SM: one thread alone cannot keep HBM busy
+    if w.kind == "chunks":     # six bulk-copy CTAs per SM: one thread alone cannot keep HBM busy
         return {"group": max(1, sms // len(w.senders())), "programs": 1, "threads": 256,
-                "opts": dtt_plan_opts_default(method=1, piece_bytes=32768, stages=2, ctas_per_sm=3,
+                "opts": dtt_plan_opts_default(method=1, piece_bytes=16384, stages=2, ctas_per_sm=6,
                                               early_copier_us=early)}
     if w.kind == "whole":
         # the copier is launched after the producer's launch (it has nothing to do before the

@@ -308,7 +308,9 @@ typedef struct dtt_report {
  * stays allocated ("Triggered Plans", The kernel author's contract).
  * Unless opts->deferred_copier is 1, the copier runs beside the producer, so its launch must leave
  * every SM room for producer CTAs: creation fails with DTT_EINVAL when the copier CTAs of one
- * SM would take more than 1024 threads or 32768 registers.
+ * SM would take more than 1024 threads or 32768 registers, or (bulk-copy path) more shared
+ * memory than the SM has (a copier CTA left waiting for shared memory would keep the producer
+ * from starting).
  * Errors: DTT_EINVAL, DTT_EOUTOFROWS, DTT_EOVERLAP, DTT_ECAPACITY, DTT_ENOMEM, DTT_ECUDA. */
 int dtt_plan_create(void* const* bufs, uint64_t buf_bytes, uint32_t P,
                     const dtt_schedule* const* scheds, const dtt_plan_opts* opts,

@@ -207,6 +207,26 @@ def test_copier_must_leave_room_for_the_producer():
         st.plan.close()
 
 
+def test_bulk_copier_whose_rings_cannot_all_be_resident_is_refused():
+    # four bulk-copy CTAs per SM with 2 x 32 KiB rings need more shared memory than an SM has: a
+    # copier CTA waiting for room would keep the producer from starting, so creation refuses
+    # it (unless the copier is deferred); three such CTAs fit
+    bufs = [torch.zeros(WS.buf_bytes, dtype=torch.uint8, device="cuda") for _ in range(2)]
+    for cps, stages, piece in [(4, 2, 32768), (3, 3, 32768), (2, 2, 65536)]:
+        with pytest.raises(D.DttError) as e:
+            D.Plan(bufs, WS.buf_bytes, runner.schedules_for(WS),
+                   D.dtt_plan_opts_default(method=D.COPY_TMA, ctas_per_sm=cps, stages=stages, piece_bytes=piece))
+        assert e.value.code == D.EINVAL and "shared memory" in str(e.value)
+    for opts in (D.dtt_plan_opts_default(method=D.COPY_TMA, ctas_per_sm=3, stages=2, piece_bytes=32768),
+                 D.dtt_plan_opts_default(method=D.COPY_TMA, ctas_per_sm=4, stages=2, piece_bytes=32768,
+                                         deferred_copier=1)):
+        st = runner.make(WS, opts=opts)
+        try:
+            assert runner.run_round(st).status == D.OK
+        finally:
+            st.plan.close()
+
+
 def test_bulk_copier_needs_two_stages():
     bufs = [torch.zeros(WS.buf_bytes, dtype=torch.uint8, device="cuda") for _ in range(2)]
     with pytest.raises(D.DttError) as e:
