@@ -54,17 +54,21 @@ class RoundLimitError(RuntimeError):
     pass
 
 
-def copy_region(src: np.ndarray, dst: np.ndarray, reg: S.Region) -> None:
-    """Copy one region between two byte buffers, at the same offsets."""
+def copy_region(src: np.ndarray, dst: np.ndarray, reg: S.Region,
+                dest: Optional[S.Region] = None) -> None:
+    """Copy one region between two byte buffers: to the same offsets, or to ``dest`` (the same
+    rows and width at another offset and pitch)."""
     off, rb, rows, pitch = reg
+    doff, _, _, dpitch = reg if dest is None else dest
     if rows == 0 or rb == 0:
         return
     if rows == 1:
-        dst[off:off + rb] = src[off:off + rb]
+        dst[doff:doff + rb] = src[off:off + rb]
         return
-    span = (rows - 1) * pitch + rb
-    sv = np.lib.stride_tricks.as_strided(src[off:off + span], shape=(rows, rb), strides=(pitch, 1))
-    dv = np.lib.stride_tricks.as_strided(dst[off:off + span], shape=(rows, rb), strides=(pitch, 1))
+    sv = np.lib.stride_tricks.as_strided(src[off:off + (rows - 1) * pitch + rb], shape=(rows, rb),
+                                         strides=(pitch, 1))
+    dv = np.lib.stride_tricks.as_strided(dst[doff:doff + (rows - 1) * dpitch + rb], shape=(rows, rb),
+                                         strides=(dpitch, 1))
     dv[...] = sv
 
 
@@ -73,7 +77,7 @@ class Plan:
 
     def __init__(self, bufs: Sequence[np.ndarray], schedules: Sequence[S.Schedule],
                  allgather: bool = True, initial_round: int = 1, validate: bool = True,
-                 copy_data: bool = True):
+                 copy_data: bool = True, dst_bufs: Optional[Sequence[np.ndarray]] = None):
         self.P = len(bufs)
         if len(schedules) != self.P:
             raise ValueError("one schedule per rank")
@@ -82,9 +86,13 @@ class Plan:
             raise ValueError("symmetric buffers must have one size")
         if not (1 <= initial_round <= ROUND_LIMIT):
             raise ValueError("initial round out of range")
+        if dst_bufs is not None and (len(dst_bufs) != self.P or any(len(b) != len(dst_bufs[0]) for b in dst_bufs)):
+            raise ValueError("one destination buffer per rank, all of one size")
         if validate:
-            S.validate(schedules, nbytes, allgather)
+            S.validate(schedules, nbytes, allgather,
+                       dst_bytes=None if dst_bufs is None else len(dst_bufs[0]))
         self.bufs = list(bufs)
+        self.dst = list(dst_bufs) if dst_bufs is not None else self.bufs   # where copies land
         self.copy_data = copy_data      # False: gate bookkeeping only (large workloads)
         self.schedules = list(schedules)
         self.first = S.first_chunks(schedules)
@@ -102,10 +110,9 @@ class Plan:
             s = self.owner[c]
             self.gates[s, c, READY] = prior
             self.gates[s, c, COUNTER] = prior * ch.writers
-            self.gates[s, c, COMPLETION] = prior * (self.P - 1)
-            for p in range(self.P):
-                if p != s:
-                    self.gates[p, c, ARRIVAL] = prior
+            self.gates[s, c, COMPLETION] = prior * len(ch.receivers(self.P, s))
+            for p in ch.receivers(self.P, s):
+                self.gates[p, c, ARRIVAL] = prior
         self.delivered = set()          # (chunk, peer) delivered in the current round
         self.delivery_log: List[Tuple[int, int, int]] = []   # (source, peer, chunk) in order
         self.state = "PREPARED"
@@ -131,8 +138,17 @@ class Plan:
                 self.groups_of[c].append(i)
         prior = self.round - 1
         self.group_counters = np.zeros((self.P, len(self.groups)), dtype=np.uint64)
-        for i, g in enumerate(self.groups):
-            self.group_counters[:, i] = prior * len(g)
+        for q in range(self.P):
+            for i in range(len(self.groups)):
+                self.group_counters[q, i] = prior * self.group_size(q, i)
+
+    def reaches(self, rank: int, c: int) -> bool:
+        """Does chunk c become readable at rank: it is rank's own, or rank receives it?"""
+        return self.owner[c] == rank or rank in self.chunks[c].receivers(self.P, self.owner[c])
+
+    def group_size(self, rank: int, g: int) -> int:
+        """Members of group g that become readable at rank each round."""
+        return sum(1 for c in self.groups[g] if self.reaches(rank, c))
 
     def chunk_readable(self, rank: int, c: int) -> bool:
         """Has chunk c become readable at rank this round (own chunk: gate open; another
@@ -142,8 +158,9 @@ class Plan:
         return int(self.gates[rank, c, ARRIVAL]) >= self.round
 
     def group_ready(self, rank: int, g: int) -> bool:
-        """The one test a group wait makes: the rank's counter of group g >= round * |g|."""
-        return int(self.group_counters[rank, g]) >= self.round * len(self.groups[g])
+        """The one test a group wait makes: the rank's counter of group g >= round * (members
+        that reach the rank; all of them unless chunks go to only some peers)."""
+        return int(self.group_counters[rank, g]) >= self.round * self.group_size(rank, g)
 
     def _count_group(self, rank: int, c: int) -> None:
         for g in self.groups_of[c]:
@@ -188,27 +205,29 @@ class Plan:
         word holds round * (P - 1)."""
         if self.owner[c] != rank:
             raise ValueError("reusable is asked of a rank's own chunk")
-        return int(self.gates[rank, c, COMPLETION]) >= self.round * (self.P - 1)
+        return int(self.gates[rank, c, COMPLETION]) >= self.round * len(self.chunks[c].receivers(self.P, rank))
 
     def gate_open(self, c: int) -> bool:
         s = self.owner[c]
         return (int(self.gates[s, c, READY]) & 0xFFFFFFFF) >= self.round
 
     def copier_progress(self) -> int:
-        """Run every (source, peer) queue as far as its gates allow; returns deliveries made."""
+        """Run every (source, peer) queue as far as its gates allow; returns deliveries made.
+        Queue (s, p) holds s's chunks addressed to p, in schedule order."""
         n = 0
         for s in range(self.P):
             for p in range(self.P):
                 if p == s:
                     continue
                 for c in self.chunks_of(s):
-                    if (c, p) in self.delivered:
+                    ch = self.chunks[c]
+                    if p not in ch.receivers(self.P, s) or (c, p) in self.delivered:
                         continue
                     if not self.gate_open(c):
                         break                       # head of line: later chunks wait
                     if self.copy_data:
-                        for reg in self.chunks[c].regions:
-                            copy_region(self.bufs[s], self.bufs[p], reg)
+                        for i, reg in enumerate(ch.regions):
+                            copy_region(self.bufs[s], self.dst[p], reg, ch.dest_region(i))
                     self.signal_arrival(s, p, c)
                     self.delivered.add((c, p))
                     self.delivery_log.append((s, p, c))
@@ -228,7 +247,7 @@ class Plan:
                 extra.append(c)
             elif cnt < R * ch.writers:
                 short.append(c)
-            elif any(int(self.gates[p, c, ARRIVAL]) < R for p in range(self.P) if p != s):
+            elif any(int(self.gates[p, c, ARRIVAL]) < R for p in ch.receivers(self.P, s)):
                 short.append(c)
         if extra:
             self.state = "FAILED"

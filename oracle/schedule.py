@@ -22,6 +22,16 @@ Sources ("Triggered Plans", Iris docs, section Model and section Requirements an
 
 A region is the tuple ``(offset, row_bytes, rows, pitch)``; a byte range has ``rows == 1`` and
 ``pitch == row_bytes``.  Offsets are relative to the start of the buffer.
+
+Other destinations ("Triggered Plans", Not supported yet: a copy cannot change offset, pitch or
+buffer, and a chunk cannot go to only some peers; reduce-scatter and two-shot all-reduce need
+both).  Reading: a chunk may name, per region, a destination ``(offset, pitch)`` -- the same
+rows of the same width land there instead of at the source's offset -- and a set of receiving
+peers (a bit mask; none given: every other rank).  The destination is the receiving rank's
+buffer, or its destination buffer when the plan has separate ones (a staging buffer).  The
+checks that keep ranks from sending the same bytes extend to destinations: no two copies land
+on the same bytes of one buffer, and, in place, no copy lands on bytes the receiving rank
+itself sends.
 """
 from __future__ import annotations
 
@@ -40,10 +50,24 @@ Region = Tuple[int, int, int, int]   # (offset, row_bytes, rows, pitch)
 class Chunk:
     regions: List[Region]
     writers: int
+    dests: Optional[List[Tuple[int, int]]] = None   # per region (dst offset, dst pitch); None: same
+    peers: Optional[int] = None                     # receiving ranks as a bit mask; None: all
 
     @property
     def nbytes(self) -> int:
         return sum(rb * rows for (_, rb, rows, _) in self.regions)
+
+    def dest_region(self, i: int) -> Region:
+        """Where region i lands: the same rows and width at the destination offset and pitch."""
+        off, rb, rows, pitch = self.regions[i]
+        if self.dests is None:
+            return self.regions[i]
+        doff, dpitch = self.dests[i]
+        return (doff, rb, rows, dpitch if rows > 1 else rb)
+
+    def receivers(self, P: int, owner: int) -> List[int]:
+        """The ranks this chunk is copied to (never its owner)."""
+        return [q for q in range(P) if q != owner and (self.peers is None or (self.peers >> q) & 1)]
 
 
 @dataclass
@@ -188,15 +212,58 @@ def region_byte_mask(reg: Region, nbytes: int) -> np.ndarray:
 
 
 def validate(schedules: Sequence[Schedule], buf_bytes: int, allgather: bool,
-             max_regions: Optional[int] = None) -> None:
+             max_regions: Optional[int] = None, dst_bytes: Optional[int] = None) -> None:
     """Reject a plan the pages say must not be created (raises PlanError).
 
     * every region lies inside the buffer;
     * all-gather: rank r's regions lie inside its own rows, bytes [r*S, (r+1)*S) with
       S = buf_bytes / P;
-    * no byte is sent by two ranks (checked byte by byte);
-    * optional capacity: at most ``max_regions`` regions in the plan.
+    * no byte is sent by two ranks to the same offsets (checked byte by byte);
+    * optional capacity: at most ``max_regions`` regions in the plan;
+    * destinations (see the module notes): inside the destination buffer (``dst_bytes`` when the
+      plan has separate destination buffers, else the buffer), no two copies on the same bytes
+      of one buffer, and in place no copy on bytes its receiving rank sends.
     """
+    _validate_sources(schedules, buf_bytes, allgather, max_regions)
+    _validate_destinations(schedules, buf_bytes, dst_bytes)
+
+
+def _validate_destinations(schedules: Sequence[Schedule], buf_bytes: int,
+                           dst_bytes: Optional[int]) -> None:
+    P = len(schedules)
+    nbytes = buf_bytes if dst_bytes is None else dst_bytes
+    for r, sch in enumerate(schedules):
+        for ch in sch.chunks:
+            if ch.dests is not None and len(ch.dests) != len(ch.regions):
+                raise PlanError("EINVAL", "one destination per region")
+            if ch.peers is not None and (ch.peers >> P):
+                raise PlanError("EINVAL", "peer mask names a rank outside the plan")
+    for q in range(P):
+        landed = np.zeros(nbytes, dtype=bool)
+        if dst_bytes is None:            # in place: q's own sent bytes are not to be overwritten
+            for ch in schedules[q].chunks:
+                for reg in ch.regions:
+                    landed |= region_byte_mask(reg, nbytes)
+        for r, sch in enumerate(schedules):
+            for ch in sch.chunks:
+                if q not in ch.receivers(P, r):
+                    continue
+                for i in range(len(ch.regions)):
+                    d = ch.dest_region(i)
+                    doff, rb, rows, dpitch = d
+                    if rows > 1 and dpitch < rb:
+                        raise PlanError("EINVAL", "destination rows overlap (pitch < row_bytes)")
+                    lo, hi = region_extent(d)
+                    if lo < 0 or hi > nbytes:
+                        raise PlanError("EINVAL", "destination outside the buffer")
+                    m = region_byte_mask(d, nbytes)
+                    if np.any(landed & m):
+                        raise PlanError("EOVERLAP", f"two copies land on the same bytes of buffer {q}")
+                    landed |= m
+
+
+def _validate_sources(schedules: Sequence[Schedule], buf_bytes: int, allgather: bool,
+                      max_regions: Optional[int]) -> None:
     P = len(schedules)
     if P < 1:
         raise PlanError("EINVAL", "no ranks")
@@ -219,6 +286,8 @@ def validate(schedules: Sequence[Schedule], buf_bytes: int, allgather: bool,
                     raise PlanError("EINVAL", "region outside the buffer")
                 if allgather and not (r * S <= lo and hi <= (r + 1) * S):
                     raise PlanError("EOUTOFROWS", f"rank {r} region outside its own rows")
+                if ch.dests is not None:
+                    continue        # lands elsewhere: the destination checks govern it
                 m = region_byte_mask(reg, buf_bytes)
                 clash = owner[m]
                 if np.any((clash >= 0) & (clash != r)):

@@ -81,6 +81,8 @@ class ThreadedRound:
         plan = self.plan
         log = self.queue_log.setdefault((s, p), [])
         for c in plan.chunks_of(s):
+            if p not in plan.chunks[c].receivers(plan.P, s):
+                continue                    # not on this queue
             polls = 0
             while not self._ready(c):
                 polls += 1
@@ -89,8 +91,9 @@ class ThreadedRound:
                         self.timeouts.append((s, p, c))
                     return
                 time.sleep(self.poll_sleep)
-            for reg in plan.chunks[c].regions:
-                copy_region(plan.bufs[s], plan.bufs[p], reg)
+            ch = plan.chunks[c]
+            for i, reg in enumerate(ch.regions):
+                copy_region(plan.bufs[s], plan.dst[p], reg, ch.dest_region(i))
             with self.lock:
                 plan.signal_arrival(s, p, c)
                 plan.delivered.add((c, p))
@@ -111,10 +114,14 @@ class ThreadedRound:
         ok = True
         for c in plan.groups[g]:
             s = plan.owner[c]
-            for (off, nb, rows, pitch) in plan.chunks[c].regions:
+            if s == rank or not plan.reaches(rank, c):
+                continue                    # its own bytes, or not addressed to this rank
+            ch = plan.chunks[c]
+            for j, (off, nb, rows, pitch) in enumerate(ch.regions):
+                doff, _, _, dpitch = ch.dest_region(j)
                 for i in range(rows):
-                    a = off + i * pitch
-                    ok = ok and bool(np.array_equal(plan.bufs[rank][a:a + nb], plan.bufs[s][a:a + nb]))
+                    a, d = off + i * pitch, doff + i * dpitch
+                    ok = ok and bool(np.array_equal(plan.dst[rank][d:d + nb], plan.bufs[s][a:a + nb]))
         self.consumer_results[(rank, g)] = "ok" if ok else "stale"
 
     def run(self, close_after: Optional[float] = None):

@@ -394,3 +394,147 @@ def test_group_exhaustive_interleavings_tiny_plan():
                 for g, members in enumerate(groups):
                     assert plan.group_ready(q, g) == all(plan.chunk_readable(q, c) for c in members)
         assert all(plan.group_ready(q, g) for q in range(P) for g in range(2))
+
+
+# ---- other destinations ("Triggered Plans", Not supported yet: "Other destinations") ---------------
+def _reduce_scatter_plan(P, B, dst_bufs=False, initial_round=1):
+    """Rank s holds P partial blocks of B bytes at [0, P*B) and a staging area of P slots at
+    [P*B, 2*P*B).  Chunk b of rank s is its partial block b, sent only to rank b, landing in
+    rank b's staging slot s (or in rank b's separate destination buffer, slot s)."""
+    nbytes = 2 * P * B
+    bufs = [np.zeros(nbytes, dtype=np.uint8) for _ in range(P)]
+    dst = [np.zeros(P * B, dtype=np.uint8) for _ in range(P)] if dst_bufs else None
+    scheds = []
+    for s in range(P):
+        chunks = []
+        for b in range(P):
+            if b == s:
+                continue
+            slot = (s * B) if dst_bufs else (P * B + s * B)
+            chunks.append(S.Chunk([(b * B, B, 1, B)], 1, dests=[(slot, B)], peers=1 << b))
+        scheds.append(S.Schedule(chunks))
+    plan = PL.Plan(bufs, scheds, allgather=False, initial_round=initial_round, dst_bufs=dst)
+    return plan
+
+
+@pytest.mark.parametrize("dst_bufs", [False, True])
+def test_reduce_scatter_staging_closed_form(dst_bufs):
+    # every rank's partial for block b lands in rank b's slot of its own rank number, nowhere
+    # else; arrivals only at the receiver; completion counts one receiver per chunk
+    P, B = 4, 16
+    plan = _reduce_scatter_plan(P, B, dst_bufs)
+    for R in (1, 2, 3):
+        plan.start()
+        for s in range(P):
+            plan.bufs[s][:P * B] = (np.arange(P * B) * 7 + 31 * s + 101 * R) % 251
+            for c in plan.chunks_of(s):
+                plan.mark_ready(s, c)
+        plan.copier_progress()
+        assert plan.wait()[0] == PL.OK
+        for b in range(P):
+            base = 0 if dst_bufs else P * B
+            out = plan.dst[b]
+            for s in range(P):
+                slot = out[base + s * B: base + (s + 1) * B]
+                if s == b:
+                    assert np.all(slot == 0)                  # nothing lands in one's own slot
+                else:
+                    assert np.array_equal(slot, plan.bufs[s][b * B:(b + 1) * B])
+        for c in range(plan.G):
+            s = plan.owner[c]
+            (b,) = plan.chunks[c].receivers(P, s)
+            for q in range(P):
+                assert int(plan.gates[q, c, ARRIVAL]) == (R if q == b else 0)
+            assert int(plan.gates[s, c, COMPLETION]) == R
+        plan.next_round()
+
+
+def test_pitched_destination_lands_row_by_row():
+    # a 2D window of 3 rows x 8 bytes (source pitch 16) lands with destination pitch 40
+    src_reg, dest = (4, 8, 3, 16), (100, 40)
+    bufs = [np.zeros(256, dtype=np.uint8) for _ in range(2)]
+    scheds = [S.Schedule([S.Chunk([src_reg], 1, dests=[dest])]), S.Schedule()]
+    plan = PL.Plan(bufs, scheds, allgather=False)
+    plan.start()
+    bufs[0][:64] = np.arange(64)
+    plan.mark_ready(0, 0)
+    plan.copier_progress()
+    assert plan.wait()[0] == PL.OK
+    want = np.zeros(256, dtype=np.uint8)
+    for i in range(3):
+        want[100 + 40 * i:108 + 40 * i] = np.arange(4 + 16 * i, 12 + 16 * i)
+    assert np.array_equal(bufs[1], want)
+
+
+def test_queues_hold_only_their_peers_chunks():
+    # rank 0's chunk 0 goes to rank 1 only and is never marked; chunk 1 goes to rank 2 only: it
+    # is not behind chunk 0 on any queue, so it arrives; chunk 2 (to everyone) waits behind
+    # chunk 0 on queue (0, 1) only
+    B = 8
+    bufs = [np.zeros(3 * 3 * B, dtype=np.uint8) for _ in range(3)]
+    scheds = [S.Schedule([S.Chunk([(0, B, 1, B)], 1, peers=0b010), S.Chunk([(B, B, 1, B)], 1, peers=0b100),
+                          S.Chunk([(2 * B, B, 1, B)], 1)]), S.Schedule(), S.Schedule()]
+    plan = PL.Plan(bufs, scheds, allgather=False)
+    plan.start()
+    plan.mark_ready(0, 1)
+    plan.mark_ready(0, 2)
+    plan.copier_progress()
+    assert int(plan.gates[2, 1, ARRIVAL]) == 1 and int(plan.gates[2, 2, ARRIVAL]) == 1
+    assert int(plan.gates[1, 2, ARRIVAL]) == 0          # head of line behind chunk 0 on (0, 1)
+    assert plan.reusable(0, 1) and not plan.reusable(0, 2)
+    status, short, extra = plan.wait()
+    assert status == PL.TIMEOUT and short == [0, 2]
+
+
+def test_destination_validation():
+    B = 8
+    def plan_of(scheds, nbytes=64, dst=None):
+        return PL.Plan([np.zeros(nbytes, dtype=np.uint8) for _ in range(len(scheds))], scheds,
+                       allgather=False, dst_bufs=dst)
+    # two ranks' copies land on the same bytes of rank 2
+    with pytest.raises(S.PlanError) as e:
+        plan_of([S.Schedule([S.Chunk([(0, B, 1, B)], 1, dests=[(40, B)], peers=0b100)]),
+                 S.Schedule([S.Chunk([(B, B, 1, B)], 1, dests=[(44, B)], peers=0b100)]), S.Schedule()])
+    assert e.value.code == "EOVERLAP"
+    # in place, a copy onto bytes the receiving rank itself sends
+    with pytest.raises(S.PlanError) as e:
+        plan_of([S.Schedule([S.Chunk([(0, B, 1, B)], 1, dests=[(16, B)])]),
+                 S.Schedule([S.Chunk([(16, B, 1, B)], 1, peers=0b01)])])
+    assert e.value.code == "EOVERLAP"
+    # ... allowed into separate destination buffers
+    plan_of([S.Schedule([S.Chunk([(0, B, 1, B)], 1, dests=[(16, B)])]),
+             S.Schedule([S.Chunk([(16, B, 1, B)], 1, peers=0b01)])], dst=[np.zeros(32, np.uint8)] * 2)
+    for bad in (S.Chunk([(0, B, 1, B)], 1, dests=[(60, B)]),              # past the end
+                S.Chunk([(0, B, 2, B)], 1, dests=[(0, B - 1)]),          # destination rows overlap
+                S.Chunk([(0, B, 1, B)], 1, dests=[]),                     # one destination per region
+                S.Chunk([(0, B, 1, B)], 1, peers=0b100)):                 # a rank outside the plan
+        with pytest.raises(S.PlanError) as e:
+            plan_of([S.Schedule([bad]), S.Schedule()])
+        assert e.value.code == "EINVAL"
+
+
+def test_groups_with_chunks_for_some_peers():
+    # a group counts, at each rank, only the members that reach it (its own, or addressed to
+    # it); the wait passes exactly when those are readable there, at every step of random orders
+    rng = np.random.default_rng(12)
+    P, B = 4, 8
+    plan = _reduce_scatter_plan(P, B)
+    groups = [[c for c in range(plan.G) if plan.chunks[c].receivers(P, plan.owner[c]) == [b]]
+              for b in range(P)] + [list(range(plan.G))]
+    plan.define_groups(groups)
+    for R in (1, 2):
+        plan.start()
+        marks = [(r, c) for r in range(P) for c in plan.chunks_of(r)]
+        for i in rng.permutation(len(marks)):
+            plan.mark_ready(*marks[i])
+            if rng.random() < 0.5:
+                plan.copier_progress()
+            for q in range(P):
+                for g, members in enumerate(groups):
+                    want = all(plan.chunk_readable(q, c) for c in members if plan.reaches(q, c))
+                    assert plan.group_ready(q, g) == want
+        plan.copier_progress()
+        assert plan.wait()[0] == PL.OK
+        for q in range(P):
+            assert int(plan.group_counters[q, q]) == R * (P - 1)         # its P - 1 partials
+        plan.next_round()

@@ -112,3 +112,30 @@ def test_group_wait_times_out_on_a_missing_mark():
     assert status == PL.TIMEOUT and short == [3]
     assert tr.consumer_results[(0, 0)] == "timeout" and tr.consumer_results[(1, 0)] == "timeout"
     assert tr.consumer_results[(0, 1)] == "ok" and tr.consumer_results[(1, 1)] == "ok"
+
+
+def test_reduce_scatter_with_threads_and_group_waits():
+    # each rank sends partial block b only to rank b's staging slot; rank b's consumer waits once
+    # on the group of its P - 1 incoming partials and then reads them all
+    P, B = 3, 16
+    bufs = [np.zeros(2 * P * B, dtype=np.uint8) for _ in range(P)]
+    scheds = [S.Schedule([S.Chunk([(b * B, B, 1, B)], 1, dests=[(P * B + s * B, B)], peers=1 << b)
+                          for b in range(P) if b != s]) for s in range(P)]
+    plan = PL.Plan(bufs, scheds, allgather=False)
+    groups = [[c for c in range(plan.G) if plan.chunks[c].peers == 1 << b] for b in range(P)]
+    plan.define_groups(groups)
+    data = {s: ((np.arange(P * B) * 3 + 17 * s) % 256).astype(np.uint8) for s in range(P)}
+
+    def write_unit(rank, c, u):
+        off, nb, _, _ = plan.chunks[c].regions[0]
+        plan.bufs[rank][off:off + nb] = data[rank][off:off + nb]
+
+    order = {r: [(c, 0) for c in reversed(list(plan.chunks_of(r)))] for r in range(P)}
+    tr = ThreadedRound(plan, write_unit, order, group_waits=[(b, b) for b in range(P)],
+                       delay={(c, 0): 0.002 for c in range(plan.G)})
+    assert tr.run()[0] == PL.OK
+    assert all(tr.consumer_results[(b, b)] == "ok" for b in range(P))
+    for b in range(P):
+        for s in range(P):
+            if s != b:
+                assert np.array_equal(plan.bufs[b][P * B + s * B:P * B + (s + 1) * B], data[s][b * B:(b + 1) * B])
