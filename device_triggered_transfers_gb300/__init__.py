@@ -44,6 +44,10 @@ class dtt_region(C.Structure):
                 ("pitch", C.c_uint64)]
 
 
+class dtt_dest(C.Structure):
+    _fields_ = [("offset", C.c_uint64), ("pitch", C.c_uint64)]
+
+
 class dtt_order(C.Structure):
     _fields_ = [("kind", C.c_uint32), ("group_m", C.c_uint32)]
 
@@ -55,7 +59,7 @@ class dtt_plan_opts(C.Structure):
                 ("initial_round", C.c_uint32), ("max_polls", C.c_uint64),
                 ("max_regions", C.c_uint64), ("deferred_copier", C.c_uint32),
                 ("stages", C.c_uint32), ("time_copier", C.c_uint32), ("host_piece_bytes", C.c_uint32),
-                ("early_copier_us", C.c_uint32)]
+                ("dst_bufs", C.c_void_p), ("dst_bytes", C.c_uint64), ("early_copier_us", C.c_uint32)]
 
 
 class dtt_group_table(C.Structure):
@@ -68,7 +72,7 @@ class dtt_handle(C.Structure):
                 ("round", C.c_uint32), ("rank", C.c_uint32), ("P", C.c_uint32),
                 ("n_global", C.c_uint32), ("first_chunk", C.c_uint32), ("n_chunks", C.c_uint32),
                 ("flags", C.c_uint32), ("reserved", C.c_uint32), ("groups", dtt_group_table),
-                ("host_ready", C.c_void_p)]
+                ("peer_masks", C.c_void_p), ("host_ready", C.c_void_p)]
 
 
 class dtt_report(C.Structure):
@@ -112,6 +116,8 @@ _SIGS = {
                                            C.POINTER(dtt_order), ORDER_FN, _P, C.POINTER(_P)]),
     "dtt_schedule_empty": (C.c_int, [C.POINTER(_P)]),
     "dtt_schedule_add_chunk": (C.c_int, [_P, C.POINTER(dtt_region), _u32, _u32]),
+    "dtt_schedule_add_chunk_to": (C.c_int, [_P, C.POINTER(dtt_region), C.POINTER(dtt_dest), _u32, _u32, _u32]),
+    "dtt_schedule_get_dests": (C.c_int, [_P, _u32, C.POINTER(dtt_dest), _u64, C.POINTER(_u64), C.POINTER(_u32)]),
     "dtt_schedule_info": (C.c_int, [_P, C.POINTER(_u32), C.POINTER(_u64)]),
     "dtt_schedule_get": (C.c_int, [_P, _u32, C.POINTER(dtt_region), _u64, C.POINTER(_u64), C.POINTER(_u32)]),
     "dtt_schedule_free": (None, [_P]),
@@ -246,9 +252,29 @@ class Schedule:
     def chunks(self):
         return [self.chunk(i) for i in range(self.n_chunks)]
 
-    def add_chunk(self, regions, writers: int) -> None:
+    def add_chunk(self, regions, writers: int, dests=None, peers: int = 0) -> None:
+        """regions: (offset, row_bytes, rows, pitch) tuples; dests (optional): one (offset, pitch)
+        per region, where it lands; peers: bit mask of receiving ranks (0: every other rank)."""
         arr = (dtt_region * max(1, len(regions)))(*[dtt_region(*r) for r in regions])
-        _check(lib().dtt_schedule_add_chunk(self._h, arr, len(regions), writers))
+        if dests is None and not peers:
+            _check(lib().dtt_schedule_add_chunk(self._h, arr, len(regions), writers))
+            return
+        d = None
+        if dests is not None:
+            if len(dests) != len(regions):
+                raise DttError(EINVAL, "add_chunk: one destination per region")
+            d = (dtt_dest * max(1, len(dests)))(*[dtt_dest(*x) for x in dests])
+        _check(lib().dtt_schedule_add_chunk_to(self._h, arr, d, len(regions), writers, peers))
+
+    def dests(self, i: int):
+        """(list of (offset, pitch) or None when chunk i lands at its own offsets, peer mask)."""
+        n, m = _u64(), _u32()
+        _check(lib().dtt_schedule_get_dests(self._h, i, None, 0, C.byref(n), C.byref(m)))
+        if n.value == 0:
+            return None, m.value
+        arr = (dtt_dest * n.value)()
+        _check(lib().dtt_schedule_get_dests(self._h, i, arr, n.value, C.byref(n), C.byref(m)))
+        return [(x.offset, x.pitch) for x in arr], m.value
 
     def free(self) -> None:
         if self._h and self._h.value:
@@ -321,11 +347,22 @@ class Plan:
     """Owner of a dtt_plan* over P device buffers (kept alive here)."""
 
     def __init__(self, bufs: Sequence, buf_bytes: int, schedules: Sequence[Optional[Schedule]],
-                 opts: Optional[dtt_plan_opts] = None, copy_stream=None):
+                 opts: Optional[dtt_plan_opts] = None, copy_stream=None, dst_bufs=None,
+                 dst_bytes: int = 0):
+        """dst_bufs (optional): P separate destination buffers of dst_bytes each that every copy
+        lands in (opts.dst_bufs)."""
         self.bufs = list(bufs)
         self.P = len(self.bufs)
         self.buf_bytes = buf_bytes
         self.copy_stream = copy_stream
+        self.dst_bufs = list(dst_bufs) if dst_bufs is not None else None
+        if dst_bufs is not None:
+            if len(self.dst_bufs) != self.P:
+                raise DttError(EINVAL, "Plan: one destination buffer per rank")
+            opts = dtt_plan_opts.from_buffer_copy(opts) if opts is not None else dtt_plan_opts_default()
+            self._dst_arr = _ptr_array(self.dst_bufs)
+            opts.dst_bufs = C.cast(self._dst_arr, C.c_void_p).value
+            opts.dst_bytes = dst_bytes
         scheds = (C.c_void_p * self.P)(*[(s.handle.value if s is not None else None)
                                          for s in schedules])
         out = C.c_void_p()

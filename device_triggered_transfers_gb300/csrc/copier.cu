@@ -53,7 +53,8 @@ __device__ __forceinline__ void notify_host(const CopierParams& p, uint32_t c) {
 // fence followed by relaxed writes is a release pattern in the PTX memory model): it orders
 // every copy of the chunk -- this thread's, or those acquired from the CTAs that made them
 // through the piece counter -- before each of them.
-__device__ __forceinline__ void signal_arrivals(const CopierParams& p, uint32_t s, uint32_t c) {
+__device__ __forceinline__ void signal_arrivals(const CopierParams& p, uint32_t s, uint32_t c,
+                                                uint32_t peers, uint32_t receivers) {
     constexpr uint32_t kIdsInRegs = 4;
     uint32_t ga = 0, gb = 0, ids[kIdsInRegs];
     if (p.groups.counters) {
@@ -64,7 +65,7 @@ __device__ __forceinline__ void signal_arrivals(const CopierParams& p, uint32_t 
     }
     dtt_dev::fence_acq_rel();
     for (uint32_t q = 0; q < p.P; ++q) {
-        if (q == s) continue;
+        if (!((peers >> q) & 1u)) continue;
         uint64_t* prow = p.gates + ((uint64_t)q * p.n_global + c) * DTT_GATE_WORDS;
         if (p.flags & DTT_HANDLE_TIMESTAMPS) dtt_dev::st_relaxed(prow + DTT_GATE_T_ARRIVE, dtt_dev::globaltimer());
         dtt_dev::red_relaxed_add(prow + DTT_GATE_ARRIVAL, 1);
@@ -77,13 +78,13 @@ __device__ __forceinline__ void signal_arrivals(const CopierParams& p, uint32_t 
         }
     }
     uint64_t* row = p.gates + ((uint64_t)s * p.n_global + c) * DTT_GATE_WORDS;
-    dtt_dev::red_relaxed_add(row + DTT_GATE_COMPLETION, p.P - 1);
+    dtt_dev::red_relaxed_add(row + DTT_GATE_COMPLETION, receivers);
     notify_host(p, c);
 }
 
-// Copy one piece from buffer s to every other buffer: 16-byte vectors, kUnroll loads in
-// flight per thread, each value stored to all peers.
-__device__ __forceinline__ void copy_piece_vec(const CopierParams& p, uint32_t s,
+// Copy one piece from buffer s to each receiver's landing place: 16-byte vectors, kUnroll loads
+// in flight per thread, each value stored to every receiver (at the piece's destination).
+__device__ __forceinline__ void copy_piece_vec(const CopierParams& p, uint32_t s, uint32_t peers,
                                                const PieceDesc& pc) {
     const uint32_t rv = pc.row_bytes >> 4;
     const uint32_t total = rv * pc.rows;
@@ -91,7 +92,7 @@ __device__ __forceinline__ void copy_piece_vec(const CopierParams& p, uint32_t s
     const uint32_t stride = blockDim.x * kUnroll;
     for (uint32_t v0 = threadIdx.x; v0 < total; v0 += stride) {
         uint4 val[kUnroll];
-        uint64_t off[kUnroll];
+        uint64_t doff[kUnroll];
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
             const uint32_t v = v0 + u * blockDim.x;
@@ -101,34 +102,34 @@ __device__ __forceinline__ void copy_piece_vec(const CopierParams& p, uint32_t s
                     row = v / rv;
                     col = v - row * rv;
                 }
-                off[u] = (uint64_t)row * pc.pitch + ((uint64_t)col << 4);
-                val[u] = ld_cg16(src + off[u]);
+                val[u] = ld_cg16(src + (uint64_t)row * pc.pitch + ((uint64_t)col << 4));
+                doff[u] = (uint64_t)row * pc.dst_pitch + ((uint64_t)col << 4);
             }
         }
 #pragma unroll 1
         for (uint32_t q = 0; q < p.P; ++q) {
-            if (q == s) continue;
-            char* dst = p.bufs[q] + pc.off;
+            if (!((peers >> q) & 1u)) continue;
+            char* dst = p.dst[q] + pc.dst_off;
 #pragma unroll
             for (int u = 0; u < kUnroll; ++u) {
                 const uint32_t v = v0 + u * blockDim.x;
-                if (v < total) st_cs16(dst + off[u], val[u]);
+                if (v < total) st_cs16(dst + doff[u], val[u]);
             }
         }
     }
 }
 
 // Byte-wise copy for pieces that are not 16-byte aligned.
-__device__ __forceinline__ void copy_piece_bytes(const CopierParams& p, uint32_t s,
+__device__ __forceinline__ void copy_piece_bytes(const CopierParams& p, uint32_t s, uint32_t peers,
                                                  const PieceDesc& pc) {
     const uint64_t total = (uint64_t)pc.row_bytes * pc.rows;
     const uint8_t* src = reinterpret_cast<const uint8_t*>(p.bufs[s]) + pc.off;
     for (uint64_t b = threadIdx.x; b < total; b += blockDim.x) {
         const uint64_t row = b / pc.row_bytes, col = b - row * pc.row_bytes;
-        const uint64_t o = row * pc.pitch + col;
-        const uint8_t v = ld_cg8(src + o);
+        const uint8_t v = ld_cg8(src + row * pc.pitch + col);
+        const uint64_t o = pc.dst_off + row * pc.dst_pitch + col;
         for (uint32_t q = 0; q < p.P; ++q)
-            if (q != s) reinterpret_cast<uint8_t*>(p.bufs[q])[pc.off + o] = v;
+            if ((peers >> q) & 1u) reinterpret_cast<uint8_t*>(p.dst[q])[o] = v;
     }
 }
 
@@ -174,15 +175,15 @@ __device__ __forceinline__ void copier_body(const CopierParams& p) {
         for (uint32_t i = i0; i < cd.n_pieces; i += G) {
             const PieceDesc pc = p.pieces[cd.piece_begin + i];
             if (pc.vec)
-                copy_piece_vec(p, s, pc);
+                copy_piece_vec(p, s, cd.peers, pc);
             else
-                copy_piece_bytes(p, s, pc);
+                copy_piece_bytes(p, s, cd.peers, pc);
         }
         __syncthreads();   // every thread's stores of this chunk precede thread 0's release
         if (threadIdx.x == 0) {
             uint64_t* row = p.gates + ((uint64_t)s * p.n_global + c) * DTT_GATE_WORDS;
             const uint64_t done = dtt_dev::atom_add_acq_rel(row + DTT_GATE_COPIER, 1) + 1;
-            if (done == (uint64_t)p.round * cd.n_part) signal_arrivals(p, s, c);   // the chunk's last piece
+            if (done == (uint64_t)p.round * cd.n_part) signal_arrivals(p, s, c, cd.peers, cd.receivers);   // the chunk's last piece
         }
     }
 }
@@ -391,18 +392,19 @@ __device__ __forceinline__ void copier_bulk_body(const CopierParams& p) {
         }
         loads_hi = idx + 1;
     };
+    uint32_t peers = 0;        // receivers of the chunk being copied
     auto store = [&](const PieceDesc& pc, uint64_t idx) {
         const uint32_t st = (uint32_t)(idx % S);
         const uint32_t src = smem_addr(stage0 + (size_t)st * p.stage_bytes);
         for (uint32_t q = 0; q < p.P; ++q) {
-            if (q == s) continue;
-            if (pc.tmap != kNoMap) {
+            if (!((peers >> q) & 1u)) continue;
+            if (pc.tmap != kNoMap) {       // lands at its own offsets: the same map shape
                 tensor_store(p.tmaps + (size_t)pc.tmap * p.P + q, pc.x, pc.y, src, pol);
                 continue;
             }
-            char* dst = p.bufs[q] + pc.off;
+            char* dst = p.dst[q] + pc.dst_off;
             for (uint32_t r = 0; r < pc.rows; ++r)
-                bulk_store(dst + (uint64_t)r * pc.pitch, src + r * pc.row_bytes, pc.row_bytes, pol);
+                bulk_store(dst + (uint64_t)r * pc.dst_pitch, src + r * pc.row_bytes, pc.row_bytes, pol);
         }
         bulk_commit();
     };
@@ -416,6 +418,7 @@ __device__ __forceinline__ void copier_bulk_body(const CopierParams& p) {
             break;
         }
         fence_proxy_async_global();   // the producer's writes, acquired above, precede the bulk loads
+        peers = cd.peers;
         const uint32_t i0 = (j + G - cd.rot) % G;
         if (i0 >= cd.n_pieces) continue;
         const uint32_t n = (cd.n_pieces - i0 + G - 1) / G;       // my pieces of this chunk
@@ -443,7 +446,7 @@ __device__ __forceinline__ void copier_bulk_body(const CopierParams& p) {
         if (failed) break;
         uint64_t* row = p.gates + ((uint64_t)s * p.n_global + c) * DTT_GATE_WORDS;
         const uint64_t done = dtt_dev::atom_add_acq_rel(row + DTT_GATE_COPIER, 1) + 1;
-        if (done == (uint64_t)p.round * cd.n_part) signal_arrivals(p, s, c);
+        if (done == (uint64_t)p.round * cd.n_part) signal_arrivals(p, s, c, cd.peers, cd.receivers);
     }
     // leave nothing in flight: stores, and (after a failed wait) loads still landing in the ring
     bulk_wait_all();
@@ -497,7 +500,7 @@ __global__ void check_kernel(const __grid_constant__ CheckParams p) {
         const uint64_t err = dtt_dev::ld_relaxed(row + DTT_GATE_ERROR);
         bool arrived = true;
         for (uint32_t q = 0; q < p.P; ++q) {
-            if (q == cd.owner) continue;
+            if (!((cd.peers >> q) & 1u)) continue;
             const uint64_t* prow = p.gates + ((uint64_t)q * p.n_global + c) * DTT_GATE_WORDS;
             arrived &= dtt_dev::ld_relaxed(prow + DTT_GATE_ARRIVAL) >= p.round;
         }
@@ -554,7 +557,7 @@ __global__ void ce_signal_kernel(const __grid_constant__ CeSignalParams p) {
     if (threadIdx.x != 0) return;
     dtt_dev::fence_acq_rel();
     for (uint32_t q = 0; q < p.P; ++q) {
-        if (q == p.s) continue;
+        if (!((p.peers >> q) & 1u)) continue;
         uint64_t* prow = p.gates + ((uint64_t)q * p.n_global + p.c) * DTT_GATE_WORDS;
         if (p.flags & DTT_HANDLE_TIMESTAMPS) dtt_dev::st_relaxed(prow + DTT_GATE_T_ARRIVE, dtt_dev::globaltimer());
         dtt_dev::red_relaxed_add(prow + DTT_GATE_ARRIVAL, 1);
@@ -565,7 +568,7 @@ __global__ void ce_signal_kernel(const __grid_constant__ CeSignalParams p) {
         }
     }
     uint64_t* row = p.gates + ((uint64_t)p.s * p.n_global + p.c) * DTT_GATE_WORDS;
-    dtt_dev::red_relaxed_add(row + DTT_GATE_COMPLETION, p.P - 1);
+    dtt_dev::red_relaxed_add(row + DTT_GATE_COMPLETION, p.receivers);
     if (p.host_arrived)
         asm volatile("st.release.sys.global.u32 [%0], %1;" ::"l"(p.host_arrived + p.c), "r"(p.round) : "memory");
 }
@@ -596,20 +599,20 @@ __global__ void consumer_kernel(const __grid_constant__ CopierParams p, dtt_hand
                                 uint64_t max_polls, int32_t* status) {
     for (uint32_t c = blockIdx.x; c < p.n_global; c += gridDim.x) {
         const ChunkDesc cd = p.chunks[c];
-        if (cd.owner == h.rank) {
+        if (!((cd.peers >> h.rank) & 1u)) {       // its own chunk, or not addressed to it
             if (threadIdx.x == 0) status[c] = 0;
             continue;
         }
         const int w = dtt_wait(h, c, max_polls);
         if (threadIdx.x == 0) status[c] = w;
         if (w != 0) continue;
-        const char* src = p.bufs[h.rank];
+        const char* src = p.dst[h.rank];          // where this rank's copies landed
         for (uint32_t i = 0; i < cd.n_pieces; ++i) {
             const PieceDesc pc = p.pieces[cd.piece_begin + i];
             const uint64_t total = (uint64_t)pc.row_bytes * pc.rows;
             for (uint64_t x = threadIdx.x; x < total; x += blockDim.x) {
                 const uint64_t row = x / pc.row_bytes, col = x - row * pc.row_bytes;
-                const uint64_t o = pc.off + row * pc.pitch + col;
+                const uint64_t o = pc.dst_off + row * pc.dst_pitch + col;
                 dst[o] = src[o];
             }
         }

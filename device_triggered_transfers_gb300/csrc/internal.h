@@ -51,6 +51,8 @@ constexpr uint32_t kNoMap = 0xFFFFFFFFu;
 struct PieceDesc {
     uint64_t off;
     uint64_t pitch;
+    uint64_t dst_off;           // where it lands (the same as off unless the chunk has destinations)
+    uint64_t dst_pitch;
     uint32_t row_bytes;
     uint32_t rows;
     uint32_t vec;
@@ -69,6 +71,8 @@ struct ChunkDesc {
     uint32_t owner;
     uint32_t writers;
     uint64_t bytes;
+    uint32_t peers;             // receiving ranks as a bit mask (never the owner)
+    uint32_t receivers;         // popcount of peers
 };
 
 // Plan-wide device status block.
@@ -110,6 +114,7 @@ struct HostStatus {
 
 struct CopierParams {
     char* bufs[DTT_MAX_RANKS];
+    char* dst[DTT_MAX_RANKS];   // where copies land: the buffers, or the destination buffers
     const CUtensorMap* tmaps;   // bulk-copy path: [shape][rank] maps of the 2D windows (or null)
     uint64_t* gates;
     const ChunkDesc* chunks;
@@ -174,6 +179,7 @@ struct CeSignalParams {
     dtt_group_table groups;
     uint32_t* host_arrived;     // or null
     uint32_t P, n_global, s, c, round, flags;
+    uint32_t peers, receivers;  // the chunk's receiving ranks
 };
 cudaError_t launch_ce_signal(const CeSignalParams& p, cudaStream_t s);
 cudaError_t launch_consumer(const CopierParams& p, dtt_handle h, char* dst, uint64_t max_polls,
@@ -232,6 +238,8 @@ int preload_once();
 struct HostChunk {
     std::vector<dtt_region> regions;
     uint32_t writers;
+    std::vector<dtt_dest> dests;   // empty: every region lands at its own offsets
+    uint32_t peers = 0;            // DTT_ALL_PEERS or a bit mask of receiving ranks
 };
 
 }  // namespace dtt

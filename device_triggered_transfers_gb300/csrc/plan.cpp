@@ -48,6 +48,7 @@ struct CeProxy {
     std::vector<cudaEvent_t> ev;        // [s * P + q]
     std::vector<uint32_t> reg_begin;    // chunk c's regions: regs[reg_begin[c] .. reg_begin[c + 1])
     std::vector<dtt_region> regs;
+    std::vector<dtt_dest> dests;        // where each region lands
 };
 
 }  // namespace
@@ -56,6 +57,11 @@ struct dtt_plan {
     uint32_t P = 0;
     uint64_t buf_bytes = 0;
     char* bufs[DTT_MAX_RANKS] = {};
+    char* dst[DTT_MAX_RANKS] = {};    // where copies land: bufs, or the separate destination buffers
+    uint64_t dst_bytes = 0;
+    bool separate_dst = false;
+    bool other_dests = false;         // some chunk lands elsewhere or goes to only some peers
+    uint32_t* d_peer_masks = nullptr; // per global chunk, when other_dests
     dtt_plan_opts opts{};
     int device = 0;
 
@@ -65,6 +71,7 @@ struct dtt_plan {
     std::vector<ChunkDesc> chunks;
     std::vector<PieceDesc> pieces;
     std::vector<uint32_t> writers;
+    std::vector<uint32_t> peer_masks; // receivers of each global chunk
     std::vector<MapShape> shapes;     // bulk-copy path: the tensor-map shapes of the 2D windows
 
     uint32_t copier_ctas = 0;
@@ -191,6 +198,8 @@ void free_device(dtt_plan* p) {
     p->d_cons = nullptr;
     cudaFree(p->d_group_counters);
     cudaFree(p->d_group_arrays);
+    cudaFree(p->d_peer_masks);
+    p->d_peer_masks = nullptr;
     p->d_group_counters = nullptr;
     p->d_group_arrays = nullptr;
     p->ev_copier_end = nullptr;
@@ -249,17 +258,24 @@ bool tensor_window(const dtt_region& r, const CutCtx& cx) {
 }
 
 // Cut one region into copier pieces of at most piece_bytes: whole rows when a row fits,
-// otherwise column pieces of single rows.  On the bulk-copy path a 2D window's pieces of whole
-// rows (at most 256 rows each, the tallest box) are tensor-map boxes when the window allows it.
-void cut_region(const dtt_region& r, const CutCtx& cx, std::vector<PieceDesc>* out) {
+// otherwise column pieces of single rows.  Each piece lands at the matching rows and columns of
+// the region's destination `d`.  On the bulk-copy path a 2D window's pieces of whole rows (at
+// most 256 rows each, the tallest box) are tensor-map boxes when the window allows it and lands
+// at its own offsets (a box is stored through the same map shape it was loaded with).
+void cut_region(const dtt_region& r, const dtt_dest& d, const CutCtx& cx, std::vector<PieceDesc>* out) {
     const uint64_t piece_bytes = cx.piece_bytes;
-    auto push = [&](uint64_t off, uint64_t rb, uint64_t rows, uint64_t pitch, uint32_t tmap) {
+    const bool same_place = d.offset == r.offset && (r.rows <= 1 || d.pitch == r.pitch);
+    auto push = [&](uint64_t off, uint64_t doff, uint64_t rb, uint64_t rows, uint64_t pitch, uint64_t dpitch,
+                    uint32_t tmap) {
         PieceDesc pc{};
         pc.off = off;
         pc.pitch = rows > 1 ? pitch : rb;
+        pc.dst_off = doff;
+        pc.dst_pitch = rows > 1 ? dpitch : rb;
         pc.row_bytes = (uint32_t)rb;
         pc.rows = (uint32_t)rows;
-        pc.vec = cx.bases_aligned && (off % 16 == 0) && (rb % 16 == 0) && (rows <= 1 || pitch % 16 == 0);
+        pc.vec = cx.bases_aligned && (off % 16 == 0) && (rb % 16 == 0) && (rows <= 1 || pitch % 16 == 0) &&
+                 (doff % 16 == 0) && (rows <= 1 || dpitch % 16 == 0);
         pc.tmap = tmap;
         if (tmap != kNoMap) {
             pc.x = (uint32_t)((off % pitch) / 8);
@@ -271,9 +287,10 @@ void cut_region(const dtt_region& r, const CutCtx& cx, std::vector<PieceDesc>* o
     if (r.row_bytes >= piece_bytes) {
         for (uint64_t i = 0; i < r.rows; ++i)
             for (uint64_t c = 0; c < r.row_bytes; c += piece_bytes)
-                push(r.offset + i * r.pitch + c, std::min(piece_bytes, r.row_bytes - c), 1, 0, kNoMap);
+                push(r.offset + i * r.pitch + c, d.offset + i * d.pitch + c, std::min(piece_bytes, r.row_bytes - c), 1,
+                     0, 0, kNoMap);
     } else {
-        const bool tensor = tensor_window(r, cx);
+        const bool tensor = same_place && tensor_window(r, cx);
         uint64_t per = std::max<uint64_t>(1, piece_bytes / r.row_bytes);
         if (tensor) per = std::min<uint64_t>(per, 256);
         for (uint64_t i = 0; i < r.rows; i += per) {
@@ -281,7 +298,7 @@ void cut_region(const dtt_region& r, const CutCtx& cx, std::vector<PieceDesc>* o
             const uint32_t tmap = tensor && rows > 1
                 ? shape_of(MapShape{(uint32_t)(r.row_bytes / 8), (uint32_t)rows, r.pitch}, cx.shapes)
                 : kNoMap;
-            push(r.offset + i * r.pitch, r.row_bytes, rows, r.pitch, tmap);
+            push(r.offset + i * r.pitch, d.offset + i * d.pitch, r.row_bytes, rows, r.pitch, d.pitch, tmap);
         }
     }
 }
@@ -386,8 +403,8 @@ dtt_group_table group_table(const dtt_plan* p) {
     if (!p->n_groups) return t;
     t.counters = p->d_group_counters;
     t.size = p->d_group_arrays;
-    t.chunk_off = p->d_group_arrays + p->n_groups;
-    t.chunk_ids = p->d_group_arrays + p->n_groups + (p->n_global + 1);
+    t.chunk_off = p->d_group_arrays + (size_t)p->P * p->n_groups;
+    t.chunk_ids = p->d_group_arrays + (size_t)p->P * p->n_groups + (p->n_global + 1);
     t.n_groups = p->n_groups;
     return t;
 }
@@ -405,6 +422,7 @@ dtt_handle make_handle(const dtt_plan* p, uint32_t r) {
     h.n_chunks = p->n_chunks[r];
     h.flags = p->opts.timestamps ? DTT_HANDLE_TIMESTAMPS : 0u;
     h.groups = group_table(p);
+    h.peer_masks = p->d_peer_masks;
     h.host_ready = p->ce ? p->ce->h_ready_dev : nullptr;
     return h;
 }
@@ -413,6 +431,7 @@ CopierParams copier_params(const dtt_plan* p) {
     CopierParams cp{};
     for (uint32_t r = 0; r < p->P; ++r) {
         cp.bufs[r] = p->bufs[r];
+        cp.dst[r] = p->dst[r];
         cp.first_chunk[r] = p->first_chunk[r];
         cp.n_chunks[r] = p->n_chunks[r];
     }
@@ -513,25 +532,27 @@ int ce_issue(dtt_plan* p, uint32_t s, uint32_t c, uint32_t round) {
     CeProxy& ce = *p->ce;
     const uint32_t P = p->P;
     uint32_t last = UINT32_MAX;
+    const uint32_t peers = p->chunks[c].peers;
     for (uint32_t q = 0; q < P; ++q) {
-        if (q == s) continue;
+        if (!((peers >> q) & 1u)) continue;
         cudaStream_t st = ce.streams[s * P + q];
         for (uint32_t i = ce.reg_begin[c]; i < ce.reg_begin[c + 1]; ++i) {
             const dtt_region& r = ce.regs[i];
+            const dtt_dest& d = ce.dests[i];
             if (r.rows == 0 || r.row_bytes == 0) continue;
             if (r.rows == 1)
-                DTT_CUDA_TRY(cudaMemcpyAsync(p->bufs[q] + r.offset, p->bufs[s] + r.offset, r.row_bytes,
+                DTT_CUDA_TRY(cudaMemcpyAsync(p->dst[q] + d.offset, p->bufs[s] + r.offset, r.row_bytes,
                                              cudaMemcpyDeviceToDevice, st));
             else
-                DTT_CUDA_TRY(cudaMemcpy2DAsync(p->bufs[q] + r.offset, r.pitch, p->bufs[s] + r.offset, r.pitch,
+                DTT_CUDA_TRY(cudaMemcpy2DAsync(p->dst[q] + d.offset, d.pitch, p->bufs[s] + r.offset, r.pitch,
                                                r.row_bytes, r.rows, cudaMemcpyDeviceToDevice, st));
         }
         last = q;
     }
-    if (last == UINT32_MAX) return DTT_OK;        // one rank: nothing to copy or signal
+    if (last == UINT32_MAX) return DTT_OK;        // no receivers: nothing to copy or signal
     cudaStream_t sl = ce.streams[s * P + last];
     for (uint32_t q = 0; q < P; ++q) {
-        if (q == s || q == last) continue;
+        if (q == last || !((peers >> q) & 1u)) continue;
         DTT_CUDA_TRY(cudaEventRecord(ce.ev[s * P + q], ce.streams[s * P + q]));
         DTT_CUDA_TRY(cudaStreamWaitEvent(sl, ce.ev[s * P + q], 0));
     }
@@ -545,6 +566,8 @@ int ce_issue(dtt_plan* p, uint32_t s, uint32_t c, uint32_t round) {
     sp.c = c;
     sp.round = round;
     sp.flags = p->opts.timestamps ? DTT_HANDLE_TIMESTAMPS : 0u;
+    sp.peers = peers;
+    sp.receivers = p->chunks[c].receivers;
     DTT_CUDA_TRY(launch_ce_signal(sp, sl));
     return DTT_OK;
 }
@@ -629,6 +652,8 @@ int start_ce(dtt_plan* p, const dtt_schedule* const* scheds) {
         if (!sc) continue;
         for (const HostChunk& ch : sc->chunks) {
             ce.regs.insert(ce.regs.end(), ch.regions.begin(), ch.regions.end());
+            for (size_t i = 0; i < ch.regions.size(); ++i)
+                ce.dests.push_back(ch.dests.empty() ? dtt_dest{ch.regions[i].offset, ch.regions[i].pitch} : ch.dests[i]);
             ce.reg_begin.push_back((uint32_t)ce.regs.size());
         }
     }
@@ -690,6 +715,65 @@ int ce_join(dtt_plan* p, cudaStream_t after) {
     return ce.rc;
 }
 
+// Does rank q receive a chunk of rank r with peer mask `peers`?
+inline bool receives(uint32_t peers, uint32_t r, uint32_t q) {
+    return q != r && (peers == 0 || ((peers >> q) & 1u));
+}
+
+// Destinations ("Triggered Plans", Not supported yet, "Other destinations", as this library reads
+// it): every copy lands inside its receiving buffer, no two copies land on the same bytes of one
+// buffer, and in place no copy lands on bytes its receiving rank itself sends.
+int validate_destinations(const dtt_plan* p, const dtt_schedule* const* scheds) {
+    const uint32_t P = p->P;
+    const uint64_t nbytes = p->separate_dst ? p->dst_bytes : p->buf_bytes;
+    std::vector<dtt_region> landed;   // one buffer's landed (and, in place, sent) windows
+    std::vector<RegionRef> refs;
+    for (uint32_t q = 0; q < P; ++q) {
+        landed.clear();
+        refs.clear();
+        std::vector<uint32_t> who;    // rank of each entry: q itself for its sent windows
+        if (!p->separate_dst && scheds && scheds[q])
+            for (const HostChunk& ch : scheds[q]->chunks)
+                for (const dtt_region& reg : ch.regions) {
+                    landed.push_back(reg);
+                    who.push_back(q);
+                }
+        for (uint32_t r = 0; r < P; ++r) {
+            const dtt_schedule* s = scheds ? scheds[r] : nullptr;
+            if (!s) continue;
+            for (const HostChunk& ch : s->chunks) {
+                if (!receives(ch.peers, r, q)) continue;
+                for (size_t i = 0; i < ch.regions.size(); ++i) {
+                    const dtt_region& reg = ch.regions[i];
+                    dtt_region d = reg;
+                    if (!ch.dests.empty()) {
+                        d.offset = ch.dests[i].offset;
+                        d.pitch = reg.rows > 1 ? ch.dests[i].pitch : reg.row_bytes;
+                    }
+                    if (d.rows == 0 || d.row_bytes == 0) continue;
+                    const uint64_t span = (d.rows - 1) * d.pitch + d.row_bytes;
+                    if (d.offset > nbytes || span > nbytes - d.offset)
+                        return fail(DTT_EINVAL, "plan: a chunk of rank %u lands outside rank %u's %llu-byte buffer",
+                                    r, q, (unsigned long long)nbytes);
+                    landed.push_back(d);
+                    who.push_back(r);
+                }
+            }
+        }
+        for (size_t i = 0; i < landed.size(); ++i) {
+            const dtt_region& d = landed[i];
+            refs.push_back(RegionRef{d.offset, d.offset + (d.rows - 1) * d.pitch + d.row_bytes, who[i], &landed[i]});
+        }
+        std::sort(refs.begin(), refs.end(), [](const RegionRef& a, const RegionRef& b) { return a.lo < b.lo; });
+        for (size_t i = 0; i < refs.size(); ++i)
+            for (size_t k = i + 1; k < refs.size() && refs[k].lo < refs[i].hi; ++k)
+                if (regions_intersect(*refs[i].reg, *refs[k].reg))
+                    return fail(DTT_EOVERLAP, "plan: copies from ranks %u and %u land on the same bytes of rank %u's buffer",
+                                refs[i].rank, refs[k].rank, q);
+    }
+    return DTT_OK;
+}
+
 int validate_plan(dtt_plan* p, const dtt_schedule* const* scheds) {
     const uint32_t P = p->P;
     // ---- validation --------------------------------------------------------------------
@@ -705,6 +789,11 @@ int validate_plan(dtt_plan* p, const dtt_schedule* const* scheds) {
         if (!s) continue;
         for (const HostChunk& ch : s->chunks) {
             if (ch.writers == 0) return fail(DTT_EINVAL, "plan: rank %u has a chunk with no writers", r);
+            if (!ch.dests.empty() && ch.dests.size() != ch.regions.size())
+                return fail(DTT_EINVAL, "plan: rank %u has a chunk with a destination count unlike its regions", r);
+            if (P < 32 && (ch.peers >> P))
+                return fail(DTT_EINVAL, "plan: rank %u's peer mask names a rank outside the plan", r);
+            if (!ch.dests.empty() || ch.peers) p->other_dests = true;
             for (const dtt_region& reg : ch.regions) {
                 ++total_regions;
                 if (reg.rows == 0 || reg.row_bytes == 0) continue;
@@ -719,7 +808,7 @@ int validate_plan(dtt_plan* p, const dtt_schedule* const* scheds) {
                 const uint64_t hi = lo + span;
                 if (p->opts.allgather && (lo < r * S || hi > (uint64_t)(r + 1) * S))
                     return fail(DTT_EOUTOFROWS, "plan: rank %u sends bytes outside its own rows", r);
-                refs.push_back(RegionRef{lo, hi, r, &reg});
+                if (ch.dests.empty()) refs.push_back(RegionRef{lo, hi, r, &reg});   // lands at its own offsets
             }
         }
     }
@@ -732,7 +821,7 @@ int validate_plan(dtt_plan* p, const dtt_schedule* const* scheds) {
             if (refs[k].rank != refs[i].rank && regions_intersect(*refs[i].reg, *refs[k].reg))
                 return fail(DTT_EOVERLAP, "plan: ranks %u and %u send the same bytes", refs[i].rank,
                             refs[k].rank);
-
+    if (p->other_dests || p->separate_dst) return validate_destinations(p, scheds);
     return DTT_OK;
 }
 
@@ -740,7 +829,9 @@ int build_plan(dtt_plan* p, const dtt_schedule* const* scheds) {
     const uint32_t P = p->P;
     // ---- global chunk numbering and copier work ------------------------------------------
     bool bases_aligned = true;
-    for (uint32_t r = 0; r < P; ++r) bases_aligned &= (reinterpret_cast<uintptr_t>(p->bufs[r]) % 16 == 0);
+    for (uint32_t r = 0; r < P; ++r)
+        bases_aligned &= (reinterpret_cast<uintptr_t>(p->bufs[r]) % 16 == 0) &&
+                         (reinterpret_cast<uintptr_t>(p->dst[r]) % 16 == 0);
     uint64_t src_bytes[DTT_MAX_RANKS] = {};
     uint32_t n = 0;
     for (uint32_t r = 0; r < P; ++r) {
@@ -792,10 +883,15 @@ int build_plan(dtt_plan* p, const dtt_schedule* const* scheds) {
         for (const HostChunk& ch : s->chunks) {
             ChunkDesc cd{};
             cd.piece_begin = (uint32_t)p->pieces.size();
-            for (const dtt_region& reg : ch.regions) {
-                cut_region(reg, cx, &p->pieces);
+            for (size_t i = 0; i < ch.regions.size(); ++i) {
+                const dtt_region& reg = ch.regions[i];
+                const dtt_dest d = ch.dests.empty() ? dtt_dest{reg.offset, reg.pitch} : ch.dests[i];
+                cut_region(reg, d, cx, &p->pieces);
                 cd.bytes += reg.rows * reg.row_bytes;
             }
+            for (uint32_t q = 0; q < P; ++q)
+                if (receives(ch.peers, r, q)) cd.peers |= 1u << q;
+            cd.receivers = (uint32_t)__builtin_popcount(cd.peers);
             if (p->pieces.size() == cd.piece_begin) {   // an empty chunk still signals arrival
                 PieceDesc empty{};
                 empty.tmap = kNoMap;
@@ -809,6 +905,7 @@ int build_plan(dtt_plan* p, const dtt_schedule* const* scheds) {
             dealt += cd.n_pieces;
             p->chunks.push_back(cd);
             p->writers.push_back(ch.writers);
+            p->peer_masks.push_back(cd.peers);
         }
     }
     if (p->pieces.size() > 0xFFFFFFFFull) return fail(DTT_ECAPACITY, "plan: too many copier pieces");
@@ -829,10 +926,10 @@ int upload(dtt_plan* p) {
         uint64_t* own = &gates[((uint64_t)cd.owner * n + c) * DTT_GATE_WORDS];
         own[DTT_GATE_READY] = prior;
         own[DTT_GATE_COUNTER] = prior * cd.writers;
-        own[DTT_GATE_COMPLETION] = prior * (P - 1);
+        own[DTT_GATE_COMPLETION] = prior * cd.receivers;
         own[DTT_GATE_COPIER] = prior * cd.n_part;
         for (uint32_t q = 0; q < P; ++q)
-            if (q != cd.owner) gates[((uint64_t)q * n + c) * DTT_GATE_WORDS + DTT_GATE_ARRIVAL] = prior;
+            if ((cd.peers >> q) & 1u) gates[((uint64_t)q * n + c) * DTT_GATE_WORDS + DTT_GATE_ARRIVAL] = prior;
     }
     const size_t n_gate_bytes = std::max<size_t>(1, gates.size() * sizeof(uint64_t));
     DTT_CUDA_TRY(cudaMalloc(&p->d_gates, n_gate_bytes));
@@ -856,6 +953,10 @@ int upload(dtt_plan* p) {
     }
     if (!gates.empty())
         DTT_CUDA_TRY(cudaMemcpy(p->d_gates, gates.data(), gates.size() * sizeof(uint64_t), cudaMemcpyHostToDevice));
+    if (n && p->other_dests) {
+        DTT_CUDA_TRY(cudaMalloc(&p->d_peer_masks, n * sizeof(uint32_t)));
+        DTT_CUDA_TRY(cudaMemcpy(p->d_peer_masks, p->peer_masks.data(), n * sizeof(uint32_t), cudaMemcpyHostToDevice));
+    }
     if (n) {
         DTT_CUDA_TRY(cudaMemcpy(p->d_writers, p->writers.data(), n * sizeof(uint32_t), cudaMemcpyHostToDevice));
         DTT_CUDA_TRY(cudaMemcpy(p->d_chunks, p->chunks.data(), n * sizeof(ChunkDesc), cudaMemcpyHostToDevice));
@@ -981,7 +1082,24 @@ int dtt_plan_create(void* const* bufs, uint64_t buf_bytes, uint32_t P,
             return fail(DTT_EINVAL, "dtt_plan_create: buffer %u is NULL", r);
         }
         p->bufs[r] = static_cast<char*>(bufs[r]);
+        p->dst[r] = p->bufs[r];
     }
+    if (o.dst_bufs) {                 // separate destination (staging) buffers
+        if (o.dst_bytes == 0) {
+            delete p;
+            return fail(DTT_EINVAL, "dtt_plan_create: dst_bufs needs dst_bytes > 0");
+        }
+        for (uint32_t r = 0; r < P; ++r) {
+            if (!o.dst_bufs[r]) {
+                delete p;
+                return fail(DTT_EINVAL, "dtt_plan_create: destination buffer %u is NULL", r);
+            }
+            p->dst[r] = static_cast<char*>(o.dst_bufs[r]);
+        }
+        p->separate_dst = true;
+        p->dst_bytes = o.dst_bytes;
+    }
+    o.dst_bufs = nullptr;             // the plan keeps its own copy of the pointers
     int rc = validate_plan(p, scheds);    // host-only checks come first
     if (rc != DTT_OK) {
         delete p;
@@ -1337,8 +1455,9 @@ int dtt_plan_define_groups(dtt_plan* p, uint32_t n_groups, const uint32_t* offse
     if (p->state != DTT_PLAN_PREPARED || p->round != p->opts.initial_round || p->wait_seq || p->early_launched)
         return fail(DTT_ESTATE, "dtt_plan_define_groups: groups are defined before the plan's first start");
     if (offsets[0] != 0) return fail(DTT_EINVAL, "dtt_plan_define_groups: offsets[0] must be 0");
-    // per group: its members, distinct and in range; per chunk: the groups it belongs to (CSR)
-    std::vector<uint32_t> size(n_groups), chunk_off(p->n_global + 1, 0);
+    // per group: its members, distinct and in range; per chunk: the groups it belongs to (CSR);
+    // per (rank, group): the members that reach the rank (its own, or addressed to it)
+    std::vector<uint32_t> size((size_t)p->P * n_groups, 0), chunk_off(p->n_global + 1, 0);
     std::vector<uint32_t> seen(p->n_global, UINT32_MAX);
     for (uint32_t g = 0; g < n_groups; ++g) {
         if (offsets[g + 1] <= offsets[g])
@@ -1349,8 +1468,10 @@ int dtt_plan_define_groups(dtt_plan* p, uint32_t n_groups, const uint32_t* offse
             if (seen[c] == g) return fail(DTT_EINVAL, "dtt_plan_define_groups: chunk %u twice in group %u", c, g);
             seen[c] = g;
             ++chunk_off[c + 1];
+            const ChunkDesc& cd = p->chunks[c];
+            for (uint32_t q = 0; q < p->P; ++q)
+                if (q == cd.owner || ((cd.peers >> q) & 1u)) ++size[(size_t)q * n_groups + g];
         }
-        size[g] = offsets[g + 1] - offsets[g];
     }
     for (uint32_t c = 0; c < p->n_global; ++c) chunk_off[c + 1] += chunk_off[c];
     std::vector<uint32_t> ids(chunk_off[p->n_global]), fill(chunk_off.begin(), chunk_off.end() - 1);
@@ -1360,7 +1481,8 @@ int dtt_plan_define_groups(dtt_plan* p, uint32_t n_groups, const uint32_t* offse
     const uint64_t prior = p->round - 1;
     std::vector<uint64_t> counters((uint64_t)p->P * n_groups);
     for (uint32_t q = 0; q < p->P; ++q)
-        for (uint32_t g = 0; g < n_groups; ++g) counters[(uint64_t)q * n_groups + g] = prior * size[g];
+        for (uint32_t g = 0; g < n_groups; ++g)
+            counters[(uint64_t)q * n_groups + g] = prior * size[(size_t)q * n_groups + g];
     std::vector<uint32_t> arrays;
     arrays.reserve(size.size() + chunk_off.size() + ids.size() + 1);
     arrays.insert(arrays.end(), size.begin(), size.end());
@@ -1383,6 +1505,8 @@ int dtt_plan_define_groups(dtt_plan* p, uint32_t n_groups, const uint32_t* offse
 
 int dtt_plan_define_block_groups(dtt_plan* p, uint64_t block_bytes, uint32_t* n_groups, uint32_t* block_group) {
     if (!p || block_bytes == 0) return fail(DTT_EINVAL, "dtt_plan_define_block_groups: bad args");
+    if (p->other_dests || p->separate_dst)
+        return fail(DTT_EINVAL, "dtt_plan_define_block_groups: needs chunks that land at their own offsets");
     const uint64_t nb = (p->buf_bytes + block_bytes - 1) / block_bytes;
     if (nb > 0xFFFFFFF0ull) return fail(DTT_EINVAL, "dtt_plan_define_block_groups: too many blocks");
     // the blocks each chunk touches, from the copier's pieces (every row of every piece)
@@ -1502,6 +1626,8 @@ int dtt_allgather_host(dtt_plan* p, const void* const* host_slices, void* host_o
     if (!p || !host_slices) return fail(DTT_EINVAL, "dtt_allgather_host: bad args");
     if (!p->opts.allgather) return fail(DTT_EINVAL, "dtt_allgather_host: needs an all-gather plan");
     if (p->ce) return fail(DTT_EINVAL, "dtt_allgather_host: needs an SM copier (not DTT_COPY_ENGINE)");
+    if (p->other_dests || p->separate_dst)
+        return fail(DTT_EINVAL, "dtt_allgather_host: needs chunks that land at their own offsets");
     if (out_rank >= p->P) return fail(DTT_EINVAL, "dtt_allgather_host: out_rank out of range");
     const uint32_t P = p->P;
     const uint64_t S = p->buf_bytes / P;
@@ -1668,6 +1794,8 @@ int dtt_gemm_consumer(dtt_plan* p, uint32_t rank, const void* Wt, uint32_t N, ui
     if (!p || !Wt || !D || !err || rank >= p->P) return fail(DTT_EINVAL, "dtt_gemm_consumer: bad args");
     if (p->state != DTT_PLAN_RUNNING) return fail(DTT_ESTATE, "dtt_gemm_consumer: plan is not RUNNING");
     if (stream == p->copy_stream) return fail(DTT_EINVAL, "dtt_gemm_consumer: use a stream other than the copy stream");
+    if (p->other_dests || p->separate_dst)
+        return fail(DTT_EINVAL, "dtt_gemm_consumer: needs chunks that land at their own offsets");
     const uint64_t row_bytes = 2ull * K;
     if (N == 0 || K == 0 || N % 128 || K % 64 || p->buf_bytes % (row_bytes * 128))
         return fail(DTT_EINVAL, "dtt_gemm_consumer: N must be a multiple of 128, K of 64, and the buffer "

@@ -93,6 +93,55 @@ int dtt_schedule_add_chunk(dtt_schedule* s, const dtt_region* regions, uint32_t 
     return DTT_OK;
 }
 
+int dtt_schedule_add_chunk_to(dtt_schedule* s, const dtt_region* regions, const dtt_dest* dests,
+                              uint32_t n, uint32_t writers, uint32_t peer_mask) {
+    if (!dests) {
+        const int rc = dtt_schedule_add_chunk(s, regions, n, writers);
+        if (rc == DTT_OK) s->chunks.back().peers = peer_mask;
+        return rc;
+    }
+    if (!s || !regions || n == 0) return fail(DTT_EINVAL, "dtt_schedule_add_chunk_to: no regions");
+    if (writers == 0) return fail(DTT_EINVAL, "dtt_schedule_add_chunk_to: a chunk needs writers >= 1");
+    HostChunk ch;
+    ch.writers = writers;
+    ch.peers = peer_mask;
+    for (uint32_t i = 0; i < n; ++i) {
+        const dtt_region& r = regions[i];
+        const dtt_dest& d = dests[i];
+        if (r.rows > 1 && (r.pitch < r.row_bytes || d.pitch < r.row_bytes))
+            return fail(DTT_EINVAL, "dtt_schedule_add_chunk_to: region %u has a (destination) pitch below its row bytes", i);
+        if (r.rows == 0 || r.row_bytes == 0) continue;
+        const bool src_contig = r.rows == 1 || r.pitch == r.row_bytes;
+        const bool dst_contig = r.rows == 1 || d.pitch == r.row_bytes;
+        if (src_contig && dst_contig) {     // one byte range on both sides, cut at 1 GiB together
+            const uint64_t bytes = r.rows * r.row_bytes;
+            for (uint64_t pos = 0; pos < bytes; pos += DTT_LINEAR_MAX) {
+                const uint64_t len = (bytes - pos) < DTT_LINEAR_MAX ? (bytes - pos) : DTT_LINEAR_MAX;
+                ch.regions.push_back(dtt_region{r.offset + pos, len, 1, len});
+                ch.dests.push_back(dtt_dest{d.offset + pos, len});
+            }
+        } else {
+            ch.regions.push_back(r);
+            ch.dests.push_back(dtt_dest{d.offset, r.rows > 1 ? d.pitch : r.row_bytes});
+        }
+    }
+    s->chunks.push_back(std::move(ch));
+    return DTT_OK;
+}
+
+int dtt_schedule_get_dests(const dtt_schedule* s, uint32_t chunk, dtt_dest* dests_out, uint64_t cap,
+                           uint64_t* n_dests, uint32_t* peer_mask) {
+    if (!s || chunk >= s->chunks.size()) return fail(DTT_EINVAL, "dtt_schedule_get_dests: no such chunk");
+    const HostChunk& c = s->chunks[chunk];
+    if (n_dests) *n_dests = c.dests.size();
+    if (peer_mask) *peer_mask = c.peers;
+    if (dests_out) {
+        const uint64_t n = c.dests.size() < cap ? c.dests.size() : cap;
+        if (n) std::memcpy(dests_out, c.dests.data(), n * sizeof(dtt_dest));
+    }
+    return DTT_OK;
+}
+
 int dtt_schedule_whole(uint64_t base_off, uint64_t rows, uint64_t row_bytes, uint64_t pitch,
                        uint32_t num_programs, dtt_schedule** out) {
     if (!out || num_programs == 0) return fail(DTT_EINVAL, "dtt_schedule_whole: num_programs must be >= 1");

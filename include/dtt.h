@@ -161,6 +161,32 @@ int dtt_schedule_empty(dtt_schedule** out);
 int dtt_schedule_add_chunk(dtt_schedule* s, const dtt_region* regions, uint32_t n,
                            uint32_t writers);
 
+/* Where a region lands: the same rows of the same width, at byte `offset` of the receiving
+ * rank's buffer (or of its destination buffer, dtt_plan_opts.dst_bufs), rows `pitch` apart. */
+typedef struct dtt_dest {
+    uint64_t offset;
+    uint64_t pitch;
+} dtt_dest;
+
+/* Other destinations ("Triggered Plans", Not supported yet: a copy could not change offset, pitch
+ * or buffer, and a chunk could not go to only some peers; reduce-scatter and two-shot all-reduce
+ * need both).  As dtt_schedule_add_chunk, and in addition:
+ *  - dests (NULL: every region lands at its own offsets): one destination per region;
+ *  - peer_mask: bit q set = rank q receives the chunk (DTT_ALL_PEERS = every other rank); the
+ *    owner's bit is ignored.  Only the receivers get arrivals; completion counts them.
+ * A byte range is split at 1 GiB together with its destination when both are contiguous.
+ * The plan checks destinations at create (see dtt_plan_create).
+ * Errors: DTT_EINVAL (as dtt_schedule_add_chunk; a destination pitch below the row bytes). */
+#define DTT_ALL_PEERS 0u
+int dtt_schedule_add_chunk_to(dtt_schedule* s, const dtt_region* regions, const dtt_dest* dests,
+                              uint32_t n, uint32_t writers, uint32_t peer_mask);
+
+/* A chunk's destinations (dests_out: at most cap of them; *n_dests = the chunk's region count,
+ * or 0 when its regions land at their own offsets) and its peer mask (DTT_ALL_PEERS or the bits
+ * given).  Errors: DTT_EINVAL. */
+int dtt_schedule_get_dests(const dtt_schedule* s, uint32_t chunk, dtt_dest* dests_out,
+                           uint64_t cap, uint64_t* n_dests, uint32_t* peer_mask);
+
 /* Number of chunks and regions. */
 int dtt_schedule_info(const dtt_schedule* s, uint32_t* n_chunks, uint64_t* n_regions);
 
@@ -203,6 +229,12 @@ typedef struct dtt_plan_opts {
                                 stream (read with dtt_plan_stats) */
     uint32_t host_piece_bytes;/* dtt_allgather_host: bytes per host-to-device copy (a multiple
                                 of 4096); 0 = a quarter of a slice, at least 4 MiB */
+    void* const* dst_bufs;    /* NULL: copies land in the P buffers themselves.  Else a host array
+                                 of P device pointers, dst_bytes each: separate destination buffers
+                                 (staging buffers) that every copy lands in, at its chunk's
+                                 destinations (dtt_schedule_add_chunk_to).  Not with
+                                 dtt_allgather_host, dtt_gemm_consumer or block groups. */
+    uint64_t dst_bytes;
     uint32_t early_copier_us; /* > 0: dtt_plan_wait launches the NEXT round's copier right after
                                 this round's check, queued behind this round's copier, so that
                                 the next dtt_plan_start launches nothing (the pages' "prepare":
@@ -231,16 +263,18 @@ void dtt_plan_opts_default(dtt_plan_opts* opts);
 #define DTT_DEV_EBADGROUP 2u       /* device status bit: a wait named a group the plan lacks */
 
 /* A plan's chunk groups (dtt_plan_define_groups): device arrays owned by the plan, their
- * addresses carried by value in every handle.  A group is a
- * set of global chunk ids, of any source ranks.  Each virtual rank q has one counter per group,
- * counters[q * n_groups + g], that goes up by one whenever a member becomes readable at q: the
- * copier adds one when it signals a member's arrival at q, and the mark that opens a member's
- * gate adds one at its own rank.  So after R rounds every counter holds R * size[g], and a wait
- * on group g passes at round * size[g] ("Triggered Plans", Not supported yet: "Waiting on a
- * group" -- no single counter covers several chunks or several source ranks). */
+ * addresses carried by value in every handle.  A group is a set of global chunk ids, of any
+ * source ranks.  Each virtual rank q has one counter per group, counters[q * n_groups + g],
+ * that goes up by one whenever a member becomes readable at q: the copier adds one when it
+ * signals a member's arrival at q, and the mark that opens a member's gate adds one at its own
+ * rank.  When chunks go to only some peers, q counts only the members that reach it (its own,
+ * or addressed to it): size[q * n_groups + g] of them per round.  So after R rounds every
+ * counter holds R * size, and a wait on group g passes at round * size ("Triggered Plans", Not
+ * supported yet: "Waiting on a group" -- no single counter covers several chunks or several
+ * source ranks). */
 typedef struct dtt_group_table {
     uint64_t* counters;          /* [P][n_groups], monotonic, never reset */
-    const uint32_t* size;        /* [n_groups] members per group */
+    const uint32_t* size;        /* [P][n_groups]: members of group g that reach rank q */
     const uint32_t* chunk_off;   /* [n_global + 1]: chunk c's groups are */
     const uint32_t* chunk_ids;   /*   chunk_ids[chunk_off[c] .. chunk_off[c + 1]) */
     uint32_t n_groups;
@@ -263,6 +297,8 @@ typedef struct dtt_handle {
     uint32_t flags;           /* bit 0: timestamps */
     uint32_t reserved;
     dtt_group_table groups;   /* the plan's groups (device arrays); counters == NULL: none */
+    const uint32_t* peer_masks; /* device: receivers of each global chunk as a bit mask, or NULL
+                                 when every chunk goes to every other rank */
     uint32_t* host_ready;     /* DTT_COPY_ENGINE plans: device address of mapped host words, word c
                                  = the round chunk c's gate last opened in (the mark that opens a
                                  gate stores it after a system-scope fence); NULL otherwise */
@@ -301,8 +337,11 @@ typedef struct dtt_report {
  * host array of P schedules; a NULL entry or empty schedule sends nothing).  Chunk ids are
  * global: rank r's chunks follow those of ranks 0..r-1 ("Triggered Plans", section Model).
  * Validates every region (inside the buffer; inside the rank's rows when opts->allgather;
- * no byte sent by two ranks), allocates the gate tables and the copier's descriptor tables
- * on the device, and leaves the plan PREPARED for round opts->initial_round (1 by default).
+ * no byte sent by two ranks to the same offsets) and every destination (inside the receiving
+ * buffer; no two copies landing on the same bytes of one buffer; in place, no copy landing on
+ * bytes its receiving rank sends: DTT_EOVERLAP), allocates the gate tables and the copier's
+ * descriptor tables on the device, and leaves the plan PREPARED for round opts->initial_round
+ * (1 by default).
  * copy_stream: a non-blocking stream for the copier, or NULL to let the plan create (and
  * own) a high-priority one.  Creation succeeds for every rank or for none: on error nothing
  * stays allocated ("Triggered Plans", The kernel author's contract).
@@ -550,11 +589,12 @@ int dtt_gemm_consumer(dtt_plan* plan, uint32_t rank, const void* Wt, uint32_t N,
                       uint64_t ldd, uint32_t num_programs, uint64_t max_polls, uint32_t* err,
                       cudaStream_t stream);
 
-/* Consumer: rank `rank` waits for every chunk of the other ranks (in global id order, with
- * the device-side wait, at most max_polls polls each) and copies its regions from the rank's
- * own buffer bufs[rank] to the same offsets of `dst` (device, buf_bytes long) -- data read
- * after the wait is this round's ("Triggered Plans", Memory ordering, Consumer).  Per-chunk
- * results go to status (device int32 [n_global]: 0, or DTT_ETIMEDOUT).  Launch with at most
+/* Consumer: rank `rank` waits for every chunk of the other ranks that it receives (in global id
+ * order, with the device-side wait, at most max_polls polls each) and copies each chunk's landed
+ * bytes from where they landed (the rank's own buffer, or its destination buffer) to the same
+ * offsets of `dst` (device, buf_bytes or dst_bytes long) -- data read after the wait is this
+ * round's ("Triggered Plans", Memory ordering, Consumer).  Per-chunk results go to status
+ * (device int32 [n_global]: 0, or DTT_ETIMEDOUT; 0 for chunks it does not receive).  Launch with at most
  * `ctas` CTAs on `stream` (a third stream, concurrent with producer and copier).
  * Errors: DTT_EINVAL, DTT_ESTATE (plan not RUNNING), DTT_ECUDA. */
 int dtt_consumer_gather(dtt_plan* plan, uint32_t rank, void* dst, uint64_t max_polls,

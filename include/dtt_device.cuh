@@ -131,8 +131,15 @@ __device__ __forceinline__ const uint64_t* group_word(const dtt_handle& h, uint3
         atomicOr(h.status, DTT_DEV_EBADGROUP);
         return nullptr;
     }
-    *target = (uint64_t)h.round * h.groups.size[g];
-    return h.groups.counters + (uint64_t)h.rank * h.groups.n_groups + g;
+    const uint64_t at = (uint64_t)h.rank * h.groups.n_groups + g;
+    *target = (uint64_t)h.round * h.groups.size[at];
+    return h.groups.counters + at;
+}
+
+/* Ranks a chunk of this rank is copied to: every other rank, or those of its peer mask. */
+__device__ __forceinline__ uint32_t receivers(const dtt_handle& h, uint32_t chunk) {
+    if (!h.peer_masks) return h.P - 1;
+    return (uint32_t)__popc(h.peer_masks[chunk] & ~(1u << h.rank));
 }
 
 /* The word a rank polls for `chunk`: its own chunks are local once ready; other ranks' chunks
@@ -236,7 +243,8 @@ __device__ __forceinline__ int dtt_wait_group(const dtt_handle& h, uint32_t g, u
 /* Source side ("Triggered SDMA Plans", API: the device view's `reusable`; Design notes: the
  * completion word of the gate row): has every copy of this rank's own `chunk` landed at every
  * peer this round, so that the chunk's bytes may be written again?  True when the chunk's
- * completion word has reached round * (P - 1), the copier's deliveries of it over all rounds.
+ * completion word has reached round * (its receivers: P - 1 unless it goes to only some peers),
+ * the copier's deliveries of it over all rounds.
  * The acquire orders the copier's reads of the chunk before the caller's later writes.  A
  * chunk of another rank sets DTT_DEV_EBADCHUNK in the plan's status word and returns false. */
 __device__ __forceinline__ bool dtt_reusable(const dtt_handle& h, uint32_t chunk) {
@@ -248,7 +256,7 @@ __device__ __forceinline__ bool dtt_reusable(const dtt_handle& h, uint32_t chunk
             atomicOr(h.status, DTT_DEV_EBADCHUNK);
         } else {
             const uint64_t* w = dtt_dev::gate_row(h, h.rank, chunk) + DTT_GATE_COMPLETION;
-            f = dtt_dev::ld_acquire(w) >= (uint64_t)h.round * (h.P - 1);
+            f = dtt_dev::ld_acquire(w) >= (uint64_t)h.round * dtt_dev::receivers(h, chunk);
         }
         dtt_reusable_flag = f;
     }
@@ -267,7 +275,7 @@ __device__ __forceinline__ int dtt_wait_reusable(const dtt_handle& h, uint32_t c
             atomicOr(h.status, DTT_DEV_EBADCHUNK);
         } else {
             const uint64_t* w = dtt_dev::gate_row(h, h.rank, chunk) + DTT_GATE_COMPLETION;
-            const uint64_t target = (uint64_t)h.round * (h.P - 1);
+            const uint64_t target = (uint64_t)h.round * dtt_dev::receivers(h, chunk);
             uint32_t ns = 0;
             for (uint64_t i = 0; i < max_polls; ++i) {
                 if (dtt_dev::ld_acquire(w) >= target) { r = 0; break; }

@@ -205,7 +205,8 @@ def test_binding_structs_match_the_c_header(tmp_path):
     import subprocess
     if not shutil.which("gcc"):
         pytest.skip("gcc not found")
-    structs = {"dtt_region": D.dtt_region, "dtt_order": D.dtt_order, "dtt_plan_opts": D.dtt_plan_opts,
+    structs = {"dtt_region": D.dtt_region, "dtt_dest": D.dtt_dest, "dtt_order": D.dtt_order,
+               "dtt_plan_opts": D.dtt_plan_opts,
                "dtt_group_table": D.dtt_group_table, "dtt_handle": D.dtt_handle, "dtt_report": D.dtt_report, "dtt_fill_desc": D.dtt_fill_desc}
     lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "dtt.h"', 'int main(void) {']
     for name, cls in structs.items():
@@ -239,3 +240,88 @@ def test_prepared_barrier_arguments_are_checked_once_at_construction():
     b._h, b.P = C.c_void_p(0), 5
     with pytest.raises(D.DttError):            # prepared for 4 ranks, barrier of 5
         b.reveal(a)
+
+
+# ---- other destinations: schedule API and plan validation against the oracle's verdicts -----------
+def test_add_chunk_to_splits_contiguous_ranges_with_their_destinations():
+    s = D.dtt_schedule_empty()
+    G = 1 << 30
+    s.add_chunk([(0, 5 * G // 2, 1, 5 * G // 2)], 1, dests=[(1000, 5 * G // 2)], peers=0b100)
+    regs, w = s.chunk(0)
+    dests, mask = s.dests(0)
+    assert [r[1] for r in regs] == [G, G, G // 2] and [r[0] for r in regs] == [0, G, 2 * G]
+    assert dests == [(1000, G), (1000 + G, G), (1000 + 2 * G, G // 2)] and mask == 0b100
+    # contiguous rows landing with a wider pitch stay one 2D window
+    s.add_chunk([(0, 64, 4, 64)], 2, dests=[(512, 128)])
+    assert s.chunk(1) == ([(0, 64, 4, 64)], 2) and s.dests(1) == ([(512, 128)], 0)
+    s.add_chunk([(0, 64, 1, 64)], 1)
+    assert s.dests(2) == (None, 0)
+    with pytest.raises(D.DttError):                       # destination pitch below the row bytes
+        s.add_chunk([(0, 64, 4, 64)], 1, dests=[(0, 32)])
+    s.free()
+
+
+def _lib_verdict(P, nbytes, chunks_per_rank, dst_bytes=0):
+    """Create a plan over fake (never dereferenced) buffer addresses: validation runs first, so
+    an invalid plan fails before any CUDA call.  Returns the error code, or None when it passes
+    validation (then creation would need a GPU, which is not tried here)."""
+    scheds = []
+    for r in range(P):
+        s = D.dtt_schedule_empty()
+        for (regs, writers, dests, peers) in chunks_per_rank[r]:
+            s.add_chunk(regs, writers, dests=dests, peers=peers)
+        scheds.append(s)
+    opts = D.dtt_plan_opts_default(allgather=0)
+    arr = (C.c_void_p * P)(*[0x100000 * (r + 1) for r in range(P)])
+    if dst_bytes:
+        darr = (C.c_void_p * P)(*[0x900000 * (r + 1) for r in range(P)])
+        opts.dst_bufs = C.cast(darr, C.c_void_p).value
+        opts.dst_bytes = dst_bytes
+    sch = (C.c_void_p * P)(*[x.handle.value for x in scheds])
+    out = C.c_void_p()
+    rc = D.lib().dtt_plan_create(arr, nbytes, P, sch, C.byref(opts), None, C.byref(out))
+    for x in scheds:
+        x.free()
+    if rc == D.OK:          # a device was there: release the plan (no kernel ever ran on it)
+        D.lib().dtt_plan_close(out)
+    return rc
+
+
+def _oracle_verdict(P, nbytes, chunks_per_rank, dst_bytes=0):
+    scheds = [OS.Schedule([OS.Chunk(list(regs), w, dests=dests, peers=(peers or None))
+                           for (regs, w, dests, peers) in chunks_per_rank[r]]) for r in range(P)]
+    try:
+        OS.validate(scheds, nbytes, False, dst_bytes=dst_bytes or None)
+    except OS.PlanError as e:
+        return {"EOVERLAP": D.EOVERLAP, "EINVAL": D.EINVAL}[e.code]
+    return None
+
+
+DEST_CASES = {
+    "two_copies_same_bytes": (3, 64, [[([(0, 8, 1, 8)], 1, [(40, 8)], 0b100)],
+                                      [([(8, 8, 1, 8)], 1, [(44, 8)], 0b100)], []], 0),
+    "onto_receivers_sent_bytes": (2, 64, [[([(0, 8, 1, 8)], 1, [(16, 8)], 0)],
+                                          [([(16, 8, 1, 8)], 1, None, 0b01)]], 0),
+    "separate_buffers_allow_it": (2, 64, [[([(0, 8, 1, 8)], 1, [(16, 8)], 0)],
+                                          [([(16, 8, 1, 8)], 1, None, 0b01)]], 32),
+    "past_the_end": (2, 64, [[([(0, 8, 1, 8)], 1, [(60, 8)], 0)], []], 0),
+    "past_separate_end": (2, 64, [[([(0, 8, 1, 8)], 1, [(28, 8)], 0)], []], 32),
+    "mask_outside_plan": (2, 64, [[([(0, 8, 1, 8)], 1, None, 0b100)], []], 0),
+    "reduce_scatter_ok": (3, 96, [[([(b * 8, 8, 1, 8)], 1, [(48 + s * 8, 8)], 1 << b) for b in range(3) if b != s]
+                                  for s in range(3)], 0),
+    "pitched_rows_overlap_other": (2, 256, [[([(0, 8, 3, 16)], 1, [(100, 40)], 0)],
+                                            [([(200, 8, 1, 8)], 1, [(180, 8)], 0b01)]], 0),
+    "pitched_rows_interleave_ok": (3, 256, [[([(0, 8, 3, 16)], 1, [(100, 16)], 0b100)],
+                                            [([(64, 8, 3, 16)], 1, [(108, 16)], 0b100)], []], 0),
+}
+
+
+@pytest.mark.parametrize("name", sorted(DEST_CASES))
+def test_destination_validation_matches_the_oracle(name):
+    P, nbytes, chunks, dst = DEST_CASES[name]
+    want = _oracle_verdict(P, nbytes, chunks, dst)
+    got = _lib_verdict(P, nbytes, chunks, dst)
+    if want is None:
+        assert got not in (D.EOVERLAP, D.EINVAL), name      # passes validation (no GPU here)
+    else:
+        assert got == want, (name, got, want)
