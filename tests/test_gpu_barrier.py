@@ -88,11 +88,12 @@ def test_prepared_arguments_give_the_same_barriers():
     y = [torch.zeros(P, dtype=torch.int32, device="cuda") for _ in range(P)]
     status = torch.full((P,), 99, dtype=torch.int32, device="cuda")
     ha = D.HandrolledArgs(sig, y, status)
+    osig = np.zeros((P, P), dtype=np.int64)          # the oracle's windows, across generations
     for gen in (1, 2, 3):
         D.dtt_barrier_handrolled(ha, gen=gen, max_polls=1 << 24)
         torch.cuda.synchronize()
         assert status.cpu().tolist() == [0] * P
-        want = OB.handrolled(np.zeros((P, P), dtype=np.int64), gen)
+        want = OB.handrolled(osig, gen)
         for r in range(P):
             assert y[r].cpu().tolist() == want[r].tolist()
     x_np = W.barrier_payload(P, size, seed=3)
