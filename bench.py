@@ -35,14 +35,14 @@ DEFAULT_CONFIG = W.C2.name
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of the named kernel from one ncu capture
 # of the same workload and launch configuration (the summaries under profiles/); absent until
 # taken, and dropped once the kernel changes.
-NCU_TRAFFIC = {("c2_chunks_p4", "copier_bulk_kernel"): 474172032,
+NCU_TRAFFIC = {("c2_chunks_p4", "copier_bulk_kernel"): 474281216,
                # captured with 2000 rows per rank (--rows 2000) and scaled by the rows, 4x
                ("c3_tiles_p8", "copier_bulk_kernel"): 8009827328,
                ("c5_gemm_p4", "gemm2_producer_kernel"): 185820032,
                ("c5_gemm_p4", "copier_kernel"): 204823424}
 # DRAM bytes (read, write) of one whole round, producer, copier and check together, from an
 # ncu range-replay capture of three rounds of the benchmark's launch (--profile-rounds 3)
-ROUND_TRAFFIC = {"c2_chunks_p4": (2778795, 516082432), "c3_tiles_p8": (16352085, 8237216427)}
+ROUND_TRAFFIC = {"c2_chunks_p4": (2427136, 515952469), "c3_tiles_p8": (16352085, 8237216427)}
 
 
 def describe(w, launch, copier=None) -> str:

@@ -325,3 +325,12 @@ def test_destination_validation_matches_the_oracle(name):
         assert got not in (D.EOVERLAP, D.EINVAL), name      # passes validation (no GPU here)
     else:
         assert got == want, (name, got, want)
+
+
+def test_plan_rank_count_is_checked_before_any_device_call():
+    arr = (C.c_void_p * 17)(*[0x1000 * (r + 1) for r in range(17)])
+    out = C.c_void_p()
+    rc = D.lib().dtt_plan_create(arr, 1 << 20, 17, None, None, None, C.byref(out))
+    assert rc == D.EINVAL
+    rc = D.lib().dtt_plan_create(arr, 1 << 20, 0, None, None, None, C.byref(out))
+    assert rc == D.EINVAL
