@@ -30,6 +30,18 @@ pull 573, section Design notes):
   when its gate opens.  Every chunk becomes readable once per round at every rank, so after R
   rounds the counter holds R * |group|, and a wait on the group passes when the counter reaches
   round * |group|: exactly when every chunk of the group is readable there this round.
+* Overlapping rounds ("Triggered Plans", Not supported yet: "Overlapping rounds" -- wait() must
+  return before next_round() prepares the next round).  Reading, for a plan made with
+  ``overlap=True``: next_round() may also be called while the round is RUNNING; that round then
+  stays in flight (pending) and the next one is PREPARED, so at most two rounds are in flight.
+  Each (source, peer) queue serves the pending round's chunks before the new round's, each in
+  schedule order, so it still never passes a closed gate.  Round R+1's producer may write the
+  bytes of its chunk only once every copy of that chunk made in round R has landed (its
+  completion word holds R * receivers: ``writable``); whoever reads what round R delivered is
+  done before round R+1's producers start (the model has no readers).  wait() reports the
+  pending round first.  Its check is the sequential one, except that a count above
+  R * writers may come from round R+1's marks: an extra mark shows in the error word (the mark
+  that passes its round's count records it), and that word alone reports EXTRA.
 """
 from __future__ import annotations
 
@@ -77,7 +89,8 @@ class Plan:
 
     def __init__(self, bufs: Sequence[np.ndarray], schedules: Sequence[S.Schedule],
                  allgather: bool = True, initial_round: int = 1, validate: bool = True,
-                 copy_data: bool = True, dst_bufs: Optional[Sequence[np.ndarray]] = None):
+                 copy_data: bool = True, dst_bufs: Optional[Sequence[np.ndarray]] = None,
+                 overlap: bool = False):
         self.P = len(bufs)
         if len(schedules) != self.P:
             raise ValueError("one schedule per rank")
@@ -113,8 +126,11 @@ class Plan:
             self.gates[s, c, COMPLETION] = prior * len(ch.receivers(self.P, s))
             for p in ch.receivers(self.P, s):
                 self.gates[p, c, ARRIVAL] = prior
-        self.delivered = set()          # (chunk, peer) delivered in the current round
+        self.delivered = set()          # (round, chunk, peer) delivered in a round still in flight
         self.delivery_log: List[Tuple[int, int, int]] = []   # (source, peer, chunk) in order
+        self.delivery_rounds: List[int] = []                 # the round of each of them
+        self.overlap = overlap
+        self.pending: Optional[int] = None   # overlap: a round still in flight behind this one
         self.state = "PREPARED"
         self.groups: List[List[int]] = []
         self.groups_of: List[List[int]] = [[] for _ in range(self.G)]   # chunk -> its groups
@@ -184,18 +200,49 @@ class Plan:
     def chunks_of(self, r: int) -> range:
         return range(self.first[r], self.first[r] + self.schedules[r].n_chunks)
 
-    def mark_ready(self, rank: int, c: int) -> None:
-        """One writer's mark on chunk c (global id) of its own rank."""
+    def mark_ready(self, rank: int, c: int, rnd: Optional[int] = None) -> None:
+        """One writer's mark on chunk c (global id) of its own rank, made in round ``rnd`` (the
+        current round by default; with overlap, the pending round's producers may still be
+        marking)."""
         if self.owner[c] != rank:
             raise ValueError("a rank marks only its own chunks")
+        rnd = self.round if rnd is None else rnd
+        if rnd not in self.rounds_in_flight():
+            raise StateError(f"a mark of round {rnd}, which is not in flight")
         row = self.gates[rank, c]
         row[COUNTER] += 1
-        target = self.round * self.chunks[c].writers
+        target = rnd * self.chunks[c].writers
         if row[COUNTER] == target:
-            row[READY] = self.round
+            row[READY] = rnd
             self._count_group(rank, c)     # readable at its own rank from now on
         elif row[COUNTER] > target:
-            row[ERROR] = self.round
+            row[ERROR] = max(int(row[ERROR]), rnd)
+
+    def rounds_in_flight(self) -> List[int]:
+        """Rounds whose producers may mark and whose copies may move: the pending round (with
+        overlap) and the current one once started."""
+        live = [] if self.pending is None else [self.pending]
+        if self.state in ("RUNNING", "CLOSING"):
+            live.append(self.round)
+        return live
+
+    def writable(self, rank: int, c: int, rnd: Optional[int] = None) -> bool:
+        """May round ``rnd``'s producer write rank's own chunk c: has every copy of it made in
+        round rnd - 1 landed (completion >= (rnd - 1) * receivers)?  Always true without
+        overlap, where round rnd starts after round rnd - 1's wait."""
+        if self.owner[c] != rank:
+            raise ValueError("writable is asked of a rank's own chunk")
+        rnd = self.round if rnd is None else rnd
+        return int(self.gates[rank, c, COMPLETION]) >= (rnd - 1) * len(self.chunks[c].receivers(self.P, rank))
+
+    def write_chunk(self, rank: int, c: int, data: np.ndarray, rnd: Optional[int] = None) -> None:
+        """Round rnd's producer writes chunk c of its rank: every region of it takes its bytes
+        from ``data`` (a buffer-sized array of that round's contents).  Refused while the chunk
+        is not writable."""
+        if not self.writable(rank, c, rnd):
+            raise StateError(f"chunk {c} written before round {rnd}'s previous copies of it landed")
+        for reg in self.chunks[c].regions:
+            copy_region(data, self.bufs[rank], reg)
 
     def reusable(self, rank: int, c: int) -> bool:
         """Source side: has every copy of rank's own chunk c landed at every peer this round?
@@ -207,58 +254,95 @@ class Plan:
             raise ValueError("reusable is asked of a rank's own chunk")
         return int(self.gates[rank, c, COMPLETION]) >= self.round * len(self.chunks[c].receivers(self.P, rank))
 
-    def gate_open(self, c: int) -> bool:
+    def gate_open(self, c: int, rnd: Optional[int] = None) -> bool:
         s = self.owner[c]
-        return (int(self.gates[s, c, READY]) & 0xFFFFFFFF) >= self.round
+        return (int(self.gates[s, c, READY]) & 0xFFFFFFFF) >= (self.round if rnd is None else rnd)
+
+    def queue_next(self, s: int, p: int) -> Optional[Tuple[int, int]]:
+        """The head of queue (s, p): (round, chunk) of its next copy, or None when it has
+        nothing left in flight.  The pending round's chunks come before the current round's."""
+        for rnd in self.rounds_in_flight():
+            for c in self.chunks_of(s):
+                if p in self.chunks[c].receivers(self.P, s) and (rnd, c, p) not in self.delivered:
+                    return rnd, c
+        return None
+
+    def deliver_one(self, s: int, p: int) -> bool:
+        """One step of queue (s, p): copy its head chunk if that chunk's gate is open for its
+        round (else the queue waits: head of line).  Returns whether a copy was made."""
+        head = self.queue_next(s, p)
+        if head is None:
+            return False
+        rnd, c = head
+        if not self.gate_open(c, rnd):
+            return False
+        ch = self.chunks[c]
+        if self.copy_data:
+            for i, reg in enumerate(ch.regions):
+                copy_region(self.bufs[s], self.dst[p], reg, ch.dest_region(i))
+        self.signal_arrival(s, p, c)
+        self.delivered.add((rnd, c, p))
+        self.delivery_log.append((s, p, c))
+        self.delivery_rounds.append(rnd)
+        return True
 
     def copier_progress(self) -> int:
         """Run every (source, peer) queue as far as its gates allow; returns deliveries made.
-        Queue (s, p) holds s's chunks addressed to p, in schedule order."""
+        Queue (s, p) holds s's chunks addressed to p, in schedule order (with overlap: the
+        pending round's, then the current round's)."""
         n = 0
         for s in range(self.P):
             for p in range(self.P):
                 if p == s:
                     continue
-                for c in self.chunks_of(s):
-                    ch = self.chunks[c]
-                    if p not in ch.receivers(self.P, s) or (c, p) in self.delivered:
-                        continue
-                    if not self.gate_open(c):
-                        break                       # head of line: later chunks wait
-                    if self.copy_data:
-                        for i, reg in enumerate(ch.regions):
-                            copy_region(self.bufs[s], self.dst[p], reg, ch.dest_region(i))
-                    self.signal_arrival(s, p, c)
-                    self.delivered.add((c, p))
-                    self.delivery_log.append((s, p, c))
+                while self.deliver_one(s, p):
                     n += 1
         return n
 
-    def wait(self) -> Tuple[str, List[int], List[int]]:
-        """Completion check; returns (status, short chunk ids, extra chunk ids)."""
-        if self.state != "RUNNING":
-            raise StateError(f"wait in state {self.state}")
-        R = self.round
+    def check(self, R: int, counter_extra: bool = True) -> Tuple[str, List[int], List[int]]:
+        """Round R's completion check: (status, short chunk ids, extra chunk ids).  With
+        counter_extra False (a round checked while the next one's marks may already count),
+        only the error word reports an extra mark."""
         extra, short = [], []
         for c, ch in enumerate(self.chunks):
             s = self.owner[c]
             cnt = int(self.gates[s, c, COUNTER])
-            if cnt > R * ch.writers or int(self.gates[s, c, ERROR]) != 0:
+            if (counter_extra and cnt > R * ch.writers) or int(self.gates[s, c, ERROR]) != 0:
                 extra.append(c)
             elif cnt < R * ch.writers:
                 short.append(c)
             elif any(int(self.gates[p, c, ARRIVAL]) < R for p in ch.receivers(self.P, s)):
                 short.append(c)
-        if extra:
-            self.state = "FAILED"
-            return EXTRA, short, extra
-        if short:
-            self.state = "FAILED"
-            return TIMEOUT, short, extra
-        self.state = "DONE"
-        return OK, short, extra
+        return (EXTRA if extra else TIMEOUT if short else OK), short, extra
+
+    def wait(self) -> Tuple[str, List[int], List[int]]:
+        """Completion check of the oldest round in flight; returns (status, short chunk ids,
+        extra chunk ids).  A pending round (overlap) is checked first and leaves the state as it
+        is; otherwise the current round is checked and the plan becomes DONE."""
+        if self.pending is not None:
+            R = self.pending
+            res = self.check(R, counter_extra=False)
+            self.pending = None
+            self.delivered = {d for d in self.delivered if d[0] != R}
+            if res[0] != OK:
+                self.state = "FAILED"
+            return res
+        if self.state != "RUNNING":
+            raise StateError(f"wait in state {self.state}")
+        res = self.check(self.round)
+        self.state = "DONE" if res[0] == OK else "FAILED"
+        return res
 
     def next_round(self) -> int:
+        """Advance to the next round: from DONE, or (overlap) from RUNNING with no other round
+        in flight, which leaves the running round pending."""
+        if self.state == "RUNNING" and self.overlap and self.pending is None:
+            if self.round >= ROUND_LIMIT:
+                raise RoundLimitError("a plan is limited to 2**32 - 1 rounds")
+            self.pending = self.round
+            self.round += 1
+            self.state = "PREPARED"
+            return self.round
         if self.state != "DONE":
             raise StateError(f"next_round in state {self.state}")
         if self.round >= ROUND_LIMIT:
@@ -269,12 +353,16 @@ class Plan:
         return self.round
 
     def close(self) -> None:
-        """Close; mid-round, gates not yet open are opened and chunks sent as they stand."""
-        if self.state == "RUNNING":
+        """Close; mid-round, gates not yet open are opened and chunks sent as they stand (with
+        overlap, for the pending round and the running one)."""
+        live = self.rounds_in_flight()
+        if live:
+            top = live[-1]
             for c in range(self.G):
-                if not self.gate_open(c):
-                    self.gates[self.owner[c], c, READY] = self.round
+                if not self.gate_open(c, top):
+                    self.gates[self.owner[c], c, READY] = top
             self.copier_progress()
+        self.pending = None
         self.state = "CLOSED"
 
 
