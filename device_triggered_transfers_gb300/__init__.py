@@ -37,6 +37,8 @@ DTYPE_CODES = {"bf16": BF16, "f32": F32, "u8": U8}
 COPY_VEC16, COPY_TMA, COPY_ENGINE = 0, 1, 2
 ORDER_ROW_MAJOR, ORDER_GROUPED = 0, 1
 MARK_PER_STEP, MARK_AT_END = 0, 1
+HANDLE_TIMESTAMPS, HANDLE_OVERLAP = 1, 2
+DEV_EBADCHUNK, DEV_EBADGROUP, DEV_EWRITABLE = 1, 2, 4
 
 
 class dtt_region(C.Structure):
@@ -59,7 +61,8 @@ class dtt_plan_opts(C.Structure):
                 ("initial_round", C.c_uint32), ("max_polls", C.c_uint64),
                 ("max_regions", C.c_uint64), ("deferred_copier", C.c_uint32),
                 ("stages", C.c_uint32), ("time_copier", C.c_uint32), ("host_piece_bytes", C.c_uint32),
-                ("dst_bufs", C.c_void_p), ("dst_bytes", C.c_uint64), ("early_copier_us", C.c_uint32)]
+                ("dst_bufs", C.c_void_p), ("dst_bytes", C.c_uint64), ("early_copier_us", C.c_uint32),
+                ("overlap", C.c_uint32)]
 
 
 class dtt_group_table(C.Structure):
@@ -137,6 +140,7 @@ _SIGS = {
     "dtt_plan_define_block_groups": (C.c_int, [_P, _u64, C.POINTER(_u32), C.POINTER(_u32)]),
     "dtt_plan_read_group_counters": (C.c_int, [_P, C.POINTER(_u64), _u64]),
     "dtt_plan_round": (C.c_uint32, [_P]),
+    "dtt_plan_pending_round": (C.c_uint32, [_P]),
     "dtt_plan_info": (C.c_int, [_P, C.POINTER(_u32), C.POINTER(_u32), C.POINTER(_u32), C.POINTER(_P)]),
     "dtt_plan_read_gates": (C.c_int, [_P, C.POINTER(_u64), _u64]),
     "dtt_gemm_consumer": (C.c_int, [_P, C.c_uint32, _P, C.c_uint32, C.c_uint32, _P, _u64, C.c_uint32,
@@ -440,6 +444,11 @@ class Plan:
     @property
     def round(self) -> int:
         return lib().dtt_plan_round(self._h)
+
+    @property
+    def pending(self) -> int:
+        """The round in flight behind the current one (opts.overlap), or 0."""
+        return lib().dtt_plan_pending_round(self._h)
 
     def info(self):
         n = _u32()

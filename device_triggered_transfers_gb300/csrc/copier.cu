@@ -468,7 +468,9 @@ __global__ void __launch_bounds__(32) copier_bulk_kernel(const __grid_constant__
 }
 
 // wait()'s completion check, run after the copier and the producer: one flag per chunk, written
-// straight into the mapped host block.  The last CTA to finish copies the status words out,
+// straight into the mapped host block.  A pending round (overlapping rounds) is checked while the
+// next round's marks may already count: a count above round * writers is then no extra mark by
+// itself, and only the error word -- set by the mark that passes its own round's count -- is.  The last CTA to finish copies the status words out,
 // zeroes them for the next round, and only then stores the sequence number the host polls for.
 __global__ void check_kernel(const __grid_constant__ CheckParams p) {
     // launched after the producers on their stream; the copier counts its CTAs out
@@ -505,7 +507,8 @@ __global__ void check_kernel(const __grid_constant__ CheckParams p) {
             arrived &= dtt_dev::ld_relaxed(prow + DTT_GATE_ARRIVAL) >= p.round;
         }
         const uint64_t target = (uint64_t)p.round * cd.writers;
-        p.host_flags[c] = (cnt > target || err != 0) ? 2 : (cnt < target || !arrived) ? 1 : 0;
+        const bool extra = err != 0 || (!p.pending && cnt > target);
+        p.host_flags[c] = extra ? 2 : (cnt < target || !arrived) ? 1 : 0;
     }
     __shared__ uint32_t s_last;
     __syncthreads();                     // the CTA's flag stores, then one release for all of them

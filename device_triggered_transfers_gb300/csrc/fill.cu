@@ -212,7 +212,25 @@ __global__ void __launch_bounds__(1024) fill_kernel(const __grid_constant__ Fill
     char* base = p.bufs[r] + p.slice_off[r];
     uint64_t paced = ~0ull;       // the last chunk this program waited for
     bool pacing = p.pace != 0;    // off for the rest of the launch once a pacing wait runs out
+    const bool overlap = (h.flags & DTT_HANDLE_OVERLAP) != 0;
+    uint32_t writable = 0xFFFFFFFFu;   // overlapping rounds: the chunk this CTA last found writable
+    bool write = true;            // false once a writable wait ran out: this CTA writes no more
     for (uint64_t step = prog; step < T; step += p.NP) {
+        if (overlap && write) {
+            // the previous round's copies of the chunk must have landed before its bytes change
+            // (its copier may still be reading them); every CTA of a program asks for itself.
+            // A wait that runs out leaves the rest of this CTA's writes undone (the marks still
+            // go out, so no barrier of a cluster or counter of a group is left waiting) and
+            // fails the round.
+            const uint32_t chunk = h.first_chunk + (p.mark_mode == DTT_MARK_AT_END ? 0u : (uint32_t)(step / p.TPC));
+            if (chunk != writable) {
+                if (dtt_wait_writable(h, chunk, kWritablePolls) != 0) {
+                    write = false;
+                    if (dtt_dev::first_thread()) atomicOr(h.status, DTT_DEV_EWRITABLE);
+                }
+                writable = chunk;
+            }
+        }
         if (pacing) {
             // keep the bytes written but not yet delivered within `pace` chunks of this rank:
             // the copier then reads them from L2.  The result does not depend on the outcome.
@@ -231,7 +249,7 @@ __global__ void __launch_bounds__(1024) fill_kernel(const __grid_constant__ Fill
         const uint64_t rows = min((uint64_t)p.BM, p.M - r0), cols = min((uint64_t)p.BN, p.N - c0);
         const uint64_t per = (rows + team - 1) / team;
         const uint64_t ra = r0 + min(rows, member * per), rb = r0 + min(rows, (member + 1) * per);
-        write_block<DT>(p, base, salt, ra, rb, c0, cols);
+        if (write) write_block<DT>(p, base, salt, ra, rb, c0, cols);
         if (p.mark_mode == DTT_MARK_PER_STEP) {
             const uint32_t chunk = h.first_chunk + (uint32_t)(step / p.TPC);
             if (p.group > 1)

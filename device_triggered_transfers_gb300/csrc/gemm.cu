@@ -163,6 +163,20 @@ __device__ __forceinline__ uint32_t pack_bf16x2(uint32_t lo, uint32_t hi) {
     return r;
 }
 
+// Overlapping rounds (the handle's DTT_HANDLE_OVERLAP flag): one thread waits until the chunks
+// of rank h.rank's tiles [t0, t0 + n) (row-major tile indices) may be written -- the previous
+// round's copies of them have landed -- before the epilogue stores them.  False when a wait ran
+// out (DTT_DEV_EWRITABLE is set; the caller stops the GEMM).
+__device__ __forceinline__ bool unit_writable(const dtt_handle& h, uint32_t t0, uint32_t n, uint32_t NP) {
+    if (!(h.flags & DTT_HANDLE_OVERLAP)) return true;
+    for (uint32_t c = h.first_chunk + t0 / NP; c <= h.first_chunk + (t0 + n - 1) / NP; ++c)
+        if (!dtt_dev::wait_writable_one(h, c, kWritablePolls)) {
+            atomicOr(h.status, DTT_DEV_EWRITABLE);
+            return false;
+        }
+    return true;
+}
+
 // Work is cut in units of TN / 128 adjacent tiles of one tile row.  Every rank's units form one
 // sequence, the ranks taking turns (unit 0 of rank 0, of rank 1, ..., then unit 1 of each), and
 // program p takes its places p, p + NP, ..., so no program has more than one unit above the
@@ -276,12 +290,16 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_producer_kernel(const __grid_
         bool ok = true;
         for (uint32_t gu = blockIdx.x; gu < p.P * units && ok; gu += p.NP) {
                 const uint32_t r = gu % p.P, u = gu / p.P;
+                const uint32_t tm = u / units_n, tn0 = (u % units_n) * G::UNIT;
                 bool mine = bar_wait(saddr(acc_full + acc), acc_phase, abort_flag);
                 if (!mine) fail();
+                if (threadIdx.x == 0 && mine && !unit_writable(p.h[r], tm * tiles_n + tn0, G::UNIT, p.NP)) {
+                    fail();
+                    mine = false;
+                }
                 // one decision for all 128 epilogue threads, so none is left at a barrier
                 if (!epi_all(mine && !*abort_flag)) { ok = false; break; }
                 tc_fence_after();
-                const uint32_t tm = u / units_n, tn0 = (u % units_n) * G::UNIT;
                 char* crow = p.bufs[r] + p.slice_off[r] + (uint64_t)(tm * BM + row_in_tile) * p.ldc +
                              (uint64_t)tn0 * BN * 2;
                 const uint32_t taddr = tmem_base + ((warp * 32u) << 16) + acc * TN;
@@ -695,11 +713,15 @@ gemm2_producer_kernel(const __grid_constant__ GemmParams p) {
         bool ok = true;
         for (uint32_t gu = c0; gu < p.P * units && ok; gu += NC) {
                 const uint32_t r = gu % p.P, u = gu / p.P;
+                const uint32_t tm = (u / units_n) * 2 + q, tn0 = (u % units_n) * (G2_TN / BN);
                 bool mine = bar_wait(saddr(acc_full + acc), acc_phase, abort_flag);
                 if (!mine) fail();
+                if (threadIdx.x == 0 && mine && !unit_writable(p.h[r], tm * tiles_n + tn0, G2_TN / BN, p.NP)) {
+                    fail();
+                    mine = false;
+                }
                 if (!epi_all(mine && !*abort_flag)) { ok = false; break; }
                 tc_fence_after();
-                const uint32_t tm = (u / units_n) * 2 + q, tn0 = (u % units_n) * (G2_TN / BN);
                 char* crow = p.bufs[r] + p.slice_off[r] + (uint64_t)(tm * BM + row_in_tile) * p.ldc +
                              (uint64_t)tn0 * BN * 2;
                 const uint32_t taddr = tmem_base + ((warp * 32u) << 16) + acc * G2_TN;

@@ -43,6 +43,11 @@ int fail(int code, const char* fmt, ...);
 
 constexpr uint32_t kNoMap = 0xFFFFFFFFu;
 
+// Polls of a library producer's wait for a chunk to become writable (overlapping rounds): about a
+// second with the waits' back-off, after which the producer leaves its part of the chunk unwritten
+// and sets DTT_DEV_EWRITABLE.
+constexpr uint64_t kWritablePolls = 1ull << 22;
+
 // One unit of copier work: a sub-window of a region (rows x row_bytes, pitch apart) at byte
 // offset `off` of every buffer.  `vec` = 1 when off, row_bytes and pitch are multiples of 16.
 // Bulk-copy path: `tmap` names the tensor-map shape that moves the whole window as one box
@@ -146,6 +151,8 @@ struct CheckParams {
     uint32_t P;
     uint32_t n_global;
     uint32_t round;
+    uint32_t pending;           // 1: the next round may already be marking (overlapping rounds), so
+                                // only the error word reports extra marks
     uint32_t seq;               // stored in host->done once every flag and status word is there
     uint32_t copier_ctas;       // wait until this many copier CTAs have finished (0: no copier)
     uint64_t max_polls;         // bound of that wait

@@ -39,8 +39,10 @@ struct CeProxy {
     bool stop = false;
     bool busy = false;                  // issuing `round`
     uint32_t round = 0;
+    uint32_t queued = 0;                // overlapping rounds: the round to issue after `round` (0: none)
+    uint32_t issued = 0;                // the last round whose chunks were all issued (or given up)
     std::atomic<bool> open_all{false};  // close() in mid-round: every chunk goes as it stands
-    int rc = DTT_OK;                    // DTT_ETIMEDOUT: a gate stayed closed past the bound
+    int rc_of[2] = {DTT_OK, DTT_OK};    // per round parity; DTT_ETIMEDOUT: a gate stayed closed past the bound
     uint32_t stuck_chunk = 0;
     uint32_t* h_ready = nullptr;        // pinned, mapped: word c = round of chunk c's last opening
     uint32_t* h_ready_dev = nullptr;
@@ -83,7 +85,8 @@ struct dtt_plan {
     ChunkDesc* d_chunks = nullptr;
     PieceDesc* d_pieces = nullptr;
     CUtensorMap* d_tmaps = nullptr;   // [shape][rank]
-    DevStatus* d_status = nullptr;
+    DevStatus* d_status = nullptr;    // [2]: one block per round parity (status_of), so that a
+                                      // pending round's copier and check keep their own words
     HostStatus* h_status = nullptr;   // pinned, mapped: check_kernel writes the round's outcome here
     HostStatus* h_status_dev = nullptr;   // its device address
     uint8_t* h_flags = nullptr;       // the flag bytes right after it
@@ -124,6 +127,14 @@ struct dtt_plan {
     int state = DTT_PLAN_PREPARED;
     uint32_t round = 1;
     bool copier_launched = false;   // this round's copier is on the copy stream
+    bool live_round = false;        // this round was started and its check has not run yet
+
+    // opts.overlap: the round in flight behind the current one (0: none), whether its copier was
+    // launched, and an event after its producers (its check follows that event, not the
+    // producers of the round after it)
+    uint32_t pending = 0;
+    bool pending_copier = false;
+    cudaEvent_t ev_pending = nullptr;
     CeProxy* ce = nullptr;          // opts.method == DTT_COPY_ENGINE
 
     // opts.early_copier_us: wait() launches the next round's copier behind this round's, and
@@ -184,6 +195,8 @@ void free_device(dtt_plan* p) {
     cudaFree(p->d_status);
     cudaFreeHost(p->h_status);
     if (p->ev_producer) cudaEventDestroy(p->ev_producer);
+    if (p->ev_pending) cudaEventDestroy(p->ev_pending);
+    p->ev_pending = nullptr;
     if (p->ev_done) cudaEventDestroy(p->ev_done);
     p->ev_done = nullptr;
     if (p->ev_copier_end) cudaEventDestroy(p->ev_copier_end);
@@ -303,7 +316,11 @@ void cut_region(const dtt_region& r, const dtt_dest& d, const CutCtx& cx, std::v
     }
 }
 
-CopierParams copier_params(const dtt_plan* p);
+CopierParams copier_params(const dtt_plan* p, uint32_t round);
+
+// The device status block of round `round` (rounds of one parity share one; at most two rounds
+// are in flight, and a round's check clears its block before the round two later can start).
+DevStatus* status_of(const dtt_plan* p, uint32_t round) { return p->d_status + (round & 1u); }
 
 // Add the timed copier launches up to `upto` (in launch order) to the copier statistics.
 int read_copier_times(dtt_plan* p, uint64_t upto) {
@@ -334,7 +351,7 @@ uint64_t g_launch_seq = 0;
 
 bool may_spin(const dtt_plan* q) {
     return ((q->state == DTT_PLAN_RUNNING || q->state == DTT_PLAN_CLOSING) && q->copier_launched) ||
-           q->early_pending;
+           q->early_pending || (q->pending && q->pending_copier) || (q->live_round && q->copier_launched);
 }
 
 // Is p's copier queued behind an earlier plan's copier on the same stream that has not finished?
@@ -382,7 +399,7 @@ int launch_round_copier(dtt_plan* p) {
         pair = p->ev_copier[p->timed_launches % dtt_plan::kTimeRing];
         DTT_CUDA_TRY(cudaEventRecord(pair[0], p->copy_stream));
     }
-    DTT_CUDA_TRY(launch_copier(copier_params(p), p->copier_ctas, p->copier_threads, p->opts.method,
+    DTT_CUDA_TRY(launch_copier(copier_params(p, p->round), p->copier_ctas, p->copier_threads, p->opts.method,
                                p->copy_stream));
     if (pair) {
         DTT_CUDA_TRY(cudaEventRecord(pair[1], p->copy_stream));
@@ -413,21 +430,21 @@ dtt_handle make_handle(const dtt_plan* p, uint32_t r) {
     dtt_handle h{};
     h.gates = p->d_gates;
     h.writers = p->d_writers;
-    h.status = &p->d_status->misuse;
+    h.status = &status_of(p, p->round)->misuse;
     h.round = p->round;
     h.rank = r;
     h.P = p->P;
     h.n_global = p->n_global;
     h.first_chunk = p->first_chunk[r];
     h.n_chunks = p->n_chunks[r];
-    h.flags = p->opts.timestamps ? DTT_HANDLE_TIMESTAMPS : 0u;
+    h.flags = (p->opts.timestamps ? DTT_HANDLE_TIMESTAMPS : 0u) | (p->opts.overlap ? DTT_HANDLE_OVERLAP : 0u);
     h.groups = group_table(p);
     h.peer_masks = p->d_peer_masks;
     h.host_ready = p->ce ? p->ce->h_ready_dev : nullptr;
     return h;
 }
 
-CopierParams copier_params(const dtt_plan* p) {
+CopierParams copier_params(const dtt_plan* p, uint32_t round) {
     CopierParams cp{};
     for (uint32_t r = 0; r < p->P; ++r) {
         cp.bufs[r] = p->bufs[r];
@@ -439,10 +456,10 @@ CopierParams copier_params(const dtt_plan* p) {
     cp.gates = p->d_gates;
     cp.chunks = p->d_chunks;
     cp.pieces = p->d_pieces;
-    cp.status = p->d_status;
+    cp.status = status_of(p, round);
     cp.P = p->P;
     cp.n_global = p->n_global;
-    cp.round = p->round;
+    cp.round = round;
     cp.flags = p->opts.timestamps ? DTT_HANDLE_TIMESTAMPS : 0u;
     cp.max_polls = p->opts.max_polls;
     cp.stage_bytes = bulk_stage_bytes(p->opts.piece_bytes);
@@ -465,7 +482,7 @@ bool stream_shared(const dtt_plan* p) {
 
 bool early_allowed(const dtt_plan* p) {
     return p->opts.early_copier_us && p->host_atomics && p->n_global && !p->opts.time_copier &&
-           p->opts.method != DTT_COPY_ENGINE &&
+           p->opts.method != DTT_COPY_ENGINE && !p->opts.overlap &&
            p->opts.deferred_copier != 1 && !p->suppress_early && p->round < 0xFFFFFFFFu &&
            !stream_shared(p);
 }
@@ -479,8 +496,7 @@ bool cas_go(dtt_plan* p, uint64_t* expected, uint64_t desired) {
 
 // Launch round p->round + 1's copier now, on the copy stream behind this round's.
 int launch_early(dtt_plan* p) {
-    CopierParams cp = copier_params(p);
-    cp.round = p->round + 1;
+    CopierParams cp = copier_params(p, p->round + 1);
     cp.go_host = &p->h_status_dev->go;
     cp.go_prior = p->go_shadow;
     cp.go_wait_ns = (uint64_t)p->opts.early_copier_us * 1000;
@@ -633,8 +649,14 @@ void ce_main(dtt_plan* p) {
         const int rc = ce_run_round(p, round);
         {
             std::lock_guard<std::mutex> lock(ce.mu);
-            ce.rc = rc;
-            ce.busy = false;
+            ce.rc_of[round & 1u] = rc;
+            ce.issued = round;
+            if (ce.queued) {                // the next round was started behind this one
+                ce.round = ce.queued;
+                ce.queued = 0;
+            } else {
+                ce.busy = false;
+            }
         }
         ce.cv.notify_all();
     }
@@ -697,13 +719,16 @@ void stop_ce(dtt_plan* p) {
     p->ce = nullptr;
 }
 
-// Wait until the proxy has issued (or given up on) this round's chunks, then order the producer
-// stream after every queue.  Returns the proxy's status.
-int ce_join(dtt_plan* p, cudaStream_t after) {
+// Wait until the proxy has issued (or given up on) round `round`'s chunks (0: every round handed
+// to it), then order stream `after` after every queue (or, with no stream, wait for them).
+// Returns the proxy's status for that round.
+int ce_join(dtt_plan* p, cudaStream_t after, uint32_t round) {
     CeProxy& ce = *p->ce;
+    int rc;
     {
         std::unique_lock<std::mutex> lock(ce.mu);
-        ce.cv.wait(lock, [&] { return !ce.busy; });
+        ce.cv.wait(lock, [&] { return !ce.busy || (round && ce.issued >= round); });
+        rc = ce.rc_of[(round ? round : ce.issued) & 1u];
     }
     for (uint32_t s = 0; s < p->P; ++s)
         for (uint32_t q = 0; q < p->P; ++q) {
@@ -712,7 +737,7 @@ int ce_join(dtt_plan* p, cudaStream_t after) {
             if (after) DTT_CUDA_TRY(cudaStreamWaitEvent(after, ce.ev[s * p->P + q], 0));
             else DTT_CUDA_TRY(cudaEventSynchronize(ce.ev[s * p->P + q]));
         }
-    return ce.rc;
+    return rc;
 }
 
 // Does rank q receive a chunk of rank r with peer mask `peers`?
@@ -937,7 +962,7 @@ int upload(dtt_plan* p) {
     DTT_CUDA_TRY(cudaMalloc(&p->d_chunks, std::max<size_t>(1, n * sizeof(ChunkDesc))));
     DTT_CUDA_TRY(cudaMalloc(&p->d_pieces, std::max<size_t>(1, p->pieces.size() * sizeof(PieceDesc))));
     // the round's status on the device; its outcome and the per-chunk flags in mapped host memory
-    DTT_CUDA_TRY(cudaMalloc(&p->d_status, sizeof(DevStatus)));
+    DTT_CUDA_TRY(cudaMalloc(&p->d_status, 2 * sizeof(DevStatus)));
     const size_t host_bytes = sizeof(HostStatus) + std::max<size_t>(1, n);
     DTT_CUDA_TRY(cudaHostAlloc(&p->h_status, host_bytes, cudaHostAllocMapped | cudaHostAllocPortable));
     std::memset(p->h_status, 0, host_bytes);
@@ -984,7 +1009,7 @@ int upload(dtt_plan* p) {
         DTT_CUDA_TRY(cudaMalloc(&p->d_tmaps, maps.size() * sizeof(CUtensorMap)));
         DTT_CUDA_TRY(cudaMemcpy(p->d_tmaps, maps.data(), maps.size() * sizeof(CUtensorMap), cudaMemcpyHostToDevice));
     }
-    DTT_CUDA_TRY(cudaMemset(p->d_status, 0, sizeof(DevStatus)));
+    DTT_CUDA_TRY(cudaMemset(p->d_status, 0, 2 * sizeof(DevStatus)));
     return DTT_OK;
 }
 
@@ -1060,6 +1085,16 @@ int dtt_plan_create(void* const* bufs, uint64_t buf_bytes, uint32_t P,
         delete p;
         return fail(DTT_EINVAL, "dtt_plan_create: host_piece_bytes must be a multiple of 4096");
     }
+    if (o.deferred_copier > 2) {
+        delete p;
+        return fail(DTT_EINVAL, "dtt_plan_create: deferred_copier is 0, 1 or 2");
+    }
+    if (o.overlap > 1 || (o.overlap && o.deferred_copier == 1)) {
+        // a round's producers wait for the previous round's copies, so that copier must run
+        // beside them, not after them
+        delete p;
+        return fail(DTT_EINVAL, "dtt_plan_create: overlap is 0 or 1, and overlapping rounds need deferred_copier 0 or 2");
+    }
     if (o.early_copier_us > 1000000) {
         delete p;
         return fail(DTT_EINVAL, "dtt_plan_create: early_copier_us is at most 1000000 (one second)");
@@ -1122,10 +1157,6 @@ int dtt_plan_create(void* const* bufs, uint64_t buf_bytes, uint32_t P,
     p->host_atomics = host_atomics != 0;
     p->copier_ctas = o.copier_ctas ? o.copier_ctas : (uint32_t)sms * o.ctas_per_sm;
     p->copier_threads = o.copier_threads;
-    if (o.deferred_copier > 2) {
-        delete p;
-        return fail(DTT_EINVAL, "dtt_plan_create: deferred_copier is 0, 1 or 2");
-    }
     if (o.deferred_copier != 1 && o.method != DTT_COPY_ENGINE) {
         // The copier spins while the producer runs, so it must leave an SM room for producer
         // CTAs: at most half of its threads (2048) and half of its registers (64 Ki) per SM.
@@ -1184,7 +1215,8 @@ int dtt_plan_create(void* const* bufs, uint64_t buf_bytes, uint32_t P,
     if (rc == DTT_OK && (cudaEventCreateWithFlags(&p->ev_producer, cudaEventDisableTiming) != cudaSuccess ||
                          cudaEventCreateWithFlags(&p->ev_done, cudaEventDisableTiming) != cudaSuccess ||
                          cudaEventCreateWithFlags(&p->ev_copier_end, cudaEventDisableTiming) != cudaSuccess ||
-                         cudaEventCreateWithFlags(&p->ev_h2d, cudaEventDisableTiming) != cudaSuccess))
+                         cudaEventCreateWithFlags(&p->ev_h2d, cudaEventDisableTiming) != cudaSuccess ||
+                         cudaEventCreateWithFlags(&p->ev_pending, cudaEventDisableTiming) != cudaSuccess))
         rc = fail(DTT_ECUDA, "dtt_plan_create: cannot create an event");
     if (rc == DTT_OK && (cudaStreamCreateWithFlags(&p->d2h_stream, cudaStreamNonBlocking) != cudaSuccess ||
                          cudaStreamCreateWithFlags(&p->h2d_stream, cudaStreamNonBlocking) != cudaSuccess))
@@ -1214,10 +1246,16 @@ int dtt_plan_start(dtt_plan* p, cudaStream_t producer_stream, dtt_handle* handle
     if (p->ce) {                     // the proxy issues this round's copies as gates open
         {
             std::lock_guard<std::mutex> lock(p->ce->mu);
-            p->ce->round = p->round;
-            p->ce->rc = DTT_OK;
+            p->ce->rc_of[p->round & 1u] = DTT_OK;
             p->ce->open_all.store(false);
-            p->ce->busy = p->n_global != 0;
+            if (p->n_global) {
+                if (p->ce->busy) {
+                    p->ce->queued = p->round;    // behind the pending round (overlapping rounds)
+                } else {
+                    p->ce->round = p->round;
+                    p->ce->busy = true;
+                }
+            }
         }
         p->ce->cv.notify_all();
     } else if (claim_early(p)) {
@@ -1229,6 +1267,7 @@ int dtt_plan_start(dtt_plan* p, cudaStream_t producer_stream, dtt_handle* handle
     p->producer_stream = producer_stream;
     if (handles)
         for (uint32_t r = 0; r < p->P; ++r) handles[r] = make_handle(p, r);
+    p->live_round = true;
     p->state = DTT_PLAN_RUNNING;
     return DTT_OK;
 }
@@ -1250,54 +1289,53 @@ int dtt_plan_launch_copier(dtt_plan* p) {
     return launch_round_copier(p);
 }
 
-int dtt_plan_wait(dtt_plan* p, dtt_report* report) {
-    if (!p) return fail(DTT_EINVAL, "dtt_plan_wait: NULL plan");
-    if (p->state != DTT_PLAN_RUNNING) return fail(DTT_ESTATE, "dtt_plan_wait: plan is not RUNNING (state %d)", p->state);
-    const int lc = dtt_plan_launch_copier(p);    // deferred plans: the copier runs now
-    if (lc != DTT_OK) return lc;
-    // The check follows the producers on their stream and waits on the device for the copier's
-    // CTAs to count themselves out (no event between the streams, no launch gap after the copier).
-    int ce_rc = DTT_OK;
-    if (p->ce) ce_rc = ce_join(p, p->producer_stream);   // the check follows every queue
+namespace {
+
+// Launch round `round`'s completion check on `stream`; it waits on the device for `copier_ctas`
+// copier CTAs of that round to count themselves out.  pending: the round after it may already
+// be marking, so only the error word reports extra marks.
+int launch_round_check(dtt_plan* p, uint32_t round, uint32_t copier_ctas, bool pending, cudaStream_t stream,
+                       uint32_t* seq) {
     CheckParams ck{};
-    ck.copier_ctas = p->copier_launched ? p->copier_ctas : 0;
+    ck.copier_ctas = copier_ctas;
     ck.max_polls = 8 * p->opts.max_polls;
     ck.gates = p->d_gates;
     ck.chunks = p->d_chunks;
     ck.P = p->P;
     ck.n_global = p->n_global;
-    ck.round = p->round;
+    ck.round = round;
+    ck.pending = pending ? 1u : 0u;
     ck.seq = ++p->wait_seq;
-    ck.status = p->d_status;
+    ck.status = status_of(p, round);
     ck.host = p->h_status_dev;
     ck.host_flags = p->h_status_dev ? reinterpret_cast<uint8_t*>(p->h_status_dev + 1) : nullptr;
-    DTT_CUDA_TRY(launch_check(ck, p->producer_stream));
-    // The next round's copier queues behind this one while the host waits: its launch leaves
-    // the next round's critical path.  It copies nothing until start() claims it.
-    if (early_allowed(p)) {
-        const int erc = launch_early(p);
-        if (erc != DTT_OK) return erc;
-    }
-    // The check stores its sequence number last, after every flag and status word: poll that
-    // word, and ask the stream now and then so that a failed launch or a dead context ends the
-    // wait with the CUDA error instead of spinning.
+    DTT_CUDA_TRY(launch_check(ck, stream));
+    *seq = ck.seq;
+    return DTT_OK;
+}
+
+// Poll the mapped host block until the check with sequence number `seq` has reported.  The check
+// stores its sequence number last, after every flag and status word; the stream it runs on is
+// asked now and then, so that a failed launch or a dead context ends the wait with the CUDA
+// error instead of spinning.
+int await_check(dtt_plan* p, uint32_t seq, cudaStream_t stream) {
     const uint32_t* done = &p->h_status->done;
     for (uint64_t spin = 1;; ++spin) {
-        if (__atomic_load_n(done, __ATOMIC_ACQUIRE) == ck.seq) break;
+        if (__atomic_load_n(done, __ATOMIC_ACQUIRE) == seq) return DTT_OK;
         if ((spin & 4095) == 0) {
-            const cudaError_t e = cudaStreamQuery(p->producer_stream);
+            const cudaError_t e = cudaStreamQuery(stream);
             if (e == cudaErrorNotReady) continue;
-            if (e != cudaSuccess) {
-                abort_early(p);
-                return fail(DTT_ECUDA, "dtt_plan_wait: %s", cudaGetErrorString(e));
-            }
-            if (__atomic_load_n(done, __ATOMIC_ACQUIRE) == ck.seq) break;
-            abort_early(p);
+            if (e != cudaSuccess) return fail(DTT_ECUDA, "dtt_plan_wait: %s", cudaGetErrorString(e));
+            if (__atomic_load_n(done, __ATOMIC_ACQUIRE) == seq) return DTT_OK;
             return fail(DTT_ECUDA, "dtt_plan_wait: the check kernel finished without reporting");
         }
     }
+}
+
+// Turn the reported flags and status words of round `round`'s check into a report and a code.
+int read_report(dtt_plan* p, uint32_t round, int ce_rc, dtt_report* report) {
     dtt_report rep{};
-    rep.round = p->round;
+    rep.round = round;
     rep.copier_timeouts = p->h_status->st.copier_timeouts + (ce_rc == DTT_ETIMEDOUT ? 1u : 0u);
     rep.device_status = p->h_status->st.misuse;
     const bool late = p->h_status->st.check_late != 0;
@@ -1313,20 +1351,71 @@ int dtt_plan_wait(dtt_plan* p, dtt_report* report) {
     int rc = DTT_OK;
     if (rep.n_extra) {
         rc = fail(DTT_EEXTRA, "dtt_plan_wait: %u chunk(s) got extra marks in round %u (first: %u)",
-                  rep.n_extra, p->round, rep.extra_chunks[0]);
+                  rep.n_extra, round, rep.extra_chunks[0]);
     } else if (rep.device_status) {
         rc = fail(DTT_EINVAL, "dtt_plan_wait: %s",
                   (rep.device_status & DTT_DEV_EBADCHUNK)
-                      ? "a kernel marked, or asked reusable of, a chunk its rank does not own"
-                      : "a kernel waited on a group the plan does not have");
+                      ? "a kernel marked, or asked reusable or writable of, a chunk its rank does not own"
+                  : (rep.device_status & DTT_DEV_EBADGROUP)
+                      ? "a kernel waited on a group the plan does not have"
+                      : "a producer gave up waiting for a chunk to become writable");
     } else if (rep.n_short) {
         rc = fail(DTT_ETIMEDOUT, "dtt_plan_wait: %u chunk(s) short in round %u (first: %u)",
-                  rep.n_short, p->round, rep.short_chunks[0]);
+                  rep.n_short, round, rep.short_chunks[0]);
     } else if (late) {
         rc = fail(DTT_ETIMEDOUT, "dtt_plan_wait: the copier had not finished when the check gave up");
     }
     rep.status = rc;
     if (report) *report = rep;
+    return rc;
+}
+
+// Overlapping rounds: check the pending round, on the plan's aux stream after the producers
+// queued before it became pending (not after the next round's).
+int wait_pending(dtt_plan* p, dtt_report* report) {
+    const uint32_t R = p->pending;
+    int ce_rc = DTT_OK;
+    if (p->ce) ce_rc = ce_join(p, p->aux_stream, R);   // the check follows the round's copies
+    DTT_CUDA_TRY(cudaStreamWaitEvent(p->aux_stream, p->ev_pending, 0));
+    uint32_t seq = 0;
+    int rc = launch_round_check(p, R, p->pending_copier ? p->copier_ctas : 0, true, p->aux_stream, &seq);
+    if (rc == DTT_OK) rc = await_check(p, seq, p->aux_stream);
+    if (rc != DTT_OK) return rc;
+    rc = read_report(p, R, ce_rc, report);
+    p->pending = 0;
+    p->pending_copier = false;
+    if (rc != DTT_OK) p->state = DTT_PLAN_FAILED;   // the current round, if started, is closed with the plan
+    return rc;
+}
+
+}  // namespace
+
+int dtt_plan_wait(dtt_plan* p, dtt_report* report) {
+    if (!p) return fail(DTT_EINVAL, "dtt_plan_wait: NULL plan");
+    if (p->pending && p->state != DTT_PLAN_FAILED) return wait_pending(p, report);
+    if (p->state != DTT_PLAN_RUNNING) return fail(DTT_ESTATE, "dtt_plan_wait: plan is not RUNNING (state %d)", p->state);
+    const int lc = dtt_plan_launch_copier(p);    // deferred plans: the copier runs now
+    if (lc != DTT_OK) return lc;
+    // The check follows the producers on their stream and waits on the device for the copier's
+    // CTAs to count themselves out (no event between the streams, no launch gap after the copier).
+    int ce_rc = DTT_OK;
+    if (p->ce) ce_rc = ce_join(p, p->producer_stream, p->round);   // the check follows every queue
+    uint32_t seq = 0;
+    int rc = launch_round_check(p, p->round, p->copier_launched ? p->copier_ctas : 0, false, p->producer_stream, &seq);
+    if (rc != DTT_OK) return rc;
+    // The next round's copier queues behind this one while the host waits: its launch leaves
+    // the next round's critical path.  It copies nothing until start() claims it.
+    if (early_allowed(p)) {
+        const int erc = launch_early(p);
+        if (erc != DTT_OK) return erc;
+    }
+    rc = await_check(p, seq, p->producer_stream);
+    if (rc != DTT_OK) {
+        abort_early(p);
+        return rc;
+    }
+    p->live_round = false;
+    rc = read_report(p, p->round, ce_rc, report);
     p->state = rc == DTT_OK ? DTT_PLAN_DONE : DTT_PLAN_FAILED;
     if (rc != DTT_OK) abort_early(p);    // a failed plan has no next round
     return rc;
@@ -1334,6 +1423,23 @@ int dtt_plan_wait(dtt_plan* p, dtt_report* report) {
 
 int dtt_plan_next_round(dtt_plan* p) {
     if (!p) return fail(DTT_EINVAL, "dtt_plan_next_round: NULL plan");
+    if (p->opts.overlap && p->state == DTT_PLAN_RUNNING && !p->pending) {
+        // overlapping rounds: the running round stays in flight (pending) and the next one is
+        // prepared.  Its copier goes on the copy stream now, ahead of the next round's, so every
+        // queue serves it first; its check will follow the producers queued so far.
+        if (p->round == 0xFFFFFFFFu)
+            return fail(DTT_EROUNDLIMIT, "dtt_plan_next_round: a plan is limited to 2^32 - 1 rounds");
+        const int lc = dtt_plan_launch_copier(p);
+        if (lc != DTT_OK) return lc;
+        DTT_CUDA_TRY(cudaEventRecord(p->ev_pending, p->producer_stream));
+        p->pending = p->round;
+        p->pending_copier = p->copier_launched;
+        p->live_round = false;
+        p->copier_launched = false;
+        ++p->round;
+        p->state = DTT_PLAN_PREPARED;
+        return DTT_OK;
+    }
     if (p->state != DTT_PLAN_DONE) return fail(DTT_ESTATE, "dtt_plan_next_round: plan is not DONE (state %d)", p->state);
     if (p->round == 0xFFFFFFFFu)
         return fail(DTT_EROUNDLIMIT, "dtt_plan_next_round: a plan is limited to 2^32 - 1 rounds");
@@ -1342,13 +1448,15 @@ int dtt_plan_next_round(dtt_plan* p) {
     return DTT_OK;
 }
 
+uint32_t dtt_plan_pending_round(const dtt_plan* p) { return p ? p->pending : 0; }
+
 namespace {
 
 // Wait for p's last copier to finish (its gates are open by now).
 int drain_copier(dtt_plan* p) {
     if (p->aux_stream && cudaStreamSynchronize(p->aux_stream) != cudaSuccess)
         return fail(DTT_ECUDA, "dtt_plan_close: aux stream failed");
-    if (!p->copier_launched) return DTT_OK;
+    if (!p->copier_launched && !p->pending_copier) return DTT_OK;
     const cudaError_t e = p->done_valid ? cudaEventSynchronize(p->ev_done) : cudaStreamSynchronize(p->copy_stream);
     return e == cudaSuccess ? DTT_OK : fail(DTT_ECUDA, "dtt_plan_close: copy stream failed: %s", cudaGetErrorString(e));
 }
@@ -1398,24 +1506,28 @@ int dtt_plan_close(dtt_plan* p) {
     if (p->early_launched && p->state != DTT_PLAN_RUNNING && p->state != DTT_PLAN_CLOSING &&
         cudaStreamSynchronize(p->copy_stream) != cudaSuccess)
         rc = fail(DTT_ECUDA, "dtt_plan_close: copy stream failed");
-    if (p->state == DTT_PLAN_RUNNING) {
+    // Mid-round: a started round whose check has not run, or a pending round (overlapping rounds).
+    const bool mid = (p->live_round || p->pending) && p->state != DTT_PLAN_CLOSING;
+    if (mid) {
         // what the producers queued so far is written first; then every gate still closed is
-        // opened, so the copier sends each chunk as it stands and exits
+        // opened (for the latest round in flight, which opens the pending round's too), so each
+        // copier sends its chunks as they stand and exits
+        const uint32_t top = p->live_round ? p->round : p->pending;
         if (cudaStreamSynchronize(p->producer_stream) != cudaSuccess)
             rc = fail(DTT_ECUDA, "dtt_plan_close: producer stream failed");
-        if (p->n_global && launch_force_open(p->d_gates, p->d_chunks, p->n_global, p->round, p->aux_stream) != cudaSuccess)
+        if (p->n_global && launch_force_open(p->d_gates, p->d_chunks, p->n_global, top, p->aux_stream) != cudaSuccess)
             rc = fail(DTT_ECUDA, "dtt_plan_close: force-open launch failed");
         if (p->ce) {                 // the proxy sends every chunk as it stands, then drains
             p->ce->open_all.store(true);
-            const int jr = ce_join(p, nullptr);
+            const int jr = ce_join(p, nullptr, 0);
             if (jr != DTT_OK && jr != DTT_ETIMEDOUT) rc = jr;
         }
-        if (!p->copier_launched && p->n_global) {     // deferred: send the chunks now
+        if (p->live_round && !p->copier_launched && p->n_global && !p->ce) {   // deferred: send the chunks now
             if (cudaStreamSynchronize(p->aux_stream) != cudaSuccess || launch_round_copier(p) != DTT_OK)
                 rc = fail(DTT_ECUDA, "dtt_plan_close: copier launch failed");
         }
     }
-    if (p->state == DTT_PLAN_RUNNING || p->state == DTT_PLAN_CLOSING) {
+    if (mid || p->state == DTT_PLAN_CLOSING) {
         bool blocked;
         {
             std::lock_guard<std::mutex> lock(g_plans_mu);
@@ -1451,6 +1563,9 @@ int dtt_plan_stats(dtt_plan* p, double* copier_ms_last, double* copier_ms_total,
 int dtt_plan_define_groups(dtt_plan* p, uint32_t n_groups, const uint32_t* offsets, const uint32_t* chunk_ids) {
     if (!p || !offsets || (!chunk_ids && offsets[n_groups]) || n_groups == 0)
         return fail(DTT_EINVAL, "dtt_plan_define_groups: bad args");
+    if (p->opts.overlap)
+        return fail(DTT_EINVAL, "dtt_plan_define_groups: a plan with overlapping rounds has no groups (a member's "
+                                "next-round arrival would count toward this round's wait)");
     if (p->n_groups) return fail(DTT_ESTATE, "dtt_plan_define_groups: the plan's groups are defined already");
     if (p->state != DTT_PLAN_PREPARED || p->round != p->opts.initial_round || p->wait_seq || p->early_launched)
         return fail(DTT_ESTATE, "dtt_plan_define_groups: groups are defined before the plan's first start");
@@ -1629,6 +1744,7 @@ int dtt_allgather_host(dtt_plan* p, const void* const* host_slices, void* host_o
     if (p->other_dests || p->separate_dst)
         return fail(DTT_EINVAL, "dtt_allgather_host: needs chunks that land at their own offsets");
     if (out_rank >= p->P) return fail(DTT_EINVAL, "dtt_allgather_host: out_rank out of range");
+    if (p->pending) return fail(DTT_ESTATE, "dtt_allgather_host: round %u is still pending: wait for it first", p->pending);
     const uint32_t P = p->P;
     const uint64_t S = p->buf_bytes / P;
     // the byte extent [lo, hi) of every chunk inside its rank's slice
@@ -1895,7 +2011,7 @@ int dtt_consumer_gather(dtt_plan* p, uint32_t rank, void* dst, uint64_t max_poll
     if (p->state != DTT_PLAN_RUNNING) return fail(DTT_ESTATE, "dtt_consumer_gather: plan is not RUNNING");
     if (stream == p->copy_stream) return fail(DTT_EINVAL, "dtt_consumer_gather: use a stream other than the copy stream");
     if (!p->n_global) return DTT_OK;
-    const CopierParams cp = copier_params(p);
+    const CopierParams cp = copier_params(p, p->round);
     DTT_CUDA_TRY(launch_consumer(cp, make_handle(p, rank), static_cast<char*>(dst), max_polls, status, ctas, stream));
     return DTT_OK;
 }

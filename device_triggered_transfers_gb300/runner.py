@@ -127,6 +127,27 @@ def run_round(st: Setup, raise_on_error: bool = True):
     return st.plan.wait(raise_on_error=raise_on_error)
 
 
+def run_overlapped(st: Setup, rounds: int, raise_on_error: bool = True, produce=None):
+    """`rounds` rounds two at a time on a plan made with opts.overlap: round R is started and its
+    producer launched before round R-1's wait (the producer waits, chunk by chunk, for round R-1's
+    copies of what it overwrites), then the plan advances with round R still in flight.  The
+    last round is waited for at the end.  produce(handles) launches a round's producer (default:
+    the fill).  Returns the reports in round order."""
+    reps = []
+    for i in range(rounds):
+        handles = st.plan.start(st.producer_stream)
+        if produce is None:
+            dtt_fill_producer(st.buf_ptrs, st.desc, handles, st.producer_stream)
+        else:
+            produce(handles)
+        if st.plan.pending:
+            reps.append(st.plan.wait(raise_on_error=raise_on_error))
+        if i + 1 < rounds:
+            st.plan.next_round()
+    reps.append(st.plan.wait(raise_on_error=raise_on_error))
+    return reps
+
+
 def sm_count() -> int:
     """Streaming multiprocessors of the current CUDA device (the launch shapes below scale with
     it)."""

@@ -253,14 +253,36 @@ typedef struct dtt_plan_opts {
                                 copier is launched at start) with time_copier, deferred_copier
                                 = 1, a copy stream another live plan uses, or a device without
                                 host-native atomics.  At most 1000000; 0 = off */
+    uint32_t overlap;         /* 1: overlapping rounds ("Triggered Plans", Not supported yet:
+                                "Overlapping rounds" -- wait() had to return before next_round()
+                                could prepare the next round).  dtt_plan_next_round may then also
+                                be called while the round is RUNNING: that round stays in flight
+                                (pending) and the next one is PREPARED, so at most two rounds are in
+                                flight.  The pending round's copier runs before the next round's on
+                                the copy stream, so every (source, peer) queue serves the pending
+                                round first.  A producer of round R may write a chunk only once
+                                round R-1's copies of it have landed (dtt_writable; the library's
+                                producers wait for it on their own), and whatever reads what round
+                                R-1 delivered must be done before round R's producers run.
+                                dtt_plan_wait checks the pending round first.  Not with
+                                deferred_copier = 1 (a round's producers wait for the previous
+                                round's copier) or chunk groups (a member's next-round arrival
+                                would count toward this round's group wait); the early copier is
+                                not used (the next round's copier is queued at its start, behind the
+                                pending one).  0 = rounds one at a time */
 } dtt_plan_opts;
 
 void dtt_plan_opts_default(dtt_plan_opts* opts);
 
 #define DTT_HANDLE_TIMESTAMPS 1u   /* dtt_handle.flags bit: stamp gate-open times */
+#define DTT_HANDLE_OVERLAP 2u      /* dtt_handle.flags bit: the plan overlaps rounds, so a producer
+                                      waits for dtt_writable before it writes a chunk */
 #define DTT_DEV_EBADCHUNK 1u       /* device status bit: a rank marked (or asked dtt_reusable of)
                                       a chunk it does not own */
 #define DTT_DEV_EBADGROUP 2u       /* device status bit: a wait named a group the plan lacks */
+#define DTT_DEV_EWRITABLE 4u       /* device status bit: a library producer's wait for a chunk to
+                                      become writable (overlapping rounds) ran out; it left its part
+                                      of the chunk unwritten, and wait() reports the round failed */
 
 /* A plan's chunk groups (dtt_plan_define_groups): device arrays owned by the plan, their
  * addresses carried by value in every handle.  A group is a set of global chunk ids, of any
@@ -349,7 +371,7 @@ typedef struct dtt_report {
  * every SM room for producer CTAs: creation fails with DTT_EINVAL when the copier CTAs of one
  * SM would take more than 1024 threads or 32768 registers, or (bulk-copy path) more shared
  * memory than the SM has (a copier CTA left waiting for shared memory would keep the producer
- * from starting).
+ * from starting).  opts->overlap needs deferred_copier 0 or 2 (DTT_EINVAL otherwise).
  * Errors: DTT_EINVAL, DTT_EOUTOFROWS, DTT_EOVERLAP, DTT_ECAPACITY, DTT_ENOMEM, DTT_ECUDA. */
 int dtt_plan_create(void* const* bufs, uint64_t buf_bytes, uint32_t P,
                     const dtt_schedule* const* scheds, const dtt_plan_opts* opts,
@@ -360,7 +382,8 @@ int dtt_plan_create(void* const* bufs, uint64_t buf_bytes, uint32_t P,
  * orders its check after the work queued there.  It must differ from the copy stream.
  * The copier polls each source's gates in schedule order, so chunks completed out of order
  * are correct but wait for earlier ones ("Triggered Plans", The kernel author's contract,
- * item 1).  Errors: DTT_ESTATE (not PREPARED), DTT_EINVAL, DTT_ECUDA. */
+ * item 1).  With a round pending (opts.overlap) the copier queues behind the pending round's on
+ * the copy stream.  Errors: DTT_ESTATE (not PREPARED), DTT_EINVAL, DTT_ECUDA. */
 int dtt_plan_start(dtt_plan* plan, cudaStream_t producer_stream, dtt_handle* handles);
 
 /* Plans with opts.deferred_copier set: launch this round's copier now on the copy stream --
@@ -377,15 +400,29 @@ int dtt_plan_handle(const dtt_plan* plan, uint32_t rank, dtt_handle* out);
  * rounds; "Triggered SDMA Plans", Design notes, completion).  The check kernel is queued on
  * the producer stream (after everything the producers queued) and waits on the device, at
  * most 8 x max_polls polls, for the round's copier CTAs to finish; it writes its verdict into
- * mapped host memory, which this call polls.  Fills *report when non-NULL.
- * Returns DTT_OK (plan DONE), DTT_EEXTRA or DTT_ETIMEDOUT (plan FAILED; the report names the
- * chunks, or the copier had not finished), DTT_ESTATE (not RUNNING) or DTT_ECUDA. */
+ * mapped host memory, which this call polls.  Fills *report when non-NULL (report->round names
+ * the round checked).
+ * Overlapping rounds (opts.overlap): while a round is pending, this call checks that round, on an
+ * internal stream ordered after the producers queued before its dtt_plan_next_round (not after
+ * the next round's); the next round's marks may already count, so a count above writers is not
+ * read as an extra mark there -- the gate row's error word, which the mark that passes its own
+ * round's count sets, reports extra marks.  On success the plan's state is left as it was
+ * (PREPARED or RUNNING, for the next round); on failure the plan is FAILED.
+ * Returns DTT_OK (plan DONE, or no longer pending), DTT_EEXTRA or DTT_ETIMEDOUT (plan FAILED; the
+ * report names the chunks, or the copier had not finished), DTT_ESTATE (not RUNNING and nothing
+ * pending) or DTT_ECUDA. */
 int dtt_plan_wait(dtt_plan* plan, dtt_report* report);
 
 /* Advance to the next round: "done reading this round's data" ("Triggered Plans", The kernel
- * author's contract, item 6).  Errors: DTT_ESTATE (not DONE), DTT_EROUNDLIMIT (the round is
- * already 2^32 - 1; the plan stays DONE). */
+ * author's contract, item 6).  With opts.overlap, also from RUNNING when no round is pending: the
+ * running round becomes pending (its copier is launched now if it was deferred, and its check
+ * will follow the producers queued so far on the producer stream) and the next round is PREPARED.
+ * Errors: DTT_ESTATE (not DONE, nor RUNNING with overlap and nothing pending), DTT_EROUNDLIMIT
+ * (the round is already 2^32 - 1; the state is unchanged), DTT_ECUDA. */
 int dtt_plan_next_round(dtt_plan* plan);
+
+/* The round in flight behind the current one (opts.overlap), or 0 when none is. */
+uint32_t dtt_plan_pending_round(const dtt_plan* plan);
 
 /* Close the plan ("Triggered Plans", The kernel author's contract, close()).  In the middle of
  * a round, the work already queued on the producer stream finishes first, then every gate
@@ -429,7 +466,8 @@ int dtt_plan_stats(dtt_plan* plan, double* copier_ms_last, double* copier_ms_tot
  * with dtt_wait_group.  Allowed once per plan, before its first dtt_plan_start; the counters
  * begin as after the rounds before opts.initial_round.  The tables live on the device until the
  * plan is closed.  Errors: DTT_EINVAL (empty group, id out of range or repeated in a group,
- * n_groups == 0), DTT_ESTATE (started already, or groups defined already), DTT_ECUDA. */
+ * n_groups == 0, a plan with opts.overlap), DTT_ESTATE (started already, or groups defined
+ * already), DTT_ECUDA. */
 int dtt_plan_define_groups(dtt_plan* plan, uint32_t n_groups, const uint32_t* offsets,
                            const uint32_t* chunk_ids);
 
@@ -468,7 +506,8 @@ int dtt_plan_read_gates(dtt_plan* plan, uint64_t* host, uint64_t n_words);
  * arrival into pinned, mapped host memory, and the host copies every slice of out_rank's
  * buffer back, on another stream of the plan, as far as its chunks have arrived.  The call
  * returns when everything has landed in host_out.  Needs an all-gather plan in state
- * PREPARED.  The report is filled as by dtt_plan_wait.  Errors: as start / wait / next_round,
+ * PREPARED with no round pending (opts.overlap: check the pending round first).  The report
+ * is filled as by dtt_plan_wait.  Errors: as start / wait / next_round,
  * DTT_ETIMEDOUT if a slice could not be copied back completely. */
 int dtt_allgather_host(dtt_plan* plan, const void* const* host_slices, void* host_out,
                        uint32_t out_rank, cudaStream_t stream, dtt_report* report);
@@ -563,7 +602,9 @@ int dtt_gemm_producer(const void* A, const void* Bt, void* const* bufs, uint32_t
  * dtt_plan_start).  Work queued earlier on `stream` -- host-to-device copies of the chunk's
  * data, other kernels -- precedes the marks.  It serves host-fed rounds and lets a caller give
  * a chunk an extra mark or leave one short ("Triggered Plans", The kernel author's contract,
- * item 2, names both).  Errors: DTT_EINVAL, DTT_ECUDA. */
+ * item 2, names both).  With overlapping rounds the bytes of a chunk copied in before its marks
+ * must not land before the previous round's copies of it have (dtt_writable): the marks
+ * themselves do not wait.  Errors: DTT_EINVAL, DTT_ECUDA. */
 int dtt_publish(const dtt_handle* handles, uint32_t P, uint32_t first_chunk, uint32_t n_chunks,
                 uint32_t marks, cudaStream_t stream);
 

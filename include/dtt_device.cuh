@@ -1,6 +1,6 @@
 /*
- * dtt_device.cuh -- device side of a triggered plan: mark_ready, arrived, wait, reusable and
- * the group waits.
+ * dtt_device.cuh -- device side of a triggered plan: mark_ready, arrived, wait, reusable,
+ * writable and the group waits.
  *
  * Include from producer and consumer kernels; the kernel receives a dtt_handle (include/dtt.h)
  * by value.  Every function here is called by ALL threads of a CTA (dtt_mark_ready_cluster:
@@ -18,8 +18,9 @@
  *  - arrived / wait: thread 0 reads the gate with an acquire load (gpu scope); a CTA barrier
  *    passes the result to the other threads, and data they load afterwards is this round's.
  *    Polls are counted, never clock-bounded.
- *  - reusable: thread 0 acquires the chunk's completion word, which the copier bumps with a
- *    release add after every copy of the chunk has landed (and so after its reads of it).
+ *  - reusable / writable: thread 0 acquires the chunk's completion word, which the copier bumps
+ *    after a release fence once every copy of the chunk has landed (and so after its reads of
+ *    it); writable asks for the previous round's count (overlapping rounds).
  *  - groups: the mark that opens a gate, and the copier's arrival signal at a peer, add one to
  *    that rank's counters of the chunk's groups after a release fence; dtt_wait_group acquires
  *    the counter, so data of every member read after it is this round's.
@@ -287,6 +288,66 @@ __device__ __forceinline__ int dtt_wait_reusable(const dtt_handle& h, uint32_t c
     }
     __syncthreads();
     return dtt_wait_reusable_result;
+}
+
+namespace dtt_dev {
+
+/* The completion count at which rank h.rank's own `chunk` may be written in round h.round:
+ * every copy of it made in round h.round - 1 has landed, (round - 1) * receivers deliveries. */
+__device__ __forceinline__ const uint64_t* writable_word(const dtt_handle& h, uint32_t chunk, uint64_t* target) {
+    if (chunk < h.first_chunk || chunk >= h.first_chunk + h.n_chunks) {
+        atomicOr(h.status, DTT_DEV_EBADCHUNK);
+        return nullptr;
+    }
+    *target = (uint64_t)(h.round - 1) * receivers(h, chunk);
+    return gate_row(h, h.rank, chunk) + DTT_GATE_COMPLETION;
+}
+
+/* One thread: bounded wait until writable (true), or false when the polls ran out. */
+__device__ __forceinline__ bool wait_writable_one(const dtt_handle& h, uint32_t chunk, uint64_t max_polls) {
+    uint64_t target = 0;
+    const uint64_t* w = writable_word(h, chunk, &target);
+    if (!w) return false;
+    uint32_t ns = 0;
+    for (uint64_t i = 0; i < max_polls; ++i) {
+        if (ld_acquire(w) >= target) return true;
+        __nanosleep(ns);
+        ns = ns < 256 ? ns + 32 : 256;
+    }
+    return false;
+}
+
+}  // namespace dtt_dev
+
+/* Overlapping rounds ("Triggered Plans", Not supported yet: "Overlapping rounds"; plans made with
+ * opts.overlap): may this rank write its own `chunk` in round h.round -- has every copy of it
+ * made in the previous round landed, so that no copier still reads the previous round's bytes?
+ * That is the chunk's completion word at (round - 1) * receivers.  Always true when rounds do
+ * not overlap (the previous round was checked before this one started).  The acquire orders the
+ * copier's reads before the caller's later writes.  A chunk of another rank sets
+ * DTT_DEV_EBADCHUNK and reads false. */
+__device__ __forceinline__ bool dtt_writable(const dtt_handle& h, uint32_t chunk) {
+    __shared__ int dtt_writable_flag;
+    __syncthreads();
+    if (dtt_dev::first_thread()) {
+        uint64_t target = 0;
+        const uint64_t* w = dtt_dev::writable_word(h, chunk, &target);
+        dtt_writable_flag = w && dtt_dev::ld_acquire(w) >= target;
+    }
+    __syncthreads();
+    return dtt_writable_flag != 0;
+}
+
+/* Wait until dtt_writable(h, chunk), polling at most max_polls times; call it before the first
+ * write of a chunk in a round.  Returns 0, or DTT_ETIMEDOUT if the polls ran out (or the chunk is
+ * not this rank's): the chunk must then be left unwritten. */
+__device__ __forceinline__ int dtt_wait_writable(const dtt_handle& h, uint32_t chunk, uint64_t max_polls) {
+    __shared__ int dtt_wait_writable_result;
+    __syncthreads();
+    if (dtt_dev::first_thread())
+        dtt_wait_writable_result = dtt_dev::wait_writable_one(h, chunk, max_polls) ? 0 : DTT_ETIMEDOUT;
+    __syncthreads();
+    return dtt_wait_writable_result;
 }
 
 #endif /* DTT_DEVICE_CUH */

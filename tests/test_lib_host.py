@@ -334,3 +334,16 @@ def test_plan_rank_count_is_checked_before_any_device_call():
     assert rc == D.EINVAL
     rc = D.lib().dtt_plan_create(arr, 1 << 20, 0, None, None, None, C.byref(out))
     assert rc == D.EINVAL
+
+
+def test_overlap_options_are_checked_before_any_device_call():
+    # overlapping rounds need the copier beside the producers: a copier ordered after them
+    # (deferred_copier = 1) would leave the next round's producers waiting on nothing
+    arr = (C.c_void_p * 2)(0x1000, 0x2000)
+    out = C.c_void_p()
+    for over in (dict(overlap=1, deferred_copier=1), dict(overlap=2)):
+        opts = D.dtt_plan_opts_default(**over)
+        rc = D.lib().dtt_plan_create(arr, 1 << 20, 2, None, C.byref(opts), None, C.byref(out))
+        assert rc == D.EINVAL, over
+        assert b"overlap" in D.lib().dtt_last_error()
+    assert D.lib().dtt_plan_pending_round(None) == 0
