@@ -322,15 +322,19 @@ def run_reference(args):
 
 
 def measure_workload(w, args, K, warmup, latency_rounds, isolated_rounds, with_e2e, world=1,
-                     clocks_dev=None, early_us=None, method=None):
+                     clocks_dev=None, early_us=None, method=None, overlap=None, pace=None):
     """Time K rounds of workload w in the launch the benchmark uses for it (runner.bench_launch),
     then the kernel-timing pass, the gate timestamps, the isolated kernels and (optionally) the
-    host-buffer round.  Returns a dict of raw measurements (seconds, milliseconds, bytes)."""
+    host-buffer round.  overlap (None: the launch's choice): rounds two at a time (opts.overlap):
+    each step starts its round, launches the producer, waits for the round before it and leaves
+    its own round pending; the timed region ends with the wait for the last round.  pace: the
+    fill producer's pacing (None: the launch's own).  Returns a dict of raw measurements
+    (seconds, milliseconds, bytes)."""
     import torch
     import device_triggered_transfers_gb300 as D
     from device_triggered_transfers_gb300 import runner
 
-    launch = dict(runner.bench_launch(w))
+    launch = dict(runner.bench_launch(w, overlap))
     # the copier runs on a stream the bench can put events on
     copy_stream = torch.cuda.Stream(priority=-1)
     # the headline pass records no per-launch events (a timed event between two launches on a
@@ -344,8 +348,12 @@ def measure_workload(w, args, K, warmup, latency_rounds, isolated_rounds, with_e
         launch.pop("pace", None)
     if args.deferred:
         opts.deferred_copier = 1
+        opts.overlap = 0      # a round's producer would wait for a copier that runs after it
     if early_us is not None:
         opts.early_copier_us = early_us
+    overlap = bool(opts.overlap)
+    if pace is not None and w.K == 0:
+        launch["pace"] = pace
     opts.time_copier = 0
     copier_method = {"method": opts.method, "piece_bytes": opts.piece_bytes, "stages": opts.stages,
                      "copier_threads": opts.copier_threads, "ctas_per_sm": opts.ctas_per_sm}
@@ -371,9 +379,10 @@ def measure_workload(w, args, K, warmup, latency_rounds, isolated_rounds, with_e
             D.dtt_fill_producer(st.buf_ptrs, desc_unpaced if deferred else st.desc, h, prod)
     prod = st.producer_stream
 
-    def make_step(plan, deferred):
+    def make_step(plan, deferred, overlapped=False):
         """One round.  ev: two events around the producer launch (producer stream), or None.
-        deferred: the plan's copier starts only after the producer."""
+        deferred: the plan's copier starts only after the producer.  overlapped: the round is
+        left pending (its wait comes in the next step, or in drain)."""
         def step(ev=None):
             h = plan.start(prod)
             if ev is not None:
@@ -381,11 +390,21 @@ def measure_workload(w, args, K, warmup, latency_rounds, isolated_rounds, with_e
             produce(h, deferred)
             if ev is not None:
                 ev[1].record(prod)
+            if overlapped:
+                if plan.pending:
+                    plan.wait()
+                plan.next_round()
+                return
             if deferred:      # the copier starts once the producer has finished
                 plan.launch_copier()
             plan.wait()
             plan.next_round()
         return step
+
+    def drain(plan):
+        """Wait for a round still pending (overlapped steps)."""
+        if plan.pending:
+            plan.wait()
 
     def timed(plan, step, K, producer_events):
         """K steps between two events on the producer stream; returns (seconds, copier ms per
@@ -397,6 +416,7 @@ def measure_workload(w, args, K, warmup, latency_rounds, isolated_rounds, with_e
         e0.record(prod)
         for i in range(K):
             step(evs[i])
+        drain(plan)
         e1.record(prod)
         e1.synchronize()
         torch.cuda.synchronize()
@@ -405,18 +425,21 @@ def measure_workload(w, args, K, warmup, latency_rounds, isolated_rounds, with_e
         prod_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs) if producer_events else None
         return e0.elapsed_time(e1) / 1e3, cop, prod_ms
 
-    step = make_step(st.plan, opts.deferred_copier == 1)
+    step = make_step(st.plan, opts.deferred_copier == 1, overlap)
     for _ in range(warmup):
         step()
+    drain(st.plan)
     torch.cuda.synchronize()
     out = {"w": w, "launch": launch, "copier_method": copier_method, "gemm": gemm,
-           "deferred_copier": opts.deferred_copier, "early_copier_us": opts.early_copier_us}
+           "deferred_copier": opts.deferred_copier, "early_copier_us": opts.early_copier_us,
+           "overlap": overlap}
     if args.profile_rounds:
         # whole rounds (producer, copier and check together) inside one profiler range, for a
         # range-replay capture of their DRAM traffic; no timing
         torch.cuda.profiler.start()
         for _ in range(args.profile_rounds):
             step()
+        drain(st.plan)
         torch.cuda.synchronize()
         torch.cuda.profiler.stop()
         st.plan.close()
@@ -455,10 +478,11 @@ def measure_workload(w, args, K, warmup, latency_rounds, isolated_rounds, with_e
     if opts.method == D.COPY_ENGINE:      # no copier kernel: the round is the transport's time
         out.update(timing_pass_s=elapsed, copier_ms=elapsed / K * 1e3, producer_ms=None)
     else:
-        plan3 = side_plan(time_copier=1, deferred_copier=opts.deferred_copier)
-        step3 = make_step(plan3, opts.deferred_copier == 1)
+        plan3 = side_plan(time_copier=1, deferred_copier=opts.deferred_copier, overlap=opts.overlap)
+        step3 = make_step(plan3, opts.deferred_copier == 1, overlap)
         for _ in range(3):
             step3()
+        drain(plan3)
         torch.cuda.synchronize()
         t3, copier_ms, producer_ms = timed(plan3, step3, K, producer_events=gemm)
         plan3.close()
@@ -470,6 +494,9 @@ def measure_workload(w, args, K, warmup, latency_rounds, isolated_rounds, with_e
     out["n_chunks_total"] = sum(n_chunks_all[r] for r in w.senders())
     for _ in range(latency_rounds):
         step()
+        if overlap:           # a round whose producer ran beside the previous round's copier
+            step()
+            drain(st.plan)
         g = st.plan.read_gates()
         n_global, first, n_chunks, _ = st.plan.info()
         t_open_min, t_arr_max = None, 0
@@ -613,8 +640,10 @@ def run_ours(args):
     w = workload(args)
     K = args.steps
     early = None if args.early_us < 0 else args.early_us
+    pace = None if args.pace < 0 else args.pace
     m = measure_workload(w, args, K, args.warmup, args.latency_rounds, args.isolated_rounds,
-                         with_e2e=not args.no_e2e, world=world, clocks_dev=dev, early_us=early)
+                         with_e2e=not args.no_e2e, world=world, clocks_dev=dev, early_us=early,
+                         overlap=args.overlap, pace=pace)
     if m.get("profiled"):
         if rank == 0:
             print(json.dumps({"profile_rounds": args.profile_rounds, "workload": w.name,
@@ -638,7 +667,8 @@ def run_ours(args):
             if name == w.name:
                 continue
             wc = W.CONFIGS[name]
-            mc = measure_workload(wc, args, steps, 3, 5, 5, with_e2e=False, early_us=early)
+            mc = measure_workload(wc, args, steps, 3, 5, 5, with_e2e=False, early_us=early,
+                                  overlap=args.overlap)
             Dc = wc.delivered_bytes_per_round()
             sc = summarize(mc, steps, mc["elapsed_s"], Dc * steps, peak, peak_kind)
             per_config[name] = {
@@ -677,14 +707,21 @@ def run_ours(args):
     if m["early_copier_us"] and m["deferred_copier"] != 1:
         mode += ("; each round's copier launched early, by the previous round's plan_wait, and "
                  "claimed by plan_start (waits up to %d us for it)" % m["early_copier_us"])
+    if m["overlap"]:
+        mode += ("; overlapping rounds: a round's producer runs while the previous round's copier "
+                 "still copies (each chunk written once its previous copies landed), its copier "
+                 "queued behind the previous one")
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": t_max / K * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
         "config": {"workload": describe(w, m["launch"], m["copier_method"]), "parallelism": f"replicas{world}",
                    "l2": l2_note(w, dev),
-                   "step": "plan_start + %s producer + copier + plan_wait + next_round"
-                           % ("GEMM" if gemm else "fill"),
+                   "step": (("plan_start + %s producer + copier + plan_wait of the previous round + "
+                             "next_round (this round left pending); the timed region ends with the "
+                             "last round's plan_wait" if m["overlap"] else
+                             "plan_start + %s producer + copier + plan_wait + next_round")
+                            % ("GEMM" if gemm else "fill")),
                    "mode": mode},
         "hbm_frac_end_to_end": s["hbm_frac_end_to_end"],
         "roofline": s["roofline"],
@@ -724,7 +761,7 @@ def run_consumer(args):
     copy_stream, cons = torch.cuda.Stream(priority=-1), torch.cuda.Stream()
     # the producer of the benchmark's launch (its chunks open one wave after another), with the
     # vector copier
-    launch = {k: v for k, v in runner.bench_launch(w).items() if k != "opts"}
+    launch = {k: v for k, v in runner.bench_launch(w, overlap=False).items() if k != "opts"}
     if args.consumer_copier == "bulk":    # one CTA per SM with a ring small enough for the GEMM's
         copier_desc = "bulk copies, one CTA per SM, 2 x 32 KiB stages"
     else:
@@ -818,7 +855,7 @@ def run_ce_fanout(args):
     from device_triggered_transfers_gb300 import runner
     w = workload(args)
     S = w.slice_bytes
-    launch = dict(runner.bench_launch(w))
+    launch = dict(runner.bench_launch(w, overlap=False))
     launch.pop("pace", None)          # the copier starts after the producer here
     opts = launch.pop("opts", None) or D.dtt_plan_opts_default()
     opts.deferred_copier, opts.time_copier = 1, 1
@@ -944,6 +981,14 @@ def main(argv=None):
                     help="launch each round's copier after its producer (for profilers that "
                          "serialise kernels)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--overlap", dest="overlap", action="store_const", const=True, default=None,
+                    help="overlapping rounds (opts.overlap) for every workload: each round's "
+                         "producer runs while the previous round's copier still copies (default: "
+                         "where the benchmark's launch uses them)")
+    ap.add_argument("--sequential", dest="overlap", action="store_const", const=False,
+                    help="rounds one at a time for every workload")
+    ap.add_argument("--pace", type=int, default=-1,
+                    help="the fill producer's pacing in chunks (default: the launch's own)")
     ap.add_argument("--latency-rounds", type=int, default=20)
     ap.add_argument("--isolated-rounds", type=int, default=20)
     ap.add_argument("--barrier", action="store_true",

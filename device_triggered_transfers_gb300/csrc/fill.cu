@@ -199,8 +199,40 @@ __device__ __forceinline__ void group_mark(const dtt_handle& h, uint32_t chunk, 
     __syncthreads();
 }
 
+// Per-chunk waits of a fill CTA, made when it reaches chunk k of its rank (bits of `waits`):
+//  - kWritable (overlapping rounds): the previous round's copies of chunk k must have landed
+//    before its bytes change (that round's copier may still be reading them); every CTA of a
+//    program asks for itself.  A wait that runs out sets kNoWrite -- the rest of this CTA's
+//    writes are left undone, while its marks still go out, so no barrier of a cluster or counter
+//    of a group is left waiting -- and DTT_DEV_EWRITABLE, which fails the round.
+//  - kPacing: keep the bytes written but not yet delivered within `pace` chunks of this rank,
+//    so that the copier reads them from L2; the result does not depend on the outcome.  A wait
+//    that runs out means the copier is not keeping up (or not running): the CTA stops pacing, so
+//    it stalls at most once per launch.  With overlapping rounds the chunks before this round's
+//    first `pace` are the previous round's last ones (its copier runs just before this round's):
+//    chunk k < pace waits for the previous round's delivery of chunk n - pace + k.
+// The loop carries two words for them: the waits still made, and the current chunk.
+constexpr uint32_t kPacing = 1u, kWritable = 2u, kNoWrite = 4u;
+
+__device__ __forceinline__ uint32_t chunk_waits(const dtt_handle& h, uint32_t k, uint32_t waits, uint32_t pace) {
+    if ((waits & kWritable) && !(waits & kNoWrite) &&
+        dtt_wait_writable(h, h.first_chunk + k, kWritablePolls) != 0) {
+        waits |= kNoWrite;
+        if (dtt_dev::first_thread()) atomicOr(h.status, DTT_DEV_EWRITABLE);
+    }
+    if (waits & kPacing) {
+        int w = 0;
+        if (k >= pace)
+            w = dtt_wait_reusable(h, h.first_chunk + (k - pace), kPacePolls);
+        else if ((waits & kWritable) && h.n_chunks + k >= pace)
+            w = dtt_wait_writable(h, h.first_chunk + (h.n_chunks + k - pace), kPacePolls);
+        if (w != 0) waits &= ~kPacing;
+    }
+    return waits;
+}
+
 template <int DT>
-__global__ void __launch_bounds__(1024) fill_kernel(const __grid_constant__ FillParams p) {
+__device__ __forceinline__ void fill_body(const FillParams& p) {
     const uint32_t r = blockIdx.y;
     if (!((p.rank_mask >> r) & 1u)) return;
     const dtt_handle& h = p.h[r];
@@ -210,38 +242,15 @@ __global__ void __launch_bounds__(1024) fill_kernel(const __grid_constant__ Fill
     const uint64_t T = tiles_m * tiles_n;
     const uint32_t salt = fmix32(p.seed ^ fmix32(r ^ fmix32(h.round)));
     char* base = p.bufs[r] + p.slice_off[r];
-    uint64_t paced = ~0ull;       // the last chunk this program waited for
-    bool pacing = p.pace != 0;    // off for the rest of the launch once a pacing wait runs out
-    const bool overlap = (h.flags & DTT_HANDLE_OVERLAP) != 0;
-    uint32_t writable = 0xFFFFFFFFu;   // overlapping rounds: the chunk this CTA last found writable
-    bool write = true;            // false once a writable wait ran out: this CTA writes no more
+    // the waits a CTA makes when it reaches a new chunk (chunk_waits): bits of kPacing,
+    // kWritable and kNoWrite, two words carried through the loop
+    uint32_t waits = (p.pace ? kPacing : 0u) | ((h.flags & DTT_HANDLE_OVERLAP) ? kWritable : 0u);
+    uint32_t cur = 0xFFFFFFFFu;   // index within the rank of the chunk of the last step
     for (uint64_t step = prog; step < T; step += p.NP) {
-        if (overlap && write) {
-            // the previous round's copies of the chunk must have landed before its bytes change
-            // (its copier may still be reading them); every CTA of a program asks for itself.
-            // A wait that runs out leaves the rest of this CTA's writes undone (the marks still
-            // go out, so no barrier of a cluster or counter of a group is left waiting) and
-            // fails the round.
-            const uint32_t chunk = h.first_chunk + (p.mark_mode == DTT_MARK_AT_END ? 0u : (uint32_t)(step / p.TPC));
-            if (chunk != writable) {
-                if (dtt_wait_writable(h, chunk, kWritablePolls) != 0) {
-                    write = false;
-                    if (dtt_dev::first_thread()) atomicOr(h.status, DTT_DEV_EWRITABLE);
-                }
-                writable = chunk;
-            }
-        }
-        if (pacing) {
-            // keep the bytes written but not yet delivered within `pace` chunks of this rank:
-            // the copier then reads them from L2.  The result does not depend on the outcome.
-            // A wait that runs out means the copier is not keeping up (or not running): this
-            // CTA stops pacing, so it stalls at most once per launch.
-            const uint64_t k = step / p.TPC;
-            if (k >= p.pace && k != paced) {
-                if (dtt_wait_reusable(h, h.first_chunk + (uint32_t)(k - p.pace), kPacePolls) != 0)
-                    pacing = false;
-                paced = k;
-            }
+        const uint32_t k = p.mark_mode == DTT_MARK_AT_END ? 0u : (uint32_t)step / p.TPC;   // T < 2^31
+        if (k != cur) {
+            cur = k;
+            if (waits & (kPacing | kWritable)) waits = chunk_waits(h, k, waits, p.pace);
         }
         uint32_t tm, tn;
         tile_of(p.order_kind, p.group_m, step, (uint32_t)tiles_m, (uint32_t)tiles_n, &tm, &tn);
@@ -249,9 +258,9 @@ __global__ void __launch_bounds__(1024) fill_kernel(const __grid_constant__ Fill
         const uint64_t rows = min((uint64_t)p.BM, p.M - r0), cols = min((uint64_t)p.BN, p.N - c0);
         const uint64_t per = (rows + team - 1) / team;
         const uint64_t ra = r0 + min(rows, member * per), rb = r0 + min(rows, (member + 1) * per);
-        if (write) write_block<DT>(p, base, salt, ra, rb, c0, cols);
+        if (!(waits & kNoWrite)) write_block<DT>(p, base, salt, ra, rb, c0, cols);
         if (p.mark_mode == DTT_MARK_PER_STEP) {
-            const uint32_t chunk = h.first_chunk + (uint32_t)(step / p.TPC);
+            const uint32_t chunk = h.first_chunk + k;
             if (p.group > 1)
                 group_mark(h, chunk, p.counters + (uint64_t)r * T + step, p.group);
             else
@@ -259,6 +268,22 @@ __global__ void __launch_bounds__(1024) fill_kernel(const __grid_constant__ Fill
         }
     }
     if (p.mark_mode == DTT_MARK_AT_END) mark(h, h.first_chunk, p.cluster);
+}
+
+// The fill with up to 64 registers a thread (its fastest inner loop; 1024-thread CTAs still fit
+// an SM).  The cap is stated: left to itself the compiler laid one instance out in 32 registers
+// with spills.
+template <int DT>
+__global__ void __maxnreg__(64) fill_kernel(const __grid_constant__ FillParams p) {
+    fill_body<DT>(p);
+}
+
+// The same fill in at most 56 registers a thread, for paced launches that need several
+// producer CTAs of an SM resident at once beside the copier's: eight 128-thread CTAs then leave
+// the registers of three copier CTAs free (with 64 registers they would take all of them).
+template <int DT>
+__global__ void __maxnreg__(56) fill_kernel_lean(const __grid_constant__ FillParams p) {
+    fill_body<DT>(p);
 }
 
 }  // namespace
@@ -275,8 +300,26 @@ cudaError_t preload_fill_kernels() {
     cudaError_t e = prepare_fill(fill_kernel<DTT_BF16>);
     if (e == cudaSuccess) e = prepare_fill(fill_kernel<DTT_F32>);
     if (e == cudaSuccess) e = prepare_fill(fill_kernel<DTT_U8>);
+    if (e == cudaSuccess) e = prepare_fill(fill_kernel_lean<DTT_BF16>);
+    if (e == cudaSuccess) e = prepare_fill(fill_kernel_lean<DTT_F32>);
+    if (e == cudaSuccess) e = prepare_fill(fill_kernel_lean<DTT_U8>);
     return e;
 }
+
+namespace {
+
+// The fill kernel for a dtype, lean (register-capped) or not.
+const void* fill_entry(uint32_t dtype, bool lean) {
+    if (lean)
+        return dtype == DTT_BF16 ? (const void*)fill_kernel_lean<DTT_BF16>
+             : dtype == DTT_F32  ? (const void*)fill_kernel_lean<DTT_F32>
+                                 : (const void*)fill_kernel_lean<DTT_U8>;
+    return dtype == DTT_BF16 ? (const void*)fill_kernel<DTT_BF16>
+         : dtype == DTT_F32  ? (const void*)fill_kernel<DTT_F32>
+                             : (const void*)fill_kernel<DTT_U8>;
+}
+
+}  // namespace
 
 }  // namespace dtt
 
@@ -301,6 +344,8 @@ extern "C" int dtt_fill_producer(void* const* bufs, uint32_t P, const dtt_fill_d
     if ((uint64_t)d->num_programs * cluster * group > 0x7FFFFFFFull)
         return fail(DTT_EINVAL, "dtt_fill_producer: grid too large");
     const uint32_t eb = d->dtype == DTT_BF16 ? 2 : d->dtype == DTT_F32 ? 4 : 1;
+    if (((d->M + d->BM - 1) / d->BM) * ((d->N + d->BN - 1) / d->BN) >= (1ull << 31))
+        return fail(DTT_EINVAL, "dtt_fill_producer: a rank's slice must have fewer than 2^31 tiles");
     if ((uint64_t)d->BM * d->BN >= (1ull << 31))
         return fail(DTT_EINVAL, "dtt_fill_producer: a BM x BN tile must hold fewer than 2^31 elements");
     if (d->M > 1 && d->pitch < d->N * eb) return fail(DTT_EINVAL, "dtt_fill_producer: pitch < row bytes");
@@ -336,6 +381,7 @@ extern "C" int dtt_fill_producer(void* const* bufs, uint32_t P, const dtt_fill_d
     p.group = group;
     p.counters = d->group_counters;
     p.pace = d->pace;
+    bool lean = false;     // the register-capped fill (paced launches with several CTAs per SM)
     if (p.pace) {
         // a paced program waits for chunks that other programs write: they must all be
         // resident at once, or the waits only run out (the copier's CTAs take room too, so this
@@ -344,9 +390,13 @@ extern "C" int dtt_fill_producer(void* const* bufs, uint32_t P, const dtt_fill_d
         // for cluster > 1 the count that matters is of clusters the device can hold at once.
         uint32_t producing = 0;
         for (uint32_t r = 0; r < P; ++r) producing += (d->rank_mask >> r) & 1u;
-        const void* k = d->dtype == DTT_BF16 ? (const void*)fill_kernel<DTT_BF16>
-                      : d->dtype == DTT_F32  ? (const void*)fill_kernel<DTT_F32>
-                                             : (const void*)fill_kernel<DTT_U8>;
+        // several CTAs of an SM must be resident at once beside the copier: the lean fill
+        int sms = 0, dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+            return fail(DTT_ECUDA, "dtt_fill_producer: cannot query the SM count");
+        lean = (uint64_t)d->num_programs * cluster * group * producing > (uint64_t)sms;
+        const void* k = fill_entry(d->dtype, lean);
         if (cluster > 1) {
             cudaLaunchConfig_t occ{};
             occ.gridDim = dim3(d->num_programs * cluster * group, P, 1);
@@ -366,10 +416,8 @@ extern "C" int dtt_fill_producer(void* const* bufs, uint32_t P, const dtt_fill_d
                 return fail(DTT_EINVAL, "dtt_fill_producer: a paced producer needs all its %llu clusters "
                                         "resident at once (at most %d here)", (unsigned long long)need, clusters);
         } else {
-            int per_sm = 0, sms = 0, dev = 0;
-            if (cudaGetDevice(&dev) != cudaSuccess ||
-                cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-                cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, (int)threads, 0) != cudaSuccess)
+            int per_sm = 0;
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, (int)threads, 0) != cudaSuccess)
                 return fail(DTT_ECUDA, "dtt_fill_producer: cannot query the producer's occupancy");
             const uint64_t ctas = (uint64_t)d->num_programs * group * producing;
             if (ctas > (uint64_t)per_sm * (uint64_t)sms)
@@ -390,12 +438,8 @@ extern "C" int dtt_fill_producer(void* const* bufs, uint32_t P, const dtt_fill_d
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = cluster > 1 ? 1 : 0;
-    cudaError_t e;
-    switch (d->dtype) {
-        case DTT_BF16: e = cudaLaunchKernelEx(&cfg, fill_kernel<DTT_BF16>, p); break;
-        case DTT_F32: e = cudaLaunchKernelEx(&cfg, fill_kernel<DTT_F32>, p); break;
-        default: e = cudaLaunchKernelEx(&cfg, fill_kernel<DTT_U8>, p); break;
-    }
+    void* args[] = {&p};
+    const cudaError_t e = cudaLaunchKernelExC(&cfg, fill_entry(d->dtype, lean), args);
     if (e != cudaSuccess) return fail(DTT_ECUDA, "dtt_fill_producer: launch failed: %s", cudaGetErrorString(e));
     return DTT_OK;
 }

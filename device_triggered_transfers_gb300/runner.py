@@ -154,17 +154,34 @@ def sm_count() -> int:
     return int(torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count)
 
 
-def bench_launch(w) -> dict:
+def l2_bytes() -> int:
+    """L2 size of the current CUDA device in bytes."""
+    props = torch.cuda.get_device_properties(torch.cuda.current_device())
+    return int(getattr(props, "L2_cache_size", 0) or (129 << 20))
+
+
+def bench_launch(w, overlap: Optional[bool] = None) -> dict:
     """The launch configuration the benchmark times for workload ``w`` (tests use it too).
 
+    overlap: rounds two at a time (opts.overlap: a round's producer runs while the previous
+    round's copier still copies).  None: where the benchmark uses them -- the chunked, whole()
+    and GEMM workloads; the tiled fill's paced rounds already run at the DRAM roofline, and a
+    round started early would only take its L2 away.
+
     Chunked workloads: the bulk-copy copier (six one-warp CTAs per SM, each with a ring of two
-    16 KiB stages, so the producer keeps the SM's threads and registers; c2 rounds ~0.5-1 us
-    shorter than three CTAs with 32 KiB stages), and one program per rank made of a group of
-    SMs / P CTAs (one per SM in all) that writes the rank's chunks in order and marks each once,
-    so every rank's chunk k opens in wave k and the copier follows the waves.
+    16 KiB stages, so the producer keeps the SM's threads and registers), and one program per
+    rank made of a group of SMs / P CTAs (one per SM in all) that writes the rank's chunks in
+    order and marks each once, so every rank's chunk k opens in wave k and the copier follows the
+    waves.  With overlapping rounds the producer is paced across rounds: it writes chunk k once
+    chunk k - pace is delivered, chunk k < pace once the previous round's chunk n - pace + k is,
+    with pace the number of chunk waves whose bytes fill about two thirds of L2, so the copier
+    reads what the producer wrote from L2 and its next round's first chunks are ready when it
+    starts (c2: ~106 -> ~92 us per round).  Rounds one at a time use the early copier instead:
+    each round's copier launched by the previous round's wait and claimed by start (it waits up
+    to 2 ms), so its launch leaves the round's critical path.
     whole(): the bulk-copy copier (two CTAs per SM, 2 x 56 KiB stages each) over the contiguous
-    slices; the single chunk per rank opens only when the whole slice is written, so the fill
-    gets as many CTAs as the writers allow.
+    slices, launched after the producer's launch; the single chunk per rank opens only when the
+    whole slice is written, so the fill gets as many CTAs as the writers allow.
     tile_chunks (fill producer): the bulk-copy copier moving each 32 KiB tile as one tensor-map
     box (three CTAs per SM, two stages each), and a producer paced two chunks ahead of the
     copier (each program waits for chunk k - 2 of its rank to be delivered before it writes
@@ -172,20 +189,25 @@ def bench_launch(w) -> dict:
     CTA resident at once (128-thread CTAs).  The GEMM producer keeps the vector copier: its own
     shared-memory ring leaves no room for a bulk-copy ring on the same SM."""
     sms = sm_count()
-    # Chunked and tiled workloads: each round's copier is launched early, by the previous
-    # round's wait, and claimed by start (it waits up to 2 ms for that), so the copier's launch
-    # leaves the round's critical path (c2: ~114 -> ~112 us per round).  whole() rounds are
-    # bound by the host's launches, where the early launch only moves one: they launch at start.
-    early = 2000
+    if overlap is None:
+        overlap = w.kind != "tile_chunks" or w.K > 0
+    ov = 1 if overlap else 0
+    early = 0 if overlap else 2000
     if w.kind == "chunks":     # six bulk-copy CTAs per SM: one thread alone cannot keep HBM busy
-        return {"group": max(1, sms // len(w.senders())), "programs": 1, "threads": 256,
-                "opts": dtt_plan_opts_default(method=1, piece_bytes=16384, stages=2, ctas_per_sm=6,
-                                              early_copier_us=early)}
+        launch = {"group": max(1, sms // len(w.senders())), "programs": 1, "threads": 256,
+                  "opts": dtt_plan_opts_default(method=1, piece_bytes=16384, stages=2, ctas_per_sm=6,
+                                                early_copier_us=early, overlap=ov)}
+        if overlap:
+            rows = -(-w.M // w.num_chunks)
+            n = -(-w.M // rows)
+            wave = len(w.senders()) * rows * w.row_bytes
+            launch["pace"] = max(1, min(n, int(0.65 * l2_bytes() / wave)))
+        return launch
     if w.kind == "whole":
         # the copier is launched after the producer's launch (it has nothing to do before the
         # whole slice is written)
         opts = dtt_plan_opts_default(method=1, piece_bytes=57344, stages=2, ctas_per_sm=2,
-                                     deferred_copier=2)
+                                     deferred_copier=2, overlap=ov)
         NP = w.num_programs
         if -(-w.M // -(-w.M // NP)) == NP:
             # one step per program: each writer becomes a group of CTAs (up to 8, enough to
@@ -196,9 +218,10 @@ def bench_launch(w) -> dict:
     if w.K == 0:       # the tiled fill in 128-thread CTAs: all of them resident at once
         return {"threads": 128, "pace": 2,
                 "opts": dtt_plan_opts_default(method=1, piece_bytes=32768, stages=2, ctas_per_sm=3,
-                                              early_copier_us=early)}
+                                              early_copier_us=early, overlap=ov)}
     # the GEMM producer: two 256-thread vector copier CTAs per SM beside the GEMM's CTA
-    return {"opts": dtt_plan_opts_default(copier_threads=256, ctas_per_sm=2, early_copier_us=early)}
+    return {"opts": dtt_plan_opts_default(copier_threads=256, ctas_per_sm=2, early_copier_us=early,
+                                          overlap=ov)}
 
 
 @dataclass

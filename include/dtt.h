@@ -562,9 +562,13 @@ typedef struct dtt_fill_desc {
                                 CTA stalls at most once (~1 ms) per launch when the copier lags.
                                 Timing only: the data and marks are the same, and the wait is
                                 on a chunk earlier in schedule order whose writers have all
-                                marked it, so it cannot hold up any mark.  Needs the copier
-                                running beside the producer (deferred_copier 0 or 2) and every
-                                producer CTA resident at once (checked: DTT_EINVAL otherwise). */
+                                marked it, so it cannot hold up any mark.  With overlapping
+                                rounds (the handles' DTT_HANDLE_OVERLAP), chunk k < pace waits in
+                                the same way for the previous round's delivery of chunk n - pace + k
+                                (n: the rank's chunks), whose copier runs just before this round's.
+                                Needs the copier running beside the producer (deferred_copier 0 or
+                                2) and every producer CTA resident at once (checked: DTT_EINVAL
+                                otherwise). */
     uint32_t* group_counters;/* group > 1: device uint32[P * steps per rank], zero before the
                                 first round (the producer leaves them zero after each round) */
 } dtt_fill_desc;

@@ -106,7 +106,7 @@ def test_consumer_gemm_full_size_bench_launch():
     w = W.C2
     K, N2 = w.N, 4096
     rows = w.buf_bytes // (2 * K)
-    launch = {k: v for k, v in runner.bench_launch(w).items() if k != "opts"}
+    launch = {k: v for k, v in runner.bench_launch(w, overlap=False).items() if k != "opts"}
     st = runner.make(w, opts=D.dtt_plan_opts_default(copier_threads=256), **launch)
     Wt = _weights(N2, K, 5)
     Wt_dev = Wt.cuda()

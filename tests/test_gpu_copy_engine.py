@@ -76,7 +76,7 @@ def test_copy_engine_c2_full_size():
     # the benchmark's c2 producer (chunks opening wave by wave) with the copy engines moving them:
     # every byte of every buffer against the oracle's closed form, and the gates
     w = W.C2
-    launch = {k: v for k, v in runner.bench_launch(w).items() if k != "opts"}
+    launch = {k: v for k, v in runner.bench_launch(w, overlap=False).items() if k != "opts"}
     st = runner.make(w, opts=_ce(), **launch)
     o = oracle_plan(w, copy_data=False)
     try:

@@ -177,7 +177,7 @@ def test_early_copier_c2_full_size_bench_launch():
     # stays well inside the early copier's wait.
     from oracle import cfill
     w = W.C2
-    launch = dict(runner.bench_launch(w))
+    launch = dict(runner.bench_launch(w, overlap=False))     # rounds one at a time
     launch["opts"].early_copier_us = 1000000
     want = [cfill.expected_buffer(w, R) for R in range(1, w.rounds + 1)]
     # load the comparison's kernels now: with lazy module loading a kernel's first launch waits
