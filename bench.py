@@ -35,14 +35,16 @@ DEFAULT_CONFIG = W.C2.name
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of the named kernel from one ncu capture
 # of the same workload and launch configuration (the summaries under profiles/); absent until
 # taken, and dropped once the kernel changes.
-NCU_TRAFFIC = {("c2_chunks_p4", "copier_bulk_kernel"): 474281216,
+NCU_TRAFFIC = {("c2_chunks_p4", "copier_bulk_kernel"): 474470912,
                # captured with 2000 rows per rank (--rows 2000) and scaled by the rows, 4x
                ("c3_tiles_p8", "copier_bulk_kernel"): 8009827328,
-               ("c5_gemm_p4", "gemm2_producer_kernel"): 185820032,
-               ("c5_gemm_p4", "copier_kernel"): 204823424}
+               ("c5_gemm_p4", "gemm2_producer_kernel"): 184814208,
+               ("c5_gemm_p4", "copier_kernel"): 206425216}
 # DRAM bytes (read, write) of one whole round, producer, copier and check together, from an
-# ncu range-replay capture of three rounds of the benchmark's launch (--profile-rounds 3)
-ROUND_TRAFFIC = {"c2_chunks_p4": (2427136, 515952469), "c3_tiles_p8": (16352085, 8237216427)}
+# ncu range-replay capture of three rounds of the benchmark's launch (--profile-rounds 3;
+# c2 and c5 with overlapping rounds)
+ROUND_TRAFFIC = {"c2_chunks_p4": (799317, 515392085), "c3_tiles_p8": (16352085, 8237216427),
+                 "c5_gemm_p4": (272514048, 252129451)}
 
 
 def describe(w, launch, copier=None) -> str:
@@ -379,10 +381,11 @@ def measure_workload(w, args, K, warmup, latency_rounds, isolated_rounds, with_e
             D.dtt_fill_producer(st.buf_ptrs, desc_unpaced if deferred else st.desc, h, prod)
     prod = st.producer_stream
 
-    def make_step(plan, deferred, overlapped=False):
+    def make_step(plan, deferred, overlapped=False, after_producer=False):
         """One round.  ev: two events around the producer launch (producer stream), or None.
         deferred: the plan's copier starts only after the producer.  overlapped: the round is
-        left pending (its wait comes in the next step, or in drain)."""
+        left pending (its wait comes in the next step, or in drain).  after_producer: the
+        plan's copier is launched right after the producer's launch (deferred_copier = 2)."""
         def step(ev=None):
             h = plan.start(prod)
             if ev is not None:
@@ -390,6 +393,8 @@ def measure_workload(w, args, K, warmup, latency_rounds, isolated_rounds, with_e
             produce(h, deferred)
             if ev is not None:
                 ev[1].record(prod)
+            if after_producer:
+                plan.launch_copier()
             if overlapped:
                 if plan.pending:
                     plan.wait()
@@ -425,7 +430,7 @@ def measure_workload(w, args, K, warmup, latency_rounds, isolated_rounds, with_e
         prod_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs) if producer_events else None
         return e0.elapsed_time(e1) / 1e3, cop, prod_ms
 
-    step = make_step(st.plan, opts.deferred_copier == 1, overlap)
+    step = make_step(st.plan, opts.deferred_copier == 1, overlap, opts.deferred_copier == 2)
     for _ in range(warmup):
         step()
     drain(st.plan)
@@ -479,7 +484,7 @@ def measure_workload(w, args, K, warmup, latency_rounds, isolated_rounds, with_e
         out.update(timing_pass_s=elapsed, copier_ms=elapsed / K * 1e3, producer_ms=None)
     else:
         plan3 = side_plan(time_copier=1, deferred_copier=opts.deferred_copier, overlap=opts.overlap)
-        step3 = make_step(plan3, opts.deferred_copier == 1, overlap)
+        step3 = make_step(plan3, opts.deferred_copier == 1, overlap, opts.deferred_copier == 2)
         for _ in range(3):
             step3()
         drain(plan3)

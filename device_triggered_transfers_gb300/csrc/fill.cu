@@ -339,6 +339,12 @@ extern "C" int dtt_fill_producer(void* const* bufs, uint32_t P, const dtt_fill_d
     const uint32_t threads = d->threads ? d->threads : 256;
     if (cluster > 16 || threads % 32 || threads > 1024)
         return fail(DTT_EINVAL, "dtt_fill_producer: cluster <= 16, threads a multiple of 32 <= 1024");
+    if ((handles[0].flags & DTT_HANDLE_OVERLAP) && threads > 512)
+        // with overlapping rounds the next round's copier is queued behind this round's and may
+        // take an SM before this producer's CTAs do: each CTA must fit beside the copier's CTAs
+        // (which keep to half an SM), so at most 512 threads of up to 64 registers
+        return fail(DTT_EINVAL, "dtt_fill_producer: with overlapping rounds a producer CTA has at most 512 threads "
+                                "(it must fit on an SM beside the copier's CTAs)");
     if (group > 1 && (cluster > 1 || d->mark_mode != DTT_MARK_PER_STEP || !d->group_counters))
         return fail(DTT_EINVAL, "dtt_fill_producer: group writers need cluster 1, per-step marks and counters");
     if ((uint64_t)d->num_programs * cluster * group > 0x7FFFFFFFull)

@@ -164,9 +164,12 @@ def bench_launch(w, overlap: Optional[bool] = None) -> dict:
     """The launch configuration the benchmark times for workload ``w`` (tests use it too).
 
     overlap: rounds two at a time (opts.overlap: a round's producer runs while the previous
-    round's copier still copies).  None: where the benchmark uses them -- the chunked, whole()
-    and GEMM workloads; the tiled fill's paced rounds already run at the DRAM roofline, and a
-    round started early would only take its L2 away.
+    round's copier still copies).  None: where the benchmark uses them -- the chunked and GEMM
+    workloads, and whole() with one step per program (c1, c4a).  The tiled fill's paced rounds
+    already run at the DRAM roofline, and a round started early would only take its L2 away; a
+    whole() slice written by many steps per program (the c4b broadcast) is one chunk, so its
+    rounds have little to overlap, and its fill is fastest in 1024-thread CTAs, which cannot sit
+    beside the copier's (overlapping rounds need that).
 
     Chunked workloads: the bulk-copy copier (six one-warp CTAs per SM, each with a ring of two
     16 KiB stages, so the producer keeps the SM's threads and registers), and one program per
@@ -190,7 +193,10 @@ def bench_launch(w, overlap: Optional[bool] = None) -> dict:
     shared-memory ring leaves no room for a bulk-copy ring on the same SM."""
     sms = sm_count()
     if overlap is None:
-        overlap = w.kind != "tile_chunks" or w.K > 0
+        if w.kind == "whole":
+            overlap = -(-w.M // -(-w.M // w.num_programs)) == w.num_programs
+        else:
+            overlap = w.kind == "chunks" or w.K > 0
     ov = 1 if overlap else 0
     early = 0 if overlap else 2000
     if w.kind == "chunks":     # six bulk-copy CTAs per SM: one thread alone cannot keep HBM busy
@@ -214,7 +220,8 @@ def bench_launch(w, overlap: Optional[bool] = None) -> dict:
             # cover the SMs) that marks the chunk once
             g = max(1, min(8, sms // (len(w.senders()) * NP)))
             return {"group": g, "threads": 512, "opts": opts}
-        return {"threads": 1024, "opts": opts}
+        # overlapping rounds: a producer CTA must fit on an SM beside the copier's
+        return {"threads": 512 if overlap else 1024, "opts": opts}
     if w.K == 0:       # the tiled fill in 128-thread CTAs: all of them resident at once
         return {"threads": 128, "pace": 2,
                 "opts": dtt_plan_opts_default(method=1, piece_bytes=32768, stages=2, ctas_per_sm=3,

@@ -269,7 +269,11 @@ typedef struct dtt_plan_opts {
                                 round's copier) or chunk groups (a member's next-round arrival
                                 would count toward this round's group wait); the early copier is
                                 not used (the next round's copier is queued at its start, behind the
-                                pending one).  0 = rounds one at a time */
+                                pending one).  The next round's copier may take an SM's room before
+                                the next round's producer does, so producer CTAs must fit on an SM
+                                beside the copier's (which keep to half its threads and registers):
+                                the library's fill takes at most 512 threads per CTA on such plans.
+                                0 = rounds one at a time */
 } dtt_plan_opts;
 
 void dtt_plan_opts_default(dtt_plan_opts* opts);
@@ -549,7 +553,7 @@ typedef struct dtt_fill_desc {
     uint32_t mark_mode;
     uint32_t cluster;        /* 1..16 CTAs per program (above 8 needs non-portable clusters) */
     uint32_t rank_mask;
-    uint32_t threads;        /* threads per CTA; 0 = 256 */
+    uint32_t threads;        /* threads per CTA; 0 = 256; at most 512 with overlapping rounds */
     uint32_t group;          /* > 1: a program is `group` CTAs that split each step's rows; the
                                 last of them to finish a step issues its one mark (per-step
                                 marks only, cluster must be 1) */

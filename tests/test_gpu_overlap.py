@@ -475,3 +475,20 @@ def test_overlapped_round_limit():
         np.testing.assert_array_equal(st.plan.read_gates()[:, :, :5], o.gates)
     finally:
         st.plan.close()
+
+
+def test_overlap_refuses_producer_ctas_larger_than_half_an_sm():
+    # the next round's copier may take an SM before the next round's producer: a fill CTA of
+    # 1024 threads could then never start beside it, so such a launch is refused up front
+    w = W.small(W.C2, P=2, M=64, N=256, num_chunks=2, rounds=1)
+    st = runner.make(w, opts=_opts(), threads=1024)
+    try:
+        h = st.plan.start(st.producer_stream)
+        with pytest.raises(D.DttError) as e:
+            D.dtt_fill_producer(st.buf_ptrs, st.desc, h, st.producer_stream)
+        assert e.value.code == D.EINVAL
+        st.desc.threads = 512
+        D.dtt_fill_producer(st.buf_ptrs, st.desc, h, st.producer_stream)
+        assert st.plan.wait().status == D.OK
+    finally:
+        st.plan.close()
