@@ -353,6 +353,10 @@ def measure_workload(w, args, K, warmup, latency_rounds, isolated_rounds, with_e
         opts.overlap = 0      # a round's producer would wait for a copier that runs after it
     if early_us is not None:
         opts.early_copier_us = early_us
+    for k in ("piece_bytes", "stages", "ctas_per_sm", "copier_threads"):   # launch overrides
+        v = getattr(args, k, 0)
+        if v:
+            setattr(opts, k, v)
     overlap = bool(opts.overlap)
     if pace is not None and w.K == 0:
         launch["pace"] = pace
@@ -992,6 +996,10 @@ def main(argv=None):
                          "where the benchmark's launch uses them)")
     ap.add_argument("--sequential", dest="overlap", action="store_const", const=False,
                     help="rounds one at a time for every workload")
+    ap.add_argument("--piece-bytes", type=int, default=0, help="copier piece size (default: the launch's)")
+    ap.add_argument("--stages", type=int, default=0, help="bulk copier stages per CTA (default: the launch's)")
+    ap.add_argument("--ctas-per-sm", type=int, default=0, help="copier CTAs per SM (default: the launch's)")
+    ap.add_argument("--copier-threads", type=int, default=0, help="vector copier threads per CTA")
     ap.add_argument("--pace", type=int, default=-1,
                     help="the fill producer's pacing in chunks (default: the launch's own)")
     ap.add_argument("--latency-rounds", type=int, default=20)

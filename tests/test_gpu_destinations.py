@@ -44,14 +44,14 @@ class Case:
     def region(self, b):
         return (b * self.rows * self.rb, self.rows * self.rb, 1, self.rows * self.rb)
 
-    def oracle(self):
+    def oracle(self, overlap=False):
         scheds = [OS.Schedule([OS.Chunk([self.region(b)], 1, dests=d, peers=(m or None))
                                for b, (d, m) in enumerate(self.spec[s])]) for s in range(self.P)]
         bufs = [np.zeros(self.buf_bytes, dtype=np.uint8) for _ in range(self.P)]
         dst = [np.zeros(self.dst_bytes, dtype=np.uint8) for _ in range(self.P)] if self.dst_bytes else None
-        return OP.Plan(bufs, scheds, allgather=False, dst_bufs=dst)
+        return OP.Plan(bufs, scheds, allgather=False, dst_bufs=dst, overlap=overlap)
 
-    def library(self, transport):
+    def library(self, transport, overlap=False):
         scheds = []
         for s in range(self.P):
             sc = D.dtt_schedule_empty()
@@ -61,7 +61,8 @@ class Case:
         bufs = [torch.zeros(self.buf_bytes, dtype=torch.uint8, device="cuda") for _ in range(self.P)]
         dst = [torch.zeros(self.dst_bytes, dtype=torch.uint8, device="cuda") for _ in range(self.P)] \
             if self.dst_bytes else None
-        plan = D.Plan(bufs, self.buf_bytes, scheds, _opts(transport), dst_bufs=dst, dst_bytes=self.dst_bytes)
+        plan = D.Plan(bufs, self.buf_bytes, scheds, _opts(transport, overlap=int(overlap)), dst_bufs=dst,
+                      dst_bytes=self.dst_bytes)
         for sc in scheds:
             sc.free()
         desc = D.fill_desc("bf16", self.seed, self.M, self.N, self.rb, self.buf_bytes, [0] * self.P,
@@ -102,6 +103,47 @@ class Case:
             plan.close()
 
 
+    def run_overlapped(self, transport, rounds=4):
+        """Rounds two at a time (opts.overlap) on the library and the oracle through the same
+        host calls; every buffer, destination buffer and gate word after the last round."""
+        plan, bufs, dst, desc = self.library(transport, overlap=True)
+        o = self.oracle(overlap=True)
+        prod = torch.cuda.Stream()
+        try:
+            for i in range(rounds):
+                R = i + 1
+                h = plan.start(prod)
+                D.dtt_fill_producer(bufs, desc, h, prod)
+                assert o.start() == R
+                for s in range(self.P):
+                    data = np.zeros(self.buf_bytes, dtype=np.uint8)
+                    data[:self.M * self.rb] = H.fill_slice_bytes("bf16", self.seed, s, R, self.M, self.N)
+                    for c in o.chunks_of(s):
+                        while not o.writable(s, c, R):
+                            assert o.copier_progress() > 0
+                        o.write_chunk(s, c, data, R)
+                        o.mark_ready(s, c, R)
+                if plan.pending:
+                    rep = plan.wait()
+                    assert rep.status == D.OK and rep.round == R - 1 and rep.copier_timeouts == 0
+                    o.copier_progress()
+                    assert o.wait()[0] == OP.OK
+                if i + 1 < rounds:
+                    plan.next_round()
+                    o.next_round()
+            rep = plan.wait()
+            assert rep.status == D.OK and rep.round == rounds
+            o.copier_progress()
+            assert o.wait()[0] == OP.OK
+            for q in range(self.P):
+                np.testing.assert_array_equal(bufs[q].cpu().numpy(), o.bufs[q], err_msg=f"{transport} buf {q}")
+                if dst:
+                    np.testing.assert_array_equal(dst[q].cpu().numpy(), o.dst[q], err_msg=f"{transport} dst {q}")
+            np.testing.assert_array_equal(plan.read_gates()[:, :, :5], o.gates)
+        finally:
+            plan.close()
+
+
 def _reduce_scatter(P=4, rows=64, N=256, separate=False):
     """Block b of every rank goes only to rank b, into rank b's staging slot of the sender (after
     the partials in place, or at the start of a separate destination buffer)."""
@@ -119,6 +161,14 @@ def _reduce_scatter(P=4, rows=64, N=256, separate=False):
 @pytest.mark.parametrize("separate", [False, True], ids=["in_place", "staging_buffers"])
 def test_reduce_scatter_into_staging_slots(transport, separate):
     _reduce_scatter(separate=separate).run(transport)
+
+
+@pytest.mark.parametrize("transport", sorted(TRANSPORTS))
+@pytest.mark.parametrize("separate", [False, True], ids=["in_place", "staging_buffers"])
+def test_reduce_scatter_overlapped_rounds(transport, separate):
+    # overlapping rounds: a round's partial blocks are written while the previous round's are
+    # still being sent to their owners' slots
+    _reduce_scatter(separate=separate).run_overlapped(transport)
 
 
 @pytest.mark.parametrize("transport", sorted(TRANSPORTS))

@@ -492,3 +492,59 @@ def test_overlap_refuses_producer_ctas_larger_than_half_an_sm():
         assert st.plan.wait().status == D.OK
     finally:
         st.plan.close()
+
+
+def test_consumers_on_overlapped_rounds():
+    # Each round's consumers -- the tcgen05 consumer GEMM and the gather, both waiting per chunk
+    # -- run on a stream of their own, launched before the round's producer; the next round's
+    # producer is ordered after them (whoever reads a round is done before the next round's
+    # producers run), while the round's copier and check still overlap the next round.  Every
+    # round's gathered bytes and product are checked against the oracle's closed form.
+    w = W.small(W.C2, M=512, N=1024, num_chunks=4, rounds=4)
+    K, N2, q = w.N, 256, 2
+    rows = w.buf_bytes // (2 * K)
+    g = torch.Generator().manual_seed(91)
+    Wt = (torch.randn(N2, K, generator=g) / K ** 0.5).to(torch.bfloat16)
+    Wt_dev = Wt.cuda()
+    Wt64 = Wt.to(torch.float64).numpy()
+    st = runner.make(w, opts=_opts())
+    n_global = st.plan.info()[0]
+    cons = torch.cuda.Stream()
+    outs = [torch.zeros(rows, N2, dtype=torch.bfloat16, device="cuda") for _ in range(w.rounds)]
+    gath = [torch.zeros(w.buf_bytes, dtype=torch.uint8, device="cuda") for _ in range(w.rounds)]
+    status = [torch.full((n_global,), 99, dtype=torch.int32, device="cuda") for _ in range(w.rounds)]
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    torch.cuda.synchronize()
+    readers_done = None
+    try:
+        for i in range(w.rounds):
+            h = st.plan.start(st.producer_stream)
+            st.plan.gemm_consumer(q, Wt_dev, outs[i], N2, K, err, stream=cons)
+            st.plan.consumer_gather(q, gath[i], 1 << 24, status[i], 8, cons)
+            if readers_done is not None:
+                st.producer_stream.wait_event(readers_done)
+            D.dtt_fill_producer(st.buf_ptrs, st.desc, h, st.producer_stream)
+            readers_done = torch.cuda.Event()
+            readers_done.record(cons)
+            if st.plan.pending:
+                rep = st.plan.wait()
+                assert rep.status == D.OK and rep.round == i
+            if i + 1 < w.rounds:
+                st.plan.next_round()
+        rep = st.plan.wait()
+        assert rep.status == D.OK and rep.round == w.rounds
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        S = w.slice_bytes
+        for i in range(w.rounds):
+            want = OP.expected_allgather(w.P, w.M, w.N, w.dtype, w.seed, i + 1, w.elem_bytes)
+            assert status[i].cpu().tolist() == [0] * n_global, i
+            got = gath[i].cpu().numpy()
+            for r in range(w.P):
+                sl = slice(r * S, (r + 1) * S)
+                np.testing.assert_array_equal(got[sl], want[sl] if r != q else 0, err_msg=f"round {i + 1} slice {r}")
+            X = torch.from_numpy(want.copy()).view(torch.bfloat16).view(rows, K)
+            e = OG.rel_frobenius(outs[i].cpu().to(torch.float64).numpy(), OG.product(X.to(torch.float64).numpy(), Wt64))
+            assert e <= 1e-2, (i + 1, e)
+    finally:
+        st.plan.close()
