@@ -65,6 +65,8 @@ def describe(w, launch, copier=None) -> str:
     if launch.get("pace"):
         prod += (f"; producer paced: a program writes chunk k once chunk k-{launch['pace']} of its "
                  f"rank is delivered")
+        if copier is not None and copier.get("overlap"):
+            prod += " (the previous round's chunk n-%d+k for k < %d)" % (launch["pace"], launch["pace"])
     cop = ""
     if copier is not None:
         cop = ("; copier: bulk copies, %d CTA(s) per SM with %d x %d KiB stages each"
@@ -362,7 +364,8 @@ def measure_workload(w, args, K, warmup, latency_rounds, isolated_rounds, with_e
         launch["pace"] = pace
     opts.time_copier = 0
     copier_method = {"method": opts.method, "piece_bytes": opts.piece_bytes, "stages": opts.stages,
-                     "copier_threads": opts.copier_threads, "ctas_per_sm": opts.ctas_per_sm}
+                     "copier_threads": opts.copier_threads, "ctas_per_sm": opts.ctas_per_sm,
+                     "overlap": opts.overlap}
     gemm = w.K > 0
     if gemm:           # the GEMM producer: C_r = A_r . B, marking each tile's chunk
         A, Bt = W.gemm_inputs(w.P, w.M, w.N, w.K, w.seed)
@@ -547,7 +550,7 @@ def measure_workload(w, args, K, warmup, latency_rounds, isolated_rounds, with_e
     # the same copier and producer one after the other (deferred plan): each kernel alone
     out["isolated"] = None
     if not args.deferred and isolated_rounds and opts.method != D.COPY_ENGINE:
-        plan2 = side_plan(time_copier=1, deferred_copier=1)
+        plan2 = side_plan(time_copier=1, deferred_copier=1, overlap=0)
         step2 = make_step(plan2, True)
         for _ in range(3):
             step2()

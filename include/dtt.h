@@ -251,8 +251,8 @@ typedef struct dtt_plan_opts {
                                 first launch of a kernel not yet loaded (lazy module loading
                                 waits for the device to idle).  Ignored (the
                                 copier is launched at start) with time_copier, deferred_copier
-                                = 1, a copy stream another live plan uses, or a device without
-                                host-native atomics.  At most 1000000; 0 = off */
+                                = 1, overlap, a copy stream another live plan uses, or a device
+                                without host-native atomics.  At most 1000000; 0 = off */
     uint32_t overlap;         /* 1: overlapping rounds ("Triggered Plans", Not supported yet:
                                 "Overlapping rounds" -- wait() had to return before next_round()
                                 could prepare the next round).  dtt_plan_next_round may then also
