@@ -355,7 +355,9 @@ def measure_workload(w, args, K, warmup, latency_rounds, isolated_rounds, with_e
         opts.overlap = 0      # a round's producer would wait for a copier that runs after it
     if early_us is not None:
         opts.early_copier_us = early_us
-    for k in ("piece_bytes", "stages", "ctas_per_sm", "copier_threads"):   # launch overrides
+    if getattr(args, "copier", None):            # launch overrides
+        opts.method = {"vector": D.COPY_VEC16, "bulk": D.COPY_TMA}[args.copier]
+    for k in ("piece_bytes", "stages", "ctas_per_sm", "copier_threads"):
         v = getattr(args, k, 0)
         if v:
             setattr(opts, k, v)
@@ -999,6 +1001,8 @@ def main(argv=None):
                          "where the benchmark's launch uses them)")
     ap.add_argument("--sequential", dest="overlap", action="store_const", const=False,
                     help="rounds one at a time for every workload")
+    ap.add_argument("--copier", choices=["vector", "bulk"], default=None,
+                    help="copier data path (default: the launch's)")
     ap.add_argument("--piece-bytes", type=int, default=0, help="copier piece size (default: the launch's)")
     ap.add_argument("--stages", type=int, default=0, help="bulk copier stages per CTA (default: the launch's)")
     ap.add_argument("--ctas-per-sm", type=int, default=0, help="copier CTAs per SM (default: the launch's)")

@@ -184,7 +184,8 @@ def bench_launch(w, overlap: Optional[bool] = None) -> dict:
     to 2 ms), so its launch leaves the round's critical path.
     whole(): the bulk-copy copier (two CTAs per SM, 2 x 56 KiB stages each) over the contiguous
     slices, launched after the producer's launch; the single chunk per rank opens only when the
-    whole slice is written, so the fill gets as many CTAs as the writers allow.
+    whole slice is written, so the fill gets as many CTAs as the writers allow.  A round of at
+    most 2 MiB (c1) is latency-bound and gets the vector copier in 4 KiB pieces instead.
     tile_chunks (fill producer): the bulk-copy copier moving each 32 KiB tile as one tensor-map
     box (three CTAs per SM, two stages each), and a producer paced two chunks ahead of the
     copier (each program waits for chunk k - 2 of its rank to be delivered before it writes
@@ -212,8 +213,14 @@ def bench_launch(w, overlap: Optional[bool] = None) -> dict:
     if w.kind == "whole":
         # the copier is launched after the producer's launch (it has nothing to do before the
         # whole slice is written)
-        opts = dtt_plan_opts_default(method=1, piece_bytes=57344, stages=2, ctas_per_sm=2,
-                                     deferred_copier=2, overlap=ov)
+        if len(w.senders()) * w.slice_bytes <= (2 << 20):
+            # a round of at most 2 MiB is latency-bound: the vector copier in 4 KiB pieces spreads
+            # each chunk over many CTAs (c1 gate-to-arrival 4.6 -> 3.4 us median)
+            opts = dtt_plan_opts_default(method=0, piece_bytes=4096, copier_threads=256, ctas_per_sm=1,
+                                         deferred_copier=2, overlap=ov)
+        else:
+            opts = dtt_plan_opts_default(method=1, piece_bytes=57344, stages=2, ctas_per_sm=2,
+                                         deferred_copier=2, overlap=ov)
         NP = w.num_programs
         if -(-w.M // -(-w.M // NP)) == NP:
             # one step per program: each writer becomes a group of CTAs (up to 8, enough to
