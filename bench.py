@@ -357,7 +357,7 @@ def measure_workload(w, args, K, warmup, latency_rounds, isolated_rounds, with_e
         opts.early_copier_us = early_us
     if getattr(args, "copier", None):            # launch overrides
         opts.method = {"vector": D.COPY_VEC16, "bulk": D.COPY_TMA}[args.copier]
-    for k in ("piece_bytes", "stages", "ctas_per_sm", "copier_threads"):
+    for k in ("piece_bytes", "stages", "ctas_per_sm", "copier_threads", "copier_ctas"):
         v = getattr(args, k, 0)
         if v:
             setattr(opts, k, v)
@@ -367,7 +367,7 @@ def measure_workload(w, args, K, warmup, latency_rounds, isolated_rounds, with_e
     opts.time_copier = 0
     copier_method = {"method": opts.method, "piece_bytes": opts.piece_bytes, "stages": opts.stages,
                      "copier_threads": opts.copier_threads, "ctas_per_sm": opts.ctas_per_sm,
-                     "overlap": opts.overlap}
+                     "copier_ctas": opts.copier_ctas, "overlap": opts.overlap}
     gemm = w.K > 0
     if gemm:           # the GEMM producer: C_r = A_r . B, marking each tile's chunk
         A, Bt = W.gemm_inputs(w.P, w.M, w.N, w.K, w.seed)
@@ -1007,6 +1007,7 @@ def main(argv=None):
     ap.add_argument("--stages", type=int, default=0, help="bulk copier stages per CTA (default: the launch's)")
     ap.add_argument("--ctas-per-sm", type=int, default=0, help="copier CTAs per SM (default: the launch's)")
     ap.add_argument("--copier-threads", type=int, default=0, help="vector copier threads per CTA")
+    ap.add_argument("--copier-ctas", type=int, default=0, help="copier CTAs in all (default: per SM)")
     ap.add_argument("--pace", type=int, default=-1,
                     help="the fill producer's pacing in chunks (default: the launch's own)")
     ap.add_argument("--latency-rounds", type=int, default=20)
