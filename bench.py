@@ -111,6 +111,16 @@ def load_tensor_peak():
         return 1900.0, "fallback"
 
 
+def load_tensor_peak_sustained():
+    """Dense bf16 tensor peak under the power cap (a seconds-long matmul loop), or None."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["bf16_tflops_sustained"])
+    except Exception:
+        return None
+
+
 # ---- clocks ------------------------------------------------------------------------------------
 class ClockSampler:
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -586,9 +596,11 @@ def summarize(m, K, t_max, units, peak, peak_kind):
         NP = m["num_programs"] or w.num_programs
         gname = "gemm2_producer_kernel" if (w.M % 256 == 0 and w.N % 256 == 0 and NP >= 2) \
             else "gemm_producer_kernel"
+        sustained = load_tensor_peak_sustained()
         roofline = {"kernel": gname, "bound": "tensor",
                     "achieved": flops / prod_s / 1e12, "peak": tf_peak, "peak_kind": tf_kind,
                     "unit": "TFLOP/s", "frac": flops / prod_s / 1e12 / tf_peak,
+                    "frac_of_sustained": (flops / prod_s / 1e12 / sustained) if sustained else None,
                     "traffic": NCU_TRAFFIC.get((w.name, gname)),
                     "flops_per_launch": flops}
     else:
