@@ -548,3 +548,29 @@ def test_consumers_on_overlapped_rounds():
             assert e <= 1e-2, (i + 1, e)
     finally:
         st.plan.close()
+
+
+def test_many_overlapped_rounds_keep_the_gates_and_data_right():
+    # 500 rounds of the benchmark's c2 launch two at a time: every wait reports its own round,
+    # the gates follow the closed form of the round count, and the data is the last round's
+    # everywhere (every byte)
+    w = W.C2
+    R = 500
+    st = runner.make(w, **_launch(w, "bench", {}))
+    try:
+        reps = runner.run_overlapped(st, R)
+        assert [r.round for r in reps] == list(range(1, R + 1))
+        assert all(r.status == D.OK and r.copier_timeouts == 0 for r in reps)
+        g = st.plan.read_gates()
+        n_global, first, n_chunks, _ = st.plan.info()
+        for s in range(w.P):
+            for c in range(first[s], first[s] + n_chunks[s]):
+                assert int(g[s, c, D.GATE_READY]) == R and int(g[s, c, D.GATE_COUNTER]) == R
+                assert int(g[s, c, D.GATE_COMPLETION]) == R * (w.P - 1)
+                assert int(g[s, c, D.GATE_ERROR]) == 0
+                for q in range(w.P):
+                    if q != s:
+                        assert int(g[q, c, D.GATE_ARRIVAL]) == R
+        assert_buffers_equal(st.bufs, expected_on_device(w, R), f"{w.name} round {R}")
+    finally:
+        st.plan.close()

@@ -44,6 +44,8 @@ def _build():
                                        C.c_void_p]
     lib.user_group_probe_launch.argtypes = [C.POINTER(D.dtt_handle), C.c_uint32, C.c_uint32, C.c_void_p,
                                             C.c_void_p]
+    lib.user_probe_writable_launch.argtypes = [C.POINTER(D.dtt_handle), C.c_uint32, C.c_uint32, C.c_uint64,
+                                               C.c_void_p, C.c_void_p, C.c_void_p]
     return lib
 
 
@@ -301,5 +303,54 @@ def test_group_waits_in_a_users_consumer_kernel():
         rep = plan.wait(raise_on_error=False)
         assert rep.status == D.EINVAL and rep.device_status & 2
         assert int(probe[0].item()) == 0
+    finally:
+        plan.close()
+
+
+def test_writable_with_overlapping_rounds():
+    # Overlapping rounds (opts.overlap): round 1 marks every chunk but rank 0's second one, so
+    # its copier delivers rank 0's first chunk and gives that one up.  With round 2 started
+    # behind it, rank 0's first chunk is writable (its round-1 copies landed) and the second is
+    # not: a bounded dtt_wait_writable on it returns DTT_ETIMEDOUT.  Round 1's check names the
+    # unmarked chunk, as the oracle's overlapped plan does.
+    from oracle import plan as OP
+    from oracle import schedule as OS
+    lib = _build()
+    assert lib.user_kernels_prepare() == 0
+    P, n, chunk = 2, 2, 1 << 16
+    S = n * chunk
+    bufs = [torch.zeros(P * S, dtype=torch.uint8, device="cuda") for _ in range(P)]
+    scheds = [D.dtt_schedule_chunks(r * S, n, chunk, chunk, n) for r in range(P)]
+    plan = D.Plan(bufs, P * S, scheds, D.dtt_plan_opts_default(overlap=1, max_polls=1 << 12))
+    for s in scheds:
+        s.free()
+    o = OP.Plan([np.zeros(1, dtype=np.uint8) for _ in range(P)],
+                [OS.chunks(r * S, n, chunk, chunk, n) for r in range(P)], validate=False, copy_data=False,
+                overlap=True)
+    prod = torch.cuda.Stream()
+    now = torch.full((n,), 7, dtype=torch.int32, device="cuda")
+    waited = torch.full((n,), 7, dtype=torch.int32, device="cuda")
+    torch.cuda.synchronize()
+    try:
+        h = plan.start(prod)
+        o.start()
+        for c in (0, 2, 3):                   # chunk 1 (rank 0's second) is never marked
+            D.dtt_publish(h, c, 1, 0, prod)
+            o.mark_ready(o.owner[c], c)
+        plan.next_round()
+        o.next_round()
+        h = plan.start(prod)
+        o.start()
+        o.copier_progress()
+        torch.cuda.synchronize()              # round 1's copier has delivered or given up
+        assert lib.user_probe_writable_launch(C.byref(h[0]), h[0].first_chunk, n, 4096,
+                                              C.c_void_p(now.data_ptr()), C.c_void_p(waited.data_ptr()),
+                                              C.c_void_p(prod.cuda_stream)) == 0
+        prod.synchronize()
+        assert now.cpu().tolist() == [int(o.writable(0, 0, 2)), int(o.writable(0, 1, 2))] == [1, 0]
+        assert waited.cpu().tolist() == [0, D.ETIMEDOUT]
+        assert o.wait() == (OP.TIMEOUT, [1], [])
+        rep = plan.wait(raise_on_error=False)
+        assert rep.status == D.ETIMEDOUT and rep.round == 1 and rep.shorts == [1]
     finally:
         plan.close()

@@ -108,6 +108,18 @@ __global__ void user_probe_reusable(dtt_handle h, uint32_t first, int32_t* out) 
     if (threadIdx.x == 0) out[blockIdx.x] = r ? 1 : 0;
 }
 
+// Overlapping rounds: CTA i records dtt_writable of global chunk first + i, then waits for it
+// (dtt_wait_writable, at most max_polls polls) and records the wait's result.
+__global__ void user_probe_writable(dtt_handle h, uint32_t first, uint64_t max_polls, int32_t* now,
+                                    int32_t* waited) {
+    const bool w = dtt_writable(h, first + blockIdx.x);
+    const int r = dtt_wait_writable(h, first + blockIdx.x, max_polls);
+    if (threadIdx.x == 0) {
+        now[blockIdx.x] = w ? 1 : 0;
+        waited[blockIdx.x] = r;
+    }
+}
+
 }  // namespace
 
 // What the documented contract asks of a user's kernels before the first round: loaded now,
@@ -133,6 +145,7 @@ extern "C" int user_kernels_prepare(void) {
     if (cudaFuncGetAttributes(&a, user_group_probe) != cudaSuccess) return 1;
     if (cudaFuncGetAttributes(&a, user_producer_paced) != cudaSuccess) return 1;
     if (cudaFuncGetAttributes(&a, user_probe_reusable) != cudaSuccess) return 1;
+    if (cudaFuncGetAttributes(&a, user_probe_writable) != cudaSuccess) return 1;
     if (cudaFuncSetAttribute(user_producer_paced, cudaFuncAttributePreferredSharedMemoryCarveout,
                              cudaSharedmemCarveoutMaxShared) != cudaSuccess)
         return 1;
@@ -185,5 +198,12 @@ extern "C" int user_group_probe_launch(const dtt_handle* h, uint32_t first, uint
                                        cudaStream_t s) {
     if (n == 0) return 0;
     user_group_probe<<<n, 64, 0, s>>>(*h, first, out);
+    return cudaGetLastError() == cudaSuccess ? 0 : 1;
+}
+
+extern "C" int user_probe_writable_launch(const dtt_handle* h, uint32_t first, uint32_t n, uint64_t max_polls,
+                                          int32_t* now, int32_t* waited, cudaStream_t s) {
+    if (n == 0) return 0;
+    user_probe_writable<<<n, 64, 0, s>>>(*h, first, max_polls, now, waited);
     return cudaGetLastError() == cudaSuccess ? 0 : 1;
 }
