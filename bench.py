@@ -35,11 +35,11 @@ DEFAULT_CONFIG = W.C2.name
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of the named kernel from one ncu capture
 # of the same workload and launch configuration (the summaries under profiles/); absent until
 # taken, and dropped once the kernel changes.
-NCU_TRAFFIC = {("c2_chunks_p4", "copier_bulk_kernel"): 474470912,
+NCU_TRAFFIC = {("c2_chunks_p4", "copier_bulk_kernel"): 474700544,
                # captured with 2000 rows per rank (--rows 2000) and scaled by the rows, 4x
-               ("c3_tiles_p8", "copier_bulk_kernel"): 8009827328,
+               ("c3_tiles_p8", "copier_bulk_kernel"): 8009544192,
                ("c5_gemm_p4", "gemm2_producer_kernel"): 184814208,
-               ("c5_gemm_p4", "copier_kernel"): 206425216}
+               ("c5_gemm_p4", "copier_kernel"): 206209536}
 # DRAM bytes (read, write) of one whole round, producer, copier and check together, from an
 # ncu range-replay capture of three rounds of the benchmark's launch (--profile-rounds 3;
 # c2 and c5 with overlapping rounds)
@@ -513,7 +513,7 @@ def measure_workload(w, args, K, warmup, latency_rounds, isolated_rounds, with_e
         out.update(timing_pass_s=t3, copier_ms=copier_ms, producer_ms=producer_ms)
 
     # gate-to-arrival latency and the copier window, from the gate timestamps of extra rounds
-    lat, windows = [], []
+    lat, windows, queue, xfer = [], [], [], []
     _, _, n_chunks_all, _ = st.plan.info()
     out["n_chunks_total"] = sum(n_chunks_all[r] for r in w.senders())
     for _ in range(latency_rounds):
@@ -528,13 +528,18 @@ def measure_workload(w, args, K, warmup, latency_rounds, isolated_rounds, with_e
             for c in range(first[r], first[r] + n_chunks[r]):
                 to = int(g[r, c, D.GATE_T_OPEN])
                 t_open_min = to if t_open_min is None else min(t_open_min, to)
+                tc = int(g[r, c, D.GATE_T_ARRIVE])     # owner's row: when the copier began the chunk
+                if tc >= to > 0:
+                    queue.append(tc - to)
                 for p in range(w.P):
                     if p != r:
                         ta = int(g[p, c, D.GATE_T_ARRIVE])
                         lat.append(ta - to)
                         t_arr_max = max(t_arr_max, ta)
+                        if tc >= to > 0:
+                            xfer.append(ta - tc)
         windows.append((t_arr_max - t_open_min) / 1e9)
-    out.update(lat=lat, windows=windows)
+    out.update(lat=lat, windows=windows, queue=queue, xfer=xfer)
 
     # e2e: the host-buffer round through the public API: H2D of every rank's slice from pinned
     # memory, the triggered fan-out, D2H of rank 0's gathered buffer
@@ -605,9 +610,12 @@ def summarize(m, K, t_max, units, peak, peak_kind):
                     "flops_per_launch": flops}
     else:
         roofline = copier_roof
-    lat_sorted = sorted(m["lat"]) or [0]
-    lat_med = lat_sorted[len(lat_sorted) // 2]
-    lat_p99 = lat_sorted[min(len(lat_sorted) - 1, int(len(lat_sorted) * 0.99))]
+    def med_p99(xs):
+        xs = sorted(xs) or [0]
+        return xs[len(xs) // 2], xs[min(len(xs) - 1, int(len(xs) * 0.99))]
+    lat_med, lat_p99 = med_p99(m["lat"])
+    q_med, q_p99 = med_p99(m.get("queue") or [])
+    x_med, x_p99 = med_p99(m.get("xfer") or [])
     # the ideal time of one chunk's fan-out at the measured copy peak: one read of the chunk and
     # P-1 writes of it, (S_c + (P-1) S_c) / peak
     chunk_mean = len(w.senders()) * w.slice_bytes / max(1, m["n_chunks_total"])
@@ -642,7 +650,13 @@ def summarize(m, K, t_max, units, peak, peak_kind):
                                "chunk_bytes_mean": chunk_mean,
                                "ideal_chunk_ns": ideal_ns,
                                "median_over_ideal": lat_med / ideal_ns if ideal_ns else None,
-                               "p99_over_ideal": lat_p99 / ideal_ns if ideal_ns else None},
+                               "p99_over_ideal": lat_p99 / ideal_ns if ideal_ns else None,
+                               # the same split in two: the chunk's wait in its queue (gate open to
+                               # the copier beginning it) and its transfer (to each arrival)
+                               "queue_median": q_med if m.get("queue") else None,
+                               "queue_p99": q_p99 if m.get("queue") else None,
+                               "transfer_median": x_med if m.get("xfer") else None,
+                               "transfer_p99": x_p99 if m.get("xfer") else None},
         "early_copier": {"wait_us": m["early_copier_us"], **(m.get("early") or {})},
         "e2e": e2e,
     }
@@ -705,7 +719,8 @@ def run_ours(args):
                 "copier_window_hbm_frac": (sc["copier_window"] or {}).get("hbm_frac"),
                 "isolated": sc["isolated"],
                 "gate_to_arrival_ns": {k: sc["gate_to_arrival_ns"][k] for k in
-                                       ("median", "p99", "median_over_ideal", "p99_over_ideal")},
+                                       ("median", "p99", "median_over_ideal", "p99_over_ideal",
+                                        "queue_median", "transfer_median", "transfer_p99")},
                 "early_copier": sc["early_copier"],
                 "workload": describe(wc, mc["launch"], mc["copier_method"]),
                 "l2": l2_note(wc, dev)}

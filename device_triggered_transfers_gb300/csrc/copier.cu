@@ -82,6 +82,16 @@ __device__ __forceinline__ void signal_arrivals(const CopierParams& p, uint32_t 
     notify_host(p, c);
 }
 
+// The CTA that takes a chunk's first piece stamps, in the owner's gate row, when the copier began
+// the chunk this round (the row's arrival-time word, which only peer rows use otherwise): the
+// time from the gate's opening to it is the chunk's wait in its queue, the time from it to each
+// arrival the transfer's.
+__device__ __forceinline__ void stamp_copy_start(const CopierParams& p, uint32_t s, uint32_t c) {
+    if (p.flags & DTT_HANDLE_TIMESTAMPS)
+        dtt_dev::st_relaxed(p.gates + ((uint64_t)s * p.n_global + c) * DTT_GATE_WORDS + DTT_GATE_T_ARRIVE,
+                            dtt_dev::globaltimer());
+}
+
 // Copy one piece from buffer s to each receiver's landing place: 16-byte vectors, kUnroll loads
 // in flight per thread, each value stored to every receiver (at the piece's destination).
 __device__ __forceinline__ void copy_piece_vec(const CopierParams& p, uint32_t s, uint32_t peers,
@@ -172,6 +182,7 @@ __device__ __forceinline__ void copier_body(const CopierParams& p) {
         if (!s_go[k & 1]) return;
         const uint32_t i0 = (j + G - cd.rot) % G;
         if (i0 >= cd.n_pieces) continue;
+        if (i0 == 0 && threadIdx.x == 0) stamp_copy_start(p, s, c);
         for (uint32_t i = i0; i < cd.n_pieces; i += G) {
             const PieceDesc pc = p.pieces[cd.piece_begin + i];
             if (pc.vec)
@@ -421,6 +432,7 @@ __device__ __forceinline__ void copier_bulk_body(const CopierParams& p) {
         peers = cd.peers;
         const uint32_t i0 = (j + G - cd.rot) % G;
         if (i0 >= cd.n_pieces) continue;
+        if (i0 == 0) stamp_copy_start(p, s, c);
         const uint32_t n = (cd.n_pieces - i0 + G - 1) / G;       // my pieces of this chunk
         const PieceDesc* mine = p.pieces + cd.piece_begin + i0;  // stride G
         const uint32_t pre = n < S - 1 ? n : S - 1;

@@ -341,7 +341,8 @@ enum {
     DTT_GATE_ERROR = 3,       /* owner's row: round of an extra mark, else 0 */
     DTT_GATE_COUNTER = 4,     /* owner's row: writer marks, round*writers after a round */
     DTT_GATE_T_OPEN = 5,      /* owner's row: globaltimer when the gate opened */
-    DTT_GATE_T_ARRIVE = 6,    /* peer's row: globaltimer when the arrival was signalled */
+    DTT_GATE_T_ARRIVE = 6,    /* peer's row: globaltimer when the arrival was signalled; owner's
+                                 row: when the copier began the chunk (SM copiers) */
     DTT_GATE_COPIER = 7,      /* owner's row: copier-internal progress counter */
     DTT_GATE_WORDS = 8
 };
