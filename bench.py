@@ -367,7 +367,7 @@ def measure_workload(w, args, K, warmup, latency_rounds, isolated_rounds, with_e
         opts.early_copier_us = early_us
     if getattr(args, "copier", None):            # launch overrides
         opts.method = {"vector": D.COPY_VEC16, "bulk": D.COPY_TMA}[args.copier]
-    for k in ("piece_bytes", "stages", "ctas_per_sm", "copier_threads", "copier_ctas"):
+    for k in ("piece_bytes", "stages", "ctas_per_sm", "copier_threads", "copier_ctas", "host_piece_bytes"):
         v = getattr(args, k, 0)
         if v:
             setattr(opts, k, v)
@@ -551,17 +551,25 @@ def measure_workload(w, args, K, warmup, latency_rounds, isolated_rounds, with_e
             host_in[r].copy_(st.bufs[r][w.slice_offset(r):w.slice_offset(r) + S].cpu())
         host_out = torch.empty(w.buf_bytes, dtype=torch.uint8).pin_memory()
         e2e_steps = max(1, min(K, 20))
-        for _ in range(2):
-            st.plan.allgather_host(host_in, host_out, 0, prod)
+        if overlap:
+            # rounds back to back in one call, pipelined: a round's slices go in while the round
+            # before comes back (each round's copies in and back are all inside the timed region)
+            def run_e2e(n):
+                st.plan.allgather_host_rounds([host_in] * n, [host_out] * n, 0, prod)
+        else:
+            def run_e2e(n):
+                for _ in range(n):
+                    st.plan.allgather_host(host_in, host_out, 0, prod)
+        run_e2e(2)
         torch.cuda.synchronize()
         x0, x1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         x0.record(prod)
-        for _ in range(e2e_steps):
-            st.plan.allgather_host(host_in, host_out, 0, prod)
+        run_e2e(e2e_steps)
         x1.record(prod)
         torch.cuda.synchronize()
         out["e2e"] = {"elapsed_s": x0.elapsed_time(x1) / 1e3, "steps": e2e_steps,
-                      "h2d_bytes_per_step": S * w.P, "d2h_bytes_per_step": w.buf_bytes}
+                      "h2d_bytes_per_step": S * w.P, "d2h_bytes_per_step": w.buf_bytes,
+                      "call": "dtt_allgather_host_rounds" if overlap else "dtt_allgather_host"}
     st.plan.close()
 
     # the same copier and producer one after the other (deferred plan): each kernel alone
@@ -632,7 +640,7 @@ def summarize(m, K, t_max, units, peak, peak_kind):
     if m["e2e"]:
         e2e = {"value": D_round * m["e2e"]["steps"] / m["e2e"]["elapsed_s"] / 1e9, "unit": "GB/s",
                "h2d_bytes_per_step": m["e2e"]["h2d_bytes_per_step"],
-               "d2h_bytes_per_step": m["e2e"]["d2h_bytes_per_step"]}
+               "d2h_bytes_per_step": m["e2e"]["d2h_bytes_per_step"], "call": m["e2e"]["call"]}
     return {
         "ms_per_round": t_max / K * 1e3,
         "gbs_delivered": units / t_max / 1e9,
@@ -1035,6 +1043,8 @@ def main(argv=None):
     ap.add_argument("--ctas-per-sm", type=int, default=0, help="copier CTAs per SM (default: the launch's)")
     ap.add_argument("--copier-threads", type=int, default=0, help="vector copier threads per CTA")
     ap.add_argument("--copier-ctas", type=int, default=0, help="copier CTAs in all (default: per SM)")
+    ap.add_argument("--host-piece-bytes", type=int, default=0,
+                    help="host-buffer round: bytes per host-to-device copy (default: the plan's)")
     ap.add_argument("--pace", type=int, default=-1,
                     help="the fill producer's pacing in chunks (default: the launch's own)")
     ap.add_argument("--latency-rounds", type=int, default=20)

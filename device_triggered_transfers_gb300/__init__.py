@@ -147,6 +147,8 @@ _SIGS = {
                                     _u64, _P, _P]),
     "dtt_plan_stats": (C.c_int, [_P, C.POINTER(C.c_double), C.POINTER(C.c_double), C.POINTER(_u64)]),
     "dtt_allgather_host": (C.c_int, [_P, C.POINTER(_P), _P, _u32, _P, C.POINTER(dtt_report)]),
+    "dtt_allgather_host_rounds": (C.c_int, [_P, _u32, C.POINTER(_P), C.POINTER(_P), _u32, _P,
+                                            C.POINTER(dtt_report)]),
     "dtt_fill_producer": (C.c_int, [C.POINTER(_P), _u32, C.POINTER(dtt_fill_desc),
                                     C.POINTER(dtt_handle), _P]),
     "dtt_publish": (C.c_int, [C.POINTER(dtt_handle), _u32, _u32, _u32, _u32, _P]),
@@ -514,6 +516,24 @@ class Plan:
         if raise_on_error:
             _check(rc)
         return rep
+
+    def allgather_host_rounds(self, host_slices: Sequence[Sequence], host_outs=None, out_rank: int = 0,
+                              stream=None, raise_on_error: bool = True) -> List[dtt_report]:
+        """Several host-buffer rounds back to back, pipelined (dtt_allgather_host_rounds).
+        host_slices: one list of P slices per round (None: as it stands); host_outs: one buffer
+        (or None) per round, or None.  Returns the rounds' reports."""
+        n = len(host_slices)
+        if any(len(sl) != self.P for sl in host_slices):
+            raise DttError(EINVAL, "allgather_host_rounds: P slices per round")
+        if host_outs is not None and len(host_outs) != n:
+            raise DttError(EINVAL, "allgather_host_rounds: one output (or None) per round")
+        slices = _ptr_array([x for sl in host_slices for x in sl])
+        outs = _ptr_array(list(host_outs)) if host_outs is not None else None
+        reps = (dtt_report * max(1, n))()
+        rc = lib().dtt_allgather_host_rounds(self._h, n, slices, outs, out_rank, _stream(stream), reps)
+        if raise_on_error:
+            _check(rc)
+        return list(reps[:n])
 
     def gemm_consumer(self, rank: int, Wt, D, N: int, K: int, err, ldd: int = 0,
                       num_programs: int = 0, max_polls: int = 0, stream=None) -> None:

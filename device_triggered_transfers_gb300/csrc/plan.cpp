@@ -100,6 +100,7 @@ struct dtt_plan {
     cudaEvent_t ev_copier_end = nullptr;   // after that launch: the copier has exited
     cudaEvent_t ev_h2d = nullptr;
     std::vector<cudaEvent_t> ev_pieces;   // one per host-to-device piece of the output rank's slice
+    std::vector<cudaEvent_t> ev_free;     // dtt_allgather_host_rounds: events not in use
     cudaStream_t h2d_stream = nullptr;
     cudaStream_t d2h_stream = nullptr;
 
@@ -203,6 +204,8 @@ void free_device(dtt_plan* p) {
     if (p->ev_h2d) cudaEventDestroy(p->ev_h2d);
     for (cudaEvent_t e : p->ev_pieces) cudaEventDestroy(e);
     p->ev_pieces.clear();
+    for (cudaEvent_t e : p->ev_free) cudaEventDestroy(e);
+    p->ev_free.clear();
     if (p->d2h_stream) cudaStreamDestroy(p->d2h_stream);
     if (p->h2d_stream) cudaStreamDestroy(p->h2d_stream);
     p->h2d_stream = nullptr;
@@ -1901,6 +1904,305 @@ int dtt_allgather_host(dtt_plan* p, const void* const* host_slices, void* host_o
         for (uint32_t r = 0; r < P; ++r)
             if (back[r] != S) return fail(DTT_ETIMEDOUT, "dtt_allgather_host: slice %u came back short", r);
     }
+    return dtt_plan_next_round(p);
+}
+
+namespace {
+
+// One round of dtt_allgather_host_rounds: its host buffers and how far each slice has gone in
+// (copied), been marked and come back (back), with the copy-back events later rounds gate on.
+struct HostRound {
+    uint32_t R = 0;
+    bool started = false, checked = false;
+    dtt_handle h[DTT_MAX_RANKS];
+    const void* const* slices = nullptr;    // P host pointers (NULL: the slice as it stands)
+    char* out = nullptr;                    // the output rank's gathered buffer (or NULL)
+    uint64_t copied[DTT_MAX_RANKS] = {}, back[DTT_MAX_RANKS] = {};
+    uint32_t marked[DTT_MAX_RANKS] = {};
+    // per slice: (prefix copied back once the copy is done, event after that copy)
+    std::vector<std::pair<uint64_t, cudaEvent_t>> d2h[DTT_MAX_RANKS];
+    // the output rank's own pieces: (prefix copied in, event after that copy)
+    std::vector<std::pair<uint64_t, cudaEvent_t>> own;
+    size_t own_next = 0;
+    cudaEvent_t copier_end = nullptr;       // after this round's copier on the copy stream
+};
+
+cudaEvent_t take_event(dtt_plan* p) {
+    if (!p->ev_free.empty()) {
+        cudaEvent_t e = p->ev_free.back();
+        p->ev_free.pop_back();
+        return e;
+    }
+    cudaEvent_t e = nullptr;
+    return cudaEventCreateWithFlags(&e, cudaEventDisableTiming) == cudaSuccess ? e : nullptr;
+}
+
+void give_events(dtt_plan* p, HostRound& x) {
+    for (auto& v : x.d2h) {
+        for (auto& pe : v) p->ev_free.push_back(pe.second);
+        v.clear();
+    }
+    for (auto& pe : x.own) p->ev_free.push_back(pe.second);
+    x.own.clear();
+    if (x.copier_end) p->ev_free.push_back(x.copier_end);
+    x.copier_end = nullptr;
+}
+
+// The event after the first copy back of slice r that reaches `upto`, or nullptr if none has
+// been issued yet.
+cudaEvent_t back_event(const HostRound& x, uint32_t r, uint64_t upto) {
+    for (const auto& pe : x.d2h[r])
+        if (pe.first >= upto) return pe.second;
+    return nullptr;
+}
+
+}  // namespace
+
+int dtt_allgather_host_rounds(dtt_plan* p, uint32_t n_rounds, const void* const* host_slices,
+                              void* const* host_outs, uint32_t out_rank, cudaStream_t stream,
+                              dtt_report* reports) {
+    if (!p || !host_slices) return fail(DTT_EINVAL, "dtt_allgather_host_rounds: bad args");
+    if (!p->opts.overlap) return fail(DTT_EINVAL, "dtt_allgather_host_rounds: needs a plan with overlapping rounds");
+    if (!p->opts.allgather) return fail(DTT_EINVAL, "dtt_allgather_host_rounds: needs an all-gather plan");
+    if (p->ce) return fail(DTT_EINVAL, "dtt_allgather_host_rounds: needs an SM copier (not DTT_COPY_ENGINE)");
+    if (p->other_dests || p->separate_dst)
+        return fail(DTT_EINVAL, "dtt_allgather_host_rounds: needs chunks that land at their own offsets");
+    if (out_rank >= p->P) return fail(DTT_EINVAL, "dtt_allgather_host_rounds: out_rank out of range");
+    if (p->state != DTT_PLAN_PREPARED || p->pending)
+        return fail(DTT_ESTATE, "dtt_allgather_host_rounds: needs a PREPARED plan with no round pending");
+    if (n_rounds == 0) return DTT_OK;
+    if ((uint64_t)p->round + n_rounds - 1 > 0xFFFFFFFFull)
+        return fail(DTT_EROUNDLIMIT, "dtt_allgather_host_rounds: the rounds would pass 2^32 - 1");
+    const uint32_t P = p->P;
+    const uint64_t S = p->buf_bytes / P;
+    std::vector<uint64_t> lo, hi;            // each chunk's byte extent inside its rank's slice
+    chunk_extents(p, &lo, &hi);
+    for (uint32_t c = 0; c < p->n_global; ++c) {
+        const uint64_t base = (uint64_t)p->chunks[c].owner * S;
+        if (hi[c]) {
+            lo[c] -= base;
+            hi[c] -= base;
+        }
+    }
+    const uint64_t kPiece = p->opts.host_piece_bytes
+                                ? p->opts.host_piece_bytes
+                                : std::max<uint64_t>(4ull << 20, (S / 4 + 4095) & ~uint64_t(4095));
+    std::vector<HostRound> rounds(n_rounds);
+    for (uint32_t k = 0; k < n_rounds; ++k) {
+        HostRound& x = rounds[k];
+        x.slices = host_slices + (size_t)k * P;
+        x.out = host_outs ? static_cast<char*>(host_outs[k]) : nullptr;
+        for (uint32_t r = 0; r < P; ++r) {
+            x.marked[r] = p->first_chunk[r];
+            if (!x.slices[r]) x.copied[r] = S;
+        }
+    }
+    int rc = DTT_OK;
+    auto fail_all = [&](int code) -> int {
+        for (HostRound& x : rounds) give_events(p, x);
+        return code;
+    };
+
+    // Start round k: its copier (queued behind the round in flight, if any) stamps each chunk's
+    // arrival into mapped host memory.
+    auto start_round = [&](HostRound& x) -> int {
+        p->notify_host = true;
+        int src = dtt_plan_start(p, stream, x.h);
+        if (src == DTT_OK && p->opts.deferred_copier == 2) src = dtt_plan_launch_copier(p);
+        p->notify_host = false;
+        if (src != DTT_OK) return src;
+        x.R = p->round;
+        x.started = true;
+        x.copier_end = take_event(p);
+        if (!x.copier_end) return fail(DTT_ECUDA, "dtt_allgather_host_rounds: cannot create an event");
+        DTT_CUDA_TRY(cudaEventRecord(x.copier_end, p->copy_stream));
+        return DTT_OK;
+    };
+    // Rank r's chunks [marked, k) whose bytes are all in go to the copier.  prev: the round
+    // before, still coming back: a chunk's copies land in the output rank's buffer, so they wait
+    // (on the device) for that round's copy back of the same bytes.
+    auto publish = [&](HostRound& x, const HostRound* prev, uint32_t r) -> int {
+        const uint32_t end = p->first_chunk[r] + p->n_chunks[r];
+        uint32_t k = x.marked[r];
+        while (k < end && hi[k] <= x.copied[r]) ++k;
+        if (k == x.marked[r]) return DTT_OK;
+        if (prev && prev->out && r != out_rank) {
+            uint32_t q = x.marked[r];
+            while (q < k) {                       // as far as that round's copies back reach
+                cudaEvent_t e = back_event(*prev, r, hi[q]);
+                if (!e) break;
+                uint32_t q2 = q;
+                while (q2 < k && back_event(*prev, r, hi[q2]) == e) ++q2;
+                DTT_CUDA_TRY(cudaStreamWaitEvent(stream, e, 0));
+                const int prc = dtt_publish(x.h, P, q, q2 - q, 0, stream);
+                if (prc != DTT_OK) return prc;
+                q = q2;
+            }
+            x.marked[r] = q;
+            return DTT_OK;
+        }
+        const int prc = dtt_publish(x.h, P, x.marked[r], k - x.marked[r], 0, stream);
+        x.marked[r] = k;
+        return prc;
+    };
+    // Copy in the next piece of rank r's slice if it may be overwritten: the round before has
+    // delivered every chunk it touches, and (the output rank's own slice) copied those bytes back.
+    auto copy_in = [&](HostRound& x, const HostRound* prev, uint32_t r) -> int {
+        if (x.copied[r] >= S) return DTT_OK;
+        const uint64_t a = x.copied[r], n = std::min(kPiece, S - a), b = a + n;
+        if (prev) {
+            for (uint32_t c = p->first_chunk[r]; c < p->first_chunk[r] + p->n_chunks[r]; ++c)
+                if (hi[c] && lo[c] < b && hi[c] > a &&
+                    __atomic_load_n(&p->h_arrived[c], __ATOMIC_ACQUIRE) < prev->R)
+                    return DTT_OK;                // still being sent: not yet
+            if (prev->out && r == out_rank) {
+                cudaEvent_t e = back_event(*prev, r, b);
+                if (!e) return DTT_OK;            // not yet copied back
+                DTT_CUDA_TRY(cudaStreamWaitEvent(p->h2d_stream, e, 0));
+            }
+        }
+        DTT_CUDA_TRY(cudaMemcpyAsync(p->bufs[r] + r * S + a, static_cast<const char*>(x.slices[r]) + a, n,
+                                     cudaMemcpyHostToDevice, p->h2d_stream));
+        x.copied[r] = b;
+        DTT_CUDA_TRY(cudaEventRecord(p->ev_h2d, p->h2d_stream));
+        DTT_CUDA_TRY(cudaStreamWaitEvent(stream, p->ev_h2d, 0));
+        if (x.out && r == out_rank) {
+            cudaEvent_t e = take_event(p);
+            if (!e) return fail(DTT_ECUDA, "dtt_allgather_host_rounds: cannot create an event");
+            DTT_CUDA_TRY(cudaEventRecord(e, p->h2d_stream));
+            x.own.emplace_back(b, e);
+        }
+        return publish(x, prev, r);
+    };
+    // Copy back slice r of the output rank's buffer up to `upto`.
+    auto copy_back = [&](HostRound& x, uint32_t r, uint64_t upto) -> int {
+        if (upto <= x.back[r]) return DTT_OK;
+        DTT_CUDA_TRY(cudaMemcpyAsync(x.out + r * S + x.back[r], p->bufs[out_rank] + r * S + x.back[r],
+                                     upto - x.back[r], cudaMemcpyDeviceToHost, p->d2h_stream));
+        x.back[r] = upto;
+        cudaEvent_t e = take_event(p);
+        if (!e) return fail(DTT_ECUDA, "dtt_allgather_host_rounds: cannot create an event");
+        DTT_CUDA_TRY(cudaEventRecord(e, p->d2h_stream));
+        x.d2h[r].emplace_back(upto, e);
+        return DTT_OK;
+    };
+    // Copies back as far as chunks have arrived (the output rank's own pieces once copied in).
+    // final: the round's copier has exited, so whatever arrived is all there is.
+    auto come_back = [&](HostRound& x, bool final) -> int {
+        if (!x.out) return DTT_OK;
+        while (x.own_next < x.own.size()) {
+            const cudaError_t e = cudaEventQuery(x.own[x.own_next].second);
+            if (e == cudaErrorNotReady) break;
+            if (e != cudaSuccess) return fail(DTT_ECUDA, "dtt_allgather_host_rounds: %s", cudaGetErrorString(e));
+            const int prc = copy_back(x, out_rank, x.own[x.own_next++].first);
+            if (prc != DTT_OK) return prc;
+        }
+        if (!x.slices[out_rank] && x.back[out_rank] < S) {     // its rows as they stand
+            const int prc = copy_back(x, out_rank, S);
+            if (prc != DTT_OK) return prc;
+        }
+        for (uint32_t r = 0; r < P; ++r) {
+            if (r == out_rank) continue;
+            // a chunk's stamp is the round of its last arrival everywhere: this round's, or (for
+            // bytes already copied back) the next round's
+            uint64_t upto = S;
+            for (uint32_t c = p->first_chunk[r]; c < p->first_chunk[r] + p->n_chunks[r]; ++c)
+                if (hi[c] > x.back[r] && __atomic_load_n(&p->h_arrived[c], __ATOMIC_ACQUIRE) < x.R)
+                    upto = std::min(upto, lo[c]);
+            if (upto == S || upto >= x.back[r] + kPiece || (final && upto > x.back[r])) {
+                const int prc = copy_back(x, r, upto);
+                if (prc != DTT_OK) return prc;
+            }
+        }
+        return DTT_OK;
+    };
+    auto all_in = [&](const HostRound& x) {
+        for (uint32_t r = 0; r < P; ++r)
+            if (x.copied[r] < S || x.marked[r] < p->first_chunk[r] + p->n_chunks[r]) return false;
+        return true;
+    };
+    auto all_back = [&](const HostRound& x) {
+        if (!x.out) return true;
+        for (uint32_t r = 0; r < P; ++r)
+            if (x.back[r] < S) return false;
+        return true;
+    };
+
+    // Round k's bytes go in, are marked, fanned out and come back while round k + 1's go in
+    // behind them; round k is checked (the pending round) once it has come back.
+    DTT_CUDA_TRY(cudaEventRecord(p->ev_h2d, stream));      // after the caller's work on `stream`
+    DTT_CUDA_TRY(cudaStreamWaitEvent(p->h2d_stream, p->ev_h2d, 0));
+    if ((rc = start_round(rounds[0])) != DTT_OK) return fail_all(rc);
+    uint32_t cur = 0;                         // the oldest round not yet checked
+    for (uint64_t spin = 1; cur < n_rounds; ++spin) {
+        HostRound& x = rounds[cur];
+        HostRound* y = cur + 1 < n_rounds ? &rounds[cur + 1] : nullptr;
+        const HostRound* before = cur > 0 && !rounds[cur - 1].checked ? &rounds[cur - 1] : nullptr;
+        for (uint32_t r = 0; r < P && rc == DTT_OK; ++r) {
+            while (x.copied[r] < S && rc == DTT_OK) {
+                const uint64_t was = x.copied[r];
+                rc = copy_in(x, before, r);
+                if (x.copied[r] == was) break;
+            }
+            if (rc == DTT_OK) rc = publish(x, before, r);
+        }
+        if (rc == DTT_OK) rc = come_back(x, false);
+        // the next round starts once this one is all in: this round is left pending
+        if (rc == DTT_OK && y && !y->started && all_in(x)) {
+            rc = dtt_plan_next_round(p);
+            if (rc == DTT_OK) rc = start_round(*y);
+        }
+        if (rc == DTT_OK && y && y->started) {
+            for (uint32_t r = 0; r < P && rc == DTT_OK; ++r) {
+                while (y->copied[r] < S && rc == DTT_OK) {
+                    const uint64_t was = y->copied[r];
+                    rc = copy_in(*y, &x, r);
+                    if (y->copied[r] == was) break;
+                }
+                if (rc == DTT_OK) rc = publish(*y, &x, r);
+            }
+            if (rc == DTT_OK) rc = come_back(*y, false);
+        }
+        if (rc != DTT_OK) return fail_all(rc);
+        bool done_back = all_in(x) && all_back(x);
+        if (!done_back && (spin & 1023) == 0) {
+            const cudaError_t e = cudaEventQuery(x.copier_end);
+            if (e == cudaSuccess) {               // nothing more will arrive
+                if ((rc = come_back(x, true)) != DTT_OK) return fail_all(rc);
+                done_back = true;
+            } else if (e != cudaErrorNotReady) {
+                return fail_all(fail(DTT_ECUDA, "dtt_allgather_host_rounds: %s", cudaGetErrorString(e)));
+            }
+        }
+        if (done_back && all_in(x)) {
+            // check round x: the pending one when the next has started, else the current one
+            DTT_CUDA_TRY(cudaStreamWaitEvent(stream, p->ev_h2d, 0));   // every copy in precedes the check
+            p->suppress_early = true;
+            rc = dtt_plan_wait(p, reports ? &reports[cur] : nullptr);
+            p->suppress_early = false;
+            if (rc != DTT_OK) {
+                cudaStreamSynchronize(p->d2h_stream);
+                return fail_all(rc);
+            }
+            x.checked = true;
+            if (x.out) {
+                DTT_CUDA_TRY(cudaStreamSynchronize(p->d2h_stream));
+                for (uint32_t r = 0; r < P; ++r)
+                    if (x.back[r] != S)
+                        return fail_all(fail(DTT_ETIMEDOUT, "dtt_allgather_host_rounds: round %u's slice %u came back short",
+                                             x.R, r));
+            }
+            if (cur > 0) give_events(p, rounds[cur - 1]);
+            ++cur;
+            if (cur < n_rounds && !rounds[cur].started) {     // a round of its own: nothing pending
+                rc = dtt_plan_next_round(p);
+                if (rc == DTT_OK) rc = start_round(rounds[cur]);
+                if (rc != DTT_OK) return fail_all(rc);
+            }
+        }
+    }
+    give_events(p, rounds[n_rounds - 1]);
+    if (n_rounds > 1) give_events(p, rounds[n_rounds - 2]);
     return dtt_plan_next_round(p);
 }
 

@@ -517,6 +517,29 @@ int dtt_plan_read_gates(dtt_plan* plan, uint64_t* host, uint64_t n_words);
 int dtt_allgather_host(dtt_plan* plan, const void* const* host_slices, void* host_out,
                        uint32_t out_rank, cudaStream_t stream, dtt_report* report);
 
+/* Host-buffer all-gather over n_rounds rounds back to back, pipelined across rounds (a plan made
+ * with opts.overlap): each round as dtt_allgather_host, but round k + 1's slices start going in
+ * while round k's gathered buffer is still coming back, so the host link carries both directions
+ * nearly all the time.  Round k + 1's bytes of a slice go in only once round k has delivered the
+ * chunks they overwrite (the copier's arrival stamps in mapped host memory, polled here) and, in
+ * the output rank's own rows, copied them back; a chunk of round k + 1 is marked only once round
+ * k's copy back of the bytes its copies will overwrite in the output rank's buffer is done (an
+ * event the marking kernel's stream waits on).  Round k is checked (the plan's pending round)
+ * once it has come back.
+ *  - host_slices: n_rounds * P pinned host pointers, round-major (round k's at [k * P, k * P + P)),
+ *    S = buf_bytes / P bytes each; NULL: that slice as it stands.
+ *  - host_outs: n_rounds pinned host pointers of buf_bytes each; the array or an entry may be NULL
+ *    (that round is not copied back).
+ *  - reports: n_rounds reports (may be NULL), filled as by dtt_plan_wait.
+ * The call returns when every round has come back and been checked, and leaves the plan PREPARED
+ * for the round after them.  Needs an all-gather plan made with opts.overlap, PREPARED with no
+ * round pending, an SM copier and chunks that land at their own offsets.
+ * Errors: DTT_EINVAL, DTT_ESTATE, DTT_EROUNDLIMIT, those of dtt_plan_wait (the plan is then FAILED),
+ * DTT_ETIMEDOUT (a slice came back short), DTT_ECUDA. */
+int dtt_allgather_host_rounds(dtt_plan* plan, uint32_t n_rounds, const void* const* host_slices,
+                              void* const* host_outs, uint32_t out_rank, cudaStream_t stream,
+                              dtt_report* reports);
+
 /* ---------------------------------------------------------------------------------------- */
 /* Producers and consumers shipped with the library                                          */
 /* ---------------------------------------------------------------------------------------- */

@@ -574,3 +574,108 @@ def test_many_overlapped_rounds_keep_the_gates_and_data_right():
         assert_buffers_equal(st.bufs, expected_on_device(w, R), f"{w.name} round {R}")
     finally:
         st.plan.close()
+
+
+# ---- host-buffer rounds, pipelined across rounds ----------------------------------------------
+
+HOST_ROUND_CASES = {
+    "chunks_one_piece": (W.small(W.C2, M=128, N=512, num_chunks=4), {}),
+    # 8 MiB slices go in as two 4 MiB pieces; 1 MiB chunks open as their bytes land
+    "chunks_two_pieces_bulk": (W.small(W.C2, M=2048, N=2048, num_chunks=8),
+                               {"opts": dict(method=1, piece_bytes=65536, stages=3)}),
+    # 2D tile windows (tensor-map boxes), grouped order, slices of two pieces
+    "tiles_two_pieces": (W.Workload("ht", P=3, M=3000, N=1024, dtype=W.BF16, kind="tile_chunks",
+                                    rounds=2, seed=41, BM=128, BN=128, num_programs=6,
+                                    tiles_per_chunk=6, group_m=4),
+                         {"opts": dict(method=1, piece_bytes=16384, stages=12)}),
+    # host copies of 12 KiB: many pieces per slice, chunk edges inside pieces
+    "chunks_small_host_pieces": (W.small(W.C2, M=96, N=1024, num_chunks=6),
+                                 {"opts": dict(host_piece_bytes=12288)}),
+}
+
+
+def _host_slices(w, R):
+    """Round R's host slices: every round's values differ (a copy carrying another round's bytes
+    shows), and the closed form of the gathered buffer is their concatenation."""
+    return [torch.from_numpy(H.fill_slice_bytes(w.dtype, w.seed + R, r, R, w.M, w.N)).pin_memory()
+            for r in range(w.P)]
+
+
+@pytest.mark.parametrize("out_rank", ["first", "last"])
+@pytest.mark.parametrize("name", sorted(HOST_ROUND_CASES))
+def test_host_rounds_pipelined(name, out_rank):
+    # rounds from and to host memory back to back, round k + 1's slices going in while round k's
+    # gathered buffer comes back: every round's copy back is that round's concatenation
+    w, kw = HOST_ROUND_CASES[name]
+    q = 0 if out_rank == "first" else w.P - 1
+    st = runner.make(w, opts=_opts(**kw.get("opts", {})))
+    n = 5
+    host = [_host_slices(w, R) for R in range(1, n + 1)]
+    outs = [torch.zeros(w.buf_bytes, dtype=torch.uint8).pin_memory() for _ in range(n)]
+    try:
+        reps = st.plan.allgather_host_rounds(host, outs, q, st.producer_stream)
+        assert [r.round for r in reps] == list(range(1, n + 1))
+        assert all(r.status == D.OK and r.copier_timeouts == 0 for r in reps)
+        for k in range(n):
+            want = np.concatenate([h.numpy() for h in host[k]])
+            np.testing.assert_array_equal(outs[k].numpy(), want, err_msg=f"round {k + 1}")
+        want = np.concatenate([h.numpy() for h in host[-1]])
+        for b in st.bufs:
+            np.testing.assert_array_equal(b.cpu().numpy(), want)
+        assert st.plan.round == n + 1 and st.plan.state == D.PREPARED and st.plan.pending == 0
+        # and one more round of the ordinary kind on the same plan
+        more = _host_slices(w, n + 1)
+        out = torch.zeros(w.buf_bytes, dtype=torch.uint8).pin_memory()
+        assert st.plan.allgather_host(more, out, q, st.producer_stream).status == D.OK
+        np.testing.assert_array_equal(out.numpy(), np.concatenate([h.numpy() for h in more]))
+    finally:
+        st.plan.close()
+
+
+def test_host_rounds_edges():
+    # a round with a slice left as it stands, a round with no copy back, one round alone, and a
+    # plan without overlapping rounds (refused)
+    w = W.small(W.C2, M=1024, N=2048, num_chunks=4)
+    S = w.slice_bytes
+    st = runner.make(w, opts=_opts(), fill_byte=5)
+    try:
+        host = [_host_slices(w, R) for R in (1, 2, 3)]
+        host[0][1] = None                       # round 1: rank 1's rows as they stand (5s)
+        outs = [torch.zeros(w.buf_bytes, dtype=torch.uint8).pin_memory() for _ in range(3)]
+        outs[1] = None                          # round 2: nothing copied back
+        reps = st.plan.allgather_host_rounds(host, outs, 0, st.producer_stream)
+        assert [r.status for r in reps] == [D.OK] * 3
+        want1 = np.concatenate([h.numpy() if h is not None else np.full(S, 5, np.uint8) for h in host[0]])
+        np.testing.assert_array_equal(outs[0].numpy(), want1)
+        np.testing.assert_array_equal(outs[2].numpy(), np.concatenate([h.numpy() for h in host[2]]))
+        one = [_host_slices(w, 4)]
+        out = [torch.zeros(w.buf_bytes, dtype=torch.uint8).pin_memory()]
+        rep = st.plan.allgather_host_rounds(one, out, w.P - 1, st.producer_stream)
+        assert rep[0].status == D.OK and rep[0].round == 4
+        np.testing.assert_array_equal(out[0].numpy(), np.concatenate([h.numpy() for h in one[0]]))
+    finally:
+        st.plan.close()
+    seq = runner.make(w)
+    try:
+        with pytest.raises(D.DttError) as e:
+            seq.plan.allgather_host_rounds([_host_slices(w, 1)], None, 0, seq.producer_stream)
+        assert e.value.code == D.EINVAL
+    finally:
+        seq.plan.close()
+
+
+def test_host_rounds_c2_full_size():
+    # the benchmark's c2 launch from and to host memory, five rounds pipelined
+    w = W.C2
+    st = runner.make(w, **_launch(w, "bench", {}))
+    n = 5
+    host = [_host_slices(w, R) for R in range(1, n + 1)]
+    outs = [torch.zeros(w.buf_bytes, dtype=torch.uint8).pin_memory() for _ in range(n)]
+    try:
+        reps = st.plan.allgather_host_rounds(host, outs, 0, st.producer_stream)
+        assert all(r.status == D.OK for r in reps)
+        for k in range(n):
+            want = torch.cat(host[k])
+            assert torch.equal(outs[k], want), f"round {k + 1}"
+    finally:
+        st.plan.close()
