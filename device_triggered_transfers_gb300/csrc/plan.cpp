@@ -1984,9 +1984,11 @@ int dtt_allgather_host_rounds(dtt_plan* p, uint32_t n_rounds, const void* const*
             hi[c] -= base;
         }
     }
-    const uint64_t kPiece = p->opts.host_piece_bytes
-                                ? p->opts.host_piece_bytes
-                                : std::max<uint64_t>(4ull << 20, (S / 4 + 4095) & ~uint64_t(4095));
+    // a whole slice per copy unless asked otherwise: the rounds overlap one another, so a round
+    // needs no finer pieces, and larger copies move faster over the host link (c2: 436 GB/s with
+    // 8 MiB pieces, 476 GB/s with whole 32 MiB slices)
+    const uint64_t kPiece = p->opts.host_piece_bytes ? p->opts.host_piece_bytes
+                                                     : std::max<uint64_t>(4ull << 20, (S + 4095) & ~uint64_t(4095));
     std::vector<HostRound> rounds(n_rounds);
     for (uint32_t k = 0; k < n_rounds; ++k) {
         HostRound& x = rounds[k];

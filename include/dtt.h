@@ -228,7 +228,8 @@ typedef struct dtt_plan_opts {
     uint32_t time_copier;    /* 1: time every copier launch with CUDA events on the copy
                                 stream (read with dtt_plan_stats) */
     uint32_t host_piece_bytes;/* dtt_allgather_host: bytes per host-to-device copy (a multiple
-                                of 4096); 0 = a quarter of a slice, at least 4 MiB */
+                                of 4096); 0 = a quarter of a slice, at least 4 MiB (rounds back
+                                to back, dtt_allgather_host_rounds: 0 = a whole slice) */
     void* const* dst_bufs;    /* NULL: copies land in the P buffers themselves.  Else a host array
                                  of P device pointers, dst_bytes each: separate destination buffers
                                  (staging buffers) that every copy lands in, at its chunk's
