@@ -347,3 +347,13 @@ def test_overlap_options_are_checked_before_any_device_call():
         assert rc == D.EINVAL, over
         assert b"overlap" in D.lib().dtt_last_error()
     assert D.lib().dtt_plan_pending_round(None) == 0
+
+
+def test_new_entry_points_refuse_a_null_plan_without_a_gpu():
+    L = D.lib()
+    rep = D.dtt_report()
+    slices = (C.c_void_p * 2)()
+    assert L.dtt_allgather_host_rounds(None, 1, slices, None, 0, None, C.byref(rep)) == D.EINVAL
+    assert L.dtt_plan_next_round(None) == D.EINVAL
+    assert L.dtt_plan_wait(None, C.byref(rep)) == D.EINVAL
+    assert L.dtt_plan_pending_round(None) == 0
