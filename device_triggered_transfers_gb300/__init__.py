@@ -333,6 +333,64 @@ def dtt_schedule_empty() -> Schedule:
     return Schedule(out.value)
 
 
+# ---- schedules from tensor slices, in the pages' form ---------------------------------------------
+# "Triggered Plans" (section Model) builds a rank's schedule from its own part of the output,
+# `mine`, a view into the output tensor `base`: whole(mine), chunks(mine, n, base=out) and
+# tile_chunks(mine, (BM, BN), tiles_per_chunk, order=..., base=out).  The functions below take
+# the same arguments (torch tensors) and turn them into the byte offset, row bytes and pitch of
+# the C builders; regions are relative to base's first byte.
+
+def _slice_geometry(mine, base):
+    """(offset of mine's first byte in base, rows, row bytes, pitch in bytes, element bytes, cols)
+    of a 1D or 2D view `mine` whose rows are contiguous."""
+    e = mine.element_size()
+    if mine.dim() == 1:
+        rows, cols, pitch = 1, mine.shape[0], mine.shape[0] * e
+        if mine.shape[0] and mine.stride(0) != 1:
+            raise DttError(EINVAL, "schedule: a 1D slice must be contiguous")
+    elif mine.dim() == 2:
+        rows, cols = mine.shape
+        if cols > 1 and mine.stride(1) != 1:
+            raise DttError(EINVAL, "schedule: a slice's rows must be contiguous")
+        pitch = mine.stride(0) * e if rows > 1 else cols * e
+    else:
+        raise DttError(EINVAL, "schedule: the slice must be 1D or 2D")
+    off = 0
+    if base is not None:
+        off = mine.data_ptr() - base.data_ptr()
+        if off < 0 or off + max(0, rows - 1) * pitch + cols * e > base.numel() * base.element_size():
+            raise DttError(EINVAL, "schedule: the slice lies outside base")
+    return off, rows, cols * e, pitch, e, cols
+
+
+def whole(mine, num_programs: int = 1, base=None) -> Schedule:
+    """One chunk holding all of `mine`, marked once by each of num_programs programs at their end."""
+    off, rows, rb, pitch, _, _ = _slice_geometry(mine, base)
+    return dtt_schedule_whole(off, rows, rb, pitch, num_programs)
+
+
+def chunks(mine, n: int, base=None) -> Schedule:
+    """Row blocks of `mine` completed in order, one writer each."""
+    off, rows, rb, pitch, _, _ = _slice_geometry(mine, base)
+    return dtt_schedule_chunks(off, rows, rb, pitch, n)
+
+
+def tile_chunks(mine, tile, tiles_per_chunk: int, order=None, base=None) -> Schedule:
+    """Consecutive (BM, BN) tiles of a tiled producer over `mine`, tiles_per_chunk steps per chunk.
+    order: None (row-major), ("grouped", GROUP_M) (the library's grouped order), or a callable
+    step -> (tm, tn), the producer's own mapping."""
+    off, rows, _, pitch, e, cols = _slice_geometry(mine, base)
+    BM, BN = tile
+    if order is None:
+        return dtt_schedule_tile_chunks(off, rows, cols, e, pitch, BM, BN, tiles_per_chunk)
+    if isinstance(order, tuple) and len(order) == 2 and order[0] == "grouped":
+        return dtt_schedule_tile_chunks(off, rows, cols, e, pitch, BM, BN, tiles_per_chunk,
+                                        ORDER_GROUPED, int(order[1]))
+    if callable(order):
+        return dtt_schedule_tile_chunks(off, rows, cols, e, pitch, BM, BN, tiles_per_chunk, order_fn=order)
+    raise DttError(EINVAL, "tile_chunks: order is None, ('grouped', GROUP_M) or a callable")
+
+
 def dtt_tile_of(order_kind, group_m, step, tiles_m, tiles_n):
     tm, tn = _u32(), _u32()
     order = dtt_order(order_kind, group_m)
@@ -549,6 +607,43 @@ class Plan:
 
 def dtt_plan_create(bufs, buf_bytes, schedules, opts=None, copy_stream=None) -> Plan:
     return Plan(bufs, buf_bytes, schedules, opts, copy_stream)
+
+
+class TriggeredPlan(Plan):
+    """The pages' TriggeredPlan(ctx, out, schedules) for P virtual ranks: `outs` is the list of
+    the P ranks' output tensors (one size), `schedules` one schedule per rank built from slices of
+    them (whole / chunks / tile_chunks with base=outs[r]).  free_schedules: free the schedules once
+    the plan has taken its own copy (the default)."""
+
+    def __init__(self, outs: Sequence, schedules: Sequence[Optional[Schedule]], opts=None,
+                 copy_stream=None, allgather: bool = False, free_schedules: bool = True):
+        nbytes = [t.numel() * t.element_size() for t in outs]
+        if len(set(nbytes)) != 1:
+            raise DttError(EINVAL, "TriggeredPlan: the P outputs have one size")
+        opts = dtt_plan_opts.from_buffer_copy(opts) if opts is not None else dtt_plan_opts_default()
+        opts.allgather = 1 if allgather else 0
+        super().__init__(list(outs), nbytes[0], schedules, opts, copy_stream=copy_stream)
+        self.outs = list(outs)
+        if free_schedules:
+            for sc in schedules:
+                if sc is not None:
+                    sc.free()
+
+
+def prepare_all_gather(outs: Sequence, schedules: Optional[Sequence[Optional[Schedule]]] = None, opts=None,
+                       copy_stream=None) -> TriggeredPlan:
+    """The pages' ctx.ccl.prepare_all_gather(out, schedule) for P virtual ranks: an in-place
+    all-gather plan over the P outputs whose rank r owns rows [r*M, (r+1)*M) of its output (M =
+    rows / P, the outputs seen as 2D [rows, ...] tensors), checking that each schedule stays inside
+    its rank's rows.  schedules None: whole() of each rank's rows, as on the pages."""
+    P = len(outs)
+    if schedules is None:
+        schedules = []
+        for r, out in enumerate(outs):
+            o2 = out if out.dim() == 2 else out.reshape(out.shape[0], -1)
+            M = o2.shape[0] // P
+            schedules.append(whole(o2[r * M:(r + 1) * M], 1, base=out))
+    return TriggeredPlan(outs, schedules, opts, copy_stream, allgather=True)
 
 
 # ---- producers and barriers -----------------------------------------------------------------

@@ -446,3 +446,34 @@ def test_paced_producer_that_cannot_be_resident_is_rejected():
         assert e.value.code == D.EINVAL
     finally:
         st.plan.close()
+
+
+def test_prepare_all_gather_in_the_pages_form():
+    # "Triggered Plans", section Model: schedules from each rank's own rows of its output (whole
+    # by default, or chunks(mine, n, base=out)), the plan checking that they stay inside them; the
+    # round's data (written here by the host, marked by dtt_publish) ends up everywhere
+    P, M, N = 4, 64, 256
+    outs = [torch.zeros(P * M, N, dtype=torch.bfloat16, device="cuda") for _ in range(P)]
+    for scheds in (None, [D.chunks(outs[r][r * M:(r + 1) * M], 4, base=outs[r]) for r in range(P)]):
+        plan = D.prepare_all_gather(outs, scheds)
+        prod = torch.cuda.Stream()
+        try:
+            for R in (1, 2):
+                h = plan.start(prod)
+                with torch.cuda.stream(prod):
+                    for r in range(P):
+                        outs[r][r * M:(r + 1) * M] = float(10 * R + r)
+                n_global = plan.info()[0]
+                D.dtt_publish(h, 0, n_global, 0, prod)
+                assert plan.wait().status == D.OK
+                want = torch.cat([torch.full((M, N), float(10 * R + r), dtype=torch.bfloat16) for r in range(P)])
+                for q in range(P):
+                    assert torch.equal(outs[q].cpu(), want), (R, q)
+                plan.next_round()
+        finally:
+            plan.close()
+    # a schedule reaching into another rank's rows is refused at creation
+    bad = [D.chunks(outs[r][0:2 * M], 2, base=outs[r]) for r in range(P)]
+    with pytest.raises(D.DttError) as e:
+        D.prepare_all_gather(outs, bad)
+    assert e.value.code in (D.EOUTOFROWS, D.EOVERLAP)

@@ -357,3 +357,30 @@ def test_new_entry_points_refuse_a_null_plan_without_a_gpu():
     assert L.dtt_plan_next_round(None) == D.EINVAL
     assert L.dtt_plan_wait(None, C.byref(rep)) == D.EINVAL
     assert L.dtt_plan_pending_round(None) == 0
+
+
+def test_schedules_from_tensor_slices_match_the_offset_builders():
+    # the pages' form -- whole(mine), chunks(mine, n, base=out), tile_chunks(mine, (BM, BN), T,
+    # order=..., base=out) -- gives the same regions as the offset-based builders
+    import torch
+    P, M, N = 4, 96, 160
+    out = torch.zeros(P * M, N, dtype=torch.bfloat16)
+    rb = N * 2
+    for r in (0, 2, 3):
+        mine = out[r * M:(r + 1) * M]
+        assert _regions(D.chunks(mine, 5, base=out)) == _regions(D.dtt_schedule_chunks(r * M * rb, M, rb, rb, 5))
+        assert _regions(D.whole(mine, 3, base=out)) == _regions(D.dtt_schedule_whole(r * M * rb, M, rb, rb, 3))
+        got = D.tile_chunks(mine, (32, 48), 4, order=("grouped", 2), base=out)
+        want = D.dtt_schedule_tile_chunks(r * M * rb, M, N, 2, rb, 32, 48, 4, D.ORDER_GROUPED, 2)
+        assert _regions(got) == _regions(want)
+        tm, tn = -(-M // 32), -(-N // 48)
+        fn = lambda s: D.dtt_tile_of(D.ORDER_GROUPED, 2, s, tm, tn)   # the producer's own mapping
+        assert _regions(D.tile_chunks(mine, (32, 48), 4, order=fn, base=out)) == _regions(want)
+    # a column window: strided rows, pitch = the full row
+    win = out[M:2 * M, 32:96]
+    assert _regions(D.chunks(win, 3, base=out)) == \
+        _regions(D.dtt_schedule_chunks(M * rb + 64, M, 128, rb, 3))
+    with pytest.raises(D.DttError):
+        D.chunks(out.t()[:, :8], 2, base=out)          # rows not contiguous
+    with pytest.raises(D.DttError):
+        D.chunks(torch.zeros(8, 8, dtype=torch.bfloat16), 2, base=out)   # not inside base
