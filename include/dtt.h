@@ -427,7 +427,8 @@ int dtt_plan_wait(dtt_plan* plan, dtt_report* report);
  * (the round is already 2^32 - 1; the state is unchanged), DTT_ECUDA. */
 int dtt_plan_next_round(dtt_plan* plan);
 
-/* The round in flight behind the current one (opts.overlap), or 0 when none is. */
+/* The round in flight behind the current one (opts.overlap: "Triggered Plans", Not supported
+ * yet, "Overlapping rounds"), or 0 when none is (and for a NULL plan). */
 uint32_t dtt_plan_pending_round(const dtt_plan* plan);
 
 /* Close the plan ("Triggered Plans", The kernel author's contract, close()).  In the middle of
@@ -519,7 +520,8 @@ int dtt_allgather_host(dtt_plan* plan, const void* const* host_slices, void* hos
                        uint32_t out_rank, cudaStream_t stream, dtt_report* report);
 
 /* Host-buffer all-gather over n_rounds rounds back to back, pipelined across rounds (a plan made
- * with opts.overlap): each round as dtt_allgather_host, but round k + 1's slices start going in
+ * with opts.overlap; like dtt_allgather_host, this library's own addition: the pages move device
+ * data only, and this call feeds a plan's rounds from host memory): each round as dtt_allgather_host, but round k + 1's slices start going in
  * while round k's gathered buffer is still coming back, so the host link carries both directions
  * nearly all the time.  Round k + 1's bytes of a slice go in only once round k has delivered the
  * chunks they overwrite (the copier's arrival stamps in mapped host memory, polled here) and, in
