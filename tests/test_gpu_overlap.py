@@ -679,3 +679,55 @@ def test_host_rounds_c2_full_size():
             assert torch.equal(outs[k], want), f"round {k + 1}"
     finally:
         st.plan.close()
+
+
+@pytest.mark.parametrize("method", [0, 1, 2], ids=["vector", "bulk", "copy_engines"])
+def test_overlap_close_and_wait_states(method):
+    # close right after next_round (the next round PREPARED, this one pending), a second wait with
+    # nothing left to check, and close with two rounds in flight on every transport
+    w = W.small(W.C2, P=2, M=64, N=256, num_chunks=2, rounds=2)
+    extra = dict(piece_bytes=16384, stages=2) if method == 1 else {}
+    st = runner.make(w, opts=_opts(method=method, **extra))
+    try:
+        h = st.plan.start(st.producer_stream)
+        D.dtt_fill_producer(st.buf_ptrs, st.desc, h, st.producer_stream)
+        st.plan.next_round()
+        assert st.plan.state == D.PREPARED and st.plan.pending == 1
+        rep = st.plan.wait()                  # round 1, with round 2 not started
+        assert rep.status == D.OK and rep.round == 1
+        assert st.plan.state == D.PREPARED and st.plan.pending == 0
+        with pytest.raises(D.DttError) as e:
+            st.plan.wait()                    # nothing running, nothing pending
+        assert e.value.code == D.ESTATE
+        want = OP.expected_allgather(w.P, w.M, w.N, w.dtype, w.seed, 1, w.elem_bytes)
+        for q in range(w.P):
+            np.testing.assert_array_equal(st.bufs[q].cpu().numpy(), want)
+        h = st.plan.start(st.producer_stream)
+        D.dtt_fill_producer(st.buf_ptrs, st.desc, h, st.producer_stream)
+        st.plan.next_round()                  # round 2 pending, round 3 PREPARED
+    finally:
+        assert st.plan.close() == D.OK        # the pending round drains
+    st = runner.make(w, opts=_opts(method=method, **extra))
+    try:
+        h = st.plan.start(st.producer_stream)
+        D.dtt_fill_producer(st.buf_ptrs, st.desc, h, st.producer_stream)
+        st.plan.next_round()
+        st.plan.start(st.producer_stream)     # round 2 running with no producer: close opens it
+    finally:
+        assert st.plan.close() == D.OK
+
+
+def test_overlap_with_copier_timing():
+    # the copier timed by the library's events on overlapped rounds: one timed launch per round
+    w = W.small(W.C2, M=128, N=512, num_chunks=4, rounds=6)
+    st = runner.make(w, opts=_opts(time_copier=1))
+    try:
+        reps = runner.run_overlapped(st, w.rounds)
+        assert [r.status for r in reps] == [D.OK] * w.rounds
+        last, total, n = st.plan.stats()
+        assert n == w.rounds and total >= last > 0
+        want = OP.expected_allgather(w.P, w.M, w.N, w.dtype, w.seed, w.rounds, w.elem_bytes)
+        for q in range(w.P):
+            np.testing.assert_array_equal(st.bufs[q].cpu().numpy(), want)
+    finally:
+        st.plan.close()
