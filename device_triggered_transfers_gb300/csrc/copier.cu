@@ -566,26 +566,29 @@ __global__ void force_open_kernel(uint64_t* gates, const ChunkDesc* chunks, uint
     }
 }
 
-// The copy-engine transport's ATOMIC step: stream-ordered after every copy of chunk c to every
-// peer (so those bytes are visible to this kernel), one thread signals as the SM copier does.
+// The copy-engine transport's ATOMIC step: stream-ordered after every copy of the run of chunks
+// [c, c_end) to every peer (so those bytes are visible to this kernel), one thread signals each
+// chunk of the run, in order, as the SM copier does.
 __global__ void ce_signal_kernel(const __grid_constant__ CeSignalParams p) {
     if (threadIdx.x != 0) return;
     dtt_dev::fence_acq_rel();
-    for (uint32_t q = 0; q < p.P; ++q) {
-        if (!((p.peers >> q) & 1u)) continue;
-        uint64_t* prow = p.gates + ((uint64_t)q * p.n_global + p.c) * DTT_GATE_WORDS;
-        if (p.flags & DTT_HANDLE_TIMESTAMPS) dtt_dev::st_relaxed(prow + DTT_GATE_T_ARRIVE, dtt_dev::globaltimer());
-        dtt_dev::red_relaxed_add(prow + DTT_GATE_ARRIVAL, 1);
-        if (p.groups.counters) {
-            uint64_t* grow = p.groups.counters + (uint64_t)q * p.groups.n_groups;
-            for (uint32_t i = p.groups.chunk_off[p.c]; i < p.groups.chunk_off[p.c + 1]; ++i)
-                dtt_dev::red_relaxed_add(grow + p.groups.chunk_ids[i], 1);
+    for (uint32_t c = p.c; c < p.c_end; ++c) {
+        for (uint32_t q = 0; q < p.P; ++q) {
+            if (!((p.peers >> q) & 1u)) continue;
+            uint64_t* prow = p.gates + ((uint64_t)q * p.n_global + c) * DTT_GATE_WORDS;
+            if (p.flags & DTT_HANDLE_TIMESTAMPS) dtt_dev::st_relaxed(prow + DTT_GATE_T_ARRIVE, dtt_dev::globaltimer());
+            dtt_dev::red_relaxed_add(prow + DTT_GATE_ARRIVAL, 1);
+            if (p.groups.counters) {
+                uint64_t* grow = p.groups.counters + (uint64_t)q * p.groups.n_groups;
+                for (uint32_t i = p.groups.chunk_off[c]; i < p.groups.chunk_off[c + 1]; ++i)
+                    dtt_dev::red_relaxed_add(grow + p.groups.chunk_ids[i], 1);
+            }
         }
+        uint64_t* row = p.gates + ((uint64_t)p.s * p.n_global + c) * DTT_GATE_WORDS;
+        dtt_dev::red_relaxed_add(row + DTT_GATE_COMPLETION, p.receivers);
+        if (p.host_arrived)
+            asm volatile("st.release.sys.global.u32 [%0], %1;" ::"l"(p.host_arrived + c), "r"(p.round) : "memory");
     }
-    uint64_t* row = p.gates + ((uint64_t)p.s * p.n_global + p.c) * DTT_GATE_WORDS;
-    dtt_dev::red_relaxed_add(row + DTT_GATE_COMPLETION, p.receivers);
-    if (p.host_arrived)
-        asm volatile("st.release.sys.global.u32 [%0], %1;" ::"l"(p.host_arrived + p.c), "r"(p.round) : "memory");
 }
 
 struct PublishParams {

@@ -186,7 +186,8 @@ struct CeSignalParams {
     dtt_group_table groups;
     uint32_t* host_arrived;     // or null
     uint32_t P, n_global, s, c, round, flags;
-    uint32_t peers, receivers;  // the chunk's receiving ranks
+    uint32_t peers, receivers;  // the chunks' receiving ranks
+    uint32_t c_end;             // the run of chunks [c, c_end) of source s, copied together
 };
 cudaError_t launch_ce_signal(const CeSignalParams& p, cudaStream_t s);
 cudaError_t launch_consumer(const CopierParams& p, dtt_handle h, char* dst, uint64_t max_polls,

@@ -545,26 +545,52 @@ bool claim_early(dtt_plan* p) {
 }
 
 // ---- the copy-engine transport (opts.method = DTT_COPY_ENGINE) -----------------------------------
-// Issue chunk c of source s: every region to every peer on the (s, q) queue, then -- once all of
-// them have landed (the other queues' events joined onto the last one) -- the signal kernel.
-int ce_issue(dtt_plan* p, uint32_t s, uint32_t c, uint32_t round) {
+// Chunk c's bytes as one contiguous range (source offset, destination offset, length), or a zero
+// length when its regions are not one contiguous range on both sides.
+struct CeRange {
+    uint64_t src, dst, len;
+};
+
+CeRange ce_range(const CeProxy& ce, uint32_t c) {
+    if (ce.reg_begin[c + 1] - ce.reg_begin[c] != 1) return {0, 0, 0};
+    const dtt_region& r = ce.regs[ce.reg_begin[c]];
+    const dtt_dest& d = ce.dests[ce.reg_begin[c]];
+    if (r.rows != 1 && (r.pitch != r.row_bytes || d.pitch != r.row_bytes)) return {0, 0, 0};
+    return {r.offset, d.offset, r.rows * r.row_bytes};
+}
+
+// Issue the run of chunks [c, c_end) of source s (one chunk, or consecutive chunks whose bytes
+// follow each other on both sides, so that one copy per peer moves them all): every region to
+// every peer on the (s, q) queue, then -- once all of them have landed (the other queues'
+// events joined onto the last one) -- one signal kernel for the run.
+int ce_issue(dtt_plan* p, uint32_t s, uint32_t c, uint32_t c_end, uint32_t round) {
     CeProxy& ce = *p->ce;
     const uint32_t P = p->P;
     uint32_t last = UINT32_MAX;
     const uint32_t peers = p->chunks[c].peers;
+    CeRange run{0, 0, 0};
+    if (c_end > c + 1) {
+        run = ce_range(ce, c);
+        run.len = ce_range(ce, c_end - 1).src + ce_range(ce, c_end - 1).len - run.src;
+    }
     for (uint32_t q = 0; q < P; ++q) {
         if (!((peers >> q) & 1u)) continue;
         cudaStream_t st = ce.streams[s * P + q];
-        for (uint32_t i = ce.reg_begin[c]; i < ce.reg_begin[c + 1]; ++i) {
-            const dtt_region& r = ce.regs[i];
-            const dtt_dest& d = ce.dests[i];
-            if (r.rows == 0 || r.row_bytes == 0) continue;
-            if (r.rows == 1)
-                DTT_CUDA_TRY(cudaMemcpyAsync(p->dst[q] + d.offset, p->bufs[s] + r.offset, r.row_bytes,
-                                             cudaMemcpyDeviceToDevice, st));
-            else
-                DTT_CUDA_TRY(cudaMemcpy2DAsync(p->dst[q] + d.offset, d.pitch, p->bufs[s] + r.offset, r.pitch,
-                                               r.row_bytes, r.rows, cudaMemcpyDeviceToDevice, st));
+        if (run.len) {
+            DTT_CUDA_TRY(cudaMemcpyAsync(p->dst[q] + run.dst, p->bufs[s] + run.src, run.len,
+                                         cudaMemcpyDeviceToDevice, st));
+        } else {
+            for (uint32_t i = ce.reg_begin[c]; i < ce.reg_begin[c_end]; ++i) {
+                const dtt_region& r = ce.regs[i];
+                const dtt_dest& d = ce.dests[i];
+                if (r.rows == 0 || r.row_bytes == 0) continue;
+                if (r.rows == 1)
+                    DTT_CUDA_TRY(cudaMemcpyAsync(p->dst[q] + d.offset, p->bufs[s] + r.offset, r.row_bytes,
+                                                 cudaMemcpyDeviceToDevice, st));
+                else
+                    DTT_CUDA_TRY(cudaMemcpy2DAsync(p->dst[q] + d.offset, d.pitch, p->bufs[s] + r.offset, r.pitch,
+                                                   r.row_bytes, r.rows, cudaMemcpyDeviceToDevice, st));
+            }
         }
         last = q;
     }
@@ -583,12 +609,24 @@ int ce_issue(dtt_plan* p, uint32_t s, uint32_t c, uint32_t round) {
     sp.n_global = p->n_global;
     sp.s = s;
     sp.c = c;
+    sp.c_end = c_end;
     sp.round = round;
     sp.flags = p->opts.timestamps ? DTT_HANDLE_TIMESTAMPS : 0u;
     sp.peers = peers;
     sp.receivers = p->chunks[c].receivers;
     DTT_CUDA_TRY(launch_ce_signal(sp, sl));
     return DTT_OK;
+}
+
+// May chunk c join the run ending with chunk c - 1 of the same source: the same receivers, and
+// its bytes right after the run's on both sides?  Runs stop at kCeRunBytes, so that the first
+// chunk of a run is not signalled too long after it landed.
+constexpr uint64_t kCeRunBytes = 64ull << 20;
+
+bool ce_joins(const dtt_plan* p, const CeProxy& ce, uint32_t c, uint64_t run_bytes) {
+    if (p->chunks[c].peers != p->chunks[c - 1].peers) return false;
+    const CeRange a = ce_range(ce, c - 1), b = ce_range(ce, c);
+    return a.len && b.len && b.src == a.src + a.len && b.dst == a.dst + a.len && run_bytes + b.len <= kCeRunBytes;
 }
 
 // One round on the proxy thread: every source's chunks in schedule order, each as soon as its
@@ -611,13 +649,22 @@ int ce_run_round(dtt_plan* p, uint32_t round) {
         for (uint32_t s = 0; s < P; ++s) {
             while (next[s] < end[s]) {
                 const uint32_t c = next[s];
-                const bool open = __atomic_load_n(&ce.h_ready[c], __ATOMIC_ACQUIRE) >= round ||
-                                  ce.open_all.load(std::memory_order_acquire);
-                if (!open) break;                 // head of line: this source's later chunks wait
-                const int rc = ce_issue(p, s, c, round);
+                auto is_open = [&](uint32_t x) {
+                    return __atomic_load_n(&ce.h_ready[x], __ATOMIC_ACQUIRE) >= round ||
+                           ce.open_all.load(std::memory_order_acquire);
+                };
+                if (!is_open(c)) break;           // head of line: this source's later chunks wait
+                // the open chunks right behind it whose bytes follow on go in the same copies
+                uint32_t c_end = c + 1;
+                uint64_t run_bytes = ce_range(ce, c).len;
+                while (c_end < end[s] && is_open(c_end) && ce_joins(p, ce, c_end, run_bytes)) {
+                    run_bytes += ce_range(ce, c_end).len;
+                    ++c_end;
+                }
+                const int rc = ce_issue(p, s, c, c_end, round);
                 if (rc != DTT_OK) return rc;
-                ++next[s];
-                --remaining;
+                remaining -= c_end - c;
+                next[s] = c_end;
                 progress = true;
             }
         }

@@ -81,7 +81,9 @@ enum {
                               (POLL_REGMEM), issues one cudaMemcpyAsync / cudaMemcpy2DAsync per
                               region and peer on one stream per (source, peer) queue (COPY), and
                               once the chunk's copies to every peer are done a one-warp kernel adds
-                              its arrivals, group counts and completion (ATOMIC).  Each source
+                              its arrivals, group counts and completion (ATOMIC).  Consecutive open
+                              chunks of a source whose bytes follow each other on both sides (up to
+                              64 MiB) go as one copy per peer and one signal kernel.  Each source
                               byte is read once per peer.  dtt_allgather_host needs an SM copier. */
 };
 
