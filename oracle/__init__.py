@@ -30,6 +30,12 @@ Modules and what pins each (see the test files named):
 * ``barrier``   hand-rolled notify/wait barrier and the builtin reveal, plus the Set/Eq
   shared-cell pitfall.  Pinned by the page's golden values (tests/golden/barrier_p*.txt).
 * ``gemm``      fp64 product of the bf16 operands and the relative Frobenius error.  Pinned by
-  brute force on tiny inputs and closed forms (tests/test_oracle_gemm.py).
+  brute force on tiny inputs and closed forms (tests/test_oracle_barrier_gemm.py).
+* ``allreduce`` the two-shot all-reduce ("Triggered Plans", Not supported yet, names it): the
+  sum in f32 in rank order, rounded once (a reading: the pages fix no precision), and the
+  protocol of a reduce-scatter plan, the reduce step and an all-gather plan on the ``plan``
+  model.  Pinned by hand-worked sums (tests/golden/allreduce_sums.txt), closed forms, the f32
+  summation error bound against the exact sum, a brute-force bf16 rounding check and the
+  protocol against the definition (tests/test_oracle_allreduce.py).
 """
-from . import hashfill, schedule, plan, barrier, gemm  # noqa: F401
+from . import hashfill, schedule, plan, barrier, gemm, allreduce  # noqa: F401
