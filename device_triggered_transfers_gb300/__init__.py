@@ -104,6 +104,12 @@ class dtt_fill_desc(C.Structure):
                 ("group_counters", C.c_void_p)]
 
 
+class dtt_allreduce_desc(C.Structure):
+    _fields_ = [("dtype", C.c_uint32), ("sub_blocks", C.c_uint32), ("block_rows", C.c_uint64),
+                ("cols", C.c_uint64), ("pitch", C.c_uint64), ("reduce_ctas", C.c_uint32),
+                ("reduce_threads", C.c_uint32)]
+
+
 ORDER_FN = C.CFUNCTYPE(C.c_int, C.c_uint64, C.c_void_p, C.POINTER(C.c_uint32),
                        C.POINTER(C.c_uint32))
 
@@ -155,6 +161,15 @@ _SIGS = {
     "dtt_gemm_producer": (C.c_int, [_P, _P, C.POINTER(_P), _u32, _u32, _u32, _u32, _u64,
                                     C.POINTER(_u64), _u32, C.POINTER(dtt_handle), _P, _P]),
     "dtt_consumer_gather": (C.c_int, [_P, _u32, _P, _u64, _P, _u32, _P]),
+    "dtt_allreduce_create": (C.c_int, [C.POINTER(_P), _u64, C.POINTER(_P), _u64, _u32,
+                                       C.POINTER(dtt_allreduce_desc), C.POINTER(dtt_plan_opts),
+                                       C.POINTER(dtt_plan_opts), _P, _P, C.POINTER(_P)]),
+    "dtt_allreduce_plans": (C.c_int, [_P, C.POINTER(_P), C.POINTER(_P)]),
+    "dtt_allreduce_start": (C.c_int, [_P, _P, C.POINTER(dtt_handle)]),
+    "dtt_allreduce_reduce": (C.c_int, [_P, _P, _P]),
+    "dtt_allreduce_wait": (C.c_int, [_P, C.POINTER(dtt_report), C.POINTER(dtt_report)]),
+    "dtt_allreduce_next_round": (C.c_int, [_P]),
+    "dtt_allreduce_destroy": (C.c_int, [_P]),
     "dtt_barrier_handrolled": (C.c_int, [C.POINTER(_P), C.POINTER(_P), _u32, _u32, _u64, _P, _P]),
     "dtt_barrier_create": (C.c_int, [_u32, C.POINTER(_P)]),
     "dtt_barrier_destroy": (None, [_P]),
@@ -644,6 +659,100 @@ def prepare_all_gather(outs: Sequence, schedules: Optional[Sequence[Optional[Sch
             M = o2.shape[0] // P
             schedules.append(whole(o2[r * M:(r + 1) * M], 1, base=out))
     return TriggeredPlan(outs, schedules, opts, copy_stream, allgather=True)
+
+
+# ---- two-shot all-reduce --------------------------------------------------------------------
+class PlanView(Plan):
+    """A plan owned by something else (an all-reduce's two plans): the read calls of Plan
+    (info, read_gates, read_group_counters, stats), never closed from here."""
+
+    def __init__(self, handle: C.c_void_p, bufs: Sequence, buf_bytes: int, n_groups: int = 0):
+        self._h = handle
+        self.bufs = list(bufs)
+        self.P = len(self.bufs)
+        self.buf_bytes = buf_bytes
+        self.n_groups = n_groups
+
+    def close(self) -> int:
+        return OK
+
+    def __del__(self):
+        pass
+
+
+class AllReduce:
+    """Owner of a dtt_allreduce*: the two-shot all-reduce over P device buffers (see
+    dtt_allreduce_create).  Rank r's vector is P * block_rows rows of `cols` elements of `dtype`
+    at the start of bufs[r]; every rank ends with the sum of the P vectors there.  A round:
+    start() -> handles for the producers' reduce-scatter marks, the producers, reduce(), wait(),
+    next_round()."""
+
+    def __init__(self, bufs: Sequence, buf_bytes: int, dtype: str, block_rows: int, cols: int,
+                 sub_blocks: int = 1, pitch: int = 0, staging: Optional[Sequence] = None,
+                 staging_bytes: int = 0, rs_opts: Optional[dtt_plan_opts] = None,
+                 ag_opts: Optional[dtt_plan_opts] = None, reduce_ctas: int = 0, reduce_threads: int = 0,
+                 rs_copy_stream=None, ag_copy_stream=None):
+        self.bufs = list(bufs)
+        self.P = len(self.bufs)
+        self.staging = list(staging) if staging is not None else None
+        if self.staging is not None and len(self.staging) != self.P:
+            raise DttError(EINVAL, "AllReduce: one staging buffer per rank")
+        self.buf_bytes, self.dtype = buf_bytes, dtype
+        self.block_rows, self.cols, self.sub_blocks = block_rows, cols, sub_blocks
+        d = dtt_allreduce_desc()
+        d.dtype = DTYPE_CODES[dtype]
+        d.sub_blocks, d.block_rows, d.cols, d.pitch = sub_blocks, block_rows, cols, pitch
+        d.reduce_ctas, d.reduce_threads = reduce_ctas, reduce_threads
+        self.desc = d
+        out = C.c_void_p()
+        stg = _ptr_array(self.staging) if self.staging is not None else None
+        _check(lib().dtt_allreduce_create(_ptr_array(self.bufs), buf_bytes, stg, staging_bytes, self.P,
+                                          C.byref(d), C.byref(rs_opts) if rs_opts is not None else None,
+                                          C.byref(ag_opts) if ag_opts is not None else None,
+                                          _stream(rs_copy_stream), _stream(ag_copy_stream), C.byref(out)))
+        self._h = out
+        self.handles = (dtt_handle * self.P)()
+        rs, ag = C.c_void_p(), C.c_void_p()
+        _check(lib().dtt_allreduce_plans(self._h, C.byref(rs), C.byref(ag)))
+        self.rs = PlanView(rs, self.bufs, buf_bytes, n_groups=self.P * sub_blocks)
+        self.ag = PlanView(ag, self.bufs, buf_bytes)
+
+    def start(self, producer_stream=None):
+        _check(lib().dtt_allreduce_start(self._h, _stream(producer_stream), self.handles))
+        return self.handles
+
+    def reduce(self, err, stream=None) -> None:
+        _check(lib().dtt_allreduce_reduce(self._h, _ptr(err), _stream(stream)))
+
+    def wait(self, raise_on_error: bool = True):
+        a, b = dtt_report(), dtt_report()
+        rc = lib().dtt_allreduce_wait(self._h, C.byref(a), C.byref(b))
+        if rc and raise_on_error:
+            _check(rc)
+        return a, b
+
+    def next_round(self) -> None:
+        _check(lib().dtt_allreduce_next_round(self._h))
+
+    def close(self) -> int:
+        if self._h and self._h.value:
+            rc = lib().dtt_allreduce_destroy(self._h)
+            self._h = C.c_void_p(0)
+            _check(rc)
+        return OK
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+        return False
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 # ---- producers and barriers -----------------------------------------------------------------

@@ -1,0 +1,519 @@
+// The two-shot all-reduce ("Triggered Plans", Not supported yet: reduce-scatter and two-shot
+// all-reduce are what other destinations make possible): a reduce-scatter plan whose chunks land
+// in staging slots of the block's owner, one kernel that waits for each sub-block's group, adds
+// the P parts in f32 in rank order and marks the sum for an in-place all-gather plan.
+//
+// One launch covers every virtual rank.  Its CTAs walk the sub-blocks (b, j) b-major -- the
+// order a producer writing its vector row by row completes them -- and each CTA takes the same
+// share of every sub-block's 16-byte vectors, so all of them work on one sub-block at a time
+// and the sub-block's all-gather copies can start while the next one is being added.
+#include <cstdint>
+#include <cstring>
+#include <new>
+#include <string>
+#include <vector>
+
+#include <cuda_bf16.h>
+
+#include "dtt_device.cuh"
+#include "internal.h"
+
+namespace dtt {
+namespace {
+
+struct ReduceParams {
+    char* bufs[DTT_MAX_RANKS];          // rank r's vector, from byte 0
+    const char* stage[DTT_MAX_RANKS];   // rank r's staging area (its buffer, or its staging buffer)
+    dtt_handle rs[DTT_MAX_RANKS];       // reduce-scatter plan, per rank
+    dtt_handle ag[DTT_MAX_RANKS];       // all-gather plan, per rank
+    uint64_t pitch;        // bytes between rows
+    uint64_t slot_off;     // slot 0 in each staging area
+    uint64_t slot_bytes;   // from one slot to the next: block_rows * pitch
+    uint64_t Mb, Mj;       // block rows, sub-block rows
+    uint64_t max_polls;    // of one group wait
+    uint32_t J;            // sub-blocks per block
+    uint32_t vrow;         // 16-byte vectors per row
+    uint32_t contig;       // rows back to back (pitch == vrow * 16): a sub-block is one range
+    uint32_t* counters;    // [P * J]: CTAs done with (b, j) this launch; zero between launches
+    uint32_t* err;         // group waits that ran out
+};
+
+// f32 lanes of a 16-byte vector, and the conversions (bf16 -> f32 is exact; f32 -> bf16 rounds
+// to nearest even).
+template <int DT> struct Lanes;
+template <> struct Lanes<DTT_BF16> {
+    static constexpr int n = 8;
+    static __device__ __forceinline__ void unpack(const uint4& v, float* f) {
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            f[2 * i] = __uint_as_float(w[i] << 16);
+            f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+        }
+    }
+    static __device__ __forceinline__ uint4 pack(const float* f) {
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const __nv_bfloat162 h = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+            w[i] = *reinterpret_cast<const uint32_t*>(&h);
+        }
+        return make_uint4(w[0], w[1], w[2], w[3]);
+    }
+};
+template <> struct Lanes<DTT_F32> {
+    static constexpr int n = 4;
+    static __device__ __forceinline__ void unpack(const uint4& v, float* f) {
+        f[0] = __uint_as_float(v.x);
+        f[1] = __uint_as_float(v.y);
+        f[2] = __uint_as_float(v.z);
+        f[3] = __uint_as_float(v.w);
+    }
+    static __device__ __forceinline__ uint4 pack(const float* f) {
+        return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
+                          __float_as_uint(f[3]));
+    }
+};
+
+__device__ __forceinline__ uint4 ld16(const char* p) { return *reinterpret_cast<const uint4*>(p); }
+__device__ __forceinline__ void st16(char* p, const uint4& v) { *reinterpret_cast<uint4*>(p) = v; }
+
+// P ranks known at compile time, so each thread's loads of a vector's parts (at most 8 at a
+// time, U vectors at once) are in flight together; the adds still go in rank order.
+template <int DT, int P>
+__global__ void __launch_bounds__(1024) reduce_kernel(const __grid_constant__ ReduceParams p) {
+    using E = Lanes<DT>;
+    constexpr int B = P < 8 ? P : 8;                 // parts loaded together
+    constexpr int U = P <= 2 ? 4 : (P <= 4 ? 2 : 1); // vectors a thread takes at once
+    const uint32_t G = gridDim.x;
+    const uint64_t per_unit = p.Mj * p.vrow;         // vectors in one sub-block
+    const uint64_t lo = per_unit * blockIdx.x / G, hi = per_unit * (blockIdx.x + 1) / G;
+    const uint64_t stride = (uint64_t)blockDim.x * U;
+
+    for (uint32_t b = 0; b < (uint32_t)P; ++b) {
+        for (uint32_t j = 0; j < p.J; ++j) {
+            const uint32_t u = b * p.J + j;          // the group (b, j), and its counter
+            if (dtt_wait_group(p.rs[b], u, p.max_polls) != 0) {
+                // this CTA stops: (b, j) and every later sub-block stay unmarked, so the
+                // all-gather plan's wait reports them short
+                if (dtt_dev::first_thread()) atomicAdd(p.err, 1u);
+                return;
+            }
+            const uint64_t first = (b * p.Mb + j * p.Mj) * p.pitch;   // the sub-block in the vector
+            const char* slot0 = p.stage[b] + p.slot_off + j * p.Mj * p.pitch;
+            char* own = p.bufs[b] + first;
+            for (uint64_t t0 = lo + threadIdx.x; t0 < hi; t0 += stride) {
+                uint64_t off[U];
+                bool in[U];
+#pragma unroll
+                for (int k = 0; k < U; ++k) {
+                    const uint64_t t = t0 + (uint64_t)k * blockDim.x;
+                    in[k] = t < hi;
+                    off[k] = p.contig ? t * 16 : (t / p.vrow) * p.pitch + (t % p.vrow) * 16;
+                }
+                float acc[U][E::n];
+#pragma unroll
+                for (int s0 = 0; s0 < P; s0 += B) {
+                    uint4 v[U][B] = {};   // lanes past the sub-block's end stay zero (never stored)
+#pragma unroll
+                    for (int k = 0; k < U; ++k)
+#pragma unroll
+                        for (int i = 0; i < B; ++i) {
+                            const uint32_t s = (uint32_t)(s0 + i);
+                            if (in[k] && s < (uint32_t)P)
+                                v[k][i] = ld16((s == b ? own : slot0 + s * p.slot_bytes) + off[k]);
+                        }
+#pragma unroll
+                    for (int k = 0; k < U; ++k)
+#pragma unroll
+                        for (int i = 0; i < B; ++i) {
+                            if (s0 + i >= P) continue;
+                            float f[E::n];
+                            E::unpack(v[k][i], f);
+#pragma unroll
+                            for (int e = 0; e < E::n; ++e) acc[k][e] = (s0 + i == 0) ? f[e] : acc[k][e] + f[e];
+                        }
+                }
+#pragma unroll
+                for (int k = 0; k < U; ++k)
+                    if (in[k]) st16(own + off[k], E::pack(acc[k]));
+            }
+            // One mark for (b, j): each CTA orders its stores before an acq_rel add; the CTA whose
+            // add completes the count has acquired every other CTA's stores, resets the counter
+            // for the next launch (stream-ordered after this one) and marks.
+            __syncthreads();
+            if (dtt_dev::first_thread()) {
+                uint32_t old;
+                asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(p.counters + u) : "memory");
+                if (old + 1 == G) {
+                    asm volatile("st.relaxed.gpu.global.u32 [%0], 0;" ::"l"(p.counters + u) : "memory");
+                    dtt_dev::mark_one(p.ag[b], p.ag[b].first_chunk + j);
+                }
+            }
+        }
+    }
+}
+
+using ReduceFn = void (*)(ReduceParams);
+
+// The instance for a dtype and P = 2 .. DTT_MAX_RANKS.
+template <int DT>
+ReduceFn reduce_for(uint32_t P) {
+    static_assert(DTT_MAX_RANKS == 16, "one instance per rank count");
+    switch (P) {
+        case 2: return reduce_kernel<DT, 2>;
+        case 3: return reduce_kernel<DT, 3>;
+        case 4: return reduce_kernel<DT, 4>;
+        case 5: return reduce_kernel<DT, 5>;
+        case 6: return reduce_kernel<DT, 6>;
+        case 7: return reduce_kernel<DT, 7>;
+        case 8: return reduce_kernel<DT, 8>;
+        case 9: return reduce_kernel<DT, 9>;
+        case 10: return reduce_kernel<DT, 10>;
+        case 11: return reduce_kernel<DT, 11>;
+        case 12: return reduce_kernel<DT, 12>;
+        case 13: return reduce_kernel<DT, 13>;
+        case 14: return reduce_kernel<DT, 14>;
+        case 15: return reduce_kernel<DT, 15>;
+        case 16: return reduce_kernel<DT, 16>;
+        default: return nullptr;
+    }
+}
+
+ReduceFn reduce_entry(uint32_t dtype, uint32_t P) {
+    return dtype == DTT_BF16 ? reduce_for<DTT_BF16>(P) : reduce_for<DTT_F32>(P);
+}
+
+}  // namespace
+
+cudaError_t preload_allreduce_kernels() {
+    for (uint32_t P = 2; P <= DTT_MAX_RANKS; ++P)
+        for (uint32_t dt : {(uint32_t)DTT_BF16, (uint32_t)DTT_F32}) {
+            const cudaError_t e = prepare_kernel(reduce_entry(dt, P));
+            if (e != cudaSuccess) return e;
+        }
+    return cudaSuccess;
+}
+
+}  // namespace dtt
+
+using namespace dtt;
+
+struct dtt_allreduce {
+    uint32_t P = 0;
+    dtt_allreduce_desc d{};
+    uint64_t Mj = 0, rb = 0, pitch = 0, slot_off = 0, slot_bytes = 0;
+    char* bufs[DTT_MAX_RANKS] = {};
+    char* stage[DTT_MAX_RANKS] = {};
+    dtt_plan* rs = nullptr;
+    dtt_plan* ag = nullptr;
+    uint32_t* d_counters = nullptr;
+    uint64_t max_polls = 0;
+};
+
+namespace {
+
+void release(dtt_allreduce* ar) {
+    if (!ar) return;
+    if (ar->rs) dtt_plan_close(ar->rs);
+    if (ar->ag) dtt_plan_close(ar->ag);
+    if (ar->d_counters) cudaFree(ar->d_counters);
+    delete ar;
+}
+
+struct ScheduleSet {
+    std::vector<dtt_schedule*> s;
+    ~ScheduleSet() {
+        for (dtt_schedule* x : s) dtt_schedule_free(x);
+    }
+};
+
+// The bulk-copy copier the all-reduce defaults to: two one-warp CTAs per SM, two 16 KiB stages
+// each -- light on registers and threads, so both plans' copiers and the reduce fit an SM.
+dtt_plan_opts default_opts() {
+    dtt_plan_opts o;
+    dtt_plan_opts_default(&o);
+    o.method = DTT_COPY_TMA;
+    o.ctas_per_sm = 2;
+    o.piece_bytes = 16384;
+    o.stages = 2;
+    return o;
+}
+
+int check_opts(const dtt_plan_opts& o, const char* which) {
+    if (o.method == DTT_COPY_ENGINE)
+        return fail(DTT_EINVAL, "dtt_allreduce_create: the %s plan cannot use the copy-engine transport", which);
+    if (o.deferred_copier || o.overlap)
+        return fail(DTT_EINVAL, "dtt_allreduce_create: the %s plan's copier runs from start, rounds one at a time "
+                                "(deferred_copier and overlap must be 0)", which);
+    return DTT_OK;
+}
+
+// The reduce kernel's CTAs beside both copiers' on one SM.
+int check_room(const dtt_allreduce* ar) {
+    CopierRoom a, b;
+    int rc = plan_copier_room(ar->rs, &a);
+    if (rc == DTT_OK) rc = plan_copier_room(ar->ag, &b);
+    if (rc != DTT_OK) return rc;
+    int dev = 0, sms = 0, thr = 0, regs = 0, smem = 0, reserved = 0, blocks = 0;
+    cudaFuncAttributes fa{};
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&thr, cudaDevAttrMaxThreadsPerMultiProcessor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&regs, cudaDevAttrMaxRegistersPerMultiprocessor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&blocks, cudaDevAttrMaxBlocksPerMultiprocessor, dev) != cudaSuccess ||
+        cudaFuncGetAttributes(&fa, reduce_entry(ar->d.dtype, ar->P)) != cudaSuccess || sms <= 0)
+        return fail(DTT_ECUDA, "dtt_allreduce_create: cannot query the device or the reduce kernel");
+    const uint64_t per_sm = (ar->d.reduce_ctas + (uint64_t)sms - 1) / (uint64_t)sms;
+    const uint64_t r_thr = per_sm * ar->d.reduce_threads;
+    const uint64_t r_regs = r_thr * (((uint64_t)fa.numRegs + 7) / 8 * 8);
+    const uint64_t r_smem = per_sm * (fa.sharedSizeBytes + (uint64_t)reserved);
+    if (a.ctas + b.ctas + per_sm > (uint64_t)blocks || a.threads + b.threads + r_thr > (uint64_t)thr ||
+        a.regs + b.regs + r_regs > (uint64_t)regs || a.smem + b.smem + r_smem > (uint64_t)smem)
+        return fail(DTT_EINVAL,
+                    "dtt_allreduce_create: per SM, the two copiers (%u + %u CTAs, %u + %u threads, %llu + %llu "
+                    "registers, %llu + %llu bytes of shared memory) and %llu reduce CTA(s) of %u threads x %d "
+                    "registers do not fit (%d threads, %d registers, %d bytes): the reduce waits on the copiers, "
+                    "so all of them must be resident at once",
+                    a.ctas, b.ctas, a.threads, b.threads, (unsigned long long)a.regs, (unsigned long long)b.regs,
+                    (unsigned long long)a.smem, (unsigned long long)b.smem, (unsigned long long)per_sm,
+                    ar->d.reduce_threads, fa.numRegs, thr, regs, smem);
+    return DTT_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int dtt_allreduce_create(void* const* bufs, uint64_t buf_bytes, void* const* staging, uint64_t staging_bytes,
+                         uint32_t P, const dtt_allreduce_desc* desc, const dtt_plan_opts* rs_opts,
+                         const dtt_plan_opts* ag_opts, cudaStream_t rs_copy_stream, cudaStream_t ag_copy_stream,
+                         dtt_allreduce** out) {
+    if (!out) return fail(DTT_EINVAL, "dtt_allreduce_create: out is NULL");
+    *out = nullptr;
+    if (!bufs || !desc || P < 2 || P > DTT_MAX_RANKS)
+        return fail(DTT_EINVAL, "dtt_allreduce_create: need buffers, a descriptor and 2 <= P <= %d", DTT_MAX_RANKS);
+    dtt_allreduce_desc d = *desc;
+    if (d.dtype != DTT_BF16 && d.dtype != DTT_F32)
+        return fail(DTT_EINVAL, "dtt_allreduce_create: dtype must be DTT_BF16 or DTT_F32");
+    if (d.sub_blocks == 0) d.sub_blocks = 1;
+    if (d.reduce_threads == 0) d.reduce_threads = 512;
+    const uint64_t eb = d.dtype == DTT_BF16 ? 2 : 4;
+    if (d.block_rows == 0 || d.cols == 0 || d.block_rows % d.sub_blocks)
+        return fail(DTT_EINVAL, "dtt_allreduce_create: block_rows and cols must be positive, sub_blocks must divide block_rows");
+    if (d.cols > (1ull << 40) || d.block_rows > (1ull << 40))
+        return fail(DTT_EINVAL, "dtt_allreduce_create: block too large");
+    const uint64_t rb = d.cols * eb;
+    if (d.pitch == 0) d.pitch = rb;
+    if (rb % 16 || d.pitch % 16 || d.pitch < rb)
+        return fail(DTT_EINVAL, "dtt_allreduce_create: row bytes and pitch must be multiples of 16, pitch >= row bytes");
+    if (d.reduce_threads % 32 || d.reduce_threads > 1024)
+        return fail(DTT_EINVAL, "dtt_allreduce_create: reduce_threads must be a multiple of 32, at most 1024");
+    const uint64_t Mj = d.block_rows / d.sub_blocks;
+    if (Mj * (rb / 16) >= (1ull << 40) || (uint64_t)P * d.sub_blocks > (1ull << 20))
+        return fail(DTT_EINVAL, "dtt_allreduce_create: too many sub-blocks or too large a sub-block");
+    const uint64_t M = (uint64_t)P * d.block_rows;
+    const uint64_t vec_bytes = (M - 1) * d.pitch + rb;
+    const uint64_t slots = (uint64_t)P * d.block_rows * d.pitch;   // the P slots
+    const uint64_t slot_off = staging ? 0 : M * d.pitch;
+    if (vec_bytes > buf_bytes || (!staging && slot_off + slots > buf_bytes))
+        return fail(DTT_EINVAL, "dtt_allreduce_create: a %llu-byte buffer cannot hold the vector%s (%llu bytes)",
+                    (unsigned long long)buf_bytes, staging ? "" : " and the P slots after it",
+                    (unsigned long long)(staging ? vec_bytes : slot_off + slots));
+    if (staging && staging_bytes < slots)
+        return fail(DTT_EINVAL, "dtt_allreduce_create: staging buffers need %llu bytes", (unsigned long long)slots);
+    for (uint32_t r = 0; r < P; ++r) {
+        if (!bufs[r] || reinterpret_cast<uintptr_t>(bufs[r]) % 16 ||
+            (staging && (!staging[r] || reinterpret_cast<uintptr_t>(staging[r]) % 16)))
+            return fail(DTT_EINVAL, "dtt_allreduce_create: buffers must be non-NULL and 16-byte aligned");
+    }
+    dtt_plan_opts ro = rs_opts ? *rs_opts : default_opts();
+    dtt_plan_opts ao = ag_opts ? *ag_opts : default_opts();
+    int rc = check_opts(ro, "reduce-scatter");
+    if (rc == DTT_OK) rc = check_opts(ao, "all-gather");
+    if (rc == DTT_OK) rc = preload_once();
+    if (rc != DTT_OK) return rc;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return fail(DTT_ECUDA, "dtt_allreduce_create: cannot query the device");
+    if (d.reduce_ctas == 0) d.reduce_ctas = (uint32_t)sms;
+
+    ro.allgather = 0;
+    ao.allgather = 0;
+    ro.dst_bufs = staging;
+    ro.dst_bytes = staging ? staging_bytes : 0;
+    ao.dst_bufs = nullptr;
+    ao.dst_bytes = 0;
+
+    dtt_allreduce* ar = new (std::nothrow) dtt_allreduce();
+    if (!ar) return fail(DTT_ENOMEM, "dtt_allreduce_create: out of memory");
+    ar->P = P;
+    ar->d = d;
+    ar->Mj = Mj;
+    ar->rb = rb;
+    ar->pitch = d.pitch;
+    ar->slot_off = slot_off;
+    ar->slot_bytes = d.block_rows * d.pitch;
+    ar->max_polls = ro.max_polls ? ro.max_polls : (1ull << 22);
+    for (uint32_t r = 0; r < P; ++r) {
+        ar->bufs[r] = static_cast<char*>(bufs[r]);
+        ar->stage[r] = static_cast<char*>(staging ? staging[r] : bufs[r]);
+    }
+
+    // a sub-block's rows: one byte range when they are back to back, else a 2D window
+    auto rows_region = [&](uint64_t row) {
+        dtt_region g{};
+        g.offset = row * d.pitch;
+        if (d.pitch == rb) {
+            g.row_bytes = Mj * rb;
+            g.rows = 1;
+            g.pitch = Mj * rb;
+        } else {
+            g.row_bytes = rb;
+            g.rows = Mj;
+            g.pitch = Mj > 1 ? d.pitch : rb;
+        }
+        return g;
+    };
+    ScheduleSet rs_s, ag_s;
+    for (uint32_t s = 0; s < P && rc == DTT_OK; ++s) {
+        dtt_schedule* sc = nullptr;
+        rc = dtt_schedule_empty(&sc);
+        if (rc != DTT_OK) break;
+        rs_s.s.push_back(sc);
+        for (uint32_t b = 0; b < P && rc == DTT_OK; ++b)
+            for (uint32_t j = 0; j < d.sub_blocks && rc == DTT_OK; ++j) {
+                const dtt_region g = rows_region((uint64_t)b * d.block_rows + (uint64_t)j * Mj);
+                dtt_dest dst{};
+                dst.offset = slot_off + ((uint64_t)s * d.block_rows + (uint64_t)j * Mj) * d.pitch;
+                dst.pitch = g.pitch;
+                rc = dtt_schedule_add_chunk_to(sc, &g, &dst, 1, 1, 1u << b);
+            }
+        dtt_schedule* ac = nullptr;
+        if (rc == DTT_OK) rc = dtt_schedule_chunks((uint64_t)s * d.block_rows * d.pitch, d.block_rows, rb, d.pitch,
+                                                   d.sub_blocks, &ac);
+        if (ac) ag_s.s.push_back(ac);
+    }
+    if (rc == DTT_OK) rc = dtt_plan_create(bufs, buf_bytes, P, rs_s.s.data(), &ro, rs_copy_stream, &ar->rs);
+    if (rc == DTT_OK) {
+        // group (b, j) = b * J + j: chunk (s, b, j) of every rank s, rank s's chunks numbered
+        // after the P * J of each lower rank
+        const uint32_t J = d.sub_blocks, n = P * J;
+        std::vector<uint32_t> offs(n + 1), ids((size_t)n * P);
+        for (uint32_t g = 0; g <= n; ++g) offs[g] = g * P;
+        for (uint32_t b = 0; b < P; ++b)
+            for (uint32_t j = 0; j < J; ++j)
+                for (uint32_t s = 0; s < P; ++s) ids[(size_t)(b * J + j) * P + s] = s * P * J + b * J + j;
+        rc = dtt_plan_define_groups(ar->rs, n, offs.data(), ids.data());
+    }
+    if (rc == DTT_OK) rc = dtt_plan_create(bufs, buf_bytes, P, ag_s.s.data(), &ao, ag_copy_stream, &ar->ag);
+    if (rc == DTT_OK) rc = check_room(ar);
+    if (rc == DTT_OK) {
+        const size_t cb = (size_t)P * d.sub_blocks * sizeof(uint32_t);
+        if (cudaMalloc(reinterpret_cast<void**>(&ar->d_counters), cb) != cudaSuccess)
+            rc = fail(DTT_ENOMEM, "dtt_allreduce_create: cannot allocate the reduce counters");
+        else if (cudaMemset(ar->d_counters, 0, cb) != cudaSuccess)
+            rc = fail(DTT_ECUDA, "dtt_allreduce_create: cannot clear the reduce counters");
+    }
+    if (rc != DTT_OK) {
+        const std::string msg = dtt_last_error();
+        release(ar);
+        return fail(rc, "%s", msg.c_str());
+    }
+    *out = ar;
+    return DTT_OK;
+}
+
+int dtt_allreduce_plans(const dtt_allreduce* ar, dtt_plan** rs, dtt_plan** ag) {
+    if (!ar) return fail(DTT_EINVAL, "dtt_allreduce_plans: NULL all-reduce");
+    if (rs) *rs = ar->rs;
+    if (ag) *ag = ar->ag;
+    return DTT_OK;
+}
+
+int dtt_allreduce_start(dtt_allreduce* ar, cudaStream_t producer_stream, dtt_handle* rs_handles) {
+    if (!ar) return fail(DTT_EINVAL, "dtt_allreduce_start: NULL all-reduce");
+    if (dtt_plan_state(ar->rs) != DTT_PLAN_PREPARED || dtt_plan_state(ar->ag) != DTT_PLAN_PREPARED ||
+        dtt_plan_round(ar->rs) != dtt_plan_round(ar->ag))
+        return fail(DTT_ESTATE, "dtt_allreduce_start: both plans must be PREPARED for the same round");
+    dtt_handle tmp[DTT_MAX_RANKS];
+    int rc = dtt_plan_start(ar->rs, producer_stream, rs_handles ? rs_handles : tmp);
+    if (rc == DTT_OK) rc = dtt_plan_start(ar->ag, producer_stream, tmp);
+    return rc;
+}
+
+int dtt_allreduce_reduce(dtt_allreduce* ar, uint32_t* err, cudaStream_t stream) {
+    if (!ar || !err) return fail(DTT_EINVAL, "dtt_allreduce_reduce: NULL argument");
+    if (dtt_plan_state(ar->rs) != DTT_PLAN_RUNNING || dtt_plan_state(ar->ag) != DTT_PLAN_RUNNING ||
+        dtt_plan_round(ar->rs) != dtt_plan_round(ar->ag))
+        return fail(DTT_ESTATE, "dtt_allreduce_reduce: both plans must be RUNNING in the same round");
+    if (stream == plan_copy_stream(ar->rs) || stream == plan_copy_stream(ar->ag))
+        return fail(DTT_EINVAL, "dtt_allreduce_reduce: use a stream other than the plans' copy streams");
+    ReduceParams p{};
+    for (uint32_t r = 0; r < ar->P; ++r) {
+        p.bufs[r] = ar->bufs[r];
+        p.stage[r] = ar->stage[r];
+        int rc = dtt_plan_handle(ar->rs, r, &p.rs[r]);
+        if (rc == DTT_OK) rc = dtt_plan_handle(ar->ag, r, &p.ag[r]);
+        if (rc != DTT_OK) return rc;
+    }
+    p.pitch = ar->pitch;
+    p.slot_off = ar->slot_off;
+    p.slot_bytes = ar->slot_bytes;
+    p.Mb = ar->d.block_rows;
+    p.Mj = ar->Mj;
+    p.max_polls = ar->max_polls;
+    p.J = ar->d.sub_blocks;
+    p.vrow = (uint32_t)(ar->rb / 16);
+    p.contig = ar->pitch == ar->rb ? 1u : 0u;
+    p.counters = ar->d_counters;
+    p.err = err;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(ar->d.reduce_ctas, 1, 1);
+    cfg.blockDim = dim3(ar->d.reduce_threads, 1, 1);
+    cfg.stream = stream;
+    void* args[] = {&p};
+    const cudaError_t e = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(reduce_entry(ar->d.dtype, ar->P)), args);
+    if (e != cudaSuccess) return fail(DTT_ECUDA, "dtt_allreduce_reduce: launch failed: %s", cudaGetErrorString(e));
+    return DTT_OK;
+}
+
+int dtt_allreduce_wait(dtt_allreduce* ar, dtt_report* rs_report, dtt_report* ag_report) {
+    if (!ar) return fail(DTT_EINVAL, "dtt_allreduce_wait: NULL all-reduce");
+    const int a = dtt_plan_wait(ar->rs, rs_report);
+    const std::string msg = a != DTT_OK ? std::string(dtt_last_error()) : std::string();
+    const int b = dtt_plan_wait(ar->ag, ag_report);
+    if (a != DTT_OK) return fail(a, "reduce-scatter: %s", msg.c_str());
+    if (b != DTT_OK) return fail(b, "all-gather: %s", dtt_last_error());
+    return DTT_OK;
+}
+
+int dtt_allreduce_next_round(dtt_allreduce* ar) {
+    if (!ar) return fail(DTT_EINVAL, "dtt_allreduce_next_round: NULL all-reduce");
+    if (dtt_plan_state(ar->rs) != DTT_PLAN_DONE || dtt_plan_state(ar->ag) != DTT_PLAN_DONE)
+        return fail(DTT_ESTATE, "dtt_allreduce_next_round: both plans must be DONE");
+    int rc = dtt_plan_next_round(ar->rs);
+    if (rc == DTT_OK) rc = dtt_plan_next_round(ar->ag);
+    return rc;
+}
+
+int dtt_allreduce_destroy(dtt_allreduce* ar) {
+    if (!ar) return DTT_OK;
+    int rc = DTT_OK;
+    if (ar->rs) {
+        const int a = dtt_plan_close(ar->rs);
+        if (a != DTT_OK) rc = a;
+        ar->rs = nullptr;
+    }
+    if (ar->ag) {
+        const int b = dtt_plan_close(ar->ag);
+        if (b != DTT_OK && rc == DTT_OK) rc = b;
+        ar->ag = nullptr;
+    }
+    release(ar);
+    return rc;
+}
+
+}  // extern "C"

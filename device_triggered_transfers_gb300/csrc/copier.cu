@@ -688,6 +688,14 @@ cudaError_t copier_regs_per_thread(uint32_t method, int* regs) {
     return e;
 }
 
+cudaError_t copier_static_smem(uint32_t method, size_t* bytes) {
+    cudaFuncAttributes a{};
+    const cudaError_t e = method == DTT_COPY_TMA ? cudaFuncGetAttributes(&a, copier_bulk_kernel)
+                                                 : cudaFuncGetAttributes(&a, copier_kernel);
+    *bytes = a.sharedSizeBytes;
+    return e;
+}
+
 cudaError_t preload_copier_kernels() {
     cudaError_t e = prepare_kernel(copier_kernel);
     if (e == cudaSuccess) e = prepare_kernel(copier_bulk_kernel);

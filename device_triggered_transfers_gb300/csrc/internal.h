@@ -213,6 +213,18 @@ cudaError_t prepare_kernel(K kernel) {
 // Force-load each translation unit's kernels on the current device (see dtt_preload).
 cudaError_t preload_copier_kernels();
 cudaError_t copier_regs_per_thread(uint32_t method, int* regs);   // of the copier kernel for `method`
+cudaError_t copier_static_smem(uint32_t method, size_t* bytes);  // its static shared memory
+
+// What a plan's copier holds on each SM while it runs (nothing for the copy-engine transport,
+// whose copies need no SM): CTAs, threads, registers (per-thread count rounded up to the
+// allocation unit of 8) and shared memory including the per-CTA reservation.
+struct CopierRoom {
+    uint32_t ctas = 0, threads = 0;
+    uint64_t regs = 0, smem = 0;
+};
+int plan_copier_room(const dtt_plan* p, CopierRoom* out);
+cudaStream_t plan_copy_stream(const dtt_plan* p);   // the stream its copier runs on
+cudaError_t preload_allreduce_kernels();
 
 // The consumer GEMM (gemm.cu): D = X . W^T over one rank's gathered buffer X [rows, K] bf16,
 // each 128-row block loaded once the chunk ids [c0[b], c1[b]] have arrived at that rank.

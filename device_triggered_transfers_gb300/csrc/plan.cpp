@@ -1080,10 +1080,35 @@ int preload_once() {
     if (e == cudaSuccess) e = preload_fill_kernels();
     if (e == cudaSuccess) e = preload_barrier_kernels();
     if (e == cudaSuccess) e = preload_gemm_kernels();
+    if (e == cudaSuccess) e = preload_allreduce_kernels();
     if (e != cudaSuccess) return fail(DTT_ECUDA, "dtt_preload: %s", cudaGetErrorString(e));
     g_preloaded |= bit;
     return DTT_OK;
 }
+
+int plan_copier_room(const dtt_plan* p, CopierRoom* out) {
+    *out = CopierRoom{};
+    if (p->opts.method == DTT_COPY_ENGINE || p->copier_ctas == 0) return DTT_OK;
+    int sms = 0, reserved = 0, regs = 0;
+    size_t smem = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, p->device) != cudaSuccess || sms <= 0 ||
+        cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, p->device) != cudaSuccess ||
+        copier_regs_per_thread(p->opts.method, &regs) != cudaSuccess ||
+        copier_static_smem(p->opts.method, &smem) != cudaSuccess)
+        return fail(DTT_ECUDA, "cannot query the copier kernel or the device");
+    const uint32_t per_sm = (p->copier_ctas + (uint32_t)sms - 1) / (uint32_t)sms;
+    const uint32_t thr = p->opts.method == DTT_COPY_TMA ? 32 : p->copier_threads;
+    const uint64_t cta_smem = p->opts.method == DTT_COPY_TMA
+                                  ? bulk_smem_bytes(bulk_stage_bytes(p->opts.piece_bytes), p->opts.stages)
+                                  : smem;
+    out->ctas = per_sm;
+    out->threads = per_sm * thr;
+    out->regs = (uint64_t)per_sm * thr * (((uint64_t)regs + 7) / 8 * 8);
+    out->smem = (uint64_t)per_sm * (cta_smem + (uint64_t)reserved);
+    return DTT_OK;
+}
+
+cudaStream_t plan_copy_stream(const dtt_plan* p) { return p->copy_stream; }
 
 }  // namespace dtt
 

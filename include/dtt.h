@@ -679,6 +679,93 @@ int dtt_consumer_gather(dtt_plan* plan, uint32_t rank, void* dst, uint64_t max_p
                         int32_t* status, uint32_t ctas, cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------------------- */
+/* Two-shot all-reduce ("Triggered Plans", Not supported yet: reduce-scatter and two-shot      */
+/* all-reduce are what other destinations make possible)                                     */
+/* ---------------------------------------------------------------------------------------- */
+
+/* The pages name the two-shot all-reduce and say nothing more of it; this is the plain
+ * reading, built from two plans over the same P buffers and one library kernel between them.
+ *  - Data: rank r's vector x_r is M = P * block_rows rows of `cols` elements (bf16 or f32),
+ *    rows `pitch` bytes apart from byte 0 of bufs[r].  Every rank ends with
+ *    y = x_0 + ... + x_{P-1} there, added in f32 in rank order 0..P-1 (IEEE round to nearest
+ *    even after each add) and rounded once to the element type (bf16: nearest even).
+ *  - Rank b owns block b, rows [b * block_rows, (b + 1) * block_rows), cut into sub_blocks
+ *    chunks of block_rows / sub_blocks rows (Mj).
+ *  - Reduce-scatter plan: rank s's chunk b * sub_blocks + j (sub-block j of block b of its
+ *    vector) goes to rank b only, into slot s of b's staging area -- the same rows of the block,
+ *    from byte slot_off + s * block_rows * pitch.  The staging area is b's own buffer after the
+ *    vector (slot_off = M * pitch, so buf_bytes >= 2 M pitch) or, with staging buffers, that
+ *    buffer from byte 0 (staging_bytes >= P * block_rows * pitch).  Rank b's own chunks of block
+ *    b go nowhere (only b's bit in their peer mask) and its own slot stays unused.  Group
+ *    b * sub_blocks + j holds the P chunks (s, b, j): at rank b its own one counts when marked
+ *    and the others when they land, so one group wait covers them all.
+ *  - dtt_allreduce_reduce: for every (b, j), b-major, waits for that group at rank b, adds rank
+ *    b's own rows and the P - 1 slots in rank order, writes the sum over b's own rows and marks
+ *    rank b's all-gather chunk j (once: the last of its CTAs to finish issues the mark).
+ *  - All-gather plan: rank b's chunk j (sub-block j of block b) goes to every other rank at the
+ *    same rows.
+ * A round: dtt_allreduce_start, the producers write every rank's vector and mark its
+ * reduce-scatter chunks (with the handles start returns), dtt_allreduce_reduce,
+ * dtt_allreduce_wait, dtt_allreduce_next_round.  Rounds run one at a time. */
+typedef struct dtt_allreduce dtt_allreduce;
+
+typedef struct dtt_allreduce_desc {
+    uint32_t dtype;          /* DTT_BF16 or DTT_F32 */
+    uint32_t sub_blocks;     /* chunks per block, dividing block_rows; 0 = 1 */
+    uint64_t block_rows;     /* rows each rank reduces (its block), >= 1 */
+    uint64_t cols;           /* elements per row; cols x element bytes a multiple of 16 */
+    uint64_t pitch;          /* bytes between rows, a multiple of 16; 0 = cols x element bytes */
+    uint32_t reduce_ctas;    /* CTAs of the reduce kernel; 0 = one per SM */
+    uint32_t reduce_threads; /* threads per reduce CTA (a multiple of 32, <= 1024); 0 = 512 */
+} dtt_allreduce_desc;
+
+/* Build both plans and the reduce kernel's counters.  bufs: host array of P (2..16) device
+ * pointers, buf_bytes each, 16-byte aligned; staging: NULL (slots in bufs after the vector) or
+ * a host array of P device pointers, staging_bytes each, 16-byte aligned.  rs_opts / ag_opts:
+ * the plans' options (NULL: bulk-copy copiers of two 32-thread CTAs per SM with two 16 KiB
+ * stages each); the library sets allgather = 0 and the destination buffers itself.  Both
+ * copiers spin while the reduce kernel waits on the first one's deliveries, so the two
+ * copiers' CTAs and the reduce's must fit on an SM together (threads, registers, shared
+ * memory): checked here, DTT_EINVAL otherwise.  Not with the copy-engine transport,
+ * deferred_copier or overlap (DTT_EINVAL).  Copy streams: as dtt_plan_create (NULL: each plan
+ * makes its own).  The caller owns the buffers; the all-reduce owns its plans.
+ * Errors: DTT_EINVAL, DTT_EOVERLAP, DTT_ENOMEM, DTT_ECUDA (nothing stays allocated). */
+int dtt_allreduce_create(void* const* bufs, uint64_t buf_bytes, void* const* staging,
+                         uint64_t staging_bytes, uint32_t P, const dtt_allreduce_desc* desc,
+                         const dtt_plan_opts* rs_opts, const dtt_plan_opts* ag_opts,
+                         cudaStream_t rs_copy_stream, cudaStream_t ag_copy_stream,
+                         dtt_allreduce** out);
+
+/* The two plans, owned by the all-reduce (for dtt_plan_read_gates, dtt_plan_stats and the
+ * like; not to be started, waited on or closed directly).  Either pointer may be NULL.
+ * Errors: DTT_EINVAL. */
+int dtt_allreduce_plans(const dtt_allreduce* ar, dtt_plan** rs, dtt_plan** ag);
+
+/* Start the current round on both plans (their copiers launch on their copy streams).
+ * rs_handles (host array of P, may be NULL) receives the reduce-scatter plan's handles, for
+ * the producers' marks.  Errors: as dtt_plan_start (both plans PREPARED). */
+int dtt_allreduce_start(dtt_allreduce* ar, cudaStream_t producer_stream, dtt_handle* rs_handles);
+
+/* Launch the reduce kernel on `stream`, normally the producer stream after the producers: its
+ * CTAs spin on group waits, so on another stream the producers' CTAs must fit beside it.
+ * err: device uint32, incremented by a CTA whose group wait ran out (at most the
+ * reduce-scatter plan's max_polls polls); that CTA stops, the all-gather chunks it had not
+ * finished stay unmarked and dtt_allreduce_wait fails.  Errors: DTT_ESTATE (a plan not
+ * RUNNING), DTT_EINVAL, DTT_ECUDA. */
+int dtt_allreduce_reduce(dtt_allreduce* ar, uint32_t* err, cudaStream_t stream);
+
+/* dtt_plan_wait on the reduce-scatter plan, then on the all-gather plan (reports may be NULL).
+ * Returns the first error (both plans are waited on either way). */
+int dtt_allreduce_wait(dtt_allreduce* ar, dtt_report* rs_report, dtt_report* ag_report);
+
+/* dtt_plan_next_round on both plans.  Errors: as dtt_plan_next_round. */
+int dtt_allreduce_next_round(dtt_allreduce* ar);
+
+/* Close both plans (draining their copiers) and free the rest.  Returns the first error of the
+ * two closes; the all-reduce is released either way. */
+int dtt_allreduce_destroy(dtt_allreduce* ar);
+
+/* ---------------------------------------------------------------------------------------- */
 /* N-rank notify/wait barrier (PyPTO, "Barrier: Signals Only")                               */
 /* ---------------------------------------------------------------------------------------- */
 

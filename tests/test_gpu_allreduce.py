@@ -1,0 +1,189 @@
+"""GPU parity: the two-shot all-reduce ("Triggered Plans", Not supported yet: two-shot all-reduce,
+which other destinations make possible) -- the reduce-scatter plan, the reduce kernel and the
+all-gather plan of libdtt -- against the oracle's two-shot model (oracle/allreduce.py): every
+byte of every buffer and staging buffer, both plans' gate words 0-4 and the reduce-scatter
+plan's group counters, round after round; at full size every element against the definition."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import allreduce as A
+from oracle import cfill
+
+pytestmark = pytest.mark.gpu
+
+if torch.cuda.is_available():
+    from conftest import ensure_built
+    ensure_built()
+    import device_triggered_transfers_gb300 as D
+
+SEED = 4242
+
+COPIERS = {
+    "bulk": None,   # the all-reduce's default: bulk-copy copiers, 2 CTAs x 2 x 16 KiB per SM
+    "vector": dict(method=0, copier_threads=256, ctas_per_sm=1),
+}
+
+
+def _opts(copier, **kw):
+    if COPIERS[copier] is None and not kw:
+        return None
+    base = dict(method=1, ctas_per_sm=2, piece_bytes=16384, stages=2) if COPIERS[copier] is None else COPIERS[copier]
+    return D.dtt_plan_opts_default(**{**base, **kw})
+
+
+class Case:
+    def __init__(self, P, Mb, cols, J, dtype, separate=False, pitch=0, copier="bulk", reduce_ctas=0,
+                 reduce_threads=0, group=1, max_polls=0, oracle=True):
+        self.P, self.Mb, self.cols, self.J, self.dtype = P, Mb, cols, J, dtype
+        # the oracle's model of both plans (small cases; at full size only its layout is used)
+        self.o = A.TwoShot(P, Mb, cols, dtype, J, pitch=pitch or None, separate=separate) if oracle else None
+        _, self.pitch, self.buf_bytes, _, staging_bytes = A.layout(P, Mb, cols, dtype, pitch or None, separate)
+        self.M = P * Mb
+        self.Mj = Mb // J
+        dev = torch.device("cuda")
+        self.bufs = [torch.zeros(self.buf_bytes, dtype=torch.uint8, device=dev) for _ in range(P)]
+        self.staging = [torch.zeros(staging_bytes, dtype=torch.uint8, device=dev) for _ in range(P)] \
+            if separate else None
+        kw = dict(max_polls=max_polls) if max_polls else {}
+        self.ar = D.AllReduce(self.bufs, self.buf_bytes, dtype, Mb, cols, sub_blocks=J, pitch=pitch,
+                              staging=self.staging, staging_bytes=staging_bytes,
+                              rs_opts=_opts(copier, **kw), ag_opts=_opts(copier, **kw),
+                              reduce_ctas=reduce_ctas, reduce_threads=reduce_threads)
+        steps = self.M // self.Mj
+        self.counters = torch.zeros(P * steps, dtype=torch.int32, device=dev) if group > 1 else None
+        self.desc = D.fill_desc(dtype, SEED, self.M, cols, self.pitch, self.buf_bytes, [0] * P, self.Mj, cols,
+                                1, 1, mark_mode=D.MARK_PER_STEP, group=group, group_counters=self.counters)
+        self.err = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.prod = torch.cuda.Stream()
+        torch.cuda.synchronize()
+
+    def round(self, reduce_stream=None):
+        h = self.ar.start(self.prod)
+        if reduce_stream is not None:
+            # the reduce first, on a stream of its own: its group waits order it after the
+            # producers' marks and the reduce-scatter copies
+            self.ar.reduce(self.err, reduce_stream)
+            D.dtt_fill_producer(self.bufs, self.desc, h, self.prod)
+        else:
+            D.dtt_fill_producer(self.bufs, self.desc, h, self.prod)
+            self.ar.reduce(self.err, self.prod)
+        rs, ag = self.ar.wait()
+        assert rs.status == D.OK and ag.status == D.OK
+        torch.cuda.synchronize()       # the reduce may have run on a stream of its own
+        assert int(self.err.item()) == 0
+
+    def oracle_round(self, R):
+        parts = A.hashed_partials(self.dtype, SEED, self.P, self.M, self.cols, R)
+        assert self.o.round(parts) == R
+        return parts
+
+    def compare(self, what):
+        for r in range(self.P):
+            np.testing.assert_array_equal(self.bufs[r].cpu().numpy(), self.o.bufs[r], err_msg=f"{what} buf {r}")
+            if self.staging is not None:
+                np.testing.assert_array_equal(self.staging[r].cpu().numpy(), self.o.staging[r],
+                                              err_msg=f"{what} staging {r}")
+        np.testing.assert_array_equal(self.ar.rs.read_gates()[:, :, :5], self.o.rs.gates, err_msg=f"{what} rs gates")
+        np.testing.assert_array_equal(self.ar.ag.read_gates()[:, :, :5], self.o.ag.gates, err_msg=f"{what} ag gates")
+        np.testing.assert_array_equal(self.ar.rs.read_group_counters(), self.o.rs.group_counters,
+                                      err_msg=f"{what} group counters")
+
+    def close(self):
+        self.ar.close()
+
+
+CASES = {
+    "p2_bf16_in_place": dict(P=2, Mb=64, cols=256, J=2, dtype="bf16"),
+    "p4_bf16_staging": dict(P=4, Mb=48, cols=384, J=3, dtype="bf16", separate=True),
+    "p3_f32_pitched_vector": dict(P=3, Mb=40, cols=128, J=5, dtype="f32", pitch=768, copier="vector"),
+    "p8_bf16": dict(P=8, Mb=16, cols=512, J=2, dtype="bf16"),
+    "p4_f32_staging_vector": dict(P=4, Mb=64, cols=1024, J=4, dtype="f32", separate=True, copier="vector"),
+    "p16_bf16": dict(P=16, Mb=8, cols=64, J=1, dtype="bf16"),
+    "p5_bf16_one_row_sub_blocks": dict(P=5, Mb=3, cols=256, J=3, dtype="bf16"),   # 32 vectors, 152 CTAs
+    "p4_bf16_few_ctas": dict(P=4, Mb=256, cols=2048, J=4, dtype="bf16", reduce_ctas=7, reduce_threads=96),
+    "p6_f32_pitched_staging": dict(P=6, Mb=12, cols=36, J=4, dtype="f32", pitch=160, separate=True),
+}
+
+
+@pytest.mark.parametrize("name", sorted(CASES))
+def test_allreduce_matches_the_oracle(name):
+    c = Case(**CASES[name])
+    try:
+        for R in range(1, 4):
+            c.round()
+            parts = c.oracle_round(R)
+            c.compare(f"{name} R{R}")
+            want = A.allreduce(c.dtype, parts)     # and the definition, directly
+            for r in range(c.P):
+                got = c.o._rows(c.bufs[r].cpu().numpy(), 0, c.M)
+                assert np.array_equal(got.view(np.uint8), want.view(np.uint8)), (name, R, r)
+            c.ar.next_round()
+    finally:
+        c.close()
+
+
+def test_allreduce_reduce_launched_first_on_its_own_stream():
+    c = Case(P=4, Mb=64, cols=512, J=4, dtype="bf16", group=8)
+    side = torch.cuda.Stream()
+    try:
+        for R in range(1, 3):
+            c.round(reduce_stream=side)
+            c.oracle_round(R)
+            c.compare(f"reduce first R{R}")
+            c.ar.next_round()
+    finally:
+        c.close()
+
+
+def test_allreduce_full_size_every_element():
+    """P = 4 ranks of bf16 [16384, 4096] (128 MiB each, the 4-rank chunked all-gather's size),
+    blocks of 4096 rows in 8 sub-blocks of 512 rows (4 MiB), the producer a 38-CTA group per
+    rank: every element of every rank's result against the definition, two rounds."""
+    P, Mb, cols, J = 4, 4096, 4096, 8
+    c = Case(P=P, Mb=Mb, cols=cols, J=J, dtype="bf16", group=38, oracle=False)
+    try:
+        for R in range(1, 3):
+            c.round()
+            rb = cols * 2
+            for b in range(P):
+                parts = []
+                for s in range(P):
+                    raw = np.empty(Mb * rb, dtype=np.uint8)
+                    cfill.fill_rows_into(raw, "bf16", SEED, s, R, cols, b * Mb, (b + 1) * Mb)
+                    parts.append(raw.view(np.uint16).reshape(Mb, cols))
+                want = A.allreduce("bf16", parts).view(np.uint8).reshape(-1)
+                for r in range(P):
+                    got = c.bufs[r][b * Mb * rb:(b + 1) * Mb * rb].cpu().numpy()
+                    np.testing.assert_array_equal(got, want, err_msg=f"R{R} block {b} at rank {r}")
+            c.ar.next_round()
+    finally:
+        c.close()
+
+
+def test_allreduce_missing_mark_fails_the_round_and_counts_the_reduce_wait():
+    """One reduce-scatter chunk never marked (the producers of the other chunks run): the
+    group of its sub-block never completes, the reduce's CTAs give up after the plan's poll
+    limit and count it, the all-gather chunks they did not reach stay unmarked, and both waits
+    fail.  Bounded waits only: nothing spins past its limit."""
+    P, Mb, cols, J = 3, 8, 256, 2
+    c = Case(P=P, Mb=Mb, cols=cols, J=J, dtype="bf16", max_polls=2000)
+    try:
+        h = c.ar.start(c.prod)
+        # rank 1 writes nothing and marks every chunk but (b = 2, j = 1); the others fill
+        c.desc.rank_mask = 0b101
+        D.dtt_fill_producer(c.bufs, c.desc, h, c.prod)
+        first = c.ar.rs.info()[1][1]
+        D.dtt_publish(h, first, P * J - 1, 0, c.prod)
+        c.ar.reduce(c.err, c.prod)
+        rs, ag = c.ar.wait(raise_on_error=False)
+        assert rs.status == D.ETIMEDOUT and ag.status == D.ETIMEDOUT
+        torch.cuda.synchronize()
+        assert int(c.err.item()) > 0
+        # the reduce-scatter short chunk is rank 1's last; the all-gather chunks of block 2
+        # from sub-block 1 on were never marked
+        assert first + P * J - 1 in list(rs.short_chunks[:rs.n_short])
+        ag_first = c.ar.ag.info()[1]
+        assert ag_first[2] + 1 in list(ag.short_chunks[:ag.n_short])
+    finally:
+        c.close()

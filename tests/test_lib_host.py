@@ -207,7 +207,8 @@ def test_binding_structs_match_the_c_header(tmp_path):
         pytest.skip("gcc not found")
     structs = {"dtt_region": D.dtt_region, "dtt_dest": D.dtt_dest, "dtt_order": D.dtt_order,
                "dtt_plan_opts": D.dtt_plan_opts,
-               "dtt_group_table": D.dtt_group_table, "dtt_handle": D.dtt_handle, "dtt_report": D.dtt_report, "dtt_fill_desc": D.dtt_fill_desc}
+               "dtt_group_table": D.dtt_group_table, "dtt_handle": D.dtt_handle, "dtt_report": D.dtt_report, "dtt_fill_desc": D.dtt_fill_desc,
+               "dtt_allreduce_desc": D.dtt_allreduce_desc}
     lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "dtt.h"', 'int main(void) {']
     for name, cls in structs.items():
         lines.append(f'printf("{name} %zu\\n", sizeof({name}));')
@@ -384,3 +385,52 @@ def test_schedules_from_tensor_slices_match_the_offset_builders():
         D.chunks(out.t()[:, :8], 2, base=out)          # rows not contiguous
     with pytest.raises(D.DttError):
         D.chunks(torch.zeros(8, 8, dtype=torch.bfloat16), 2, base=out)   # not inside base
+
+
+def _allreduce_create(P=2, bufs=None, buf_bytes=1 << 20, staging=None, staging_bytes=0, rs=None, ag=None, **desc):
+    d = D.dtt_allreduce_desc()
+    d.dtype, d.sub_blocks, d.block_rows, d.cols, d.pitch = D.BF16, 2, 64, 256, 0
+    for k, v in desc.items():
+        setattr(d, k, v)
+    arr = (C.c_void_p * max(P, 1))(*(bufs or [0x10000 * (r + 1) for r in range(P)]))
+    stg = (C.c_void_p * P)(*staging) if staging is not None else None
+    out = C.c_void_p()
+    rc = D.lib().dtt_allreduce_create(arr, buf_bytes, stg, staging_bytes, P, C.byref(d),
+                                      C.byref(rs) if rs is not None else None,
+                                      C.byref(ag) if ag is not None else None, None, None, C.byref(out))
+    return rc, D.lib().dtt_last_error().decode()
+
+
+@pytest.mark.parametrize("case,kw,words", [
+    ("one rank", dict(P=1), "P <="),
+    ("seventeen ranks", dict(P=17), "P <="),
+    ("u8", dict(dtype=D.U8), "dtype"),
+    ("no rows", dict(block_rows=0), "block_rows"),
+    ("sub-blocks not dividing", dict(sub_blocks=3), "divide"),
+    ("rows not 16-byte multiples", dict(cols=4), "multiples of 16"),
+    ("pitch not a 16-byte multiple", dict(pitch=520), "multiples of 16"),
+    ("pitch below the row", dict(pitch=496), "pitch >= row bytes"),
+    ("reduce threads", dict(reduce_threads=100), "reduce_threads"),
+    ("buffer too small in place", dict(buf_bytes=2 * 128 * 512 - 16), "cannot hold"),
+    ("staging too small", dict(staging=[0x100000, 0x200000], staging_bytes=1000), "staging buffers need"),
+    ("unaligned buffer", dict(bufs=[0x10000, 0x20008]), "16-byte aligned"),
+    ("copy-engine reduce-scatter", dict(rs=D.dtt_plan_opts_default(method=2)), "copy-engine"),
+    ("overlapped all-gather", dict(ag=D.dtt_plan_opts_default(overlap=1)), "overlap"),
+    ("deferred reduce-scatter", dict(rs=D.dtt_plan_opts_default(deferred_copier=2)), "deferred_copier"),
+])
+def test_allreduce_arguments_are_checked_before_any_device_call(case, kw, words):
+    rc, msg = _allreduce_create(**kw)
+    assert rc == D.EINVAL, (case, msg)
+    assert words in msg, (case, msg)
+
+
+def test_allreduce_calls_refuse_a_null_all_reduce_without_a_gpu():
+    L = D.lib()
+    a, b = D.dtt_report(), D.dtt_report()
+    err = C.c_void_p(0x1000)
+    assert L.dtt_allreduce_start(None, None, None) == D.EINVAL
+    assert L.dtt_allreduce_reduce(None, err, None) == D.EINVAL
+    assert L.dtt_allreduce_wait(None, C.byref(a), C.byref(b)) == D.EINVAL
+    assert L.dtt_allreduce_next_round(None) == D.EINVAL
+    assert L.dtt_allreduce_plans(None, None, None) == D.EINVAL
+    assert L.dtt_allreduce_destroy(None) == D.OK
