@@ -273,6 +273,27 @@ def time_oracle_gemm(w, budget_s: float = 10.0, rows: int = 128):
 
 
 # ---- distributed helpers ---------------------------------------------------------------------------
+def time_oracle_allreduce(budget_s: float = 10.0, rows: int = 32):
+    """The oracle's two-shot all-reduce (both plans and the reduce step on the plan model) on a
+    sample of the benchmark's workload: P = 4 ranks of `rows` rows of 4096 bf16 per block,
+    8 sub-blocks.  Returns (GB/s of vector bytes per rank, rounds, seconds, sample)."""
+    from oracle import allreduce as OA
+    a = W.ALLREDUCE
+    P, cols, J = a["P"], a["cols"], a["sub_blocks"]
+    o = OA.TwoShot(P, rows, cols, a["dtype"], J)
+    M = P * rows
+    parts = [OA.hashed_partials(a["dtype"], a["seed"], P, M, cols, R) for R in (1, 2)]
+    n, t0 = 0, time.perf_counter()
+    while True:
+        o.round(parts[n % 2])
+        n += 1
+        dt = time.perf_counter() - t0
+        if dt >= budget_s or n >= 1000:
+            break
+    S = M * cols * 2
+    return S * n / dt / 1e9, n, dt, f"{rows} of {a['block_rows']} rows per block, P={P}, {J} sub-blocks"
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     return ws, int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0"))
@@ -733,6 +754,17 @@ def run_ours(args):
                 "workload": describe(wc, mc["launch"], mc["copier_method"]),
                 "l2": l2_note(wc, dev)}
 
+        # the two-shot all-reduce, built from a reduce-scatter plan and an all-gather plan
+        ma = measure_allreduce(20, 3, isolated_rounds=5, fill_rounds=5)
+        sa = summarize_allreduce(ma, peak, peak_kind)
+        per_config[W.ALLREDUCE["name"]] = {
+            "steps": 20, "ms_per_round": sa["ms_per_round"], "algbw_gbs": sa["algbw_gbs"],
+            "busbw_gbs": sa["busbw_gbs"], "hbm_frac_end_to_end": sa["hbm_frac_end_to_end"]["of_measured"],
+            "with_fill_producer_ms_per_round": ma.get("fill_round_ms"),
+            "dominant_kernel": {k: (sa.get("reduce_roofline") or {}).get(k)
+                                for k in ("kernel", "bound", "achieved", "unit", "frac")},
+            "workload": "P=4 bf16 [16384, 4096] per rank, 8 sub-blocks of 512 rows per block (bench.py --allreduce)"}
+
     if rank != 0:
         return 0
     gemm = m["gemm"]
@@ -969,6 +1001,220 @@ def run_ce_fanout(args):
     return 0
 
 
+def measure_allreduce(K: int, warmup: int, isolated_rounds: int = 10, e2e_steps: int = 0,
+                      clocks_dev=None, rows: int = 0, in_order: bool = False, ctas_per_sm: int = 0,
+                      stages: int = 0, piece_bytes: int = 0, fill_rounds: int = 0):
+    """The two-shot all-reduce of W.ALLREDUCE.  The collective: K rounds of start + a producer that
+    only marks (dtt_publish: the vectors were written before the timed region, as an all-reduce
+    benchmark's inputs are) + reduce kernel + wait + next_round (both plans' copiers launched at
+    start), CUDA events on the producer stream with a synchronize on both sides -- in place, so
+    each round's result is the next round's input (the values grow by P a round, finite over
+    these rounds).  Then fill_rounds rounds whose producer is the fill (writing every rank's
+    whole vector), the reduce kernel alone (launched once the reduce-scatter copier has finished,
+    on a stream of its own), and (e2e_steps > 0) rounds fed from pinned host memory through
+    dtt_publish with rank 0's result read back.  in_order: both plans with deferred_copier = 1,
+    every kernel after its inputs (for profilers that serialise launches; the isolated reduce
+    then includes its wait for the copier)."""
+    import torch
+    import device_triggered_transfers_gb300 as D
+    a = W.ALLREDUCE
+    P, cols, J, dtype = a["P"], a["cols"], a["sub_blocks"], a["dtype"]
+    Mb = rows or a["block_rows"]
+    M = P * Mb
+    rb = cols * W.ELEM_BYTES[dtype]
+    S = M * rb                      # one rank's vector
+    buf_bytes = 2 * S               # the vector, then the P slots
+    dev = torch.device("cuda")
+    bufs = [torch.zeros(buf_bytes, dtype=torch.uint8, device=dev) for _ in range(P)]
+    prod, side = torch.cuda.Stream(), torch.cuda.Stream()
+    rs_cs, ag_cs = torch.cuda.Stream(priority=-1), torch.cuda.Stream(priority=-1)
+    opts = None
+    if in_order or ctas_per_sm or stages or piece_bytes:
+        opts = D.dtt_plan_opts_default(method=D.COPY_TMA, ctas_per_sm=ctas_per_sm or 3,
+                                       piece_bytes=piece_bytes or 16384, stages=stages or 2,
+                                       deferred_copier=1 if in_order else 0)
+    ar = D.AllReduce(bufs, buf_bytes, dtype, Mb, cols, sub_blocks=J, rs_opts=opts, ag_opts=opts,
+                     rs_copy_stream=rs_cs, ag_copy_stream=ag_cs)
+    Mj = Mb // J
+    counters = torch.zeros(P * (M // Mj), dtype=torch.int32, device=dev)
+    desc = D.fill_desc(dtype, a["seed"], M, cols, rb, buf_bytes, [0] * P, Mj, cols, 1, 1,
+                       mark_mode=D.MARK_PER_STEP, group=a["fill_group"], group_counters=counters)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    n_rs = ar.rs.info()[0]
+
+    def one(fill=False):
+        h = ar.start(prod)
+        if fill:
+            D.dtt_fill_producer(bufs, desc, h, prod)
+        else:
+            D.dtt_publish(h, 0, n_rs, 0, prod)      # every reduce-scatter chunk's marks
+        ar.reduce(err, prod)
+        ar.wait()
+        ar.next_round()
+
+    for _ in range(warmup):
+        one(fill=True)
+    one(fill=True)                                   # fresh inputs for the timed rounds
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    out = {}
+    sampler = ClockSampler(clocks_dev) if clocks_dev is not None else None
+    if sampler:
+        sampler.__enter__()
+    e0.record(prod)
+    for _ in range(K):
+        one()
+    e1.record(prod)
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.__exit__(None, None, None)
+        out["clocks"] = sampler.summary()
+    out["round_ms"] = e0.elapsed_time(e1) / K
+    assert int(err.item()) == 0
+    if fill_rounds:
+        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        f0.record(prod)
+        for _ in range(fill_rounds):
+            one(fill=True)
+        f1.record(prod)
+        torch.cuda.synchronize()
+        out["fill_round_ms"] = f0.elapsed_time(f1) / fill_rounds
+
+    # the reduce kernel alone, on an all-reduce over the same buffers whose kernels run in order:
+    # its reduce-scatter copier (launched here, after the fill) has finished before the reduce
+    # starts on a stream of its own, and its all-gather copier starts after the reduce
+    iso = []
+    if isolated_rounds:
+        serial = D.dtt_plan_opts_default(method=D.COPY_TMA, ctas_per_sm=ctas_per_sm or 3,
+                                         piece_bytes=piece_bytes or 16384, stages=stages or 2, deferred_copier=1)
+        ars = D.AllReduce(bufs, buf_bytes, dtype, Mb, cols, sub_blocks=J, rs_opts=serial, ag_opts=serial,
+                          rs_copy_stream=rs_cs, ag_copy_stream=ag_cs)
+        for i in range(isolated_rounds + 2):
+            h = ars.start(prod)
+            D.dtt_fill_producer(bufs, desc, h, prod)
+            ars.rs.launch_copier()
+            ev = torch.cuda.Event()
+            ev.record(rs_cs)
+            side.wait_event(ev)
+            r0, r1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            r0.record(side)
+            ars.reduce(err, side)
+            r1.record(side)
+            ars.wait()
+            ars.next_round()
+            torch.cuda.synchronize()
+            if i >= 2:
+                iso.append(r0.elapsed_time(r1))
+        ars.close()
+    out["reduce_isolated_ms"] = statistics.median(iso) if iso else None
+    assert int(err.item()) == 0
+
+    if e2e_steps:
+        g = torch.Generator().manual_seed(a["seed"])
+        host = [torch.randn(M, cols, generator=g).to(torch.bfloat16).view(torch.uint8).reshape(-1).pin_memory()
+                for _ in range(P)]
+        host_out = torch.empty(S, dtype=torch.uint8).pin_memory()
+        n_global = ar.rs.info()[0]
+
+        def host_round():
+            h = ar.start(prod)
+            with torch.cuda.stream(prod):
+                for r in range(P):
+                    bufs[r][:S].copy_(host[r], non_blocking=True)
+            D.dtt_publish(h, 0, n_global, 0, prod)      # every chunk's marks, after its bytes
+            ar.reduce(err, prod)
+            ar.wait()
+            ar.next_round()
+            with torch.cuda.stream(prod):
+                host_out.copy_(bufs[0][:S], non_blocking=True)
+            prod.synchronize()
+
+        for _ in range(2):
+            host_round()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(e2e_steps):
+            host_round()
+        torch.cuda.synchronize()
+        out["e2e_round_ms"] = (time.perf_counter() - t0) / e2e_steps * 1e3
+        out["e2e_bytes"] = (P * S, S)
+        assert int(err.item()) == 0
+    ar.close()
+    out.update(P=P, S=S, Mb=Mb, cols=cols, J=J, dtype=dtype)
+    return out
+
+
+def summarize_allreduce(m, peak, peak_kind):
+    """Bandwidths and roofline fractions of measure_allreduce's numbers.  Algorithmic HBM bytes
+    of a round (the producer's writes aside, as for the all-gathers): the reduce-scatter copies
+    read and write (P-1) S, the reduce reads P S and writes S, the all-gather copies read S and
+    write (P-1) S: (4P - 1) S in all, S = one rank's vector."""
+    P, S = m["P"], m["S"]
+    t = m["round_ms"] * 1e-3
+    alg = (4 * P - 1) * S
+    red = (P + 1) * S               # the reduce kernel: P parts of every block read, one written
+    algbw = S / t / 1e9
+    res = {"ms_per_round": m["round_ms"], "algbw_gbs": algbw, "busbw_gbs": algbw * 2 * (P - 1) / P,
+           "algorithmic_bytes_per_round": alg,
+           "hbm_frac_end_to_end": {"of_measured": alg / t / 1e9 / peak, "peak_kind": peak_kind}}
+    if m.get("reduce_isolated_ms"):
+        achieved = red / (m["reduce_isolated_ms"] * 1e-3) / 1e9
+        res["reduce_roofline"] = {"kernel": "reduce_kernel", "bound": "hbm", "achieved": achieved, "peak": peak,
+                                  "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
+                                  "traffic": NCU_TRAFFIC.get(("allreduce_p4", "reduce_kernel")),
+                                  "algorithmic_bytes_per_launch": red, "ms": m["reduce_isolated_ms"]}
+    return res
+
+
+def run_allreduce(args):
+    """One JSON line for the two-shot all-reduce (W.ALLREDUCE)."""
+    import torch
+    dev = torch.cuda.current_device()
+    K = args.steps
+    m = measure_allreduce(K, args.warmup, isolated_rounds=10, e2e_steps=0 if args.no_e2e else 10,
+                          clocks_dev=dev, rows=args.rows, in_order=args.in_order,
+                          ctas_per_sm=args.ctas_per_sm, stages=args.stages, piece_bytes=args.piece_bytes,
+                          fill_rounds=20)
+    peak, peak_kind = load_peaks()
+    s = summarize_allreduce(m, peak, peak_kind)
+    a = W.ALLREDUCE
+    cpu = None
+    if not args.no_cpu_baseline:
+        v, n, dt, what = time_oracle_allreduce(budget_s=args.cpu_seconds)
+        cpu = {"value": v, "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": f"{what}; {n} oracle round(s) in {dt:.1f} s"}
+    e2e = None
+    if "e2e_round_ms" in m:
+        e2e = {"value": m["S"] / (m["e2e_round_ms"] * 1e-3) / 1e9, "unit": "GB/s",
+               "h2d_bytes_per_step": m["e2e_bytes"][0], "d2h_bytes_per_step": m["e2e_bytes"][1],
+               "call": "partials copied in from pinned host memory, dtt_publish, reduce, wait; rank 0's result copied out"}
+    line = {
+        "metric": "two-shot all-reduce algorithm GB/s (one rank's vector bytes per round, 1 GB300)",
+        "value": s["algbw_gbs"], "unit": "GB/s", "n_gpus": 1, "steps": K, "warmup": args.warmup,
+        "ms_per_step": s["ms_per_round"], "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32 sums of bf16", "data": "synthetic",
+        "config": {"workload": (f"{a['name']}: P={m['P']} virtual ranks, {m['dtype']} [{m['P'] * m['Mb']}, {m['cols']}] "
+                                f"per rank, blocks of {m['Mb']} rows in {m['J']} sub-blocks; reduce-scatter into "
+                                "staging slots after each vector, reduce kernel, in-place all-gather; both "
+                                "plans bulk-copy copiers of 3 CTAs x 2 x 16 KiB per SM; fill producer a group "
+                                f"of {a['fill_group']} CTAs per rank"),
+                   "step": ("start (both plans) + marks of every reduce-scatter chunk (inputs resident, "
+                            "in place) + reduce + wait (both) + next_round"),
+                   "l2": f"inputs larger than L2 ({m['P'] * 2 * m['S'] >> 20} MiB of buffers)"},
+        "busbw_gbs": s["busbw_gbs"],
+        "hbm_frac_end_to_end": s["hbm_frac_end_to_end"],
+        "with_fill_producer_ms_per_round": m.get("fill_round_ms"),
+        "roofline": s.get("reduce_roofline"),
+        "e2e": e2e,
+        "gpu_launches": 6 * K,      # marks, 2 copiers, reduce, 2 checks per round
+        "clocks": m.get("clocks"),
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line))
+    return 0
+
+
 def run_barrier(args):
     """Latency of the N-rank notify/wait barrier and the builtin reveal (P = 8 virtual ranks,
     reveal SIZE = 256): one cooperative launch per barrier, CUDA events around K of them."""
@@ -1053,6 +1299,10 @@ def main(argv=None):
                     help="time the N-rank barrier and the builtin reveal instead")
     ap.add_argument("--ce-fanout", action="store_true",
                     help="time the fan-out with copy engines (device-to-device memcpy) against the SM copier")
+    ap.add_argument("--allreduce", action="store_true",
+                    help="time the two-shot all-reduce (reduce-scatter plan, reduce kernel, all-gather plan)")
+    ap.add_argument("--in-order", action="store_true",
+                    help="--allreduce: each kernel after its inputs (deferred copiers), for profiler captures")
     ap.add_argument("--consumer", action="store_true",
                     help="time the all-gather with a consumer GEMM over its output, overlapped")
     ap.add_argument("--consumer-n", type=int, default=4096)
@@ -1077,6 +1327,8 @@ def main(argv=None):
         return run_barrier(args)
     if args.consumer and args.impl == "ours":
         return run_consumer(args)
+    if args.allreduce and args.impl == "ours":
+        return run_allreduce(args)
     if args.ce_fanout and args.impl == "ours":
         return run_ce_fanout(args)
     if args.impl == "reference":

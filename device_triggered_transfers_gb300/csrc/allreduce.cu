@@ -3,10 +3,13 @@
 // in staging slots of the block's owner, one kernel that waits for each sub-block's group, adds
 // the P parts in f32 in rank order and marks the sum for an in-place all-gather plan.
 //
-// One launch covers every virtual rank.  Its CTAs walk the sub-blocks (b, j) b-major -- the
-// order a producer writing its vector row by row completes them -- and each CTA takes the same
-// share of every sub-block's 16-byte vectors, so all of them work on one sub-block at a time
-// and the sub-block's all-gather copies can start while the next one is being added.
+// One launch covers every virtual rank; it walks the sub-blocks (b, j) b-major, the order a
+// producer writing its vector row by row completes them.  In each CTA one control thread does
+// all the GPU-scope synchronisation -- it polls the sub-blocks' groups ahead of the work, and
+// counts the CTA's finished sub-blocks into global counters whose last CTA marks the all-gather
+// chunk -- and hands both ends to the compute warps through shared memory.  The compute warps
+// only load, add and store, striding over each sub-block as one grid so that at any moment the
+// whole GPU reads neighbouring vectors of each part.
 #include <cstdint>
 #include <cstring>
 #include <new>
@@ -35,7 +38,7 @@ struct ReduceParams {
     uint32_t vrow;         // 16-byte vectors per row
     uint32_t contig;       // rows back to back (pitch == vrow * 16): a sub-block is one range
     uint32_t* counters;    // [P * J]: CTAs done with (b, j) this launch; zero between launches
-    uint32_t* err;         // group waits that ran out
+    uint32_t* err;         // waits that ran out
 };
 
 // f32 lanes of a 16-byte vector, and the conversions (bf16 -> f32 is exact; f32 -> bf16 rounds
@@ -75,86 +78,164 @@ template <> struct Lanes<DTT_F32> {
     }
 };
 
-__device__ __forceinline__ uint4 ld16(const char* p) { return *reinterpret_cast<const uint4*>(p); }
 __device__ __forceinline__ void st16(char* p, const uint4& v) { *reinterpret_cast<uint4*>(p) = v; }
 
-// P ranks known at compile time, so each thread's loads of a vector's parts (at most 8 at a
-// time, U vectors at once) are in flight together; the adds still go in rank order.
+// Threads per reduce CTA at most: a control warp and up to 15 compute warps of ~60 registers.
+constexpr uint32_t kReduceMaxThreads = 512;
+
+__device__ __forceinline__ uint32_t sm_addr(const void* q) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(q));
+}
+__device__ __forceinline__ uint32_t ld_acquire_cta(const uint32_t* q) {
+    uint32_t v;
+    asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(sm_addr(q)) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release_cta(uint32_t* q, uint32_t v) {
+    asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(sm_addr(q)), "r"(v) : "memory");
+}
+__device__ __forceinline__ void red_release_cta(uint32_t* q, uint32_t v) {
+    asm volatile("red.release.cta.shared::cta.add.u32 [%0], %1;" ::"r"(sm_addr(q)), "r"(v) : "memory");
+}
+// 16 bytes through L2 only: every part is read once, and no line read before the control
+// thread's acquire can be served from L1.
+__device__ __forceinline__ uint4 ld_cg(const char* q) {
+    return __ldcg(reinterpret_cast<const uint4*>(q));
+}
+
+// Shared memory of a CTA: the sub-blocks published to the compute warps, the abort flag, and
+// per sub-block the CTA's compute warps done with it.
+enum { kReady = 0, kAbort = 1, kDone = 2 };
+
 template <int DT, int P>
-__global__ void __launch_bounds__(1024) reduce_kernel(const __grid_constant__ ReduceParams p) {
+__global__ void __launch_bounds__(kReduceMaxThreads) reduce_kernel(const __grid_constant__ ReduceParams p) {
+    extern __shared__ __align__(16) uint32_t ctl[];   // [kDone + P * J]
     using E = Lanes<DT>;
     constexpr int B = P < 8 ? P : 8;                 // parts loaded together
-    constexpr int U = P <= 2 ? 4 : (P <= 4 ? 2 : 1); // vectors a thread takes at once
-    const uint32_t G = gridDim.x;
-    const uint64_t per_unit = p.Mj * p.vrow;         // vectors in one sub-block
-    const uint64_t lo = per_unit * blockIdx.x / G, hi = per_unit * (blockIdx.x + 1) / G;
-    const uint64_t stride = (uint64_t)blockDim.x * U;
+    constexpr int U = P <= 2 ? 4 : (P <= 4 ? 2 : 1); // vectors a lane takes at once
+    const uint32_t units = (uint32_t)P * p.J;
+    for (uint32_t i = threadIdx.x; i < kDone + units; i += blockDim.x) ctl[i] = 0;
+    __syncthreads();
+    const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31u;
+    const uint32_t NCW = (blockDim.x >> 5) - 1;       // compute warps
 
-    for (uint32_t b = 0; b < (uint32_t)P; ++b) {
-        for (uint32_t j = 0; j < p.J; ++j) {
-            const uint32_t u = b * p.J + j;          // the group (b, j), and its counter
-            if (dtt_wait_group(p.rs[b], u, p.max_polls) != 0) {
-                // this CTA stops: (b, j) and every later sub-block stay unmarked, so the
-                // all-gather plan's wait reports them short
-                if (dtt_dev::first_thread()) atomicAdd(p.err, 1u);
-                return;
-            }
-            const uint64_t first = (b * p.Mb + j * p.Mj) * p.pitch;   // the sub-block in the vector
-            const char* slot0 = p.stage[b] + p.slot_off + j * p.Mj * p.pitch;
-            char* own = p.bufs[b] + first;
-            for (uint64_t t0 = lo + threadIdx.x; t0 < hi; t0 += stride) {
-                uint64_t off[U];
-                bool in[U];
-#pragma unroll
-                for (int k = 0; k < U; ++k) {
-                    const uint64_t t = t0 + (uint64_t)k * blockDim.x;
-                    in[k] = t < hi;
-                    off[k] = p.contig ? t * 16 : (t / p.vrow) * p.pitch + (t % p.vrow) * 16;
+    if (warp == 0) {
+        if (lane != 0) return;
+        // The control thread.  Publishing unit u (ready = u + 1, release at CTA scope) follows
+        // its acquire of u's group at GPU scope, so the compute warps' loads of u follow every
+        // copy of u.  Completing u follows its acquire of the compute warps' count (CTA scope),
+        // so its acq_rel add on the global counter releases all of the CTA's stores of u; the
+        // CTA whose add completes the count has every CTA's stores, resets the counter for the
+        // next launch (stream-ordered after this one) and marks the all-gather chunk.
+        uint32_t nw = 0, nd = 0;                      // next to publish, next to complete
+        uint64_t idle = 0;
+        uint32_t ns = 0;
+        while (nd < units) {
+            bool progress = false;
+            if (nw < units) {
+                uint64_t target = 0;
+                const uint64_t* w = dtt_dev::group_word(p.rs[nw / p.J], nw, &target);
+                if (!w) break;                        // a plan without the group (misuse bit set)
+                if (dtt_dev::ld_acquire(w) >= target) {
+                    st_release_cta(ctl + kReady, ++nw);
+                    progress = true;
                 }
-                float acc[U][E::n];
-#pragma unroll
-                for (int s0 = 0; s0 < P; s0 += B) {
-                    uint4 v[U][B] = {};   // lanes past the sub-block's end stay zero (never stored)
-#pragma unroll
-                    for (int k = 0; k < U; ++k)
-#pragma unroll
-                        for (int i = 0; i < B; ++i) {
-                            const uint32_t s = (uint32_t)(s0 + i);
-                            if (in[k] && s < (uint32_t)P)
-                                v[k][i] = ld16((s == b ? own : slot0 + s * p.slot_bytes) + off[k]);
-                        }
-#pragma unroll
-                    for (int k = 0; k < U; ++k)
-#pragma unroll
-                        for (int i = 0; i < B; ++i) {
-                            if (s0 + i >= P) continue;
-                            float f[E::n];
-                            E::unpack(v[k][i], f);
-#pragma unroll
-                            for (int e = 0; e < E::n; ++e) acc[k][e] = (s0 + i == 0) ? f[e] : acc[k][e] + f[e];
-                        }
-                }
-#pragma unroll
-                for (int k = 0; k < U; ++k)
-                    if (in[k]) st16(own + off[k], E::pack(acc[k]));
             }
-            // One mark for (b, j): each CTA orders its stores before an acq_rel add; the CTA whose
-            // add completes the count has acquired every other CTA's stores, resets the counter
-            // for the next launch (stream-ordered after this one) and marks.
-            __syncthreads();
-            if (dtt_dev::first_thread()) {
+            if (nd < nw && ld_acquire_cta(ctl + kDone + nd) == NCW) {
                 uint32_t old;
-                asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(p.counters + u) : "memory");
-                if (old + 1 == G) {
-                    asm volatile("st.relaxed.gpu.global.u32 [%0], 0;" ::"l"(p.counters + u) : "memory");
+                asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(p.counters + nd) : "memory");
+                if (old + 1 == gridDim.x) {
+                    asm volatile("st.relaxed.gpu.global.u32 [%0], 0;" ::"l"(p.counters + nd) : "memory");
+                    const uint32_t b = nd / p.J, j = nd - b * p.J;
                     dtt_dev::mark_one(p.ag[b], p.ag[b].first_chunk + j);
                 }
+                ++nd;
+                progress = true;
+            }
+            if (progress) {
+                idle = 0;
+                ns = 0;
+                continue;
+            }
+            if (++idle > p.max_polls) break;          // nothing moved for max_polls polls
+            __nanosleep(ns);
+            ns = ns < 256 ? ns + 32 : 256;
+        }
+        if (nd < units) {
+            // gave up: the sub-blocks from nd on stay unmarked, so the all-gather plan's wait
+            // reports them short; the compute warps stop at the next one not yet published
+            atomicAdd(p.err, 1u);
+            st_release_cta(ctl + kAbort, 1);
+        }
+        return;
+    }
+
+    // compute warps: each sub-block as one grid of NCW * gridDim.x warps
+    const uint64_t per_unit = p.Mj * p.vrow;          // vectors in one sub-block
+    const uint64_t stride = (uint64_t)gridDim.x * NCW * 32;
+    const uint64_t first_t = ((uint64_t)blockIdx.x * NCW + (warp - 1)) * 32 + lane;
+    for (uint32_t u = 0; u < units; ++u) {
+        int go = 1;
+        if (lane == 0) {
+            uint32_t ns = 0;
+            for (uint64_t i = 0;; ++i) {
+                if (ld_acquire_cta(ctl + kReady) > u) break;
+                if (ld_acquire_cta(ctl + kAbort) || i > 4 * p.max_polls + (1u << 20)) { go = 0; break; }
+                __nanosleep(ns);
+                ns = ns < 128 ? ns + 16 : 128;
             }
         }
+        go = __shfl_sync(0xFFFFFFFFu, go, 0);
+        if (!go) return;
+        __syncwarp();        // the lanes' loads below follow lane 0's acquire
+        const uint32_t b = u / p.J, j = u - b * p.J;
+        char* own = p.bufs[b] + (b * p.Mb + j * p.Mj) * p.pitch;
+        const char* slot0 = p.stage[b] + p.slot_off + j * p.Mj * p.pitch;
+        for (uint64_t t0 = first_t; t0 < per_unit; t0 += stride * U) {
+            uint64_t off[U];
+            bool in[U];
+#pragma unroll
+            for (int k = 0; k < U; ++k) {
+                const uint64_t t = t0 + (uint64_t)k * stride;
+                in[k] = t < per_unit;
+                off[k] = p.contig ? t * 16 : (t / p.vrow) * p.pitch + (t % p.vrow) * 16;
+            }
+            float acc[U][E::n];
+#pragma unroll
+            for (int s0 = 0; s0 < P; s0 += B) {
+                uint4 v[U][B] = {};   // lanes past the sub-block's end stay zero (never stored)
+#pragma unroll
+                for (int k = 0; k < U; ++k)
+#pragma unroll
+                    for (int i = 0; i < B; ++i) {
+                        const uint32_t s = (uint32_t)(s0 + i);
+                        if (in[k] && s < (uint32_t)P)
+                            v[k][i] = ld_cg((s == b ? own : slot0 + s * p.slot_bytes) + off[k]);
+                    }
+#pragma unroll
+                for (int k = 0; k < U; ++k)
+#pragma unroll
+                    for (int i = 0; i < B; ++i) {
+                        if (s0 + i >= P) continue;
+                        float f[E::n];
+                        E::unpack(v[k][i], f);
+#pragma unroll
+                        for (int e = 0; e < E::n; ++e) acc[k][e] = (s0 + i == 0) ? f[e] : acc[k][e] + f[e];
+                    }
+            }
+#pragma unroll
+            for (int k = 0; k < U; ++k)
+                if (in[k]) st16(own + off[k], E::pack(acc[k]));
+        }
+        __syncwarp();        // the warp's stores before lane 0's release
+        if (lane == 0) red_release_cta(ctl + kDone + u, 1);
     }
 }
 
 using ReduceFn = void (*)(ReduceParams);
+
+// Sub-blocks of one all-reduce in all: the reduce kernel keeps a shared-memory counter for each.
+constexpr uint32_t kMaxUnits = 4096;
 
 // The instance for a dtype and P = 2 .. DTT_MAX_RANKS.
 template <int DT>
@@ -187,12 +268,17 @@ ReduceFn reduce_entry(uint32_t dtype, uint32_t P) {
 }  // namespace
 
 cudaError_t preload_allreduce_kernels() {
-    for (uint32_t P = 2; P <= DTT_MAX_RANKS; ++P)
+    int dev = 0, optin = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    for (uint32_t P = 2; P <= DTT_MAX_RANKS && e == cudaSuccess; ++P)
         for (uint32_t dt : {(uint32_t)DTT_BF16, (uint32_t)DTT_F32}) {
-            const cudaError_t e = prepare_kernel(reduce_entry(dt, P));
-            if (e != cudaSuccess) return e;
+            e = prepare_kernel(reduce_entry(dt, P));
+            if (e == cudaSuccess)
+                e = cudaFuncSetAttribute(reduce_entry(dt, P), cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+            if (e != cudaSuccess) break;
         }
-    return cudaSuccess;
+    return e;
 }
 
 }  // namespace dtt
@@ -209,6 +295,10 @@ struct dtt_allreduce {
     dtt_plan* ag = nullptr;
     uint32_t* d_counters = nullptr;
     uint64_t max_polls = 0;
+    size_t smem = 0;                     // the reduce kernel's dynamic shared memory
+    bool serial = false;                 // deferred_copier = 1: every kernel after its inputs
+    cudaEvent_t ev_rs = nullptr;         // serial: the reduce-scatter copier has finished
+    cudaEvent_t ev_reduce = nullptr;     // serial: the reduce has finished
 };
 
 namespace {
@@ -218,6 +308,8 @@ void release(dtt_allreduce* ar) {
     if (ar->rs) dtt_plan_close(ar->rs);
     if (ar->ag) dtt_plan_close(ar->ag);
     if (ar->d_counters) cudaFree(ar->d_counters);
+    if (ar->ev_rs) cudaEventDestroy(ar->ev_rs);
+    if (ar->ev_reduce) cudaEventDestroy(ar->ev_reduce);
     delete ar;
 }
 
@@ -228,13 +320,14 @@ struct ScheduleSet {
     }
 };
 
-// The bulk-copy copier the all-reduce defaults to: two one-warp CTAs per SM, two 16 KiB stages
-// each -- light on registers and threads, so both plans' copiers and the reduce fit an SM.
+// The bulk-copy copier the all-reduce defaults to: three one-warp CTAs per SM, two 16 KiB
+// stages each -- light on registers and threads, so both plans' copiers and the reduce fit an SM
+// (the reduce takes almost no shared memory).
 dtt_plan_opts default_opts() {
     dtt_plan_opts o;
     dtt_plan_opts_default(&o);
     o.method = DTT_COPY_TMA;
-    o.ctas_per_sm = 2;
+    o.ctas_per_sm = 3;
     o.piece_bytes = 16384;
     o.stages = 2;
     return o;
@@ -243,14 +336,14 @@ dtt_plan_opts default_opts() {
 int check_opts(const dtt_plan_opts& o, const char* which) {
     if (o.method == DTT_COPY_ENGINE)
         return fail(DTT_EINVAL, "dtt_allreduce_create: the %s plan cannot use the copy-engine transport", which);
-    if (o.deferred_copier || o.overlap)
-        return fail(DTT_EINVAL, "dtt_allreduce_create: the %s plan's copier runs from start, rounds one at a time "
-                                "(deferred_copier and overlap must be 0)", which);
+    if (o.deferred_copier > 1 || o.overlap)
+        return fail(DTT_EINVAL, "dtt_allreduce_create: the %s plan runs rounds one at a time with its copier "
+                                "launched at start or in order (overlap 0, deferred_copier 0 or 1)", which);
     return DTT_OK;
 }
 
-// The reduce kernel's CTAs beside both copiers' on one SM.
-int check_room(const dtt_allreduce* ar) {
+// The reduce kernel's CTAs beside both copiers' on one SM (quiet: report no error, only the code).
+int check_room(const dtt_allreduce* ar, bool quiet = false) {
     CopierRoom a, b;
     int rc = plan_copier_room(ar->rs, &a);
     if (rc == DTT_OK) rc = plan_copier_room(ar->ag, &b);
@@ -269,9 +362,10 @@ int check_room(const dtt_allreduce* ar) {
     const uint64_t per_sm = (ar->d.reduce_ctas + (uint64_t)sms - 1) / (uint64_t)sms;
     const uint64_t r_thr = per_sm * ar->d.reduce_threads;
     const uint64_t r_regs = r_thr * (((uint64_t)fa.numRegs + 7) / 8 * 8);
-    const uint64_t r_smem = per_sm * (fa.sharedSizeBytes + (uint64_t)reserved);
+    const uint64_t r_smem = per_sm * (fa.sharedSizeBytes + ar->smem + (uint64_t)reserved);
     if (a.ctas + b.ctas + per_sm > (uint64_t)blocks || a.threads + b.threads + r_thr > (uint64_t)thr ||
-        a.regs + b.regs + r_regs > (uint64_t)regs || a.smem + b.smem + r_smem > (uint64_t)smem)
+        a.regs + b.regs + r_regs > (uint64_t)regs || a.smem + b.smem + r_smem > (uint64_t)smem) {
+        if (quiet) return DTT_EINVAL;
         return fail(DTT_EINVAL,
                     "dtt_allreduce_create: per SM, the two copiers (%u + %u CTAs, %u + %u threads, %llu + %llu "
                     "registers, %llu + %llu bytes of shared memory) and %llu reduce CTA(s) of %u threads x %d "
@@ -280,6 +374,7 @@ int check_room(const dtt_allreduce* ar) {
                     a.ctas, b.ctas, a.threads, b.threads, (unsigned long long)a.regs, (unsigned long long)b.regs,
                     (unsigned long long)a.smem, (unsigned long long)b.smem, (unsigned long long)per_sm,
                     ar->d.reduce_threads, fa.numRegs, thr, regs, smem);
+    }
     return DTT_OK;
 }
 
@@ -299,7 +394,7 @@ int dtt_allreduce_create(void* const* bufs, uint64_t buf_bytes, void* const* sta
     if (d.dtype != DTT_BF16 && d.dtype != DTT_F32)
         return fail(DTT_EINVAL, "dtt_allreduce_create: dtype must be DTT_BF16 or DTT_F32");
     if (d.sub_blocks == 0) d.sub_blocks = 1;
-    if (d.reduce_threads == 0) d.reduce_threads = 512;
+    if (d.reduce_threads == 0) d.reduce_threads = 512;   // a control warp and 15 compute warps
     const uint64_t eb = d.dtype == DTT_BF16 ? 2 : 4;
     if (d.block_rows == 0 || d.cols == 0 || d.block_rows % d.sub_blocks)
         return fail(DTT_EINVAL, "dtt_allreduce_create: block_rows and cols must be positive, sub_blocks must divide block_rows");
@@ -309,11 +404,13 @@ int dtt_allreduce_create(void* const* bufs, uint64_t buf_bytes, void* const* sta
     if (d.pitch == 0) d.pitch = rb;
     if (rb % 16 || d.pitch % 16 || d.pitch < rb)
         return fail(DTT_EINVAL, "dtt_allreduce_create: row bytes and pitch must be multiples of 16, pitch >= row bytes");
-    if (d.reduce_threads % 32 || d.reduce_threads > 1024)
-        return fail(DTT_EINVAL, "dtt_allreduce_create: reduce_threads must be a multiple of 32, at most 1024");
+    if (d.reduce_threads % 32 || d.reduce_threads < 64 || d.reduce_threads > kReduceMaxThreads)
+        return fail(DTT_EINVAL, "dtt_allreduce_create: reduce_threads must be a multiple of 32 in [64, %u] "
+                                "(a control warp and compute warps)", kReduceMaxThreads);
     const uint64_t Mj = d.block_rows / d.sub_blocks;
-    if (Mj * (rb / 16) >= (1ull << 40) || (uint64_t)P * d.sub_blocks > (1ull << 20))
-        return fail(DTT_EINVAL, "dtt_allreduce_create: too many sub-blocks or too large a sub-block");
+    if (Mj * (rb / 16) >= (1ull << 40) || (uint64_t)P * d.sub_blocks > kMaxUnits)
+        return fail(DTT_EINVAL, "dtt_allreduce_create: at most %u sub-blocks in all (P x sub_blocks), "
+                                "each under 2^40 vectors", kMaxUnits);
     const uint64_t M = (uint64_t)P * d.block_rows;
     const uint64_t vec_bytes = (M - 1) * d.pitch + rb;
     const uint64_t slots = (uint64_t)P * d.block_rows * d.pitch;   // the P slots
@@ -333,6 +430,9 @@ int dtt_allreduce_create(void* const* bufs, uint64_t buf_bytes, void* const* sta
     dtt_plan_opts ao = ag_opts ? *ag_opts : default_opts();
     int rc = check_opts(ro, "reduce-scatter");
     if (rc == DTT_OK) rc = check_opts(ao, "all-gather");
+    if (rc == DTT_OK && ro.deferred_copier != ao.deferred_copier)
+        rc = fail(DTT_EINVAL, "dtt_allreduce_create: both plans launch their copiers the same way "
+                              "(deferred_copier 0 for both, or 1 for both)");
     if (rc == DTT_OK) rc = preload_once();
     if (rc != DTT_OK) return rc;
     int dev = 0, sms = 0;
@@ -357,6 +457,7 @@ int dtt_allreduce_create(void* const* bufs, uint64_t buf_bytes, void* const* sta
     ar->slot_off = slot_off;
     ar->slot_bytes = d.block_rows * d.pitch;
     ar->max_polls = ro.max_polls ? ro.max_polls : (1ull << 22);
+    ar->serial = ro.deferred_copier == 1;
     for (uint32_t r = 0; r < P; ++r) {
         ar->bufs[r] = static_cast<char*>(bufs[r]);
         ar->stage[r] = static_cast<char*>(staging ? staging[r] : bufs[r]);
@@ -409,7 +510,13 @@ int dtt_allreduce_create(void* const* bufs, uint64_t buf_bytes, void* const* sta
         rc = dtt_plan_define_groups(ar->rs, n, offs.data(), ids.data());
     }
     if (rc == DTT_OK) rc = dtt_plan_create(bufs, buf_bytes, P, ag_s.s.data(), &ao, ag_copy_stream, &ar->ag);
-    if (rc == DTT_OK) rc = check_room(ar);
+    // in order (serial) nothing spins beside the reduce: no room to check
+    ar->smem = (2 + (size_t)P * d.sub_blocks) * sizeof(uint32_t);
+    if (rc == DTT_OK && !ar->serial) rc = check_room(ar);
+    if (rc == DTT_OK && ar->serial &&
+        (cudaEventCreateWithFlags(&ar->ev_rs, cudaEventDisableTiming) != cudaSuccess ||
+         cudaEventCreateWithFlags(&ar->ev_reduce, cudaEventDisableTiming) != cudaSuccess))
+        rc = fail(DTT_ECUDA, "dtt_allreduce_create: cannot create an event");
     if (rc == DTT_OK) {
         const size_t cb = (size_t)P * d.sub_blocks * sizeof(uint32_t);
         if (cudaMalloc(reinterpret_cast<void**>(&ar->d_counters), cb) != cudaSuccess)
@@ -470,13 +577,28 @@ int dtt_allreduce_reduce(dtt_allreduce* ar, uint32_t* err, cudaStream_t stream) 
     p.contig = ar->pitch == ar->rb ? 1u : 0u;
     p.counters = ar->d_counters;
     p.err = err;
+    if (ar->serial) {
+        // the reduce-scatter copier after the producers (on the producer stream so far), the
+        // reduce after that copier
+        const int rc = dtt_plan_launch_copier(ar->rs);
+        if (rc != DTT_OK) return rc;
+        DTT_CUDA_TRY(cudaEventRecord(ar->ev_rs, plan_copy_stream(ar->rs)));
+        DTT_CUDA_TRY(cudaStreamWaitEvent(stream, ar->ev_rs, 0));
+    }
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(ar->d.reduce_ctas, 1, 1);
     cfg.blockDim = dim3(ar->d.reduce_threads, 1, 1);
+    cfg.dynamicSmemBytes = ar->smem;
     cfg.stream = stream;
     void* args[] = {&p};
     const cudaError_t e = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(reduce_entry(ar->d.dtype, ar->P)), args);
     if (e != cudaSuccess) return fail(DTT_ECUDA, "dtt_allreduce_reduce: launch failed: %s", cudaGetErrorString(e));
+    if (ar->serial) {
+        // the all-gather copier after the reduce (and after the producer stream's work)
+        DTT_CUDA_TRY(cudaEventRecord(ar->ev_reduce, stream));
+        DTT_CUDA_TRY(cudaStreamWaitEvent(plan_copy_stream(ar->ag), ar->ev_reduce, 0));
+        return dtt_plan_launch_copier(ar->ag);
+    }
     return DTT_OK;
 }
 
@@ -486,7 +608,10 @@ int dtt_allreduce_wait(dtt_allreduce* ar, dtt_report* rs_report, dtt_report* ag_
     const std::string msg = a != DTT_OK ? std::string(dtt_last_error()) : std::string();
     const int b = dtt_plan_wait(ar->ag, ag_report);
     if (a != DTT_OK) return fail(a, "reduce-scatter: %s", msg.c_str());
-    if (b != DTT_OK) return fail(b, "all-gather: %s", dtt_last_error());
+    if (b != DTT_OK) {
+        const std::string m2 = dtt_last_error();
+        return fail(b, "all-gather: %s", m2.c_str());
+    }
     return DTT_OK;
 }
 

@@ -701,7 +701,8 @@ int dtt_consumer_gather(dtt_plan* plan, uint32_t rank, void* dst, uint64_t max_p
  *    and the others when they land, so one group wait covers them all.
  *  - dtt_allreduce_reduce: for every (b, j), b-major, waits for that group at rank b, adds rank
  *    b's own rows and the P - 1 slots in rank order, writes the sum over b's own rows and marks
- *    rank b's all-gather chunk j (once: the last of its CTAs to finish issues the mark).
+ *    rank b's all-gather chunk j (once: the last of its warps to finish issues the mark).  At
+ *    most 4096 sub-blocks in all (P x sub_blocks).
  *  - All-gather plan: rank b's chunk j (sub-block j of block b) goes to every other rank at the
  *    same rows.
  * A round: dtt_allreduce_start, the producers write every rank's vector and mark its
@@ -716,19 +717,26 @@ typedef struct dtt_allreduce_desc {
     uint64_t cols;           /* elements per row; cols x element bytes a multiple of 16 */
     uint64_t pitch;          /* bytes between rows, a multiple of 16; 0 = cols x element bytes */
     uint32_t reduce_ctas;    /* CTAs of the reduce kernel; 0 = one per SM */
-    uint32_t reduce_threads; /* threads per reduce CTA (a multiple of 32, <= 1024); 0 = 512 */
+    uint32_t reduce_threads; /* threads per reduce CTA: one control warp (the group waits, the
+                                counts and marks) and the rest compute warps (loads, adds,
+                                stores); a multiple of 32 in [64, 512]; 0 = 512 */
 } dtt_allreduce_desc;
 
 /* Build both plans and the reduce kernel's counters.  bufs: host array of P (2..16) device
  * pointers, buf_bytes each, 16-byte aligned; staging: NULL (slots in bufs after the vector) or
  * a host array of P device pointers, staging_bytes each, 16-byte aligned.  rs_opts / ag_opts:
- * the plans' options (NULL: bulk-copy copiers of two 32-thread CTAs per SM with two 16 KiB
+ * the plans' options (NULL: bulk-copy copiers of three 32-thread CTAs per SM with two 16 KiB
  * stages each); the library sets allgather = 0 and the destination buffers itself.  Both
  * copiers spin while the reduce kernel waits on the first one's deliveries, so the two
  * copiers' CTAs and the reduce's must fit on an SM together (threads, registers, shared
- * memory): checked here, DTT_EINVAL otherwise.  Not with the copy-engine transport,
- * deferred_copier or overlap (DTT_EINVAL).  Copy streams: as dtt_plan_create (NULL: each plan
- * makes its own).  The caller owns the buffers; the all-reduce owns its plans.
+ * memory): checked here, DTT_EINVAL otherwise.  deferred_copier = 1 on both plans runs the
+ * round in order instead -- the reduce-scatter copier after the producers, the reduce after that
+ * copier, the all-gather copier after the reduce (dtt_allreduce_reduce launches all three), so
+ * it completes where kernels run one at a time (a profiler that serialises launches); nothing
+ * then runs beside the reduce and no room is checked.  Not with the copy-engine transport,
+ * overlap, deferred_copier = 2 or the two plans' deferred_copier differing (DTT_EINVAL).  Copy
+ * streams: as dtt_plan_create (NULL: each plan makes its own).  The caller owns the buffers;
+ * the all-reduce owns its plans.
  * Errors: DTT_EINVAL, DTT_EOVERLAP, DTT_ENOMEM, DTT_ECUDA (nothing stays allocated). */
 int dtt_allreduce_create(void* const* bufs, uint64_t buf_bytes, void* const* staging,
                          uint64_t staging_bytes, uint32_t P, const dtt_allreduce_desc* desc,
@@ -747,10 +755,14 @@ int dtt_allreduce_plans(const dtt_allreduce* ar, dtt_plan** rs, dtt_plan** ag);
 int dtt_allreduce_start(dtt_allreduce* ar, cudaStream_t producer_stream, dtt_handle* rs_handles);
 
 /* Launch the reduce kernel on `stream`, normally the producer stream after the producers: its
- * CTAs spin on group waits, so on another stream the producers' CTAs must fit beside it.
- * err: device uint32, incremented by a CTA whose group wait ran out (at most the
- * reduce-scatter plan's max_polls polls); that CTA stops, the all-gather chunks it had not
- * finished stay unmarked and dtt_allreduce_wait fails.  Errors: DTT_ESTATE (a plan not
+ * CTAs spin on group waits, so on another stream the producers' CTAs must fit beside it.  In
+ * order (deferred_copier = 1) it also launches the reduce-scatter copier before the reduce
+ * (ordered after the producer stream's work so far) and the all-gather copier after it.
+ * In each CTA one control thread polls the sub-blocks' groups ahead of the work and counts the
+ * CTA's finished sub-blocks (the marks); the compute warps only load, add and store.
+ * err: device uint32, incremented by a CTA whose control thread saw nothing move for the
+ * reduce-scatter plan's max_polls polls; that CTA stops, the all-gather chunks not yet marked
+ * stay so and dtt_allreduce_wait fails.  Errors: DTT_ESTATE (a plan not
  * RUNNING), DTT_EINVAL, DTT_ECUDA. */
 int dtt_allreduce_reduce(dtt_allreduce* ar, uint32_t* err, cudaStream_t stream);
 

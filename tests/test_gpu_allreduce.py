@@ -34,7 +34,7 @@ def _opts(copier, **kw):
 
 class Case:
     def __init__(self, P, Mb, cols, J, dtype, separate=False, pitch=0, copier="bulk", reduce_ctas=0,
-                 reduce_threads=0, group=1, max_polls=0, oracle=True):
+                 reduce_threads=0, group=1, max_polls=0, oracle=True, in_order=False):
         self.P, self.Mb, self.cols, self.J, self.dtype = P, Mb, cols, J, dtype
         # the oracle's model of both plans (small cases; at full size only its layout is used)
         self.o = A.TwoShot(P, Mb, cols, dtype, J, pitch=pitch or None, separate=separate) if oracle else None
@@ -46,6 +46,8 @@ class Case:
         self.staging = [torch.zeros(staging_bytes, dtype=torch.uint8, device=dev) for _ in range(P)] \
             if separate else None
         kw = dict(max_polls=max_polls) if max_polls else {}
+        if in_order:
+            kw["deferred_copier"] = 1   # each kernel after its inputs (a serialising profiler's case)
         self.ar = D.AllReduce(self.bufs, self.buf_bytes, dtype, Mb, cols, sub_blocks=J, pitch=pitch,
                               staging=self.staging, staging_bytes=staging_bytes,
                               rs_opts=_opts(copier, **kw), ag_opts=_opts(copier, **kw),
@@ -103,6 +105,9 @@ CASES = {
     "p5_bf16_one_row_sub_blocks": dict(P=5, Mb=3, cols=256, J=3, dtype="bf16"),   # 32 vectors, 152 CTAs
     "p4_bf16_few_ctas": dict(P=4, Mb=256, cols=2048, J=4, dtype="bf16", reduce_ctas=7, reduce_threads=96),
     "p6_f32_pitched_staging": dict(P=6, Mb=12, cols=36, J=4, dtype="f32", pitch=160, separate=True),
+    "p4_bf16_in_order": dict(P=4, Mb=32, cols=512, J=4, dtype="bf16", in_order=True),
+    "p3_f32_in_order_staging_vector": dict(P=3, Mb=20, cols=64, J=2, dtype="f32", separate=True,
+                                           copier="vector", in_order=True),
 }
 
 

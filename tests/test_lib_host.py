@@ -411,12 +411,14 @@ def _allreduce_create(P=2, bufs=None, buf_bytes=1 << 20, staging=None, staging_b
     ("pitch not a 16-byte multiple", dict(pitch=520), "multiples of 16"),
     ("pitch below the row", dict(pitch=496), "pitch >= row bytes"),
     ("reduce threads", dict(reduce_threads=100), "reduce_threads"),
+    ("one warp", dict(reduce_threads=32), "reduce_threads"),
     ("buffer too small in place", dict(buf_bytes=2 * 128 * 512 - 16), "cannot hold"),
     ("staging too small", dict(staging=[0x100000, 0x200000], staging_bytes=1000), "staging buffers need"),
     ("unaligned buffer", dict(bufs=[0x10000, 0x20008]), "16-byte aligned"),
     ("copy-engine reduce-scatter", dict(rs=D.dtt_plan_opts_default(method=2)), "copy-engine"),
     ("overlapped all-gather", dict(ag=D.dtt_plan_opts_default(overlap=1)), "overlap"),
-    ("deferred reduce-scatter", dict(rs=D.dtt_plan_opts_default(deferred_copier=2)), "deferred_copier"),
+    ("copier beside, deferred", dict(rs=D.dtt_plan_opts_default(deferred_copier=2)), "deferred_copier"),
+    ("one plan in order", dict(rs=D.dtt_plan_opts_default(deferred_copier=1)), "same way"),
 ])
 def test_allreduce_arguments_are_checked_before_any_device_call(case, kw, words):
     rc, msg = _allreduce_create(**kw)
