@@ -39,7 +39,9 @@ NCU_TRAFFIC = {("c2_chunks_p4", "copier_bulk_kernel"): 474700544,
                # captured with 2000 rows per rank (--rows 2000) and scaled by the rows, 4x
                ("c3_tiles_p8", "copier_bulk_kernel"): 8009544192,
                ("c5_gemm_p4", "gemm2_producer_kernel"): 184814208,
-               ("c5_gemm_p4", "copier_kernel"): 206209536}
+               ("c5_gemm_p4", "copier_kernel"): 206209536,
+               # the two-shot all-reduce's reduce kernel (bench.py --allreduce --in-order), 256 threads
+               ("allreduce_p4", "reduce_kernel"): 651607040}
 # DRAM bytes (read, write) of one whole round, producer, copier and check together, from an
 # ncu range-replay capture of three rounds of the benchmark's launch (--profile-rounds 3;
 # c2 and c5 with overlapping rounds)
@@ -1003,7 +1005,8 @@ def run_ce_fanout(args):
 
 def measure_allreduce(K: int, warmup: int, isolated_rounds: int = 10, e2e_steps: int = 0,
                       clocks_dev=None, rows: int = 0, in_order: bool = False, ctas_per_sm: int = 0,
-                      stages: int = 0, piece_bytes: int = 0, fill_rounds: int = 0):
+                      stages: int = 0, piece_bytes: int = 0, fill_rounds: int = 0, reduce_ctas: int = 0,
+                      reduce_threads: int = 0):
     """The two-shot all-reduce of W.ALLREDUCE.  The collective: K rounds of start + a producer that
     only marks (dtt_publish: the vectors were written before the timed region, as an all-reduce
     benchmark's inputs are) + reduce kernel + wait + next_round (both plans' copiers launched at
@@ -1034,6 +1037,7 @@ def measure_allreduce(K: int, warmup: int, isolated_rounds: int = 10, e2e_steps:
                                        piece_bytes=piece_bytes or 16384, stages=stages or 2,
                                        deferred_copier=1 if in_order else 0)
     ar = D.AllReduce(bufs, buf_bytes, dtype, Mb, cols, sub_blocks=J, rs_opts=opts, ag_opts=opts,
+                     reduce_ctas=reduce_ctas, reduce_threads=reduce_threads,
                      rs_copy_stream=rs_cs, ag_copy_stream=ag_cs)
     Mj = Mb // J
     counters = torch.zeros(P * (M // Mj), dtype=torch.int32, device=dev)
@@ -1089,6 +1093,7 @@ def measure_allreduce(K: int, warmup: int, isolated_rounds: int = 10, e2e_steps:
         serial = D.dtt_plan_opts_default(method=D.COPY_TMA, ctas_per_sm=ctas_per_sm or 3,
                                          piece_bytes=piece_bytes or 16384, stages=stages or 2, deferred_copier=1)
         ars = D.AllReduce(bufs, buf_bytes, dtype, Mb, cols, sub_blocks=J, rs_opts=serial, ag_opts=serial,
+                          reduce_ctas=reduce_ctas, reduce_threads=reduce_threads,
                           rs_copy_stream=rs_cs, ag_copy_stream=ag_cs)
         for i in range(isolated_rounds + 2):
             h = ars.start(prod)
@@ -1175,7 +1180,7 @@ def run_allreduce(args):
     m = measure_allreduce(K, args.warmup, isolated_rounds=10, e2e_steps=0 if args.no_e2e else 10,
                           clocks_dev=dev, rows=args.rows, in_order=args.in_order,
                           ctas_per_sm=args.ctas_per_sm, stages=args.stages, piece_bytes=args.piece_bytes,
-                          fill_rounds=20)
+                          fill_rounds=20, reduce_ctas=args.reduce_ctas, reduce_threads=args.reduce_threads)
     peak, peak_kind = load_peaks()
     s = summarize_allreduce(m, peak, peak_kind)
     a = W.ALLREDUCE
@@ -1301,6 +1306,8 @@ def main(argv=None):
                     help="time the fan-out with copy engines (device-to-device memcpy) against the SM copier")
     ap.add_argument("--allreduce", action="store_true",
                     help="time the two-shot all-reduce (reduce-scatter plan, reduce kernel, all-gather plan)")
+    ap.add_argument("--reduce-ctas", type=int, default=0, help="--allreduce: reduce kernel CTAs (default: one per SM)")
+    ap.add_argument("--reduce-threads", type=int, default=0, help="--allreduce: threads per reduce CTA (default 256)")
     ap.add_argument("--in-order", action="store_true",
                     help="--allreduce: each kernel after its inputs (deferred copiers), for profiler captures")
     ap.add_argument("--consumer", action="store_true",

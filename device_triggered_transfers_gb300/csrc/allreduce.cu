@@ -170,10 +170,13 @@ __global__ void __launch_bounds__(kReduceMaxThreads) reduce_kernel(const __grid_
         return;
     }
 
-    // compute warps: each sub-block as one grid of NCW * gridDim.x warps
+    // compute warps: each sub-block as one grid of NCW * gridDim.x warps.  A warp counts itself
+    // done with a sub-block (a release at CTA scope) only after it has issued its first loads of
+    // the next one, so that the release's wait for the warp's stores overlaps those loads
     const uint64_t per_unit = p.Mj * p.vrow;          // vectors in one sub-block
     const uint64_t stride = (uint64_t)gridDim.x * NCW * 32;
     const uint64_t first_t = ((uint64_t)blockIdx.x * NCW + (warp - 1)) * 32 + lane;
+    uint32_t pending = ~0u;                           // the sub-block whose count is still owed
     for (uint32_t u = 0; u < units; ++u) {
         int go = 1;
         if (lane == 0) {
@@ -186,7 +189,7 @@ __global__ void __launch_bounds__(kReduceMaxThreads) reduce_kernel(const __grid_
             }
         }
         go = __shfl_sync(0xFFFFFFFFu, go, 0);
-        if (!go) return;
+        if (!go) return;     // (an owed count is left unpaid: nothing after it gets marked)
         __syncwarp();        // the lanes' loads below follow lane 0's acquire
         const uint32_t b = u / p.J, j = u - b * p.J;
         char* own = p.bufs[b] + (b * p.Mb + j * p.Mj) * p.pitch;
@@ -212,6 +215,10 @@ __global__ void __launch_bounds__(kReduceMaxThreads) reduce_kernel(const __grid_
                         if (in[k] && s < (uint32_t)P)
                             v[k][i] = ld_cg((s == b ? own : slot0 + s * p.slot_bytes) + off[k]);
                     }
+                if (pending != ~0u) {          // the stores it covers were ordered by __syncwarp
+                    if (lane == 0) red_release_cta(ctl + kDone + pending, 1);
+                    pending = ~0u;
+                }
 #pragma unroll
                 for (int k = 0; k < U; ++k)
 #pragma unroll
@@ -227,9 +234,13 @@ __global__ void __launch_bounds__(kReduceMaxThreads) reduce_kernel(const __grid_
             for (int k = 0; k < U; ++k)
                 if (in[k]) st16(own + off[k], E::pack(acc[k]));
         }
+        if (pending != ~0u) {                         // no vector of this sub-block here
+            if (lane == 0) red_release_cta(ctl + kDone + pending, 1);
+        }
         __syncwarp();        // the warp's stores before lane 0's release
-        if (lane == 0) red_release_cta(ctl + kDone + u, 1);
+        pending = u;
     }
+    if (lane == 0) red_release_cta(ctl + kDone + pending, 1);
 }
 
 using ReduceFn = void (*)(ReduceParams);
@@ -394,7 +405,9 @@ int dtt_allreduce_create(void* const* bufs, uint64_t buf_bytes, void* const* sta
     if (d.dtype != DTT_BF16 && d.dtype != DTT_F32)
         return fail(DTT_EINVAL, "dtt_allreduce_create: dtype must be DTT_BF16 or DTT_F32");
     if (d.sub_blocks == 0) d.sub_blocks = 1;
-    if (d.reduce_threads == 0) d.reduce_threads = 512;   // a control warp and 15 compute warps
+    // a control warp and 7 compute warps: the reduce alone is as fast with 15, but in the round
+    // the copiers then have less of each SM (418 us rounds against 440 on the benchmark's size)
+    if (d.reduce_threads == 0) d.reduce_threads = 256;
     const uint64_t eb = d.dtype == DTT_BF16 ? 2 : 4;
     if (d.block_rows == 0 || d.cols == 0 || d.block_rows % d.sub_blocks)
         return fail(DTT_EINVAL, "dtt_allreduce_create: block_rows and cols must be positive, sub_blocks must divide block_rows");

@@ -719,7 +719,7 @@ typedef struct dtt_allreduce_desc {
     uint32_t reduce_ctas;    /* CTAs of the reduce kernel; 0 = one per SM */
     uint32_t reduce_threads; /* threads per reduce CTA: one control warp (the group waits, the
                                 counts and marks) and the rest compute warps (loads, adds,
-                                stores); a multiple of 32 in [64, 512]; 0 = 512 */
+                                stores); a multiple of 32 in [64, 512]; 0 = 256 */
 } dtt_allreduce_desc;
 
 /* Build both plans and the reduce kernel's counters.  bufs: host array of P (2..16) device
