@@ -24,6 +24,9 @@ peers) make possible, and says nothing more about it.  The reading taken here is
   marks all-gather chunk (b, j).
 * Chunk numbering: rank s's reduce-scatter chunks are (b, j) in the order b*J + j (row order of
   its vector); rank b's all-gather chunks are j = 0..J-1.  Group (b, j) is group b*J + j.
+* Reduce-scatter, the other operation the same bullet names, is the first shot alone: rank b
+  ends with the sum over its own block b; its other rows keep its own partial, and no
+  all-gather plan exists (``gather=False``).
 """
 from __future__ import annotations
 
@@ -118,7 +121,7 @@ class TwoShot:
     them, driven through the oracle's plan model one round at a time."""
 
     def __init__(self, P: int, Mb: int, cols: int, dtype: str, J: int, pitch: Optional[int] = None,
-                 separate: bool = False, initial_round: int = 1):
+                 separate: bool = False, initial_round: int = 1, gather: bool = True):
         if Mb % J:
             raise ValueError("J must divide the block rows")
         self.P, self.Mb, self.cols, self.dtype, self.J = P, Mb, cols, dtype, J
@@ -130,8 +133,9 @@ class TwoShot:
         self.rs = OP.Plan(self.bufs, reduce_scatter_schedules(P, Mb, J, self.rb, self.pitch, self.slot_off),
                           allgather=False, dst_bufs=self.staging, initial_round=initial_round)
         self.rs.define_groups(reduce_groups(P, J))
+        self.gather = gather
         self.ag = OP.Plan(self.bufs, allgather_schedules(P, Mb, J, self.rb, self.pitch),
-                          allgather=False, initial_round=initial_round)
+                          allgather=False, initial_round=initial_round) if gather else None
 
     # rows of a byte buffer as storage values
     def _rows(self, buf: np.ndarray, off: int, rows: int) -> np.ndarray:
@@ -164,14 +168,15 @@ class TwoShot:
             else:
                 parts.append(self._rows(self.stage(b), self.slot_off + (s * self.Mb + j * self.Mj) * self.pitch, self.Mj))
         self._put_rows(self.bufs[b], row0 * self.pitch, allreduce(self.dtype, parts))
-        self.ag.mark_ready(b, self.ag.first[b] + j)
+        if self.gather:
+            self.ag.mark_ready(b, self.ag.first[b] + j)
 
     def round(self, partials: Sequence[np.ndarray]) -> int:
         """One round: every rank's partial vector ([M, cols] storage values) written and its
         reduce-scatter chunks marked, the copies, the reduce of every (b, j), the all-gather
         copies, both waits, both next_rounds.  Returns the round."""
         R = self.rs.start()
-        if self.ag.start() != R:
+        if self.gather and self.ag.start() != R:
             raise OP.StateError("the two plans are in different rounds")
         for s in range(self.P):
             self._put_rows(self.bufs[s], 0, np.asarray(partials[s]))
@@ -181,8 +186,9 @@ class TwoShot:
         for b in range(self.P):
             for j in range(self.J):
                 self.reduce_chunk(b, j)
-        self.ag.copier_progress()
-        for pl in (self.rs, self.ag):
+        if self.gather:
+            self.ag.copier_progress()
+        for pl in (self.rs, self.ag) if self.gather else (self.rs,):
             st = pl.wait()
             if st[0] != OP.OK:
                 raise OP.StateError(f"round {R} failed: {st}")
@@ -192,6 +198,18 @@ class TwoShot:
     def result(self, r: int) -> np.ndarray:
         """Rank r's vector rows as storage values."""
         return self._rows(self.bufs[r], 0, self.P * self.Mb)
+
+
+def reduce_scatter(dtype: str, parts: Sequence[np.ndarray], P: int, Mb: int) -> List[np.ndarray]:
+    """Each rank's vector after a reduce-scatter: block b of rank b is the sum (as ``allreduce``)
+    of every rank's block b; its other blocks are its own partial as it was."""
+    y = allreduce(dtype, parts)
+    out = []
+    for b in range(P):
+        v = np.array(parts[b], copy=True)
+        v[b * Mb:(b + 1) * Mb] = y[b * Mb:(b + 1) * Mb]
+        out.append(v)
+    return out
 
 
 def hashed_partials(dtype: str, seed: int, P: int, M: int, cols: int, rnd: int) -> List[np.ndarray]:

@@ -220,3 +220,27 @@ def test_schedules_and_groups_by_hand():
     assert A.reduce_groups(2, 2) == [[0, 4], [1, 5], [2, 6], [3, 7]]
     ag = A.allgather_schedules(2, 4, 2, 8, 8)
     assert [len(s.chunks) for s in ag] == [2, 2]
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("P,J,separate", [(2, 2, False), (4, 1, True), (3, 3, False)])
+def test_reduce_scatter_leaves_the_other_blocks_alone(dtype, P, J, separate):
+    """The first shot alone: rank b holds the sum of block b and its own partial elsewhere; the
+    slots hold the peers' partials as in the all-reduce; no all-gather plan."""
+    Mb, cols = 6, 16
+    o = A.TwoShot(P, Mb, cols, dtype, J, separate=separate, gather=False)
+    assert o.ag is None
+    for R in (1, 2):
+        parts = A.hashed_partials(dtype, 8, P, P * Mb, cols, R)
+        o.round(parts)
+        want = A.reduce_scatter(dtype, parts, P, Mb)
+        y = A.allreduce(dtype, parts)
+        for r in range(P):
+            got = o.result(r)
+            assert np.array_equal(_bits(dtype, got), _bits(dtype, want[r]))
+            # block r is the sum; every other block is rank r's own partial
+            assert np.array_equal(_bits(dtype, got[r * Mb:(r + 1) * Mb]), _bits(dtype, y[r * Mb:(r + 1) * Mb]))
+            for b in range(P):
+                if b != r:
+                    assert np.array_equal(_bits(dtype, got[b * Mb:(b + 1) * Mb]),
+                                          _bits(dtype, parts[r][b * Mb:(b + 1) * Mb]))
