@@ -1006,7 +1006,7 @@ def run_ce_fanout(args):
 def measure_allreduce(K: int, warmup: int, isolated_rounds: int = 10, e2e_steps: int = 0,
                       clocks_dev=None, rows: int = 0, in_order: bool = False, ctas_per_sm: int = 0,
                       stages: int = 0, piece_bytes: int = 0, fill_rounds: int = 0, reduce_ctas: int = 0,
-                      reduce_threads: int = 0):
+                      reduce_threads: int = 0, gather: bool = True):
     """The two-shot all-reduce of W.ALLREDUCE.  The collective: K rounds of start + a producer that
     only marks (dtt_publish: the vectors were written before the timed region, as an all-reduce
     benchmark's inputs are) + reduce kernel + wait + next_round (both plans' copiers launched at
@@ -1038,7 +1038,7 @@ def measure_allreduce(K: int, warmup: int, isolated_rounds: int = 10, e2e_steps:
                                        deferred_copier=1 if in_order else 0)
     ar = D.AllReduce(bufs, buf_bytes, dtype, Mb, cols, sub_blocks=J, rs_opts=opts, ag_opts=opts,
                      reduce_ctas=reduce_ctas, reduce_threads=reduce_threads,
-                     rs_copy_stream=rs_cs, ag_copy_stream=ag_cs)
+                     rs_copy_stream=rs_cs, ag_copy_stream=ag_cs, gather=gather)
     Mj = Mb // J
     counters = torch.zeros(P * (M // Mj), dtype=torch.int32, device=dev)
     desc = D.fill_desc(dtype, a["seed"], M, cols, rb, buf_bytes, [0] * P, Mj, cols, 1, 1,
@@ -1183,6 +1183,14 @@ def run_allreduce(args):
                           fill_rounds=20, reduce_ctas=args.reduce_ctas, reduce_threads=args.reduce_threads)
     peak, peak_kind = load_peaks()
     s = summarize_allreduce(m, peak, peak_kind)
+    # the reduce-scatter alone (the first shot: no all-gather plan), the same way
+    mr = measure_allreduce(K, args.warmup, isolated_rounds=0, rows=args.rows, in_order=args.in_order,
+                           ctas_per_sm=args.ctas_per_sm, stages=args.stages, piece_bytes=args.piece_bytes,
+                           reduce_ctas=args.reduce_ctas, reduce_threads=args.reduce_threads, gather=False)
+    t_rs = mr["round_ms"] * 1e-3
+    reduce_scatter = {"ms_per_round": mr["round_ms"], "algbw_gbs": mr["S"] / t_rs / 1e9,
+                      "algorithmic_bytes_per_round": (3 * mr["P"] - 1) * mr["S"],
+                      "hbm_frac_of_measured": (3 * mr["P"] - 1) * mr["S"] / t_rs / 1e9 / peak}
     a = W.ALLREDUCE
     cpu = None
     if not args.no_cpu_baseline:
@@ -1210,6 +1218,7 @@ def run_allreduce(args):
         "busbw_gbs": s["busbw_gbs"],
         "hbm_frac_end_to_end": s["hbm_frac_end_to_end"],
         "with_fill_producer_ms_per_round": m.get("fill_round_ms"),
+        "reduce_scatter": reduce_scatter,
         "roofline": s.get("reduce_roofline"),
         "e2e": e2e,
         "gpu_launches": 6 * K,      # marks, 2 copiers, reduce, 2 checks per round

@@ -107,7 +107,7 @@ class dtt_fill_desc(C.Structure):
 class dtt_allreduce_desc(C.Structure):
     _fields_ = [("dtype", C.c_uint32), ("sub_blocks", C.c_uint32), ("block_rows", C.c_uint64),
                 ("cols", C.c_uint64), ("pitch", C.c_uint64), ("reduce_ctas", C.c_uint32),
-                ("reduce_threads", C.c_uint32)]
+                ("reduce_threads", C.c_uint32), ("scatter_only", C.c_uint32)]
 
 
 ORDER_FN = C.CFUNCTYPE(C.c_int, C.c_uint64, C.c_void_p, C.POINTER(C.c_uint32),
@@ -683,15 +683,16 @@ class PlanView(Plan):
 class AllReduce:
     """Owner of a dtt_allreduce*: the two-shot all-reduce over P device buffers (see
     dtt_allreduce_create).  Rank r's vector is P * block_rows rows of `cols` elements of `dtype`
-    at the start of bufs[r]; every rank ends with the sum of the P vectors there.  A round:
-    start() -> handles for the producers' reduce-scatter marks, the producers, reduce(), wait(),
+    at the start of bufs[r]; every rank ends with the sum of the P vectors there (gather=False:
+    a reduce-scatter, rank b ends with the sum over its own block b only).  A round: start() ->
+    handles for the producers' reduce-scatter marks, the producers, reduce(), wait(),
     next_round()."""
 
     def __init__(self, bufs: Sequence, buf_bytes: int, dtype: str, block_rows: int, cols: int,
                  sub_blocks: int = 1, pitch: int = 0, staging: Optional[Sequence] = None,
                  staging_bytes: int = 0, rs_opts: Optional[dtt_plan_opts] = None,
                  ag_opts: Optional[dtt_plan_opts] = None, reduce_ctas: int = 0, reduce_threads: int = 0,
-                 rs_copy_stream=None, ag_copy_stream=None):
+                 rs_copy_stream=None, ag_copy_stream=None, gather: bool = True):
         self.bufs = list(bufs)
         self.P = len(self.bufs)
         self.staging = list(staging) if staging is not None else None
@@ -703,6 +704,8 @@ class AllReduce:
         d.dtype = DTYPE_CODES[dtype]
         d.sub_blocks, d.block_rows, d.cols, d.pitch = sub_blocks, block_rows, cols, pitch
         d.reduce_ctas, d.reduce_threads = reduce_ctas, reduce_threads
+        d.scatter_only = 0 if gather else 1
+        self.gather = gather
         self.desc = d
         out = C.c_void_p()
         stg = _ptr_array(self.staging) if self.staging is not None else None
@@ -715,7 +718,7 @@ class AllReduce:
         rs, ag = C.c_void_p(), C.c_void_p()
         _check(lib().dtt_allreduce_plans(self._h, C.byref(rs), C.byref(ag)))
         self.rs = PlanView(rs, self.bufs, buf_bytes, n_groups=self.P * sub_blocks)
-        self.ag = PlanView(ag, self.bufs, buf_bytes)
+        self.ag = PlanView(ag, self.bufs, buf_bytes) if gather else None
 
     def start(self, producer_stream=None):
         _check(lib().dtt_allreduce_start(self._h, _stream(producer_stream), self.handles))

@@ -37,6 +37,7 @@ struct ReduceParams {
     uint32_t J;            // sub-blocks per block
     uint32_t vrow;         // 16-byte vectors per row
     uint32_t contig;       // rows back to back (pitch == vrow * 16): a sub-block is one range
+    uint32_t gather;       // 1: mark each summed sub-block for the all-gather plan (all-reduce)
     uint32_t* counters;    // [P * J]: CTAs done with (b, j) this launch; zero between launches
     uint32_t* err;         // waits that ran out
 };
@@ -147,7 +148,7 @@ __global__ void __launch_bounds__(kReduceMaxThreads) reduce_kernel(const __grid_
                 if (old + 1 == gridDim.x) {
                     asm volatile("st.relaxed.gpu.global.u32 [%0], 0;" ::"l"(p.counters + nd) : "memory");
                     const uint32_t b = nd / p.J, j = nd - b * p.J;
-                    dtt_dev::mark_one(p.ag[b], p.ag[b].first_chunk + j);
+                    if (p.gather) dtt_dev::mark_one(p.ag[b], p.ag[b].first_chunk + j);
                 }
                 ++nd;
                 progress = true;
@@ -308,8 +309,10 @@ struct dtt_allreduce {
     uint64_t max_polls = 0;
     size_t smem = 0;                     // the reduce kernel's dynamic shared memory
     bool serial = false;                 // deferred_copier = 1: every kernel after its inputs
+    bool gather = true;                  // all-reduce (false: reduce-scatter, no all-gather plan)
     cudaEvent_t ev_rs = nullptr;         // serial: the reduce-scatter copier has finished
-    cudaEvent_t ev_reduce = nullptr;     // serial: the reduce has finished
+    cudaEvent_t ev_reduce = nullptr;     // the reduce has finished (serial; and what a
+                                         // reduce-scatter's wait waits for)
 };
 
 namespace {
@@ -357,7 +360,7 @@ int check_opts(const dtt_plan_opts& o, const char* which) {
 int check_room(const dtt_allreduce* ar, bool quiet = false) {
     CopierRoom a, b;
     int rc = plan_copier_room(ar->rs, &a);
-    if (rc == DTT_OK) rc = plan_copier_room(ar->ag, &b);
+    if (rc == DTT_OK && ar->ag) rc = plan_copier_room(ar->ag, &b);
     if (rc != DTT_OK) return rc;
     int dev = 0, sms = 0, thr = 0, regs = 0, smem = 0, reserved = 0, blocks = 0;
     cudaFuncAttributes fa{};
@@ -442,8 +445,8 @@ int dtt_allreduce_create(void* const* bufs, uint64_t buf_bytes, void* const* sta
     dtt_plan_opts ro = rs_opts ? *rs_opts : default_opts();
     dtt_plan_opts ao = ag_opts ? *ag_opts : default_opts();
     int rc = check_opts(ro, "reduce-scatter");
-    if (rc == DTT_OK) rc = check_opts(ao, "all-gather");
-    if (rc == DTT_OK && ro.deferred_copier != ao.deferred_copier)
+    if (rc == DTT_OK && !d.scatter_only) rc = check_opts(ao, "all-gather");
+    if (rc == DTT_OK && !d.scatter_only && ro.deferred_copier != ao.deferred_copier)
         rc = fail(DTT_EINVAL, "dtt_allreduce_create: both plans launch their copiers the same way "
                               "(deferred_copier 0 for both, or 1 for both)");
     if (rc == DTT_OK) rc = preload_once();
@@ -471,6 +474,7 @@ int dtt_allreduce_create(void* const* bufs, uint64_t buf_bytes, void* const* sta
     ar->slot_bytes = d.block_rows * d.pitch;
     ar->max_polls = ro.max_polls ? ro.max_polls : (1ull << 22);
     ar->serial = ro.deferred_copier == 1;
+    ar->gather = d.scatter_only == 0;
     for (uint32_t r = 0; r < P; ++r) {
         ar->bufs[r] = static_cast<char*>(bufs[r]);
         ar->stage[r] = static_cast<char*>(staging ? staging[r] : bufs[r]);
@@ -522,11 +526,12 @@ int dtt_allreduce_create(void* const* bufs, uint64_t buf_bytes, void* const* sta
                 for (uint32_t s = 0; s < P; ++s) ids[(size_t)(b * J + j) * P + s] = s * P * J + b * J + j;
         rc = dtt_plan_define_groups(ar->rs, n, offs.data(), ids.data());
     }
-    if (rc == DTT_OK) rc = dtt_plan_create(bufs, buf_bytes, P, ag_s.s.data(), &ao, ag_copy_stream, &ar->ag);
+    if (rc == DTT_OK && ar->gather)
+        rc = dtt_plan_create(bufs, buf_bytes, P, ag_s.s.data(), &ao, ag_copy_stream, &ar->ag);
     // in order (serial) nothing spins beside the reduce: no room to check
     ar->smem = (2 + (size_t)P * d.sub_blocks) * sizeof(uint32_t);
     if (rc == DTT_OK && !ar->serial) rc = check_room(ar);
-    if (rc == DTT_OK && ar->serial &&
+    if (rc == DTT_OK &&
         (cudaEventCreateWithFlags(&ar->ev_rs, cudaEventDisableTiming) != cudaSuccess ||
          cudaEventCreateWithFlags(&ar->ev_reduce, cudaEventDisableTiming) != cudaSuccess))
         rc = fail(DTT_ECUDA, "dtt_allreduce_create: cannot create an event");
@@ -555,28 +560,28 @@ int dtt_allreduce_plans(const dtt_allreduce* ar, dtt_plan** rs, dtt_plan** ag) {
 
 int dtt_allreduce_start(dtt_allreduce* ar, cudaStream_t producer_stream, dtt_handle* rs_handles) {
     if (!ar) return fail(DTT_EINVAL, "dtt_allreduce_start: NULL all-reduce");
-    if (dtt_plan_state(ar->rs) != DTT_PLAN_PREPARED || dtt_plan_state(ar->ag) != DTT_PLAN_PREPARED ||
-        dtt_plan_round(ar->rs) != dtt_plan_round(ar->ag))
+    if (dtt_plan_state(ar->rs) != DTT_PLAN_PREPARED ||
+        (ar->ag && (dtt_plan_state(ar->ag) != DTT_PLAN_PREPARED || dtt_plan_round(ar->rs) != dtt_plan_round(ar->ag))))
         return fail(DTT_ESTATE, "dtt_allreduce_start: both plans must be PREPARED for the same round");
     dtt_handle tmp[DTT_MAX_RANKS];
     int rc = dtt_plan_start(ar->rs, producer_stream, rs_handles ? rs_handles : tmp);
-    if (rc == DTT_OK) rc = dtt_plan_start(ar->ag, producer_stream, tmp);
+    if (rc == DTT_OK && ar->ag) rc = dtt_plan_start(ar->ag, producer_stream, tmp);
     return rc;
 }
 
 int dtt_allreduce_reduce(dtt_allreduce* ar, uint32_t* err, cudaStream_t stream) {
     if (!ar || !err) return fail(DTT_EINVAL, "dtt_allreduce_reduce: NULL argument");
-    if (dtt_plan_state(ar->rs) != DTT_PLAN_RUNNING || dtt_plan_state(ar->ag) != DTT_PLAN_RUNNING ||
-        dtt_plan_round(ar->rs) != dtt_plan_round(ar->ag))
+    if (dtt_plan_state(ar->rs) != DTT_PLAN_RUNNING ||
+        (ar->ag && (dtt_plan_state(ar->ag) != DTT_PLAN_RUNNING || dtt_plan_round(ar->rs) != dtt_plan_round(ar->ag))))
         return fail(DTT_ESTATE, "dtt_allreduce_reduce: both plans must be RUNNING in the same round");
-    if (stream == plan_copy_stream(ar->rs) || stream == plan_copy_stream(ar->ag))
+    if (stream == plan_copy_stream(ar->rs) || (ar->ag && stream == plan_copy_stream(ar->ag)))
         return fail(DTT_EINVAL, "dtt_allreduce_reduce: use a stream other than the plans' copy streams");
     ReduceParams p{};
     for (uint32_t r = 0; r < ar->P; ++r) {
         p.bufs[r] = ar->bufs[r];
         p.stage[r] = ar->stage[r];
         int rc = dtt_plan_handle(ar->rs, r, &p.rs[r]);
-        if (rc == DTT_OK) rc = dtt_plan_handle(ar->ag, r, &p.ag[r]);
+        if (rc == DTT_OK && ar->ag) rc = dtt_plan_handle(ar->ag, r, &p.ag[r]);
         if (rc != DTT_OK) return rc;
     }
     p.pitch = ar->pitch;
@@ -588,6 +593,7 @@ int dtt_allreduce_reduce(dtt_allreduce* ar, uint32_t* err, cudaStream_t stream) 
     p.J = ar->d.sub_blocks;
     p.vrow = (uint32_t)(ar->rb / 16);
     p.contig = ar->pitch == ar->rb ? 1u : 0u;
+    p.gather = ar->gather ? 1u : 0u;
     p.counters = ar->d_counters;
     p.err = err;
     if (ar->serial) {
@@ -606,9 +612,9 @@ int dtt_allreduce_reduce(dtt_allreduce* ar, uint32_t* err, cudaStream_t stream) 
     void* args[] = {&p};
     const cudaError_t e = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(reduce_entry(ar->d.dtype, ar->P)), args);
     if (e != cudaSuccess) return fail(DTT_ECUDA, "dtt_allreduce_reduce: launch failed: %s", cudaGetErrorString(e));
-    if (ar->serial) {
+    DTT_CUDA_TRY(cudaEventRecord(ar->ev_reduce, stream));
+    if (ar->serial && ar->ag) {
         // the all-gather copier after the reduce (and after the producer stream's work)
-        DTT_CUDA_TRY(cudaEventRecord(ar->ev_reduce, stream));
         DTT_CUDA_TRY(cudaStreamWaitEvent(plan_copy_stream(ar->ag), ar->ev_reduce, 0));
         return dtt_plan_launch_copier(ar->ag);
     }
@@ -619,6 +625,13 @@ int dtt_allreduce_wait(dtt_allreduce* ar, dtt_report* rs_report, dtt_report* ag_
     if (!ar) return fail(DTT_EINVAL, "dtt_allreduce_wait: NULL all-reduce");
     const int a = dtt_plan_wait(ar->rs, rs_report);
     const std::string msg = a != DTT_OK ? std::string(dtt_last_error()) : std::string();
+    if (!ar->ag) {
+        // a reduce-scatter: its result is the reduce kernel's stores (bounded: its waits end)
+        if (ag_report) *ag_report = dtt_report{};
+        if (a != DTT_OK) return fail(a, "reduce-scatter: %s", msg.c_str());
+        DTT_CUDA_TRY(cudaEventSynchronize(ar->ev_reduce));
+        return DTT_OK;
+    }
     const int b = dtt_plan_wait(ar->ag, ag_report);
     if (a != DTT_OK) return fail(a, "reduce-scatter: %s", msg.c_str());
     if (b != DTT_OK) {
@@ -630,10 +643,10 @@ int dtt_allreduce_wait(dtt_allreduce* ar, dtt_report* rs_report, dtt_report* ag_
 
 int dtt_allreduce_next_round(dtt_allreduce* ar) {
     if (!ar) return fail(DTT_EINVAL, "dtt_allreduce_next_round: NULL all-reduce");
-    if (dtt_plan_state(ar->rs) != DTT_PLAN_DONE || dtt_plan_state(ar->ag) != DTT_PLAN_DONE)
+    if (dtt_plan_state(ar->rs) != DTT_PLAN_DONE || (ar->ag && dtt_plan_state(ar->ag) != DTT_PLAN_DONE))
         return fail(DTT_ESTATE, "dtt_allreduce_next_round: both plans must be DONE");
     int rc = dtt_plan_next_round(ar->rs);
-    if (rc == DTT_OK) rc = dtt_plan_next_round(ar->ag);
+    if (rc == DTT_OK && ar->ag) rc = dtt_plan_next_round(ar->ag);
     return rc;
 }
 

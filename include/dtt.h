@@ -679,8 +679,8 @@ int dtt_consumer_gather(dtt_plan* plan, uint32_t rank, void* dst, uint64_t max_p
                         int32_t* status, uint32_t ctas, cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------------------- */
-/* Two-shot all-reduce ("Triggered Plans", Not supported yet: reduce-scatter and two-shot      */
-/* all-reduce are what other destinations make possible)                                     */
+/* Two-shot all-reduce and reduce-scatter ("Triggered Plans", Not supported yet: reduce-     */
+/* scatter and two-shot all-reduce are what other destinations make possible)                */
 /* ---------------------------------------------------------------------------------------- */
 
 /* The pages name the two-shot all-reduce and say nothing more of it; this is the plain
@@ -720,6 +720,10 @@ typedef struct dtt_allreduce_desc {
     uint32_t reduce_threads; /* threads per reduce CTA: one control warp (the group waits, the
                                 counts and marks) and the rest compute warps (loads, adds,
                                 stores); a multiple of 32 in [64, 512]; 0 = 256 */
+    uint32_t scatter_only;   /* 1: a reduce-scatter -- the first shot alone: rank b ends with the
+                                sum over its block b and its own partial in its other rows; no
+                                all-gather plan (ag_opts ignored, dtt_allreduce_plans gives NULL
+                                for it, and dtt_allreduce_wait also waits for the reduce kernel) */
 } dtt_allreduce_desc;
 
 /* Build both plans and the reduce kernel's counters.  bufs: host array of P (2..16) device

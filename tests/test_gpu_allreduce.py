@@ -34,10 +34,12 @@ def _opts(copier, **kw):
 
 class Case:
     def __init__(self, P, Mb, cols, J, dtype, separate=False, pitch=0, copier="bulk", reduce_ctas=0,
-                 reduce_threads=0, group=1, max_polls=0, oracle=True, in_order=False):
+                 reduce_threads=0, group=1, max_polls=0, oracle=True, in_order=False, gather=True):
         self.P, self.Mb, self.cols, self.J, self.dtype = P, Mb, cols, J, dtype
         # the oracle's model of both plans (small cases; at full size only its layout is used)
-        self.o = A.TwoShot(P, Mb, cols, dtype, J, pitch=pitch or None, separate=separate) if oracle else None
+        self.o = A.TwoShot(P, Mb, cols, dtype, J, pitch=pitch or None, separate=separate,
+                           gather=gather) if oracle else None
+        self.gather = gather
         _, self.pitch, self.buf_bytes, _, staging_bytes = A.layout(P, Mb, cols, dtype, pitch or None, separate)
         self.M = P * Mb
         self.Mj = Mb // J
@@ -51,7 +53,7 @@ class Case:
         self.ar = D.AllReduce(self.bufs, self.buf_bytes, dtype, Mb, cols, sub_blocks=J, pitch=pitch,
                               staging=self.staging, staging_bytes=staging_bytes,
                               rs_opts=_opts(copier, **kw), ag_opts=_opts(copier, **kw),
-                              reduce_ctas=reduce_ctas, reduce_threads=reduce_threads)
+                              reduce_ctas=reduce_ctas, reduce_threads=reduce_threads, gather=gather)
         steps = self.M // self.Mj
         self.counters = torch.zeros(P * steps, dtype=torch.int32, device=dev) if group > 1 else None
         self.desc = D.fill_desc(dtype, SEED, self.M, cols, self.pitch, self.buf_bytes, [0] * P, self.Mj, cols,
@@ -71,7 +73,7 @@ class Case:
             D.dtt_fill_producer(self.bufs, self.desc, h, self.prod)
             self.ar.reduce(self.err, self.prod)
         rs, ag = self.ar.wait()
-        assert rs.status == D.OK and ag.status == D.OK
+        assert rs.status == D.OK and ag.status == D.OK   # (no all-gather plan: a zeroed report)
         torch.cuda.synchronize()       # the reduce may have run on a stream of its own
         assert int(self.err.item()) == 0
 
@@ -87,7 +89,10 @@ class Case:
                 np.testing.assert_array_equal(self.staging[r].cpu().numpy(), self.o.staging[r],
                                               err_msg=f"{what} staging {r}")
         np.testing.assert_array_equal(self.ar.rs.read_gates()[:, :, :5], self.o.rs.gates, err_msg=f"{what} rs gates")
-        np.testing.assert_array_equal(self.ar.ag.read_gates()[:, :, :5], self.o.ag.gates, err_msg=f"{what} ag gates")
+        if self.gather:
+            np.testing.assert_array_equal(self.ar.ag.read_gates()[:, :, :5], self.o.ag.gates, err_msg=f"{what} ag gates")
+        else:
+            assert self.ar.ag is None
         np.testing.assert_array_equal(self.ar.rs.read_group_counters(), self.o.rs.group_counters,
                                       err_msg=f"{what} group counters")
 
@@ -123,6 +128,32 @@ def test_allreduce_matches_the_oracle(name):
             for r in range(c.P):
                 got = c.o._rows(c.bufs[r].cpu().numpy(), 0, c.M)
                 assert np.array_equal(got.view(np.uint8), want.view(np.uint8)), (name, R, r)
+            c.ar.next_round()
+    finally:
+        c.close()
+
+
+SCATTER_CASES = {
+    "p4_bf16_in_place": dict(P=4, Mb=48, cols=512, J=3, dtype="bf16"),
+    "p3_f32_staging_vector": dict(P=3, Mb=20, cols=64, J=2, dtype="f32", separate=True, copier="vector"),
+    "p5_bf16_in_order_pitched": dict(P=5, Mb=8, cols=128, J=4, dtype="bf16", pitch=320, in_order=True),
+}
+
+
+@pytest.mark.parametrize("name", sorted(SCATTER_CASES))
+def test_reduce_scatter_matches_the_oracle(name):
+    """The first shot alone (scatter_only): rank b ends with the sum over its block b and its own
+    partial elsewhere; every byte of every buffer, the plan's gates and group counters."""
+    c = Case(**SCATTER_CASES[name], gather=False)
+    try:
+        for R in range(1, 4):
+            c.round()
+            parts = c.oracle_round(R)
+            c.compare(f"{name} R{R}")
+            want = A.reduce_scatter(c.dtype, parts, c.P, c.Mb)
+            for r in range(c.P):
+                got = c.o._rows(c.bufs[r].cpu().numpy(), 0, c.M)
+                assert np.array_equal(got.view(np.uint8), want[r].view(np.uint8)), (name, R, r)
             c.ar.next_round()
     finally:
         c.close()
