@@ -1006,7 +1006,7 @@ def run_ce_fanout(args):
 def measure_allreduce(K: int, warmup: int, isolated_rounds: int = 10, e2e_steps: int = 0,
                       clocks_dev=None, rows: int = 0, in_order: bool = False, ctas_per_sm: int = 0,
                       stages: int = 0, piece_bytes: int = 0, fill_rounds: int = 0, reduce_ctas: int = 0,
-                      reduce_threads: int = 0, gather: bool = True):
+                      reduce_threads: int = 0, gather: bool = True, ag_ctas_per_sm: int = 0):
     """The two-shot all-reduce of W.ALLREDUCE.  The collective: K rounds of start + a producer that
     only marks (dtt_publish: the vectors were written before the timed region, as an all-reduce
     benchmark's inputs are) + reduce kernel + wait + next_round (both plans' copiers launched at
@@ -1031,12 +1031,15 @@ def measure_allreduce(K: int, warmup: int, isolated_rounds: int = 10, e2e_steps:
     bufs = [torch.zeros(buf_bytes, dtype=torch.uint8, device=dev) for _ in range(P)]
     prod, side = torch.cuda.Stream(), torch.cuda.Stream()
     rs_cs, ag_cs = torch.cuda.Stream(priority=-1), torch.cuda.Stream(priority=-1)
-    opts = None
-    if in_order or ctas_per_sm or stages or piece_bytes:
+    opts = ag_opts = None
+    if in_order or ctas_per_sm or stages or piece_bytes or ag_ctas_per_sm:
         opts = D.dtt_plan_opts_default(method=D.COPY_TMA, ctas_per_sm=ctas_per_sm or 3,
                                        piece_bytes=piece_bytes or 16384, stages=stages or 2,
                                        deferred_copier=1 if in_order else 0)
-    ar = D.AllReduce(bufs, buf_bytes, dtype, Mb, cols, sub_blocks=J, rs_opts=opts, ag_opts=opts,
+        ag_opts = D.dtt_plan_opts_default(method=D.COPY_TMA, ctas_per_sm=ag_ctas_per_sm or ctas_per_sm or 3,
+                                          piece_bytes=piece_bytes or 16384, stages=stages or 2,
+                                          deferred_copier=1 if in_order else 0)
+    ar = D.AllReduce(bufs, buf_bytes, dtype, Mb, cols, sub_blocks=J, rs_opts=opts, ag_opts=ag_opts,
                      reduce_ctas=reduce_ctas, reduce_threads=reduce_threads,
                      rs_copy_stream=rs_cs, ag_copy_stream=ag_cs, gather=gather)
     Mj = Mb // J
@@ -1180,7 +1183,8 @@ def run_allreduce(args):
     m = measure_allreduce(K, args.warmup, isolated_rounds=10, e2e_steps=0 if args.no_e2e else 10,
                           clocks_dev=dev, rows=args.rows, in_order=args.in_order,
                           ctas_per_sm=args.ctas_per_sm, stages=args.stages, piece_bytes=args.piece_bytes,
-                          fill_rounds=20, reduce_ctas=args.reduce_ctas, reduce_threads=args.reduce_threads)
+                          fill_rounds=20, reduce_ctas=args.reduce_ctas, reduce_threads=args.reduce_threads,
+                          ag_ctas_per_sm=args.ag_ctas_per_sm)
     peak, peak_kind = load_peaks()
     s = summarize_allreduce(m, peak, peak_kind)
     # the reduce-scatter alone (the first shot: no all-gather plan), the same way
@@ -1315,6 +1319,8 @@ def main(argv=None):
                     help="time the fan-out with copy engines (device-to-device memcpy) against the SM copier")
     ap.add_argument("--allreduce", action="store_true",
                     help="time the two-shot all-reduce (reduce-scatter plan, reduce kernel, all-gather plan)")
+    ap.add_argument("--ag-ctas-per-sm", type=int, default=0,
+                    help="--allreduce: the all-gather plan's copier CTAs per SM (default: --ctas-per-sm, else 3)")
     ap.add_argument("--reduce-ctas", type=int, default=0, help="--allreduce: reduce kernel CTAs (default: one per SM)")
     ap.add_argument("--reduce-threads", type=int, default=0, help="--allreduce: threads per reduce CTA (default 256)")
     ap.add_argument("--in-order", action="store_true",

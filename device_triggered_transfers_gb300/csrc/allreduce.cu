@@ -428,9 +428,12 @@ int dtt_allreduce_create(void* const* bufs, uint64_t buf_bytes, void* const* sta
         return fail(DTT_EINVAL, "dtt_allreduce_create: at most %u sub-blocks in all (P x sub_blocks), "
                                 "each under 2^40 vectors", kMaxUnits);
     const uint64_t M = (uint64_t)P * d.block_rows;
-    const uint64_t vec_bytes = (M - 1) * d.pitch + rb;
-    const uint64_t slots = (uint64_t)P * d.block_rows * d.pitch;   // the P slots
-    const uint64_t slot_off = staging ? 0 : M * d.pitch;
+    uint64_t vec_span = 0, slots = 0, ends = 0;
+    if (__builtin_mul_overflow(M, d.pitch, &vec_span) || __builtin_add_overflow(vec_span, vec_span, &ends))
+        return fail(DTT_EINVAL, "dtt_allreduce_create: rows x pitch overflows 64 bits");
+    const uint64_t vec_bytes = vec_span - d.pitch + rb;
+    slots = vec_span;                                            // the P slots: P x block_rows rows
+    const uint64_t slot_off = staging ? 0 : vec_span;
     if (vec_bytes > buf_bytes || (!staging && slot_off + slots > buf_bytes))
         return fail(DTT_EINVAL, "dtt_allreduce_create: a %llu-byte buffer cannot hold the vector%s (%llu bytes)",
                     (unsigned long long)buf_bytes, staging ? "" : " and the P slots after it",

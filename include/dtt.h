@@ -771,7 +771,9 @@ int dtt_allreduce_start(dtt_allreduce* ar, cudaStream_t producer_stream, dtt_han
 int dtt_allreduce_reduce(dtt_allreduce* ar, uint32_t* err, cudaStream_t stream);
 
 /* dtt_plan_wait on the reduce-scatter plan, then on the all-gather plan (reports may be NULL).
- * Returns the first error (both plans are waited on either way). */
+ * Returns the first error (both plans are waited on either way).  After a failed wait the plans
+ * are FAILED (and the reduce kernel's counters may hold a partial count): destroy the
+ * all-reduce. */
 int dtt_allreduce_wait(dtt_allreduce* ar, dtt_report* rs_report, dtt_report* ag_report);
 
 /* dtt_plan_next_round on both plans.  Errors: as dtt_plan_next_round. */
