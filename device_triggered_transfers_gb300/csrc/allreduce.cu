@@ -81,7 +81,8 @@ template <> struct Lanes<DTT_F32> {
 
 __device__ __forceinline__ void st16(char* p, const uint4& v) { *reinterpret_cast<uint4*>(p) = v; }
 
-// Threads per reduce CTA at most: a control warp and up to 15 compute warps of ~60 registers.
+// Threads per reduce CTA at most: a control warp (lane 0 publishes, lane 1 completes) and up
+// to 15 compute warps of ~60 registers.
 constexpr uint32_t kReduceMaxThreads = 512;
 
 __device__ __forceinline__ uint32_t sm_addr(const void* q) {
@@ -104,16 +105,85 @@ __device__ __forceinline__ uint4 ld_cg(const char* q) {
     return __ldcg(reinterpret_cast<const uint4*>(q));
 }
 
+// One compute warp's share of sub-block (b, j): vectors first_t, first_t + stride, ... of it, U
+// at a time, the P parts of each loaded together and added in rank order -- part b is the
+// owner's rows (own), part s != b slot s (slot0 + s * slot_bytes).  CONTIG: rows back to back,
+// so vector t of a part is its t-th 16 bytes (a separate instance: with padded rows the offset
+// needs a division).
+template <int DT, int P, bool CONTIG>
+__device__ __forceinline__ void add_sub_block(const ReduceParams& p, uint32_t b, char* own, const char* slot0,
+                                              uint64_t first_t, uint64_t stride, uint64_t per_unit) {
+    using E = Lanes<DT>;
+    auto part = [&](int s) -> const char* { return (uint32_t)s == b ? own : slot0 + (uint64_t)s * p.slot_bytes; };
+    constexpr int U = P <= 2 ? 4 : (P <= 4 ? 2 : 1); // vectors a lane takes at once
+    for (uint64_t t0 = first_t; t0 < per_unit; t0 += stride * U) {
+        uint64_t off[U];
+#pragma unroll
+        for (int k = 0; k < U; ++k) {
+            const uint64_t t = t0 + (uint64_t)k * stride;
+            off[k] = CONTIG ? t : (t / p.vrow) * (p.pitch / 16) + t % p.vrow;   // in 16-byte vectors
+        }
+        if constexpr (P <= 8) {
+            // every part of the U vectors in flight at once, then each vector added and stored
+            // in turn (one accumulator live)
+            const char* src[P];
+#pragma unroll
+            for (int s = 0; s < P; ++s) src[s] = part(s);
+            uint4 v[U][P];
+#pragma unroll
+            for (int k = 0; k < U; ++k)
+                if (t0 + (uint64_t)k * stride < per_unit) {
+#pragma unroll
+                    for (int s = 0; s < P; ++s) v[k][s] = ld_cg(src[s] + off[k] * 16);
+                }
+#pragma unroll
+            for (int k = 0; k < U; ++k) {
+                if (t0 + (uint64_t)k * stride >= per_unit) continue;
+                float acc[E::n];
+#pragma unroll
+                for (int s = 0; s < P; ++s) {
+                    float f[E::n];
+                    E::unpack(v[k][s], f);
+#pragma unroll
+                    for (int e = 0; e < E::n; ++e) acc[e] = s == 0 ? f[e] : acc[e] + f[e];
+                }
+                st16(own + off[k] * 16, E::pack(acc));
+            }
+        } else {
+            // P > 8 (one vector at a time): the parts in batches of 8 into one accumulator
+            static_assert(U == 1, "one vector a lane above 4 parts");
+            float acc[E::n];
+#pragma unroll
+            for (int s0 = 0; s0 < P; s0 += 8) {
+                uint4 v[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    if (s0 + i < P) v[i] = ld_cg(part(s0 + i) + off[0] * 16);   // addresses made here:
+                                                                                 // 16 pointers would not
+                                                                                 // fit the registers
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    if (s0 + i >= P) continue;
+                    float f[E::n];
+                    E::unpack(v[i], f);
+#pragma unroll
+                    for (int e = 0; e < E::n; ++e) acc[e] = s0 + i == 0 ? f[e] : acc[e] + f[e];
+                }
+            }
+            st16(own + off[0] * 16, E::pack(acc));
+        }
+    }
+}
+
 // Shared memory of a CTA: the sub-blocks published to the compute warps, the abort flag, and
 // per sub-block the CTA's compute warps done with it.
 enum { kReady = 0, kAbort = 1, kDone = 2 };
 
-template <int DT, int P>
-__global__ void __launch_bounds__(kReduceMaxThreads) reduce_kernel(const __grid_constant__ ReduceParams p) {
+// At most 64 registers a thread, so that four 256-thread CTAs fit an SM (the kernel is bound by
+// the loads each SM keeps in flight; the compiler alone takes ~85 registers and halves that).
+template <int DT, int P, bool CONTIG>
+__global__ void __maxnreg__(64) reduce_kernel(const __grid_constant__ ReduceParams p) {
     extern __shared__ __align__(16) uint32_t ctl[];   // [kDone + P * J]
-    using E = Lanes<DT>;
-    constexpr int B = P < 8 ? P : 8;                 // parts loaded together
-    constexpr int U = P <= 2 ? 4 : (P <= 4 ? 2 : 1); // vectors a lane takes at once
     const uint32_t units = (uint32_t)P * p.J;
     for (uint32_t i = threadIdx.x; i < kDone + units; i += blockDim.x) ctl[i] = 0;
     __syncthreads();
@@ -121,63 +191,92 @@ __global__ void __launch_bounds__(kReduceMaxThreads) reduce_kernel(const __grid_
     const uint32_t NCW = (blockDim.x >> 5) - 1;       // compute warps
 
     if (warp == 0) {
-        if (lane != 0) return;
-        // The control thread.  Publishing unit u (ready = u + 1, release at CTA scope) follows
-        // its acquire of u's group at GPU scope, so the compute warps' loads of u follow every
-        // copy of u.  Completing u follows its acquire of the compute warps' count (CTA scope),
-        // so its acq_rel add on the global counter releases all of the CTA's stores of u; the
-        // CTA whose add completes the count has every CTA's stores, resets the counter for the
-        // next launch (stream-ordered after this one) and marks the all-gather chunk.
-        uint32_t nw = 0, nd = 0;                      // next to publish, next to complete
-        uint64_t idle = 0;
-        uint32_t ns = 0;
-        while (nd < units) {
-            bool progress = false;
+        if (lane == 0) {
+            // The publisher.  It reads the counters of up to 8 groups ahead (relaxed, all in
+            // flight together) and publishes the ready prefix behind one fence: a relaxed read
+            // followed by fence.acq_rel is an acquire, and the release at CTA scope that
+            // publishes (ready = n) hands it on to the compute warps, so their loads of a
+            // published sub-block follow every copy of it.
+            uint32_t nw = 0;
+            uint64_t idle = 0;
+            uint32_t ns = 0;
+            bool bad = false;
+            while (nw < units) {
+                const uint32_t n = units - nw < 8 ? units - nw : 8;
+                uint64_t have[8], want[8];
+#pragma unroll
+                for (uint32_t i = 0; i < 8; ++i) {
+                    if (i >= n) break;
+                    const uint32_t g = nw + i;
+                    const uint64_t* w = dtt_dev::group_word(p.rs[g / p.J], g, &want[i]);
+                    if (!w) { bad = true; break; }
+                    have[i] = dtt_dev::ld_relaxed(w);
+                }
+                if (bad) break;                        // a plan without the group (misuse bit set)
+                uint32_t r = 0;
+                while (r < n && have[r] >= want[r]) ++r;
+                if (r) {
+                    dtt_dev::fence_acq_rel();
+                    nw += r;
+                    st_release_cta(ctl + kReady, nw);
+                    idle = 0;
+                    ns = 0;
+                    continue;
+                }
+                if (++idle > p.max_polls) break;      // nothing arrived for max_polls polls
+                __nanosleep(ns);
+                ns = ns < 256 ? ns + 32 : 256;
+            }
             if (nw < units) {
-                uint64_t target = 0;
-                const uint64_t* w = dtt_dev::group_word(p.rs[nw / p.J], nw, &target);
-                if (!w) break;                        // a plan without the group (misuse bit set)
-                if (dtt_dev::ld_acquire(w) >= target) {
-                    st_release_cta(ctl + kReady, ++nw);
-                    progress = true;
+                // gave up: the sub-blocks from nw on are never added, so they stay unmarked and
+                // the all-gather plan's wait reports them short
+                atomicAdd(p.err, 1u);
+                st_release_cta(ctl + kAbort, 1);
+            }
+        } else if (lane == 1) {
+            // The completer.  Its acquire of the CTA's count of a sub-block (CTA scope) lets its
+            // acq_rel add on the global counter release all of the CTA's stores of it; the CTA
+            // whose add completes the count has every CTA's stores, resets the counter for the
+            // next launch (stream-ordered after this one) and marks the all-gather chunk.
+            uint32_t nd = 0, ns = 0;
+            for (uint64_t i = 0; nd < units; ++i) {
+                if (ld_acquire_cta(ctl + kDone + nd) == NCW) {
+                    uint32_t old;
+                    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(p.counters + nd) : "memory");
+                    if (old + 1 == gridDim.x) {
+                        asm volatile("st.relaxed.gpu.global.u32 [%0], 0;" ::"l"(p.counters + nd) : "memory");
+                        const uint32_t b = nd / p.J, j = nd - b * p.J;
+                        if (p.gather) dtt_dev::mark_one(p.ag[b], p.ag[b].first_chunk + j);
+                    }
+                    ++nd;
+                    i = 0;
+                    ns = 0;
+                    continue;
                 }
+                // the compute warps stop only after an abort; the bound is a backstop.  The
+                // back-off grows to ~1 us: a sub-block takes a few microseconds to add, and a
+                // faster spin only takes issue slots from the compute warps of its SM
+                // sub-partition (every CTA's control warp may share one)
+                if (ld_acquire_cta(ctl + kAbort) || i > 4 * p.max_polls + (1u << 20)) break;
+                __nanosleep(ns);
+                ns = ns < 1024 ? ns + 64 : 1024;
             }
-            if (nd < nw && ld_acquire_cta(ctl + kDone + nd) == NCW) {
-                uint32_t old;
-                asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(p.counters + nd) : "memory");
-                if (old + 1 == gridDim.x) {
-                    asm volatile("st.relaxed.gpu.global.u32 [%0], 0;" ::"l"(p.counters + nd) : "memory");
-                    const uint32_t b = nd / p.J, j = nd - b * p.J;
-                    if (p.gather) dtt_dev::mark_one(p.ag[b], p.ag[b].first_chunk + j);
-                }
-                ++nd;
-                progress = true;
-            }
-            if (progress) {
-                idle = 0;
-                ns = 0;
-                continue;
-            }
-            if (++idle > p.max_polls) break;          // nothing moved for max_polls polls
-            __nanosleep(ns);
-            ns = ns < 256 ? ns + 32 : 256;
-        }
-        if (nd < units) {
-            // gave up: the sub-blocks from nd on stay unmarked, so the all-gather plan's wait
-            // reports them short; the compute warps stop at the next one not yet published
-            atomicAdd(p.err, 1u);
-            st_release_cta(ctl + kAbort, 1);
         }
         return;
     }
 
-    // compute warps: each sub-block as one grid of NCW * gridDim.x warps.  A warp counts itself
-    // done with a sub-block (a release at CTA scope) only after it has issued its first loads of
-    // the next one, so that the release's wait for the warp's stores overlaps those loads
+    // compute warps: each sub-block as one grid of NCW * gridDim.x warps; a warp counts itself
+    // done with a sub-block (a release at CTA scope) when it reaches the next one
     const uint64_t per_unit = p.Mj * p.vrow;          // vectors in one sub-block
     const uint64_t stride = (uint64_t)gridDim.x * NCW * 32;
     const uint64_t first_t = ((uint64_t)blockIdx.x * NCW + (warp - 1)) * 32 + lane;
     uint32_t pending = ~0u;                           // the sub-block whose count is still owed
+    // the sub-blocks are walked in order, the pointers stepped one sub-block at a time (no
+    // division or multiply per sub-block: a warp does its setup between two rounds of loads)
+    uint32_t b = 0, j = 0;
+    const uint64_t step = p.Mj * p.pitch;
+    char* own = p.bufs[0];
+    const char* slot0 = p.stage[0] + p.slot_off;
     for (uint32_t u = 0; u < units; ++u) {
         int go = 1;
         if (lane == 0) {
@@ -192,54 +291,20 @@ __global__ void __launch_bounds__(kReduceMaxThreads) reduce_kernel(const __grid_
         go = __shfl_sync(0xFFFFFFFFu, go, 0);
         if (!go) return;     // (an owed count is left unpaid: nothing after it gets marked)
         __syncwarp();        // the lanes' loads below follow lane 0's acquire
-        const uint32_t b = u / p.J, j = u - b * p.J;
-        char* own = p.bufs[b] + (b * p.Mb + j * p.Mj) * p.pitch;
-        const char* slot0 = p.stage[b] + p.slot_off + j * p.Mj * p.pitch;
-        for (uint64_t t0 = first_t; t0 < per_unit; t0 += stride * U) {
-            uint64_t off[U];
-            bool in[U];
-#pragma unroll
-            for (int k = 0; k < U; ++k) {
-                const uint64_t t = t0 + (uint64_t)k * stride;
-                in[k] = t < per_unit;
-                off[k] = p.contig ? t * 16 : (t / p.vrow) * p.pitch + (t % p.vrow) * 16;
-            }
-            float acc[U][E::n];
-#pragma unroll
-            for (int s0 = 0; s0 < P; s0 += B) {
-                uint4 v[U][B] = {};   // lanes past the sub-block's end stay zero (never stored)
-#pragma unroll
-                for (int k = 0; k < U; ++k)
-#pragma unroll
-                    for (int i = 0; i < B; ++i) {
-                        const uint32_t s = (uint32_t)(s0 + i);
-                        if (in[k] && s < (uint32_t)P)
-                            v[k][i] = ld_cg((s == b ? own : slot0 + s * p.slot_bytes) + off[k]);
-                    }
-                if (pending != ~0u) {          // the stores it covers were ordered by __syncwarp
-                    if (lane == 0) red_release_cta(ctl + kDone + pending, 1);
-                    pending = ~0u;
-                }
-#pragma unroll
-                for (int k = 0; k < U; ++k)
-#pragma unroll
-                    for (int i = 0; i < B; ++i) {
-                        if (s0 + i >= P) continue;
-                        float f[E::n];
-                        E::unpack(v[k][i], f);
-#pragma unroll
-                        for (int e = 0; e < E::n; ++e) acc[k][e] = (s0 + i == 0) ? f[e] : acc[k][e] + f[e];
-                    }
-            }
-#pragma unroll
-            for (int k = 0; k < U; ++k)
-                if (in[k]) st16(own + off[k], E::pack(acc[k]));
-        }
-        if (pending != ~0u) {                         // no vector of this sub-block here
-            if (lane == 0) red_release_cta(ctl + kDone + pending, 1);
-        }
-        __syncwarp();        // the warp's stores before lane 0's release
+        if (pending != ~0u && lane == 0) red_release_cta(ctl + kDone + pending, 1);
+        add_sub_block<DT, P, CONTIG>(p, b, own, slot0, first_t, stride, per_unit);
+        __syncwarp();        // the warp's stores before lane 0's release (at the next sub-block)
         pending = u;
+        if (++j == p.J) {
+            j = 0;
+            if (++b < (uint32_t)P) {
+                own = p.bufs[b] + (uint64_t)b * p.Mb * p.pitch;
+                slot0 = p.stage[b] + p.slot_off;
+            }
+        } else {
+            own += step;
+            slot0 += step;
+        }
     }
     if (lane == 0) red_release_cta(ctl + kDone + pending, 1);
 }
@@ -249,32 +314,35 @@ using ReduceFn = void (*)(ReduceParams);
 // Sub-blocks of one all-reduce in all: the reduce kernel keeps a shared-memory counter for each.
 constexpr uint32_t kMaxUnits = 4096;
 
-// The instance for a dtype and P = 2 .. DTT_MAX_RANKS.
-template <int DT>
+// The instance for a dtype, P = 2 .. DTT_MAX_RANKS and rows back to back or padded (a kernel of
+// its own each: the padded form's offsets need a division, and one kernel holding both would
+// take the registers of the heavier).
+template <int DT, bool C>
 ReduceFn reduce_for(uint32_t P) {
     static_assert(DTT_MAX_RANKS == 16, "one instance per rank count");
     switch (P) {
-        case 2: return reduce_kernel<DT, 2>;
-        case 3: return reduce_kernel<DT, 3>;
-        case 4: return reduce_kernel<DT, 4>;
-        case 5: return reduce_kernel<DT, 5>;
-        case 6: return reduce_kernel<DT, 6>;
-        case 7: return reduce_kernel<DT, 7>;
-        case 8: return reduce_kernel<DT, 8>;
-        case 9: return reduce_kernel<DT, 9>;
-        case 10: return reduce_kernel<DT, 10>;
-        case 11: return reduce_kernel<DT, 11>;
-        case 12: return reduce_kernel<DT, 12>;
-        case 13: return reduce_kernel<DT, 13>;
-        case 14: return reduce_kernel<DT, 14>;
-        case 15: return reduce_kernel<DT, 15>;
-        case 16: return reduce_kernel<DT, 16>;
+        case 2: return reduce_kernel<DT, 2, C>;
+        case 3: return reduce_kernel<DT, 3, C>;
+        case 4: return reduce_kernel<DT, 4, C>;
+        case 5: return reduce_kernel<DT, 5, C>;
+        case 6: return reduce_kernel<DT, 6, C>;
+        case 7: return reduce_kernel<DT, 7, C>;
+        case 8: return reduce_kernel<DT, 8, C>;
+        case 9: return reduce_kernel<DT, 9, C>;
+        case 10: return reduce_kernel<DT, 10, C>;
+        case 11: return reduce_kernel<DT, 11, C>;
+        case 12: return reduce_kernel<DT, 12, C>;
+        case 13: return reduce_kernel<DT, 13, C>;
+        case 14: return reduce_kernel<DT, 14, C>;
+        case 15: return reduce_kernel<DT, 15, C>;
+        case 16: return reduce_kernel<DT, 16, C>;
         default: return nullptr;
     }
 }
 
-ReduceFn reduce_entry(uint32_t dtype, uint32_t P) {
-    return dtype == DTT_BF16 ? reduce_for<DTT_BF16>(P) : reduce_for<DTT_F32>(P);
+ReduceFn reduce_entry(uint32_t dtype, uint32_t P, bool contig) {
+    if (dtype == DTT_BF16) return contig ? reduce_for<DTT_BF16, true>(P) : reduce_for<DTT_BF16, false>(P);
+    return contig ? reduce_for<DTT_F32, true>(P) : reduce_for<DTT_F32, false>(P);
 }
 
 }  // namespace
@@ -285,9 +353,12 @@ cudaError_t preload_allreduce_kernels() {
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     for (uint32_t P = 2; P <= DTT_MAX_RANKS && e == cudaSuccess; ++P)
         for (uint32_t dt : {(uint32_t)DTT_BF16, (uint32_t)DTT_F32}) {
-            e = prepare_kernel(reduce_entry(dt, P));
-            if (e == cudaSuccess)
-                e = cudaFuncSetAttribute(reduce_entry(dt, P), cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+            for (bool c : {true, false}) {
+                e = prepare_kernel(reduce_entry(dt, P, c));
+                if (e == cudaSuccess)
+                    e = cudaFuncSetAttribute(reduce_entry(dt, P, c), cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+                if (e != cudaSuccess) break;
+            }
             if (e != cudaSuccess) break;
         }
     return e;
@@ -371,7 +442,7 @@ int check_room(const dtt_allreduce* ar, bool quiet = false) {
         cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&blocks, cudaDevAttrMaxBlocksPerMultiprocessor, dev) != cudaSuccess ||
-        cudaFuncGetAttributes(&fa, reduce_entry(ar->d.dtype, ar->P)) != cudaSuccess || sms <= 0)
+        cudaFuncGetAttributes(&fa, reduce_entry(ar->d.dtype, ar->P, ar->pitch == ar->rb)) != cudaSuccess || sms <= 0)
         return fail(DTT_ECUDA, "dtt_allreduce_create: cannot query the device or the reduce kernel");
     const uint64_t per_sm = (ar->d.reduce_ctas + (uint64_t)sms - 1) / (uint64_t)sms;
     const uint64_t r_thr = per_sm * ar->d.reduce_threads;
@@ -613,7 +684,7 @@ int dtt_allreduce_reduce(dtt_allreduce* ar, uint32_t* err, cudaStream_t stream) 
     cfg.dynamicSmemBytes = ar->smem;
     cfg.stream = stream;
     void* args[] = {&p};
-    const cudaError_t e = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(reduce_entry(ar->d.dtype, ar->P)), args);
+    const cudaError_t e = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(reduce_entry(ar->d.dtype, ar->P, ar->pitch == ar->rb)), args);
     if (e != cudaSuccess) return fail(DTT_ECUDA, "dtt_allreduce_reduce: launch failed: %s", cudaGetErrorString(e));
     DTT_CUDA_TRY(cudaEventRecord(ar->ev_reduce, stream));
     if (ar->serial && ar->ag) {
