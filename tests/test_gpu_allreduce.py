@@ -9,6 +9,7 @@ import torch
 
 from oracle import allreduce as A
 from oracle import cfill
+from oracle import plan as OP
 
 pytestmark = pytest.mark.gpu
 
@@ -223,3 +224,61 @@ def test_allreduce_missing_mark_fails_the_round_and_counts_the_reduce_wait():
         assert ag_first[2] + 1 in list(ag.short_chunks[:ag.n_short])
     finally:
         c.close()
+
+
+def test_allreduce_200_rounds_counters_and_gates_stay_exact():
+    """Many rounds in a row: the reduce kernel's per-sub-block counters return to zero after
+    every launch and both plans' gates keep counting, so round 200 matches the oracle exactly."""
+    c = Case(P=3, Mb=16, cols=256, J=4, dtype="bf16")
+    try:
+        for R in range(1, 201):
+            c.round()
+            parts = c.oracle_round(R)
+            if R in (1, 2, 57, 128, 200):
+                c.compare(f"stress R{R}")
+                want = A.allreduce("bf16", parts)
+                for r in range(c.P):
+                    got = c.o._rows(c.bufs[r].cpu().numpy(), 0, c.M)
+                    assert np.array_equal(got.view(np.uint8), want.view(np.uint8)), (R, r)
+            c.ar.next_round()
+    finally:
+        c.close()
+
+
+def test_allreduce_round_limit():
+    """Both plans start two rounds below the limit (initial_round = 2^32 - 2): two rounds run, and
+    the next next_round is refused (EROUNDLIMIT), as the oracle's plans refuse it."""
+    P, Mb, cols, J = 2, 8, 128, 2
+    first = (1 << 32) - 2
+    o = A.TwoShot(P, Mb, cols, "bf16", J, initial_round=first)
+    dev = torch.device("cuda")
+    bufs = [torch.zeros(o.buf_bytes, dtype=torch.uint8, device=dev) for _ in range(P)]
+    opts = D.dtt_plan_opts_default(method=1, ctas_per_sm=3, piece_bytes=16384, stages=2, initial_round=first)
+    ar = D.AllReduce(bufs, o.buf_bytes, "bf16", Mb, cols, sub_blocks=J, rs_opts=opts, ag_opts=opts)
+    desc = D.fill_desc("bf16", SEED, P * Mb, cols, cols * 2, o.buf_bytes, [0] * P, Mb // J, cols, 1, 1)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    prod = torch.cuda.Stream()
+    try:
+        for R in (first, first + 1):
+            h = ar.start(prod)
+            D.dtt_fill_producer(bufs, desc, h, prod)
+            ar.reduce(err, prod)
+            rs, ag = ar.wait()
+            assert rs.status == D.OK and ag.status == D.OK and rs.round == R
+            parts = A.hashed_partials("bf16", SEED, P, P * Mb, cols, R)
+            if R == first:
+                assert o.round(parts) == R
+            else:
+                # the oracle's round ends with next_round, refused at the limit once the
+                # round's data is final
+                with pytest.raises(OP.RoundLimitError):
+                    o.round(parts)
+            for q in range(P):
+                np.testing.assert_array_equal(bufs[q].cpu().numpy(), o.bufs[q], err_msg=f"R{R} buf {q}")
+            if R == first:
+                ar.next_round()
+        with pytest.raises(D.DttError) as e:
+            ar.next_round()
+        assert e.value.code == D.EROUNDLIMIT
+    finally:
+        ar.close()
