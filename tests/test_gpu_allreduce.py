@@ -282,3 +282,33 @@ def test_allreduce_round_limit():
         assert e.value.code == D.EROUNDLIMIT
     finally:
         ar.close()
+
+
+def test_allreduce_plans_sharing_one_copy_stream():
+    """Both plans' copiers on one copy stream (plans may share a queue): the all-gather copier
+    runs only after the reduce-scatter copier, which needs nothing from it, so the round still
+    completes -- with less overlap -- and matches the oracle."""
+    P, Mb, cols, J = 4, 32, 512, 4
+    o = A.TwoShot(P, Mb, cols, "bf16", J)
+    dev = torch.device("cuda")
+    bufs = [torch.zeros(o.buf_bytes, dtype=torch.uint8, device=dev) for _ in range(P)]
+    shared = torch.cuda.Stream(priority=-1)
+    ar = D.AllReduce(bufs, o.buf_bytes, "bf16", Mb, cols, sub_blocks=J, rs_copy_stream=shared, ag_copy_stream=shared)
+    desc = D.fill_desc("bf16", SEED, P * Mb, cols, cols * 2, o.buf_bytes, [0] * P, Mb // J, cols, 1, 1)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    prod = torch.cuda.Stream()
+    try:
+        for R in (1, 2, 3):
+            h = ar.start(prod)
+            D.dtt_fill_producer(bufs, desc, h, prod)
+            ar.reduce(err, prod)
+            rs, ag = ar.wait()
+            assert rs.status == D.OK and ag.status == D.OK
+            o.round(A.hashed_partials("bf16", SEED, P, P * Mb, cols, R))
+            for q in range(P):
+                np.testing.assert_array_equal(bufs[q].cpu().numpy(), o.bufs[q], err_msg=f"R{R} buf {q}")
+            ar.next_round()
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+    finally:
+        ar.close()
