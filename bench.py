@@ -40,6 +40,9 @@ NCU_TRAFFIC = {("c2_chunks_p4", "copier_bulk_kernel"): 474700544,
                ("c3_tiles_p8", "copier_bulk_kernel"): 8009544192,
                ("c5_gemm_p4", "gemm2_producer_kernel"): 184814208,
                ("c5_gemm_p4", "copier_kernel"): 206209536,
+               ("c4a_writers8_p8", "copier_bulk_kernel"): 205637888,
+               # captured with 256 rows (--rows 256) and scaled by the rows, 10x
+               ("c4b_bcast_p8", "copier_bulk_kernel"): 20848015360,
                # the two-shot all-reduce's reduce kernel (bench.py --allreduce --in-order), 256 threads
                ("allreduce_p4", "reduce_kernel"): 651664896}
 # DRAM bytes (read, write) of one whole round, producer, copier and check together, from an
@@ -744,7 +747,8 @@ def run_ours(args):
             sc = summarize(mc, steps, mc["elapsed_s"], Dc * steps, peak, peak_kind)
             per_config[name] = {
                 "steps": steps, "ms_per_round": sc["ms_per_round"], "gbs_delivered": sc["gbs_delivered"],
-                "dominant_kernel": {k: sc["roofline"][k] for k in ("kernel", "bound", "achieved", "unit", "frac")},
+                "dominant_kernel": {k: sc["roofline"][k] for k in ("kernel", "bound", "achieved", "unit", "frac",
+                                                                   "traffic")},
                 "copier_frac_in_round": (sc["copier_roofline"] or sc["roofline"])["frac"],
                 "hbm_frac_end_to_end": sc["hbm_frac_end_to_end"]["of_measured"],
                 "copier_window_hbm_frac": (sc["copier_window"] or {}).get("hbm_frac"),
@@ -764,7 +768,7 @@ def run_ours(args):
             "busbw_gbs": sa["busbw_gbs"], "hbm_frac_end_to_end": sa["hbm_frac_end_to_end"]["of_measured"],
             "with_fill_producer_ms_per_round": ma.get("fill_round_ms"),
             "dominant_kernel": {k: (sa.get("reduce_roofline") or {}).get(k)
-                                for k in ("kernel", "bound", "achieved", "unit", "frac")},
+                                for k in ("kernel", "bound", "achieved", "unit", "frac", "traffic")},
             "workload": "P=4 bf16 [16384, 4096] per rank, 8 sub-blocks of 512 rows per block (bench.py --allreduce)"}
 
     if rank != 0:
