@@ -25,7 +25,9 @@
  *    that rank's counters of the chunk's groups after a release fence; dtt_wait_group acquires
  *    the counter, so data of every member read after it is this round's.
  *  - A producer that writes through the async proxy (TMA stores) must complete those writes
- *    (cp.async.bulk.wait_group 0) and issue fence.proxy.async before calling mark_ready.
+ *    (cp.async.bulk.wait_group 0) and issue fence.proxy.async before calling mark_ready; a
+ *    consumer that reads landed bytes through the async proxy (TMA loads) issues
+ *    fence.proxy.async.global after its wait, as the library's consumer GEMM does.
  */
 #ifndef DTT_DEVICE_CUH
 #define DTT_DEVICE_CUH
