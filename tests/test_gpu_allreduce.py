@@ -312,3 +312,50 @@ def test_allreduce_plans_sharing_one_copy_stream():
         assert int(err.item()) == 0
     finally:
         ar.close()
+
+
+def test_allreduce_many_one_row_sub_blocks():
+    """256 sub-blocks of one row each (P = 4, 64 rows per block): the reduce's publisher reads the
+    groups eight ahead, so many batches; every byte against the oracle."""
+    c = Case(P=4, Mb=64, cols=512, J=64, dtype="bf16")
+    try:
+        for R in (1, 2):
+            c.round()
+            c.oracle_round(R)
+            c.compare(f"256 sub-blocks R{R}")
+            c.ar.next_round()
+    finally:
+        c.close()
+
+
+def test_allreduce_producer_marks_last_to_first():
+    """Each rank's partial written first, its reduce-scatter chunks then marked one by one from
+    the last to the first (one publish launch per chunk): the copier's queues keep schedule order
+    and the reduce takes the sub-blocks in order, so it waits for the last marks -- slower, still
+    the oracle's result."""
+    P, Mb, cols, J = 3, 16, 256, 4
+    c = Case(P=P, Mb=Mb, cols=cols, J=J, dtype="bf16")
+    try:
+        for R in (1, 2):
+            h = c.ar.start(c.prod)
+            # the partials copied in (the fill would mark as it writes), then the marks
+            parts = A.hashed_partials("bf16", SEED, P, P * Mb, cols, R)
+            with torch.cuda.stream(c.prod):
+                for r in range(P):
+                    c.bufs[r][:P * Mb * cols * 2].copy_(torch.from_numpy(parts[r].view(np.uint8).reshape(-1)),
+                                                        non_blocking=False)
+            n_rank = P * J
+            for r in range(P):
+                first = c.ar.rs.info()[1][r]
+                for k in reversed(range(n_rank)):
+                    D.dtt_publish(h, first + k, 1, 0, c.prod)
+            c.ar.reduce(c.err, c.prod)
+            rs, ag = c.ar.wait()
+            assert rs.status == D.OK and ag.status == D.OK
+            c.oracle_round(R)
+            c.compare(f"reversed marks R{R}")
+            c.ar.next_round()
+        torch.cuda.synchronize()
+        assert int(c.err.item()) == 0
+    finally:
+        c.close()

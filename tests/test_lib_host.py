@@ -416,6 +416,7 @@ def _allreduce_create(P=2, bufs=None, buf_bytes=1 << 20, staging=None, staging_b
     ("staging too small", dict(staging=[0x100000, 0x200000], staging_bytes=1000), "staging buffers need"),
     ("unaligned buffer", dict(bufs=[0x10000, 0x20008]), "16-byte aligned"),
     ("rows x pitch past 64 bits", dict(pitch=1 << 60), "overflows"),
+    ("more than 4096 sub-blocks", dict(P=16, block_rows=257, sub_blocks=257, buf_bytes=1 << 30), "4096 sub-blocks"),
     ("copy-engine reduce-scatter", dict(rs=D.dtt_plan_opts_default(method=2)), "copy-engine"),
     ("overlapped all-gather", dict(ag=D.dtt_plan_opts_default(overlap=1)), "overlap"),
     ("copier beside, deferred", dict(rs=D.dtt_plan_opts_default(deferred_copier=2)), "deferred_copier"),
