@@ -244,3 +244,102 @@ def test_reduce_scatter_leaves_the_other_blocks_alone(dtype, P, J, separate):
                 if b != r:
                     assert np.array_equal(_bits(dtype, got[b * Mb:(b + 1) * Mb]),
                                           _bits(dtype, parts[r][b * Mb:(b + 1) * Mb]))
+
+
+def _threaded_two_shot_round(o, parts, rng, max_polls=200000):
+    """One round of the two plans with threads in every role: a producer per rank (its partial
+    written and marked chunk by chunk, in a random order), a copier per (source, peer) queue of
+    each plan, and a reducer per sub-block that waits on its group, adds and marks.  Gate and
+    counter updates under one lock (the atomics); random short sleeps vary the interleaving."""
+    import threading
+    import time
+    lock = threading.Lock()
+    timeouts = []
+    R = o.rs.start()
+    assert o.ag.start() == R
+    P, J, Mj = o.P, o.J, o.Mj
+
+    def nap():
+        time.sleep(float(rng.uniform(0, 2e-4)))
+
+    def producer(s, order):
+        for c in order:
+            k = c - o.rs.first[s]
+            b, j = divmod(k, J)
+            row0 = b * o.Mb + j * Mj
+            nap()
+            o._put_rows(o.bufs[s], row0 * o.pitch, np.asarray(parts[s])[row0:row0 + Mj])
+            with lock:
+                o.rs.mark_ready(s, c)
+
+    def copier(plan, s, p):
+        for c in plan.chunks_of(s):
+            if p not in plan.chunks[c].receivers(plan.P, s):
+                continue
+            for _ in range(max_polls):
+                with lock:
+                    if plan.gate_open(c):
+                        break
+                time.sleep(1e-5)
+            else:
+                timeouts.append((id(plan), s, p, c))
+                return
+            nap()
+            ch = plan.chunks[c]
+            for i, reg in enumerate(ch.regions):
+                OP.copy_region(plan.bufs[s], plan.dst[p], reg, ch.dest_region(i))
+            with lock:
+                plan.signal_arrival(s, p, c)
+
+    def reducer(b, j):
+        for _ in range(max_polls):
+            with lock:
+                if o.rs.group_ready(b, b * J + j):
+                    break
+            time.sleep(1e-5)
+        else:
+            timeouts.append(("reduce", b, j))
+            return
+        nap()
+        with lock:
+            o.reduce_chunk(b, j)
+
+    threads = []
+    for s in range(P):
+        order = list(o.rs.chunks_of(s))
+        rng.shuffle(order)
+        threads.append(threading.Thread(target=producer, args=(s, order)))
+        for p in range(P):
+            if p != s:
+                threads.append(threading.Thread(target=copier, args=(o.rs, s, p)))
+                threads.append(threading.Thread(target=copier, args=(o.ag, s, p)))
+    for b in range(P):
+        for j in range(J):
+            threads.append(threading.Thread(target=reducer, args=(b, j)))
+    rng.shuffle(threads)
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not timeouts, timeouts
+    for pl in (o.rs, o.ag):
+        assert pl.wait()[0] == OP.OK
+        pl.next_round()
+    return R
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_two_shot_with_threads_in_every_role(seed):
+    """Producers marking in random orders, every copier queue and every reducer on threads: the
+    group waits alone keep the reduce after every part has landed and the all-gather off the
+    rows the reduce-scatter still reads, so every rank ends with the definition's sum."""
+    rng = np.random.default_rng(seed)
+    P, Mb, cols, J = (2, 3, 4, 4, 3, 2)[seed], 4, 16, (1, 2, 2, 4, 1, 2)[seed]
+    dtype = "bf16" if seed % 2 == 0 else "f32"
+    o = A.TwoShot(P, Mb, cols, dtype, J, separate=seed % 3 == 0)
+    for R in (1, 2):
+        parts = A.hashed_partials(dtype, 60 + seed, P, P * Mb, cols, R)
+        assert _threaded_two_shot_round(o, parts, rng) == R
+        want = A.allreduce(dtype, parts)
+        for r in range(P):
+            assert np.array_equal(_bits(dtype, o.result(r)), _bits(dtype, want)), (seed, R, r)
