@@ -173,26 +173,39 @@ def test_allreduce_reduce_launched_first_on_its_own_stream():
         c.close()
 
 
-def test_allreduce_full_size_every_element():
-    """P = 4 ranks of bf16 [16384, 4096] (128 MiB each, the 4-rank chunked all-gather's size),
-    blocks of 4096 rows in 8 sub-blocks of 512 rows (4 MiB), the producer a 38-CTA group per
-    rank: every element of every rank's result against the definition, two rounds."""
-    P, Mb, cols, J = 4, 4096, 4096, 8
-    c = Case(P=P, Mb=Mb, cols=cols, J=J, dtype="bf16", group=38, oracle=False)
+FULL = {
+    # the 4-rank chunked all-gather's size: 128 MiB per rank, blocks of 4096 rows in 4 MiB sub-blocks
+    "p4_bf16": dict(P=4, Mb=4096, cols=4096, J=8, dtype="bf16", group=38),
+    "p4_f32": dict(P=4, Mb=4096, cols=2048, J=8, dtype="f32", group=38),
+    # eight ranks of 128 MiB (2 GiB of buffers with the slots)
+    "p8_bf16": dict(P=8, Mb=2048, cols=4096, J=4, dtype="bf16", group=19),
+}
+
+
+@pytest.mark.parametrize("name", sorted(FULL))
+def test_allreduce_full_size_every_element(name):
+    """Full-size vectors (128 MiB per rank), the producer a group of CTAs per rank: every element
+    of every rank's result against the definition, two rounds; the expected sums built block by
+    block from the oracle's C restatement of the producer's values."""
+    f = FULL[name]
+    P, Mb, cols, dtype = f["P"], f["Mb"], f["cols"], f["dtype"]
+    c = Case(P=P, Mb=Mb, cols=cols, J=f["J"], dtype=dtype, group=f["group"], oracle=False)
+    eb = 2 if dtype == "bf16" else 4
+    view = np.uint16 if dtype == "bf16" else np.float32
     try:
         for R in range(1, 3):
             c.round()
-            rb = cols * 2
+            rb = cols * eb
             for b in range(P):
                 parts = []
                 for s in range(P):
                     raw = np.empty(Mb * rb, dtype=np.uint8)
-                    cfill.fill_rows_into(raw, "bf16", SEED, s, R, cols, b * Mb, (b + 1) * Mb)
-                    parts.append(raw.view(np.uint16).reshape(Mb, cols))
-                want = A.allreduce("bf16", parts).view(np.uint8).reshape(-1)
+                    cfill.fill_rows_into(raw, dtype, SEED, s, R, cols, b * Mb, (b + 1) * Mb)
+                    parts.append(raw.view(view).reshape(Mb, cols))
+                want = A.allreduce(dtype, parts).view(np.uint8).reshape(-1)
                 for r in range(P):
                     got = c.bufs[r][b * Mb * rb:(b + 1) * Mb * rb].cpu().numpy()
-                    np.testing.assert_array_equal(got, want, err_msg=f"R{R} block {b} at rank {r}")
+                    np.testing.assert_array_equal(got, want, err_msg=f"{name} R{R} block {b} at rank {r}")
             c.ar.next_round()
     finally:
         c.close()
