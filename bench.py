@@ -1010,7 +1010,8 @@ def run_ce_fanout(args):
 def measure_allreduce(K: int, warmup: int, isolated_rounds: int = 10, e2e_steps: int = 0,
                       clocks_dev=None, rows: int = 0, in_order: bool = False, ctas_per_sm: int = 0,
                       stages: int = 0, piece_bytes: int = 0, fill_rounds: int = 0, reduce_ctas: int = 0,
-                      reduce_threads: int = 0, gather: bool = True, ag_ctas_per_sm: int = 0):
+                      reduce_threads: int = 0, gather: bool = True, ag_ctas_per_sm: int = 0,
+                      host_piece_bytes: int = 0):
     """The two-shot all-reduce of W.ALLREDUCE.  The collective: K rounds of start + a producer that
     only marks (dtt_publish: the vectors were written before the timed region, as an all-reduce
     benchmark's inputs are) + reduce kernel + wait + next_round (both plans' copiers launched at
@@ -1036,10 +1037,11 @@ def measure_allreduce(K: int, warmup: int, isolated_rounds: int = 10, e2e_steps:
     prod, side = torch.cuda.Stream(), torch.cuda.Stream()
     rs_cs, ag_cs = torch.cuda.Stream(priority=-1), torch.cuda.Stream(priority=-1)
     opts = ag_opts = None
-    if in_order or ctas_per_sm or stages or piece_bytes or ag_ctas_per_sm:
+    if in_order or ctas_per_sm or stages or piece_bytes or ag_ctas_per_sm or host_piece_bytes:
         opts = D.dtt_plan_opts_default(method=D.COPY_TMA, ctas_per_sm=ctas_per_sm or 3,
                                        piece_bytes=piece_bytes or 16384, stages=stages or 2,
-                                       deferred_copier=1 if in_order else 0)
+                                       deferred_copier=1 if in_order else 0,
+                                       host_piece_bytes=host_piece_bytes)
         ag_opts = D.dtt_plan_opts_default(method=D.COPY_TMA, ctas_per_sm=ag_ctas_per_sm or ctas_per_sm or 3,
                                           piece_bytes=piece_bytes or 16384, stages=stages or 2,
                                           deferred_copier=1 if in_order else 0)
@@ -1127,20 +1129,12 @@ def measure_allreduce(K: int, warmup: int, isolated_rounds: int = 10, e2e_steps:
         host = [torch.randn(M, cols, generator=g).to(torch.bfloat16).view(torch.uint8).reshape(-1).pin_memory()
                 for _ in range(P)]
         host_out = torch.empty(S, dtype=torch.uint8).pin_memory()
-        n_global = ar.rs.info()[0]
 
         def host_round():
-            h = ar.start(prod)
-            with torch.cuda.stream(prod):
-                for r in range(P):
-                    bufs[r][:S].copy_(host[r], non_blocking=True)
-            D.dtt_publish(h, 0, n_global, 0, prod)      # every chunk's marks, after its bytes
-            ar.reduce(err, prod)
-            ar.wait()
-            ar.next_round()
-            with torch.cuda.stream(prod):
-                host_out.copy_(bufs[0][:S], non_blocking=True)
-            prod.synchronize()
+            # dtt_allreduce_host: the partials go in sub-block by sub-block, each reduce-scatter
+            # chunk marked once its rows have landed, the reduce running meanwhile, and rank 0's
+            # result coming back as the all-gather delivers it
+            ar.host_round(host, err, host_out=host_out, out_rank=0, stream=prod)
 
         for _ in range(2):
             host_round()
@@ -1188,7 +1182,7 @@ def run_allreduce(args):
                           clocks_dev=dev, rows=args.rows, in_order=args.in_order,
                           ctas_per_sm=args.ctas_per_sm, stages=args.stages, piece_bytes=args.piece_bytes,
                           fill_rounds=20, reduce_ctas=args.reduce_ctas, reduce_threads=args.reduce_threads,
-                          ag_ctas_per_sm=args.ag_ctas_per_sm)
+                          ag_ctas_per_sm=args.ag_ctas_per_sm, host_piece_bytes=args.host_piece_bytes)
     peak, peak_kind = load_peaks()
     s = summarize_allreduce(m, peak, peak_kind)
     # the reduce-scatter alone (the first shot: no all-gather plan), the same way
@@ -1209,7 +1203,9 @@ def run_allreduce(args):
     if "e2e_round_ms" in m:
         e2e = {"value": m["S"] / (m["e2e_round_ms"] * 1e-3) / 1e9, "unit": "GB/s",
                "h2d_bytes_per_step": m["e2e_bytes"][0], "d2h_bytes_per_step": m["e2e_bytes"][1],
-               "call": "partials copied in from pinned host memory, dtt_publish, reduce, wait; rank 0's result copied out"}
+               "call": ("dtt_allreduce_host: partials from pinned host memory in sub-block pieces, each "
+                        "reduce-scatter chunk marked as its rows land, the reduce meanwhile, rank 0's "
+                        "result copied back as the all-gather delivers it")}
     line = {
         "metric": "two-shot all-reduce algorithm GB/s (one rank's vector bytes per round, 1 GB300)",
         "value": s["algbw_gbs"], "unit": "GB/s", "n_gpus": 1, "steps": K, "warmup": args.warmup,

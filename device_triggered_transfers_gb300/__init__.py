@@ -34,6 +34,7 @@ PREPARED, RUNNING, DONE, FAILED, CLOSING, CLOSED = range(6)
 RC_CLOSING = 1      # dtt_plan_close left the plan CLOSING (not an error)
 BF16, F32, U8 = 0, 1, 2
 DTYPE_CODES = {"bf16": BF16, "f32": F32, "u8": U8}
+ELEM_BYTES = {"bf16": 2, "f32": 4, "u8": 1}
 COPY_VEC16, COPY_TMA, COPY_ENGINE = 0, 1, 2
 ORDER_ROW_MAJOR, ORDER_GROUPED = 0, 1
 MARK_PER_STEP, MARK_AT_END = 0, 1
@@ -168,6 +169,8 @@ _SIGS = {
     "dtt_allreduce_start": (C.c_int, [_P, _P, C.POINTER(dtt_handle)]),
     "dtt_allreduce_reduce": (C.c_int, [_P, _P, _P]),
     "dtt_allreduce_wait": (C.c_int, [_P, C.POINTER(dtt_report), C.POINTER(dtt_report)]),
+    "dtt_allreduce_host": (C.c_int, [_P, C.POINTER(_P), _P, _u32, _P, _P, C.POINTER(dtt_report),
+                                     C.POINTER(dtt_report)]),
     "dtt_allreduce_next_round": (C.c_int, [_P]),
     "dtt_allreduce_destroy": (C.c_int, [_P]),
     "dtt_barrier_handrolled": (C.c_int, [C.POINTER(_P), C.POINTER(_P), _u32, _u32, _u64, _P, _P]),
@@ -730,6 +733,26 @@ class AllReduce:
     def wait(self, raise_on_error: bool = True):
         a, b = dtt_report(), dtt_report()
         rc = lib().dtt_allreduce_wait(self._h, C.byref(a), C.byref(b))
+        if rc and raise_on_error:
+            _check(rc)
+        return a, b
+
+    def host_round(self, host_parts: Sequence, err, host_out=None, out_rank: int = 0, stream=None,
+                   raise_on_error: bool = True):
+        """One round from host memory (dtt_allreduce_host): host_parts, P pinned host tensors
+        (None: that rank's vector as it stands), each rank's vector with its rows back to back;
+        host_out (pinned, or None) receives out_rank's result.  Returns both reports."""
+        if len(host_parts) != self.P:
+            raise DttError(EINVAL, "host_round: one host vector (or None) per rank")
+        need = self.P * self.block_rows * self.cols * ELEM_BYTES[self.dtype]
+        for i, x in enumerate(list(host_parts) + [host_out]):
+            if x is None:
+                continue
+            if x.device.type != "cpu" or x.numel() * x.element_size() < need:
+                raise DttError(EINVAL, f"host_round: host buffer {i} must be host memory of at least {need} bytes")
+        a, b = dtt_report(), dtt_report()
+        rc = lib().dtt_allreduce_host(self._h, _ptr_array(host_parts), _ptr(host_out) or None, out_rank,
+                                      _ptr(err), _stream(stream), C.byref(a), C.byref(b))
         if rc and raise_on_error:
             _check(rc)
         return a, b

@@ -384,6 +384,10 @@ struct dtt_allreduce {
     cudaEvent_t ev_rs = nullptr;         // serial: the reduce-scatter copier has finished
     cudaEvent_t ev_reduce = nullptr;     // the reduce has finished (serial; and what a
                                          // reduce-scatter's wait waits for)
+    // dtt_allreduce_host (made at its first call): the reduce's stream, and events ordering it
+    // and the copies in after the round's start, and the marks after the copies in
+    cudaStream_t host_stream = nullptr;
+    cudaEvent_t ev_host = nullptr, ev_in = nullptr;
 };
 
 namespace {
@@ -395,6 +399,9 @@ void release(dtt_allreduce* ar) {
     if (ar->d_counters) cudaFree(ar->d_counters);
     if (ar->ev_rs) cudaEventDestroy(ar->ev_rs);
     if (ar->ev_reduce) cudaEventDestroy(ar->ev_reduce);
+    if (ar->ev_host) cudaEventDestroy(ar->ev_host);
+    if (ar->ev_in) cudaEventDestroy(ar->ev_in);
+    if (ar->host_stream) cudaStreamDestroy(ar->host_stream);
     delete ar;
 }
 
@@ -713,6 +720,133 @@ int dtt_allreduce_wait(dtt_allreduce* ar, dtt_report* rs_report, dtt_report* ag_
         return fail(b, "all-gather: %s", m2.c_str());
     }
     return DTT_OK;
+}
+
+int dtt_allreduce_host(dtt_allreduce* ar, const void* const* host_parts, void* host_out, uint32_t out_rank,
+                       uint32_t* err, cudaStream_t stream, dtt_report* rs_report, dtt_report* ag_report) {
+    if (!ar || !host_parts || !err) return fail(DTT_EINVAL, "dtt_allreduce_host: NULL argument");
+    if (!ar->ag) return fail(DTT_EINVAL, "dtt_allreduce_host: needs an all-reduce (not scatter_only)");
+    if (ar->serial)
+        return fail(DTT_EINVAL, "dtt_allreduce_host: the reduce runs while the vectors come in: not with "
+                                "deferred_copier = 1");
+    if (out_rank >= ar->P) return fail(DTT_EINVAL, "dtt_allreduce_host: out_rank out of range");
+    PlanHostIo in{}, out{};
+    int rc = plan_host_io(ar->rs, &in);
+    if (rc == DTT_OK) rc = plan_host_io(ar->ag, &out);
+    if (rc != DTT_OK) return rc;
+    if (!ar->host_stream) {
+        if (cudaStreamCreateWithFlags(&ar->host_stream, cudaStreamNonBlocking) != cudaSuccess ||
+            cudaEventCreateWithFlags(&ar->ev_host, cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&ar->ev_in, cudaEventDisableTiming) != cudaSuccess)
+            return fail(DTT_ECUDA, "dtt_allreduce_host: cannot create its stream or events");
+    }
+    const uint32_t P = ar->P, J = ar->d.sub_blocks;
+    const uint64_t Mb = ar->d.block_rows, Mj = ar->Mj, rb = ar->rb, pitch = ar->pitch;
+
+    // the all-gather copier stamps each chunk's arrival into mapped host memory for the copy back
+    plan_set_host_round(ar->ag, host_out != nullptr, false);
+    dtt_handle h[DTT_MAX_RANKS];
+    rc = dtt_allreduce_start(ar, stream, h);
+    plan_set_host_round(ar->ag, false, false);
+    if (rc != DTT_OK) return rc;
+    const uint32_t R = dtt_plan_round(ar->ag);
+
+    // The reduce on a stream of its own, after start's work on `stream`: it waits on each
+    // sub-block's group while the later rows are still coming in.
+    DTT_CUDA_TRY(cudaEventRecord(ar->ev_host, stream));
+    DTT_CUDA_TRY(cudaStreamWaitEvent(ar->host_stream, ar->ev_host, 0));
+    DTT_CUDA_TRY(cudaStreamWaitEvent(in.h2d, ar->ev_host, 0));
+    rc = dtt_allreduce_reduce(ar, err, ar->host_stream);
+    if (rc != DTT_OK) return rc;
+
+    // rows [r0, r0 + n) of a vector between the host (rows back to back) and the device (pitch)
+    auto rows_copy = [&](char* dst, uint64_t dpitch, const char* src, uint64_t spitch, uint64_t n,
+                         cudaMemcpyKind kind, cudaStream_t s) -> cudaError_t {
+        if (dpitch == rb && spitch == rb) return cudaMemcpyAsync(dst, src, n * rb, kind, s);
+        return cudaMemcpy2DAsync(dst, dpitch, src, spitch, rb, n, kind, s);
+    };
+    // Copy back: block b of out_rank's result, sub-block by sub-block as the all-gather delivers
+    // them (its own block once its chunks have gone out: the reduce wrote them before marking),
+    // in copies of at least 8 MiB or the rest of the block.
+    std::vector<uint32_t> back(P, 0);
+    const uint64_t kBack = 8ull << 20;
+    auto poll = [&](bool final) -> int {
+        for (uint32_t b = 0; b < P; ++b) {
+            uint32_t k = back[b];
+            while (k < J && __atomic_load_n(&out.arrived[b * J + k], __ATOMIC_ACQUIRE) == R) ++k;
+            if (k == back[b] || !(k == J || final || (k - back[b]) * Mj * rb >= kBack)) continue;
+            const uint64_t r0 = b * Mb + back[b] * Mj;
+            const cudaError_t e = rows_copy(static_cast<char*>(host_out) + r0 * rb, rb,
+                                            ar->bufs[out_rank] + r0 * pitch, pitch, (k - back[b]) * Mj,
+                                            cudaMemcpyDeviceToHost, out.d2h);
+            if (e != cudaSuccess) return fail(DTT_ECUDA, "dtt_allreduce_host: %s", cudaGetErrorString(e));
+            back[b] = k;
+        }
+        return DTT_OK;
+    };
+
+    // Copies in, in the groups' order: sub-blocks [j0, j1) of block b (at least the reduce-scatter
+    // plan's host_piece_bytes of a rank, 0: 16 MiB, or the rest of the block) of every rank, then
+    // the marks of those reduce-scatter chunks -- rank s's chunk (b, j) is s * P * J + b * J + j --
+    // once the copies have landed.  (On the host link of a GB300, copies in of 4 MiB ran at ~190
+    // GB/s against ~205 for 16 MiB and ~55 for 1 MiB.)
+    const uint64_t kIn = in.piece_bytes ? in.piece_bytes : (16ull << 20);
+    for (uint32_t b = 0; b < P; ++b) {
+        for (uint32_t j0 = 0; j0 < J;) {
+            uint32_t j1 = j0 + 1;
+            while (j1 < J && (j1 - j0) * Mj * rb < kIn) ++j1;
+            const uint64_t r0 = b * Mb + j0 * Mj, n = (j1 - j0) * Mj;
+            bool any = false;
+            for (uint32_t s = 0; s < P; ++s) {
+                if (!host_parts[s]) continue;
+                const cudaError_t e = rows_copy(ar->bufs[s] + r0 * pitch, pitch,
+                                                static_cast<const char*>(host_parts[s]) + r0 * rb, rb, n,
+                                                cudaMemcpyHostToDevice, in.h2d);
+                if (e != cudaSuccess) return fail(DTT_ECUDA, "dtt_allreduce_host: %s", cudaGetErrorString(e));
+                any = true;
+            }
+            if (any) {
+                DTT_CUDA_TRY(cudaEventRecord(ar->ev_in, in.h2d));
+                DTT_CUDA_TRY(cudaStreamWaitEvent(stream, ar->ev_in, 0));
+            }
+            for (uint32_t s = 0; s < P; ++s) {
+                rc = dtt_publish(h, P, s * P * J + b * J + j0, j1 - j0, 0, stream);
+                if (rc != DTT_OK) return rc;
+            }
+            if (host_out && (rc = poll(false)) != DTT_OK) return rc;
+            j0 = j1;
+        }
+    }
+    // the reduce before whatever follows on `stream` (its error word included)
+    DTT_CUDA_TRY(cudaStreamWaitEvent(stream, ar->ev_reduce, 0));
+    if (host_out) {
+        // the rest as it arrives; once the all-gather copier has exited, whatever arrived is final
+        for (uint64_t spin = 1;; ++spin) {
+            if ((rc = poll(false)) != DTT_OK) return rc;
+            bool all = true;
+            for (uint32_t b = 0; b < P; ++b) all = all && back[b] == J;
+            if (all) break;
+            if ((spin & 1023) == 0) {
+                const cudaError_t e = cudaEventQuery(out.copier_end);
+                if (e == cudaSuccess) break;
+                if (e != cudaErrorNotReady) return fail(DTT_ECUDA, "dtt_allreduce_host: %s", cudaGetErrorString(e));
+            }
+        }
+        if ((rc = poll(true)) != DTT_OK) return rc;
+    }
+    plan_set_host_round(ar->ag, false, true);
+    rc = dtt_allreduce_wait(ar, rs_report, ag_report);
+    plan_set_host_round(ar->ag, false, false);
+    if (rc != DTT_OK) {
+        cudaStreamSynchronize(out.d2h);
+        return rc;
+    }
+    if (host_out) {
+        DTT_CUDA_TRY(cudaStreamSynchronize(out.d2h));
+        for (uint32_t b = 0; b < P; ++b)
+            if (back[b] != J) return fail(DTT_ETIMEDOUT, "dtt_allreduce_host: block %u came back short", b);
+    }
+    return dtt_allreduce_next_round(ar);
 }
 
 int dtt_allreduce_next_round(dtt_allreduce* ar) {

@@ -223,6 +223,20 @@ struct CopierRoom {
     uint64_t regs = 0, smem = 0;
 };
 int plan_copier_room(const dtt_plan* p, CopierRoom* out);
+
+// Host-buffer rounds driven from outside the plan (the all-reduce's): the plan's streams for
+// copies in and out, its mapped arrival words (word c = the round of chunk c's last arrival,
+// stamped by a copier launched while notify is on) and the event recorded after such a launch.
+struct PlanHostIo {
+    cudaStream_t h2d = nullptr, d2h = nullptr;
+    const uint32_t* arrived = nullptr;
+    cudaEvent_t copier_end = nullptr;
+    uint64_t piece_bytes = 0;          // opts.host_piece_bytes (0: the caller's default)
+};
+int plan_host_io(const dtt_plan* p, PlanHostIo* out);
+// notify: the next copier launch stamps the arrival words; quiet: wait() launches no early
+// copier for the next round (one launched then would not stamp them).
+void plan_set_host_round(dtt_plan* p, bool notify, bool quiet);
 cudaStream_t plan_copy_stream(const dtt_plan* p);   // the stream its copier runs on
 cudaError_t preload_allreduce_kernels();
 

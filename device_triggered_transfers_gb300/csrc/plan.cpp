@@ -1110,6 +1110,21 @@ int plan_copier_room(const dtt_plan* p, CopierRoom* out) {
 
 cudaStream_t plan_copy_stream(const dtt_plan* p) { return p->copy_stream; }
 
+int plan_host_io(const dtt_plan* p, PlanHostIo* out) {
+    if (p->ce) return fail(DTT_EINVAL, "host-buffer rounds need an SM copier (not DTT_COPY_ENGINE)");
+    out->h2d = p->h2d_stream;
+    out->d2h = p->d2h_stream;
+    out->arrived = p->h_arrived;
+    out->copier_end = p->ev_copier_end;
+    out->piece_bytes = p->opts.host_piece_bytes;
+    return DTT_OK;
+}
+
+void plan_set_host_round(dtt_plan* p, bool notify, bool quiet) {
+    p->notify_host = notify;
+    p->suppress_early = quiet;
+}
+
 }  // namespace dtt
 
 extern "C" {

@@ -231,7 +231,9 @@ typedef struct dtt_plan_opts {
                                 stream (read with dtt_plan_stats) */
     uint32_t host_piece_bytes;/* dtt_allgather_host: bytes per host-to-device copy (a multiple
                                 of 4096); 0 = a quarter of a slice, at least 4 MiB (rounds back
-                                to back, dtt_allgather_host_rounds: 0 = a whole slice) */
+                                to back, dtt_allgather_host_rounds: 0 = a whole slice).  On an
+                                all-reduce's reduce-scatter plan: dtt_allreduce_host's least
+                                bytes a rank per copy in (0 = 16 MiB) */
     void* const* dst_bufs;    /* NULL: copies land in the P buffers themselves.  Else a host array
                                  of P device pointers, dst_bytes each: separate destination buffers
                                  (staging buffers) that every copy lands in, at its chunk's
@@ -775,6 +777,28 @@ int dtt_allreduce_reduce(dtt_allreduce* ar, uint32_t* err, cudaStream_t stream);
  * are FAILED (and the reduce kernel's counters may hold a partial count): destroy the
  * all-reduce. */
 int dtt_allreduce_wait(dtt_allreduce* ar, dtt_report* rs_report, dtt_report* ag_report);
+
+/* Host-buffer all-reduce, one round end to end (this library's own addition, like
+ * dtt_allgather_host: the pages move device data only).  host_parts: host array of P pointers,
+ * rank r's vector in pinned host memory as P * block_rows rows of cols elements back to back
+ * (a NULL entry: that rank's vector as it stands on the device); host_out: pinned host memory
+ * of the same size for rank out_rank's result, or NULL.  The round is pipelined: the vectors go
+ * in on a stream of the reduce-scatter plan sub-block by sub-block in the groups' order (every
+ * rank's rows of the first sub-blocks of block 0 first, in copies of at least the reduce-scatter
+ * plan's host_piece_bytes a rank -- 0: 16 MiB -- or the rest of a block), each reduce-scatter
+ * chunk is marked (a kernel on `stream`) once its rows have landed, the reduce kernel runs on
+ * a stream of the all-reduce while later rows are still coming in (err as for
+ * dtt_allreduce_reduce), and the all-gather copier stamps each chunk's arrival into pinned,
+ * mapped host memory so that out_rank's result comes back (on a stream of the all-gather plan)
+ * sub-block by sub-block as it is delivered, in copies of at least 8 MiB or the rest of a
+ * block.  Then both waits and both
+ * next_rounds; the call returns once host_out holds the result and the round is checked.  Only
+ * the concurrent form (deferred_copier 0) of an all-reduce (not scatter_only); both plans
+ * PREPARED.  The reports are filled as by dtt_allreduce_wait.  Errors: DTT_EINVAL, DTT_ESTATE,
+ * those of start, reduce and wait, DTT_ETIMEDOUT if a block of the result could not be copied
+ * back, DTT_ECUDA.  After an error other than DTT_EINVAL or DTT_ESTATE, destroy the all-reduce. */
+int dtt_allreduce_host(dtt_allreduce* ar, const void* const* host_parts, void* host_out, uint32_t out_rank,
+                       uint32_t* err, cudaStream_t stream, dtt_report* rs_report, dtt_report* ag_report);
 
 /* dtt_plan_next_round on both plans.  Errors: as dtt_plan_next_round. */
 int dtt_allreduce_next_round(dtt_allreduce* ar);

@@ -211,6 +211,128 @@ def test_allreduce_full_size_every_element(name):
         c.close()
 
 
+HOST_CASES = {
+    "p4_bf16_in_place": dict(P=4, Mb=64, cols=256, J=2, dtype="bf16"),
+    "p3_f32_pitched_staging": dict(P=3, Mb=40, cols=128, J=5, dtype="f32", pitch=768, separate=True),
+    "p5_bf16_one_row_sub_blocks": dict(P=5, Mb=3, cols=256, J=3, dtype="bf16"),
+    "p8_bf16_vector_copier": dict(P=8, Mb=16, cols=512, J=2, dtype="bf16", copier="vector"),
+    "p2_f32_large_sub_blocks": dict(P=2, Mb=1024, cols=1024, J=2, dtype="f32"),   # 4 MiB sub-blocks
+}
+
+
+def _pinned(arr):
+    return torch.from_numpy(np.ascontiguousarray(arr).view(np.uint8).reshape(-1).copy()).pin_memory()
+
+
+@pytest.mark.parametrize("name", sorted(HOST_CASES))
+def test_allreduce_host_round_matches_the_oracle(name):
+    """dtt_allreduce_host: the vectors from pinned host memory, the result of a different rank
+    copied back each round -- every byte of every buffer and staging buffer, both plans' gates
+    and the group counters against the oracle's round, and the copied-back result against the
+    definition, three rounds."""
+    c = Case(**HOST_CASES[name])
+    eb = A.ELEM_BYTES[c.dtype]
+    try:
+        for R in range(1, 4):
+            parts = A.hashed_partials(c.dtype, SEED, c.P, c.M, c.cols, R)
+            out = torch.zeros(c.M * c.cols * eb, dtype=torch.uint8).pin_memory()
+            rs, ag = c.ar.host_round([_pinned(x) for x in parts], c.err, host_out=out,
+                                     out_rank=(R - 1) % c.P, stream=c.prod)
+            assert rs.status == D.OK and ag.status == D.OK
+            torch.cuda.synchronize()
+            assert int(c.err.item()) == 0
+            assert c.o.round(parts) == R
+            c.compare(f"{name} R{R}")
+            want = A.allreduce(c.dtype, parts)
+            np.testing.assert_array_equal(out.numpy(), want.view(np.uint8).reshape(-1), err_msg=f"{name} R{R}")
+    finally:
+        c.close()
+
+
+def test_allreduce_host_round_with_a_rank_as_it_stands_and_no_copy_back():
+    """A NULL host vector leaves that rank's device vector as it stands; without host_out the
+    result stays on the device; a host round and an ordinary round alternate."""
+    c = Case(P=4, Mb=32, cols=512, J=4, dtype="bf16")
+    S = c.M * c.cols * 2
+    try:
+        for R in range(1, 5):
+            if R == 3:
+                c.round()                              # an ordinary round between host rounds
+                c.oracle_round(R)
+                c.compare(f"R{R}")
+                c.ar.next_round()
+                continue
+            parts = A.hashed_partials(c.dtype, SEED, c.P, c.M, c.cols, R)
+            c.bufs[2][:S].copy_(torch.from_numpy(parts[2].view(np.uint8).reshape(-1).copy()))
+            torch.cuda.synchronize()
+            host = [_pinned(x) for x in parts]
+            host[2] = None
+            out = torch.zeros(S, dtype=torch.uint8).pin_memory() if R == 4 else None
+            rs, ag = c.ar.host_round(host, c.err, host_out=out, out_rank=2, stream=c.prod)
+            assert rs.status == D.OK and ag.status == D.OK
+            torch.cuda.synchronize()
+            assert int(c.err.item()) == 0
+            assert c.o.round(parts) == R
+            c.compare(f"R{R}")
+            if out is not None:
+                np.testing.assert_array_equal(out.numpy(), A.allreduce(c.dtype, parts).view(np.uint8).reshape(-1))
+    finally:
+        c.close()
+
+
+def test_allreduce_host_round_refusals():
+    """Host buffers too short or on the device, a wrong count and an out-of-range out_rank are
+    refused before anything starts; the all-reduce stays usable."""
+    c = Case(P=2, Mb=16, cols=256, J=2, dtype="bf16")
+    S = c.M * c.cols * 2
+    try:
+        good = [torch.zeros(S, dtype=torch.uint8).pin_memory() for _ in range(2)]
+        for bad in ([good[0]], [good[0], torch.zeros(S - 2, dtype=torch.uint8).pin_memory()],
+                    [good[0], torch.zeros(S, dtype=torch.uint8, device="cuda")]):
+            with pytest.raises(D.DttError) as ei:
+                c.ar.host_round(bad, c.err, stream=c.prod)
+            assert ei.value.code == D.EINVAL
+        with pytest.raises(D.DttError) as ei:
+            c.ar.host_round(good, c.err, out_rank=2, stream=c.prod)
+        assert ei.value.code == D.EINVAL
+        c.round()
+        c.oracle_round(1)
+        c.compare("after the refusals")
+    finally:
+        c.close()
+
+
+def test_allreduce_host_round_full_size():
+    """The benchmark's all-reduce (P = 4, bf16 [16384, 4096] per rank, 8 sub-blocks of 4 MiB a
+    block) from pinned host memory, two rounds: the copied-back result and every rank's device
+    vector against the definition, element by element."""
+    P, Mb, cols, J = 4, 4096, 4096, 8
+    c = Case(P=P, Mb=Mb, cols=cols, J=J, dtype="bf16", oracle=False)
+    M, rb = P * Mb, cols * 2
+    try:
+        for R in range(1, 3):
+            host = []
+            for s in range(P):
+                h = torch.empty(M * rb, dtype=torch.uint8).pin_memory()
+                cfill.fill_rows_into(h.numpy(), "bf16", SEED, s, R, cols, 0, M)
+                host.append(h)
+            out = torch.zeros(M * rb, dtype=torch.uint8).pin_memory()
+            rs, ag = c.ar.host_round(host, c.err, host_out=out, out_rank=R % P, stream=c.prod)
+            assert rs.status == D.OK and ag.status == D.OK
+            torch.cuda.synchronize()
+            assert int(c.err.item()) == 0
+            for b in range(P):
+                sl = slice(b * Mb * rb, (b + 1) * Mb * rb)
+                parts = [host[s].numpy()[sl].view(np.uint16) for s in range(P)]
+                want = A.allreduce("bf16", parts).view(np.uint8)
+                np.testing.assert_array_equal(out.numpy()[sl], want, err_msg=f"R{R} block {b} copied back")
+                for r in range(P):
+                    np.testing.assert_array_equal(c.bufs[r][sl].cpu().numpy(), want,
+                                                  err_msg=f"R{R} block {b} at rank {r}")
+    finally:
+        c.close()
+
+
 def test_allreduce_missing_mark_fails_the_round_and_counts_the_reduce_wait():
     """One reduce-scatter chunk never marked (the producers of the other chunks run): the
     group of its sub-block never completes, the reduce's CTAs give up after the plan's poll

@@ -437,4 +437,6 @@ def test_allreduce_calls_refuse_a_null_all_reduce_without_a_gpu():
     assert L.dtt_allreduce_wait(None, C.byref(a), C.byref(b)) == D.EINVAL
     assert L.dtt_allreduce_next_round(None) == D.EINVAL
     assert L.dtt_allreduce_plans(None, None, None) == D.EINVAL
+    parts = (C.c_void_p * 2)()
+    assert L.dtt_allreduce_host(None, parts, None, 0, err, None, C.byref(a), C.byref(b)) == D.EINVAL
     assert L.dtt_allreduce_destroy(None) == D.OK
