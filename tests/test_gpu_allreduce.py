@@ -2,7 +2,8 @@
 which other destinations make possible) -- the reduce-scatter plan, the reduce kernel and the
 all-gather plan of libdtt -- against the oracle's two-shot model (oracle/allreduce.py): every
 byte of every buffer and staging buffer, both plans' gate words 0-4 and the reduce-scatter
-plan's group counters, round after round; at full size every element against the definition."""
+plan's group counters, round after round; at full size every element against the definition;
+the same for rounds fed from and returned to pinned host memory (dtt_allreduce_host)."""
 import numpy as np
 import pytest
 import torch
