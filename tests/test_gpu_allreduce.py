@@ -36,7 +36,8 @@ def _opts(copier, **kw):
 
 class Case:
     def __init__(self, P, Mb, cols, J, dtype, separate=False, pitch=0, copier="bulk", reduce_ctas=0,
-                 reduce_threads=0, group=1, max_polls=0, oracle=True, in_order=False, gather=True):
+                 reduce_threads=0, group=1, max_polls=0, oracle=True, in_order=False, gather=True,
+                 host_piece_bytes=0):
         self.P, self.Mb, self.cols, self.J, self.dtype = P, Mb, cols, J, dtype
         # the oracle's model of both plans (small cases; at full size only its layout is used)
         self.o = A.TwoShot(P, Mb, cols, dtype, J, pitch=pitch or None, separate=separate,
@@ -52,6 +53,8 @@ class Case:
         kw = dict(max_polls=max_polls) if max_polls else {}
         if in_order:
             kw["deferred_copier"] = 1   # each kernel after its inputs (a serialising profiler's case)
+        if host_piece_bytes:
+            kw["host_piece_bytes"] = host_piece_bytes   # dtt_allreduce_host's least bytes a copy in
         self.ar = D.AllReduce(self.bufs, self.buf_bytes, dtype, Mb, cols, sub_blocks=J, pitch=pitch,
                               staging=self.staging, staging_bytes=staging_bytes,
                               rs_opts=_opts(copier, **kw), ag_opts=_opts(copier, **kw),
@@ -218,6 +221,12 @@ HOST_CASES = {
     "p5_bf16_one_row_sub_blocks": dict(P=5, Mb=3, cols=256, J=3, dtype="bf16"),
     "p8_bf16_vector_copier": dict(P=8, Mb=16, cols=512, J=2, dtype="bf16", copier="vector"),
     "p2_f32_large_sub_blocks": dict(P=2, Mb=1024, cols=1024, J=2, dtype="f32"),   # 4 MiB sub-blocks
+    # 8 KiB sub-blocks, copies in of at least 12 KiB a rank: two sub-blocks a step, and with
+    # three sub-blocks a block a ragged last step of one
+    "p4_bf16_two_sub_blocks_a_step": dict(P=4, Mb=64, cols=256, J=4, dtype="bf16", host_piece_bytes=12288),
+    "p3_f32_ragged_steps_pitched": dict(P=3, Mb=48, cols=128, J=3, dtype="f32", pitch=640,
+                                        host_piece_bytes=12288),
+    "p16_bf16_one_sub_block_a_step": dict(P=16, Mb=8, cols=512, J=2, dtype="bf16", host_piece_bytes=4096),
 }
 
 
