@@ -734,12 +734,10 @@ int dtt_allreduce_host(dtt_allreduce* ar, const void* const* host_parts, void* h
     int rc = plan_host_io(ar->rs, &in);
     if (rc == DTT_OK) rc = plan_host_io(ar->ag, &out);
     if (rc != DTT_OK) return rc;
-    if (!ar->host_stream) {
-        if (cudaStreamCreateWithFlags(&ar->host_stream, cudaStreamNonBlocking) != cudaSuccess ||
-            cudaEventCreateWithFlags(&ar->ev_host, cudaEventDisableTiming) != cudaSuccess ||
-            cudaEventCreateWithFlags(&ar->ev_in, cudaEventDisableTiming) != cudaSuccess)
-            return fail(DTT_ECUDA, "dtt_allreduce_host: cannot create its stream or events");
-    }
+    if ((!ar->host_stream && cudaStreamCreateWithFlags(&ar->host_stream, cudaStreamNonBlocking) != cudaSuccess) ||
+        (!ar->ev_host && cudaEventCreateWithFlags(&ar->ev_host, cudaEventDisableTiming) != cudaSuccess) ||
+        (!ar->ev_in && cudaEventCreateWithFlags(&ar->ev_in, cudaEventDisableTiming) != cudaSuccess))
+        return fail(DTT_ECUDA, "dtt_allreduce_host: cannot create its stream or events");
     const uint32_t P = ar->P, J = ar->d.sub_blocks;
     const uint64_t Mb = ar->d.block_rows, Mj = ar->Mj, rb = ar->rb, pitch = ar->pitch;
 
