@@ -44,7 +44,7 @@ NCU_TRAFFIC = {("c2_chunks_p4", "copier_bulk_kernel"): 474700544,
                # captured with 256 rows (--rows 256) and scaled by the rows, 10x
                ("c4b_bcast_p8", "copier_bulk_kernel"): 20848015360,
                # the two-shot all-reduce's reduce kernel (bench.py --allreduce --in-order), 256 threads
-               ("allreduce_p4", "reduce_kernel"): 651664896}
+               ("allreduce_p4", "reduce_kernel"): 652057088}
 # DRAM bytes (read, write) of one whole round, producer, copier and check together, from an
 # ncu range-replay capture of three rounds of the benchmark's launch (--profile-rounds 3;
 # c2 and c5 with overlapping rounds)
@@ -280,8 +280,8 @@ def time_oracle_gemm(w, budget_s: float = 10.0, rows: int = 128):
 # ---- distributed helpers ---------------------------------------------------------------------------
 def time_oracle_allreduce(budget_s: float = 10.0, rows: int = 32):
     """The oracle's two-shot all-reduce (both plans and the reduce step on the plan model) on a
-    sample of the benchmark's workload: P = 4 ranks of `rows` rows of 4096 bf16 per block,
-    8 sub-blocks.  Returns (GB/s of vector bytes per rank, rounds, seconds, sample)."""
+    sample of the benchmark's workload: P = 4 ranks of `rows` rows of 4096 bf16 per block, in
+    the benchmark's sub-blocks.  Returns (GB/s of vector bytes per rank, rounds, seconds, sample)."""
     from oracle import allreduce as OA
     a = W.ALLREDUCE
     P, cols, J = a["P"], a["cols"], a["sub_blocks"]
@@ -769,7 +769,10 @@ def run_ours(args):
             "with_fill_producer_ms_per_round": ma.get("fill_round_ms"),
             "dominant_kernel": {k: (sa.get("reduce_roofline") or {}).get(k)
                                 for k in ("kernel", "bound", "achieved", "unit", "frac", "traffic")},
-            "workload": "P=4 bf16 [16384, 4096] per rank, 8 sub-blocks of 512 rows per block (bench.py --allreduce)"}
+            "workload": (f"P={W.ALLREDUCE['P']} bf16 [{W.ALLREDUCE['P'] * W.ALLREDUCE['block_rows']}, "
+                         f"{W.ALLREDUCE['cols']}] per rank, {W.ALLREDUCE['sub_blocks']} sub-blocks of "
+                         f"{W.ALLREDUCE['block_rows'] // W.ALLREDUCE['sub_blocks']} rows per block "
+                         "(bench.py --allreduce)")}
 
     if rank != 0:
         return 0

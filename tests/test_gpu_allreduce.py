@@ -178,8 +178,10 @@ def test_allreduce_reduce_launched_first_on_its_own_stream():
 
 
 FULL = {
-    # the 4-rank chunked all-gather's size: 128 MiB per rank, blocks of 4096 rows in 4 MiB sub-blocks
-    "p4_bf16": dict(P=4, Mb=4096, cols=4096, J=8, dtype="bf16", group=38),
+    # the benchmark's launch: 128 MiB per rank (the 4-rank chunked all-gather's size), blocks of
+    # 4096 rows in 8 MiB sub-blocks; and the same in 4 MiB sub-blocks
+    "p4_bf16": dict(P=4, Mb=4096, cols=4096, J=4, dtype="bf16", group=38),
+    "p4_bf16_8_sub_blocks": dict(P=4, Mb=4096, cols=4096, J=8, dtype="bf16", group=38),
     "p4_f32": dict(P=4, Mb=4096, cols=2048, J=8, dtype="f32", group=38),
     # eight ranks of 128 MiB (2 GiB of buffers with the slots)
     "p8_bf16": dict(P=8, Mb=2048, cols=4096, J=4, dtype="bf16", group=19),
@@ -313,10 +315,10 @@ def test_allreduce_host_round_refusals():
 
 
 def test_allreduce_host_round_full_size():
-    """The benchmark's all-reduce (P = 4, bf16 [16384, 4096] per rank, 8 sub-blocks of 4 MiB a
+    """The benchmark's all-reduce (P = 4, bf16 [16384, 4096] per rank, 4 sub-blocks of 8 MiB a
     block) from pinned host memory, two rounds: the copied-back result and every rank's device
     vector against the definition, element by element."""
-    P, Mb, cols, J = 4, 4096, 4096, 8
+    P, Mb, cols, J = 4, 4096, 4096, 4
     c = Case(P=P, Mb=Mb, cols=cols, J=J, dtype="bf16", oracle=False)
     M, rb = P * Mb, cols * 2
     try:
