@@ -312,6 +312,20 @@ def test_allreduce_host_round_refusals():
         c.compare("after the refusals")
     finally:
         c.close()
+    # the in-order form (the reduce could not overlap the copies in) and a reduce-scatter (no
+    # all-gather plan to deliver a result) are refused too
+    for kw in (dict(in_order=True), dict(gather=False)):
+        c = Case(P=2, Mb=16, cols=256, J=2, dtype="bf16", **kw)
+        try:
+            host = [torch.zeros(S, dtype=torch.uint8).pin_memory() for _ in range(2)]
+            with pytest.raises(D.DttError) as ei:
+                c.ar.host_round(host, c.err, stream=c.prod)
+            assert ei.value.code == D.EINVAL, kw
+            c.round()
+            c.oracle_round(1)
+            c.compare(f"after the refusal {kw}")
+        finally:
+            c.close()
 
 
 def test_allreduce_host_round_full_size():
